@@ -1,0 +1,172 @@
+"""ctypes wrapper of the double-precision RMSNorm oracle (``rmsnorm_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
+bench's CPU baseline and reference arm, never by the library.  Arrays are numpy:
+bf16 tensors as ``uint16`` bit patterns, fp32 tensors as ``float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rmsnorm_oracle.c")
+_LIB = os.path.join(_HERE, "_librmsnorm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPE_CODES = {"f32": 0, "bf16": 1}
+_P = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = f"{_LIB}.{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                           _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            I64, D, I = ctypes.c_int64, ctypes.c_double, ctypes.c_int
+            lib.oracle_rmsnorm_fwd.argtypes = [_P, _P, I64, I64, D, I, I, _P, _P, _P, _P]
+            lib.oracle_rmsnorm_fwd.restype = I
+            lib.oracle_rmsnorm_fused_add_fwd.argtypes = [_P, _P, _P, I64, I64, D, I, I,
+                                                         _P, _P, _P, _P, _P]
+            lib.oracle_rmsnorm_fused_add_fwd.restype = I
+            lib.oracle_rmsnorm_bwd.argtypes = [_P, _P, _P, _P, I64, I64, D, I, I,
+                                               _P, _P, _P, _P, _P, _P, _P]
+            lib.oracle_rmsnorm_bwd.restype = I
+            lib.oracle_round_bf16.argtypes = [D]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = D
+            _lib = lib
+    return _lib
+
+
+def _np(dtype: str):
+    return np.float32 if dtype == "f32" else np.uint16
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check_in(a, dtype, shape=None):
+    a = np.ascontiguousarray(a)
+    if a.dtype != _np(dtype):
+        raise TypeError(f"expected {_np(dtype)} for dtype {dtype}, got {a.dtype}")
+    if shape is not None and a.shape != tuple(shape):
+        raise ValueError(f"expected shape {shape}, got {a.shape}")
+    return a
+
+
+def round_bf16(v: float) -> int:
+    """Nearest bf16 bit pattern of a double (ties to even)."""
+    return int(_load().oracle_round_bf16(float(v)))
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().oracle_bf16_to_double(int(bits)))
+
+
+def bf16_array_to_f64(a: np.ndarray) -> np.ndarray:
+    """Decode uint16 bf16 bit patterns exactly (widen to the fp32 bit layout)."""
+    with np.errstate(invalid="ignore"):
+        return (np.asarray(a, dtype=np.uint16).astype(np.uint32) << 16).view(
+            np.float32).astype(np.float64)
+
+
+def to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    return bf16_array_to_f64(a) if dtype == "bf16" else np.asarray(a, np.float64)
+
+
+def fwd(x, gamma, eps, x_dtype="bf16", w_dtype=None, want64=True):
+    """RMSNorm forward of an M x N matrix.  Returns y (x_dtype), rstd (fp32) and,
+    with ``want64``, y64 / rstd64 (float64)."""
+    w_dtype = w_dtype or x_dtype
+    x = _check_in(x, x_dtype)
+    M, N = x.shape
+    gamma = _check_in(gamma, w_dtype, (N,))
+    y = np.empty((M, N), _np(x_dtype))
+    rstd = np.empty(M, np.float32)
+    y64 = np.empty((M, N), np.float64) if want64 else None
+    r64 = np.empty(M, np.float64) if want64 else None
+    rc = _load().oracle_rmsnorm_fwd(_ptr(x), _ptr(gamma), M, N, float(eps),
+                                    DTYPE_CODES[x_dtype], DTYPE_CODES[w_dtype], _ptr(y),
+                                    _ptr(y64), _ptr(rstd), _ptr(r64))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_fwd rejected its arguments")
+    out = {"y": y, "rstd": rstd}
+    if want64:
+        out.update(y64=y64, rstd64=r64)
+    return out
+
+
+def fused_add_fwd(x, residual, gamma, eps, x_dtype="bf16", w_dtype=None, want64=True):
+    """h = residual + x (stored dtype), y = RMSNorm(h) * gamma.  The residual is
+    not modified; h is returned."""
+    w_dtype = w_dtype or x_dtype
+    x = _check_in(x, x_dtype)
+    M, N = x.shape
+    residual = _check_in(residual, x_dtype, (M, N))
+    gamma = _check_in(gamma, w_dtype, (N,))
+    h = np.empty((M, N), _np(x_dtype))
+    y = np.empty((M, N), _np(x_dtype))
+    rstd = np.empty(M, np.float32)
+    y64 = np.empty((M, N), np.float64) if want64 else None
+    r64 = np.empty(M, np.float64) if want64 else None
+    rc = _load().oracle_rmsnorm_fused_add_fwd(_ptr(x), _ptr(residual), _ptr(gamma), M, N,
+                                              float(eps), DTYPE_CODES[x_dtype],
+                                              DTYPE_CODES[w_dtype], _ptr(h), _ptr(y),
+                                              _ptr(y64), _ptr(rstd), _ptr(r64))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_fused_add_fwd rejected its arguments")
+    out = {"h": h, "y": y, "rstd": rstd}
+    if want64:
+        out.update(y64=y64, rstd64=r64)
+    return out
+
+
+def bwd(dy, x, rstd, gamma, eps, x_dtype="bf16", w_dtype=None, want64=True):
+    """dx (x_dtype) and dgamma (fp32) of the forward; ``rstd`` None recomputes r
+    from x and eps.  With ``want64`` also dx64, dgamma64 and the error scales
+    c64, dot_abs64 (per row) and dgamma_sq64 (per column)."""
+    w_dtype = w_dtype or x_dtype
+    x = _check_in(x, x_dtype)
+    M, N = x.shape
+    dy = _check_in(dy, x_dtype, (M, N))
+    gamma = _check_in(gamma, w_dtype, (N,))
+    if rstd is not None:
+        rstd = _check_in(rstd, "f32", (M,))
+    dx = np.empty((M, N), _np(x_dtype))
+    dgamma = np.empty(N, np.float32)
+    extra = {}
+    if want64:
+        extra = {"dx64": np.empty((M, N), np.float64), "dgamma64": np.empty(N, np.float64),
+                 "c64": np.empty(M, np.float64), "dot_abs64": np.empty(M, np.float64),
+                 "dgamma_sq64": np.empty(N, np.float64)}
+    rc = _load().oracle_rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(rstd), _ptr(gamma), M, N,
+                                    float(eps), DTYPE_CODES[x_dtype], DTYPE_CODES[w_dtype],
+                                    _ptr(dx), _ptr(extra.get("dx64")),
+                                    _ptr(extra.get("dgamma64")), _ptr(dgamma),
+                                    _ptr(extra.get("c64")), _ptr(extra.get("dot_abs64")),
+                                    _ptr(extra.get("dgamma_sq64")))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_bwd rejected its arguments")
+    out = {"dx": dx, "dgamma": dgamma}
+    out.update(extra)
+    return out

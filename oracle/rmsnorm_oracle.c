@@ -1,0 +1,237 @@
+/*
+ * RMSNorm oracle: plain, slow, double-precision CPU reference.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and the
+ * bench's CPU-baseline / reference arm may load or run this file; the CUDA
+ * library never links it and shares no code with it.
+ *
+ * What it computes (definitions from "Pre-built kernel library guide" (FlyDSL),
+ * section 1.2 RMSNorm):
+ *   forward      RMSNorm(x) = x / sqrt(mean(x^2) + eps) * gamma, per row of an
+ *                M x N row-major matrix; rstd = 1 / sqrt(mean(x^2) + eps) is the
+ *                optional per-row output that the backward reads, so eps is
+ *                folded into rstd and the backward does not need it.
+ *   fused add    the residual-add variant named in "TIRx kernels", Kernels list
+ *                (flashinfer.norm: fused_add_rmsnorm): h = residual + x, stored in
+ *                the activation dtype, then y = RMSNorm(h) * gamma of that stored h.
+ *   backward     dx and the weight gradient of the forward (same section: reads
+ *                Input, Gamma, DY, Rstd; writes DX and DWeight).  The pages give
+ *                no formula; differentiating y_j = gamma_j x_j r with
+ *                r = (sum_k x_k^2 / N + eps)^(-1/2) gives
+ *                  dx_j     = r (gamma_j dy_j - x_j c),  c = r^2/N sum_k gamma_k dy_k x_k
+ *                  dgamma_j = sum_rows dy_j x_j r
+ *                with r the saved rstd when one is given.
+ *
+ * Every sum is a plain left-to-right double-precision loop; every stored
+ * output is rounded once, from double, to its dtype (round to nearest even).
+ * Pins: all functions are pinned by the CPU tests (closed forms, the eps = 0
+ * invariants, the backward orthogonality identity, central finite differences,
+ * library routines on special cases, hand-derived fixtures).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* ---- storage types -------------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32: widen the bits, reinterpret. */
+double oracle_bf16_to_double(uint16_t b) {
+  uint32_t w = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* Nearest bf16 to v, ties to even, straight from double (no fp32 step, which
+ * could round twice).  bf16: sign, 8-bit exponent (bias 127), 7-bit fraction;
+ * subnormals below 2^-126 with spacing 2^-133; overflow to infinity. */
+uint16_t oracle_round_bf16(double v) {
+  if (v != v) return 0x7FC0;                       /* NaN stays NaN */
+  uint16_t s = signbit(v) ? 0x8000u : 0u;
+  double a = fabs(v);
+  if (isinf(a)) return (uint16_t)(s | 0x7F80u);
+  /* find the binade: 2^k <= a < 2^(k+1); spacing of bf16 there is 2^(k-7) */
+  int k;
+  if (a == 0.0) return s;
+  frexp(a, &k);
+  k -= 1;
+  if (k < -126) k = -126;
+  double ulp = ldexp(1.0, k - 7);
+  double n = a / ulp;                              /* exact (power of two) */
+  double lo = floor(n);
+  double frac = n - lo;
+  double m = lo;
+  if (frac > 0.5) m = lo + 1.0;
+  else if (frac == 0.5) m = (fmod(lo, 2.0) == 0.0) ? lo : lo + 1.0;
+  /* m * ulp is the rounded magnitude; m in [0, 256] */
+  double rounded = m * ulp;
+  if (rounded > 3.3895313892515355e38) return (uint16_t)(s | 0x7F80u); /* > max finite */
+  float rf = (float)rounded;                       /* exact: 8 significant bits */
+  uint32_t w;
+  memcpy(&w, &rf, sizeof w);
+  return (uint16_t)(s | (uint16_t)((w >> 16) & 0x7FFFu));
+}
+
+static double load(const void* p, int dt, int64_t i) {
+  if (dt == ORACLE_F32) return (double)((const float*)p)[i];
+  return oracle_bf16_to_double(((const uint16_t*)p)[i]);
+}
+
+static void store(void* p, int dt, int64_t i, double v) {
+  if (dt == ORACLE_F32)
+    ((float*)p)[i] = (float)v;                     /* C conversion: nearest even */
+  else
+    ((uint16_t*)p)[i] = oracle_round_bf16(v);
+}
+
+static int bad_dtypes(int x_dtype, int w_dtype) {
+  if (x_dtype == ORACLE_F32) return w_dtype != ORACLE_F32;
+  if (x_dtype == ORACLE_BF16) return w_dtype != ORACLE_F32 && w_dtype != ORACLE_BF16;
+  return 1;
+}
+
+/* ---- forward ------------------------------------------------------------- */
+
+/* One row: r = 1/sqrt(mean(v^2) + eps), y = v * r * gamma. */
+static void fwd_row(const double* v, const void* gamma, int w_dtype, int64_t N, double eps,
+                    double* r_out, double* y_row) {
+  double ss = 0.0;
+  for (int64_t j = 0; j < N; ++j) ss += v[j] * v[j];
+  double mean_sq = ss / (double)N;
+  double r = 1.0 / sqrt(mean_sq + eps);
+  *r_out = r;
+  for (int64_t j = 0; j < N; ++j) y_row[j] = v[j] * r * load(gamma, w_dtype, j);
+}
+
+/* x: M x N (x_dtype); gamma: N (w_dtype).  Outputs (each may be NULL):
+ * y (x_dtype, rounded once), y64 (exact-ish double), rstd (fp32, rounded once),
+ * rstd64 (double).  Returns 0, or -1 on bad arguments. */
+int oracle_rmsnorm_fwd(const void* x, const void* gamma, int64_t M, int64_t N, double eps,
+                       int x_dtype, int w_dtype, void* y, double* y64, float* rstd,
+                       double* rstd64) {
+  if (M < 0 || N <= 0 || bad_dtypes(x_dtype, w_dtype) || (M > 0 && (!x || !gamma)))
+    return -1;
+  double* v = (double*)malloc((size_t)N * sizeof(double));
+  double* yr = (double*)malloc((size_t)N * sizeof(double));
+  if (!v || !yr) { free(v); free(yr); return -1; }
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) v[j] = load(x, x_dtype, i * N + j);
+    double r;
+    fwd_row(v, gamma, w_dtype, N, eps, &r, yr);
+    if (rstd) rstd[i] = (float)r;
+    if (rstd64) rstd64[i] = r;
+    for (int64_t j = 0; j < N; ++j) {
+      if (y) store(y, x_dtype, i * N + j, yr[j]);
+      if (y64) y64[i * N + j] = yr[j];
+    }
+  }
+  free(v);
+  free(yr);
+  return 0;
+}
+
+/* ---- fused residual add + forward ---------------------------------------- */
+
+/* h = residual + x rounded to x_dtype (the stored new residual), then the
+ * forward of that stored h.  residual is read only; h is a separate output
+ * (may be NULL).  Other outputs as in oracle_rmsnorm_fwd. */
+int oracle_rmsnorm_fused_add_fwd(const void* x, const void* residual, const void* gamma,
+                                 int64_t M, int64_t N, double eps, int x_dtype, int w_dtype,
+                                 void* h, void* y, double* y64, float* rstd, double* rstd64) {
+  if (M < 0 || N <= 0 || bad_dtypes(x_dtype, w_dtype) ||
+      (M > 0 && (!x || !residual || !gamma)))
+    return -1;
+  double* v = (double*)malloc((size_t)N * sizeof(double));
+  double* yr = (double*)malloc((size_t)N * sizeof(double));
+  void* hr = malloc((size_t)N * 4);
+  if (!v || !yr || !hr) { free(v); free(yr); free(hr); return -1; }
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      double sum = load(residual, x_dtype, i * N + j) + load(x, x_dtype, i * N + j);
+      store(hr, x_dtype, j, sum);
+      v[j] = load(hr, x_dtype, j);                 /* normalise the stored h */
+      if (h) store(h, x_dtype, i * N + j, sum);
+    }
+    double r;
+    fwd_row(v, gamma, w_dtype, N, eps, &r, yr);
+    if (rstd) rstd[i] = (float)r;
+    if (rstd64) rstd64[i] = r;
+    for (int64_t j = 0; j < N; ++j) {
+      if (y) store(y, x_dtype, i * N + j, yr[j]);
+      if (y64) y64[i * N + j] = yr[j];
+    }
+  }
+  free(v);
+  free(yr);
+  free(hr);
+  return 0;
+}
+
+/* ---- backward ------------------------------------------------------------ */
+
+/* dy, x: M x N (x_dtype); rstd: M fp32 saved by the forward, or NULL to
+ * recompute r = 1/sqrt(mean(x^2) + eps) from x; gamma: N (w_dtype).
+ * Outputs (each may be NULL):
+ *   dx (x_dtype, rounded once), dx64 (double) -- M x N
+ *   dgamma64 (double, N), dgamma (fp32, N, rounded once from dgamma64)
+ *   c64 (double, M): c of each row;  dot_abs64 (double, M): sum_k |gamma_k dy_k x_k|
+ *   dgamma_sq64 (double, N): sum over rows of (dy x r)^2
+ * The last three size the error of a finite-precision evaluation. */
+int oracle_rmsnorm_bwd(const void* dy, const void* x, const float* rstd, const void* gamma,
+                       int64_t M, int64_t N, double eps, int x_dtype, int w_dtype, void* dx,
+                       double* dx64, double* dgamma64, float* dgamma, double* c64,
+                       double* dot_abs64, double* dgamma_sq64) {
+  if (M < 0 || N <= 0 || bad_dtypes(x_dtype, w_dtype) ||
+      (M > 0 && (!dy || !x || !gamma)))
+    return -1;
+  double* g = (double*)malloc((size_t)N * sizeof(double));
+  double* acc = (double*)calloc((size_t)N, sizeof(double));
+  double* acc2 = (double*)calloc((size_t)N, sizeof(double));
+  if (!g || !acc || !acc2) { free(g); free(acc); free(acc2); return -1; }
+  for (int64_t j = 0; j < N; ++j) g[j] = load(gamma, w_dtype, j);
+  for (int64_t i = 0; i < M; ++i) {
+    double r;
+    if (rstd) {
+      r = (double)rstd[i];
+    } else {
+      double ss = 0.0;
+      for (int64_t j = 0; j < N; ++j) {
+        double xv = load(x, x_dtype, i * N + j);
+        ss += xv * xv;
+      }
+      r = 1.0 / sqrt(ss / (double)N + eps);
+    }
+    double dot = 0.0, dabs = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+      double t = g[j] * load(dy, x_dtype, i * N + j) * load(x, x_dtype, i * N + j);
+      dot += t;
+      dabs += fabs(t);
+    }
+    double c = r * r / (double)N * dot;
+    if (c64) c64[i] = c;
+    if (dot_abs64) dot_abs64[i] = dabs;
+    for (int64_t j = 0; j < N; ++j) {
+      double dyv = load(dy, x_dtype, i * N + j);
+      double xv = load(x, x_dtype, i * N + j);
+      double d = r * (g[j] * dyv - xv * c);
+      if (dx) store(dx, x_dtype, i * N + j, d);
+      if (dx64) dx64[i * N + j] = d;
+      double t = dyv * xv * r;
+      acc[j] += t;
+      acc2[j] += t * t;
+    }
+  }
+  for (int64_t j = 0; j < N; ++j) {
+    if (dgamma64) dgamma64[j] = acc[j];
+    if (dgamma) dgamma[j] = (float)acc[j];
+    if (dgamma_sq64) dgamma_sq64[j] = acc2[j];
+  }
+  free(g);
+  free(acc);
+  free(acc2);
+  return 0;
+}
