@@ -1,0 +1,529 @@
+"""RMSNorm throughput on GB300: achieved HBM GB/s of forward, fused residual-add
+forward and backward, bf16, against the HBM roofline.
+
+One step = the whole path once on the three full-size workloads:
+  forward    16384 x 8192  bf16 (bf16 gamma, writes y and fp32 rstd)
+  fused add  32768 x 4096  bf16 (h = r + x over r, y; 0.1 % outliers in r, x)
+  backward   16384 x 8192  bf16 (fp32 gamma, saved rstd; dx and fp32 dgamma)
+value = algorithmic HBM bytes of the step / device time of the step.  Every
+operand is at least 256 MiB, larger than the 126 MiB L2, so no flush is
+needed between steps.  Launch with torchrun for N > 1: every rank runs the
+same workload on its own GPU (independent replicas, weak scaling) and the
+slowest rank's time counts.
+
+--impl reference times the double-precision CPU oracle on the same step
+(bounded row samples of each workload), on this host's cores.
+--sweep prints one line per shape of the fwd/bwd shape sweep instead (each
+launch timed alone with an L2 flush before it).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm fwd/fused-add/bwd achieved HBM GB/s and % of GB300 peak (bf16, M x N)"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+STEP_WORKLOADS = ("fwd_bf16_m16384_n8192", "fadd_bf16_m32768_n4096", "bwd_bf16_m16384_n8192")
+LAUNCHES_PER_OP = {"fwd": 1, "fused_add": 1, "bwd": 2}
+
+
+def esize(dt):
+    return 4 if dt == "f32" else 2
+
+
+def alg_bytes(wl, rows=None) -> int:
+    """Bytes the operation must move: activations per row, plus gamma (and
+    dgamma) once per call; the dgamma workspace is not counted."""
+    M = wl.M if rows is None else rows
+    sx, sw, N = esize(wl.x_dtype), esize(wl.w_dtype), wl.N
+    rstd = 4 * M if (wl.store_rstd and wl.op != "bwd") else 0
+    if wl.op == "fwd":
+        return M * N * 2 * sx + N * sw + rstd
+    if wl.op == "fused_add":
+        return M * N * 4 * sx + N * sw + rstd
+    return M * N * 3 * sx + 4 * M + N * sw + 4 * N
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_wise_normalization_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(op: str):
+    """DRAM bytes per launch of an op from the committed ncu summary, or None
+    when the summary is missing or was taken on other kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != source_hash():
+        return None
+    v = d.get("per_launch_bytes", {}).get(op)
+    return int(v) if v is not None else None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while it runs."""
+
+    QUERY = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid=None, period_ms=50):
+        self.proc = None
+        self.uuid = (device_uuid or "").lower().replace("gpu-", "")
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               f"-lms={period_ms}"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        self.lines = []
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        uuids = {ln.split(",")[0].strip().lower() for ln in self.lines}
+        for ln in self.lines:
+            f = [c.strip() for c in ln.split(",")]
+            if len(uuids) > 1 and self.uuid and not f[0].lower().endswith(self.uuid):
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names[1:], f[5:9]):
+                if v.lower().startswith("active") or v == "0x1":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world):
+    import torch
+
+    import __graft_entry__
+    import row_wise_normalization_02_gb300 as rn
+    import seeded_inputs as si
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    wls = [si.WORKLOADS[n] for n in STEP_WORKLOADS]
+
+    def to_dev(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.to(dev)
+
+    ops = []
+    host = []
+    for wl in wls:
+        inp = si.make_inputs(wl)
+        d = {k: to_dev(v) for k, v in inp.items()}
+        act = torch.int16 if wl.x_dtype == "bf16" else torch.float32
+        M, N, eps = wl.M, wl.N, float(np.float32(wl.eps))
+        if wl.op == "fwd":
+            d["y"] = torch.empty((M, N), dtype=act, device=dev)
+            d["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
+
+            def launch(d=d, wl=wl, M=M, N=N, eps=eps):
+                rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"], d["rstd"], M, N, eps, wl.x_dtype,
+                               wl.w_dtype, stream)
+            outs = ("y", "rstd")
+            ins = ("x", "gamma")
+        elif wl.op == "fused_add":
+            d["y"] = torch.empty((M, N), dtype=act, device=dev)
+
+            def launch(d=d, wl=wl, M=M, N=N, eps=eps):
+                rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], d["y"], None, M, N,
+                                         eps, wl.x_dtype, wl.w_dtype, stream)
+            outs = ("residual", "y")
+            ins = ("x", "residual", "gamma")
+        else:
+            d["dx"] = torch.empty((M, N), dtype=act, device=dev)
+            d["dgamma"] = torch.empty(N, dtype=torch.float32, device=dev)
+            d["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
+            ws = rn.rmsnorm_bwd_workspace_size(M, N, wl.x_dtype, wl.w_dtype)
+            d["ws"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+            # saved rstd of this x, from the forward kernel (outside timing)
+            ytmp = torch.empty((M, N), dtype=act, device=dev)
+            with torch.cuda.stream(stream):
+                rn.rmsnorm_fwd(d["x"], d["gamma"], ytmp, d["rstd"], M, N, eps, wl.x_dtype,
+                               wl.w_dtype, stream)
+            stream.synchronize()
+            del ytmp
+
+            def launch(d=d, wl=wl, M=M, N=N, eps=eps, ws=ws):
+                rn.rmsnorm_bwd(d["dy"], d["x"], d["rstd"], d["gamma"], d["dx"], d["dgamma"],
+                               d["ws"], ws, M, N, eps, wl.x_dtype, wl.w_dtype, stream)
+            outs = ("dx", "dgamma")
+            ins = ("x", "dy", "rstd", "gamma")
+        plan = rn.rmsnorm_describe_plan({"fwd": 0, "fused_add": 1, "bwd": 2}[wl.op], M, N,
+                                        wl.x_dtype, wl.w_dtype)
+        ops.append(dict(wl=wl, d=d, launch=launch, outs=outs, ins=ins, plan=plan,
+                        bytes=alg_bytes(wl)))
+        host.append(inp)
+    torch.cuda.synchronize()
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            for op in ops:
+                op["launch"]()
+    stream.synchronize()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)] for _ in ops]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(K):
+            for j, op in enumerate(ops):
+                ev[j][i][0].record(stream)
+                op["launch"]()
+                ev[j][i][1].record(stream)
+        t_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    step_bytes = sum(op["bytes"] for op in ops)
+    ms_per_step = total_ms / K
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    per_op = {}
+    for j, op in enumerate(ops):
+        times = [a.elapsed_time(b) for a, b in ev[j]]
+        avg = sum(times) / len(times)
+        gbs = op["bytes"] / (avg * 1e-3) / 1e9
+        wl = op["wl"]
+        per_op[wl.op] = {"workload": wl.name, "avg_us": round(avg * 1e3, 2),
+                         "median_us": round(statistics.median(times) * 1e3, 2),
+                         "min_us": round(min(times) * 1e3, 2), "gbs": round(gbs, 1),
+                         "frac_of_measured_peak": round(gbs / peak, 4),
+                         "rows_per_s": round(wl.M / (avg * 1e-3), 1),
+                         "alg_bytes": op["bytes"], "launches": LAUNCHES_PER_OP[wl.op],
+                         "variant": op["plan"]}
+    dom = max(per_op, key=lambda k: per_op[k]["avg_us"])
+    d = per_op[dom]
+    roofline = {"bound": "hbm", "achieved": d["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": round(d["gbs"] / peak, 4), "traffic": ncu_traffic(dom),
+                "kernel": f"{dom} ({d['workload']}, {d['variant']})",
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src ==
+                "measured" else "fallback 6800 GB/s"}
+
+    # ---- end to end through the C ABI with pinned host buffers
+    Ke = max(3, min(K, args.e2e_steps))
+    pin = []
+    h2d = d2h = 0
+    for op, inp in zip(ops, host):
+        hin = {k: torch.from_numpy(inp[k].view(np.int16) if inp[k].dtype == np.uint16
+                                   else inp[k]).pin_memory() for k in op["ins"] if k in inp}
+        if "rstd" in op["ins"]:
+            hin["rstd"] = op["d"]["rstd"].cpu().pin_memory()
+        hout = {k: torch.empty_like(op["d"][k], device="cpu").pin_memory() for k in op["outs"]}
+        h2d += sum(t.numel() * t.element_size() for t in hin.values())
+        d2h += sum(t.numel() * t.element_size() for t in hout.values())
+        pin.append((hin, hout))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke):
+            for op, (hin, hout) in zip(ops, pin):
+                for k, t in hin.items():
+                    op["d"][k].copy_(t, non_blocking=True)
+                op["launch"]()
+                for k, t in hout.items():
+                    t.copy_(op["d"][k], non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+           "ms_per_step": round(e2e_ms, 3), "pinned": True}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "rmsnorm step: fwd bf16 16384x8192 (+rstd) + fused-add bf16 "
+                                   "32768x4096 + bwd bf16 16384x8192 (fp32 gamma, dgamma)",
+                       "step_alg_bytes": step_bytes,
+                       "l2": "inputs larger than L2 (every operand >= 256 MiB; L2 126 MiB)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "frac_of_measured_peak": round(value / world / peak, 4),
+            "frac_of_nominal_7900": round(value / world / NOMINAL_HBM_GBS, 4),
+            "roofline": roofline, "ops": per_op, "e2e": e2e,
+            "gpu_launches": K * sum(LAUNCHES_PER_OP[op["wl"].op] for op in ops),
+            "clocks": sampler.summary() if sampler else None}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------------ oracle
+
+def _oracle_step(samples):
+    """Run the oracle once over the sampled rows of the three workloads."""
+    import oracle
+    t0 = time.perf_counter()
+    done = 0
+    for wl, inp in samples:
+        eps = float(np.float32(wl.eps))
+        if wl.op == "fwd":
+            oracle.fwd(inp["x"], inp["gamma"], eps, wl.x_dtype, wl.w_dtype, want64=False)
+        elif wl.op == "fused_add":
+            oracle.fused_add_fwd(inp["x"], inp["residual"], inp["gamma"], eps, wl.x_dtype,
+                                 wl.w_dtype, want64=False)
+        else:
+            oracle.bwd(inp["dy"], inp["x"], inp["rstd"], inp["gamma"], eps, wl.x_dtype,
+                       wl.w_dtype, want64=False)
+        done += alg_bytes(wl, rows=inp["x"].shape[0])
+    return time.perf_counter() - t0, done
+
+
+def _samples(rows_fraction):
+    import oracle
+    import seeded_inputs as si
+    out = []
+    for n in STEP_WORKLOADS:
+        wl = si.WORKLOADS[n]
+        rows = max(1, int(wl.M * rows_fraction))
+        inp = si.make_inputs(wl, rows=rows)
+        if wl.op == "bwd":
+            inp["rstd"] = oracle.fwd(inp["x"], inp["gamma"], float(np.float32(wl.eps)),
+                                     wl.x_dtype, wl.w_dtype, want64=False)["rstd"]
+        out.append((wl, inp))
+    return out
+
+
+def cpu_baseline(target_s=12.0):
+    """The oracle as it stands (single-threaded C, double precision) on a
+    bounded row sample of each workload of the step, scaled to GB/s."""
+    probe = _samples(1 / 256)
+    t, b = _oracle_step(probe)
+    frac = min(1.0, max(1 / 256, target_s / max(t, 1e-6) / 256))
+    samples = _samples(frac)
+    t, b = _oracle_step(samples)
+    rows = {wl.name: inp["x"].shape[0] for wl, inp in samples}
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(t, 2),
+            "sample": "first rows of each step workload: " +
+                      ", ".join(f"{k} {v} rows" for k, v in rows.items())}
+
+
+def run_reference(args):
+    """Reference arm: the oracle on the host cores, K timed steps after W
+    warm-up steps, each step a bounded row sample of the three workloads."""
+    budget_s = 120.0
+    probe = _samples(1 / 512)
+    t, _ = _oracle_step(probe)
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1 / 16384, per_step / max(t, 1e-6) / 512))
+    samples = _samples(frac)
+    for _ in range(args.warmup):
+        _oracle_step(samples)
+    tot_t = tot_b = 0.0
+    for _ in range(args.steps):
+        t, b = _oracle_step(samples)
+        tot_t += t
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    rows = {wl.name: inp["x"].shape[0] for wl, inp in samples}
+    sample = "first rows of each step workload: " + ", ".join(f"{k} {v} rows"
+                                                             for k, v in rows.items())
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "rmsnorm step: fwd bf16 16384x8192 (+rstd) + fused-add bf16 "
+                                   "32768x4096 + bwd bf16 16384x8192 (fp32 gamma, dgamma)",
+                       "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ sweep
+
+def run_sweep(args):
+    import torch
+
+    import __graft_entry__
+    import row_wise_normalization_02_gb300 as rn
+    import seeded_inputs as si
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    peak, _ = measured_peak()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(4 * l2, dtype=torch.uint8, device=dev)
+    names = args.workloads.split(",") if args.workloads else [
+        n for n, w in si.WORKLOADS.items() if "sweep" in w.tags or "headline" in w.tags]
+    for name in names:
+        wl = si.WORKLOADS[name]
+        inp = si.make_inputs(wl)
+        d = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev)
+             for k, v in inp.items()}
+        act = torch.int16 if wl.x_dtype == "bf16" else torch.float32
+        M, N, eps = wl.M, wl.N, float(np.float32(wl.eps))
+        y = torch.empty((M, N), dtype=act, device=dev)
+        rstd = torch.empty(M, dtype=torch.float32, device=dev)
+        rn.rmsnorm_fwd(d["x"], d["gamma"], y, rstd, M, N, eps, wl.x_dtype, wl.w_dtype, stream)
+        if wl.op == "fwd":
+            def launch():
+                rn.rmsnorm_fwd(d["x"], d["gamma"], y, rstd if wl.store_rstd else None, M, N, eps,
+                               wl.x_dtype, wl.w_dtype, stream)
+        elif wl.op == "fused_add":
+            def launch():
+                rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], y, None, M, N, eps,
+                                         wl.x_dtype, wl.w_dtype, stream)
+        else:
+            dg = torch.empty(N, dtype=torch.float32, device=dev)
+            ws = rn.rmsnorm_bwd_workspace_size(M, N, wl.x_dtype, wl.w_dtype)
+            wsb = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
+
+            def launch():
+                rn.rmsnorm_bwd(d["dy"], d["x"], rstd, d["gamma"], y, dg, wsb, ws, M, N, eps,
+                               wl.x_dtype, wl.w_dtype, stream)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.add_(1)  # write 4 x L2 between launches: every launch starts cold
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                launch()
+                b.record(stream)
+                if i >= args.warmup:
+                    times.append((a, b))
+        stream.synchronize()
+        us = [a.elapsed_time(b) * 1e3 for a, b in times]
+        med = statistics.median(us)
+        byts = alg_bytes(wl)
+        op = {"fwd": 0, "fused_add": 1, "bwd": 2}[wl.op]
+        print(json.dumps({"workload": name, "op": wl.op, "M": M, "N": N,
+                          "variant": rn.rmsnorm_describe_plan(op, M, N, wl.x_dtype, wl.w_dtype),
+                          "median_us": round(med, 2), "min_us": round(min(us), 2),
+                          "max_us": round(max(us), 2), "gbs": round(byts / med / 1e3, 1),
+                          "frac_of_measured_peak": round(byts / med / 1e3 / peak, 4),
+                          "rows_per_s": round(M / med * 1e6, 1), "alg_bytes": byts,
+                          "l2": "flushed (4 x L2 written) before every launch"}), flush=True)
+        del d, y, rstd
+        torch.cuda.empty_cache()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--workloads", default="")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.sweep:
+        run_sweep(args)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

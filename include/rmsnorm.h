@@ -1,0 +1,126 @@
+/*
+ * rmsnorm.h -- C ABI of the GB300 (sm_103a) row-wise RMSNorm library.
+ *
+ * Operation ("Pre-built kernel library guide" (FlyDSL), section 1.2 RMSNorm):
+ * for every row i of an M x N row-major matrix,
+ *     rstd_i = 1 / sqrt(mean_j(x_ij^2) + eps)
+ *     y_ij   = x_ij * rstd_i * gamma_j
+ * with fp32 accumulation and one final round-to-nearest-even to the output
+ * dtype.  The same section names the optional per-row rstd output read by the
+ * backward (eps folded into it) and fp32 weights with 16-bit activations.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller.  The library never
+ *    allocates, frees or synchronises; work is enqueued on `stream` (0 = the
+ *    legacy default stream) of the current device.
+ *  - Layout: contiguous row-major, row stride N elements.
+ *  - Dtypes: output dtype = x_dtype; rstd and dgamma are always fp32.
+ *    Supported (x_dtype, w_dtype) pairs: (F32, F32), (BF16, BF16), (BF16, F32).
+ *  - Alignment: each pointer must be aligned to its element size; 16-byte
+ *    alignment of the rows is NOT required (ragged rows take a slower path).
+ *  - Sizes: M == 0 returns RMSNORM_OK without launching; M < 0, N < 1,
+ *    N > 2^30, or eps < 0 / NaN return RMSNORM_ERR_INVALID_ARG.
+ *  - Aliasing: only fused-add's `residual` is in-out.  Any other overlap of
+ *    an output with another operand returns RMSNORM_ERR_INVALID_ARG.
+ *  - Errors: a status is returned, no exception crosses the ABI, the device
+ *    never traps.  Argument errors launch nothing.  RMSNORM_ERR_CUDA means a
+ *    CUDA call failed (the sticky error of `cudaGetLastError` is consumed).
+ *  - Non-finite inputs propagate (a zero row with eps = 0 gives NaN).
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same declaration as the CUDA runtime's, so either header may come first. */
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum rmsnorm_dtype {
+  RMSNORM_F32 = 0,  /* IEEE binary32 */
+  RMSNORM_BF16 = 1  /* bfloat16 (upper half of binary32) */
+} rmsnorm_dtype_t;
+
+typedef enum rmsnorm_status {
+  RMSNORM_OK = 0,
+  RMSNORM_ERR_INVALID_ARG = 1,       /* bad size, NULL pointer, overlap, eps */
+  RMSNORM_ERR_UNSUPPORTED_DTYPE = 2, /* (x_dtype, w_dtype) pair not supported */
+  RMSNORM_ERR_MISALIGNED = 3,        /* pointer not aligned to its element size */
+  RMSNORM_ERR_WORKSPACE = 4,         /* backward workspace NULL or too small */
+  RMSNORM_ERR_CUDA = 5               /* a CUDA runtime call failed */
+} rmsnorm_status_t;
+
+/*
+ * Forward.  x: M x N (x_dtype), gamma: N (w_dtype), y: M x N (x_dtype).
+ * rstd: M fp32, or NULL to skip it.  Reads x and gamma once, writes y (and
+ * rstd).
+ */
+rmsnorm_status_t rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
+                             int64_t M, int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                             rmsnorm_dtype_t w_dtype, cudaStream_t stream);
+
+/*
+ * Fused residual add + forward (the fused-add variant listed in "TIRx
+ * kernels", Kernels list, flashinfer.norm ports).  Per element
+ *     h_ij = round_xdtype(residual_ij + x_ij)      written over residual
+ *     y_ij = RMSNorm(h)_ij * gamma_j               (of the stored, rounded h)
+ * x: M x N (read only); residual: M x N, in: r, out: h; gamma: N; y: M x N;
+ * rstd: M fp32 of h, or NULL.
+ */
+rmsnorm_status_t rmsnorm_fused_add_fwd(const void* x, void* residual, const void* gamma,
+                                       void* y, float* rstd, int64_t M, int64_t N, float eps,
+                                       rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                                       cudaStream_t stream);
+
+/*
+ * Workspace of rmsnorm_bwd, in bytes, for these sizes on `device` (-1: the
+ * current device).  It depends on the device's SM count.  Writes *bytes
+ * (0 when M == 0 or no dgamma is wanted is still a valid answer to pass).
+ */
+rmsnorm_status_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
+                                            rmsnorm_dtype_t w_dtype, int device,
+                                            size_t* bytes);
+
+/*
+ * Backward ("Pre-built kernel library guide", section 1.2: reads the forward's
+ * input, gamma, dy and rstd; writes dx and the weight gradient).  With
+ *     c_i = rstd_i^2 / N * sum_k gamma_k dy_ik x_ik
+ *     dx_ij     = rstd_i * (gamma_j dy_ij - x_ij c_i)         (x_dtype)
+ *     dgamma_j  = sum_i dy_ij x_ij rstd_i                      (fp32)
+ * dy, x, dx: M x N; gamma: N; rstd: M fp32 from the forward (eps is then
+ * ignored), or NULL to recompute it from x and eps.  dgamma: N fp32, or NULL
+ * to skip the weight gradient.  dgamma is reduced over the rows in a fixed
+ * order through `workspace` (device memory of at least
+ * rmsnorm_bwd_workspace_size bytes, 16-byte aligned, contents ignored), so it
+ * is bit-for-bit reproducible run to run on the same device.  Two launches on
+ * `stream`.
+ */
+rmsnorm_status_t rmsnorm_bwd(const void* dy, const void* x, const float* rstd,
+                             const void* gamma, void* dx, float* dgamma, void* workspace,
+                             size_t workspace_bytes, int64_t M, int64_t N, float eps,
+                             rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                             cudaStream_t stream);
+
+/* Static text of a status code ("unknown status" for other values). */
+const char* rmsnorm_status_string(rmsnorm_status_t status);
+
+/*
+ * The kernel variant the library would launch for this call shape, as text
+ * (for example "fwd/cta/vpt4/t256"), into buf (NUL-terminated, truncated to
+ * len).  op: 0 forward, 1 fused add, 2 backward.  aligned16: nonzero when all
+ * operand base pointers are 16-byte aligned.  Returns RMSNORM_OK or an
+ * argument error; launches nothing.
+ */
+rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
+                                       rmsnorm_dtype_t w_dtype, int aligned16, int device,
+                                       char* buf, size_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

@@ -1,0 +1,142 @@
+"""Python binding of the GB300 RMSNorm C ABI (``include/rmsnorm.h``).
+
+Argument marshalling only: every function forwards to the entry point of the
+same name in ``librmsnorm_gb300.so`` and raises :class:`RMSNormError` on a
+non-OK status.  Pointers are device addresses (ints, or objects with a
+``data_ptr()`` method such as torch tensors); ``stream`` is a raw
+``cudaStream_t`` (int), an object with a ``cuda_stream`` attribute, or None
+for the legacy default stream.  Importing works without the library; the
+first call raises if it has not been built (``__graft_entry__.build()``) --
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "RMSNormError", "library_path",
+           "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
+           "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
+           "EXPORTED_SYMBOLS"]
+
+F32 = 0
+BF16 = 1
+OP_FWD, OP_FUSED_ADD, OP_BWD = 0, 1, 2
+_DT_NAMES = {"f32": F32, "bf16": BF16}
+
+EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspace_size",
+                    "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "librmsnorm_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class RMSNormError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {rmsnorm_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the shared library (raises if it is missing: no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(f"{_LIB_PATH} is not built; run __graft_entry__.build() "
+                                  "(nvcc, sm_103a) first")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I64, I, F, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                                ctypes.c_size_t)
+            lib.rmsnorm_fwd.argtypes = [P, P, P, P, I64, I64, F, I, I, P]
+            lib.rmsnorm_fwd.restype = I
+            lib.rmsnorm_fused_add_fwd.argtypes = [P, P, P, P, P, I64, I64, F, I, I, P]
+            lib.rmsnorm_fused_add_fwd.restype = I
+            lib.rmsnorm_bwd_workspace_size.argtypes = [I64, I64, I, I, I, ctypes.POINTER(SZ)]
+            lib.rmsnorm_bwd_workspace_size.restype = I
+            lib.rmsnorm_bwd.argtypes = [P, P, P, P, P, P, P, SZ, I64, I64, F, I, I, P]
+            lib.rmsnorm_bwd.restype = I
+            lib.rmsnorm_status_string.argtypes = [I]
+            lib.rmsnorm_status_string.restype = ctypes.c_char_p
+            lib.rmsnorm_describe_plan.argtypes = [I, I64, I64, I, I, I, I, ctypes.c_char_p, SZ]
+            lib.rmsnorm_describe_plan.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return int(a.data_ptr())
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _dt(d) -> int:
+    """dtype name ("f32", "bf16") or raw code (passed through unchanged)."""
+    return _DT_NAMES[d] if isinstance(d, str) else int(d)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise RMSNormError(status, where)
+
+
+def rmsnorm_fwd(x, gamma, y, rstd, M, N, eps, x_dtype, w_dtype, stream=None):
+    _check(load_library().rmsnorm_fwd(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), M, N, eps,
+                                      _dt(x_dtype), _dt(w_dtype), _stream(stream)),
+           "rmsnorm_fwd")
+
+
+def rmsnorm_fused_add_fwd(x, residual, gamma, y, rstd, M, N, eps, x_dtype, w_dtype,
+                          stream=None):
+    _check(load_library().rmsnorm_fused_add_fwd(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(y),
+                                                _ptr(rstd), M, N, eps, _dt(x_dtype),
+                                                _dt(w_dtype), _stream(stream)),
+           "rmsnorm_fused_add_fwd")
+
+
+def rmsnorm_bwd_workspace_size(M, N, x_dtype, w_dtype, device=-1) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().rmsnorm_bwd_workspace_size(M, N, _dt(x_dtype), _dt(w_dtype), device,
+                                                     ctypes.byref(out)),
+           "rmsnorm_bwd_workspace_size")
+    return int(out.value)
+
+
+def rmsnorm_bwd(dy, x, rstd, gamma, dx, dgamma, workspace, workspace_bytes, M, N, eps, x_dtype,
+                w_dtype, stream=None):
+    _check(load_library().rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(rstd), _ptr(gamma), _ptr(dx),
+                                      _ptr(dgamma), _ptr(workspace), workspace_bytes, M, N, eps,
+                                      _dt(x_dtype), _dt(w_dtype), _stream(stream)),
+           "rmsnorm_bwd")
+
+
+def rmsnorm_status_string(status: int) -> str:
+    try:
+        return load_library().rmsnorm_status_string(status).decode()
+    except ImportError:
+        return f"status {status}"
+
+
+def rmsnorm_describe_plan(op, M, N, x_dtype, w_dtype, aligned16=True, device=-1) -> str:
+    buf = ctypes.create_string_buffer(256)
+    _check(load_library().rmsnorm_describe_plan(op, M, N, _dt(x_dtype), _dt(w_dtype),
+                                                1 if aligned16 else 0, device, buf, 256),
+           "rmsnorm_describe_plan")
+    return buf.value.decode()

@@ -1,0 +1,583 @@
+// C ABI of the RMSNorm library: argument validation, the per-(op, dtype, N)
+// dispatch table, grid sizing and launches.  No kernels live here.
+//
+// Dispatch (aligned rows = every base pointer 16-byte aligned and N * size a
+// multiple of 16 bytes; E = elements per 16-byte vector):
+//   N / E <= 128        kSubwarp  G lanes per row (4..32), VPT vectors per lane,
+//                                 several rows per 256-thread CTA; the short-row
+//                                 packing idea of the softmax kernel's
+//                                 THREADS_PER_ROW / ROWS_PER_BLOCK knobs
+//                                 ("Pre-built kernel library guide", 2.1)
+//   N / E <= 4096       kCta      one row per CTA of ceil(N / E / VPT) threads,
+//                                 row in registers
+//   otherwise           kGeneric
+// Rows that are not 16-byte aligned but whose operands agree modulo 16 bytes
+// take kRagged (N <= kRaggedMaxN), anything else kGeneric.  Grids are
+// persistent: min(rows, SMs x resident CTAs per SM).
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/rmsnorm.h"
+#include "rmsnorm_internal.h"
+
+namespace rmsn {
+namespace {
+
+constexpr int64_t kMaxN = int64_t(1) << 30;
+constexpr int kRaggedMaxN = 24576;
+
+int esize(int dt) { return dt == kF32 ? 4 : 2; }
+int per_vec(int dt) { return 16 / esize(dt); }
+
+bool dtype_pair_ok(int xd, int wd) {
+  return (xd == kF32 && wd == kF32) || (xd == kBF16 && (wd == kBF16 || wd == kF32));
+}
+
+FwdKernel fwd_kernel(const FwdKey& k) {
+  if (k.xd == kF32 && k.wd == kF32) return get_fwd_kernel_f32_f32(k);
+  if (k.xd == kBF16 && k.wd == kBF16) return get_fwd_kernel_bf16_bf16(k);
+  if (k.xd == kBF16 && k.wd == kF32) return get_fwd_kernel_bf16_f32(k);
+  return nullptr;
+}
+BwdKernel bwd_kernel(const BwdKey& k) {
+  if (k.xd == kF32 && k.wd == kF32) return get_bwd_kernel_f32_f32(k);
+  if (k.xd == kBF16 && k.wd == kBF16) return get_bwd_kernel_bf16_bf16(k);
+  if (k.xd == kBF16 && k.wd == kF32) return get_bwd_kernel_bf16_f32(k);
+  return nullptr;
+}
+
+// ---------------------------------------------------------------- device info
+
+struct DevInfo {
+  int sms = 0;
+  int max_smem_optin = 0;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+cudaError_t device_info(int device, DevInfo* out) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev[device].sms == 0) {
+    int sms = 0, smem = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess) return e;
+    g_dev[device].sms = sms;
+    g_dev[device].max_smem_optin = smem;
+  }
+  *out = g_dev[device];
+  return cudaSuccess;
+}
+
+// Resident CTAs per SM of (kernel, threads, smem), cached.  Raises the
+// kernel's dynamic shared memory limit when a launch needs more than 48 KB.
+struct OccEntry {
+  const void* fn;
+  int device, threads, smem, blocks;
+};
+OccEntry g_occ[512];
+int g_nocc = 0;
+
+cudaError_t occupancy(const void* fn, int device, int threads, int smem, int* blocks) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < g_nocc; ++i)
+    if (g_occ[i].fn == fn && g_occ[i].device == device && g_occ[i].threads == threads &&
+        g_occ[i].smem == smem) {
+      *blocks = g_occ[i].blocks;
+      return cudaSuccess;
+    }
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  int b = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (b < 1) return cudaErrorInvalidConfiguration;
+  if (g_nocc < 512) g_occ[g_nocc++] = OccEntry{fn, device, threads, smem, b};
+  *blocks = b;
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- plans
+
+enum Op { kFwd = 0, kFused = 1, kBwd = 2 };
+
+struct Plan {
+  int family = kGeneric;
+  int g = 0, vpt = 0;
+  bool prefetch = false, acc_smem = false;
+  int threads = 256;
+  int smem = 0;
+  int rows_per_cta = 1;      // rows one CTA iteration covers
+  int cta_per_sm_cap = 0;    // 0: occupancy limit
+  const void* fn = nullptr;
+  FwdKernel fwd = nullptr;
+  BwdKernel bwd = nullptr;
+  int grid = 0;
+};
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+// Subwarp shape for nvec 16-byte vectors per row.
+void subwarp_shape(int nvec, int* g, int* vpt) {
+  if (nvec <= 4) { *g = 4; *vpt = 1; }
+  else if (nvec <= 8) { *g = 8; *vpt = 1; }
+  else if (nvec <= 16) { *g = 8; *vpt = 2; }
+  else if (nvec <= 32) { *g = 16; *vpt = 2; }
+  else if (nvec <= 64) { *g = 32; *vpt = 2; }
+  else if (nvec <= 96) { *g = 32; *vpt = 3; }
+  else { *g = 32; *vpt = 4; }
+}
+
+// Vectors per thread for a row of nvec vectors in one CTA, and the CTA size.
+bool cta_shape(int op, int nvec, int* vpt, int* threads) {
+  static const int pref_fwd[] = {4, 2, 8, 1};
+  static const int pref_fused[] = {2, 4, 1, 8};
+  static const int pref_bwd[] = {4, 2, 1, 8};
+  const int* pref = op == kFwd ? pref_fwd : op == kFused ? pref_fused : pref_bwd;
+  for (int i = 0; i < 4; ++i) {
+    const int v = pref[i];
+    const int t = round_up((nvec + v - 1) / v, 32);
+    if (t >= 64 && t <= kCtaMaxThreads) {
+      *vpt = v;
+      *threads = t;
+      return true;
+    }
+  }
+  // very short rows: smallest CTA
+  if (nvec <= 64) {
+    *vpt = 1;
+    *threads = 64;
+    return true;
+  }
+  return false;
+}
+
+// RMSNORM_FORCE_VARIANT="family[:key=value...]" with family one of subwarp,
+// cta, ragged, generic and keys g, vpt, t (threads), pf (0/1), acc (0/1
+// shared-memory dgamma partials), cps (CTAs per SM cap).  For profiling A/B
+// runs; a forced variant that cannot serve the call is an argument error.
+struct Force {
+  bool on = false;
+  int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0;
+};
+
+Force read_force() {
+  Force f;
+  const char* s = getenv("RMSNORM_FORCE_VARIANT");
+  if (!s || !*s) return f;
+  f.on = true;
+  char buf[128];
+  strncpy(buf, s, sizeof buf - 1);
+  buf[sizeof buf - 1] = 0;
+  char* save = nullptr;
+  char* tok = strtok_r(buf, ":", &save);
+  if (!tok) return f;
+  if (!strcmp(tok, "subwarp")) f.family = kSubwarp;
+  else if (!strcmp(tok, "cta")) f.family = kCta;
+  else if (!strcmp(tok, "ragged")) f.family = kRagged;
+  else if (!strcmp(tok, "generic")) f.family = kGeneric;
+  while ((tok = strtok_r(nullptr, ":", &save))) {
+    char* eq = strchr(tok, '=');
+    if (!eq) continue;
+    *eq = 0;
+    const int v = atoi(eq + 1);
+    if (!strcmp(tok, "g")) f.g = v;
+    else if (!strcmp(tok, "vpt")) f.vpt = v;
+    else if (!strcmp(tok, "t")) f.threads = v;
+    else if (!strcmp(tok, "pf")) f.pf = v;
+    else if (!strcmp(tok, "acc")) f.acc = v;
+    else if (!strcmp(tok, "cps")) f.cps = v;
+  }
+  return f;
+}
+
+// Choose the variant.  aligned16: all base pointers 16-byte aligned;
+// same_mod16: all activation base pointers agree modulo 16 bytes.
+rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligned16,
+                           bool same_mod16, bool has_rstd, Plan* pl) {
+  const int E = per_vec(xd);
+  const bool rows_aligned = aligned16 && ((int64_t)N * esize(xd)) % 16 == 0;
+  const int nvec = rows_aligned ? N / E : 0;
+  Plan p;
+  if (rows_aligned && nvec <= 128) {
+    p.family = kSubwarp;
+    subwarp_shape(nvec, &p.g, &p.vpt);
+    p.threads = kSubwarpThreads;
+    p.rows_per_cta = kSubwarpThreads / p.g;
+    p.prefetch = true;
+  } else if (rows_aligned && nvec <= 4096) {
+    p.family = kCta;
+    if (!cta_shape(op, nvec, &p.vpt, &p.threads)) p.family = kGeneric;
+    p.prefetch = p.vpt <= 2 || (op == kFwd && p.vpt <= 4);
+    p.acc_smem = op == kBwd && p.vpt >= 4;
+  } else if (same_mod16 && N <= kRaggedMaxN) {
+    p.family = kRagged;
+    if (!cta_shape(op, N / E + 1, &p.vpt, &p.threads)) p.family = kGeneric;
+    p.prefetch = p.vpt <= 2;
+  } else {
+    p.family = kGeneric;
+  }
+  if (p.family == kGeneric) {
+    p.threads = 256;
+    p.g = p.vpt = 0;
+    p.prefetch = false;
+  }
+
+  const Force f = read_force();
+  if (f.on) {
+    if (f.family >= 0) p.family = f.family;
+    if (f.g) p.g = f.g;
+    if (f.vpt) p.vpt = f.vpt;
+    if (f.threads) p.threads = f.threads;
+    if (f.pf >= 0) p.prefetch = f.pf != 0;
+    if (f.acc >= 0) p.acc_smem = f.acc != 0;
+    p.cta_per_sm_cap = f.cps;
+    if (p.family == kSubwarp) {
+      p.threads = kSubwarpThreads;
+      if (!rows_aligned || p.g < 1 || p.g > 32 || p.g * p.vpt * 1LL < nvec) return RMSNORM_ERR_INVALID_ARG;
+      p.rows_per_cta = kSubwarpThreads / p.g;
+    } else if (p.family == kCta) {
+      if (!rows_aligned) return RMSNORM_ERR_INVALID_ARG;
+      if (!f.threads) p.threads = round_up((nvec + p.vpt - 1) / (p.vpt ? p.vpt : 1), 32);
+      if (p.vpt < 1 || (int64_t)p.threads * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
+    } else if (p.family == kRagged) {
+      if (!same_mod16 || N > kRaggedMaxN) return RMSNORM_ERR_INVALID_ARG;
+      if (!f.threads) p.threads = round_up((N / E + 1 + p.vpt - 1) / (p.vpt ? p.vpt : 1), 32);
+      if (p.vpt < 1 || (int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
+    } else if (p.family == kGeneric) {
+      if (!f.threads) p.threads = 256;
+      if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
+    }
+    if (p.family != kSubwarp) p.rows_per_cta = 1;
+    if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32) return RMSNORM_ERR_INVALID_ARG;
+  }
+
+  // kernel and shared memory
+  if (op == kBwd) {
+    BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch};
+    p.bwd = bwd_kernel(k);
+    p.fn = reinterpret_cast<const void*>(p.bwd);
+    const int ld = round_up(N, 4);
+    if (p.family == kSubwarp) p.smem = p.rows_per_cta * nvec * E * 4;
+    else if (p.family == kCta) p.smem = 512 + (p.acc_smem ? ld * 4 : 0);
+    else if (p.family == kRagged) p.smem = 512 + 2 * ld * 4;
+    else p.smem = 0;
+  } else {
+    FwdKey k{xd, wd, p.family, p.g, p.vpt, op == kFused, p.prefetch};
+    p.fwd = fwd_kernel(k);
+    p.fn = reinterpret_cast<const void*>(p.fwd);
+    if (p.family == kCta) p.smem = 256;
+    else if (p.family == kRagged) p.smem = 256 + N * 4;
+    else p.smem = 0;
+  }
+  if (p.fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
+  *pl = p;
+  return RMSNORM_OK;
+}
+
+// Grid of a plan on a device: persistent, at most SMs x resident CTAs.
+rmsnorm_status_t size_grid(Plan* p, int64_t M, int device) {
+  DevInfo di;
+  if (device_info(device, &di) != cudaSuccess) return RMSNORM_ERR_CUDA;
+  if (p->smem > di.max_smem_optin) return RMSNORM_ERR_INVALID_ARG;
+  int per_sm = 0;
+  if (occupancy(p->fn, device, p->threads, p->smem, &per_sm) != cudaSuccess)
+    return RMSNORM_ERR_CUDA;
+  if (p->cta_per_sm_cap > 0 && per_sm > p->cta_per_sm_cap) per_sm = p->cta_per_sm_cap;
+  const int64_t units = (M + p->rows_per_cta - 1) / p->rows_per_cta;
+  const int64_t cap = (int64_t)di.sms * per_sm;
+  p->grid = (int)(units < cap ? units : cap);
+  if (p->grid < 1) p->grid = 1;
+  return RMSNORM_OK;
+}
+
+const char* family_name(int f) {
+  switch (f) {
+    case kSubwarp: return "subwarp";
+    case kCta: return "cta";
+    case kRagged: return "ragged";
+    default: return "generic";
+  }
+}
+
+void describe(int op, const Plan& p, char* buf, size_t len) {
+  static const char* ops[] = {"fwd", "fused_add", "bwd"};
+  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d%s/grid%d/smem%d", ops[op], family_name(p.family),
+           p.g, p.vpt, p.threads, p.prefetch ? 1 : 0,
+           op == kBwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem);
+}
+
+// ---------------------------------------------------------------- validation
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || !na || !nb) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+rmsnorm_status_t check_sizes(int64_t M, int64_t N, float eps) {
+  if (M < 0 || N < 1 || N > kMaxN) return RMSNORM_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || isinf(eps)) return RMSNORM_ERR_INVALID_ARG;
+  return RMSNORM_OK;
+}
+
+rmsnorm_status_t current_device(int* dev) {
+  return cudaGetDevice(dev) == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+rmsnorm_status_t launched() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- forward
+
+rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gamma, void* y,
+                          float* rstd, int64_t M, int64_t N, float eps, int xd, int wd,
+                          cudaStream_t stream) {
+  rmsnorm_status_t st = check_sizes(M, N, eps);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if (M == 0) return RMSNORM_OK;
+  if (!x || !gamma || !y || (op == kFused && !residual)) return RMSNORM_ERR_INVALID_ARG;
+  const size_t xs = (size_t)esize(xd), ws = (size_t)esize(wd);
+  if (!aligned_to(x, xs) || !aligned_to(y, xs) || !aligned_to(gamma, ws) ||
+      (residual && !aligned_to(residual, xs)) || (rstd && !aligned_to(rstd, 4)))
+    return RMSNORM_ERR_MISALIGNED;
+  const size_t act = (size_t)M * (size_t)N * xs, gb = (size_t)N * ws, rb = (size_t)M * 4;
+  if (overlap(y, act, x, act) || overlap(y, act, gamma, gb) || overlap(y, act, rstd, rb) ||
+      overlap(rstd, rb, x, act) || overlap(rstd, rb, gamma, gb))
+    return RMSNORM_ERR_INVALID_ARG;
+  if (op == kFused && (overlap(residual, act, x, act) || overlap(residual, act, y, act) ||
+                       overlap(residual, act, gamma, gb) || overlap(residual, act, rstd, rb)))
+    return RMSNORM_ERR_INVALID_ARG;
+
+  const uintptr_t mx = reinterpret_cast<uintptr_t>(x) & 15;
+  bool same = (reinterpret_cast<uintptr_t>(y) & 15) == mx;
+  if (op == kFused) same = same && (reinterpret_cast<uintptr_t>(residual) & 15) == mx;
+  const bool aligned16 = same && mx == 0 && aligned_to(gamma, 16);
+
+  int dev;
+  if ((st = current_device(&dev)) != RMSNORM_OK) return st;
+  Plan pl;
+  if ((st = make_plan(op, M, (int)N, xd, wd, aligned16, same, false, &pl)) != RMSNORM_OK)
+    return st;
+  if ((st = size_grid(&pl, M, dev)) != RMSNORM_OK) return st;
+
+  FwdParams prm;
+  prm.x = x;
+  prm.residual = residual;
+  prm.gamma = gamma;
+  prm.y = y;
+  prm.rstd = rstd;
+  prm.M = M;
+  prm.N = (int)N;
+  prm.nvec = (int)(N / per_vec(xd));
+  prm.eps = eps;
+  prm.inv_n = 1.0f / (float)N;
+  pl.fwd<<<pl.grid, pl.threads, pl.smem, stream>>>(prm);
+  return launched();
+}
+
+// ---------------------------------------------------------------- backward
+
+// Stage-1 CTA count bound for these sizes: the grid of the plan for 16-byte
+// aligned operands.  Every launch clamps its stage-1 grid to it, so the
+// workspace query does not need the pointers.
+rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, int* rows) {
+  Plan pl;
+  rmsnorm_status_t st = make_plan(kBwd, M, N, xd, wd, true, true, true, &pl);
+  if (st != RMSNORM_OK) {
+    // a forced variant that does not fit aligned operands: fall back to the
+    // unforced plan for the bound
+    return st;
+  }
+  if ((st = size_grid(&pl, M, device)) != RMSNORM_OK) return st;
+  *rows = pl.grid;
+  return RMSNORM_OK;
+}
+
+rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, const void* gamma,
+                          void* dx, float* dgamma, void* workspace, size_t workspace_bytes,
+                          int64_t M, int64_t N, float eps, int xd, int wd,
+                          cudaStream_t stream) {
+  rmsnorm_status_t st = check_sizes(M, N, eps);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if (M == 0) {
+    if (dgamma) {
+      if (cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    }
+    return RMSNORM_OK;
+  }
+  if (!dy || !x || !gamma || !dx) return RMSNORM_ERR_INVALID_ARG;
+  const size_t xs = (size_t)esize(xd), ws = (size_t)esize(wd);
+  if (!aligned_to(dy, xs) || !aligned_to(x, xs) || !aligned_to(dx, xs) ||
+      !aligned_to(gamma, ws) || (rstd && !aligned_to(rstd, 4)) ||
+      (dgamma && !aligned_to(dgamma, 4)))
+    return RMSNORM_ERR_MISALIGNED;
+  const size_t act = (size_t)M * (size_t)N * xs, gb = (size_t)N * ws, rb = (size_t)M * 4,
+               db = (size_t)N * 4;
+  if (overlap(dx, act, dy, act) || overlap(dx, act, x, act) || overlap(dx, act, gamma, gb) ||
+      overlap(dx, act, rstd, rb) || overlap(dx, act, dgamma, db) ||
+      overlap(dgamma, db, dy, act) || overlap(dgamma, db, x, act) ||
+      overlap(dgamma, db, gamma, gb) || overlap(dgamma, db, rstd, rb))
+    return RMSNORM_ERR_INVALID_ARG;
+
+  int dev;
+  if ((st = current_device(&dev)) != RMSNORM_OK) return st;
+  const int ld = round_up((int)N, 4);
+  int prows = 0;
+  if (dgamma) {
+    if ((st = bwd_partial_rows(M, (int)N, xd, wd, dev, &prows)) != RMSNORM_OK) return st;
+    const size_t need = (size_t)prows * ld * 4;
+    if (!workspace || workspace_bytes < need || !aligned_to(workspace, 16))
+      return RMSNORM_ERR_WORKSPACE;
+    if (overlap(workspace, need, dx, act) || overlap(workspace, need, dgamma, db) ||
+        overlap(workspace, need, dy, act) || overlap(workspace, need, x, act) ||
+        overlap(workspace, need, gamma, gb) || overlap(workspace, need, rstd, rb))
+      return RMSNORM_ERR_INVALID_ARG;
+  }
+
+  const uintptr_t mx = reinterpret_cast<uintptr_t>(x) & 15;
+  const bool same = (reinterpret_cast<uintptr_t>(dy) & 15) == mx &&
+                    (reinterpret_cast<uintptr_t>(dx) & 15) == mx;
+  const bool aligned16 = same && mx == 0 && aligned_to(gamma, 16);
+  Plan pl;
+  if ((st = make_plan(kBwd, M, (int)N, xd, wd, aligned16, same, rstd != nullptr, &pl)) !=
+      RMSNORM_OK)
+    return st;
+  if ((st = size_grid(&pl, M, dev)) != RMSNORM_OK) return st;
+  if (dgamma && pl.grid > prows) pl.grid = prows;
+
+  BwdParams prm;
+  prm.dy = dy;
+  prm.x = x;
+  prm.rstd = rstd;
+  prm.gamma = gamma;
+  prm.dx = dx;
+  prm.partial = dgamma ? static_cast<float*>(workspace) : nullptr;
+  prm.M = M;
+  prm.N = (int)N;
+  prm.nvec = (int)(N / per_vec(xd));
+  prm.ld_partial = ld;
+  prm.eps = eps;
+  prm.inv_n = 1.0f / (float)N;
+  pl.bwd<<<pl.grid, pl.threads, pl.smem, stream>>>(prm);
+  if ((st = launched()) != RMSNORM_OK || !dgamma) return st;
+
+  // stage 2, as a programmatic dependent launch of stage 1
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((ld / 4 + kRedCols - 1) / kRedCols));
+  cfg.blockDim = dim3(kRedCols * kRedRows);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* part = static_cast<const float*>(workspace);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, get_dgamma_reduce_kernel(), part, pl.grid,
+                                           (int)N, ld, dgamma);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RMSNORM_ERR_CUDA;
+  }
+  return RMSNORM_OK;
+}
+
+}  // namespace
+}  // namespace rmsn
+
+// ======================================================================= C ABI
+
+using namespace rmsn;
+
+extern "C" {
+
+rmsnorm_status_t rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t M,
+                             int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                             rmsnorm_dtype_t w_dtype, cudaStream_t stream) {
+  return fwd_impl(kFwd, x, nullptr, gamma, y, rstd, M, N, eps, (int)x_dtype, (int)w_dtype,
+                  stream);
+}
+
+rmsnorm_status_t rmsnorm_fused_add_fwd(const void* x, void* residual, const void* gamma, void* y,
+                                       float* rstd, int64_t M, int64_t N, float eps,
+                                       rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                                       cudaStream_t stream) {
+  return fwd_impl(kFused, x, residual, gamma, y, rstd, M, N, eps, (int)x_dtype, (int)w_dtype,
+                  stream);
+}
+
+rmsnorm_status_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
+                                            rmsnorm_dtype_t w_dtype, int device,
+                                            size_t* bytes) {
+  if (!bytes) return RMSNORM_ERR_INVALID_ARG;
+  *bytes = 0;
+  rmsnorm_status_t st = check_sizes(M, N, 0.f);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok((int)x_dtype, (int)w_dtype)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if (M == 0) return RMSNORM_OK;
+  if (device < 0 && (st = current_device(&device)) != RMSNORM_OK) return st;
+  int rows = 0;
+  if ((st = bwd_partial_rows(M, (int)N, (int)x_dtype, (int)w_dtype, device, &rows)) !=
+      RMSNORM_OK)
+    return st;
+  *bytes = (size_t)rows * (size_t)round_up((int)N, 4) * 4;
+  return RMSNORM_OK;
+}
+
+rmsnorm_status_t rmsnorm_bwd(const void* dy, const void* x, const float* rstd, const void* gamma,
+                             void* dx, float* dgamma, void* workspace, size_t workspace_bytes,
+                             int64_t M, int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                             rmsnorm_dtype_t w_dtype, cudaStream_t stream) {
+  return bwd_impl(dy, x, rstd, gamma, dx, dgamma, workspace, workspace_bytes, M, N, eps,
+                  (int)x_dtype, (int)w_dtype, stream);
+}
+
+const char* rmsnorm_status_string(rmsnorm_status_t status) {
+  switch (status) {
+    case RMSNORM_OK: return "ok";
+    case RMSNORM_ERR_INVALID_ARG: return "invalid argument";
+    case RMSNORM_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype pair";
+    case RMSNORM_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case RMSNORM_ERR_WORKSPACE: return "workspace missing or too small";
+    case RMSNORM_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
+                                       rmsnorm_dtype_t w_dtype, int aligned16, int device,
+                                       char* buf, size_t len) {
+  if (!buf || len == 0 || op < 0 || op > 2) return RMSNORM_ERR_INVALID_ARG;
+  buf[0] = 0;
+  rmsnorm_status_t st = check_sizes(M, N, 0.f);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok((int)x_dtype, (int)w_dtype)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if (device < 0 && (st = current_device(&device)) != RMSNORM_OK) return st;
+  Plan pl;
+  if ((st = make_plan(op, M, (int)N, (int)x_dtype, (int)w_dtype, aligned16 != 0, aligned16 != 0,
+                      true, &pl)) != RMSNORM_OK)
+    return st;
+  if ((st = size_grid(&pl, M > 0 ? M : 1, device)) != RMSNORM_OK) return st;
+  describe(op, pl, buf, len);
+  return RMSNORM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,507 @@
+// RMSNorm backward kernels for sm_103a.
+//
+// The backward reads the forward's input, gamma, dy and the saved rstd, and
+// writes dx and the weight gradient ("Pre-built kernel library guide", section
+// 1.2 RMSNorm: Input, Gamma, DY, Rstd -> DX, DWeight; eps is folded into
+// rstd).  The guide does not print the formula; differentiating
+// y_j = gamma_j x_j r, r = (mean(x^2) + eps)^(-1/2) gives, per row,
+//     c    = r^2 / N * sum_k gamma_k dy_k x_k
+//     dx_j = r * (gamma_j dy_j - x_j c)
+//     dgamma_j = sum over rows of dy_j x_j r.
+//
+// Where the guide's kernel atomically adds every row into DWeight, this
+// library reduces dgamma in a fixed order so the result is bit-for-bit
+// reproducible: stage 1 runs a persistent grid of P CTAs with a fixed
+// row -> CTA map, each CTA accumulating its rows' dy*x*r per column in fp32
+// and writing one partial row; stage 2 sums the P partial rows per column in
+// a fixed order.  Stage 2 is launched with programmatic dependent launch so
+// its launch overlaps stage 1's tail; it waits on stage 1 before reading.
+#include <type_traits>
+
+#include "rmsnorm_device.cuh"
+#include "rmsnorm_internal.h"
+
+#ifndef RMSN_PAIR
+#error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
+#endif
+
+namespace rmsn {
+namespace {
+
+template <typename TW, int E>
+__device__ __forceinline__ void load_gamma_vec(const void* gamma, int v, float (&g)[E]) {
+  constexpr int GW = E * (int)sizeof(TW) / 16;
+  const char* gp = static_cast<const char*>(gamma) + (size_t)v * GW * 16;
+  if constexpr (std::is_same<TW, float>::value) {
+#pragma unroll
+    for (int w = 0; w < GW; ++w) {
+      float t[4];
+      unpack(ld_cached(gp + w * 16), t);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) g[w * 4 + i] = t[i];
+    }
+  } else {
+    unpack(ld_cached(gp), g);
+  }
+}
+
+__device__ __forceinline__ void signal_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int VPT>
+struct BSlice {
+  uint4 x[VPT];
+  uint4 dy[VPT];
+  float r;        // saved rstd of the row
+  float xs, dys;  // ragged scalar
+  int h, nb, tl;  // ragged layout
+};
+
+template <typename TX, int VPT, bool HAS_RSTD>
+__device__ __forceinline__ void bload_aligned(BSlice<VPT>& s, const BwdParams& p, int64_t row,
+                                              bool valid, int lane, int stride) {
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const char* xr = static_cast<const char*>(p.x) + row * rb;
+  const char* dr = static_cast<const char*>(p.dy) + row * rb;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * stride;
+    if (valid && v < p.nvec) {
+      s.x[k] = ld_stream(xr + (size_t)v * 16);
+      s.dy[k] = ld_stream(dr + (size_t)v * 16);
+    } else {
+      s.x[k] = make_uint4(0, 0, 0, 0);
+      s.dy[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (HAS_RSTD) s.r = valid ? __ldg(p.rstd + row) : 0.f;
+}
+
+template <typename TX, int VPT, bool HAS_RSTD>
+__device__ __forceinline__ void bload_ragged(BSlice<VPT>& s, const BwdParams& p, int64_t row,
+                                             int tid, int T) {
+  constexpr int E = Elem<TX>::kPerVec;
+  const int N = p.N;
+  const TX* xrow = static_cast<const TX*>(p.x) + row * (int64_t)N;
+  const TX* drow = static_cast<const TX*>(p.dy) + row * (int64_t)N;
+  const int mis = (int)(reinterpret_cast<uintptr_t>(xrow) & 15);
+  int h = mis ? (16 - mis) / (int)sizeof(TX) : 0;
+  if (h > N) h = N;
+  const int nb = (N - h) / E;
+  s.h = h;
+  s.nb = nb;
+  s.tl = N - h - nb * E;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < nb) {
+      s.x[k] = ld_stream(xrow + h + v * E);
+      s.dy[k] = ld_stream(drow + h + v * E);
+    } else {
+      s.x[k] = make_uint4(0, 0, 0, 0);
+      s.dy[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  s.xs = 0.f;
+  s.dys = 0.f;
+  int col = -1;
+  if (tid < h) col = tid;
+  else if (tid >= 8 && tid - 8 < s.tl) col = h + nb * E + (tid - 8);
+  if (col >= 0) {
+    s.xs = ld_scalar(xrow + col);
+    s.dys = ld_scalar(drow + col);
+  }
+  if (HAS_RSTD) s.r = __ldg(p.rstd + row);
+}
+
+// ---------------------------------------------------------------------------
+// kSubwarp: G lanes per row, 256 / G rows per CTA iteration; gamma and the
+// dgamma partials in registers; the row groups of a CTA are combined in
+// shared memory (in group order) at the end.
+template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF>
+__global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdParams p) {
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int RPC = kSubwarpThreads / G;
+  extern __shared__ float4 smem4[];
+  float* sacc = reinterpret_cast<float*>(smem4);   // [RPC][nvec * E]
+  const int lane = threadIdx.x % G, grp = threadIdx.x / G;
+  const bool want_dg = p.partial != nullptr;
+
+  float g[VPT][E];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+    if (v < p.nvec) load_gamma_vec<TW, E>(p.gamma, v, g[k]);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) g[k][e] = 0.f;
+  }
+  float acc[VPT][E];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+
+  const int64_t stride = (int64_t)gridDim.x * RPC;
+  int64_t base = (int64_t)blockIdx.x * RPC;
+  BSlice<VPT> cur, nxt;
+  bload_aligned<TX, VPT, HAS_RSTD>(cur, p, base + grp, base + grp < p.M, lane, G);
+  for (; base < p.M; base += stride) {
+    const int64_t row = base + grp;
+    const bool valid = row < p.M;
+    const int64_t nrow = row + stride;
+    if (PF) bload_aligned<TX, VPT, HAS_RSTD>(nxt, p, nrow, nrow < p.M, lane, G);
+
+    float dot = 0.f, ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      float xf[E], df[E];
+      unpack(cur.x[k], xf);
+      unpack(cur.dy[k], df);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        dot = fmaf(g[k][e] * df[e], xf[e], dot);
+        if (!HAS_RSTD) ss = fmaf(xf[e], xf[e], ss);
+      }
+    }
+    dot = group_sum<G>(dot);
+    float r;
+    if constexpr (HAS_RSTD) {
+      r = cur.r;
+    } else {
+      ss = group_sum<G>(ss);
+      r = rsqrtf(fmaf(ss, p.inv_n, p.eps));
+    }
+    const float c = r * r * p.inv_n * dot;
+    char* dxr = static_cast<char*>(p.dx) + row * (size_t)p.N * sizeof(TX);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * G;
+      float xf[E], df[E], o[E];
+      unpack(cur.x[k], xf);
+      unpack(cur.dy[k], df);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
+        acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
+      }
+      if (valid && v < p.nvec) st_stream(dxr + (size_t)v * 16, pack(o));
+    }
+    if (PF) cur = nxt;
+    else bload_aligned<TX, VPT, HAS_RSTD>(cur, p, nrow, nrow < p.M, lane, G);
+  }
+  signal_dependents();
+  if (!want_dg) return;
+  const int ncol = p.nvec * E;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+    if (v < p.nvec) {
+      float4* d = reinterpret_cast<float4*>(sacc + grp * ncol + v * E);
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q)
+        d[q] = make_float4(acc[k][4 * q], acc[k][4 * q + 1], acc[k][4 * q + 2],
+                           acc[k][4 * q + 3]);
+    }
+  }
+  __syncthreads();
+  float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
+  for (int j = threadIdx.x; j < ncol; j += kSubwarpThreads) {
+    float s = 0.f;
+    for (int q = 0; q < RPC; ++q) s += sacc[q * ncol + j];
+    prow[j] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kCta / kRagged: one row per CTA iteration.  dgamma partials live in
+// registers (ACC_SMEM false, aligned rows) or in shared memory (ACC_SMEM, and
+// always for ragged rows, whose columns shift with each row's alignment).  A
+// column is updated by one thread per row and rows are separated by the
+// reduction barrier, so the shared-memory accumulation is race free and adds
+// rows in order.
+template <typename TX, typename TW, int VPT, bool RAGGED, bool HAS_RSTD, bool ACC_SMEM, bool PF>
+__global__ void __launch_bounds__(kCtaMaxThreads) bwd_cta_kernel(const BwdParams p) {
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr bool SMEM_ACC = ACC_SMEM || RAGGED;
+  constexpr int K = HAS_RSTD ? 1 : 2;
+  extern __shared__ float4 smem4[];
+  float* red = reinterpret_cast<float*>(smem4);                // 2 * K * 32
+  float* sg = red + 128;                                       // ragged: gamma fp32 [ld]
+  float* sacc = sg + (RAGGED ? p.ld_partial : 0);              // [ld]
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int N = p.N;
+  const bool want_dg = p.partial != nullptr;
+
+  if constexpr (RAGGED) {
+    const TW* gp = static_cast<const TW*>(p.gamma);
+    for (int j = tid; j < N; j += T) sg[j] = ld_scalar(gp + j);
+  }
+  if constexpr (SMEM_ACC) {
+    for (int j = tid; j < p.ld_partial; j += T) sacc[j] = 0.f;
+  }
+  if constexpr (RAGGED || SMEM_ACC) __syncthreads();
+
+  float acc[SMEM_ACC ? 1 : VPT][E];
+#pragma unroll
+  for (int k = 0; k < (SMEM_ACC ? 1 : VPT); ++k)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+
+  int parity = 0;
+  BSlice<VPT> cur, nxt;
+  int64_t row = blockIdx.x;
+  if (row < p.M) {
+    if constexpr (RAGGED) bload_ragged<TX, VPT, HAS_RSTD>(cur, p, row, tid, T);
+    else bload_aligned<TX, VPT, HAS_RSTD>(cur, p, row, true, tid, T);
+  }
+  for (; row < p.M; row += gridDim.x) {
+    const int64_t nrow = row + gridDim.x;
+    if (PF && nrow < p.M) {
+      if constexpr (RAGGED) bload_ragged<TX, VPT, HAS_RSTD>(nxt, p, nrow, tid, T);
+      else bload_aligned<TX, VPT, HAS_RSTD>(nxt, p, nrow, true, tid, T);
+    }
+    const int h = RAGGED ? cur.h : 0;
+    const int nv = RAGGED ? cur.nb : p.nvec;
+
+    float sums[K];
+#pragma unroll
+    for (int q = 0; q < K; ++q) sums[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      float xf[E], df[E], g[E];
+      unpack(cur.x[k], xf);
+      unpack(cur.dy[k], df);
+      if constexpr (RAGGED) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) g[e] = v < nv ? sg[h + v * E + e] : 0.f;
+      } else {
+        if (v < nv) load_gamma_vec<TW, E>(p.gamma, v, g);
+        else
+#pragma unroll
+          for (int e = 0; e < E; ++e) g[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        sums[0] = fmaf(g[e] * df[e], xf[e], sums[0]);
+        if (!HAS_RSTD) sums[K - 1] = fmaf(xf[e], xf[e], sums[K - 1]);
+      }
+    }
+    int scol = -1;
+    float sg_s = 0.f;
+    if constexpr (RAGGED) {
+      scol = (tid < cur.h) ? tid
+             : (tid >= 8 && tid - 8 < cur.tl) ? cur.h + cur.nb * E + (tid - 8) : -1;
+      if (scol >= 0) sg_s = sg[scol];
+      sums[0] = fmaf(sg_s * cur.dys, cur.xs, sums[0]);
+      if (!HAS_RSTD) sums[K - 1] = fmaf(cur.xs, cur.xs, sums[K - 1]);
+    }
+    cta_sum<K>(sums, red, parity);
+    parity ^= 1;
+    const float r = HAS_RSTD ? cur.r : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
+    const float c = r * r * p.inv_n * sums[0];
+
+    TX* dxrow = static_cast<TX*>(p.dx) + row * (int64_t)N;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < nv) {
+        float xf[E], df[E], g[E], o[E];
+        unpack(cur.x[k], xf);
+        unpack(cur.dy[k], df);
+        if constexpr (RAGGED) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) g[e] = sg[h + v * E + e];
+        } else {
+          load_gamma_vec<TW, E>(p.gamma, v, g);
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = r * fmaf(-xf[e], c, g[e] * df[e]);
+        st_stream(dxrow + h + v * E, pack(o));
+        if constexpr (SMEM_ACC) {
+          float* a = sacc + h + v * E;
+#pragma unroll
+          for (int e = 0; e < E; ++e) a[e] = fmaf(df[e] * xf[e], r, a[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
+        }
+      }
+    }
+    if constexpr (RAGGED) {
+      if (scol >= 0) {
+        st_scalar(dxrow + scol, r * fmaf(-cur.xs, c, sg_s * cur.dys));
+        sacc[scol] = fmaf(cur.dys * cur.xs, r, sacc[scol]);
+      }
+    }
+    if (PF) {
+      cur = nxt;
+    } else if (nrow < p.M) {
+      if constexpr (RAGGED) bload_ragged<TX, VPT, HAS_RSTD>(cur, p, nrow, tid, T);
+      else bload_aligned<TX, VPT, HAS_RSTD>(cur, p, nrow, true, tid, T);
+    }
+  }
+  signal_dependents();
+  if (!want_dg) return;
+  float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
+  if constexpr (SMEM_ACC) {
+    __syncthreads();
+    for (int j = tid; j < N; j += T) prow[j] = sacc[j];
+  } else {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < p.nvec) {
+        float4* d = reinterpret_cast<float4*>(prow + v * E);
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q)
+          d[q] = make_float4(acc[k][4 * q], acc[k][4 * q + 1], acc[k][4 * q + 2],
+                             acc[k][4 * q + 3]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kGeneric: any N, any element-aligned pointers.  Pass 1 reduces, pass 2
+// writes dx; the partial row of this CTA is accumulated in place in global
+// memory, each column always by the same thread.
+template <typename TX, typename TW, bool HAS_RSTD>
+__global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
+  constexpr int K = HAS_RSTD ? 1 : 2;
+  __shared__ float red[2 * 2 * 32];
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int N = p.N;
+  const TW* gp = static_cast<const TW*>(p.gamma);
+  float* prow = p.partial ? p.partial + (size_t)blockIdx.x * p.ld_partial : nullptr;
+  if (prow)
+    for (int j = tid; j < N; j += T) prow[j] = 0.f;
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const TX* xr = static_cast<const TX*>(p.x) + row * (int64_t)N;
+    const TX* dr = static_cast<const TX*>(p.dy) + row * (int64_t)N;
+    TX* dxr = static_cast<TX*>(p.dx) + row * (int64_t)N;
+    float sums[K];
+#pragma unroll
+    for (int q = 0; q < K; ++q) sums[q] = 0.f;
+    for (int j = tid; j < N; j += T) {
+      const float xv = ld_scalar(xr + j);
+      sums[0] = fmaf(ld_scalar(gp + j) * ld_scalar(dr + j), xv, sums[0]);
+      if (!HAS_RSTD) sums[K - 1] = fmaf(xv, xv, sums[K - 1]);
+    }
+    cta_sum<K>(sums, red, parity);
+    parity ^= 1;
+    const float r = HAS_RSTD ? __ldg(p.rstd + row) : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
+    const float c = r * r * p.inv_n * sums[0];
+    for (int j = tid; j < N; j += T) {
+      const float xv = ld_scalar(xr + j), dv = ld_scalar(dr + j);
+      st_scalar(dxr + j, r * fmaf(-xv, c, ld_scalar(gp + j) * dv));
+      if (prow) prow[j] = fmaf(dv * xv, r, prow[j]);
+    }
+  }
+  signal_dependents();
+}
+
+template <typename TX, typename TW, bool HAS_RSTD>
+BwdKernel pick_subwarp(int g, int vpt, bool pf) {
+#define RMSN_SW(G_, V_)                                                  \
+  if (g == G_ && vpt == V_)                                              \
+    return pf ? bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, true>       \
+              : bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, false>;
+  RMSN_SW(4, 1) RMSN_SW(8, 1) RMSN_SW(16, 1) RMSN_SW(32, 1)
+  RMSN_SW(8, 2) RMSN_SW(16, 2) RMSN_SW(32, 2) RMSN_SW(32, 3) RMSN_SW(32, 4)
+#undef RMSN_SW
+  return nullptr;
+}
+
+template <typename TX, typename TW, bool RAGGED, bool HAS_RSTD, bool ACC_SMEM>
+BwdKernel pick_cta(int vpt, bool pf) {
+  switch (vpt) {
+    case 1: return pf ? bwd_cta_kernel<TX, TW, 1, RAGGED, HAS_RSTD, ACC_SMEM, true>
+                      : bwd_cta_kernel<TX, TW, 1, RAGGED, HAS_RSTD, ACC_SMEM, false>;
+    case 2: return pf ? bwd_cta_kernel<TX, TW, 2, RAGGED, HAS_RSTD, ACC_SMEM, true>
+                      : bwd_cta_kernel<TX, TW, 2, RAGGED, HAS_RSTD, ACC_SMEM, false>;
+    case 4: return pf ? bwd_cta_kernel<TX, TW, 4, RAGGED, HAS_RSTD, ACC_SMEM, true>
+                      : bwd_cta_kernel<TX, TW, 4, RAGGED, HAS_RSTD, ACC_SMEM, false>;
+    case 8: return pf ? nullptr : bwd_cta_kernel<TX, TW, 8, RAGGED, HAS_RSTD, ACC_SMEM, false>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW, bool HAS_RSTD>
+BwdKernel pick_family(const BwdKey& k) {
+  switch (k.family) {
+    case kSubwarp: return pick_subwarp<TX, TW, HAS_RSTD>(k.g, k.vpt, k.prefetch);
+    case kCta:
+      return k.acc_smem ? pick_cta<TX, TW, false, HAS_RSTD, true>(k.vpt, k.prefetch)
+                        : pick_cta<TX, TW, false, HAS_RSTD, false>(k.vpt, k.prefetch);
+    case kRagged: return pick_cta<TX, TW, true, HAS_RSTD, true>(k.vpt, k.prefetch);
+    case kGeneric: return bwd_generic_kernel<TX, TW, HAS_RSTD>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW>
+BwdKernel pick_rstd(const BwdKey& k) {
+  return k.has_rstd ? pick_family<TX, TW, true>(k) : pick_family<TX, TW, false>(k);
+}
+
+#if RMSN_PAIR == 0
+// Stage 2: dgamma_j = sum_b partial[b][j] over the P stage-1 CTAs, in a fixed
+// order: thread (tx, ty) adds rows b = ty, ty + kRedRows, ... in sequence,
+// then the kRedRows chunk sums are added in ty order.  Launched as a
+// programmatic dependent of stage 1; griddepcontrol.wait returns once stage 1
+// has completed and its writes are visible.
+__global__ void __launch_bounds__(kRedCols* kRedRows)
+    dgamma_reduce_kernel(const float* partial, int P, int N, int ld, float* dgamma) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float4 sh[kRedRows][kRedCols];
+  const int tx = threadIdx.x % kRedCols, ty = threadIdx.x / kRedCols;
+  const int q = blockIdx.x * kRedCols + tx;       // float4 column group
+  const int nq = ld / 4;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (q < nq) {
+    const float4* src = reinterpret_cast<const float4*>(partial) + q;
+#pragma unroll 4
+    for (int b = ty; b < P; b += kRedRows) {
+      const float4 v = __ldcs(src + (size_t)b * nq);
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+  }
+  sh[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && q < nq) {
+    float4 t = sh[0][tx];
+    for (int r = 1; r < kRedRows; ++r) {
+      const float4 v = sh[r][tx];
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
+    }
+    const int j = q * 4;
+    if (j + 0 < N) dgamma[j + 0] = t.x;
+    if (j + 1 < N) dgamma[j + 1] = t.y;
+    if (j + 2 < N) dgamma[j + 2] = t.z;
+    if (j + 3 < N) dgamma[j + 3] = t.w;
+  }
+}
+#endif
+
+}  // namespace
+
+#if RMSN_PAIR == 0
+ReduceKernel get_dgamma_reduce_kernel() { return dgamma_reduce_kernel; }
+BwdKernel get_bwd_kernel_f32_f32(const BwdKey& k) { return pick_rstd<float, float>(k); }
+#elif RMSN_PAIR == 1
+BwdKernel get_bwd_kernel_bf16_bf16(const BwdKey& k) { return pick_rstd<bf16, bf16>(k); }
+#else
+BwdKernel get_bwd_kernel_bf16_f32(const BwdKey& k) { return pick_rstd<bf16, float>(k); }
+#endif
+
+}  // namespace rmsn

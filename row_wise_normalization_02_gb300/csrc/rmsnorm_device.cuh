@@ -1,0 +1,147 @@
+// Device building blocks shared by the RMSNorm kernels: 16-byte vector
+// loads/stores with explicit cache policy, bf16 <-> fp32 conversion, and the
+// two-level (warp shuffle, then CTA shared memory) sum.
+//
+// Prior art on the pages: 128-bit vector I/O and __shfl_xor_sync reductions
+// ("GPU Kernel Suite (gks)", techniques list); XOR-shuffle reduction inside a
+// wave followed by a shared-memory combine across waves, round-to-nearest-even
+// bf16 packing, non-temporal output stores ("Pre-built kernel library guide",
+// section 1.1 LayerNorm, algorithm and configuration constants, which RMSNorm
+// shares); warp_sum / cta_sum and float22bfloat162_rn ("CUDA Authoring and
+// Support APIs", CUDA helpers).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------- element types
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kPerVec = 4;   // elements per 16-byte vector
+  __device__ static __forceinline__ float to_f32(float v) { return v; }
+};
+template <> struct Elem<bf16> {
+  static constexpr int kPerVec = 8;
+  __device__ static __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+};
+
+// Unpack one 16-byte vector of T into fp32 values.
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void unpack_word_bf16(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xFFFF0000u);
+}
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+  unpack_word_bf16(v.x, f[0], f[1]);
+  unpack_word_bf16(v.y, f[2], f[3]);
+  unpack_word_bf16(v.z, f[4], f[5]);
+  unpack_word_bf16(v.w, f[6], f[7]);
+}
+
+// Pack fp32 values into one 16-byte vector; bf16 rounds to nearest even.
+__device__ __forceinline__ uint4 pack(const float (&f)[4]) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+__device__ __forceinline__ uint32_t pack_word_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+  return make_uint4(pack_word_bf16(f[0], f[1]), pack_word_bf16(f[2], f[3]),
+                    pack_word_bf16(f[4], f[5]), pack_word_bf16(f[6], f[7]));
+}
+
+__device__ __forceinline__ float round_to(float v, float*) { return v; }
+__device__ __forceinline__ float round_to(float v, bf16*) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// ---------------------------------------------------------------- global memory
+
+// Streaming read of data that this kernel never writes: read-only path, no L1
+// allocation (each byte is used once).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+// Read of data that this kernel later overwrites (the fused-add residual):
+// coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_rw(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+// Read of small data every CTA re-reads (gamma): cached in L1.
+__device__ __forceinline__ uint4 ld_cached(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+// Streaming write: evict-first in L2, the output is not re-read by this kernel.
+__device__ __forceinline__ void st_stream(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_scalar(const T* p) {
+  return Elem<T>::to_f32(*p);
+}
+__device__ __forceinline__ void st_scalar(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st_scalar(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------- reductions
+
+// Sum over aligned groups of G consecutive lanes (G a power of two <= 32).
+// Every lane of the warp must execute it; each lane receives its group's sum,
+// combined in the same order for every lane of the group.
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// CTA-wide sum of K values per thread.  red: shared scratch of at least
+// 2 * K * 32 floats; `parity` alternates between consecutive calls so one
+// barrier per call suffices (a warp cannot re-enter the same half before every
+// warp has left the previous call).  Every thread gets the same totals: the
+// warp partials are added in warp order by every thread.
+template <int K>
+__device__ __forceinline__ void cta_sum(float (&v)[K], float* red, int parity) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int k = 0; k < K; ++k) v[k] = group_sum<32>(v[k]);
+  float* buf = red + parity * (K * 32);
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) buf[k * 32 + warp] = v[k];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += buf[k * 32 + w];
+    v[k] = s;
+  }
+}
+
+}  // namespace rmsn

@@ -1,0 +1,388 @@
+// RMSNorm forward and fused residual-add forward kernels for sm_103a.
+//
+// y_ij = x_ij * rstd_i * gamma_j,  rstd_i = 1 / sqrt(mean_j x_ij^2 + eps)
+// ("Pre-built kernel library guide", section 1.2 RMSNorm).  The fused variant
+// first forms h = residual + x, rounds it to the activation dtype, writes it
+// over the residual and normalises that stored h ("TIRx kernels", Kernels list:
+// fused_add_rmsnorm among the flashinfer.norm ports).
+//
+// The operation moves 2 (or 4, fused) bytes of HBM traffic per activation
+// byte and does ~4 flops per element, so every kernel here is an HBM-streaming
+// kernel: each element is read once with 16-byte loads, the row stays in
+// registers across the reduction (the register-resident fast path of the same
+// guide's section 1.1, rather than its shared-memory row cache), and results
+// leave through 16-byte evict-first stores.  Persistent grids walk rows with a
+// fixed stride and issue the next row's loads before reducing the current one.
+#include <type_traits>
+
+#include "rmsnorm_device.cuh"
+#include "rmsnorm_internal.h"
+
+#ifndef RMSN_PAIR
+#error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
+#endif
+
+namespace rmsn {
+namespace {
+
+template <typename TX, typename TW>
+struct Cfg {
+  static constexpr int E = Elem<TX>::kPerVec;            // elements per x vector
+  static constexpr int GW = E * (int)sizeof(TW) / 16;    // gamma vectors per x vector
+  static_assert(GW >= 1, "unsupported dtype pair");
+};
+
+template <typename TW, int E, int GW>
+__device__ __forceinline__ void unpack_gamma(const uint4 (&gw)[GW], float (&gf)[E]) {
+  if constexpr (std::is_same<TW, float>::value) {
+#pragma unroll
+    for (int w = 0; w < GW; ++w) {
+      float t[4];
+      unpack(gw[w], t);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gf[w * 4 + i] = t[i];
+    }
+  } else {
+    unpack(gw[0], gf);
+  }
+}
+
+// Registers of one row slice: VPT vectors of x (and of the residual), plus
+// one scalar element for ragged rows.
+template <int VPT, bool FUSED>
+struct Slice {
+  uint4 x[VPT];
+  uint4 r[FUSED ? VPT : 1];
+  float xs, rs;   // ragged scalar (head or tail element)
+  int h, nb, tl;  // ragged layout: head scalars, body vectors, tail scalars
+};
+
+template <typename TX, int VPT, bool FUSED>
+__device__ __forceinline__ void load_aligned(Slice<VPT, FUSED>& s, const FwdParams& p,
+                                             int64_t row, bool valid, int lane, int stride) {
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const char* xr = static_cast<const char*>(p.x) + row * rb;
+  const char* rr = static_cast<const char*>(p.residual) + row * rb;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * stride;
+    if (valid && v < p.nvec) {
+      s.x[k] = ld_stream(xr + (size_t)v * 16);
+      if (FUSED) s.r[k] = ld_rw(rr + (size_t)v * 16);
+    } else {
+      s.x[k] = make_uint4(0, 0, 0, 0);
+      if (FUSED) s.r[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+template <typename TX, int VPT, bool FUSED>
+__device__ __forceinline__ void load_ragged(Slice<VPT, FUSED>& s, const FwdParams& p,
+                                            int64_t row, int tid, int T) {
+  constexpr int E = Elem<TX>::kPerVec;
+  const int N = p.N;
+  const TX* xrow = static_cast<const TX*>(p.x) + row * (int64_t)N;
+  const TX* rrow = static_cast<const TX*>(p.residual) + row * (int64_t)N;
+  const int mis = (int)(reinterpret_cast<uintptr_t>(xrow) & 15);
+  int h = mis ? (16 - mis) / (int)sizeof(TX) : 0;
+  if (h > N) h = N;
+  const int nb = (N - h) / E;
+  s.h = h;
+  s.nb = nb;
+  s.tl = N - h - nb * E;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < nb) {
+      s.x[k] = ld_stream(xrow + h + v * E);
+      if (FUSED) s.r[k] = ld_rw(rrow + h + v * E);
+    } else {
+      s.x[k] = make_uint4(0, 0, 0, 0);
+      if (FUSED) s.r[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  s.xs = 0.f;
+  s.rs = 0.f;
+  int col = -1;
+  if (tid < h) col = tid;
+  else if (tid >= 8 && tid - 8 < s.tl) col = h + nb * E + (tid - 8);
+  if (col >= 0) {
+    s.xs = ld_scalar(xrow + col);
+    if (FUSED) s.rs = ld_scalar(rrow + col);
+  }
+}
+
+// Column of the ragged scalar held by thread tid, or -1.
+__device__ __forceinline__ int ragged_scalar_col(int tid, int h, int nb, int tl, int E) {
+  if (tid < h) return tid;
+  if (tid >= 8 && tid - 8 < tl) return h + nb * E + (tid - 8);
+  return -1;
+}
+
+// Sum of squares of this thread's part of the row.  Fused add: the vectors
+// become h = round(r + x), which is written back over the residual and kept
+// (packed) in s.x for the output pass.
+template <typename TX, int VPT, bool FUSED>
+__device__ __forceinline__ float slice_sumsq(Slice<VPT, FUSED>& s, char* res_row_vec0, int lane,
+                                             int stride, int nvec_valid, bool valid) {
+  constexpr int E = Elem<TX>::kPerVec;
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    float f[E];
+    unpack(s.x[k], f);
+    if constexpr (FUSED) {
+      float rf[E];
+      unpack(s.r[k], rf);
+#pragma unroll
+      for (int e = 0; e < E; ++e) f[e] += rf[e];
+      s.x[k] = pack(f);   // rounds to TX (nearest even)
+      unpack(s.x[k], f);  // the stored h, exactly
+      const int v = lane + k * stride;
+      if (valid && v < nvec_valid) st_stream(res_row_vec0 + (size_t)v * 16, s.x[k]);
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+  }
+  return ss;
+}
+
+// ---------------------------------------------------------------------------
+// kSubwarp: G lanes per row, 256 / G rows per CTA iteration, persistent grid.
+template <typename TX, typename TW, int G, int VPT, bool FUSED, bool PF>
+__global__ void __launch_bounds__(kSubwarpThreads)
+    fwd_subwarp_kernel(const FwdParams p) {
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW;
+  constexpr int RPC = kSubwarpThreads / G;
+  const int lane = threadIdx.x % G, grp = threadIdx.x / G;
+
+  uint4 gw[VPT][GW];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+#pragma unroll
+    for (int w = 0; w < GW; ++w)
+      gw[k][w] = v < p.nvec ? ld_cached(static_cast<const char*>(p.gamma) +
+                                        ((size_t)v * GW + w) * 16)
+                            : make_uint4(0, 0, 0, 0);
+  }
+
+  const int64_t stride = (int64_t)gridDim.x * RPC;
+  int64_t base = (int64_t)blockIdx.x * RPC;
+  Slice<VPT, FUSED> cur, nxt;
+  load_aligned<TX, VPT, FUSED>(cur, p, base + grp, base + grp < p.M, lane, G);
+  for (; base < p.M; base += stride) {
+    const int64_t row = base + grp;
+    const bool valid = row < p.M;
+    const int64_t nrow = row + stride;
+    if (PF) load_aligned<TX, VPT, FUSED>(nxt, p, nrow, nrow < p.M, lane, G);
+
+    const size_t rb = (size_t)p.N * sizeof(TX);
+    float ss = slice_sumsq<TX, VPT, FUSED>(cur, static_cast<char*>(p.residual) + row * rb, lane,
+                                           G, p.nvec, valid);
+    ss = group_sum<G>(ss);
+    const float rs = rsqrtf(fmaf(ss, p.inv_n, p.eps));
+    if (valid && lane == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+    char* yr = static_cast<char*>(p.y) + row * rb;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * G;
+      if (valid && v < p.nvec) {
+        float g[E], o[E];
+        unpack_gamma<TW, E, GW>(gw[k], g);
+        unpack(cur.x[k], o);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
+        st_stream(yr + (size_t)v * 16, pack(o));
+      }
+    }
+    if (PF) cur = nxt;
+    else load_aligned<TX, VPT, FUSED>(cur, p, nrow, nrow < p.M, lane, G);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kCta / kRagged: one row per CTA iteration, blockDim.x threads, persistent.
+template <typename TX, typename TW, int VPT, bool FUSED, bool RAGGED, bool PF>
+__global__ void __launch_bounds__(kCtaMaxThreads) fwd_cta_kernel(const FwdParams p) {
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW;
+  extern __shared__ float4 smem4[];
+  float* red = reinterpret_cast<float*>(smem4);    // 2 x 32 warp partials
+  float* sg = red + 64;                            // ragged: gamma as fp32
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int N = p.N;
+
+  uint4 gw[RAGGED ? 1 : VPT][GW];
+  if constexpr (RAGGED) {
+    const TW* g = static_cast<const TW*>(p.gamma);
+    for (int j = tid; j < N; j += T) sg[j] = ld_scalar(g + j);
+    __syncthreads();
+  } else {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+#pragma unroll
+      for (int w = 0; w < GW; ++w)
+        gw[k][w] = v < p.nvec ? ld_cached(static_cast<const char*>(p.gamma) +
+                                          ((size_t)v * GW + w) * 16)
+                              : make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  int parity = 0;
+  Slice<VPT, FUSED> cur, nxt;
+  int64_t row = blockIdx.x;
+  if (row < p.M) {
+    if constexpr (RAGGED) load_ragged<TX, VPT, FUSED>(cur, p, row, tid, T);
+    else load_aligned<TX, VPT, FUSED>(cur, p, row, true, tid, T);
+  }
+  for (; row < p.M; row += gridDim.x) {
+    const int64_t nrow = row + gridDim.x;
+    if (PF && nrow < p.M) {
+      if constexpr (RAGGED) load_ragged<TX, VPT, FUSED>(nxt, p, nrow, tid, T);
+      else load_aligned<TX, VPT, FUSED>(nxt, p, nrow, true, tid, T);
+    }
+    TX* yrow = static_cast<TX*>(p.y) + row * (int64_t)N;
+    TX* hrow = static_cast<TX*>(p.residual) + row * (int64_t)N;
+    const int h = RAGGED ? cur.h : 0;
+    const int nv = RAGGED ? cur.nb : p.nvec;
+
+    float ss[1];
+    ss[0] = slice_sumsq<TX, VPT, FUSED>(cur, reinterpret_cast<char*>(hrow + h), tid, T, nv, true);
+    int scol = -1;
+    float sv = 0.f;
+    if constexpr (RAGGED) {
+      scol = ragged_scalar_col(tid, cur.h, cur.nb, cur.tl, E);
+      sv = cur.xs;
+      if (FUSED) {
+        sv = round_to(cur.rs + cur.xs, (TX*)nullptr);
+        if (scol >= 0) st_scalar(hrow + scol, sv);
+      }
+      ss[0] = fmaf(sv, sv, ss[0]);
+    }
+    cta_sum<1>(ss, red, parity);
+    parity ^= 1;
+    const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
+    if (tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < nv) {
+        float g[E], o[E];
+        if constexpr (RAGGED) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) g[e] = sg[h + v * E + e];
+        } else {
+          unpack_gamma<TW, E, GW>(gw[k], g);
+        }
+        unpack(cur.x[k], o);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
+        st_stream(yrow + h + v * E, pack(o));
+      }
+    }
+    if constexpr (RAGGED) {
+      if (scol >= 0) st_scalar(yrow + scol, sv * rs * sg[scol]);
+    }
+    if (PF) {
+      cur = nxt;
+    } else if (nrow < p.M) {
+      if constexpr (RAGGED) load_ragged<TX, VPT, FUSED>(cur, p, nrow, tid, T);
+      else load_aligned<TX, VPT, FUSED>(cur, p, nrow, true, tid, T);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kGeneric: any N and any element-aligned pointers.  Pass 1 reads the row
+// (fused: forms, rounds and stores h) and reduces; pass 2 re-reads it.
+template <typename TX, typename TW, bool FUSED>
+__global__ void __launch_bounds__(256) fwd_generic_kernel(const FwdParams p) {
+  __shared__ float red[64];
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int N = p.N;
+  const TW* g = static_cast<const TW*>(p.gamma);
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const TX* xr = static_cast<const TX*>(p.x) + row * (int64_t)N;
+    TX* hr = static_cast<TX*>(p.residual) + row * (int64_t)N;
+    TX* yr = static_cast<TX*>(p.y) + row * (int64_t)N;
+    float ss[1] = {0.f};
+    for (int j = tid; j < N; j += T) {
+      float v = ld_scalar(xr + j);
+      if (FUSED) {
+        v = round_to(ld_scalar(hr + j) + v, (TX*)nullptr);
+        st_scalar(hr + j, v);
+      }
+      ss[0] = fmaf(v, v, ss[0]);
+    }
+    cta_sum<1>(ss, red, parity);
+    parity ^= 1;
+    const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
+    if (tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+    for (int j = tid; j < N; j += T) {
+      const float v = FUSED ? ld_scalar(hr + j) : ld_scalar(xr + j);
+      st_scalar(yr + j, v * rs * ld_scalar(g + j));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Instantiation table (one dtype pair per translation unit, see RMSN_PAIR).
+
+template <typename TX, typename TW, bool FUSED, bool PF>
+FwdKernel pick_subwarp(int g, int vpt) {
+#define RMSN_SW(G_, V_) \
+  if (g == G_ && vpt == V_) return fwd_subwarp_kernel<TX, TW, G_, V_, FUSED, PF>;
+  RMSN_SW(4, 1) RMSN_SW(8, 1) RMSN_SW(16, 1) RMSN_SW(32, 1)
+  RMSN_SW(8, 2) RMSN_SW(16, 2) RMSN_SW(32, 2) RMSN_SW(32, 3) RMSN_SW(32, 4)
+#undef RMSN_SW
+  return nullptr;
+}
+
+template <typename TX, typename TW, bool FUSED, bool RAGGED>
+FwdKernel pick_cta(int vpt, bool pf) {
+  switch (vpt) {
+    case 1: return pf ? fwd_cta_kernel<TX, TW, 1, FUSED, RAGGED, true>
+                      : fwd_cta_kernel<TX, TW, 1, FUSED, RAGGED, false>;
+    case 2: return pf ? fwd_cta_kernel<TX, TW, 2, FUSED, RAGGED, true>
+                      : fwd_cta_kernel<TX, TW, 2, FUSED, RAGGED, false>;
+    case 4: return pf ? fwd_cta_kernel<TX, TW, 4, FUSED, RAGGED, true>
+                      : fwd_cta_kernel<TX, TW, 4, FUSED, RAGGED, false>;
+    case 8: return pf ? nullptr : fwd_cta_kernel<TX, TW, 8, FUSED, RAGGED, false>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW, bool FUSED>
+FwdKernel pick_family(const FwdKey& k) {
+  switch (k.family) {
+    case kSubwarp:
+      return k.prefetch ? pick_subwarp<TX, TW, FUSED, true>(k.g, k.vpt)
+                        : pick_subwarp<TX, TW, FUSED, false>(k.g, k.vpt);
+    case kCta: return pick_cta<TX, TW, FUSED, false>(k.vpt, k.prefetch);
+    case kRagged: return pick_cta<TX, TW, FUSED, true>(k.vpt, k.prefetch);
+    case kGeneric: return fwd_generic_kernel<TX, TW, FUSED>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW>
+FwdKernel pick_fused(const FwdKey& k) {
+  return k.fused ? pick_family<TX, TW, true>(k) : pick_family<TX, TW, false>(k);
+}
+
+}  // namespace
+
+#if RMSN_PAIR == 0
+FwdKernel get_fwd_kernel_f32_f32(const FwdKey& k) { return pick_fused<float, float>(k); }
+#elif RMSN_PAIR == 1
+FwdKernel get_fwd_kernel_bf16_bf16(const FwdKey& k) { return pick_fused<bf16, bf16>(k); }
+#else
+FwdKernel get_fwd_kernel_bf16_f32(const FwdKey& k) { return pick_fused<bf16, float>(k); }
+#endif
+
+}  // namespace rmsn

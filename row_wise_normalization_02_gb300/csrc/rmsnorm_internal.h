@@ -1,0 +1,92 @@
+// Internal interface between the kernel translation units and the C ABI /
+// dispatch layer.  Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+enum DT : int { kF32 = 0, kBF16 = 1 };
+
+// Kernel families.
+//  kSubwarp : G (<= 32) lanes per row, several rows per 256-thread CTA,
+//             reduction by shuffles only; rows must be 16-byte aligned.
+//  kCta     : one row per CTA (blockDim chosen per N), row held in registers,
+//             reduction by shuffles + shared memory; rows 16-byte aligned.
+//  kRagged  : as kCta, for rows that are not 16-byte aligned (N * size % 16
+//             != 0, or unaligned bases that agree modulo 16): per-row scalar
+//             head and tail around an aligned vector body; gamma staged in
+//             shared memory as fp32.
+//  kGeneric : any N, any element-aligned pointers; scalar two-pass loop.
+enum Family : int { kSubwarp = 0, kCta = 1, kRagged = 2, kGeneric = 3 };
+
+struct FwdParams {
+  const void* x;
+  void* residual;     // fused add only: in r, out h
+  const void* gamma;
+  void* y;
+  float* rstd;        // may be null
+  int64_t M;
+  int N;
+  int nvec;           // 16-byte vectors per row (aligned families)
+  float eps;
+  float inv_n;
+};
+
+struct BwdParams {
+  const void* dy;
+  const void* x;
+  const float* rstd;  // null: recompute from x and eps
+  const void* gamma;
+  void* dx;
+  float* partial;     // [gridDim.x][ld_partial] fp32 dgamma partials, or null
+  int64_t M;
+  int N;
+  int nvec;
+  int ld_partial;     // row stride of partial, a multiple of 4 floats
+  float eps;
+  float inv_n;
+};
+
+using FwdKernel = void (*)(FwdParams);
+using BwdKernel = void (*)(BwdParams);
+using ReduceKernel = void (*)(const float*, int, int, int, float*);
+
+struct FwdKey {
+  int xd, wd;
+  int family;
+  int g;         // lanes per row (kSubwarp)
+  int vpt;       // 16-byte vectors per thread
+  bool fused;
+  bool prefetch; // issue the next row's loads before reducing the current row
+};
+
+struct BwdKey {
+  int xd, wd;
+  int family;
+  int g;
+  int vpt;
+  bool has_rstd;
+  bool acc_smem; // kCta: dgamma partials in shared memory instead of registers
+  bool prefetch;
+};
+
+// Kernel for a key, or nullptr when that instantiation does not exist.  Each
+// dtype pair is instantiated in its own translation unit.
+FwdKernel get_fwd_kernel_f32_f32(const FwdKey& k);
+FwdKernel get_fwd_kernel_bf16_bf16(const FwdKey& k);
+FwdKernel get_fwd_kernel_bf16_f32(const FwdKey& k);
+BwdKernel get_bwd_kernel_f32_f32(const BwdKey& k);
+BwdKernel get_bwd_kernel_bf16_bf16(const BwdKey& k);
+BwdKernel get_bwd_kernel_bf16_f32(const BwdKey& k);
+ReduceKernel get_dgamma_reduce_kernel();
+
+// Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
+constexpr int kSubwarpThreads = 256;
+constexpr int kCtaMaxThreads = 512;
+// Stage-2 reduction tile: kRedCols float4 column groups x kRedRows row chunks.
+constexpr int kRedCols = 16;
+constexpr int kRedRows = 16;
+
+}  // namespace rmsn

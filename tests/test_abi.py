@@ -1,0 +1,115 @@
+"""The C ABI library: it loads, it exports every entry point the header
+declares, and argument errors are reported before any CUDA call (so these run
+without a GPU).  The GPU-side error paths are at the end, marked gpu."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import row_wise_normalization_02_gb300 as rn
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rmsnorm_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from row_wise_normalization_02_gb300 import _build
+    _build.build()
+    return rn.load_library()
+
+
+def test_header_and_binding_agree():
+    assert header_functions() == sorted(rn.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_header_symbol(lib):
+    raw = ctypes.CDLL(rn.library_path())
+    for name in header_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    assert rn.rmsnorm_status_string(0) == "ok"
+    assert "workspace" in rn.rmsnorm_status_string(4)
+    assert rn.rmsnorm_status_string(99) == "unknown status"
+
+
+FAKE = 1 << 40     # an address never dereferenced: these calls fail validation first
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(M=-1), 1), (dict(N=0), 1), (dict(N=(1 << 30) + 1), 1), (dict(eps=-1.0), 1),
+    (dict(eps=float("nan")), 1), (dict(x=None), 1), (dict(gamma=None), 1), (dict(y=None), 1),
+    (dict(x_dtype=rn.F32, w_dtype=rn.BF16), 2), (dict(x_dtype=7), 2),
+    (dict(x=FAKE + 1), 3), (dict(rstd=FAKE + 2), 3),
+    (dict(y=FAKE), 1),   # y overlaps x
+])
+def test_fwd_argument_errors_without_gpu(lib, args, status):
+    a = dict(x=FAKE, gamma=FAKE + (1 << 32), y=FAKE + (2 << 32), rstd=None, M=4, N=64, eps=1e-5,
+             x_dtype=rn.BF16, w_dtype=rn.BF16)
+    a.update(args)
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_fwd(a["x"], a["gamma"], a["y"], a["rstd"], a["M"], a["N"], a["eps"],
+                       a["x_dtype"], a["w_dtype"])
+    assert e.value.status == status
+
+
+def test_fused_and_bwd_argument_errors_without_gpu(lib):
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_fused_add_fwd(FAKE, None, FAKE + (1 << 32), FAKE + (2 << 32), None, 4, 64,
+                                 1e-5, rn.BF16, rn.BF16)
+    assert e.value.status == 1
+    with pytest.raises(rn.RMSNormError) as e:    # residual aliases y
+        rn.rmsnorm_fused_add_fwd(FAKE, FAKE + (3 << 32), FAKE + (1 << 32), FAKE + (3 << 32), None,
+                                 4, 64, 1e-5, rn.BF16, rn.BF16)
+    assert e.value.status == 1
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_bwd(None, FAKE, None, FAKE, FAKE, None, None, 0, 4, 64, 1e-5, rn.BF16,
+                       rn.BF16)
+    assert e.value.status == 1
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_bwd(FAKE, FAKE + (1 << 32), None, FAKE + (2 << 32), FAKE + (3 << 32), None,
+                       None, 0, 4, 64, 1e-5, rn.F32, rn.BF16)
+    assert e.value.status == 2
+    with pytest.raises(rn.RMSNormError) as e:   # dgamma misaligned
+        rn.rmsnorm_bwd(FAKE, FAKE + (1 << 32), None, FAKE + (2 << 32), FAKE + (3 << 32),
+                       FAKE + (4 << 32) + 2, None, 0, 4, 64, 1e-5, rn.BF16, rn.BF16)
+    assert e.value.status == 3
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_bwd_workspace_size(-3, 64, rn.BF16, rn.BF16)
+    assert e.value.status == 1
+
+
+def test_zero_rows_is_a_no_op(lib):
+    # M == 0: nothing to do, no pointer is touched and no CUDA call is made
+    rn.rmsnorm_fwd(None, None, None, None, 0, 64, 1e-5, rn.BF16, rn.BF16)
+    rn.rmsnorm_fused_add_fwd(None, None, None, None, None, 0, 64, 1e-5, rn.BF16, rn.BF16)
+    rn.rmsnorm_bwd(None, None, None, None, None, None, None, 0, 0, 64, 1e-5, rn.BF16, rn.BF16)
+    assert rn.rmsnorm_bwd_workspace_size(0, 64, rn.BF16, rn.BF16) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import row_wise_normalization_02_gb300 as mod
+    monkeypatch.setattr(mod, "_LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(ImportError):
+        mod.rmsnorm_fwd(1, 1, 1, None, 1, 8, 1e-5, "bf16", "bf16")
+
+
+@pytest.mark.gpu
+def test_workspace_size_matches_plan_on_gpu(lib):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    for M, N in [(16384, 8192), (262144, 128), (4096, 2049), (1, 1), (3, 40000)]:
+        b = rn.rmsnorm_bwd_workspace_size(M, N, "bf16", "f32")
+        assert b > 0 and b % 16 == 0
+        assert b <= min(M, 152 * 32) * ((N + 3) // 4 * 4) * 4 * 2

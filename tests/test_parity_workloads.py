@@ -1,0 +1,36 @@
+"""The measured workloads at full size, through the same default dispatch the
+bench times, compared with the oracle on every output element."""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from tests import parity_util as pu
+from tests.test_parity_bwd import check_bwd
+from tests.test_parity_fwd import check_fused, check_fwd
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+@pytest.mark.parametrize("name", list(si.WORKLOADS))
+def test_workload_matches_oracle(name):
+    wl = si.WORKLOADS[name]
+    inp = si.make_inputs(wl)
+    eps = float(np.float32(wl.eps))
+    x, g = inp["x"], inp["gamma"]
+    if wl.op == "fwd":
+        out = pu.run_fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd)
+        check_fwd(x, g, eps, wl.x_dtype, wl.w_dtype, out, want_rstd=wl.store_rstd)
+    elif wl.op == "fused_add":
+        r = inp["residual"]
+        out = pu.run_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd)
+        check_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, out, want_rstd=wl.store_rstd)
+    else:
+        # the saved rstd comes from the oracle forward
+        rstd = oracle.fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want64=False)["rstd"]
+        out = pu.run_bwd(inp["dy"], x, rstd, g, eps, wl.x_dtype, wl.w_dtype)
+        info = check_bwd(x, inp["dy"], g, rstd, eps, wl.x_dtype, wl.w_dtype, out)
+        print(name, info)
