@@ -90,6 +90,24 @@ def ncu_traffic(op: str):
     return int(v) if v is not None else None
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (all ranks get it)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(step_bytes: int, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank moves step_bytes per step (replicas)."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -250,15 +268,10 @@ def run_ours(args, rank, world):
         dist.barrier()
     if sampler:
         sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     step_bytes = sum(op["bytes"] for op in ops)
     ms_per_step = total_ms / K
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(step_bytes, ms_per_step, world)
     peak, peak_src = measured_peak()
     per_op = {}
     for j, op in enumerate(ops):
@@ -307,12 +320,8 @@ def run_ours(args, rank, world):
                     t.copy_(op["d"][k], non_blocking=True)
         e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, world, dev)
+    e2e = {"value": round(job_gbs(step_bytes, e2e_ms, world), 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
            "ms_per_step": round(e2e_ms, 3), "pinned": True}
 

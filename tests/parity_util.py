@@ -9,8 +9,11 @@ oracle):
     cannot keep 2 ulp of a result much smaller than its terms, so an element
     may instead be within 2 ulp(exact) + 64 u32 r (|gamma dy| + |x| r^2/N S) of
     the exact value, S = sum_k |gamma_k dy_k x_k| (u32 = 2^-24; 64 bounds the
-    depth of the fp32 sums and products).  Such elements are counted and must
-    stay rare.
+    depth of the fp32 sums and products).  Such elements are counted and, for
+    rows of 32 or more elements, must stay rare (at most 1e-4 of the tensor).
+    Short rows cancel by construction: for N = 1, dx = r gamma dy eps /
+    (x^2 + eps) is a 1e-5 sliver of its terms, and every element may need the
+    floor.
   * fp32 outputs (y, rstd): |gpu - ref| <= 1e-5 (1 + |ref|).
   * dgamma (fp32): |gpu - ref| <= 1e-4 max(|ref|, sqrt(sum_rows (dy x r)^2)).
   * h of the fused add: bit exact (a correctly rounded sum on both sides).
@@ -191,7 +194,7 @@ def check_dx_bf16(gpu_bits, ref_bits, dx64, x64, dy64, g64, r, dot_abs, max_floo
         bad = strict_bad & ~ok
         assert not bad.any(), (f"dx: {int(bad.sum())} elements beyond 2 ulp and the cancellation "
                                f"floor, at {np.argwhere(bad)[:5].tolist()}")
-        assert n_strict <= max(1, max_floor_frac * d.size), (
+        assert N < 32 or n_strict <= max(1, max_floor_frac * d.size), (
             f"dx: {n_strict} of {d.size} elements needed the cancellation floor")
     return n_strict, int(d.max())
 

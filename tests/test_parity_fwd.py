@@ -170,7 +170,10 @@ def test_zero_row_with_zero_eps_gives_nan():
     g = si.fill(256, seed=1, tensor_id=3, dtype="bf16")
     out = pu.run_fwd(x, g, 0.0, "bf16", "bf16")
     y = oracle.bf16_array_to_f64(out["y"])
-    assert np.isnan(y[0]).all() and np.isnan(out["rstd"][0])
+    ref = oracle.fwd(x, g, 0.0, "bf16", "bf16")
+    # rstd = 1/sqrt(0) = +inf and y = 0 * inf = NaN, on both sides
+    assert np.isinf(ref["rstd64"][0]) and np.isnan(ref["y64"][0]).all()
+    assert np.isposinf(out["rstd"][0]) and np.isnan(y[0]).all()
     assert np.isfinite(y[1]).all()
 
 
