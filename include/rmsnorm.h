@@ -105,6 +105,41 @@ rmsnorm_status_t rmsnorm_bwd(const void* dy, const void* x, const float* rstd,
                              rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
                              cudaStream_t stream);
 
+/*
+ * Backward for callers that cannot allocate device memory.  No counterpart in
+ * the source pages: this entry point exists for integration only.
+ *
+ * Some callers have no way to provide the workspace rmsnorm_bwd needs: a
+ * serving runtime that has handed all device memory to its own pool and
+ * forbids other allocations, a plugin interface that gives an operator its
+ * inputs and outputs but no allocator, or a latency-critical path where a
+ * cudaMalloc / cudaFree (which can synchronise the device) is not acceptable.
+ * This call computes exactly what rmsnorm_bwd computes, with the same
+ * arguments minus the workspace; the dgamma partial rows go to a scratch
+ * array of RMSNORM_BWD_NOALLOC_SCRATCH_BYTES that is part of the library's
+ * device image.  Neither the library nor the caller allocates anything.
+ *
+ *  - Limit: shapes whose partial rows need more than the scratch (the size
+ *    rmsnorm_bwd_workspace_size reports exceeds RMSNORM_BWD_NOALLOC_SCRATCH_BYTES)
+ *    are rejected with RMSNORM_ERR_WORKSPACE before any launch.
+ *  - Memory: every GPU that loads the library keeps the scratch until the
+ *    process exits.
+ *  - Set-up: the first call on each device looks up the scratch's device
+ *    address (cudaGetSymbolAddress, with that device current); make that
+ *    first call before any stream capture.
+ *  - Sharing: all calls on a device share the one scratch, which keeps the
+ *    last call's contents (each call rewrites every part it reads, so nothing
+ *    needs clearing).  Calls that overlap on the GPU -- for example on two
+ *    streams without ordering between them -- race on it and may return a
+ *    wrong dgamma; order them on one stream or with events.
+ */
+#define RMSNORM_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+rmsnorm_status_t rmsnorm_bwd_noalloc(const void* dy, const void* x, const float* rstd,
+                                     const void* gamma, void* dx, float* dgamma, int64_t M,
+                                     int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                                     rmsnorm_dtype_t w_dtype, cudaStream_t stream);
+
 /* Static text of a status code ("unknown status" for other values). */
 const char* rmsnorm_status_string(rmsnorm_status_t status);
 

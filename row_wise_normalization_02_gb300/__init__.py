@@ -18,7 +18,7 @@ import threading
 __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "RMSNormError", "library_path",
            "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
-           "EXPORTED_SYMBOLS"]
+           "rmsnorm_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS"]
 
 F32 = 0
 BF16 = 1
@@ -26,7 +26,11 @@ OP_FWD, OP_FUSED_ADD, OP_BWD = 0, 1, 2
 _DT_NAMES = {"f32": F32, "bf16": BF16}
 
 EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspace_size",
-                    "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan")
+                    "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan",
+                    "rmsnorm_bwd_noalloc")
+
+# Size of the library-owned scratch of rmsnorm_bwd_noalloc (16 MiB).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "librmsnorm_gb300.so")
@@ -67,6 +71,8 @@ def load_library():
             lib.rmsnorm_status_string.restype = ctypes.c_char_p
             lib.rmsnorm_describe_plan.argtypes = [I, I64, I64, I, I, I, I, ctypes.c_char_p, SZ]
             lib.rmsnorm_describe_plan.restype = I
+            lib.rmsnorm_bwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, F, I, I, P]
+            lib.rmsnorm_bwd_noalloc.restype = I
             _lib = lib
     return _lib
 
@@ -125,6 +131,17 @@ def rmsnorm_bwd(dy, x, rstd, gamma, dx, dgamma, workspace, workspace_bytes, M, N
                                       _ptr(dgamma), _ptr(workspace), workspace_bytes, M, N, eps,
                                       _dt(x_dtype), _dt(w_dtype), _stream(stream)),
            "rmsnorm_bwd")
+
+
+def rmsnorm_bwd_noalloc(dy, x, rstd, gamma, dx, dgamma, M, N, eps, x_dtype, w_dtype,
+                        stream=None):
+    """rmsnorm_bwd without a workspace argument: for callers that cannot
+    allocate, the dgamma partials use a scratch array owned by the library
+    (see include/rmsnorm.h for its limit and sharing rules)."""
+    _check(load_library().rmsnorm_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(rstd), _ptr(gamma),
+                                              _ptr(dx), _ptr(dgamma), M, N, eps, _dt(x_dtype),
+                                              _dt(w_dtype), _stream(stream)),
+           "rmsnorm_bwd_noalloc")
 
 
 def rmsnorm_status_string(status: int) -> str:

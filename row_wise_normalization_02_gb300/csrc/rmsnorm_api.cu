@@ -500,6 +500,35 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   return RMSNORM_OK;
 }
 
+// ---------------------------------------------------------------- backward
+// without allocation
+
+// Scratch for the dgamma partial rows of rmsnorm_bwd_noalloc.  It lives in
+// the library's device image, so every GPU that loads the library holds it
+// until the process exits; calls share it and it keeps the last call's
+// partial rows (each call overwrites every partial it later reads).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RMSNORM_BWD_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_addr[64];
+
+// Device address of the scratch on `device` (the current device), looked up
+// once per device with cudaGetSymbolAddress: in host code the array's name is
+// only a host-side stand-in and must never be handed to a kernel.
+rmsnorm_status_t noalloc_scratch(int device, void** out) {
+  if (device < 0 || device >= 64) return RMSNORM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_addr[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return RMSNORM_ERR_CUDA;
+    }
+    g_noalloc_addr[device] = p;
+  }
+  *out = g_noalloc_addr[device];
+  return RMSNORM_OK;
+}
+
 }  // namespace
 }  // namespace rmsn
 
@@ -547,6 +576,24 @@ rmsnorm_status_t rmsnorm_bwd(const void* dy, const void* x, const float* rstd, c
                              int64_t M, int64_t N, float eps, rmsnorm_dtype_t x_dtype,
                              rmsnorm_dtype_t w_dtype, cudaStream_t stream) {
   return bwd_impl(dy, x, rstd, gamma, dx, dgamma, workspace, workspace_bytes, M, N, eps,
+                  (int)x_dtype, (int)w_dtype, stream);
+}
+
+rmsnorm_status_t rmsnorm_bwd_noalloc(const void* dy, const void* x, const float* rstd,
+                                     const void* gamma, void* dx, float* dgamma, int64_t M,
+                                     int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                                     rmsnorm_dtype_t w_dtype, cudaStream_t stream) {
+  void* scratch = nullptr;
+  if (dgamma != nullptr && M > 0 && check_sizes(M, N, eps) == RMSNORM_OK) {
+    int dev;
+    rmsnorm_status_t st = current_device(&dev);
+    if (st != RMSNORM_OK) return st;
+    if ((st = noalloc_scratch(dev, &scratch)) != RMSNORM_OK) return st;
+  }
+  // the workspace entry point with the static scratch as its workspace: a
+  // shape whose partial rows exceed the scratch gets RMSNORM_ERR_WORKSPACE
+  return bwd_impl(dy, x, rstd, gamma, dx, dgamma, scratch,
+                  scratch ? (size_t)RMSNORM_BWD_NOALLOC_SCRATCH_BYTES : 0, M, N, eps,
                   (int)x_dtype, (int)w_dtype, stream);
 }
 
