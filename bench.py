@@ -13,8 +13,9 @@ slowest rank's time counts.
 
 --impl reference times the double-precision CPU oracle on the same step
 (bounded row samples of each workload), on this host's cores.
---sweep prints one line per shape of the fwd/bwd shape sweep instead (each
-launch timed alone with an L2 flush before it).
+--sweep prints one line per workload of the shape sweep (and the three step
+workloads) instead: back-to-back launches rotating over enough operand copies
+that no launch finds its operands in L2.
 """
 from __future__ import annotations
 
@@ -430,6 +431,67 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ sweep
 
+def _op_code(op):
+    return {"fwd": 0, "fused_add": 1, "bwd": 2}[op]
+
+
+def device_sets(wl, inp, dev, l2_bytes, rn):
+    """Device copies of one workload's operands, repeated until the rotation
+    covers at least 3 x L2 (so every launch reads operands that are not in L2)
+    -- one set when a single call already streams that much."""
+    import torch
+    per_set = alg_bytes(wl)
+    nsets = 1 if per_set >= 3 * l2_bytes else min(64, -(-3 * l2_bytes // per_set))
+    act = torch.int16 if wl.x_dtype == "bf16" else torch.float32
+    host = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v)
+            for k, v in inp.items()}
+    M, N = wl.M, wl.N
+    sets = []
+    for _ in range(nsets):
+        d = {k: v.to(dev) for k, v in host.items()}
+        d["y"] = torch.empty((M, N), dtype=act, device=dev)
+        d["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
+        if wl.op == "bwd":
+            d["dgamma"] = torch.empty(N, dtype=torch.float32, device=dev)
+        sets.append(d)
+    return sets
+
+
+def make_launch(wl, d, stream, rn):
+    """A closure that enqueues one call of the workload's op on `stream`."""
+    M, N, eps = wl.M, wl.N, float(np.float32(wl.eps))
+    if wl.op == "fwd":
+        return lambda: rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"],
+                                      d["rstd"] if wl.store_rstd else None, M, N, eps,
+                                      wl.x_dtype, wl.w_dtype, stream)
+    if wl.op == "fused_add":
+        return lambda: rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], d["y"],
+                                                d["rstd"] if wl.store_rstd else None, M, N,
+                                                eps, wl.x_dtype, wl.w_dtype, stream)
+    ws = rn.rmsnorm_bwd_workspace_size(M, N, wl.x_dtype, wl.w_dtype)
+    import torch
+    d["ws"] = torch.empty(max(16, ws), dtype=torch.uint8, device=d["x"].device)
+    return lambda: rn.rmsnorm_bwd(d["dy"], d["x"], d["rstd"], d["gamma"], d["y"], d["dgamma"],
+                                  d["ws"], ws, M, N, eps, wl.x_dtype, wl.w_dtype, stream)
+
+
+def time_rotation(launches, steps, warmup, stream):
+    """Per-launch device times (ms) of `steps` back-to-back launches cycling
+    through the operand sets, after `warmup` untimed ones."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            launches[i % len(launches)]()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            launches[(warmup + i) % len(launches)]()
+            ev[i][1].record(stream)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def run_sweep(args):
     import torch
 
@@ -442,58 +504,29 @@ def run_sweep(args):
     stream = torch.cuda.Stream(device=dev)
     peak, _ = measured_peak()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(4 * l2, dtype=torch.uint8, device=dev)
     names = args.workloads.split(",") if args.workloads else [
         n for n, w in si.WORKLOADS.items() if "sweep" in w.tags or "headline" in w.tags]
     for name in names:
         wl = si.WORKLOADS[name]
         inp = si.make_inputs(wl)
-        d = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).to(dev)
-             for k, v in inp.items()}
-        act = torch.int16 if wl.x_dtype == "bf16" else torch.float32
-        M, N, eps = wl.M, wl.N, float(np.float32(wl.eps))
-        y = torch.empty((M, N), dtype=act, device=dev)
-        rstd = torch.empty(M, dtype=torch.float32, device=dev)
-        rn.rmsnorm_fwd(d["x"], d["gamma"], y, rstd, M, N, eps, wl.x_dtype, wl.w_dtype, stream)
-        if wl.op == "fwd":
-            def launch():
-                rn.rmsnorm_fwd(d["x"], d["gamma"], y, rstd if wl.store_rstd else None, M, N, eps,
-                               wl.x_dtype, wl.w_dtype, stream)
-        elif wl.op == "fused_add":
-            def launch():
-                rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], y, None, M, N, eps,
-                                         wl.x_dtype, wl.w_dtype, stream)
-        else:
-            dg = torch.empty(N, dtype=torch.float32, device=dev)
-            ws = rn.rmsnorm_bwd_workspace_size(M, N, wl.x_dtype, wl.w_dtype)
-            wsb = torch.empty(max(16, ws), dtype=torch.uint8, device=dev)
-
-            def launch():
-                rn.rmsnorm_bwd(d["dy"], d["x"], rstd, d["gamma"], y, dg, wsb, ws, M, N, eps,
-                               wl.x_dtype, wl.w_dtype, stream)
-        times = []
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup + args.steps):
-                flush.add_(1)  # write 4 x L2 between launches: every launch starts cold
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                launch()
-                b.record(stream)
-                if i >= args.warmup:
-                    times.append((a, b))
-        stream.synchronize()
-        us = [a.elapsed_time(b) * 1e3 for a, b in times]
+        sets = device_sets(wl, inp, dev, l2, rn)
+        for d in sets:   # rstd of x for the backward (the forward kernel, untimed)
+            rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"], d["rstd"], wl.M, wl.N,
+                           float(np.float32(wl.eps)), wl.x_dtype, wl.w_dtype, stream)
+        launches = [make_launch(wl, d, stream, rn) for d in sets]
+        us = [t * 1e3 for t in time_rotation(launches, args.steps, args.warmup, stream)]
         med = statistics.median(us)
         byts = alg_bytes(wl)
-        op = {"fwd": 0, "fused_add": 1, "bwd": 2}[wl.op]
-        print(json.dumps({"workload": name, "op": wl.op, "M": M, "N": N,
-                          "variant": rn.rmsnorm_describe_plan(op, M, N, wl.x_dtype, wl.w_dtype),
+        print(json.dumps({"workload": name, "op": wl.op, "M": wl.M, "N": wl.N,
+                          "variant": rn.rmsnorm_describe_plan(_op_code(wl.op), wl.M, wl.N,
+                                                              wl.x_dtype, wl.w_dtype),
                           "median_us": round(med, 2), "min_us": round(min(us), 2),
                           "max_us": round(max(us), 2), "gbs": round(byts / med / 1e3, 1),
                           "frac_of_measured_peak": round(byts / med / 1e3 / peak, 4),
-                          "rows_per_s": round(M / med * 1e6, 1), "alg_bytes": byts,
-                          "l2": "flushed (4 x L2 written) before every launch"}), flush=True)
-        del d, y, rstd
+                          "rows_per_s": round(wl.M / med * 1e6, 1), "alg_bytes": byts,
+                          "l2": f"rotation over {len(sets)} operand set(s) "
+                                f">= 3 x L2, back-to-back launches"}), flush=True)
+        del sets, launches
         torch.cuda.empty_cache()
 
 

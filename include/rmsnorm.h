@@ -51,7 +51,8 @@ typedef enum rmsnorm_status {
   RMSNORM_ERR_UNSUPPORTED_DTYPE = 2, /* (x_dtype, w_dtype) pair not supported */
   RMSNORM_ERR_MISALIGNED = 3,        /* pointer not aligned to its element size */
   RMSNORM_ERR_WORKSPACE = 4,         /* backward workspace NULL or too small */
-  RMSNORM_ERR_CUDA = 5               /* a CUDA runtime call failed */
+  RMSNORM_ERR_CUDA = 5,              /* a CUDA runtime call failed */
+  RMSNORM_ERR_TIMEOUT = 6            /* rmsnorm_check_device: a bounded wait gave up */
 } rmsnorm_status_t;
 
 /*
@@ -139,6 +140,27 @@ rmsnorm_status_t rmsnorm_bwd_noalloc(const void* dy, const void* x, const float*
                                      const void* gamma, void* dx, float* dgamma, int64_t M,
                                      int64_t N, float eps, rmsnorm_dtype_t x_dtype,
                                      rmsnorm_dtype_t w_dtype, cudaStream_t stream);
+
+/*
+ * Device-side status of the current device, for the kernels that stream rows
+ * through bulk copies (cp.async.bulk) and wait for them on mbarriers.  Every
+ * such wait is bounded (about 2 s of SM clock); a kernel whose wait runs out
+ * writes nothing more for that row, waits (bounded) for the copies it still
+ * has in flight, sets a flag in a device status word and returns, so the
+ * context stays usable.  This call waits for `stream` to finish, reads and
+ * clears that flag, and returns RMSNORM_ERR_TIMEOUT if it was set, else
+ * RMSNORM_OK.  Unlike the other entry points it synchronises (the stream).
+ * No page this library follows has this call; it is the error channel of
+ * the bounded waits.
+ */
+rmsnorm_status_t rmsnorm_check_device(cudaStream_t stream);
+
+/*
+ * Text naming the CUDA call that failed and its error, for the last
+ * RMSNORM_ERR_CUDA returned to the calling thread ("" if none).  The string
+ * belongs to the library and stays valid until that thread's next call.
+ */
+const char* rmsnorm_last_error(void);
 
 /* Static text of a status code ("unknown status" for other values). */
 const char* rmsnorm_status_string(rmsnorm_status_t status);

@@ -18,7 +18,8 @@ import threading
 __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "RMSNormError", "library_path",
            "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
-           "rmsnorm_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS"]
+           "rmsnorm_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "rmsnorm_check_device",
+           "rmsnorm_last_error", "EXPORTED_SYMBOLS"]
 
 F32 = 0
 BF16 = 1
@@ -27,7 +28,7 @@ _DT_NAMES = {"f32": F32, "bf16": BF16}
 
 EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspace_size",
                     "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan",
-                    "rmsnorm_bwd_noalloc")
+                    "rmsnorm_bwd_noalloc", "rmsnorm_check_device", "rmsnorm_last_error")
 
 # Size of the library-owned scratch of rmsnorm_bwd_noalloc (16 MiB).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -41,7 +42,8 @@ _lib = None
 class RMSNormError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {rmsnorm_status_string(status)} (status {status})")
+        detail = f" [{rmsnorm_last_error()}]" if status == 5 else ""
+        super().__init__(f"{where}: {rmsnorm_status_string(status)} (status {status}){detail}")
 
 
 def library_path() -> str:
@@ -73,6 +75,10 @@ def load_library():
             lib.rmsnorm_describe_plan.restype = I
             lib.rmsnorm_bwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, F, I, I, P]
             lib.rmsnorm_bwd_noalloc.restype = I
+            lib.rmsnorm_check_device.argtypes = [P]
+            lib.rmsnorm_check_device.restype = I
+            lib.rmsnorm_last_error.argtypes = []
+            lib.rmsnorm_last_error.restype = ctypes.c_char_p
             _lib = lib
     return _lib
 
@@ -142,6 +148,20 @@ def rmsnorm_bwd_noalloc(dy, x, rstd, gamma, dx, dgamma, M, N, eps, x_dtype, w_dt
                                               _ptr(dx), _ptr(dgamma), M, N, eps, _dt(x_dtype),
                                               _dt(w_dtype), _stream(stream)),
            "rmsnorm_bwd_noalloc")
+
+
+def rmsnorm_check_device(stream=None):
+    """Wait for `stream`, then raise RMSNormError(RMSNORM_ERR_TIMEOUT) if a
+    kernel on the current device gave up a bounded wait (clears the flag)."""
+    _check(load_library().rmsnorm_check_device(_stream(stream)), "rmsnorm_check_device")
+
+
+def rmsnorm_last_error() -> str:
+    """The failing CUDA call behind this thread's last RMSNORM_ERR_CUDA."""
+    try:
+        return load_library().rmsnorm_last_error().decode()
+    except ImportError:
+        return ""
 
 
 def rmsnorm_status_string(status: int) -> str:

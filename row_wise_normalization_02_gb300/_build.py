@@ -1,7 +1,7 @@
 """Build librmsnorm_gb300.so in-tree with nvcc for sm_103a.
 
-Seven translation units (forward and backward once per dtype pair, plus the
-C ABI) compile in parallel, then link into one shared library with the CUDA
+Ten translation units (forward, backward and the staged kernels once per
+dtype pair, plus the C ABI) compile in parallel, then link into one shared library with the CUDA
 runtime linked statically.  Rebuilds only when a source is newer than the
 library.
 """
@@ -29,6 +29,9 @@ UNITS = [("rmsnorm_fwd.cu", ["-DRMSN_PAIR=0"], "fwd_p0.o"),
          ("rmsnorm_bwd.cu", ["-DRMSN_PAIR=0"], "bwd_p0.o"),
          ("rmsnorm_bwd.cu", ["-DRMSN_PAIR=1"], "bwd_p1.o"),
          ("rmsnorm_bwd.cu", ["-DRMSN_PAIR=2"], "bwd_p2.o"),
+         ("rmsnorm_staged.cu", ["-DRMSN_PAIR=0"], "staged_p0.o"),
+         ("rmsnorm_staged.cu", ["-DRMSN_PAIR=1"], "staged_p1.o"),
+         ("rmsnorm_staged.cu", ["-DRMSN_PAIR=2"], "staged_p2.o"),
          ("rmsnorm_api.cu", [], "api.o")]
 
 

@@ -30,6 +30,18 @@ namespace {
 
 constexpr int64_t kMaxN = int64_t(1) << 30;
 constexpr int kRaggedMaxN = 24576;
+// Shared memory of a staged CTA: aim for two CTAs per SM, allow one.
+constexpr int64_t kStagedSmemBudget = 110 * 1024;
+constexpr int64_t kStagedSmemMax = 226 * 1024;
+constexpr long long kDefaultWaitLimit = 1LL << 32;   // clock cycles (about 2 s)
+
+// Clock cycles a staged kernel waits for a row before giving up: the
+// RMSNORM_WAIT_LIMIT_CYCLES environment variable (a test knob), else ~2 s.
+long long wait_limit() {
+  const char* s = getenv("RMSNORM_WAIT_LIMIT_CYCLES");
+  if (s && *s) return atoll(s);
+  return kDefaultWaitLimit;
+}
 
 int esize(int dt) { return dt == kF32 ? 4 : 2; }
 int per_vec(int dt) { return 16 / esize(dt); }
@@ -39,16 +51,40 @@ bool dtype_pair_ok(int xd, int wd) {
 }
 
 FwdKernel fwd_kernel(const FwdKey& k) {
-  if (k.xd == kF32 && k.wd == kF32) return get_fwd_kernel_f32_f32(k);
-  if (k.xd == kBF16 && k.wd == kBF16) return get_fwd_kernel_bf16_bf16(k);
-  if (k.xd == kBF16 && k.wd == kF32) return get_fwd_kernel_bf16_f32(k);
+  const bool st = k.family == kStaged;
+  if (k.xd == kF32 && k.wd == kF32) return st ? get_fwd_staged_f32_f32(k) : get_fwd_kernel_f32_f32(k);
+  if (k.xd == kBF16 && k.wd == kBF16)
+    return st ? get_fwd_staged_bf16_bf16(k) : get_fwd_kernel_bf16_bf16(k);
+  if (k.xd == kBF16 && k.wd == kF32)
+    return st ? get_fwd_staged_bf16_f32(k) : get_fwd_kernel_bf16_f32(k);
   return nullptr;
 }
 BwdKernel bwd_kernel(const BwdKey& k) {
-  if (k.xd == kF32 && k.wd == kF32) return get_bwd_kernel_f32_f32(k);
-  if (k.xd == kBF16 && k.wd == kBF16) return get_bwd_kernel_bf16_bf16(k);
-  if (k.xd == kBF16 && k.wd == kF32) return get_bwd_kernel_bf16_f32(k);
+  const bool st = k.family == kStaged;
+  if (k.xd == kF32 && k.wd == kF32) return st ? get_bwd_staged_f32_f32(k) : get_bwd_kernel_f32_f32(k);
+  if (k.xd == kBF16 && k.wd == kBF16)
+    return st ? get_bwd_staged_bf16_bf16(k) : get_bwd_kernel_bf16_bf16(k);
+  if (k.xd == kBF16 && k.wd == kF32)
+    return st ? get_bwd_staged_bf16_f32(k) : get_bwd_kernel_bf16_f32(k);
   return nullptr;
+}
+
+// ---------------------------------------------------------------- status word
+
+// Bits raised by kernels (kStatusWaitTimeout: a bounded wait gave up).  Read
+// and cleared by rmsnorm_check_device.  Its device address is looked up once
+// per device: in host code the name is only a host-side stand-in.
+static __device__ unsigned int g_device_status;
+
+// ---------------------------------------------------------------- errors
+
+// Text of the last CUDA failure seen by this thread's calls into the library.
+thread_local char g_last_error[256] = "";
+
+rmsnorm_status_t cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorString(e),
+           cudaGetErrorName(e));
+  return RMSNORM_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- device info
@@ -56,6 +92,7 @@ BwdKernel bwd_kernel(const BwdKey& k) {
 struct DevInfo {
   int sms = 0;
   int max_smem_optin = 0;
+  unsigned* status = nullptr;
 };
 
 std::mutex g_mu;
@@ -70,15 +107,43 @@ cudaError_t device_info(int device, DevInfo* out) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
+    void* st = nullptr;
+    e = cudaGetSymbolAddress(&st, g_device_status);
+    if (e != cudaSuccess) return e;
     g_dev[device].sms = sms;
     g_dev[device].max_smem_optin = smem;
+    g_dev[device].status = static_cast<unsigned*>(st);
   }
   *out = g_dev[device];
   return cudaSuccess;
 }
 
-// Resident CTAs per SM of (kernel, threads, smem), cached.  Raises the
-// kernel's dynamic shared memory limit when a launch needs more than 48 KB.
+// Dynamic shared memory limit of each (kernel, device): the attribute is a
+// maximum, so it is only ever raised, to the largest size any launch of that
+// kernel has needed (lowering it for a smaller launch would break a later,
+// larger launch whose occupancy is already cached).
+struct SmemEntry {
+  const void* fn;
+  int device, limit;
+};
+SmemEntry g_smem[256];
+int g_nsmem = 0;
+
+cudaError_t ensure_smem(const void* fn, int device, int smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(g_mu);
+  SmemEntry* ent = nullptr;
+  for (int i = 0; i < g_nsmem; ++i)
+    if (g_smem[i].fn == fn && g_smem[i].device == device) ent = &g_smem[i];
+  if (ent && ent->limit >= smem) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (ent) ent->limit = smem;
+  else if (g_nsmem < 256) g_smem[g_nsmem++] = SmemEntry{fn, device, smem};
+  return cudaSuccess;
+}
+
+// Resident CTAs per SM of (kernel, threads, smem), cached.
 struct OccEntry {
   const void* fn;
   int device, threads, smem, blocks;
@@ -87,6 +152,8 @@ OccEntry g_occ[512];
 int g_nocc = 0;
 
 cudaError_t occupancy(const void* fn, int device, int threads, int smem, int* blocks) {
+  cudaError_t e = ensure_smem(fn, device, smem);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < g_nocc; ++i)
     if (g_occ[i].fn == fn && g_occ[i].device == device && g_occ[i].threads == threads &&
@@ -94,12 +161,8 @@ cudaError_t occupancy(const void* fn, int device, int threads, int smem, int* bl
       *blocks = g_occ[i].blocks;
       return cudaSuccess;
     }
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-  }
   int b = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
   if (e != cudaSuccess) return e;
   if (b < 1) return cudaErrorInvalidConfiguration;
   if (g_nocc < 512) g_occ[g_nocc++] = OccEntry{fn, device, threads, smem, b};
@@ -117,6 +180,7 @@ struct Plan {
   bool prefetch = false, acc_smem = false;
   int threads = 256;
   int smem = 0;
+  int stages = 0;            // kStaged: ring of row buffers
   int rows_per_cta = 1;      // rows one CTA iteration covers
   int cta_per_sm_cap = 0;    // 0: occupancy limit
   const void* fn = nullptr;
@@ -140,7 +204,7 @@ void subwarp_shape(int nvec, int* g, int* vpt) {
 
 // Vectors per thread for a row of nvec vectors in one CTA, and the CTA size.
 bool cta_shape(int op, int nvec, int* vpt, int* threads) {
-  static const int pref_fwd[] = {4, 2, 8, 1};
+  static const int pref_fwd[] = {2, 4, 8, 1};
   static const int pref_fused[] = {2, 4, 1, 8};
   static const int pref_bwd[] = {4, 2, 1, 8};
   const int* pref = op == kFwd ? pref_fwd : op == kFused ? pref_fused : pref_bwd;
@@ -163,12 +227,12 @@ bool cta_shape(int op, int nvec, int* vpt, int* threads) {
 }
 
 // RMSNORM_FORCE_VARIANT="family[:key=value...]" with family one of subwarp,
-// cta, ragged, generic and keys g, vpt, t (threads), pf (0/1), acc (0/1
-// shared-memory dgamma partials), cps (CTAs per SM cap).  For profiling A/B
+// cta, ragged, generic, staged and keys g, vpt, t (threads), pf (0/1), acc
+// (0/1 shared-memory dgamma partials), cps (CTAs per SM cap), st (stages).  For profiling A/B
 // runs; a forced variant that cannot serve the call is an argument error.
 struct Force {
   bool on = false;
-  int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0;
+  int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0, st = 0;
 };
 
 Force read_force() {
@@ -186,6 +250,7 @@ Force read_force() {
   else if (!strcmp(tok, "cta")) f.family = kCta;
   else if (!strcmp(tok, "ragged")) f.family = kRagged;
   else if (!strcmp(tok, "generic")) f.family = kGeneric;
+  else if (!strcmp(tok, "staged")) f.family = kStaged;
   while ((tok = strtok_r(nullptr, ":", &save))) {
     char* eq = strchr(tok, '=');
     if (!eq) continue;
@@ -197,6 +262,7 @@ Force read_force() {
     else if (!strcmp(tok, "pf")) f.pf = v;
     else if (!strcmp(tok, "acc")) f.acc = v;
     else if (!strcmp(tok, "cps")) f.cps = v;
+    else if (!strcmp(tok, "st")) f.st = v;
   }
   return f;
 }
@@ -214,11 +280,17 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     subwarp_shape(nvec, &p.g, &p.vpt);
     p.threads = kSubwarpThreads;
     p.rows_per_cta = kSubwarpThreads / p.g;
-    p.prefetch = true;
+    p.prefetch = !(op == kBwd && p.g == 32);   // full-warp rows: more CTAs beat prefetch
+  } else if (rows_aligned && op == kBwd && nvec <= 4 * kCtaMaxThreads) {
+    // backward: rows streamed by bulk copies, two stages, up to 4 vectors
+    // per thread (the dgamma partials and gamma stay in registers)
+    p.family = kStaged;
+    if (!cta_shape(op, nvec, &p.vpt, &p.threads) || p.vpt > 4) p.family = kGeneric;
+    p.stages = 2;
   } else if (rows_aligned && nvec <= 4096) {
     p.family = kCta;
     if (!cta_shape(op, nvec, &p.vpt, &p.threads)) p.family = kGeneric;
-    p.prefetch = p.vpt <= 2 || (op == kFwd && p.vpt <= 4);
+    p.prefetch = op == kFwd ? p.vpt <= 4 : (op == kFused ? p.vpt != 2 && p.vpt <= 4 : p.vpt <= 2);
     p.acc_smem = op == kBwd && p.vpt >= 4;
   } else if (same_mod16 && N <= kRaggedMaxN) {
     p.family = kRagged;
@@ -254,6 +326,12 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (!same_mod16 || N > kRaggedMaxN) return RMSNORM_ERR_INVALID_ARG;
       if (!f.threads) p.threads = round_up((N / E + 1 + p.vpt - 1) / (p.vpt ? p.vpt : 1), 32);
       if (p.vpt < 1 || (int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
+    } else if (p.family == kStaged) {
+      if (!rows_aligned) return RMSNORM_ERR_INVALID_ARG;
+      if (!p.vpt) p.vpt = 4;
+      if (!f.threads) p.threads = round_up((nvec + p.vpt - 1) / p.vpt, 32);
+      if ((int64_t)p.threads * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
+      p.stages = f.st;
     } else if (p.family == kGeneric) {
       if (!f.threads) p.threads = 256;
       if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
@@ -263,6 +341,22 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
   }
 
   // kernel and shared memory
+  if (p.family == kStaged) {
+    // ring of row buffers: as many stages as fit a half-SM budget (two CTAs
+    // per SM), at least two, at most kStagedMaxStages
+    const int ns = op == kFwd ? 1 : 2;
+    const int64_t stage_bytes = (int64_t)ns * N * esize(xd);
+    if (p.stages <= 0) {
+      int64_t st = (kStagedSmemBudget - kStagedHeader) / stage_bytes;
+      if (st < 2) st = (kStagedSmemMax - kStagedHeader) / stage_bytes;
+      p.stages = (int)(st > kStagedMaxStages ? kStagedMaxStages : st);
+    }
+    if (p.stages < 2 || p.stages > kStagedMaxStages ||
+        kStagedHeader + p.stages * stage_bytes > kStagedSmemMax)
+      return RMSNORM_ERR_INVALID_ARG;
+    p.smem = (int)(kStagedHeader + p.stages * stage_bytes);
+    p.rows_per_cta = 1;
+  }
   if (op == kBwd) {
     BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch};
     p.bwd = bwd_kernel(k);
@@ -271,14 +365,14 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (p.family == kSubwarp) p.smem = p.rows_per_cta * nvec * E * 4;
     else if (p.family == kCta) p.smem = 512 + (p.acc_smem ? ld * 4 : 0);
     else if (p.family == kRagged) p.smem = 512 + 2 * ld * 4;
-    else p.smem = 0;
+    else if (p.family != kStaged) p.smem = 0;
   } else {
     FwdKey k{xd, wd, p.family, p.g, p.vpt, op == kFused, p.prefetch};
     p.fwd = fwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.fwd);
     if (p.family == kCta) p.smem = 256;
     else if (p.family == kRagged) p.smem = 256 + N * 4;
-    else p.smem = 0;
+    else if (p.family != kStaged) p.smem = 0;
   }
   if (p.fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
   *pl = p;
@@ -286,13 +380,15 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
 }
 
 // Grid of a plan on a device: persistent, at most SMs x resident CTAs.
-rmsnorm_status_t size_grid(Plan* p, int64_t M, int device) {
+rmsnorm_status_t size_grid(Plan* p, int64_t M, int device, unsigned** status = nullptr) {
   DevInfo di;
-  if (device_info(device, &di) != cudaSuccess) return RMSNORM_ERR_CUDA;
+  cudaError_t e = device_info(device, &di);
+  if (e != cudaSuccess) return cuda_fail(e, "device attributes");
+  if (status) *status = di.status;
   if (p->smem > di.max_smem_optin) return RMSNORM_ERR_INVALID_ARG;
   int per_sm = 0;
-  if (occupancy(p->fn, device, p->threads, p->smem, &per_sm) != cudaSuccess)
-    return RMSNORM_ERR_CUDA;
+  if ((e = occupancy(p->fn, device, p->threads, p->smem, &per_sm)) != cudaSuccess)
+    return cuda_fail(e, "occupancy query");
   if (p->cta_per_sm_cap > 0 && per_sm > p->cta_per_sm_cap) per_sm = p->cta_per_sm_cap;
   const int64_t units = (M + p->rows_per_cta - 1) / p->rows_per_cta;
   const int64_t cap = (int64_t)di.sms * per_sm;
@@ -306,14 +402,15 @@ const char* family_name(int f) {
     case kSubwarp: return "subwarp";
     case kCta: return "cta";
     case kRagged: return "ragged";
+    case kStaged: return "staged";
     default: return "generic";
   }
 }
 
 void describe(int op, const Plan& p, char* buf, size_t len) {
   static const char* ops[] = {"fwd", "fused_add", "bwd"};
-  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d%s/grid%d/smem%d", ops[op], family_name(p.family),
-           p.g, p.vpt, p.threads, p.prefetch ? 1 : 0,
+  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d%s/grid%d/smem%d", ops[op],
+           family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages,
            op == kBwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem);
 }
 
@@ -334,12 +431,13 @@ rmsnorm_status_t check_sizes(int64_t M, int64_t N, float eps) {
 }
 
 rmsnorm_status_t current_device(int* dev) {
-  return cudaGetDevice(dev) == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+  const cudaError_t e = cudaGetDevice(dev);
+  return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e, "cudaGetDevice");
 }
 
-rmsnorm_status_t launched() {
+rmsnorm_status_t launched(const char* what) {
   const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+  return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e, what);
 }
 
 // ---------------------------------------------------------------- forward
@@ -374,7 +472,8 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   Plan pl;
   if ((st = make_plan(op, M, (int)N, xd, wd, aligned16, same, false, &pl)) != RMSNORM_OK)
     return st;
-  if ((st = size_grid(&pl, M, dev)) != RMSNORM_OK) return st;
+  unsigned* status = nullptr;
+  if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
 
   FwdParams prm;
   prm.x = x;
@@ -387,8 +486,11 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   prm.nvec = (int)(N / per_vec(xd));
   prm.eps = eps;
   prm.inv_n = 1.0f / (float)N;
+  prm.stages = pl.stages;
+  prm.wait_limit = wait_limit();
+  prm.status = status;
   pl.fwd<<<pl.grid, pl.threads, pl.smem, stream>>>(prm);
-  return launched();
+  return launched("forward kernel launch");
 }
 
 // ---------------------------------------------------------------- backward
@@ -418,8 +520,8 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
   if (M == 0) {
     if (dgamma) {
-      if (cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream) != cudaSuccess)
-        return RMSNORM_ERR_CUDA;
+      const cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync of dgamma");
     }
     return RMSNORM_OK;
   }
@@ -460,7 +562,8 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   if ((st = make_plan(kBwd, M, (int)N, xd, wd, aligned16, same, rstd != nullptr, &pl)) !=
       RMSNORM_OK)
     return st;
-  if ((st = size_grid(&pl, M, dev)) != RMSNORM_OK) return st;
+  unsigned* status = nullptr;
+  if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
   if (dgamma && pl.grid > prows) pl.grid = prows;
 
   BwdParams prm;
@@ -476,8 +579,11 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   prm.ld_partial = ld;
   prm.eps = eps;
   prm.inv_n = 1.0f / (float)N;
+  prm.stages = pl.stages;
+  prm.wait_limit = wait_limit();
+  prm.status = status;
   pl.bwd<<<pl.grid, pl.threads, pl.smem, stream>>>(prm);
-  if ((st = launched()) != RMSNORM_OK || !dgamma) return st;
+  if ((st = launched("backward stage-1 launch")) != RMSNORM_OK || !dgamma) return st;
 
   // stage 2, as a programmatic dependent launch of stage 1
   cudaLaunchConfig_t cfg = {};
@@ -495,7 +601,7 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
                                            (int)N, ld, dgamma);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return RMSNORM_ERR_CUDA;
+    return cuda_fail(e, "backward stage-2 launch");
   }
   return RMSNORM_OK;
 }
@@ -519,9 +625,10 @@ rmsnorm_status_t noalloc_scratch(int device, void** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_noalloc_addr[device] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
-      return RMSNORM_ERR_CUDA;
+      return cuda_fail(e, "cudaGetSymbolAddress of the scratch");
     }
     g_noalloc_addr[device] = p;
   }
@@ -597,6 +704,26 @@ rmsnorm_status_t rmsnorm_bwd_noalloc(const void* dy, const void* x, const float*
                   (int)x_dtype, (int)w_dtype, stream);
 }
 
+rmsnorm_status_t rmsnorm_check_device(cudaStream_t stream) {
+  int dev;
+  rmsnorm_status_t st = current_device(&dev);
+  if (st != RMSNORM_OK) return st;
+  DevInfo di;
+  cudaError_t e = device_info(dev, &di);
+  if (e != cudaSuccess) return cuda_fail(e, "device attributes");
+  unsigned flags = 0;
+  if ((e = cudaMemcpyAsync(&flags, di.status, sizeof flags, cudaMemcpyDeviceToHost, stream)) !=
+          cudaSuccess ||
+      (e = cudaMemsetAsync(di.status, 0, sizeof flags, stream)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "reading the device status word");
+  }
+  return (flags & kStatusWaitTimeout) ? RMSNORM_ERR_TIMEOUT : RMSNORM_OK;
+}
+
+const char* rmsnorm_last_error(void) { return g_last_error; }
+
 const char* rmsnorm_status_string(rmsnorm_status_t status) {
   switch (status) {
     case RMSNORM_OK: return "ok";
@@ -605,6 +732,7 @@ const char* rmsnorm_status_string(rmsnorm_status_t status) {
     case RMSNORM_ERR_MISALIGNED: return "pointer not aligned to its element size";
     case RMSNORM_ERR_WORKSPACE: return "workspace missing or too small";
     case RMSNORM_ERR_CUDA: return "CUDA runtime error";
+    case RMSNORM_ERR_TIMEOUT: return "a kernel gave up waiting for its own bulk copies";
     default: return "unknown status";
   }
 }

@@ -451,9 +451,10 @@ BwdKernel pick_rstd(const BwdKey& k) {
 #if RMSN_PAIR == 0
 // Stage 2: dgamma_j = sum_b partial[b][j] over the P stage-1 CTAs, in a fixed
 // order: thread (tx, ty) adds rows b = ty, ty + kRedRows, ... in sequence,
-// then the kRedRows chunk sums are added in ty order.  Launched as a
-// programmatic dependent of stage 1; griddepcontrol.wait returns once stage 1
-// has completed and its writes are visible.
+// then the kRedRows chunk sums are added in ty order.  Loads are issued in
+// batches of 8 ahead of the adds (the order of the adds does not change).
+// Launched as a programmatic dependent of stage 1; griddepcontrol.wait
+// returns once stage 1 has completed and its writes are visible.
 __global__ void __launch_bounds__(kRedCols* kRedRows)
     dgamma_reduce_kernel(const float* partial, int P, int N, int ld, float* dgamma) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -464,8 +465,21 @@ __global__ void __launch_bounds__(kRedCols* kRedRows)
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (q < nq) {
     const float4* src = reinterpret_cast<const float4*>(partial) + q;
-#pragma unroll 4
-    for (int b = ty; b < P; b += kRedRows) {
+    int b = ty;
+    constexpr int B = 8;
+    for (; b + (B - 1) * kRedRows < P; b += B * kRedRows) {
+      float4 v[B];
+#pragma unroll
+      for (int u = 0; u < B; ++u) v[u] = __ldcs(src + (size_t)(b + u * kRedRows) * nq);
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        s.x += v[u].x;
+        s.y += v[u].y;
+        s.z += v[u].z;
+        s.w += v[u].w;
+      }
+    }
+    for (; b < P; b += kRedRows) {
       const float4 v = __ldcs(src + (size_t)b * nq);
       s.x += v.x;
       s.y += v.y;

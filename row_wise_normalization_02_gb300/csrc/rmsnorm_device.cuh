@@ -144,4 +144,112 @@ __device__ __forceinline__ void cta_sum(float (&v)[K], float* red, int parity) {
   }
 }
 
+// cta_sum whose barrier also takes a vote: returns true in every thread when
+// `pred` is true in any thread (so a decision based on it is CTA-uniform).
+template <int K>
+__device__ __forceinline__ bool cta_sum_vote(float (&v)[K], float* red, int parity, bool pred) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int k = 0; k < K; ++k) v[k] = group_sum<32>(v[k]);
+  float* buf = red + parity * (K * 32);
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) buf[k * 32 + warp] = v[k];
+  }
+  const bool any = __syncthreads_or(pred ? 1 : 0) != 0;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    float s = 0.f;
+    for (int w = 0; w < nwarps; ++w) s += buf[k * 32 + w];
+    v[k] = s;
+  }
+  return any;
+}
+
+// ---------------------------------------------------------------- bulk copies
+
+// 1-D bulk copies global -> shared (the non-tensor form of TMA) completing on
+// an mbarrier, and bounded waits on that barrier.  Every wait gives up after
+// `limit` SM clock cycles and reports it, so no kernel can spin forever.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses of shared memory before
+// later bulk copies into it (the stage being refilled was just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Arrive once and expect `bytes` of bulk-copy data on the barrier.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Copy `bytes` (multiple of 16, both addresses 16-byte aligned) from global
+// to shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Potentially blocking test: the thread may be suspended up to about
+// `hint_ns` nanoseconds waiting for the phase to complete.
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase with the given parity to complete; false once `limit`
+// SM clock cycles have passed without completion (limit <= 0: do not wait
+// at all, only test).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit) {
+  if (mbar_test(bar, parity)) return true;
+  if (limit <= 0) return false;
+  const long long t0 = clock64();
+  do {
+    if (mbar_try(bar, parity, 2000u)) return true;
+  } while (clock64() - t0 <= limit);
+  return false;
+}
+
 }  // namespace rmsn

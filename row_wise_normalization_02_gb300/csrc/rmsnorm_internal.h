@@ -19,7 +19,17 @@ enum DT : int { kF32 = 0, kBF16 = 1 };
 //             head and tail around an aligned vector body; gamma staged in
 //             shared memory as fp32.
 //  kGeneric : any N, any element-aligned pointers; scalar two-pass loop.
-enum Family : int { kSubwarp = 0, kCta = 1, kRagged = 2, kGeneric = 3 };
+//  kStaged  : as kCta, but rows arrive by bulk copies (the 1-D form of TMA)
+//             into a ring of `stages` shared-memory row buffers, so several
+//             rows per CTA are in flight independently of register pressure.
+enum Family : int { kSubwarp = 0, kCta = 1, kRagged = 2, kGeneric = 3, kStaged = 4 };
+
+// Shared-memory header of the staged kernels: barriers, reduction scratch
+// and the error flag; the ring of row buffers starts after it.
+constexpr int kStagedMaxStages = 8;
+// Status bits a kernel may raise in the library's device status word.
+constexpr unsigned kStatusWaitTimeout = 1u;
+constexpr int kStagedHeader = 1024;
 
 struct FwdParams {
   const void* x;
@@ -32,6 +42,9 @@ struct FwdParams {
   int nvec;           // 16-byte vectors per row (aligned families)
   float eps;
   float inv_n;
+  int stages;         // kStaged: row buffers in the shared-memory ring
+  long long wait_limit;   // kStaged: clock cycles before a wait gives up
+  unsigned* status;   // device status word (kStatus* bits)
 };
 
 struct BwdParams {
@@ -47,6 +60,9 @@ struct BwdParams {
   int ld_partial;     // row stride of partial, a multiple of 4 floats
   float eps;
   float inv_n;
+  int stages;
+  long long wait_limit;
+  unsigned* status;
 };
 
 using FwdKernel = void (*)(FwdParams);
@@ -80,13 +96,19 @@ FwdKernel get_fwd_kernel_bf16_f32(const FwdKey& k);
 BwdKernel get_bwd_kernel_f32_f32(const BwdKey& k);
 BwdKernel get_bwd_kernel_bf16_bf16(const BwdKey& k);
 BwdKernel get_bwd_kernel_bf16_f32(const BwdKey& k);
+FwdKernel get_fwd_staged_f32_f32(const FwdKey& k);
+FwdKernel get_fwd_staged_bf16_bf16(const FwdKey& k);
+FwdKernel get_fwd_staged_bf16_f32(const FwdKey& k);
+BwdKernel get_bwd_staged_f32_f32(const BwdKey& k);
+BwdKernel get_bwd_staged_bf16_bf16(const BwdKey& k);
+BwdKernel get_bwd_staged_bf16_f32(const BwdKey& k);
 ReduceKernel get_dgamma_reduce_kernel();
 
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;
 constexpr int kCtaMaxThreads = 512;
 // Stage-2 reduction tile: kRedCols float4 column groups x kRedRows row chunks.
-constexpr int kRedCols = 16;
-constexpr int kRedRows = 16;
+constexpr int kRedCols = 8;
+constexpr int kRedRows = 32;
 
 }  // namespace rmsn

@@ -1,0 +1,350 @@
+// Bulk-copy staged RMSNorm kernels (forward, fused add, backward) for sm_103a.
+//
+// Same arithmetic as the register-resident one-row-per-CTA kernels (see
+// rmsnorm_fwd.cu / rmsnorm_bwd.cu for the formulas and their sources), but the
+// rows of the streamed operands (x; r and x; x and dy) arrive through
+// `cp.async.bulk` copies into a ring of `stages` shared-memory row buffers,
+// each tracked by an mbarrier.  One thread keeps the ring `stages` rows ahead
+// of the CTA, so the number of bytes in flight per SM is set by the ring, not
+// by how many registers the row math needs -- the GB300 way to stream rows,
+// where the pages' LDS-cached design ("Pre-built kernel library guide",
+// section 1.2, pass 0: global -> LDS row cache) loads the row with the threads
+// themselves.
+//
+// Pipeline of CTA row i (stage s = i mod stages):
+//   wait(full[s])  ->  read own vectors from stage s  ->  CTA reduction
+//   (its barrier also proves every thread is done with stage s)  ->  thread 0
+//   refills stage s with row i + stages  ->  outputs from registers.
+// Every wait is bounded by p.wait_limit clock cycles.  Whether any thread's
+// wait ran out is voted on at the reduction barrier (__syncthreads_or), so the
+// whole CTA agrees: it stores nothing for that row and leaves; thread 0 first
+// waits (bounded) for the copies it has in flight, then raises
+// kStatusWaitTimeout in p.status.
+#include <type_traits>
+
+#include "rmsnorm_device.cuh"
+#include "rmsnorm_internal.h"
+
+#ifndef RMSN_PAIR
+#error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
+#endif
+
+namespace rmsn {
+namespace {
+
+constexpr long long kDrainLimit = 1LL << 34;   // cycles: several seconds
+
+struct Ring {
+  uint64_t* full;       // kStagedMaxStages barriers
+  float* red;           // 2 x 2 x 32 reduction slots
+  unsigned char* buf;   // stages x NS x row bytes
+};
+
+__device__ __forceinline__ Ring ring_of(unsigned char* smem) {
+  Ring r;
+  r.full = reinterpret_cast<uint64_t*>(smem);
+  r.red = reinterpret_cast<float*>(smem + 128);
+  r.buf = smem + kStagedHeader;
+  return r;
+}
+
+// Thread 0: bulk-copy CTA row i of the NS streamed operands into its stage.
+template <int NS>
+__device__ __forceinline__ void issue_row(const Ring& rg, int64_t i, int64_t first, int64_t stride,
+                                          int S, const char* src0, const char* src1, size_t rb) {
+  const int s = (int)(i % S);
+  const int64_t row = first + i * stride;
+  uint64_t* bar = rg.full + s;
+  unsigned char* dst = rg.buf + (size_t)s * NS * rb;
+  mbar_arrive_expect_tx(bar, (uint32_t)(NS * rb));
+  bulk_copy_g2s(dst, src0 + row * rb, (uint32_t)rb, bar);
+  if (NS > 1) bulk_copy_g2s(dst + rb, src1 + row * rb, (uint32_t)rb, bar);
+}
+
+// Thread 0, error path: wait (bounded) for rows [from, issued) still in flight.
+__device__ __forceinline__ void drain(const Ring& rg, int64_t from, int64_t issued, int S) {
+  for (int64_t j = from; j < issued; ++j)
+    mbar_wait_bounded(rg.full + (j % S), (uint32_t)((j / S) & 1), kDrainLimit);
+}
+
+// Prologue: barriers initialised, the first min(S, nrows) rows requested.
+template <int NS>
+__device__ __forceinline__ int64_t ring_start(const Ring& rg, int S, int64_t nrows, int64_t first,
+                                              int64_t stride, const char* src0, const char* src1,
+                                              size_t rb) {
+  int64_t issued = 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int64_t n0 = nrows < S ? nrows : S;
+    for (; issued < n0; ++issued) issue_row<NS>(rg, issued, first, stride, S, src0, src1, rb);
+  }
+  return issued;
+}
+
+template <typename TW, int E>
+__device__ __forceinline__ void gamma_f32(const void* gamma, int v, float (&g)[E]) {
+  constexpr int GW = E * (int)sizeof(TW) / 16;
+  const char* gp = static_cast<const char*>(gamma) + (size_t)v * GW * 16;
+  if constexpr (std::is_same<TW, float>::value) {
+#pragma unroll
+    for (int w = 0; w < GW; ++w) {
+      float t[4];
+      unpack(ld_cached(gp + w * 16), t);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) g[w * 4 + i] = t[i];
+    }
+  } else {
+    unpack(ld_cached(gp), g);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Forward / fused add.  Stage layout: fused [r | x], forward [x].
+template <typename TX, typename TW, int VPT, bool FUSED>
+__global__ void __launch_bounds__(kCtaMaxThreads) fwd_staged_kernel(const FwdParams p) {
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int NS = FUSED ? 2 : 1;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Ring rg = ring_of(smem);
+  const int tid = threadIdx.x, T = blockDim.x, S = p.stages;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t nrows = first < p.M ? (p.M - 1 - first) / stride + 1 : 0;
+  const char* xs = static_cast<const char*>(p.x);
+  const char* rs_src = static_cast<const char*>(p.residual);
+  int64_t issued = ring_start<NS>(rg, S, nrows, first, stride, FUSED ? rs_src : xs, xs, rb);
+
+  float g[VPT][E];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < p.nvec) gamma_f32<TW, E>(p.gamma, v, g[k]);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) g[k][e] = 0.f;
+  }
+
+  int parity = 0;
+  int64_t i = 0;
+  bool failed = false;
+  for (; i < nrows; ++i) {
+    const int s = (int)(i % S);
+    const int64_t row = first + i * stride;
+    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
+    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * NS * rb);
+    uint4 hv[VPT];
+    float ss[1] = {0.f};
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      hv[k] = make_uint4(0, 0, 0, 0);
+      if (v < p.nvec) {
+        float f[E];
+        if constexpr (FUSED) {
+          float rf[E];
+          unpack(st[v], rf);
+          unpack(st[p.nvec + v], f);
+#pragma unroll
+          for (int e = 0; e < E; ++e) f[e] += rf[e];
+          hv[k] = pack(f);      // h rounded to the activation dtype
+          unpack(hv[k], f);
+        } else {
+          hv[k] = st[v];
+          unpack(hv[k], f);
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) ss[0] = fmaf(f[e], f[e], ss[0]);
+      }
+    }
+    if (cta_sum_vote<1>(ss, rg.red, parity, late)) {
+      failed = true;
+      break;
+    }
+    parity ^= 1;
+    if (tid == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue_row<NS>(rg, issued, first, stride, S, FUSED ? rs_src : xs, xs, rb);
+      ++issued;
+    }
+    const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
+    if (tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+    char* yrow = static_cast<char*>(p.y) + row * rb;
+    char* hrow = static_cast<char*>(p.residual) + row * rb;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < p.nvec) {
+        if (FUSED) st_stream(hrow + (size_t)v * 16, hv[k]);
+        float o[E];
+        unpack(hv[k], o);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[k][e];
+        st_stream(yrow + (size_t)v * 16, pack(o));
+      }
+    }
+  }
+  if (failed && tid == 0) {
+    drain(rg, i, issued, S);
+    atomicOr(p.status, kStatusWaitTimeout);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward.  Stage layout [x | dy]; dgamma partials of this CTA's rows in
+// registers, written as one partial row at the end.
+template <typename TX, typename TW, int VPT, bool HAS_RSTD>
+__global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdParams p) {
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int K = HAS_RSTD ? 1 : 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Ring rg = ring_of(smem);
+  const int tid = threadIdx.x, T = blockDim.x, S = p.stages;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t nrows = first < p.M ? (p.M - 1 - first) / stride + 1 : 0;
+  const char* xs = static_cast<const char*>(p.x);
+  const char* ds = static_cast<const char*>(p.dy);
+  int64_t issued = ring_start<2>(rg, S, nrows, first, stride, xs, ds, rb);
+
+  float g[VPT][E], acc[VPT][E];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < p.nvec) gamma_f32<TW, E>(p.gamma, v, g[k]);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) g[k][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+  }
+
+  int parity = 0;
+  int64_t i = 0;
+  bool failed = false;
+  for (; i < nrows; ++i) {
+    const int s = (int)(i % S);
+    const int64_t row = first + i * stride;
+    const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
+    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
+    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * 2 * rb);
+    uint4 xv[VPT], dv[VPT];
+    float sums[K];
+#pragma unroll
+    for (int q = 0; q < K; ++q) sums[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      xv[k] = make_uint4(0, 0, 0, 0);
+      dv[k] = make_uint4(0, 0, 0, 0);
+      if (v < p.nvec) {
+        xv[k] = st[v];
+        dv[k] = st[p.nvec + v];
+        float xf[E], df[E];
+        unpack(xv[k], xf);
+        unpack(dv[k], df);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          sums[0] = fmaf(g[k][e] * df[e], xf[e], sums[0]);
+          if (!HAS_RSTD) sums[K - 1] = fmaf(xf[e], xf[e], sums[K - 1]);
+        }
+      }
+    }
+    if (cta_sum_vote<K>(sums, rg.red, parity, late)) {
+      failed = true;
+      break;
+    }
+    parity ^= 1;
+    if (tid == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue_row<2>(rg, issued, first, stride, S, xs, ds, rb);
+      ++issued;
+    }
+    const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
+    const float c = r * r * p.inv_n * sums[0];
+    char* dxrow = static_cast<char*>(p.dx) + row * rb;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < p.nvec) {
+        float xf[E], df[E], o[E];
+        unpack(xv[k], xf);
+        unpack(dv[k], df);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
+          acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
+        }
+        st_stream(dxrow + (size_t)v * 16, pack(o));
+      }
+    }
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (failed) {
+    if (tid == 0) {
+      drain(rg, i, issued, S);
+      atomicOr(p.status, kStatusWaitTimeout);
+    }
+    return;
+  }
+  if (p.partial == nullptr) return;
+  float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < p.nvec) {
+      float4* d = reinterpret_cast<float4*>(prow + v * E);
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q)
+        d[q] = make_float4(acc[k][4 * q], acc[k][4 * q + 1], acc[k][4 * q + 2], acc[k][4 * q + 3]);
+    }
+  }
+}
+
+template <typename TX, typename TW, bool FUSED>
+FwdKernel pick_fwd(int vpt) {
+  switch (vpt) {
+    case 1: return fwd_staged_kernel<TX, TW, 1, FUSED>;
+    case 2: return fwd_staged_kernel<TX, TW, 2, FUSED>;
+    case 4: return fwd_staged_kernel<TX, TW, 4, FUSED>;
+    case 8: return fwd_staged_kernel<TX, TW, 8, FUSED>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW, bool HAS_RSTD>
+BwdKernel pick_bwd(int vpt) {
+  switch (vpt) {
+    case 1: return bwd_staged_kernel<TX, TW, 1, HAS_RSTD>;
+    case 2: return bwd_staged_kernel<TX, TW, 2, HAS_RSTD>;
+    case 4: return bwd_staged_kernel<TX, TW, 4, HAS_RSTD>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW>
+FwdKernel staged_fwd(const FwdKey& k) {
+  return k.fused ? pick_fwd<TX, TW, true>(k.vpt) : pick_fwd<TX, TW, false>(k.vpt);
+}
+template <typename TX, typename TW>
+BwdKernel staged_bwd(const BwdKey& k) {
+  return k.has_rstd ? pick_bwd<TX, TW, true>(k.vpt) : pick_bwd<TX, TW, false>(k.vpt);
+}
+
+}  // namespace
+
+#if RMSN_PAIR == 0
+FwdKernel get_fwd_staged_f32_f32(const FwdKey& k) { return staged_fwd<float, float>(k); }
+BwdKernel get_bwd_staged_f32_f32(const BwdKey& k) { return staged_bwd<float, float>(k); }
+#elif RMSN_PAIR == 1
+FwdKernel get_fwd_staged_bf16_bf16(const FwdKey& k) { return staged_fwd<bf16, bf16>(k); }
+BwdKernel get_bwd_staged_bf16_bf16(const BwdKey& k) { return staged_bwd<bf16, bf16>(k); }
+#else
+FwdKernel get_fwd_staged_bf16_f32(const FwdKey& k) { return staged_fwd<bf16, float>(k); }
+BwdKernel get_bwd_staged_bf16_f32(const BwdKey& k) { return staged_bwd<bf16, float>(k); }
+#endif
+
+}  // namespace rmsn

@@ -78,6 +78,17 @@ def test_bwd_recomputes_rstd_when_absent(N):
     check_bwd(x, dy, g, None, eps, "bf16", "f32", out)
 
 
+@pytest.mark.parametrize("force", ["staged:vpt=4:st=3:cps=1", "staged:vpt=2:st=2:cps=1"])
+def test_staged_bwd_recomputes_rstd_and_skips_dgamma(monkeypatch, force):
+    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+    x, dy, g = make(500, 4096, "bf16", "f32", seed=14)
+    eps = f32(1e-4)
+    out = pu.run_bwd(dy, x, None, g, eps, "bf16", "f32")
+    check_bwd(x, dy, g, None, eps, "bf16", "f32", out)
+    out = pu.run_bwd(dy, x, None, g, eps, "bf16", "f32", want_dgamma=False)
+    check_bwd(x, dy, g, None, eps, "bf16", "f32", out, want_dgamma=False)
+
+
 @pytest.mark.parametrize("N", [128, 8192, 2049])
 def test_bwd_without_dgamma(N):
     x, dy, g = make(200, N, "bf16", "bf16", seed=N + 13)
@@ -97,6 +108,9 @@ def test_bwd_without_dgamma(N):
     ("cta:vpt=1:pf=1:acc=0:cps=1", 2048),
     ("ragged:vpt=2:pf=1:cps=1", 2049), ("ragged:vpt=1:pf=0:cps=1", 2049),
     ("generic:cps=1", 8192), ("generic:cps=1", 2049),
+    ("staged:vpt=4:st=3:cps=1", 8192), ("staged:vpt=4:st=2:cps=1", 8192),
+    ("staged:vpt=2:st=4:cps=1", 4096), ("staged:vpt=1:st=2:cps=1", 2048),
+    ("staged:vpt=4:st=2:cps=1", 5120), ("staged:vpt=4:st=3:cps=1", 1032),
 ])
 def test_forced_variants_walk_several_rows(monkeypatch, force, N):
     monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
@@ -171,3 +185,19 @@ def test_zero_rows_zero_dgamma():
                    "bf16", "bf16")
     torch.cuda.synchronize()
     assert (bdg.download(np.float32) == 0).all()
+
+
+def test_shared_memory_limit_is_never_lowered():
+    # The staged kernels need more than 48 KB of dynamic shared memory.  A
+    # query that caches a large launch, then a smaller launch of the same
+    # kernel, then the large launch again must all work (the kernel's limit
+    # may only grow).
+    import row_wise_normalization_02_gb300 as rn
+    big, small = 8192, 7168
+    rn.rmsnorm_bwd_workspace_size(16384, big, "bf16", "f32")
+    for N in (small, big, small, big):
+        x, dy, g = make(64, N, "bf16", "f32", seed=25)
+        eps = f32(1e-5)
+        rstd = oracle.fwd(x, g, eps, "bf16", "f32")["rstd"]
+        out = pu.run_bwd(dy, x, rstd, g, eps, "bf16", "f32")
+        check_bwd(x, dy, g, rstd, eps, "bf16", "f32", out)

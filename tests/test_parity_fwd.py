@@ -98,6 +98,10 @@ def test_fused_add_matches_oracle(xd, wd, M, N):
     ("cta:vpt=1:pf=1:cps=1", 2048), ("cta:vpt=4:pf=1:t=512:cps=1", 5120),
     ("ragged:vpt=2:pf=1:cps=1", 2049), ("ragged:vpt=1:pf=0:cps=1", 2049),
     ("ragged:vpt=4:pf=1:cps=1", 4096), ("generic:cps=1", 8192), ("generic:cps=1", 2049),
+    ("staged:vpt=4:st=3:cps=1", 8192), ("staged:vpt=4:st=2:cps=1", 8192),
+    ("staged:vpt=2:st=5:cps=1", 4096), ("staged:vpt=8:st=2:cps=1", 16384),
+    ("staged:vpt=1:st=8:cps=1", 2048), ("staged:vpt=4:t=512:st=2:cps=1", 5120),
+    ("staged:vpt=4:st=4:cps=1", 1032),
 ])
 def test_forced_variants_walk_several_rows(monkeypatch, op, force, N):
     # one CTA per SM: each CTA walks several rows, exercising the persistent
@@ -208,3 +212,5 @@ def test_plan_families():
     assert "/cta/" in rn.rmsnorm_describe_plan(rn.OP_FUSED_ADD, 32768, 4096, "bf16", "bf16")
     assert "/ragged/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 4096, 2049, "bf16", "bf16")
     assert "/generic/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 40000, "bf16", "bf16")
+    assert "/staged/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 16384, 8192, "bf16", "f32")
+    assert "/subwarp/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 262144, 128, "bf16", "bf16")
