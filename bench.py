@@ -241,8 +241,6 @@ def run_ours(args, rank, world):
                 op["launch"]()
     stream.synchronize()
 
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)] for _ in ops]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -255,13 +253,14 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    # timed region 1: K steps back to back, nothing between the launches, so
+    # each kernel's launch overlaps the previous one (programmatic dependent
+    # launch) as it would in a model
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for i in range(K):
-            for j, op in enumerate(ops):
-                ev[j][i][0].record(stream)
+            for op in ops:
                 op["launch"]()
-                ev[j][i][1].record(stream)
         t_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -270,6 +269,18 @@ def run_ours(args, rank, world):
     if sampler:
         sampler.stop()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    # timed region 2: the same steps with an event pair around every call, for
+    # each op's own launch duration (the events between the launches cost the
+    # overlap, so these durations add up to slightly more than region 1)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)] for _ in ops]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            for j, op in enumerate(ops):
+                ev[j][i][0].record(stream)
+                op["launch"]()
+                ev[j][i][1].record(stream)
+    stream.synchronize()
     step_bytes = sum(op["bytes"] for op in ops)
     ms_per_step = total_ms / K
     value = job_gbs(step_bytes, ms_per_step, world)
@@ -339,6 +350,8 @@ def run_ours(args, rank, world):
             "frac_of_nominal_7900": round(value / world / NOMINAL_HBM_GBS, 4),
             "roofline": roofline, "ops": per_op, "e2e": e2e,
             "gpu_launches": K * sum(LAUNCHES_PER_OP[op["wl"].op] for op in ops),
+            "timing": {"value": "CUDA events around K back-to-back steps on the launching stream",
+                       "ops": "CUDA events around each call, over a second run of K steps"},
             "clocks": sampler.summary() if sampler else None}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -476,20 +489,21 @@ def make_launch(wl, d, stream, rn):
 
 
 def time_rotation(launches, steps, warmup, stream):
-    """Per-launch device times (ms) of `steps` back-to-back launches cycling
-    through the operand sets, after `warmup` untimed ones."""
+    """Average device time (ms) per launch of `steps` back-to-back launches
+    cycling through the operand sets, after `warmup` untimed ones: one event
+    pair around the whole batch, so the number is steady-state throughput
+    (inter-kernel gaps included, no per-launch event overhead)."""
     import torch
     with torch.cuda.stream(stream):
         for i in range(warmup):
             launches[i % len(launches)]()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
         for i in range(steps):
-            ev[i][0].record(stream)
             launches[(warmup + i) % len(launches)]()
-            ev[i][1].record(stream)
+        b.record(stream)
     stream.synchronize()
-    return [a.elapsed_time(b) for a, b in ev]
+    return a.elapsed_time(b) / steps
 
 
 def run_sweep(args):
@@ -514,18 +528,21 @@ def run_sweep(args):
             rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"], d["rstd"], wl.M, wl.N,
                            float(np.float32(wl.eps)), wl.x_dtype, wl.w_dtype, stream)
         launches = [make_launch(wl, d, stream, rn) for d in sets]
-        us = [t * 1e3 for t in time_rotation(launches, args.steps, args.warmup, stream)]
+        us = [time_rotation(launches, args.steps, args.warmup, stream) * 1e3
+              for _ in range(args.rounds)]
         med = statistics.median(us)
         byts = alg_bytes(wl)
         print(json.dumps({"workload": name, "op": wl.op, "M": wl.M, "N": wl.N,
                           "variant": rn.rmsnorm_describe_plan(_op_code(wl.op), wl.M, wl.N,
                                                               wl.x_dtype, wl.w_dtype),
-                          "median_us": round(med, 2), "min_us": round(min(us), 2),
-                          "max_us": round(max(us), 2), "gbs": round(byts / med / 1e3, 1),
+                          "us_per_call": round(med, 2), "rounds_us": [round(u, 2) for u in us],
+                          "gbs": round(byts / med / 1e3, 1),
                           "frac_of_measured_peak": round(byts / med / 1e3 / peak, 4),
                           "rows_per_s": round(wl.M / med * 1e6, 1), "alg_bytes": byts,
                           "l2": f"rotation over {len(sets)} operand set(s) "
-                                f">= 3 x L2, back-to-back launches"}), flush=True)
+                                f">= 3 x L2, back-to-back launches",
+                          "timer": "CUDA events around each round of back-to-back calls; "
+                                   "median of rounds"}), flush=True)
         del sets, launches
         torch.cuda.empty_cache()
 
@@ -539,6 +556,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--workloads", default="")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--rounds", type=int, default=5, help="--sweep: timed rounds per workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

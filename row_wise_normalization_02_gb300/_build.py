@@ -1,8 +1,8 @@
 """Build librmsnorm_gb300.so in-tree with nvcc for sm_103a.
 
-Ten translation units (forward, backward and the staged kernels once per
-dtype pair, plus the C ABI) compile in parallel, then link into one shared library with the CUDA
-runtime linked statically.  Rebuilds only when a source is newer than the
+Thirteen translation units (forward, backward, staged and ragged kernels
+once per dtype pair, plus the C ABI) compile in parallel, then link into one
+shared library with the CUDA runtime linked statically.  Rebuilds only when a source is newer than the
 library.
 """
 from __future__ import annotations
@@ -32,6 +32,9 @@ UNITS = [("rmsnorm_fwd.cu", ["-DRMSN_PAIR=0"], "fwd_p0.o"),
          ("rmsnorm_staged.cu", ["-DRMSN_PAIR=0"], "staged_p0.o"),
          ("rmsnorm_staged.cu", ["-DRMSN_PAIR=1"], "staged_p1.o"),
          ("rmsnorm_staged.cu", ["-DRMSN_PAIR=2"], "staged_p2.o"),
+         ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=0"], "ragged_p0.o"),
+         ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=1"], "ragged_p1.o"),
+         ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=2"], "ragged_p2.o"),
          ("rmsnorm_api.cu", [], "api.o")]
 
 

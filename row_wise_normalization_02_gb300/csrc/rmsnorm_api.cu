@@ -51,6 +51,12 @@ bool dtype_pair_ok(int xd, int wd) {
 }
 
 FwdKernel fwd_kernel(const FwdKey& k) {
+  if (k.family == kRagged) {
+    if (k.xd == kF32 && k.wd == kF32) return get_fwd_ragged_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16) return get_fwd_ragged_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32) return get_fwd_ragged_bf16_f32(k);
+    return nullptr;
+  }
   const bool st = k.family == kStaged;
   if (k.xd == kF32 && k.wd == kF32) return st ? get_fwd_staged_f32_f32(k) : get_fwd_kernel_f32_f32(k);
   if (k.xd == kBF16 && k.wd == kBF16)
@@ -60,6 +66,12 @@ FwdKernel fwd_kernel(const FwdKey& k) {
   return nullptr;
 }
 BwdKernel bwd_kernel(const BwdKey& k) {
+  if (k.family == kRagged) {
+    if (k.xd == kF32 && k.wd == kF32) return get_bwd_ragged_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16) return get_bwd_ragged_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32) return get_bwd_ragged_bf16_f32(k);
+    return nullptr;
+  }
   const bool st = k.family == kStaged;
   if (k.xd == kF32 && k.wd == kF32) return st ? get_bwd_staged_f32_f32(k) : get_bwd_kernel_f32_f32(k);
   if (k.xd == kBF16 && k.wd == kBF16)
@@ -182,6 +194,9 @@ struct Plan {
   int smem = 0;
   int stages = 0;            // kStaged: ring of row buffers
   int rows_per_cta = 1;      // rows one CTA iteration covers
+  int min_rows = 0;          // backward: rows per CTA at least this many (bounds
+                             // the dgamma partial rows), unless below 1 CTA/SM
+  int period = 1;            // kRagged: the grid is a multiple of it
   int cta_per_sm_cap = 0;    // 0: occupancy limit
   const void* fn = nullptr;
   FwdKernel fwd = nullptr;
@@ -226,13 +241,39 @@ bool cta_shape(int op, int nvec, int* vpt, int* threads) {
   return false;
 }
 
+// Vectors per thread (1, 2 or 4) and CTA size for a ragged row of at most
+// nvec vectors; false when the row needs more than 4 x 512.
+bool ragged_shape(int nvec, int* vpt, int* threads) {
+  static const int pref[] = {2, 4, 1};
+  for (int i = 0; i < 3; ++i) {
+    const int v = pref[i];
+    int t = round_up((nvec + v - 1) / v, 32);
+    if (t < 64) t = 64;
+    if (t <= kCtaMaxThreads) {
+      *vpt = v;
+      *threads = t;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Rows i and i + P start at the same address modulo 16 for a row of `bytes`:
+// P = 16 / gcd(bytes, 16).
+int ragged_period(int64_t bytes) {
+  int g = 1;
+  while (g < 16 && bytes % (2 * g) == 0) g *= 2;
+  return 16 / g;
+}
+
 // RMSNORM_FORCE_VARIANT="family[:key=value...]" with family one of subwarp,
 // cta, ragged, generic, staged and keys g, vpt, t (threads), pf (0/1), acc
-// (0/1 shared-memory dgamma partials), cps (CTAs per SM cap), st (stages).  For profiling A/B
+// (0/1 shared-memory dgamma partials), cps (CTAs per SM cap), st (stages),
+// mr (backward: minimum rows per CTA, 0 = none).  For profiling A/B
 // runs; a forced variant that cannot serve the call is an argument error.
 struct Force {
   bool on = false;
-  int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0, st = 0;
+  int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0, st = 0, mr = -1;
 };
 
 Force read_force() {
@@ -263,6 +304,7 @@ Force read_force() {
     else if (!strcmp(tok, "acc")) f.acc = v;
     else if (!strcmp(tok, "cps")) f.cps = v;
     else if (!strcmp(tok, "st")) f.st = v;
+    else if (!strcmp(tok, "mr")) f.mr = v;
   }
   return f;
 }
@@ -294,7 +336,8 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.acc_smem = op == kBwd && p.vpt >= 4;
   } else if (same_mod16 && N <= kRaggedMaxN) {
     p.family = kRagged;
-    if (!cta_shape(op, N / E + 1, &p.vpt, &p.threads)) p.family = kGeneric;
+    if (!ragged_shape(N / E + 1, &p.vpt, &p.threads)) p.family = kGeneric;
+    p.period = ragged_period((int64_t)N * esize(xd));
     p.prefetch = p.vpt <= 2;
   } else {
     p.family = kGeneric;
@@ -324,8 +367,13 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (p.vpt < 1 || (int64_t)p.threads * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
     } else if (p.family == kRagged) {
       if (!same_mod16 || N > kRaggedMaxN) return RMSNORM_ERR_INVALID_ARG;
-      if (!f.threads) p.threads = round_up((N / E + 1 + p.vpt - 1) / (p.vpt ? p.vpt : 1), 32);
-      if (p.vpt < 1 || (int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
+      if (!p.vpt) p.vpt = 2;
+      if (!f.threads) {
+        p.threads = round_up((N / E + 1 + p.vpt - 1) / p.vpt, 32);
+        if (p.threads < 64) p.threads = 64;
+      }
+      if ((int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
+      p.period = ragged_period((int64_t)N * esize(xd));
     } else if (p.family == kStaged) {
       if (!rows_aligned) return RMSNORM_ERR_INVALID_ARG;
       if (!p.vpt) p.vpt = 4;
@@ -337,6 +385,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
     }
     if (p.family != kSubwarp) p.rows_per_cta = 1;
+    if (p.family != kRagged) p.period = 1;
     if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32) return RMSNORM_ERR_INVALID_ARG;
   }
 
@@ -358,20 +407,25 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.rows_per_cta = 1;
   }
   if (op == kBwd) {
+    // each CTA writes one dgamma partial row (N fp32); keep that traffic to a
+    // few percent of the rows it reads
+    p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
+    const Force fr = read_force();
+    if (fr.on && fr.mr >= 0) p.min_rows = fr.mr;
     BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch};
     p.bwd = bwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.bwd);
     const int ld = round_up(N, 4);
     if (p.family == kSubwarp) p.smem = p.rows_per_cta * nvec * E * 4;
     else if (p.family == kCta) p.smem = 512 + (p.acc_smem ? ld * 4 : 0);
-    else if (p.family == kRagged) p.smem = 512 + 2 * ld * 4;
+    else if (p.family == kRagged) p.smem = 512;
     else if (p.family != kStaged) p.smem = 0;
   } else {
     FwdKey k{xd, wd, p.family, p.g, p.vpt, op == kFused, p.prefetch};
     p.fwd = fwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.fwd);
     if (p.family == kCta) p.smem = 256;
-    else if (p.family == kRagged) p.smem = 256 + N * 4;
+    else if (p.family == kRagged) p.smem = 256;
     else if (p.family != kStaged) p.smem = 0;
   }
   if (p.fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
@@ -391,9 +445,18 @@ rmsnorm_status_t size_grid(Plan* p, int64_t M, int device, unsigned** status = n
     return cuda_fail(e, "occupancy query");
   if (p->cta_per_sm_cap > 0 && per_sm > p->cta_per_sm_cap) per_sm = p->cta_per_sm_cap;
   const int64_t units = (M + p->rows_per_cta - 1) / p->rows_per_cta;
-  const int64_t cap = (int64_t)di.sms * per_sm;
+  int64_t cap = (int64_t)di.sms * per_sm;
+  if (p->min_rows > 0) {
+    const int64_t want = (units + p->min_rows - 1) / p->min_rows;
+    const int64_t floor_cap = di.sms < cap ? di.sms : cap;
+    cap = want < floor_cap ? floor_cap : (want < cap ? want : cap);
+  }
   p->grid = (int)(units < cap ? units : cap);
   if (p->grid < 1) p->grid = 1;
+  if (p->period > 1) {   // whole residue classes: a multiple of the period
+    p->grid = p->grid / p->period * p->period;
+    if (p->grid < p->period) p->grid = p->period;
+  }
   return RMSNORM_OK;
 }
 
@@ -409,9 +472,33 @@ const char* family_name(int f) {
 
 void describe(int op, const Plan& p, char* buf, size_t len) {
   static const char* ops[] = {"fwd", "fused_add", "bwd"};
-  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d%s/grid%d/smem%d", ops[op],
-           family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages,
+  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d", ops[op],
+           family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
            op == kBwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem);
+}
+
+// ---------------------------------------------------------------- launches
+
+// Every kernel is launched as a programmatic dependent of the previous work on
+// the stream (the kernels wait for it at entry, see pdl_begin), so the launch
+// of one call overlaps the end of the previous one.  RMSNORM_NO_PDL=1 turns
+// the attribute off (for A/B measurements).
+template <typename... Args>
+cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
+                   cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const char* off = getenv("RMSNORM_NO_PDL");
+  const bool pdl = !(off && *off && *off != '0');
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // ---------------------------------------------------------------- validation
@@ -433,11 +520,6 @@ rmsnorm_status_t check_sizes(int64_t M, int64_t N, float eps) {
 rmsnorm_status_t current_device(int* dev) {
   const cudaError_t e = cudaGetDevice(dev);
   return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e, "cudaGetDevice");
-}
-
-rmsnorm_status_t launched(const char* what) {
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e, what);
 }
 
 // ---------------------------------------------------------------- forward
@@ -489,8 +571,13 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   prm.stages = pl.stages;
   prm.wait_limit = wait_limit();
   prm.status = status;
-  pl.fwd<<<pl.grid, pl.threads, pl.smem, stream>>>(prm);
-  return launched("forward kernel launch");
+  prm.period = pl.period;
+  const cudaError_t e = launch(pl.fwd, pl.grid, pl.threads, pl.smem, stream, prm);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "forward kernel launch");
+  }
+  return RMSNORM_OK;
 }
 
 // ---------------------------------------------------------------- backward
@@ -565,6 +652,10 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   unsigned* status = nullptr;
   if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
   if (dgamma && pl.grid > prows) pl.grid = prows;
+  if (pl.period > 1) {   // ragged rows: whole residue classes only
+    pl.grid = pl.grid / pl.period * pl.period;
+    if (pl.grid < pl.period) return RMSNORM_ERR_WORKSPACE;
+  }
 
   BwdParams prm;
   prm.dy = dy;
@@ -582,23 +673,17 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   prm.stages = pl.stages;
   prm.wait_limit = wait_limit();
   prm.status = status;
-  pl.bwd<<<pl.grid, pl.threads, pl.smem, stream>>>(prm);
-  if ((st = launched("backward stage-1 launch")) != RMSNORM_OK || !dgamma) return st;
-
-  // stage 2, as a programmatic dependent launch of stage 1
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((ld / 4 + kRedCols - 1) / kRedCols));
-  cfg.blockDim = dim3(kRedCols * kRedRows);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  prm.period = pl.period;
+  cudaError_t e = launch(pl.bwd, pl.grid, pl.threads, pl.smem, stream, prm);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "backward stage-1 launch");
+  }
+  if (!dgamma) return RMSNORM_OK;
+  // stage 2: the P partial rows summed per column in a fixed order
   const float* part = static_cast<const float*>(workspace);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, get_dgamma_reduce_kernel(), part, pl.grid,
-                                           (int)N, ld, dgamma);
+  e = launch(get_dgamma_reduce_kernel(), (ld / 4 + kRedCols - 1) / kRedCols, kRedCols * kRedRows,
+             0, stream, part, pl.grid, (int)N, ld, dgamma);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "backward stage-2 launch");

@@ -14,8 +14,9 @@
 // reproducible: stage 1 runs a persistent grid of P CTAs with a fixed
 // row -> CTA map, each CTA accumulating its rows' dy*x*r per column in fp32
 // and writing one partial row; stage 2 sums the P partial rows per column in
-// a fixed order.  Stage 2 is launched with programmatic dependent launch so
-// its launch overlaps stage 1's tail; it waits on stage 1 before reading.
+// a fixed order.  Like every kernel here, stage 2 is a programmatic dependent
+// launch: its launch overlaps stage 1, and it waits for stage 1 to complete
+// before reading the partial rows.
 #include <type_traits>
 
 #include "rmsnorm_device.cuh"
@@ -45,17 +46,11 @@ __device__ __forceinline__ void load_gamma_vec(const void* gamma, int v, float (
   }
 }
 
-__device__ __forceinline__ void signal_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 template <int VPT>
 struct BSlice {
   uint4 x[VPT];
   uint4 dy[VPT];
   float r;        // saved rstd of the row
-  float xs, dys;  // ragged scalar
-  int h, nb, tl;  // ragged layout
 };
 
 template <typename TX, int VPT, bool HAS_RSTD>
@@ -78,49 +73,13 @@ __device__ __forceinline__ void bload_aligned(BSlice<VPT>& s, const BwdParams& p
   if (HAS_RSTD) s.r = valid ? __ldg(p.rstd + row) : 0.f;
 }
 
-template <typename TX, int VPT, bool HAS_RSTD>
-__device__ __forceinline__ void bload_ragged(BSlice<VPT>& s, const BwdParams& p, int64_t row,
-                                             int tid, int T) {
-  constexpr int E = Elem<TX>::kPerVec;
-  const int N = p.N;
-  const TX* xrow = static_cast<const TX*>(p.x) + row * (int64_t)N;
-  const TX* drow = static_cast<const TX*>(p.dy) + row * (int64_t)N;
-  const int mis = (int)(reinterpret_cast<uintptr_t>(xrow) & 15);
-  int h = mis ? (16 - mis) / (int)sizeof(TX) : 0;
-  if (h > N) h = N;
-  const int nb = (N - h) / E;
-  s.h = h;
-  s.nb = nb;
-  s.tl = N - h - nb * E;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = tid + k * T;
-    if (v < nb) {
-      s.x[k] = ld_stream(xrow + h + v * E);
-      s.dy[k] = ld_stream(drow + h + v * E);
-    } else {
-      s.x[k] = make_uint4(0, 0, 0, 0);
-      s.dy[k] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  s.xs = 0.f;
-  s.dys = 0.f;
-  int col = -1;
-  if (tid < h) col = tid;
-  else if (tid >= 8 && tid - 8 < s.tl) col = h + nb * E + (tid - 8);
-  if (col >= 0) {
-    s.xs = ld_scalar(xrow + col);
-    s.dys = ld_scalar(drow + col);
-  }
-  if (HAS_RSTD) s.r = __ldg(p.rstd + row);
-}
-
 // ---------------------------------------------------------------------------
 // kSubwarp: G lanes per row, 256 / G rows per CTA iteration; gamma and the
 // dgamma partials in registers; the row groups of a CTA are combined in
 // shared memory (in group order) at the end.
 template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF>
 __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdParams p) {
+  pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int RPC = kSubwarpThreads / G;
   extern __shared__ float4 smem4[];
@@ -191,7 +150,6 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
     if (PF) cur = nxt;
     else bload_aligned<TX, VPT, HAS_RSTD>(cur, p, nrow, nrow < p.M, lane, G);
   }
-  signal_dependents();
   if (!want_dg) return;
   const int ncol = p.nvec * E;
 #pragma unroll
@@ -215,56 +173,39 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
 }
 
 // ---------------------------------------------------------------------------
-// kCta / kRagged: one row per CTA iteration.  dgamma partials live in
-// registers (ACC_SMEM false, aligned rows) or in shared memory (ACC_SMEM, and
-// always for ragged rows, whose columns shift with each row's alignment).  A
-// column is updated by one thread per row and rows are separated by the
-// reduction barrier, so the shared-memory accumulation is race free and adds
-// rows in order.
-template <typename TX, typename TW, int VPT, bool RAGGED, bool HAS_RSTD, bool ACC_SMEM, bool PF>
+// kCta: one row per CTA iteration.  dgamma partials live in registers
+// (ACC_SMEM false) or in shared memory (ACC_SMEM, for wide rows).  A column is
+// updated by one thread per row and rows are separated by the reduction
+// barrier, so the shared-memory accumulation is race free and adds rows in
+// order.
+template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool ACC_SMEM, bool PF>
 __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cta_kernel(const BwdParams p) {
+  pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
-  constexpr bool SMEM_ACC = ACC_SMEM || RAGGED;
   constexpr int K = HAS_RSTD ? 1 : 2;
   extern __shared__ float4 smem4[];
   float* red = reinterpret_cast<float*>(smem4);                // 2 * K * 32
-  float* sg = red + 128;                                       // ragged: gamma fp32 [ld]
-  float* sacc = sg + (RAGGED ? p.ld_partial : 0);              // [ld]
+  float* sacc = red + 128;                                     // [ld]
   const int tid = threadIdx.x, T = blockDim.x;
-  const int N = p.N;
   const bool want_dg = p.partial != nullptr;
 
-  if constexpr (RAGGED) {
-    const TW* gp = static_cast<const TW*>(p.gamma);
-    for (int j = tid; j < N; j += T) sg[j] = ld_scalar(gp + j);
-  }
-  if constexpr (SMEM_ACC) {
+  if constexpr (ACC_SMEM) {
     for (int j = tid; j < p.ld_partial; j += T) sacc[j] = 0.f;
+    __syncthreads();
   }
-  if constexpr (RAGGED || SMEM_ACC) __syncthreads();
-
-  float acc[SMEM_ACC ? 1 : VPT][E];
+  float acc[ACC_SMEM ? 1 : VPT][E];
 #pragma unroll
-  for (int k = 0; k < (SMEM_ACC ? 1 : VPT); ++k)
+  for (int k = 0; k < (ACC_SMEM ? 1 : VPT); ++k)
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
 
   int parity = 0;
   BSlice<VPT> cur, nxt;
   int64_t row = blockIdx.x;
-  if (row < p.M) {
-    if constexpr (RAGGED) bload_ragged<TX, VPT, HAS_RSTD>(cur, p, row, tid, T);
-    else bload_aligned<TX, VPT, HAS_RSTD>(cur, p, row, true, tid, T);
-  }
+  if (row < p.M) bload_aligned<TX, VPT, HAS_RSTD>(cur, p, row, true, tid, T);
   for (; row < p.M; row += gridDim.x) {
     const int64_t nrow = row + gridDim.x;
-    if (PF && nrow < p.M) {
-      if constexpr (RAGGED) bload_ragged<TX, VPT, HAS_RSTD>(nxt, p, nrow, tid, T);
-      else bload_aligned<TX, VPT, HAS_RSTD>(nxt, p, nrow, true, tid, T);
-    }
-    const int h = RAGGED ? cur.h : 0;
-    const int nv = RAGGED ? cur.nb : p.nvec;
-
+    if (PF && nrow < p.M) bload_aligned<TX, VPT, HAS_RSTD>(nxt, p, nrow, true, tid, T);
     float sums[K];
 #pragma unroll
     for (int q = 0; q < K; ++q) sums[q] = 0.f;
@@ -274,54 +215,35 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cta_kernel(const BwdParams
       float xf[E], df[E], g[E];
       unpack(cur.x[k], xf);
       unpack(cur.dy[k], df);
-      if constexpr (RAGGED) {
+      if (v < p.nvec) load_gamma_vec<TW, E>(p.gamma, v, g);
+      else
 #pragma unroll
-        for (int e = 0; e < E; ++e) g[e] = v < nv ? sg[h + v * E + e] : 0.f;
-      } else {
-        if (v < nv) load_gamma_vec<TW, E>(p.gamma, v, g);
-        else
-#pragma unroll
-          for (int e = 0; e < E; ++e) g[e] = 0.f;
-      }
+        for (int e = 0; e < E; ++e) g[e] = 0.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         sums[0] = fmaf(g[e] * df[e], xf[e], sums[0]);
         if (!HAS_RSTD) sums[K - 1] = fmaf(xf[e], xf[e], sums[K - 1]);
       }
     }
-    int scol = -1;
-    float sg_s = 0.f;
-    if constexpr (RAGGED) {
-      scol = (tid < cur.h) ? tid
-             : (tid >= 8 && tid - 8 < cur.tl) ? cur.h + cur.nb * E + (tid - 8) : -1;
-      if (scol >= 0) sg_s = sg[scol];
-      sums[0] = fmaf(sg_s * cur.dys, cur.xs, sums[0]);
-      if (!HAS_RSTD) sums[K - 1] = fmaf(cur.xs, cur.xs, sums[K - 1]);
-    }
     cta_sum<K>(sums, red, parity);
     parity ^= 1;
     const float r = HAS_RSTD ? cur.r : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
     const float c = r * r * p.inv_n * sums[0];
 
-    TX* dxrow = static_cast<TX*>(p.dx) + row * (int64_t)N;
+    char* dxrow = static_cast<char*>(p.dx) + row * (size_t)p.N * sizeof(TX);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
-      if (v < nv) {
+      if (v < p.nvec) {
         float xf[E], df[E], g[E], o[E];
         unpack(cur.x[k], xf);
         unpack(cur.dy[k], df);
-        if constexpr (RAGGED) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) g[e] = sg[h + v * E + e];
-        } else {
-          load_gamma_vec<TW, E>(p.gamma, v, g);
-        }
+        load_gamma_vec<TW, E>(p.gamma, v, g);
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] = r * fmaf(-xf[e], c, g[e] * df[e]);
-        st_stream(dxrow + h + v * E, pack(o));
-        if constexpr (SMEM_ACC) {
-          float* a = sacc + h + v * E;
+        st_stream(dxrow + (size_t)v * 16, pack(o));
+        if constexpr (ACC_SMEM) {
+          float* a = sacc + v * E;
 #pragma unroll
           for (int e = 0; e < E; ++e) a[e] = fmaf(df[e] * xf[e], r, a[e]);
         } else {
@@ -330,25 +252,14 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cta_kernel(const BwdParams
         }
       }
     }
-    if constexpr (RAGGED) {
-      if (scol >= 0) {
-        st_scalar(dxrow + scol, r * fmaf(-cur.xs, c, sg_s * cur.dys));
-        sacc[scol] = fmaf(cur.dys * cur.xs, r, sacc[scol]);
-      }
-    }
-    if (PF) {
-      cur = nxt;
-    } else if (nrow < p.M) {
-      if constexpr (RAGGED) bload_ragged<TX, VPT, HAS_RSTD>(cur, p, nrow, tid, T);
-      else bload_aligned<TX, VPT, HAS_RSTD>(cur, p, nrow, true, tid, T);
-    }
+    if (PF) cur = nxt;
+    else if (nrow < p.M) bload_aligned<TX, VPT, HAS_RSTD>(cur, p, nrow, true, tid, T);
   }
-  signal_dependents();
   if (!want_dg) return;
   float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
-  if constexpr (SMEM_ACC) {
+  if constexpr (ACC_SMEM) {
     __syncthreads();
-    for (int j = tid; j < N; j += T) prow[j] = sacc[j];
+    for (int j = tid; j < p.N; j += T) prow[j] = sacc[j];
   } else {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -370,6 +281,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cta_kernel(const BwdParams
 // memory, each column always by the same thread.
 template <typename TX, typename TW, bool HAS_RSTD>
 __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
+  pdl_begin();
   constexpr int K = HAS_RSTD ? 1 : 2;
   __shared__ float red[2 * 2 * 32];
   const int tid = threadIdx.x, T = blockDim.x;
@@ -401,7 +313,6 @@ __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
       if (prow) prow[j] = fmaf(dv * xv, r, prow[j]);
     }
   }
-  signal_dependents();
 }
 
 template <typename TX, typename TW, bool HAS_RSTD>
@@ -416,16 +327,16 @@ BwdKernel pick_subwarp(int g, int vpt, bool pf) {
   return nullptr;
 }
 
-template <typename TX, typename TW, bool RAGGED, bool HAS_RSTD, bool ACC_SMEM>
+template <typename TX, typename TW, bool HAS_RSTD, bool ACC_SMEM>
 BwdKernel pick_cta(int vpt, bool pf) {
   switch (vpt) {
-    case 1: return pf ? bwd_cta_kernel<TX, TW, 1, RAGGED, HAS_RSTD, ACC_SMEM, true>
-                      : bwd_cta_kernel<TX, TW, 1, RAGGED, HAS_RSTD, ACC_SMEM, false>;
-    case 2: return pf ? bwd_cta_kernel<TX, TW, 2, RAGGED, HAS_RSTD, ACC_SMEM, true>
-                      : bwd_cta_kernel<TX, TW, 2, RAGGED, HAS_RSTD, ACC_SMEM, false>;
-    case 4: return pf ? bwd_cta_kernel<TX, TW, 4, RAGGED, HAS_RSTD, ACC_SMEM, true>
-                      : bwd_cta_kernel<TX, TW, 4, RAGGED, HAS_RSTD, ACC_SMEM, false>;
-    case 8: return pf ? nullptr : bwd_cta_kernel<TX, TW, 8, RAGGED, HAS_RSTD, ACC_SMEM, false>;
+    case 1: return pf ? bwd_cta_kernel<TX, TW, 1, HAS_RSTD, ACC_SMEM, true>
+                      : bwd_cta_kernel<TX, TW, 1, HAS_RSTD, ACC_SMEM, false>;
+    case 2: return pf ? bwd_cta_kernel<TX, TW, 2, HAS_RSTD, ACC_SMEM, true>
+                      : bwd_cta_kernel<TX, TW, 2, HAS_RSTD, ACC_SMEM, false>;
+    case 4: return pf ? bwd_cta_kernel<TX, TW, 4, HAS_RSTD, ACC_SMEM, true>
+                      : bwd_cta_kernel<TX, TW, 4, HAS_RSTD, ACC_SMEM, false>;
+    case 8: return pf ? nullptr : bwd_cta_kernel<TX, TW, 8, HAS_RSTD, ACC_SMEM, false>;
     default: return nullptr;
   }
 }
@@ -435,9 +346,8 @@ BwdKernel pick_family(const BwdKey& k) {
   switch (k.family) {
     case kSubwarp: return pick_subwarp<TX, TW, HAS_RSTD>(k.g, k.vpt, k.prefetch);
     case kCta:
-      return k.acc_smem ? pick_cta<TX, TW, false, HAS_RSTD, true>(k.vpt, k.prefetch)
-                        : pick_cta<TX, TW, false, HAS_RSTD, false>(k.vpt, k.prefetch);
-    case kRagged: return pick_cta<TX, TW, true, HAS_RSTD, true>(k.vpt, k.prefetch);
+      return k.acc_smem ? pick_cta<TX, TW, HAS_RSTD, true>(k.vpt, k.prefetch)
+                        : pick_cta<TX, TW, HAS_RSTD, false>(k.vpt, k.prefetch);
     case kGeneric: return bwd_generic_kernel<TX, TW, HAS_RSTD>;
     default: return nullptr;
   }
@@ -457,7 +367,7 @@ BwdKernel pick_rstd(const BwdKey& k) {
 // returns once stage 1 has completed and its writes are visible.
 __global__ void __launch_bounds__(kRedCols* kRedRows)
     dgamma_reduce_kernel(const float* partial, int P, int N, int ld, float* dgamma) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_begin();
   __shared__ float4 sh[kRedRows][kRedCols];
   const int tx = threadIdx.x % kRedCols, ty = threadIdx.x / kRedCols;
   const int q = blockIdx.x * kRedCols + tx;       // float4 column group

@@ -104,8 +104,26 @@ template <typename T>
 __device__ __forceinline__ float ld_scalar(const T* p) {
   return Elem<T>::to_f32(*p);
 }
+// Scalar read of small read-only data (gamma), cached in L1.
+template <typename T>
+__device__ __forceinline__ float ld_scalar_ro(const T* p) {
+  return Elem<T>::to_f32(__ldg(p));
+}
 __device__ __forceinline__ void st_scalar(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st_scalar(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------- launch order
+
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel on the stream is finishing.
+// Its first act is to wait until that kernel has completed and its writes are
+// visible (no global memory is touched before), and then to allow the next
+// kernel to launch the same way.  Without the launch attribute both
+// instructions do nothing.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- reductions
 

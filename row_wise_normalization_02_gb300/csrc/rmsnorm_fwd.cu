@@ -47,14 +47,11 @@ __device__ __forceinline__ void unpack_gamma(const uint4 (&gw)[GW], float (&gf)[
   }
 }
 
-// Registers of one row slice: VPT vectors of x (and of the residual), plus
-// one scalar element for ragged rows.
+// Registers of one row slice: VPT vectors of x (and of the residual).
 template <int VPT, bool FUSED>
 struct Slice {
   uint4 x[VPT];
   uint4 r[FUSED ? VPT : 1];
-  float xs, rs;   // ragged scalar (head or tail element)
-  int h, nb, tl;  // ragged layout: head scalars, body vectors, tail scalars
 };
 
 template <typename TX, int VPT, bool FUSED>
@@ -74,49 +71,6 @@ __device__ __forceinline__ void load_aligned(Slice<VPT, FUSED>& s, const FwdPara
       if (FUSED) s.r[k] = make_uint4(0, 0, 0, 0);
     }
   }
-}
-
-template <typename TX, int VPT, bool FUSED>
-__device__ __forceinline__ void load_ragged(Slice<VPT, FUSED>& s, const FwdParams& p,
-                                            int64_t row, int tid, int T) {
-  constexpr int E = Elem<TX>::kPerVec;
-  const int N = p.N;
-  const TX* xrow = static_cast<const TX*>(p.x) + row * (int64_t)N;
-  const TX* rrow = static_cast<const TX*>(p.residual) + row * (int64_t)N;
-  const int mis = (int)(reinterpret_cast<uintptr_t>(xrow) & 15);
-  int h = mis ? (16 - mis) / (int)sizeof(TX) : 0;
-  if (h > N) h = N;
-  const int nb = (N - h) / E;
-  s.h = h;
-  s.nb = nb;
-  s.tl = N - h - nb * E;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = tid + k * T;
-    if (v < nb) {
-      s.x[k] = ld_stream(xrow + h + v * E);
-      if (FUSED) s.r[k] = ld_rw(rrow + h + v * E);
-    } else {
-      s.x[k] = make_uint4(0, 0, 0, 0);
-      if (FUSED) s.r[k] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  s.xs = 0.f;
-  s.rs = 0.f;
-  int col = -1;
-  if (tid < h) col = tid;
-  else if (tid >= 8 && tid - 8 < s.tl) col = h + nb * E + (tid - 8);
-  if (col >= 0) {
-    s.xs = ld_scalar(xrow + col);
-    if (FUSED) s.rs = ld_scalar(rrow + col);
-  }
-}
-
-// Column of the ragged scalar held by thread tid, or -1.
-__device__ __forceinline__ int ragged_scalar_col(int tid, int h, int nb, int tl, int E) {
-  if (tid < h) return tid;
-  if (tid >= 8 && tid - 8 < tl) return h + nb * E + (tid - 8);
-  return -1;
 }
 
 // Sum of squares of this thread's part of the row.  Fused add: the vectors
@@ -152,6 +106,7 @@ __device__ __forceinline__ float slice_sumsq(Slice<VPT, FUSED>& s, char* res_row
 template <typename TX, typename TW, int G, int VPT, bool FUSED, bool PF>
 __global__ void __launch_bounds__(kSubwarpThreads)
     fwd_subwarp_kernel(const FwdParams p) {
+  pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW;
   constexpr int RPC = kSubwarpThreads / G;
@@ -203,96 +158,58 @@ __global__ void __launch_bounds__(kSubwarpThreads)
 }
 
 // ---------------------------------------------------------------------------
-// kCta / kRagged: one row per CTA iteration, blockDim.x threads, persistent.
-template <typename TX, typename TW, int VPT, bool FUSED, bool RAGGED, bool PF>
+// kCta: one row per CTA iteration, blockDim.x threads, persistent; gamma
+// vectors in registers for the whole kernel.
+template <typename TX, typename TW, int VPT, bool FUSED, bool PF>
 __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cta_kernel(const FwdParams p) {
+  pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW;
   extern __shared__ float4 smem4[];
   float* red = reinterpret_cast<float*>(smem4);    // 2 x 32 warp partials
-  float* sg = red + 64;                            // ragged: gamma as fp32
   const int tid = threadIdx.x, T = blockDim.x;
-  const int N = p.N;
 
-  uint4 gw[RAGGED ? 1 : VPT][GW];
-  if constexpr (RAGGED) {
-    const TW* g = static_cast<const TW*>(p.gamma);
-    for (int j = tid; j < N; j += T) sg[j] = ld_scalar(g + j);
-    __syncthreads();
-  } else {
+  uint4 gw[VPT][GW];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = tid + k * T;
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
 #pragma unroll
-      for (int w = 0; w < GW; ++w)
-        gw[k][w] = v < p.nvec ? ld_cached(static_cast<const char*>(p.gamma) +
-                                          ((size_t)v * GW + w) * 16)
-                              : make_uint4(0, 0, 0, 0);
-    }
+    for (int w = 0; w < GW; ++w)
+      gw[k][w] = v < p.nvec ? ld_cached(static_cast<const char*>(p.gamma) +
+                                        ((size_t)v * GW + w) * 16)
+                            : make_uint4(0, 0, 0, 0);
   }
 
   int parity = 0;
   Slice<VPT, FUSED> cur, nxt;
   int64_t row = blockIdx.x;
-  if (row < p.M) {
-    if constexpr (RAGGED) load_ragged<TX, VPT, FUSED>(cur, p, row, tid, T);
-    else load_aligned<TX, VPT, FUSED>(cur, p, row, true, tid, T);
-  }
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  if (row < p.M) load_aligned<TX, VPT, FUSED>(cur, p, row, true, tid, T);
   for (; row < p.M; row += gridDim.x) {
     const int64_t nrow = row + gridDim.x;
-    if (PF && nrow < p.M) {
-      if constexpr (RAGGED) load_ragged<TX, VPT, FUSED>(nxt, p, nrow, tid, T);
-      else load_aligned<TX, VPT, FUSED>(nxt, p, nrow, true, tid, T);
-    }
-    TX* yrow = static_cast<TX*>(p.y) + row * (int64_t)N;
-    TX* hrow = static_cast<TX*>(p.residual) + row * (int64_t)N;
-    const int h = RAGGED ? cur.h : 0;
-    const int nv = RAGGED ? cur.nb : p.nvec;
-
+    if (PF && nrow < p.M) load_aligned<TX, VPT, FUSED>(nxt, p, nrow, true, tid, T);
+    char* yrow = static_cast<char*>(p.y) + row * rb;
+    char* hrow = static_cast<char*>(p.residual) + row * rb;
     float ss[1];
-    ss[0] = slice_sumsq<TX, VPT, FUSED>(cur, reinterpret_cast<char*>(hrow + h), tid, T, nv, true);
-    int scol = -1;
-    float sv = 0.f;
-    if constexpr (RAGGED) {
-      scol = ragged_scalar_col(tid, cur.h, cur.nb, cur.tl, E);
-      sv = cur.xs;
-      if (FUSED) {
-        sv = round_to(cur.rs + cur.xs, (TX*)nullptr);
-        if (scol >= 0) st_scalar(hrow + scol, sv);
-      }
-      ss[0] = fmaf(sv, sv, ss[0]);
-    }
+    ss[0] = slice_sumsq<TX, VPT, FUSED>(cur, hrow, tid, T, p.nvec, true);
     cta_sum<1>(ss, red, parity);
     parity ^= 1;
     const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
     if (tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
-
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
-      if (v < nv) {
+      if (v < p.nvec) {
         float g[E], o[E];
-        if constexpr (RAGGED) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) g[e] = sg[h + v * E + e];
-        } else {
-          unpack_gamma<TW, E, GW>(gw[k], g);
-        }
+        unpack_gamma<TW, E, GW>(gw[k], g);
         unpack(cur.x[k], o);
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
-        st_stream(yrow + h + v * E, pack(o));
+        st_stream(yrow + (size_t)v * 16, pack(o));
       }
     }
-    if constexpr (RAGGED) {
-      if (scol >= 0) st_scalar(yrow + scol, sv * rs * sg[scol]);
-    }
-    if (PF) {
-      cur = nxt;
-    } else if (nrow < p.M) {
-      if constexpr (RAGGED) load_ragged<TX, VPT, FUSED>(cur, p, nrow, tid, T);
-      else load_aligned<TX, VPT, FUSED>(cur, p, nrow, true, tid, T);
-    }
+    if (PF) cur = nxt;
+    else if (nrow < p.M) load_aligned<TX, VPT, FUSED>(cur, p, nrow, true, tid, T);
   }
 }
 
@@ -301,6 +218,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cta_kernel(const FwdParams
 // (fused: forms, rounds and stores h) and reduces; pass 2 re-reads it.
 template <typename TX, typename TW, bool FUSED>
 __global__ void __launch_bounds__(256) fwd_generic_kernel(const FwdParams p) {
+  pdl_begin();
   __shared__ float red[64];
   const int tid = threadIdx.x, T = blockDim.x;
   const int N = p.N;
@@ -343,16 +261,13 @@ FwdKernel pick_subwarp(int g, int vpt) {
   return nullptr;
 }
 
-template <typename TX, typename TW, bool FUSED, bool RAGGED>
+template <typename TX, typename TW, bool FUSED>
 FwdKernel pick_cta(int vpt, bool pf) {
   switch (vpt) {
-    case 1: return pf ? fwd_cta_kernel<TX, TW, 1, FUSED, RAGGED, true>
-                      : fwd_cta_kernel<TX, TW, 1, FUSED, RAGGED, false>;
-    case 2: return pf ? fwd_cta_kernel<TX, TW, 2, FUSED, RAGGED, true>
-                      : fwd_cta_kernel<TX, TW, 2, FUSED, RAGGED, false>;
-    case 4: return pf ? fwd_cta_kernel<TX, TW, 4, FUSED, RAGGED, true>
-                      : fwd_cta_kernel<TX, TW, 4, FUSED, RAGGED, false>;
-    case 8: return pf ? nullptr : fwd_cta_kernel<TX, TW, 8, FUSED, RAGGED, false>;
+    case 1: return pf ? fwd_cta_kernel<TX, TW, 1, FUSED, true> : fwd_cta_kernel<TX, TW, 1, FUSED, false>;
+    case 2: return pf ? fwd_cta_kernel<TX, TW, 2, FUSED, true> : fwd_cta_kernel<TX, TW, 2, FUSED, false>;
+    case 4: return pf ? fwd_cta_kernel<TX, TW, 4, FUSED, true> : fwd_cta_kernel<TX, TW, 4, FUSED, false>;
+    case 8: return pf ? nullptr : fwd_cta_kernel<TX, TW, 8, FUSED, false>;
     default: return nullptr;
   }
 }
@@ -363,8 +278,7 @@ FwdKernel pick_family(const FwdKey& k) {
     case kSubwarp:
       return k.prefetch ? pick_subwarp<TX, TW, FUSED, true>(k.g, k.vpt)
                         : pick_subwarp<TX, TW, FUSED, false>(k.g, k.vpt);
-    case kCta: return pick_cta<TX, TW, FUSED, false>(k.vpt, k.prefetch);
-    case kRagged: return pick_cta<TX, TW, FUSED, true>(k.vpt, k.prefetch);
+    case kCta: return pick_cta<TX, TW, FUSED>(k.vpt, k.prefetch);
     case kGeneric: return fwd_generic_kernel<TX, TW, FUSED>;
     default: return nullptr;
   }

@@ -16,8 +16,9 @@ enum DT : int { kF32 = 0, kBF16 = 1 };
 //             reduction by shuffles + shared memory; rows 16-byte aligned.
 //  kRagged  : as kCta, for rows that are not 16-byte aligned (N * size % 16
 //             != 0, or unaligned bases that agree modulo 16): per-row scalar
-//             head and tail around an aligned vector body; gamma staged in
-//             shared memory as fp32.
+//             head and tail around an aligned vector body; each CTA walks
+//             rows of one start-alignment class, so gamma and the dgamma
+//             partials stay in registers.
 //  kGeneric : any N, any element-aligned pointers; scalar two-pass loop.
 //  kStaged  : as kCta, but rows arrive by bulk copies (the 1-D form of TMA)
 //             into a ring of `stages` shared-memory row buffers, so several
@@ -45,6 +46,7 @@ struct FwdParams {
   int stages;         // kStaged: row buffers in the shared-memory ring
   long long wait_limit;   // kStaged: clock cycles before a wait gives up
   unsigned* status;   // device status word (kStatus* bits)
+  int period;         // kRagged: rows i and i + period start at the same address mod 16
 };
 
 struct BwdParams {
@@ -63,6 +65,7 @@ struct BwdParams {
   int stages;
   long long wait_limit;
   unsigned* status;
+  int period;
 };
 
 using FwdKernel = void (*)(FwdParams);
@@ -102,6 +105,12 @@ FwdKernel get_fwd_staged_bf16_f32(const FwdKey& k);
 BwdKernel get_bwd_staged_f32_f32(const BwdKey& k);
 BwdKernel get_bwd_staged_bf16_bf16(const BwdKey& k);
 BwdKernel get_bwd_staged_bf16_f32(const BwdKey& k);
+FwdKernel get_fwd_ragged_f32_f32(const FwdKey& k);
+FwdKernel get_fwd_ragged_bf16_bf16(const FwdKey& k);
+FwdKernel get_fwd_ragged_bf16_f32(const FwdKey& k);
+BwdKernel get_bwd_ragged_f32_f32(const BwdKey& k);
+BwdKernel get_bwd_ragged_bf16_bf16(const BwdKey& k);
+BwdKernel get_bwd_ragged_bf16_f32(const BwdKey& k);
 ReduceKernel get_dgamma_reduce_kernel();
 
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.

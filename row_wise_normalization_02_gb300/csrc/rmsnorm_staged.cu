@@ -106,6 +106,7 @@ __device__ __forceinline__ void gamma_f32(const void* gamma, int v, float (&g)[E
 // Forward / fused add.  Stage layout: fused [r | x], forward [x].
 template <typename TX, typename TW, int VPT, bool FUSED>
 __global__ void __launch_bounds__(kCtaMaxThreads) fwd_staged_kernel(const FwdParams p) {
+  pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int NS = FUSED ? 2 : 1;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_staged_kernel(const FwdPar
 // registers, written as one partial row at the end.
 template <typename TX, typename TW, int VPT, bool HAS_RSTD>
 __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdParams p) {
+  pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int K = HAS_RSTD ? 1 : 2;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -282,7 +284,6 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
       }
     }
   }
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (failed) {
     if (tid == 0) {
       drain(rg, i, issued, S);

@@ -112,4 +112,6 @@ def test_workspace_size_matches_plan_on_gpu(lib):
     for M, N in [(16384, 8192), (262144, 128), (4096, 2049), (1, 1), (3, 40000)]:
         b = rn.rmsnorm_bwd_workspace_size(M, N, "bf16", "f32")
         assert b > 0 and b % 16 == 0
-        assert b <= min(M, 152 * 32) * ((N + 3) // 4 * 4) * 4 * 2
+        # at most one partial row per resident CTA, at least one per residue
+        # class of ragged rows (16 classes at most)
+        assert b <= max(min(M, 152 * 32), 16) * ((N + 3) // 4 * 4) * 4 * 2

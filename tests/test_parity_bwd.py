@@ -107,6 +107,8 @@ def test_bwd_without_dgamma(N):
     ("cta:vpt=4:pf=0:acc=0:cps=1", 8192), ("cta:vpt=8:pf=0:acc=1:cps=1", 16384),
     ("cta:vpt=1:pf=1:acc=0:cps=1", 2048),
     ("ragged:vpt=2:pf=1:cps=1", 2049), ("ragged:vpt=1:pf=0:cps=1", 2049),
+    ("ragged:vpt=4:pf=0:cps=1", 2049), ("ragged:vpt=2:pf=1:mr=0", 1025),
+    ("ragged:vpt=1:pf=1:cps=2", 4095),
     ("generic:cps=1", 8192), ("generic:cps=1", 2049),
     ("staged:vpt=4:st=3:cps=1", 8192), ("staged:vpt=4:st=2:cps=1", 8192),
     ("staged:vpt=2:st=4:cps=1", 4096), ("staged:vpt=1:st=2:cps=1", 2048),

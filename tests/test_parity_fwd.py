@@ -97,7 +97,7 @@ def test_fused_add_matches_oracle(xd, wd, M, N):
     ("cta:vpt=2:pf=1:cps=1", 4096), ("cta:vpt=8:pf=0:cps=1", 8192),
     ("cta:vpt=1:pf=1:cps=1", 2048), ("cta:vpt=4:pf=1:t=512:cps=1", 5120),
     ("ragged:vpt=2:pf=1:cps=1", 2049), ("ragged:vpt=1:pf=0:cps=1", 2049),
-    ("ragged:vpt=4:pf=1:cps=1", 4096), ("generic:cps=1", 8192), ("generic:cps=1", 2049),
+    ("ragged:vpt=4:pf=0:cps=1", 4096), ("ragged:vpt=2:pf=1:cps=2", 1025), ("generic:cps=1", 8192), ("generic:cps=1", 2049),
     ("staged:vpt=4:st=3:cps=1", 8192), ("staged:vpt=4:st=2:cps=1", 8192),
     ("staged:vpt=2:st=5:cps=1", 4096), ("staged:vpt=8:st=2:cps=1", 16384),
     ("staged:vpt=1:st=8:cps=1", 2048), ("staged:vpt=4:t=512:st=2:cps=1", 5120),
