@@ -198,6 +198,10 @@ def run_ours(args, rank, world):
             def launch(d=d, wl=wl, M=M, N=N, eps=eps):
                 rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"], d["rstd"], M, N, eps, wl.x_dtype,
                                wl.w_dtype, stream)
+
+            def launch_rows(r0, m, d=d, wl=wl, N=N, eps=eps):
+                rn.rmsnorm_fwd(d["x"][r0:r0 + m], d["gamma"], d["y"][r0:r0 + m],
+                               d["rstd"][r0:r0 + m], m, N, eps, wl.x_dtype, wl.w_dtype, stream)
             outs = ("y", "rstd")
             ins = ("x", "gamma")
         elif wl.op == "fused_add":
@@ -206,6 +210,11 @@ def run_ours(args, rank, world):
             def launch(d=d, wl=wl, M=M, N=N, eps=eps):
                 rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], d["y"], None, M, N,
                                          eps, wl.x_dtype, wl.w_dtype, stream)
+
+            def launch_rows(r0, m, d=d, wl=wl, N=N, eps=eps):
+                rn.rmsnorm_fused_add_fwd(d["x"][r0:r0 + m], d["residual"][r0:r0 + m], d["gamma"],
+                                         d["y"][r0:r0 + m], None, m, N, eps, wl.x_dtype,
+                                         wl.w_dtype, stream)
             outs = ("residual", "y")
             ins = ("x", "residual", "gamma")
         else:
@@ -225,12 +234,14 @@ def run_ours(args, rank, world):
             def launch(d=d, wl=wl, M=M, N=N, eps=eps, ws=ws):
                 rn.rmsnorm_bwd(d["dy"], d["x"], d["rstd"], d["gamma"], d["dx"], d["dgamma"],
                                d["ws"], ws, M, N, eps, wl.x_dtype, wl.w_dtype, stream)
+            def launch_rows(r0, m, launch=launch):
+                launch()
             outs = ("dx", "dgamma")
             ins = ("x", "dy", "rstd", "gamma")
         plan = rn.rmsnorm_describe_plan({"fwd": 0, "fused_add": 1, "bwd": 2}[wl.op], M, N,
                                         wl.x_dtype, wl.w_dtype)
-        ops.append(dict(wl=wl, d=d, launch=launch, outs=outs, ins=ins, plan=plan,
-                        bytes=alg_bytes(wl)))
+        ops.append(dict(wl=wl, d=d, launch=launch, launch_rows=launch_rows, outs=outs, ins=ins,
+                        plan=plan, bytes=alg_bytes(wl)))
         host.append(inp)
     torch.cuda.synchronize()
 
@@ -306,7 +317,11 @@ def run_ours(args, rank, world):
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src ==
                 "measured" else "fallback 6800 GB/s"}
 
-    # ---- end to end through the C ABI with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers: every step
+    # copies each op's inputs in and its outputs out.  Three streams overlap
+    # host->device copies, kernels and device->host copies; the forward and the
+    # fused add (row-independent) go in row chunks so a chunk computes while
+    # the next one arrives.  The backward is one call (dgamma sums all rows).
     Ke = max(3, min(K, args.e2e_steps))
     pin = []
     h2d = d2h = 0
@@ -319,23 +334,64 @@ def run_ours(args, rank, world):
         h2d += sum(t.numel() * t.element_size() for t in hin.values())
         d2h += sum(t.numel() * t.element_size() for t in hout.values())
         pin.append((hin, hout))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    chunks = max(1, args.e2e_chunks)
+
+    def row_chunks(wl):
+        if wl.op == "bwd":
+            return [(0, wl.M)]
+        step_rows = -(-wl.M // chunks)
+        return [(r, min(step_rows, wl.M - r)) for r in range(0, wl.M, step_rows)]
+
+    def copy_rows(dst, src, key, r0, m, wl):
+        if key in ("gamma",) or (key == "rstd" and wl.op == "bwd"):
+            if r0 == 0:
+                dst.copy_(src, non_blocking=True)
+        elif key == "rstd":
+            dst[r0:r0 + m].copy_(src[r0:r0 + m], non_blocking=True)
+        else:
+            dst[r0:r0 + m].copy_(src[r0:r0 + m], non_blocking=True)
+
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(Ke):
-            for op, (hin, hout) in zip(ops, pin):
-                for k, t in hin.items():
-                    op["d"][k].copy_(t, non_blocking=True)
-                op["launch"]()
-                for k, t in hout.items():
-                    t.copy_(op["d"][k], non_blocking=True)
-        e1.record(stream)
-    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    done = [None] * len(ops)       # last device->host copy of each op's previous step
+    e0.record(s_in)
+    for _ in range(Ke):
+        for j, (op, (hin, hout)) in enumerate(zip(ops, pin)):
+            wl = op["wl"]
+            if done[j] is not None:
+                s_in.wait_event(done[j])     # its buffers are free again
+            for r0, m in row_chunks(wl):
+                with torch.cuda.stream(s_in):
+                    for k, t in hin.items():
+                        copy_rows(op["d"][k], t, k, r0, m, wl)
+                    arrived = torch.cuda.Event()
+                    arrived.record(s_in)
+                stream.wait_event(arrived)
+                with torch.cuda.stream(stream):
+                    op["launch_rows"](r0, m)
+                    computed = torch.cuda.Event()
+                    computed.record(stream)
+                s_out.wait_event(computed)
+                with torch.cuda.stream(s_out):
+                    for k, t in hout.items():
+                        if k == "dgamma":
+                            t.copy_(op["d"][k], non_blocking=True)
+                        else:
+                            t[r0:r0 + m].copy_(op["d"][k][r0:r0 + m], non_blocking=True)
+                    out_done = torch.cuda.Event()
+                    out_done.record(s_out)
+            done[j] = out_done
+    for ev_done in done:
+        s_in.wait_event(ev_done)
+    e1.record(s_in)
+    torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, world, dev)
     e2e = {"value": round(job_gbs(step_bytes, e2e_ms, world), 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
-           "ms_per_step": round(e2e_ms, 3), "pinned": True}
+           "ms_per_step": round(e2e_ms, 3), "pinned": True,
+           "pipeline": f"3 streams (copy in / kernels / copy out), fwd and fused add in "
+                       f"{chunks} row chunks"}
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 4),
@@ -556,6 +612,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--workloads", default="")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--rounds", type=int, default=5, help="--sweep: timed rounds per workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
