@@ -49,6 +49,9 @@ def _load():
             lib.oracle_rmsnorm_bwd.argtypes = [_P, _P, _P, _P, I64, I64, D, I, I,
                                                _P, _P, _P, _P, _P, _P, _P]
             lib.oracle_rmsnorm_bwd.restype = I
+            lib.oracle_rmsnorm_fused_add_bwd.argtypes = [_P, _P, _P, _P, _P, I64, I64, D, I, I,
+                                                         _P, _P, _P, _P, _P]
+            lib.oracle_rmsnorm_fused_add_bwd.restype = I
             lib.oracle_round_bf16.argtypes = [D]
             lib.oracle_round_bf16.restype = ctypes.c_uint16
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -169,4 +172,33 @@ def bwd(dy, x, rstd, gamma, eps, x_dtype="bf16", w_dtype=None, want64=True):
         raise ValueError("oracle_rmsnorm_bwd rejected its arguments")
     out = {"dx": dx, "dgamma": dgamma}
     out.update(extra)
+    return out
+
+
+def fused_add_bwd(dy, h, rstd, gamma, dres, eps, x_dtype="bf16", w_dtype=None, want64=True):
+    """Backward of h = residual + x, y = RMSNorm(h) * gamma: dh = dx(dy; h) + dres
+    (x_dtype), the gradient of both residual and x; dgamma in fp32 and in the
+    weight dtype (dgamma_w)."""
+    w_dtype = w_dtype or x_dtype
+    h = _check_in(h, x_dtype)
+    M, N = h.shape
+    dy = _check_in(dy, x_dtype, (M, N))
+    dres = _check_in(dres, x_dtype, (M, N))
+    gamma = _check_in(gamma, w_dtype, (N,))
+    if rstd is not None:
+        rstd = _check_in(rstd, "f32", (M,))
+    dh = np.empty((M, N), _np(x_dtype))
+    dgamma = np.empty(N, np.float32)
+    dgamma_w = np.empty(N, _np(w_dtype))
+    dh64 = np.empty((M, N), np.float64) if want64 else None
+    dg64 = np.empty(N, np.float64) if want64 else None
+    rc = _load().oracle_rmsnorm_fused_add_bwd(_ptr(dy), _ptr(h), _ptr(rstd), _ptr(gamma),
+                                              _ptr(dres), M, N, float(eps), DTYPE_CODES[x_dtype],
+                                              DTYPE_CODES[w_dtype], _ptr(dh), _ptr(dh64),
+                                              _ptr(dg64), _ptr(dgamma), _ptr(dgamma_w))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_fused_add_bwd rejected its arguments")
+    out = {"dh": dh, "dgamma": dgamma, "dgamma_w": dgamma_w}
+    if want64:
+        out.update(dh64=dh64, dgamma64=dg64)
     return out

@@ -235,3 +235,38 @@ int oracle_rmsnorm_bwd(const void* dy, const void* x, const float* rstd, const v
   free(acc2);
   return 0;
 }
+
+/* ---- fused residual add: backward ---------------------------------------- */
+
+/* Backward of the fused add (the fused-add training wrapper of "Pre-built
+ * kernel library guide", section 1.2, for h = residual + x, y = RMSNorm(h)):
+ * h is the stored sum the forward normalised, dres the gradient that reaches
+ * h along the residual path.  Both r and x receive
+ *     dh = dx_rmsnorm(dy; h) + dres
+ * (rounded once to x_dtype).  dgamma as in oracle_rmsnorm_bwd, and optionally
+ * rounded once to w_dtype (dgamma_w).  Outputs may be NULL. */
+int oracle_rmsnorm_fused_add_bwd(const void* dy, const void* h, const float* rstd,
+                                 const void* gamma, const void* dres, int64_t M, int64_t N,
+                                 double eps, int x_dtype, int w_dtype, void* dh, double* dh64,
+                                 double* dgamma64, float* dgamma, void* dgamma_w) {
+  if (M < 0 || N <= 0 || bad_dtypes(x_dtype, w_dtype) || (M > 0 && !dres)) return -1;
+  double* dx64 = (double*)malloc((size_t)(M > 0 ? M : 1) * (size_t)N * sizeof(double));
+  double* dg = (double*)malloc((size_t)N * sizeof(double));
+  if (!dx64 || !dg) { free(dx64); free(dg); return -1; }
+  int rc = oracle_rmsnorm_bwd(dy, h, rstd, gamma, M, N, eps, x_dtype, w_dtype, NULL, dx64, dg,
+                              dgamma, NULL, NULL, NULL);
+  if (rc == 0) {
+    for (int64_t i = 0; i < M * N; ++i) {
+      double v = dx64[i] + load(dres, x_dtype, i);
+      if (dh) store(dh, x_dtype, i, v);
+      if (dh64) dh64[i] = v;
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      if (dgamma64) dgamma64[j] = dg[j];
+      if (dgamma_w) store(dgamma_w, w_dtype, j, dg[j]);
+    }
+  }
+  free(dx64);
+  free(dg);
+  return rc;
+}

@@ -332,3 +332,63 @@ def test_fused_add_residual_matches_torch_bf16_add():
     # y is the forward of the stored h, not of the unrounded sum
     f = oracle.fwd(bits(r + x), bits(g), 1e-6, "bf16")
     assert np.array_equal(out["y64"], f["y64"])
+
+
+# ---------------------------------------------------------------- fused add, backward
+
+@pytest.mark.parametrize("eps", [0.0, 1e-5, 0.3])
+def test_fused_add_backward_matches_torch_autograd_f64(eps):
+    # h = r + x, y = rms_norm(h) * gamma; loss = sum(dy y) + sum(dres h): the
+    # gradient of r and of x is dh = dx_rms(h) + dres
+    rng = np.random.default_rng(21)
+    M, N = 5, 48
+    r = _f32(rng.standard_normal((M, N)))
+    x = _f32(rng.standard_normal((M, N)))
+    g = _f32(rng.normal(1.0, 0.1, N))
+    dy = _f32(rng.standard_normal((M, N)))
+    dres = _f32(rng.standard_normal((M, N)))
+    h = _f32(r.astype(np.float64) + x)       # the stored h
+    rt = torch.from_numpy(r).double().requires_grad_()
+    xt = torch.from_numpy(x).double().requires_grad_()
+    gt = torch.from_numpy(g).double().requires_grad_()
+    s_ = rt + xt
+    # value: the stored h (fp32 rounding of the sum); gradient: that of h = r + x
+    ht = s_.detach().float().double() + (s_ - s_.detach())
+    y = torch.nn.functional.rms_norm(ht, (N,), gt, eps)
+    loss = (torch.from_numpy(dy).double() * y).sum() + (torch.from_numpy(dres).double() * ht).sum()
+    loss.backward()
+    out = oracle.fused_add_bwd(dy, h, None, g, dres, eps, "f32", "f32")
+    assert np.allclose(out["dh64"], xt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    assert np.allclose(out["dh64"], rt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    assert np.allclose(out["dgamma64"], gt.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_fused_add_backward_reduces_to_backward():
+    rng = np.random.default_rng(22)
+    M, N = 4, 40
+    h = _f32(rng.standard_normal((M, N)))
+    g = _f32(rng.normal(1.0, 0.1, N))
+    dy = _f32(rng.standard_normal((M, N)))
+    zero = np.zeros((M, N), np.float32)
+    a = oracle.fused_add_bwd(dy, h, None, g, zero, 1e-5, "f32", "f32")
+    b = oracle.bwd(dy, h, None, g, 1e-5, "f32", "f32")
+    assert np.array_equal(a["dh64"], b["dx64"]) and np.array_equal(a["dgamma64"], b["dgamma64"])
+    # and the residual gradient passes straight through where dy = 0
+    dres = _f32(rng.standard_normal((M, N)))
+    c = oracle.fused_add_bwd(np.zeros_like(dy), h, None, g, dres, 1e-5, "f32", "f32")
+    assert np.array_equal(c["dh64"], dres.astype(np.float64))
+
+
+def test_fused_add_backward_weight_dtype_gradient_is_rounded_once():
+    rng = np.random.default_rng(23)
+    M, N = 6, 24
+    bits = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    h = bits(rng.standard_normal((M, N)).astype(np.float32))
+    dy = bits(rng.standard_normal((M, N)).astype(np.float32))
+    dres = bits(rng.standard_normal((M, N)).astype(np.float32))
+    g = bits(rng.normal(1, 0.1, N).astype(np.float32))
+    out = oracle.fused_add_bwd(dy, h, None, g, dres, 1e-5, "bf16", "bf16")
+    want = np.array([oracle.round_bf16(v) for v in out["dgamma64"]], np.uint16)
+    assert np.array_equal(out["dgamma_w"], want)
+    want_dh = np.array([oracle.round_bf16(v) for v in out["dh64"].ravel()], np.uint16)
+    assert np.array_equal(out["dh"].ravel(), want_dh)
