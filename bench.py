@@ -54,6 +54,8 @@ def alg_bytes(wl, rows=None) -> int:
         return M * N * 2 * sx + N * sw + rstd
     if wl.op == "fused_add":
         return M * N * 4 * sx + N * sw + rstd
+    if wl.op == "fused_add_bwd":   # h, dy, dres in; dh out; dgamma in the weight dtype
+        return M * N * 4 * sx + 4 * M + N * sw + N * sw
     return M * N * 3 * sx + 4 * M + N * sw + 4 * N
 
 
@@ -501,7 +503,7 @@ def run_reference(args):
 # ------------------------------------------------------------------ sweep
 
 def _op_code(op):
-    return {"fwd": 0, "fused_add": 1, "bwd": 2}[op]
+    return {"fwd": 0, "fused_add": 1, "bwd": 2, "fused_add_bwd": 3}[op]
 
 
 def device_sets(wl, inp, dev, l2_bytes, rn):
@@ -522,6 +524,9 @@ def device_sets(wl, inp, dev, l2_bytes, rn):
         d["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
         if wl.op == "bwd":
             d["dgamma"] = torch.empty(N, dtype=torch.float32, device=dev)
+        if wl.op == "fused_add_bwd":
+            d["dgamma"] = torch.empty(N, dtype=torch.int16 if wl.w_dtype == "bf16"
+                                      else torch.float32, device=dev)
         sets.append(d)
     return sets
 
@@ -540,6 +545,10 @@ def make_launch(wl, d, stream, rn):
     ws = rn.rmsnorm_bwd_workspace_size(M, N, wl.x_dtype, wl.w_dtype)
     import torch
     d["ws"] = torch.empty(max(16, ws), dtype=torch.uint8, device=d["x"].device)
+    if wl.op == "fused_add_bwd":   # dres (the residual set) is overwritten with dh
+        return lambda: rn.rmsnorm_fused_add_bwd(d["dy"], d["x"], d["rstd"], d["gamma"],
+                                                d["residual"], d["dgamma"], wl.w_dtype, d["ws"],
+                                                ws, M, N, eps, wl.x_dtype, wl.w_dtype, stream)
     return lambda: rn.rmsnorm_bwd(d["dy"], d["x"], d["rstd"], d["gamma"], d["y"], d["dgamma"],
                                   d["ws"], ws, M, N, eps, wl.x_dtype, wl.w_dtype, stream)
 
@@ -575,7 +584,8 @@ def run_sweep(args):
     peak, _ = measured_peak()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = args.workloads.split(",") if args.workloads else [
-        n for n, w in si.WORKLOADS.items() if "sweep" in w.tags or "headline" in w.tags]
+        n for n, w in si.WORKLOADS.items()
+        if "sweep" in w.tags or "headline" in w.tags or "next" in w.tags]
     for name in names:
         wl = si.WORKLOADS[name]
         inp = si.make_inputs(wl)

@@ -107,6 +107,28 @@ rmsnorm_status_t rmsnorm_bwd(const void* dy, const void* x, const float* rstd,
                              cudaStream_t stream);
 
 /*
+ * Backward of the fused residual add (the fused-add training wrapper of "Pre-
+ * built kernel library guide", section 1.2): for h = residual + x and
+ * y = RMSNorm(h) * gamma, both the residual and x receive
+ *     dh_ij = rstd_i * (gamma_j dy_ij - h_ij c_i) + dres_ij
+ * where dres is the gradient that reaches h along the residual path and c_i
+ * is as in rmsnorm_bwd (with h in place of x).  h: M x N, the stored sum the
+ * forward normalised; rstd: M fp32 from the forward, or NULL to recompute from
+ * h and eps; dres: M x N, in: the residual-path gradient, out: dh (x_dtype,
+ * rounded once).  dgamma: N values in dgamma_dtype (RMSNORM_F32, or
+ * RMSNORM_BF16 rounded once from the fp32 sum -- the weight dtype of a bf16
+ * model), or NULL; reduced in a fixed order through `workspace` like
+ * rmsnorm_bwd, whose workspace query (rmsnorm_bwd_workspace_size) serves this
+ * call too.  Two launches on `stream`.
+ */
+rmsnorm_status_t rmsnorm_fused_add_bwd(const void* dy, const void* h, const float* rstd,
+                                       const void* gamma, void* dres, void* dgamma,
+                                       rmsnorm_dtype_t dgamma_dtype, void* workspace,
+                                       size_t workspace_bytes, int64_t M, int64_t N, float eps,
+                                       rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                                       cudaStream_t stream);
+
+/*
  * Backward for callers that cannot allocate device memory.  No counterpart in
  * the source pages: this entry point exists for integration only.
  *
@@ -168,7 +190,7 @@ const char* rmsnorm_status_string(rmsnorm_status_t status);
 /*
  * The kernel variant the library would launch for this call shape, as text
  * (for example "fwd/cta/vpt4/t256"), into buf (NUL-terminated, truncated to
- * len).  op: 0 forward, 1 fused add, 2 backward.  aligned16: nonzero when all
+ * len).  op: 0 forward, 1 fused add, 2 backward, 3 fused-add backward.  aligned16: nonzero when all
  * operand base pointers are 16-byte aligned.  Returns RMSNORM_OK or an
  * argument error; launches nothing.
  */

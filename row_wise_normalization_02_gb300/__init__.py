@@ -15,7 +15,8 @@ import ctypes
 import os
 import threading
 
-__all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "RMSNormError", "library_path",
+__all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "OP_FUSED_ADD_BWD", "RMSNormError",
+           "library_path", "rmsnorm_fused_add_bwd",
            "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
            "rmsnorm_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "rmsnorm_check_device",
@@ -23,12 +24,13 @@ __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "RMSNormError", "l
 
 F32 = 0
 BF16 = 1
-OP_FWD, OP_FUSED_ADD, OP_BWD = 0, 1, 2
+OP_FWD, OP_FUSED_ADD, OP_BWD, OP_FUSED_ADD_BWD = 0, 1, 2, 3
 _DT_NAMES = {"f32": F32, "bf16": BF16}
 
 EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspace_size",
                     "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan",
-                    "rmsnorm_bwd_noalloc", "rmsnorm_check_device", "rmsnorm_last_error")
+                    "rmsnorm_bwd_noalloc", "rmsnorm_check_device", "rmsnorm_last_error",
+                    "rmsnorm_fused_add_bwd")
 
 # Size of the library-owned scratch of rmsnorm_bwd_noalloc (16 MiB).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -77,6 +79,8 @@ def load_library():
             lib.rmsnorm_bwd_noalloc.restype = I
             lib.rmsnorm_check_device.argtypes = [P]
             lib.rmsnorm_check_device.restype = I
+            lib.rmsnorm_fused_add_bwd.argtypes = [P, P, P, P, P, P, I, P, SZ, I64, I64, F, I, I, P]
+            lib.rmsnorm_fused_add_bwd.restype = I
             lib.rmsnorm_last_error.argtypes = []
             lib.rmsnorm_last_error.restype = ctypes.c_char_p
             _lib = lib
@@ -137,6 +141,15 @@ def rmsnorm_bwd(dy, x, rstd, gamma, dx, dgamma, workspace, workspace_bytes, M, N
                                       _ptr(dgamma), _ptr(workspace), workspace_bytes, M, N, eps,
                                       _dt(x_dtype), _dt(w_dtype), _stream(stream)),
            "rmsnorm_bwd")
+
+
+def rmsnorm_fused_add_bwd(dy, h, rstd, gamma, dres, dgamma, dgamma_dtype, workspace,
+                          workspace_bytes, M, N, eps, x_dtype, w_dtype, stream=None):
+    _check(load_library().rmsnorm_fused_add_bwd(_ptr(dy), _ptr(h), _ptr(rstd), _ptr(gamma),
+                                                _ptr(dres), _ptr(dgamma), _dt(dgamma_dtype),
+                                                _ptr(workspace), workspace_bytes, M, N, eps,
+                                                _dt(x_dtype), _dt(w_dtype), _stream(stream)),
+           "rmsnorm_fused_add_bwd")
 
 
 def rmsnorm_bwd_noalloc(dy, x, rstd, gamma, dx, dgamma, M, N, eps, x_dtype, w_dtype,

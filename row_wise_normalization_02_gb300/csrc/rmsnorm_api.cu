@@ -184,7 +184,7 @@ cudaError_t occupancy(const void* fn, int device, int threads, int smem, int* bl
 
 // ---------------------------------------------------------------- plans
 
-enum Op { kFwd = 0, kFused = 1, kBwd = 2 };
+enum Op { kFwd = 0, kFused = 1, kBwd = 2, kFusedBwd = 3 };
 
 struct Plan {
   int family = kGeneric;
@@ -313,6 +313,8 @@ Force read_force() {
 // same_mod16: all activation base pointers agree modulo 16 bytes.
 rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligned16,
                            bool same_mod16, bool has_rstd, Plan* pl) {
+  const bool bwd = op == kBwd || op == kFusedBwd;
+  const bool dres = op == kFusedBwd;
   const int E = per_vec(xd);
   const bool rows_aligned = aligned16 && ((int64_t)N * esize(xd)) % 16 == 0;
   const int nvec = rows_aligned ? N / E : 0;
@@ -322,18 +324,18 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     subwarp_shape(nvec, &p.g, &p.vpt);
     p.threads = kSubwarpThreads;
     p.rows_per_cta = kSubwarpThreads / p.g;
-    p.prefetch = !(op == kBwd && p.g == 32);   // full-warp rows: more CTAs beat prefetch
-  } else if (rows_aligned && op == kBwd && nvec <= 4 * kCtaMaxThreads) {
+    p.prefetch = !(bwd && p.g == 32);   // full-warp rows: more CTAs beat prefetch
+  } else if (rows_aligned && bwd && nvec <= 4 * kCtaMaxThreads) {
     // backward: rows streamed by bulk copies, two stages, up to 4 vectors
     // per thread (the dgamma partials and gamma stay in registers)
     p.family = kStaged;
-    if (!cta_shape(op, nvec, &p.vpt, &p.threads) || p.vpt > 4) p.family = kGeneric;
+    if (!cta_shape(kBwd, nvec, &p.vpt, &p.threads) || p.vpt > 4) p.family = kGeneric;
     p.stages = 2;
   } else if (rows_aligned && nvec <= 4096) {
-    p.family = kCta;
-    if (!cta_shape(op, nvec, &p.vpt, &p.threads)) p.family = kGeneric;
+    p.family = dres ? kGeneric : kCta;   // the fused-add backward has no kCta form
+    if (p.family == kCta && !cta_shape(op, nvec, &p.vpt, &p.threads)) p.family = kGeneric;
     p.prefetch = op == kFwd ? p.vpt <= 4 : (op == kFused ? p.vpt != 2 && p.vpt <= 4 : p.vpt <= 2);
-    p.acc_smem = op == kBwd && p.vpt >= 4;
+    p.acc_smem = bwd && p.vpt >= 4;
   } else if (same_mod16 && N <= kRaggedMaxN) {
     p.family = kRagged;
     if (!ragged_shape(N / E + 1, &p.vpt, &p.threads)) p.family = kGeneric;
@@ -393,7 +395,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
   if (p.family == kStaged) {
     // ring of row buffers: as many stages as fit a half-SM budget (two CTAs
     // per SM), at least two, at most kStagedMaxStages
-    const int ns = op == kFwd ? 1 : 2;
+    const int ns = op == kFwd ? 1 : (op == kFusedBwd ? 3 : 2);
     const int64_t stage_bytes = (int64_t)ns * N * esize(xd);
     if (p.stages <= 0) {
       int64_t st = (kStagedSmemBudget - kStagedHeader) / stage_bytes;
@@ -406,13 +408,14 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.smem = (int)(kStagedHeader + p.stages * stage_bytes);
     p.rows_per_cta = 1;
   }
-  if (op == kBwd) {
+  if (bwd) {
     // each CTA writes one dgamma partial row (N fp32); keep that traffic to a
     // few percent of the rows it reads
     p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
     const Force fr = read_force();
     if (fr.on && fr.mr >= 0) p.min_rows = fr.mr;
-    BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch};
+    if (dres && p.family == kCta) return RMSNORM_ERR_INVALID_ARG;
+    BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch, dres};
     p.bwd = bwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.bwd);
     const int ld = round_up(N, 4);
@@ -471,10 +474,10 @@ const char* family_name(int f) {
 }
 
 void describe(int op, const Plan& p, char* buf, size_t len) {
-  static const char* ops[] = {"fwd", "fused_add", "bwd"};
+  static const char* ops[] = {"fwd", "fused_add", "bwd", "fused_add_bwd"};
   snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d", ops[op],
            family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
-           op == kBwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem);
+           op >= kBwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem);
 }
 
 // ---------------------------------------------------------------- launches
@@ -598,16 +601,20 @@ rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, 
   return RMSNORM_OK;
 }
 
+// Backward and fused-add backward.  dres (fused-add backward only) is the
+// residual-path gradient; its result dh = dx + dres goes to dx, which is then
+// the same buffer.  dgamma is fp32, or bf16 when dgamma_bf16.
 rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, const void* gamma,
-                          void* dx, float* dgamma, void* workspace, size_t workspace_bytes,
-                          int64_t M, int64_t N, float eps, int xd, int wd,
-                          cudaStream_t stream) {
+                          void* dx, const void* dres, void* dgamma, bool dgamma_bf16,
+                          void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                          float eps, int xd, int wd, cudaStream_t stream) {
   rmsnorm_status_t st = check_sizes(M, N, eps);
   if (st != RMSNORM_OK) return st;
   if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  const size_t gsz = dgamma_bf16 ? 2 : 4;
   if (M == 0) {
     if (dgamma) {
-      const cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)N * 4, stream);
+      const cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)N * gsz, stream);
       if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync of dgamma");
     }
     return RMSNORM_OK;
@@ -616,15 +623,16 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   const size_t xs = (size_t)esize(xd), ws = (size_t)esize(wd);
   if (!aligned_to(dy, xs) || !aligned_to(x, xs) || !aligned_to(dx, xs) ||
       !aligned_to(gamma, ws) || (rstd && !aligned_to(rstd, 4)) ||
-      (dgamma && !aligned_to(dgamma, 4)))
+      (dgamma && !aligned_to(dgamma, gsz)) || (dres && !aligned_to(dres, xs)))
     return RMSNORM_ERR_MISALIGNED;
   const size_t act = (size_t)M * (size_t)N * xs, gb = (size_t)N * ws, rb = (size_t)M * 4,
-               db = (size_t)N * 4;
+               db = (size_t)N * gsz;
   if (overlap(dx, act, dy, act) || overlap(dx, act, x, act) || overlap(dx, act, gamma, gb) ||
       overlap(dx, act, rstd, rb) || overlap(dx, act, dgamma, db) ||
       overlap(dgamma, db, dy, act) || overlap(dgamma, db, x, act) ||
       overlap(dgamma, db, gamma, gb) || overlap(dgamma, db, rstd, rb))
     return RMSNORM_ERR_INVALID_ARG;
+  if (dres && dres != dx && overlap(dres, act, dx, act)) return RMSNORM_ERR_INVALID_ARG;
 
   int dev;
   if ((st = current_device(&dev)) != RMSNORM_OK) return st;
@@ -643,11 +651,12 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
 
   const uintptr_t mx = reinterpret_cast<uintptr_t>(x) & 15;
   const bool same = (reinterpret_cast<uintptr_t>(dy) & 15) == mx &&
-                    (reinterpret_cast<uintptr_t>(dx) & 15) == mx;
+                    (reinterpret_cast<uintptr_t>(dx) & 15) == mx &&
+                    (!dres || (reinterpret_cast<uintptr_t>(dres) & 15) == mx);
   const bool aligned16 = same && mx == 0 && aligned_to(gamma, 16);
   Plan pl;
-  if ((st = make_plan(kBwd, M, (int)N, xd, wd, aligned16, same, rstd != nullptr, &pl)) !=
-      RMSNORM_OK)
+  if ((st = make_plan(dres ? kFusedBwd : kBwd, M, (int)N, xd, wd, aligned16, same,
+                      rstd != nullptr, &pl)) != RMSNORM_OK)
     return st;
   unsigned* status = nullptr;
   if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
@@ -660,6 +669,7 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   BwdParams prm;
   prm.dy = dy;
   prm.x = x;
+  prm.dres = dres;
   prm.rstd = rstd;
   prm.gamma = gamma;
   prm.dx = dx;
@@ -683,7 +693,7 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   // stage 2: the P partial rows summed per column in a fixed order
   const float* part = static_cast<const float*>(workspace);
   e = launch(get_dgamma_reduce_kernel(), (ld / 4 + kRedCols - 1) / kRedCols, kRedCols * kRedRows,
-             0, stream, part, pl.grid, (int)N, ld, dgamma);
+             0, stream, part, pl.grid, (int)N, ld, dgamma, dgamma_bf16 ? 1 : 0);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "backward stage-2 launch");
@@ -767,8 +777,21 @@ rmsnorm_status_t rmsnorm_bwd(const void* dy, const void* x, const float* rstd, c
                              void* dx, float* dgamma, void* workspace, size_t workspace_bytes,
                              int64_t M, int64_t N, float eps, rmsnorm_dtype_t x_dtype,
                              rmsnorm_dtype_t w_dtype, cudaStream_t stream) {
-  return bwd_impl(dy, x, rstd, gamma, dx, dgamma, workspace, workspace_bytes, M, N, eps,
-                  (int)x_dtype, (int)w_dtype, stream);
+  return bwd_impl(dy, x, rstd, gamma, dx, nullptr, dgamma, false, workspace, workspace_bytes, M,
+                  N, eps, (int)x_dtype, (int)w_dtype, stream);
+}
+
+rmsnorm_status_t rmsnorm_fused_add_bwd(const void* dy, const void* h, const float* rstd,
+                                       const void* gamma, void* dres, void* dgamma,
+                                       rmsnorm_dtype_t dgamma_dtype, void* workspace,
+                                       size_t workspace_bytes, int64_t M, int64_t N, float eps,
+                                       rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                                       cudaStream_t stream) {
+  if (dgamma_dtype != RMSNORM_F32 && dgamma_dtype != RMSNORM_BF16)
+    return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if (M > 0 && dres == nullptr) return RMSNORM_ERR_INVALID_ARG;
+  return bwd_impl(dy, h, rstd, gamma, dres, dres, dgamma, dgamma_dtype == RMSNORM_BF16,
+                  workspace, workspace_bytes, M, N, eps, (int)x_dtype, (int)w_dtype, stream);
 }
 
 rmsnorm_status_t rmsnorm_bwd_noalloc(const void* dy, const void* x, const float* rstd,
@@ -784,7 +807,7 @@ rmsnorm_status_t rmsnorm_bwd_noalloc(const void* dy, const void* x, const float*
   }
   // the workspace entry point with the static scratch as its workspace: a
   // shape whose partial rows exceed the scratch gets RMSNORM_ERR_WORKSPACE
-  return bwd_impl(dy, x, rstd, gamma, dx, dgamma, scratch,
+  return bwd_impl(dy, x, rstd, gamma, dx, nullptr, dgamma, false, scratch,
                   scratch ? (size_t)RMSNORM_BWD_NOALLOC_SCRATCH_BYTES : 0, M, N, eps,
                   (int)x_dtype, (int)w_dtype, stream);
 }
@@ -825,7 +848,7 @@ const char* rmsnorm_status_string(rmsnorm_status_t status) {
 rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
                                        rmsnorm_dtype_t w_dtype, int aligned16, int device,
                                        char* buf, size_t len) {
-  if (!buf || len == 0 || op < 0 || op > 2) return RMSNORM_ERR_INVALID_ARG;
+  if (!buf || len == 0 || op < 0 || op > 3) return RMSNORM_ERR_INVALID_ARG;
   buf[0] = 0;
   rmsnorm_status_t st = check_sizes(M, N, 0.f);
   if (st != RMSNORM_OK) return st;

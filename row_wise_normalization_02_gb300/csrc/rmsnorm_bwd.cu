@@ -46,28 +46,32 @@ __device__ __forceinline__ void load_gamma_vec(const void* gamma, int v, float (
   }
 }
 
-template <int VPT>
+template <int VPT, bool DRES = false>
 struct BSlice {
   uint4 x[VPT];
   uint4 dy[VPT];
-  float r;        // saved rstd of the row
+  uint4 dr[DRES ? VPT : 1];   // fused-add backward: residual-path gradient
+  float r;                    // saved rstd of the row
 };
 
-template <typename TX, int VPT, bool HAS_RSTD>
-__device__ __forceinline__ void bload_aligned(BSlice<VPT>& s, const BwdParams& p, int64_t row,
-                                              bool valid, int lane, int stride) {
+template <typename TX, int VPT, bool HAS_RSTD, bool DRES = false>
+__device__ __forceinline__ void bload_aligned(BSlice<VPT, DRES>& s, const BwdParams& p,
+                                              int64_t row, bool valid, int lane, int stride) {
   const size_t rb = (size_t)p.N * sizeof(TX);
   const char* xr = static_cast<const char*>(p.x) + row * rb;
   const char* dr = static_cast<const char*>(p.dy) + row * rb;
+  const char* rr = static_cast<const char*>(p.dres) + row * rb;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = lane + k * stride;
     if (valid && v < p.nvec) {
       s.x[k] = ld_stream(xr + (size_t)v * 16);
       s.dy[k] = ld_stream(dr + (size_t)v * 16);
+      if (DRES) s.dr[k] = ld_rw(rr + (size_t)v * 16);
     } else {
       s.x[k] = make_uint4(0, 0, 0, 0);
       s.dy[k] = make_uint4(0, 0, 0, 0);
+      if (DRES) s.dr[k] = make_uint4(0, 0, 0, 0);
     }
   }
   if (HAS_RSTD) s.r = valid ? __ldg(p.rstd + row) : 0.f;
@@ -77,7 +81,7 @@ __device__ __forceinline__ void bload_aligned(BSlice<VPT>& s, const BwdParams& p
 // kSubwarp: G lanes per row, 256 / G rows per CTA iteration; gamma and the
 // dgamma partials in registers; the row groups of a CTA are combined in
 // shared memory (in group order) at the end.
-template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF>
+template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF, bool DRES>
 __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdParams p) {
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
@@ -104,13 +108,13 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
 
   const int64_t stride = (int64_t)gridDim.x * RPC;
   int64_t base = (int64_t)blockIdx.x * RPC;
-  BSlice<VPT> cur, nxt;
-  bload_aligned<TX, VPT, HAS_RSTD>(cur, p, base + grp, base + grp < p.M, lane, G);
+  BSlice<VPT, DRES> cur, nxt;
+  bload_aligned<TX, VPT, HAS_RSTD, DRES>(cur, p, base + grp, base + grp < p.M, lane, G);
   for (; base < p.M; base += stride) {
     const int64_t row = base + grp;
     const bool valid = row < p.M;
     const int64_t nrow = row + stride;
-    if (PF) bload_aligned<TX, VPT, HAS_RSTD>(nxt, p, nrow, nrow < p.M, lane, G);
+    if (PF) bload_aligned<TX, VPT, HAS_RSTD, DRES>(nxt, p, nrow, nrow < p.M, lane, G);
 
     float dot = 0.f, ss = 0.f;
 #pragma unroll
@@ -137,18 +141,20 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lane + k * G;
-      float xf[E], df[E], o[E];
+      float xf[E], df[E], o[E], rf[E];
       unpack(cur.x[k], xf);
       unpack(cur.dy[k], df);
+      if (DRES) unpack(cur.dr[k], rf);
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
+        if (DRES) o[e] += rf[e];
         acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
       }
       if (valid && v < p.nvec) st_stream(dxr + (size_t)v * 16, pack(o));
     }
     if (PF) cur = nxt;
-    else bload_aligned<TX, VPT, HAS_RSTD>(cur, p, nrow, nrow < p.M, lane, G);
+    else bload_aligned<TX, VPT, HAS_RSTD, DRES>(cur, p, nrow, nrow < p.M, lane, G);
   }
   if (!want_dg) return;
   const int ncol = p.nvec * E;
@@ -279,7 +285,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cta_kernel(const BwdParams
 // kGeneric: any N, any element-aligned pointers.  Pass 1 reduces, pass 2
 // writes dx; the partial row of this CTA is accumulated in place in global
 // memory, each column always by the same thread.
-template <typename TX, typename TW, bool HAS_RSTD>
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
 __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
   pdl_begin();
   constexpr int K = HAS_RSTD ? 1 : 2;
@@ -307,20 +313,23 @@ __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
     parity ^= 1;
     const float r = HAS_RSTD ? __ldg(p.rstd + row) : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
     const float c = r * r * p.inv_n * sums[0];
+    const TX* rr = static_cast<const TX*>(p.dres) + row * (int64_t)N;
     for (int j = tid; j < N; j += T) {
       const float xv = ld_scalar(xr + j), dv = ld_scalar(dr + j);
-      st_scalar(dxr + j, r * fmaf(-xv, c, ld_scalar(gp + j) * dv));
+      float o = r * fmaf(-xv, c, ld_scalar(gp + j) * dv);
+      if (DRES) o += ld_scalar(rr + j);
+      st_scalar(dxr + j, o);
       if (prow) prow[j] = fmaf(dv * xv, r, prow[j]);
     }
   }
 }
 
-template <typename TX, typename TW, bool HAS_RSTD>
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
 BwdKernel pick_subwarp(int g, int vpt, bool pf) {
-#define RMSN_SW(G_, V_)                                                  \
-  if (g == G_ && vpt == V_)                                              \
-    return pf ? bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, true>       \
-              : bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, false>;
+#define RMSN_SW(G_, V_)                                                    \
+  if (g == G_ && vpt == V_)                                                \
+    return pf ? bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, true, DRES>   \
+              : bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, false, DRES>;
   RMSN_SW(4, 1) RMSN_SW(8, 1) RMSN_SW(16, 1) RMSN_SW(32, 1)
   RMSN_SW(8, 2) RMSN_SW(16, 2) RMSN_SW(32, 2) RMSN_SW(32, 3) RMSN_SW(32, 4)
 #undef RMSN_SW
@@ -343,12 +352,19 @@ BwdKernel pick_cta(int vpt, bool pf) {
 
 template <typename TX, typename TW, bool HAS_RSTD>
 BwdKernel pick_family(const BwdKey& k) {
+  if (k.dres) {   // fused-add backward: subwarp rows or the generic kernel
+    switch (k.family) {
+      case kSubwarp: return pick_subwarp<TX, TW, HAS_RSTD, true>(k.g, k.vpt, k.prefetch);
+      case kGeneric: return bwd_generic_kernel<TX, TW, HAS_RSTD, true>;
+      default: return nullptr;
+    }
+  }
   switch (k.family) {
-    case kSubwarp: return pick_subwarp<TX, TW, HAS_RSTD>(k.g, k.vpt, k.prefetch);
+    case kSubwarp: return pick_subwarp<TX, TW, HAS_RSTD, false>(k.g, k.vpt, k.prefetch);
     case kCta:
       return k.acc_smem ? pick_cta<TX, TW, HAS_RSTD, true>(k.vpt, k.prefetch)
                         : pick_cta<TX, TW, HAS_RSTD, false>(k.vpt, k.prefetch);
-    case kGeneric: return bwd_generic_kernel<TX, TW, HAS_RSTD>;
+    case kGeneric: return bwd_generic_kernel<TX, TW, HAS_RSTD, false>;
     default: return nullptr;
   }
 }
@@ -360,13 +376,14 @@ BwdKernel pick_rstd(const BwdKey& k) {
 
 #if RMSN_PAIR == 0
 // Stage 2: dgamma_j = sum_b partial[b][j] over the P stage-1 CTAs, in a fixed
-// order: thread (tx, ty) adds rows b = ty, ty + kRedRows, ... in sequence,
+// order, written in fp32 or (out_bf16) rounded once to bf16.  The order:
+// thread (tx, ty) adds rows b = ty, ty + kRedRows, ... in sequence,
 // then the kRedRows chunk sums are added in ty order.  Loads are issued in
 // batches of 8 ahead of the adds (the order of the adds does not change).
 // Launched as a programmatic dependent of stage 1; griddepcontrol.wait
 // returns once stage 1 has completed and its writes are visible.
 __global__ void __launch_bounds__(kRedCols* kRedRows)
-    dgamma_reduce_kernel(const float* partial, int P, int N, int ld, float* dgamma) {
+    dgamma_reduce_kernel(const float* partial, int P, int N, int ld, void* dgamma, int out_bf16) {
   pdl_begin();
   __shared__ float4 sh[kRedRows][kRedCols];
   const int tx = threadIdx.x % kRedCols, ty = threadIdx.x / kRedCols;
@@ -409,10 +426,14 @@ __global__ void __launch_bounds__(kRedCols* kRedRows)
       t.w += v.w;
     }
     const int j = q * 4;
-    if (j + 0 < N) dgamma[j + 0] = t.x;
-    if (j + 1 < N) dgamma[j + 1] = t.y;
-    if (j + 2 < N) dgamma[j + 2] = t.z;
-    if (j + 3 < N) dgamma[j + 3] = t.w;
+    const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (j + u < N) {
+        if (out_bf16) static_cast<bf16*>(dgamma)[j + u] = __float2bfloat16_rn(tv[u]);
+        else static_cast<float*>(dgamma)[j + u] = tv[u];
+      }
+    }
   }
 }
 #endif

@@ -52,6 +52,8 @@ struct FwdParams {
 struct BwdParams {
   const void* dy;
   const void* x;
+  const void* dres;   // fused-add backward: gradient reaching h on the residual path
+                      // (dx then holds dx + dres, and may be the same buffer)
   const float* rstd;  // null: recompute from x and eps
   const void* gamma;
   void* dx;
@@ -70,7 +72,7 @@ struct BwdParams {
 
 using FwdKernel = void (*)(FwdParams);
 using BwdKernel = void (*)(BwdParams);
-using ReduceKernel = void (*)(const float*, int, int, int, float*);
+using ReduceKernel = void (*)(const float*, int, int, int, void*, int);
 
 struct FwdKey {
   int xd, wd;
@@ -89,6 +91,7 @@ struct BwdKey {
   bool has_rstd;
   bool acc_smem; // kCta: dgamma partials in shared memory instead of registers
   bool prefetch;
+  bool dres;     // fused-add backward (adds the residual-path gradient)
 };
 
 // Kernel for a key, or nullptr when that instantiation does not exist.  Each

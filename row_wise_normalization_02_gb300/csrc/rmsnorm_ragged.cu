@@ -72,20 +72,23 @@ __device__ __forceinline__ void gather_gamma(const TW* gp, const Layout& L, int 
 
 // Registers of one row: body vectors of x (and of dy or of the residual) and
 // the one head/tail scalar of each.
-template <int VPT, bool TWO>
+template <int VPT, bool TWO, bool THREE = false>
 struct RowRegs {
   uint4 a[VPT];
   uint4 b[TWO ? VPT : 1];
-  float as, bs;
+  uint4 c[THREE ? VPT : 1];
+  float as, bs, cs;
 };
 
 // Load row `row` of up to two operands (b: the residual with `b_rw`, or dy).
-template <typename TX, int VPT, bool TWO, bool B_RW>
-__device__ __forceinline__ void load_row(RowRegs<VPT, TWO>& R, const TX* a, const TX* b,
-                                         int64_t row, int N, const Layout& L, int tid, int T) {
+template <typename TX, int VPT, bool TWO, bool B_RW, bool THREE = false>
+__device__ __forceinline__ void load_row(RowRegs<VPT, TWO, THREE>& R, const TX* a, const TX* b,
+                                         int64_t row, int N, const Layout& L, int tid, int T,
+                                         const TX* c = nullptr) {
   constexpr int E = Elem<TX>::kPerVec;
   const TX* ar = a + row * (int64_t)N;
   const TX* br = b + row * (int64_t)N;
+  const TX* cr = c + row * (int64_t)N;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = tid + k * T;
@@ -94,9 +97,11 @@ __device__ __forceinline__ void load_row(RowRegs<VPT, TWO>& R, const TX* a, cons
       if (B_RW) R.b[k] = v < L.nb ? ld_rw(br + L.h + v * E) : make_uint4(0, 0, 0, 0);
       else R.b[k] = v < L.nb ? ld_stream(br + L.h + v * E) : make_uint4(0, 0, 0, 0);
     }
+    if constexpr (THREE) R.c[k] = v < L.nb ? ld_rw(cr + L.h + v * E) : make_uint4(0, 0, 0, 0);
   }
   R.as = L.scol >= 0 ? ld_scalar(ar + L.scol) : 0.f;
   R.bs = (TWO && L.scol >= 0) ? ld_scalar(br + L.scol) : 0.f;
+  R.cs = (THREE && L.scol >= 0) ? ld_scalar(cr + L.scol) : 0.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -171,8 +176,8 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_ragged_kernel(const FwdPar
 }
 
 // ---------------------------------------------------------------------------
-// Backward (a = x, b = dy).
-template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool PF>
+// Backward (a = x, b = dy; fused-add backward: c = dres, added to dx).
+template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool PF, bool DRES>
 __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdParams p) {
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
@@ -194,11 +199,12 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
     for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
 
   int parity = 0;
-  RowRegs<VPT, true> cur, nxt;
-  if (w.first < p.M) load_row<TX, VPT, true, false>(cur, x, dy, w.first, N, L, tid, T);
+  RowRegs<VPT, true, DRES> cur, nxt;
+  const TX* dres = static_cast<const TX*>(p.dres);
+  if (w.first < p.M) load_row<TX, VPT, true, false, DRES>(cur, x, dy, w.first, N, L, tid, T, dres);
   for (int64_t row = w.first; row < p.M; row += w.stride) {
     const int64_t nrow = row + w.stride;
-    if (PF && nrow < p.M) load_row<TX, VPT, true, false>(nxt, x, dy, nrow, N, L, tid, T);
+    if (PF && nrow < p.M) load_row<TX, VPT, true, false, DRES>(nxt, x, dy, nrow, N, L, tid, T, dres);
     TX* dxr = dx + row * (int64_t)N;
     const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
     const float xs = cur.as, ds = cur.bs;
@@ -224,23 +230,25 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
       if (v < L.nb) {
-        float xf[E], df[E], o[E];
+        float xf[E], df[E], o[E], rf[E];
         unpack(cur.a[k], xf);
         unpack(cur.b[k], df);
+        if (DRES) unpack(cur.c[k], rf);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
+          if (DRES) o[e] += rf[e];
           acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
         }
         st_stream(dxr + L.h + v * E, pack(o));
       }
     }
     if (L.scol >= 0) {
-      st_scalar(dxr + L.scol, r * fmaf(-xs, c, gs * ds));
+      st_scalar(dxr + L.scol, r * fmaf(-xs, c, gs * ds) + (DRES ? cur.cs : 0.f));
       acc_s = fmaf(ds * xs, r, acc_s);
     }
     if (PF) cur = nxt;
-    else if (nrow < p.M) load_row<TX, VPT, true, false>(cur, x, dy, nrow, N, L, tid, T);
+    else if (nrow < p.M) load_row<TX, VPT, true, false, DRES>(cur, x, dy, nrow, N, L, tid, T, dres);
   }
   if (p.partial == nullptr) return;
   // every column of the partial row is written by exactly one thread
@@ -266,12 +274,14 @@ FwdKernel pick_fwd(int vpt, bool pf) {
   }
 }
 
-template <typename TX, typename TW, bool HAS_RSTD>
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
 BwdKernel pick_bwd(int vpt, bool pf) {
   switch (vpt) {
-    case 1: return pf ? bwd_ragged_kernel<TX, TW, 1, HAS_RSTD, true> : bwd_ragged_kernel<TX, TW, 1, HAS_RSTD, false>;
-    case 2: return pf ? bwd_ragged_kernel<TX, TW, 2, HAS_RSTD, true> : bwd_ragged_kernel<TX, TW, 2, HAS_RSTD, false>;
-    case 4: return pf ? nullptr : bwd_ragged_kernel<TX, TW, 4, HAS_RSTD, false>;
+    case 1: return pf ? bwd_ragged_kernel<TX, TW, 1, HAS_RSTD, true, DRES>
+                      : bwd_ragged_kernel<TX, TW, 1, HAS_RSTD, false, DRES>;
+    case 2: return pf ? bwd_ragged_kernel<TX, TW, 2, HAS_RSTD, true, DRES>
+                      : bwd_ragged_kernel<TX, TW, 2, HAS_RSTD, false, DRES>;
+    case 4: return pf ? nullptr : bwd_ragged_kernel<TX, TW, 4, HAS_RSTD, false, DRES>;
     default: return nullptr;
   }
 }
@@ -283,8 +293,11 @@ FwdKernel ragged_fwd(const FwdKey& k) {
 }
 template <typename TX, typename TW>
 BwdKernel ragged_bwd(const BwdKey& k) {
-  return k.has_rstd ? pick_bwd<TX, TW, true>(k.vpt, k.prefetch)
-                    : pick_bwd<TX, TW, false>(k.vpt, k.prefetch);
+  if (k.dres)
+    return k.has_rstd ? pick_bwd<TX, TW, true, true>(k.vpt, k.prefetch)
+                      : pick_bwd<TX, TW, false, true>(k.vpt, k.prefetch);
+  return k.has_rstd ? pick_bwd<TX, TW, true, false>(k.vpt, k.prefetch)
+                    : pick_bwd<TX, TW, false, false>(k.vpt, k.prefetch);
 }
 
 }  // namespace

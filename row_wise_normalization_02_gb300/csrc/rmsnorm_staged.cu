@@ -51,7 +51,8 @@ __device__ __forceinline__ Ring ring_of(unsigned char* smem) {
 // Thread 0: bulk-copy CTA row i of the NS streamed operands into its stage.
 template <int NS>
 __device__ __forceinline__ void issue_row(const Ring& rg, int64_t i, int64_t first, int64_t stride,
-                                          int S, const char* src0, const char* src1, size_t rb) {
+                                          int S, const char* src0, const char* src1,
+                                          const char* src2, size_t rb) {
   const int s = (int)(i % S);
   const int64_t row = first + i * stride;
   uint64_t* bar = rg.full + s;
@@ -59,6 +60,7 @@ __device__ __forceinline__ void issue_row(const Ring& rg, int64_t i, int64_t fir
   mbar_arrive_expect_tx(bar, (uint32_t)(NS * rb));
   bulk_copy_g2s(dst, src0 + row * rb, (uint32_t)rb, bar);
   if (NS > 1) bulk_copy_g2s(dst + rb, src1 + row * rb, (uint32_t)rb, bar);
+  if (NS > 2) bulk_copy_g2s(dst + 2 * rb, src2 + row * rb, (uint32_t)rb, bar);
 }
 
 // Thread 0, error path: wait (bounded) for rows [from, issued) still in flight.
@@ -71,7 +73,7 @@ __device__ __forceinline__ void drain(const Ring& rg, int64_t from, int64_t issu
 template <int NS>
 __device__ __forceinline__ int64_t ring_start(const Ring& rg, int S, int64_t nrows, int64_t first,
                                               int64_t stride, const char* src0, const char* src1,
-                                              size_t rb) {
+                                              const char* src2, size_t rb) {
   int64_t issued = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
@@ -80,7 +82,8 @@ __device__ __forceinline__ int64_t ring_start(const Ring& rg, int S, int64_t nro
   __syncthreads();
   if (threadIdx.x == 0) {
     const int64_t n0 = nrows < S ? nrows : S;
-    for (; issued < n0; ++issued) issue_row<NS>(rg, issued, first, stride, S, src0, src1, rb);
+    for (; issued < n0; ++issued)
+      issue_row<NS>(rg, issued, first, stride, S, src0, src1, src2, rb);
   }
   return issued;
 }
@@ -117,7 +120,8 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_staged_kernel(const FwdPar
   const int64_t nrows = first < p.M ? (p.M - 1 - first) / stride + 1 : 0;
   const char* xs = static_cast<const char*>(p.x);
   const char* rs_src = static_cast<const char*>(p.residual);
-  int64_t issued = ring_start<NS>(rg, S, nrows, first, stride, FUSED ? rs_src : xs, xs, rb);
+  int64_t issued =
+      ring_start<NS>(rg, S, nrows, first, stride, FUSED ? rs_src : xs, xs, nullptr, rb);
 
   float g[VPT][E];
 #pragma unroll
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_staged_kernel(const FwdPar
     parity ^= 1;
     if (tid == 0 && issued < nrows) {
       fence_proxy_async_smem();
-      issue_row<NS>(rg, issued, first, stride, S, FUSED ? rs_src : xs, xs, rb);
+      issue_row<NS>(rg, issued, first, stride, S, FUSED ? rs_src : xs, xs, nullptr, rb);
       ++issued;
     }
     const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
@@ -195,13 +199,17 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_staged_kernel(const FwdPar
 }
 
 // ---------------------------------------------------------------------------
-// Backward.  Stage layout [x | dy]; dgamma partials of this CTA's rows in
-// registers, written as one partial row at the end.
-template <typename TX, typename TW, int VPT, bool HAS_RSTD>
+// Backward.  Stage layout [x | dy] (fused-add backward: [h | dy | dres]);
+// dgamma partials of this CTA's rows in registers, written as one partial row
+// at the end.  The fused-add backward reads dres from the stage in its output
+// pass, so it refills the stage after that pass instead of right after the
+// reduction.
+template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool DRES>
 __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdParams p) {
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int K = HAS_RSTD ? 1 : 2;
+  constexpr int NS = DRES ? 3 : 2;
   extern __shared__ __align__(128) unsigned char smem[];
   const Ring rg = ring_of(smem);
   const int tid = threadIdx.x, T = blockDim.x, S = p.stages;
@@ -210,7 +218,8 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
   const int64_t nrows = first < p.M ? (p.M - 1 - first) / stride + 1 : 0;
   const char* xs = static_cast<const char*>(p.x);
   const char* ds = static_cast<const char*>(p.dy);
-  int64_t issued = ring_start<2>(rg, S, nrows, first, stride, xs, ds, rb);
+  const char* rs = static_cast<const char*>(p.dres);
+  int64_t issued = ring_start<NS>(rg, S, nrows, first, stride, xs, ds, rs, rb);
 
   float g[VPT][E], acc[VPT][E];
 #pragma unroll
@@ -232,7 +241,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
     const int64_t row = first + i * stride;
     const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
     const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
-    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * 2 * rb);
+    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * NS * rb);
     uint4 xv[VPT], dv[VPT];
     float sums[K];
 #pragma unroll
@@ -260,9 +269,9 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
       break;
     }
     parity ^= 1;
-    if (tid == 0 && issued < nrows) {
+    if (!DRES && tid == 0 && issued < nrows) {
       fence_proxy_async_smem();
-      issue_row<2>(rg, issued, first, stride, S, xs, ds, rb);
+      issue_row<NS>(rg, issued, first, stride, S, xs, ds, rs, rb);
       ++issued;
     }
     const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
@@ -272,15 +281,27 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
       if (v < p.nvec) {
-        float xf[E], df[E], o[E];
+        float xf[E], df[E], o[E], rf[E];
         unpack(xv[k], xf);
         unpack(dv[k], df);
+        if (DRES) unpack(st[2 * p.nvec + v], rf);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
+          if (DRES) o[e] += rf[e];
           acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
         }
         st_stream(dxrow + (size_t)v * 16, pack(o));
+      }
+    }
+    if (DRES) {
+      // every thread has read this stage: refill it (the barrier orders the
+      // reads before thread 0's bulk copy)
+      __syncthreads();
+      if (tid == 0 && issued < nrows) {
+        fence_proxy_async_smem();
+        issue_row<NS>(rg, issued, first, stride, S, xs, ds, rs, rb);
+        ++issued;
       }
     }
   }
@@ -316,12 +337,12 @@ FwdKernel pick_fwd(int vpt) {
   }
 }
 
-template <typename TX, typename TW, bool HAS_RSTD>
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
 BwdKernel pick_bwd(int vpt) {
   switch (vpt) {
-    case 1: return bwd_staged_kernel<TX, TW, 1, HAS_RSTD>;
-    case 2: return bwd_staged_kernel<TX, TW, 2, HAS_RSTD>;
-    case 4: return bwd_staged_kernel<TX, TW, 4, HAS_RSTD>;
+    case 1: return bwd_staged_kernel<TX, TW, 1, HAS_RSTD, DRES>;
+    case 2: return bwd_staged_kernel<TX, TW, 2, HAS_RSTD, DRES>;
+    case 4: return bwd_staged_kernel<TX, TW, 4, HAS_RSTD, DRES>;
     default: return nullptr;
   }
 }
@@ -332,7 +353,9 @@ FwdKernel staged_fwd(const FwdKey& k) {
 }
 template <typename TX, typename TW>
 BwdKernel staged_bwd(const BwdKey& k) {
-  return k.has_rstd ? pick_bwd<TX, TW, true>(k.vpt) : pick_bwd<TX, TW, false>(k.vpt);
+  if (k.dres)
+    return k.has_rstd ? pick_bwd<TX, TW, true, true>(k.vpt) : pick_bwd<TX, TW, false, true>(k.vpt);
+  return k.has_rstd ? pick_bwd<TX, TW, true, false>(k.vpt) : pick_bwd<TX, TW, false, false>(k.vpt);
 }
 
 }  // namespace

@@ -15,7 +15,7 @@ TENSOR_IDS = {"x": 1, "residual": 2, "gamma": 3, "dy": 4}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "fwd", "fused_add", "bwd"
+    op: str                 # "fwd", "fused_add", "bwd", "fused_add_bwd"
     M: int
     N: int
     x_dtype: str            # "f32" | "bf16"
@@ -37,8 +37,10 @@ def tensor_recipes(wl: Workload) -> dict:
     rec = {"x": act, "gamma": g}
     if wl.op == "fused_add":
         rec["residual"] = dict(act)
-    if wl.op == "bwd":
+    if wl.op in ("bwd", "fused_add_bwd"):
         rec["dy"] = dict(dist="normal", p0=0.0, p1=1.0, dtype=wl.x_dtype)
+    if wl.op == "fused_add_bwd":
+        rec["residual"] = dict(dist="normal", p0=0.0, p1=1.0, dtype=wl.x_dtype)  # dres
     return rec
 
 
@@ -58,6 +60,10 @@ WORKLOADS = {
                                        "bf16", "bf16", 1e-6, 2, store_rstd=False,
                                        outlier_fraction=1e-3, outlier_scale=100.0,
                                        tags=("headline",)),
+    # backward of the fused residual add at the fused-add shape: h (the stored
+    # sum), dy and the residual-path gradient dres; dgamma in the weight dtype
+    "fadd_bwd_bf16_m32768_n4096": Workload("fadd_bwd_bf16_m32768_n4096", "fused_add_bwd", 32768,
+                                           4096, "bf16", "bf16", 1e-6, 2, tags=("next",)),
     # backward: bf16 activations, fp32 gamma; rstd from the oracle forward
     "bwd_bf16_m16384_n8192": Workload("bwd_bf16_m16384_n8192", "bwd", 16384, 8192, "bf16",
                                       "f32", 1e-5, 3, tags=("headline",)),

@@ -8,6 +8,7 @@ import seeded_inputs as si
 from tests import parity_util as pu
 from tests.test_parity_bwd import check_bwd
 from tests.test_parity_fwd import check_fused, check_fwd
+from tests import test_parity_fused_bwd as fb
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 torch = pytest.importorskip("torch")
@@ -28,6 +29,14 @@ def test_workload_matches_oracle(name):
         r = inp["residual"]
         out = pu.run_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd)
         check_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, out, want_rstd=wl.store_rstd)
+    elif wl.op == "fused_add_bwd":
+        # x plays the stored sum h; the saved rstd comes from the oracle forward;
+        # dgamma in the weight dtype
+        rstd = oracle.fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want64=False)["rstd"]
+        out = fb.run(x, inp["dy"], inp["residual"], g, rstd, eps, wl.x_dtype, wl.w_dtype,
+                     dg_dtype=wl.w_dtype)
+        fb.check(x, inp["dy"], inp["residual"], g, rstd, eps, wl.x_dtype, wl.w_dtype, out,
+                 dg_dtype=wl.w_dtype)
     else:
         # the saved rstd comes from the oracle forward
         rstd = oracle.fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want64=False)["rstd"]
