@@ -52,6 +52,9 @@ def _load():
             lib.oracle_rmsnorm_fused_add_bwd.argtypes = [_P, _P, _P, _P, _P, I64, I64, D, I, I,
                                                          _P, _P, _P, _P, _P]
             lib.oracle_rmsnorm_fused_add_bwd.restype = I
+            lib.oracle_rmsnorm_fwd_strided.argtypes = [_P, I64, I64, _P, I64, I64, I64, D, I, I,
+                                                       _P, I64, I64, _P, _P]
+            lib.oracle_rmsnorm_fwd_strided.restype = I
             lib.oracle_round_bf16.argtypes = [D]
             lib.oracle_round_bf16.restype = ctypes.c_uint16
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -201,4 +204,36 @@ def fused_add_bwd(dy, h, rstd, gamma, dres, eps, x_dtype="bf16", w_dtype=None, w
     out = {"dh": dh, "dgamma": dgamma, "dgamma_w": dgamma_w}
     if want64:
         out.update(dh64=dh64, dgamma64=dg64)
+    return out
+
+
+def fwd_strided(xbuf, x_st, x_sh, gamma, T, H, D, eps, x_dtype="bf16", w_dtype=None,
+                y_st=None, y_sh=None, want64=True):
+    """Forward over the [T, H, D] rows of the flat buffer `xbuf` (row (t, h) at
+    element t * x_st + h * x_sh).  Returns y as a flat buffer shaped like xbuf
+    with rows at t * y_st + h * y_sh (default: the x layout; elements outside
+    the rows are zero), rstd [T * H], and y64 [T * H, D]."""
+    w_dtype = w_dtype or x_dtype
+    xbuf = np.ascontiguousarray(xbuf).reshape(-1)
+    if xbuf.dtype != _np(x_dtype):
+        raise TypeError("x dtype")
+    gamma = _check_in(gamma, w_dtype, (D,))
+    same = y_st is None and y_sh is None
+    y_st = x_st if y_st is None else y_st
+    y_sh = x_sh if y_sh is None else y_sh
+    ylen = max((T - 1) * y_st + (H - 1) * y_sh + D, 0) if T * H else 0
+    if same:
+        ylen = max(ylen, xbuf.size)
+    y = np.zeros(ylen, _np(x_dtype))
+    rstd = np.empty(T * H, np.float32)
+    y64 = np.empty((T * H, D), np.float64) if want64 else None
+    rc = _load().oracle_rmsnorm_fwd_strided(_ptr(xbuf), x_st, x_sh, _ptr(gamma), T, H, D,
+                                            float(eps), DTYPE_CODES[x_dtype],
+                                            DTYPE_CODES[w_dtype], _ptr(y), y_st, y_sh,
+                                            _ptr(y64), _ptr(rstd))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_fwd_strided rejected its arguments")
+    out = {"y": y, "rstd": rstd}
+    if want64:
+        out["y64"] = y64
     return out

@@ -270,3 +270,39 @@ int oracle_rmsnorm_fused_add_bwd(const void* dy, const void* h, const float* rst
   free(dg);
   return rc;
 }
+
+/* ---- strided rows (per-head q/k norm) ------------------------------------ */
+
+/* Forward over the rows of a [T, H, D] view: row (t, h) starts at element
+ * t * x_st + h * x_sh of x (and t * y_st + h * y_sh of y), its D elements are
+ * contiguous, and it is normalised over D with one gamma of length D shared by
+ * all heads -- the per-head q/k RMSNorm of "TIRx kernels", Kernels list
+ * (flashinfer.norm: qk_rmsnorm), whose rows sit inside a wider projection
+ * output.  rstd (optional) is [T * H], row t * H + h.  Strides in elements. */
+int oracle_rmsnorm_fwd_strided(const void* x, int64_t x_st, int64_t x_sh, const void* gamma,
+                               int64_t T, int64_t H, int64_t D, double eps, int x_dtype,
+                               int w_dtype, void* y, int64_t y_st, int64_t y_sh, double* y64,
+                               float* rstd) {
+  if (T < 0 || H < 0 || D <= 0 || bad_dtypes(x_dtype, w_dtype) ||
+      (T * H > 0 && (!x || !gamma)))
+    return -1;
+  double* v = (double*)malloc((size_t)D * sizeof(double));
+  double* yr = (double*)malloc((size_t)D * sizeof(double));
+  if (!v || !yr) { free(v); free(yr); return -1; }
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t xo = t * x_st + h * x_sh, yo = t * y_st + h * y_sh;
+      for (int64_t j = 0; j < D; ++j) v[j] = load(x, x_dtype, xo + j);
+      double r;
+      fwd_row(v, gamma, w_dtype, D, eps, &r, yr);
+      if (rstd) rstd[t * H + h] = (float)r;
+      for (int64_t j = 0; j < D; ++j) {
+        if (y) store(y, x_dtype, yo + j, yr[j]);
+        if (y64) y64[(t * H + h) * D + j] = yr[j];
+      }
+    }
+  }
+  free(v);
+  free(yr);
+  return 0;
+}

@@ -392,3 +392,38 @@ def test_fused_add_backward_weight_dtype_gradient_is_rounded_once():
     assert np.array_equal(out["dgamma_w"], want)
     want_dh = np.array([oracle.round_bf16(v) for v in out["dh64"].ravel()], np.uint16)
     assert np.array_equal(out["dh"].ravel(), want_dh)
+
+
+# ---------------------------------------------------------------- strided rows
+
+def test_strided_rows_equal_contiguous_rows_and_torch():
+    # q of a fused QKV projection: [T, Hq, D] rows inside a [T, (Hq + 2 Hk) D] buffer
+    rng = np.random.default_rng(31)
+    T, Hq, Hk, D = 5, 3, 1, 16
+    width = (Hq + 2 * Hk) * D
+    buf = _f32(rng.standard_normal((T, width)))
+    g = _f32(rng.normal(1.0, 0.1, D))
+    out = oracle.fwd_strided(buf, width, D, g, T, Hq, D, 1e-5, "f32", "f32")
+    q = buf[:, :Hq * D].reshape(T * Hq, D)
+    ref = oracle.fwd(np.ascontiguousarray(q), g, 1e-5, "f32", "f32")
+    assert np.array_equal(out["y64"], ref["y64"])
+    assert np.array_equal(out["rstd"], ref["rstd"])
+    yq = out["y"].reshape(-1)[: T * width].reshape(T, width)[:, :Hq * D].reshape(T * Hq, D)
+    assert np.array_equal(yq, ref["y"])
+    # untouched elements (the k and v columns) stay zero in the output buffer
+    assert (out["y"].reshape(-1)[: T * width].reshape(T, width)[:, Hq * D:] == 0).all()
+    t = torch.nn.functional.rms_norm(torch.from_numpy(buf).double().view(T, -1, D)[:, :Hq],
+                                     (D,), torch.from_numpy(g).double(), 1e-5)
+    assert np.allclose(out["y64"].reshape(T, Hq, D), t.numpy(), rtol=1e-13, atol=0)
+
+
+def test_strided_rows_follow_both_strides():
+    # output rows at different strides than the input rows
+    rng = np.random.default_rng(32)
+    T, H, D = 3, 4, 8
+    x = _f32(rng.standard_normal((T, H, D)))
+    g = _f32(rng.uniform(0.5, 1.5, D))
+    out = oracle.fwd_strided(x, H * D, D, g, T, H, D, 0.0, "f32", "f32", y_st=D, y_sh=T * D)
+    ref = oracle.fwd(x.reshape(T * H, D), g, 0.0, "f32", "f32")["y"].reshape(T, H, D)
+    y = out["y"].reshape(H, T, D)      # y[h, t] holds row (t, h)
+    assert np.array_equal(y.transpose(1, 0, 2), ref)
