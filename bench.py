@@ -50,7 +50,7 @@ def alg_bytes(wl, rows=None) -> int:
     M = wl.M if rows is None else rows
     sx, sw, N = esize(wl.x_dtype), esize(wl.w_dtype), wl.N
     rstd = 4 * M if (wl.store_rstd and wl.op != "bwd") else 0
-    if wl.op == "fwd":
+    if wl.op in ("fwd", "fwd_strided"):   # strided: only the rows move, not the gaps
         return M * N * 2 * sx + N * sw + rstd
     if wl.op == "fused_add":
         return M * N * 4 * sx + N * sw + rstd
@@ -503,7 +503,7 @@ def run_reference(args):
 # ------------------------------------------------------------------ sweep
 
 def _op_code(op):
-    return {"fwd": 0, "fused_add": 1, "bwd": 2, "fused_add_bwd": 3}[op]
+    return {"fwd": 0, "fused_add": 1, "bwd": 2, "fused_add_bwd": 3, "fwd_strided": 4}[op]
 
 
 def device_sets(wl, inp, dev, l2_bytes, rn):
@@ -520,7 +520,8 @@ def device_sets(wl, inp, dev, l2_bytes, rn):
     sets = []
     for _ in range(nsets):
         d = {k: v.to(dev) for k, v in host.items()}
-        d["y"] = torch.empty((M, N), dtype=act, device=dev)
+        if wl.op != "fwd_strided":   # the strided forward writes in place
+            d["y"] = torch.empty((M, N), dtype=act, device=dev)
         d["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
         if wl.op == "bwd":
             d["dgamma"] = torch.empty(N, dtype=torch.float32, device=dev)
@@ -542,6 +543,11 @@ def make_launch(wl, d, stream, rn):
         return lambda: rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], d["y"],
                                                 d["rstd"] if wl.store_rstd else None, M, N,
                                                 eps, wl.x_dtype, wl.w_dtype, stream)
+    if wl.op == "fwd_strided":   # the q slice of each token, normalised in place
+        st, H = wl.stride_token, wl.heads
+        return lambda: rn.rmsnorm_fwd_strided(d["x"], st, N, d["gamma"], d["x"], st, N,
+                                              d["rstd"] if wl.store_rstd else None, M // H, H,
+                                              N, eps, wl.x_dtype, wl.w_dtype, stream)
     ws = rn.rmsnorm_bwd_workspace_size(M, N, wl.x_dtype, wl.w_dtype)
     import torch
     d["ws"] = torch.empty(max(16, ws), dtype=torch.uint8, device=d["x"].device)
@@ -591,6 +597,8 @@ def run_sweep(args):
         inp = si.make_inputs(wl)
         sets = device_sets(wl, inp, dev, l2, rn)
         for d in sets:   # rstd of x for the backward (the forward kernel, untimed)
+            if wl.op not in ("bwd", "fused_add_bwd"):
+                break
             rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"], d["rstd"], wl.M, wl.N,
                            float(np.float32(wl.eps)), wl.x_dtype, wl.w_dtype, stream)
         launches = [make_launch(wl, d, stream, rn) for d in sets]

@@ -78,6 +78,28 @@ rmsnorm_status_t rmsnorm_fused_add_fwd(const void* x, void* residual, const void
                                        cudaStream_t stream);
 
 /*
+ * Forward over strided rows: the per-head q/k RMSNorm ("TIRx kernels", Kernels
+ * list, flashinfer.norm: qk_rmsnorm).  Row (t, h) of a [T, H, D] view starts
+ * at element t * x_stride_token + h * x_stride_head of x (its D elements
+ * contiguous) and is written at t * y_stride_token + h * y_stride_head of y;
+ * every row is normalised over D with the same gamma (D values).  Strides are
+ * in elements and non-negative; the rows of one view must not overlap
+ * (x_stride_head >= D when H > 1, x_stride_token >= (H-1) * x_stride_head + D
+ * when T > 1).  This covers q or k as a slice of a fused QKV projection output
+ * (x_stride_token = row width of that output, x_stride_head = D).  y may be x
+ * with the same strides (in place); otherwise the two views must not overlap.
+ * rstd: T * H fp32 (row t * H + h), or NULL.  Rows whose starts and strides
+ * are 16-byte aligned take the vectorised path; any other layout is handled
+ * by a scalar path.
+ */
+rmsnorm_status_t rmsnorm_fwd_strided(const void* x, int64_t x_stride_token,
+                                     int64_t x_stride_head, const void* gamma, void* y,
+                                     int64_t y_stride_token, int64_t y_stride_head, float* rstd,
+                                     int64_t T, int64_t H, int64_t D, float eps,
+                                     rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                                     cudaStream_t stream);
+
+/*
  * Workspace of rmsnorm_bwd, in bytes, for these sizes on `device` (-1: the
  * current device).  It depends on the device's SM count.  Writes *bytes
  * (0 when M == 0 or no dgamma is wanted is still a valid answer to pass).
@@ -190,9 +212,11 @@ const char* rmsnorm_status_string(rmsnorm_status_t status);
 /*
  * The kernel variant the library would launch for this call shape, as text
  * (for example "fwd/cta/vpt4/t256"), into buf (NUL-terminated, truncated to
- * len).  op: 0 forward, 1 fused add, 2 backward, 3 fused-add backward.  aligned16: nonzero when all
- * operand base pointers are 16-byte aligned.  Returns RMSNORM_OK or an
- * argument error; launches nothing.
+ * len).  op: 0 forward, 1 fused add, 2 backward, 3 fused-add backward,
+ * 4 strided forward (M = tokens x heads rows of N = D elements).  aligned16:
+ * nonzero when all operand base pointers (and, for op 4, all strides) are
+ * 16-byte aligned.  Returns RMSNORM_OK or an argument error; launches
+ * nothing.
  */
 rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
                                        rmsnorm_dtype_t w_dtype, int aligned16, int device,

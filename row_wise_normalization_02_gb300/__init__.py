@@ -16,7 +16,7 @@ import os
 import threading
 
 __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "OP_FUSED_ADD_BWD", "RMSNormError",
-           "library_path", "rmsnorm_fused_add_bwd",
+           "library_path", "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided",
            "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
            "rmsnorm_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "rmsnorm_check_device",
@@ -30,7 +30,7 @@ _DT_NAMES = {"f32": F32, "bf16": BF16}
 EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspace_size",
                     "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan",
                     "rmsnorm_bwd_noalloc", "rmsnorm_check_device", "rmsnorm_last_error",
-                    "rmsnorm_fused_add_bwd")
+                    "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided")
 
 # Size of the library-owned scratch of rmsnorm_bwd_noalloc (16 MiB).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -81,6 +81,9 @@ def load_library():
             lib.rmsnorm_check_device.restype = I
             lib.rmsnorm_fused_add_bwd.argtypes = [P, P, P, P, P, P, I, P, SZ, I64, I64, F, I, I, P]
             lib.rmsnorm_fused_add_bwd.restype = I
+            lib.rmsnorm_fwd_strided.argtypes = [P, I64, I64, P, P, I64, I64, P, I64, I64, I64, F,
+                                                I, I, P]
+            lib.rmsnorm_fwd_strided.restype = I
             lib.rmsnorm_last_error.argtypes = []
             lib.rmsnorm_last_error.restype = ctypes.c_char_p
             _lib = lib
@@ -141,6 +144,15 @@ def rmsnorm_bwd(dy, x, rstd, gamma, dx, dgamma, workspace, workspace_bytes, M, N
                                       _ptr(dgamma), _ptr(workspace), workspace_bytes, M, N, eps,
                                       _dt(x_dtype), _dt(w_dtype), _stream(stream)),
            "rmsnorm_bwd")
+
+
+def rmsnorm_fwd_strided(x, x_stride_token, x_stride_head, gamma, y, y_stride_token,
+                        y_stride_head, rstd, T, H, D, eps, x_dtype, w_dtype, stream=None):
+    _check(load_library().rmsnorm_fwd_strided(_ptr(x), x_stride_token, x_stride_head,
+                                              _ptr(gamma), _ptr(y), y_stride_token,
+                                              y_stride_head, _ptr(rstd), T, H, D, eps,
+                                              _dt(x_dtype), _dt(w_dtype), _stream(stream)),
+           "rmsnorm_fwd_strided")
 
 
 def rmsnorm_fused_add_bwd(dy, h, rstd, gamma, dres, dgamma, dgamma_dtype, workspace,

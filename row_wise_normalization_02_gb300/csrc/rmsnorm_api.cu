@@ -330,7 +330,11 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     // per thread (the dgamma partials and gamma stay in registers)
     p.family = kStaged;
     if (!cta_shape(kBwd, nvec, &p.vpt, &p.threads) || p.vpt > 4) p.family = kGeneric;
-    p.stages = 2;
+    // the fused-add backward streams three rows per stage (dy, h, dres): one
+    // more stage in flight pays for its longer epilogue (measured at
+    // 32768 x 4096 bf16: 0.83 -> 1.0 of the copy bandwidth); the plain
+    // backward is best at two
+    p.stages = dres && kStagedHeader + 3 * 3 * (int64_t)N * esize(xd) <= kStagedSmemMax ? 3 : 2;
   } else if (rows_aligned && nvec <= 4096) {
     p.family = dres ? kGeneric : kCta;   // the fused-add backward has no kCta form
     if (p.family == kCta && !cta_shape(op, nvec, &p.vpt, &p.threads)) p.family = kGeneric;
@@ -424,7 +428,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     else if (p.family == kRagged) p.smem = 512;
     else if (p.family != kStaged) p.smem = 0;
   } else {
-    FwdKey k{xd, wd, p.family, p.g, p.vpt, op == kFused, p.prefetch};
+    FwdKey k{xd, wd, p.family, p.g, p.vpt, op == kFused, p.prefetch, false};
     p.fwd = fwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.fwd);
     if (p.family == kCta) p.smem = 256;
@@ -474,7 +478,7 @@ const char* family_name(int f) {
 }
 
 void describe(int op, const Plan& p, char* buf, size_t len) {
-  static const char* ops[] = {"fwd", "fused_add", "bwd", "fused_add_bwd"};
+  static const char* ops[] = {"fwd", "fused_add", "bwd", "fused_add_bwd", "fwd_strided"};
   snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d", ops[op],
            family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
            op >= kBwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem);
@@ -560,7 +564,7 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   unsigned* status = nullptr;
   if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
 
-  FwdParams prm;
+  FwdParams prm = {};
   prm.x = x;
   prm.residual = residual;
   prm.gamma = gamma;
@@ -579,6 +583,123 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "forward kernel launch");
+  }
+  return RMSNORM_OK;
+}
+
+// ---------------------------------------------------------------- strided rows
+
+// Rows (t, h) of a [T, H, D] view with element strides (st, sh): non-negative,
+// rows inside a token do not overlap, tokens do not overlap.
+bool strided_layout_ok(int64_t T, int64_t H, int64_t D, int64_t st, int64_t sh) {
+  if (st < 0 || sh < 0) return false;
+  if (H > 1 && sh < D) return false;
+  if (T > 1 && st < (H - 1) * sh + D) return false;
+  return true;
+}
+
+// Plan of the strided forward: a row of at most 128 16-byte vectors with every
+// pointer and stride 16-byte aligned goes to the sub-warp kernel (G lanes walk
+// the (token, head) rows), anything else to the scalar kernel.
+rmsnorm_status_t strided_plan(int64_t D, int xd, int wd, bool vec_ok, Plan* out) {
+  const int nvec = vec_ok ? (int)(D / per_vec(xd)) : 0;
+  Plan p;
+  if (vec_ok && nvec <= 128) {
+    p.family = kSubwarp;
+    subwarp_shape(nvec, &p.g, &p.vpt);
+    p.threads = kSubwarpThreads;
+    p.rows_per_cta = kSubwarpThreads / p.g;
+    // no register prefetch: the occupancy it costs is worth more here (q norm
+    // at 32768 tokens x 32 heads x 128: 0.93 -> 0.95 of the copy bandwidth)
+    p.prefetch = false;
+  } else {
+    p.family = kGeneric;
+    p.threads = 256;
+  }
+  const Force f = read_force();
+  if (f.on) {
+    if (f.family == kGeneric) {
+      p.family = kGeneric;
+      p.threads = 256;
+      p.rows_per_cta = 1;
+    } else if (f.family == kSubwarp) {
+      if (!vec_ok || !f.g || !f.vpt || f.g * f.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
+      p.g = f.g;
+      p.vpt = f.vpt;
+      p.rows_per_cta = kSubwarpThreads / p.g;
+    } else if (f.family >= 0) {
+      return RMSNORM_ERR_INVALID_ARG;
+    }
+    if (f.pf >= 0) p.prefetch = f.pf != 0;
+    p.cta_per_sm_cap = f.cps;
+  }
+  FwdKey k{xd, wd, p.family, p.g, p.vpt, false, p.prefetch, true};
+  p.fwd = fwd_kernel(k);
+  p.fn = reinterpret_cast<const void*>(p.fwd);
+  p.smem = 0;
+  if (p.fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
+  *out = p;
+  return RMSNORM_OK;
+}
+
+rmsnorm_status_t fwd_strided_impl(const void* x, int64_t x_st, int64_t x_sh, const void* gamma,
+                                  void* y, int64_t y_st, int64_t y_sh, float* rstd, int64_t T,
+                                  int64_t H, int64_t D, float eps, int xd, int wd,
+                                  cudaStream_t stream) {
+  if (T < 0 || H < 0) return RMSNORM_ERR_INVALID_ARG;
+  rmsnorm_status_t st = check_sizes(T * H, D, eps);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  const int64_t M = T * H;
+  if (M == 0) return RMSNORM_OK;
+  if (!x || !gamma || !y) return RMSNORM_ERR_INVALID_ARG;
+  if (!strided_layout_ok(T, H, D, x_st, x_sh) || !strided_layout_ok(T, H, D, y_st, y_sh))
+    return RMSNORM_ERR_INVALID_ARG;
+  const size_t xs = (size_t)esize(xd), ws = (size_t)esize(wd);
+  if (!aligned_to(x, xs) || !aligned_to(y, xs) || !aligned_to(gamma, ws) ||
+      (rstd && !aligned_to(rstd, 4)))
+    return RMSNORM_ERR_MISALIGNED;
+  const size_t xspan = (size_t)((T - 1) * x_st + (H - 1) * x_sh + D) * xs;
+  const size_t yspan = (size_t)((T - 1) * y_st + (H - 1) * y_sh + D) * xs;
+  const size_t gb = (size_t)D * ws, rb = (size_t)M * 4;
+  const bool in_place = x == y && x_st == y_st && x_sh == y_sh;
+  if ((!in_place && overlap(x, xspan, y, yspan)) || overlap(y, yspan, gamma, gb) ||
+      overlap(y, yspan, rstd, rb) || overlap(rstd, rb, x, xspan) || overlap(rstd, rb, gamma, gb))
+    return RMSNORM_ERR_INVALID_ARG;
+
+  const bool vec_ok = aligned_to(x, 16) && aligned_to(y, 16) && aligned_to(gamma, 16) &&
+                      (D * (int64_t)xs) % 16 == 0 && (x_st * (int64_t)xs) % 16 == 0 &&
+                      (x_sh * (int64_t)xs) % 16 == 0 && (y_st * (int64_t)xs) % 16 == 0 &&
+                      (y_sh * (int64_t)xs) % 16 == 0;
+  Plan p;
+  if ((st = strided_plan(D, xd, wd, vec_ok, &p)) != RMSNORM_OK) return st;
+  const int nvec = vec_ok ? (int)(D / per_vec(xd)) : 0;
+  int dev;
+  if ((st = current_device(&dev)) != RMSNORM_OK) return st;
+  unsigned* status = nullptr;
+  if ((st = size_grid(&p, M, dev, &status)) != RMSNORM_OK) return st;
+
+  FwdParams prm = {};
+  prm.x = x;
+  prm.gamma = gamma;
+  prm.y = y;
+  prm.rstd = rstd;
+  prm.M = M;
+  prm.N = (int)D;
+  prm.nvec = nvec;
+  prm.eps = eps;
+  prm.inv_n = 1.0f / (float)D;
+  prm.status = status;
+  prm.period = 1;
+  prm.heads = H;
+  prm.x_st = x_st;
+  prm.x_sh = x_sh;
+  prm.y_st = y_st;
+  prm.y_sh = y_sh;
+  const cudaError_t e = launch(p.fwd, p.grid, p.threads, p.smem, stream, prm);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "strided forward launch");
   }
   return RMSNORM_OK;
 }
@@ -666,7 +787,7 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
     if (pl.grid < pl.period) return RMSNORM_ERR_WORKSPACE;
   }
 
-  BwdParams prm;
+  BwdParams prm = {};
   prm.dy = dy;
   prm.x = x;
   prm.dres = dres;
@@ -781,6 +902,16 @@ rmsnorm_status_t rmsnorm_bwd(const void* dy, const void* x, const float* rstd, c
                   N, eps, (int)x_dtype, (int)w_dtype, stream);
 }
 
+rmsnorm_status_t rmsnorm_fwd_strided(const void* x, int64_t x_stride_token,
+                                     int64_t x_stride_head, const void* gamma, void* y,
+                                     int64_t y_stride_token, int64_t y_stride_head, float* rstd,
+                                     int64_t T, int64_t H, int64_t D, float eps,
+                                     rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                                     cudaStream_t stream) {
+  return fwd_strided_impl(x, x_stride_token, x_stride_head, gamma, y, y_stride_token,
+                          y_stride_head, rstd, T, H, D, eps, (int)x_dtype, (int)w_dtype, stream);
+}
+
 rmsnorm_status_t rmsnorm_fused_add_bwd(const void* dy, const void* h, const float* rstd,
                                        const void* gamma, void* dres, void* dgamma,
                                        rmsnorm_dtype_t dgamma_dtype, void* workspace,
@@ -848,16 +979,22 @@ const char* rmsnorm_status_string(rmsnorm_status_t status) {
 rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
                                        rmsnorm_dtype_t w_dtype, int aligned16, int device,
                                        char* buf, size_t len) {
-  if (!buf || len == 0 || op < 0 || op > 3) return RMSNORM_ERR_INVALID_ARG;
+  if (!buf || len == 0 || op < 0 || op > 4) return RMSNORM_ERR_INVALID_ARG;
   buf[0] = 0;
   rmsnorm_status_t st = check_sizes(M, N, 0.f);
   if (st != RMSNORM_OK) return st;
   if (!dtype_pair_ok((int)x_dtype, (int)w_dtype)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
   if (device < 0 && (st = current_device(&device)) != RMSNORM_OK) return st;
   Plan pl;
-  if ((st = make_plan(op, M, (int)N, (int)x_dtype, (int)w_dtype, aligned16 != 0, aligned16 != 0,
-                      true, &pl)) != RMSNORM_OK)
+  if (op == 4) {
+    if ((st = strided_plan(N, (int)x_dtype, (int)w_dtype,
+                           aligned16 != 0 && (N * esize((int)x_dtype)) % 16 == 0, &pl)) !=
+        RMSNORM_OK)
+      return st;
+  } else if ((st = make_plan(op, M, (int)N, (int)x_dtype, (int)w_dtype, aligned16 != 0,
+                             aligned16 != 0, true, &pl)) != RMSNORM_OK) {
     return st;
+  }
   if ((st = size_grid(&pl, M > 0 ? M : 1, device)) != RMSNORM_OK) return st;
   describe(op, pl, buf, len);
   return RMSNORM_OK;

@@ -214,6 +214,117 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cta_kernel(const FwdParams
 }
 
 // ---------------------------------------------------------------------------
+// Strided rows (per-head q/k norm, "TIRx kernels", Kernels list: qk_rmsnorm):
+// row i = (t, h) of a [T, H, D] view.  Same per-row work as kSubwarp; each
+// thread steps its (t, h) by the grid stride without dividing.
+template <typename TX, typename TW, int G, int VPT, bool PF>
+__global__ void __launch_bounds__(kSubwarpThreads) fwd_strided_kernel(const FwdParams p) {
+  pdl_begin();
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW;
+  constexpr int RPC = kSubwarpThreads / G;
+  const int lane = threadIdx.x % G, grp = threadIdx.x / G;
+  const int64_t H = p.heads;
+
+  uint4 gw[VPT][GW];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+#pragma unroll
+    for (int w = 0; w < GW; ++w)
+      gw[k][w] = v < p.nvec ? ld_cached(static_cast<const char*>(p.gamma) +
+                                        ((size_t)v * GW + w) * 16)
+                            : make_uint4(0, 0, 0, 0);
+  }
+  const int64_t stride = (int64_t)gridDim.x * RPC;
+  const int64_t dt = stride / H, dh = stride % H;
+  int64_t base = (int64_t)blockIdx.x * RPC;
+  int64_t t = (base + grp) / H, h = (base + grp) % H;
+  const TX* x = static_cast<const TX*>(p.x);
+  TX* y = static_cast<TX*>(p.y);
+
+  auto load = [&](uint4 (&dst)[VPT], int64_t tt, int64_t hh, bool valid) {
+    const TX* xr = x + tt * p.x_st + hh * p.x_sh;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * G;
+      dst[k] = (valid && v < p.nvec) ? ld_stream(xr + v * E) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 cur[VPT], nxt[VPT];
+  load(cur, t, h, base + grp < p.M);
+  for (; base < p.M; base += stride) {
+    const int64_t row = base + grp;
+    const bool valid = row < p.M;
+    int64_t tn = t + dt, hn = h + dh;
+    if (hn >= H) {
+      hn -= H;
+      ++tn;
+    }
+    if (PF) load(nxt, tn, hn, row + stride < p.M);
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      float f[E];
+      unpack(cur[k], f);
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+    ss = group_sum<G>(ss);
+    const float rs = rsqrtf(fmaf(ss, p.inv_n, p.eps));
+    if (valid && lane == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+    TX* yr = y + t * p.y_st + h * p.y_sh;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * G;
+      if (valid && v < p.nvec) {
+        float g[E], o[E];
+        unpack_gamma<TW, E, GW>(gw[k], g);
+        unpack(cur[k], o);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
+        st_stream(yr + v * E, pack(o));
+      }
+    }
+    if (PF) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) cur[k] = nxt[k];
+    } else {
+      load(cur, tn, hn, row + stride < p.M);
+    }
+    t = tn;
+    h = hn;
+  }
+}
+
+// Strided rows, any alignment and any D: one row per 256-thread CTA, scalar,
+// two passes (the second re-reads the row, from L2 for rows of this size).
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(256) fwd_strided_generic_kernel(const FwdParams p) {
+  pdl_begin();
+  __shared__ float red[64];
+  const int tid = threadIdx.x, T = blockDim.x;
+  const int D = p.N;
+  const TW* g = static_cast<const TW*>(p.gamma);
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const int64_t t = row / p.heads, h = row % p.heads;
+    const TX* xr = static_cast<const TX*>(p.x) + t * p.x_st + h * p.x_sh;
+    TX* yr = static_cast<TX*>(p.y) + t * p.y_st + h * p.y_sh;
+    float ss[1] = {0.f};
+    for (int j = tid; j < D; j += T) {
+      const float v = ld_scalar(xr + j);
+      ss[0] = fmaf(v, v, ss[0]);
+    }
+    cta_sum<1>(ss, red, parity);
+    parity ^= 1;
+    const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
+    if (tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+    for (int j = tid; j < D; j += T) st_scalar(yr + j, ld_scalar(xr + j) * rs * ld_scalar(g + j));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // kGeneric: any N and any element-aligned pointers.  Pass 1 reads the row
 // (fused: forms, rounds and stores h) and reduces; pass 2 re-reads it.
 template <typename TX, typename TW, bool FUSED>
@@ -272,8 +383,25 @@ FwdKernel pick_cta(int vpt, bool pf) {
   }
 }
 
+template <typename TX, typename TW, bool PF>
+FwdKernel pick_strided(int g, int vpt) {
+#define RMSN_ST(G_, V_) \
+  if (g == G_ && vpt == V_) return fwd_strided_kernel<TX, TW, G_, V_, PF>;
+  RMSN_ST(4, 1) RMSN_ST(8, 1) RMSN_ST(16, 1) RMSN_ST(32, 1)
+  RMSN_ST(8, 2) RMSN_ST(16, 2) RMSN_ST(32, 2) RMSN_ST(32, 3) RMSN_ST(32, 4)
+#undef RMSN_ST
+  return nullptr;
+}
+
 template <typename TX, typename TW, bool FUSED>
 FwdKernel pick_family(const FwdKey& k) {
+  if (k.strided) {
+    if (FUSED) return nullptr;
+    if (k.family == kGeneric) return fwd_strided_generic_kernel<TX, TW>;
+    if (k.family != kSubwarp) return nullptr;
+    return k.prefetch ? pick_strided<TX, TW, true>(k.g, k.vpt)
+                      : pick_strided<TX, TW, false>(k.g, k.vpt);
+  }
   switch (k.family) {
     case kSubwarp:
       return k.prefetch ? pick_subwarp<TX, TW, FUSED, true>(k.g, k.vpt)

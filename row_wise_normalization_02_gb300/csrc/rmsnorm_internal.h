@@ -47,6 +47,10 @@ struct FwdParams {
   long long wait_limit;   // kStaged: clock cycles before a wait gives up
   unsigned* status;   // device status word (kStatus* bits)
   int period;         // kRagged: rows i and i + period start at the same address mod 16
+  // strided rows (per-head q/k norm): row i = (t, h) = (i / heads, i % heads)
+  // starts at element t * x_st + h * x_sh of x and t * y_st + h * y_sh of y
+  int64_t heads;
+  int64_t x_st, x_sh, y_st, y_sh;
 };
 
 struct BwdParams {
@@ -81,6 +85,7 @@ struct FwdKey {
   int vpt;       // 16-byte vectors per thread
   bool fused;
   bool prefetch; // issue the next row's loads before reducing the current row
+  bool strided;  // rows addressed through (heads, x_st, x_sh, y_st, y_sh)
 };
 
 struct BwdKey {

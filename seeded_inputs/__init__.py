@@ -127,6 +127,11 @@ def make_inputs(wl: "Workload", rows: int | None = None) -> dict:
     m = wl.M if rows is None else min(rows, wl.M)
     out = {}
     for name, rec in tensor_recipes(wl).items():
-        shape = (wl.N,) if name == "gamma" else (m, wl.N)
+        rec = dict(rec)
+        shape = rec.pop("shape", None)
+        if shape is None:
+            shape = (wl.N,) if name == "gamma" else (m, wl.N)
+        elif rows is not None:
+            shape = (min(rows, shape[0]),) + tuple(shape[1:])
         out[name] = fill(shape, seed=wl.seed, tensor_id=TENSOR_IDS[name], **rec)
     return out

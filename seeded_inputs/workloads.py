@@ -15,7 +15,7 @@ TENSOR_IDS = {"x": 1, "residual": 2, "gamma": 3, "dy": 4}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "fwd", "fused_add", "bwd", "fused_add_bwd"
+    op: str                 # "fwd", "fused_add", "bwd", "fused_add_bwd", "fwd_strided"
     M: int
     N: int
     x_dtype: str            # "f32" | "bf16"
@@ -27,6 +27,8 @@ class Workload:
     outlier_fraction: float = 0.0
     outlier_scale: float = 1.0
     tags: tuple = field(default_factory=tuple)
+    heads: int = 0          # strided rows: M = tokens * heads, x is [tokens, stride_token]
+    stride_token: int = 0
 
 
 def tensor_recipes(wl: Workload) -> dict:
@@ -35,6 +37,8 @@ def tensor_recipes(wl: Workload) -> dict:
                outlier_fraction=wl.outlier_fraction, outlier_scale=wl.outlier_scale)
     g = dict(dist=wl.gamma_dist[0], p0=wl.gamma_dist[1], p1=wl.gamma_dist[2], dtype=wl.w_dtype)
     rec = {"x": act, "gamma": g}
+    if wl.op == "fwd_strided":
+        rec["x"] = dict(act, shape=(wl.M // wl.heads, wl.stride_token))
     if wl.op == "fused_add":
         rec["residual"] = dict(act)
     if wl.op in ("bwd", "fused_add_bwd"):
@@ -64,6 +68,12 @@ WORKLOADS = {
     # sum), dy and the residual-path gradient dres; dgamma in the weight dtype
     "fadd_bwd_bf16_m32768_n4096": Workload("fadd_bwd_bf16_m32768_n4096", "fused_add_bwd", 32768,
                                            4096, "bf16", "bf16", 1e-6, 2, tags=("next",)),
+    # per-head q norm in place on a fused QKV projection output: 32768 tokens,
+    # 32 q heads and 8 kv heads of 128 (row width 6144)
+    "qnorm_bf16_t32768_h32_d128": Workload("qnorm_bf16_t32768_h32_d128", "fwd_strided",
+                                           32768 * 32, 128, "bf16", "bf16", 1e-6, 5,
+                                           store_rstd=False, heads=32, stride_token=6144,
+                                           tags=("next",)),
     # backward: bf16 activations, fp32 gamma; rstd from the oracle forward
     "bwd_bf16_m16384_n8192": Workload("bwd_bf16_m16384_n8192", "bwd", 16384, 8192, "bf16",
                                       "f32", 1e-5, 3, tags=("headline",)),

@@ -88,12 +88,33 @@ def test_fused_and_bwd_argument_errors_without_gpu(lib):
     assert e.value.status == 1
 
 
+@pytest.mark.parametrize("args,status", [
+    (dict(x_sh=64), 1),                 # heads overlap (head stride < D)
+    (dict(x_st=200), 1),                # tokens overlap (token stride < H * head stride)
+    (dict(y_st=-1), 1), (dict(T=-1), 1), (dict(D=0), 1),
+    (dict(x=FAKE + 1), 3),
+    (dict(y=FAKE, y_st=256, y_sh=128), 1),    # y overlaps x without being the same layout
+    (dict(x_dtype=rn.F32, w_dtype=rn.BF16), 2),
+])
+def test_strided_argument_errors_without_gpu(lib, args, status):
+    a = dict(x=FAKE, x_st=384, x_sh=128, gamma=FAKE + (1 << 32), y=FAKE + (2 << 32), y_st=256,
+             y_sh=128, rstd=None, T=4, H=2, D=128, x_dtype=rn.BF16, w_dtype=rn.BF16)
+    a.update(args)
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_fwd_strided(a["x"], a["x_st"], a["x_sh"], a["gamma"], a["y"], a["y_st"],
+                               a["y_sh"], a["rstd"], a["T"], a["H"], a["D"], 1e-6, a["x_dtype"],
+                               a["w_dtype"])
+    assert e.value.status == status
+
+
 def test_zero_rows_is_a_no_op(lib):
     # M == 0: nothing to do, no pointer is touched and no CUDA call is made
     rn.rmsnorm_fwd(None, None, None, None, 0, 64, 1e-5, rn.BF16, rn.BF16)
     rn.rmsnorm_fused_add_fwd(None, None, None, None, None, 0, 64, 1e-5, rn.BF16, rn.BF16)
     rn.rmsnorm_bwd(None, None, None, None, None, None, None, 0, 0, 64, 1e-5, rn.BF16, rn.BF16)
     assert rn.rmsnorm_bwd_workspace_size(0, 64, rn.BF16, rn.BF16) == 0
+    rn.rmsnorm_fwd_strided(None, 0, 0, None, None, 0, 0, None, 0, 8, 128, 1e-6, rn.BF16,
+                           rn.BF16)
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -29,6 +29,9 @@ def test_workload_matches_oracle(name):
         r = inp["residual"]
         out = pu.run_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd)
         check_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, out, want_rstd=wl.store_rstd)
+    elif wl.op == "fwd_strided":
+        from tests import test_parity_strided as ts
+        ts.check_workload(wl, inp)
     elif wl.op == "fused_add_bwd":
         # x plays the stored sum h; the saved rstd comes from the oracle forward;
         # dgamma in the weight dtype
