@@ -55,6 +55,18 @@ def _load():
             lib.oracle_rmsnorm_fwd_strided.argtypes = [_P, I64, I64, _P, I64, I64, I64, D, I, I,
                                                        _P, I64, I64, _P, _P]
             lib.oracle_rmsnorm_fwd_strided.restype = I
+            lib.oracle_rmsnorm_fwd_fp8.argtypes = [_P, _P, _P, I64, I64, D, I, I, _P, _P, _P, _P,
+                                                   _P, _P]
+            lib.oracle_rmsnorm_fwd_fp8.restype = I
+            lib.oracle_rmsnorm_fwd_nvfp4.argtypes = [_P, _P, _P, I64, I64, D, D, I, I, _P, _P,
+                                                     _P, _P, _P, _P]
+            lib.oracle_rmsnorm_fwd_nvfp4.restype = I
+            for name in ("oracle_round_e4m3", "oracle_round_e2m1"):
+                getattr(lib, name).argtypes = [D]
+                getattr(lib, name).restype = ctypes.c_uint8
+            for name in ("oracle_e4m3_to_double", "oracle_e2m1_to_double"):
+                getattr(lib, name).argtypes = [ctypes.c_uint8]
+                getattr(lib, name).restype = D
             lib.oracle_round_bf16.argtypes = [D]
             lib.oracle_round_bf16.restype = ctypes.c_uint16
             lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -236,4 +248,101 @@ def fwd_strided(xbuf, x_st, x_sh, gamma, T, H, D, eps, x_dtype="bf16", w_dtype=N
     out = {"y": y, "rstd": rstd}
     if want64:
         out["y64"] = y64
+    return out
+
+
+# ---------------------------------------------------------------- quantised
+
+def round_e4m3(v: float) -> int:
+    """FP8 E4M3 code of a double (nearest, ties to even, saturating at 448)."""
+    return int(_load().oracle_round_e4m3(float(v)))
+
+
+def e4m3_to_double(code: int) -> float:
+    return float(_load().oracle_e4m3_to_double(int(code)))
+
+
+def round_e2m1(v: float) -> int:
+    """FP4 E2M1 code (4 bits) of a double (nearest, ties to even, saturating at 6)."""
+    return int(_load().oracle_round_e2m1(float(v)))
+
+
+def e2m1_to_double(code: int) -> float:
+    return float(_load().oracle_e2m1_to_double(int(code)))
+
+
+def e4m3_values() -> np.ndarray:
+    """Value of each of the 256 E4M3 codes (NaN for 0x7F and 0xFF)."""
+    return np.array([e4m3_to_double(c) for c in range(256)])
+
+
+def e2m1_values() -> np.ndarray:
+    """Value of each of the 16 E2M1 codes."""
+    return np.array([e2m1_to_double(c) for c in range(16)])
+
+
+def fwd_fp8(x, gamma, eps, x_dtype="bf16", w_dtype=None, residual=None):
+    """Forward (of x, or of h = residual + x) with E4M3 codes q [M, N] and one
+    fp32 dequantisation scale per row.  Also scale64, v64 (the exact y / s),
+    rstd and, with a residual, h."""
+    w_dtype = w_dtype or x_dtype
+    x = _check_in(x, x_dtype)
+    M, N = x.shape
+    gamma = _check_in(gamma, w_dtype, (N,))
+    if residual is not None:
+        residual = _check_in(residual, x_dtype, (M, N))
+    h = np.empty((M, N), _np(x_dtype)) if residual is not None else None
+    q = np.empty((M, N), np.uint8)
+    scale = np.empty(M, np.float32)
+    scale64 = np.empty(M, np.float64)
+    v64 = np.empty((M, N), np.float64)
+    rstd = np.empty(M, np.float32)
+    rc = _load().oracle_rmsnorm_fwd_fp8(_ptr(x), _ptr(residual), _ptr(gamma), M, N, float(eps),
+                                        DTYPE_CODES[x_dtype], DTYPE_CODES[w_dtype], _ptr(h),
+                                        _ptr(q), _ptr(scale), _ptr(scale64), _ptr(v64),
+                                        _ptr(rstd))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_fwd_fp8 rejected its arguments")
+    out = {"q": q, "scale": scale, "scale64": scale64, "v64": v64, "rstd": rstd}
+    if h is not None:
+        out["h"] = h
+    return out
+
+
+def fwd_nvfp4(x, gamma, gs, eps, x_dtype="bf16", w_dtype=None, residual=None):
+    """Forward (of x, or of h = residual + x) with NVFP4 output: q [M, N/2]
+    (two E2M1 codes per byte, even element in the low nibble) and sf [M, N/16]
+    (E4M3 block scales) for the global scale gs.  Also sfv64 (the exact
+    gs * amax / 6 per block), v64 (the exact y * gs / S), rstd and, with a
+    residual, h."""
+    w_dtype = w_dtype or x_dtype
+    x = _check_in(x, x_dtype)
+    M, N = x.shape
+    gamma = _check_in(gamma, w_dtype, (N,))
+    if residual is not None:
+        residual = _check_in(residual, x_dtype, (M, N))
+    h = np.empty((M, N), _np(x_dtype)) if residual is not None else None
+    q = np.zeros((M, N // 2), np.uint8)
+    sf = np.empty((M, N // 16), np.uint8)
+    sfv64 = np.empty((M, N // 16), np.float64)
+    v64 = np.empty((M, N), np.float64)
+    rstd = np.empty(M, np.float32)
+    rc = _load().oracle_rmsnorm_fwd_nvfp4(_ptr(x), _ptr(residual), _ptr(gamma), M, N,
+                                          float(eps), float(gs), DTYPE_CODES[x_dtype],
+                                          DTYPE_CODES[w_dtype], _ptr(h), _ptr(q), _ptr(sf),
+                                          _ptr(sfv64), _ptr(v64), _ptr(rstd))
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_fwd_nvfp4 rejected its arguments")
+    out = {"q": q, "sf": sf, "sfv64": sfv64, "v64": v64, "rstd": rstd}
+    if h is not None:
+        out["h"] = h
+    return out
+
+
+def unpack_e2m1(q: np.ndarray) -> np.ndarray:
+    """[M, N/2] packed bytes -> [M, N] 4-bit codes (element 2k from the low nibble)."""
+    q = np.asarray(q, np.uint8)
+    out = np.empty(q.shape[:-1] + (q.shape[-1] * 2,), np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
     return out

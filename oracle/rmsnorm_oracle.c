@@ -21,6 +21,11 @@
  *                  dx_j     = r (gamma_j dy_j - x_j c),  c = r^2/N sum_k gamma_k dy_k x_k
  *                  dgamma_j = sum_rows dy_j x_j r
  *                with r the saved rstd when one is given.
+ *   quantised    the forward (and the fused add) with an FP8 E4M3 output and
+ *                one scale per row, or an NVFP4 output (FP4 E2M1 codes with an
+ *                E4M3 scale per 16 elements and a global scale); the pages name
+ *                these ops only, the formulas below each function are the
+ *                plain readings of those names.
  *
  * Every sum is a plain left-to-right double-precision loop; every stored
  * output is rounded once, from double, to its dtype (round to nearest even).
@@ -304,5 +309,193 @@ int oracle_rmsnorm_fwd_strided(const void* x, int64_t x_st, int64_t x_sh, const 
   }
   free(v);
   free(yr);
+  return 0;
+}
+
+/* ---- quantised outputs ----------------------------------------------------- */
+
+/* Nearest point of a small binary floating-point format to |v|, ties to the
+ * even significand.  The format has `mbits` fraction bits, minimum normal
+ * exponent `emin` (subnormals below 2^emin with spacing 2^(emin - mbits)) and
+ * largest finite magnitude `maxv`; larger magnitudes saturate to maxv. */
+static double round_small(double a, int mbits, int emin, double maxv) {
+  if (a == 0.0) return 0.0;
+  int k;
+  frexp(a, &k);
+  k -= 1;                                          /* 2^k <= a < 2^(k+1) */
+  if (k < emin) k = emin;
+  double ulp = ldexp(1.0, k - mbits);
+  double n = a / ulp;                              /* exact: ulp is a power of two */
+  double lo = floor(n), frac = n - lo, m = lo;
+  if (frac > 0.5) m = lo + 1.0;
+  else if (frac == 0.5) m = (fmod(lo, 2.0) == 0.0) ? lo : lo + 1.0;
+  double r = m * ulp;
+  return r > maxv ? maxv : r;
+}
+
+/* Code of a magnitude that round_small returned: subnormals (below 2^emin)
+ * have exponent field 0 and fraction r / 2^(emin - mbits); normals have
+ * exponent field e - emin + 1 for r in [2^e, 2^(e+1)). */
+static unsigned small_code(double r, int mbits, int emin) {
+  if (r < ldexp(1.0, emin)) return (unsigned)(r / ldexp(1.0, emin - mbits));
+  int e;
+  frexp(r, &e);
+  e -= 1;
+  unsigned frac = (unsigned)(r / ldexp(1.0, e - mbits)) - (1u << mbits);
+  return ((unsigned)(e - emin + 1) << mbits) | frac;
+}
+
+/* FP8 E4M3 (the "fn" flavour: no infinities): sign, 4 exponent bits (bias 7),
+ * 3 fraction bits; normals from 2^-6 to 448 = 1.75 * 2^8, subnormals with
+ * spacing 2^-9; codes 0x7F and 0xFF are NaN.  Nearest, ties to even;
+ * magnitudes above 448 saturate to 448 (finite-saturating conversion);
+ * NaN gives 0x7F. */
+uint8_t oracle_round_e4m3(double v) {
+  if (v != v) return 0x7F;
+  unsigned s = signbit(v) ? 0x80u : 0u;
+  double r = round_small(fabs(v), 3, -6, 448.0);
+  return (uint8_t)(s | small_code(r, 3, -6));
+}
+
+double oracle_e4m3_to_double(uint8_t c) {
+  unsigned e = (c >> 3) & 0xF, f = c & 7;
+  if (e == 0xF && f == 7) return NAN;
+  double m = e == 0 ? ldexp((double)f, -9) : ldexp(1.0 + f / 8.0, (int)e - 7);
+  return (c & 0x80) ? -m : m;
+}
+
+/* FP4 E2M1: sign, 2 exponent bits (bias 1), 1 fraction bit: magnitudes 0,
+ * 0.5, 1, 1.5, 2, 3, 4, 6.  Nearest, ties to the even code; magnitudes above
+ * 6 saturate to 6. */
+uint8_t oracle_round_e2m1(double v) {
+  unsigned s = signbit(v) ? 0x8u : 0u;
+  double r = round_small(fabs(v), 1, 0, 6.0);
+  return (uint8_t)(s | small_code(r, 1, 0));
+}
+
+double oracle_e2m1_to_double(uint8_t c) {
+  unsigned e = (c >> 1) & 3, f = c & 1;
+  double m = e == 0 ? 0.5 * f : ldexp(1.0 + f / 2.0, (int)e - 1);
+  return (c & 0x8) ? -m : m;
+}
+
+/* Row i of the normalised input: x, or (residual given) the stored sum
+ * h = residual + x rounded to x_dtype, also written to h_out if non-NULL. */
+static void quant_row_input(const void* x, const void* residual, int x_dtype, int64_t i,
+                            int64_t N, void* h_out, void* hr, double* v) {
+  for (int64_t j = 0; j < N; ++j) {
+    if (!residual) {
+      v[j] = load(x, x_dtype, i * N + j);
+      continue;
+    }
+    double sum = load(residual, x_dtype, i * N + j) + load(x, x_dtype, i * N + j);
+    store(hr, x_dtype, j, sum);
+    v[j] = load(hr, x_dtype, j);
+    if (h_out) store(h_out, x_dtype, i * N + j, sum);
+  }
+}
+
+/* Forward with FP8 E4M3 output and one scale per row (token): the
+ * quantised-output norms named in "TIRx kernels", Kernels list
+ * (flashinfer.norm: rmsnorm_quant, fused_add_rmsnorm_quant).  With y the
+ * forward's output (of x, or of h = residual + x when residual is given):
+ *     s_i  = max_j |y_ij| / 448          (dequantisation scale, fp32)
+ *     q_ij = e4m3(y_ij / s_i)            so that y_ij ~ e4m3_value(q_ij) * s_i
+ * The code is decided on the fp32 value of the quotient (the exact quotient
+ * rounded to fp32, then to e4m3).  A row whose x * gamma is all zero gets
+ * s = 0 and q = 0 for any eps.  Outputs (each may be NULL): h (x_dtype), q
+ * (M x N codes), scale (fp32) and scale64 (double), v64 (the exact quotients
+ * y / s, M x N), rstd (fp32). */
+int oracle_rmsnorm_fwd_fp8(const void* x, const void* residual, const void* gamma, int64_t M,
+                           int64_t N, double eps, int x_dtype, int w_dtype, void* h, uint8_t* q,
+                           float* scale, double* scale64, double* v64, float* rstd) {
+  if (M < 0 || N <= 0 || bad_dtypes(x_dtype, w_dtype) || (M > 0 && (!x || !gamma)))
+    return -1;
+  double* v = (double*)malloc((size_t)N * sizeof(double));
+  double* yr = (double*)malloc((size_t)N * sizeof(double));
+  void* hr = malloc((size_t)N * 4);
+  if (!v || !yr || !hr) { free(v); free(yr); free(hr); return -1; }
+  for (int64_t i = 0; i < M; ++i) {
+    quant_row_input(x, residual, x_dtype, i, N, h, hr, v);
+    double r;
+    fwd_row(v, gamma, w_dtype, N, eps, &r, yr);
+    if (rstd) rstd[i] = (float)r;
+    double m = 0.0;
+    for (int64_t j = 0; j < N; ++j) m = fmax(m, fabs(v[j] * load(gamma, w_dtype, j)));
+    double amax = 0.0;
+    if (m > 0.0)
+      for (int64_t j = 0; j < N; ++j) amax = fmax(amax, fabs(yr[j]));
+    double s = amax / 448.0;
+    if (scale) scale[i] = (float)s;
+    if (scale64) scale64[i] = s;
+    for (int64_t j = 0; j < N; ++j) {
+      double quo = m > 0.0 ? yr[j] / s : 0.0;
+      if (v64) v64[i * N + j] = quo;
+      if (q) q[i * N + j] = oracle_round_e4m3((double)(float)quo);
+    }
+  }
+  free(v);
+  free(yr);
+  free(hr);
+  return 0;
+}
+
+/* Forward with NVFP4 output: the FP4 norms named in "TIRx kernels", Kernels
+ * list (flashinfer.norm: rmsnorm_fp4quant, add_rmsnorm_fp4quant; the format
+ * of flashinfer.quantization: nvfp4_quantize).  N is a multiple of 16 and
+ * every row splits into blocks of 16 consecutive elements; gs > 0 is the
+ * caller's global scale.  With y the forward's output, for block b:
+ *     a_b  = max |y| over the block
+ *     sf_b = e4m3(gs * a_b / 6)          S_b = its value
+ *     q_j  = e2m1(y_j * gs / S_b)        (0 when S_b = 0)
+ * so y_j ~ e2m1_value(q_j) * S_b / gs.  Both codes are decided on fp32
+ * values (the exact value rounded to fp32, then to the small format).
+ * Outputs (each may be NULL): h (x_dtype); q (M x N/2 bytes, two codes per
+ * byte, element 2k in the low nibble); sf (M x N/16 codes, row-major);
+ * sfv64 (the exact gs * a_b / 6, M x N/16); v64 (the exact y * gs / S_b,
+ * M x N); rstd (fp32). */
+int oracle_rmsnorm_fwd_nvfp4(const void* x, const void* residual, const void* gamma, int64_t M,
+                             int64_t N, double eps, double gs, int x_dtype, int w_dtype, void* h,
+                             uint8_t* q, uint8_t* sf, double* sfv64, double* v64, float* rstd) {
+  if (M < 0 || N <= 0 || N % 16 != 0 || !(gs > 0.0) || bad_dtypes(x_dtype, w_dtype) ||
+      (M > 0 && (!x || !gamma)))
+    return -1;
+  double* v = (double*)malloc((size_t)N * sizeof(double));
+  double* yr = (double*)malloc((size_t)N * sizeof(double));
+  void* hr = malloc((size_t)N * 4);
+  if (!v || !yr || !hr) { free(v); free(yr); free(hr); return -1; }
+  const int64_t nb = N / 16;
+  for (int64_t i = 0; i < M; ++i) {
+    quant_row_input(x, residual, x_dtype, i, N, h, hr, v);
+    double r;
+    fwd_row(v, gamma, w_dtype, N, eps, &r, yr);
+    if (rstd) rstd[i] = (float)r;
+    for (int64_t b = 0; b < nb; ++b) {
+      double m = 0.0, a = 0.0;
+      for (int64_t j = 16 * b; j < 16 * b + 16; ++j) {
+        m = fmax(m, fabs(v[j] * load(gamma, w_dtype, j)));
+        a = fmax(a, fabs(yr[j]));
+      }
+      if (m == 0.0) a = 0.0;                       /* all-zero block: a = 0 for any eps */
+      double sfv = gs * a / 6.0;
+      uint8_t code = oracle_round_e4m3((double)(float)sfv);
+      double S = oracle_e4m3_to_double(code);
+      if (sf) sf[i * nb + b] = code;
+      if (sfv64) sfv64[i * nb + b] = sfv;
+      for (int64_t j = 16 * b; j < 16 * b + 16; ++j) {
+        double quo = S > 0.0 ? yr[j] * gs / S : 0.0;
+        uint8_t c = oracle_round_e2m1((double)(float)quo);
+        if (v64) v64[i * N + j] = quo;
+        if (q) {
+          uint8_t* byte = &q[(i * N + j) / 2];
+          if (j % 2 == 0) *byte = c;
+          else *byte = (uint8_t)(*byte | (c << 4));
+        }
+      }
+    }
+  }
+  free(v);
+  free(yr);
+  free(hr);
   return 0;
 }
