@@ -56,6 +56,11 @@ def alg_bytes(wl, rows=None) -> int:
         return M * N * 4 * sx + N * sw + rstd
     if wl.op == "fused_add_bwd":   # h, dy, dres in; dh out; dgamma in the weight dtype
         return M * N * 4 * sx + 4 * M + N * sw + N * sw
+    if wl.op in ("fwd_fp8", "fused_add_fp8", "fwd_nvfp4", "fused_add_nvfp4"):
+        # x (fused: r and x in, h out), then codes and scales out
+        act = M * N * (3 if wl.op.startswith("fused") else 1) * sx
+        codes = M * N + 4 * M if "fp8" in wl.op else M * N // 2 + M * N // 16
+        return act + codes + N * sw + rstd
     return M * N * 3 * sx + 4 * M + N * sw + 4 * N
 
 
@@ -503,7 +508,8 @@ def run_reference(args):
 # ------------------------------------------------------------------ sweep
 
 def _op_code(op):
-    return {"fwd": 0, "fused_add": 1, "bwd": 2, "fused_add_bwd": 3, "fwd_strided": 4}[op]
+    return {"fwd": 0, "fused_add": 1, "bwd": 2, "fused_add_bwd": 3, "fwd_strided": 4,
+            "fwd_fp8": 5, "fused_add_fp8": 6, "fwd_nvfp4": 7, "fused_add_nvfp4": 8}[op]
 
 
 def device_sets(wl, inp, dev, l2_bytes, rn):
@@ -520,7 +526,13 @@ def device_sets(wl, inp, dev, l2_bytes, rn):
     sets = []
     for _ in range(nsets):
         d = {k: v.to(dev) for k, v in host.items()}
-        if wl.op != "fwd_strided":   # the strided forward writes in place
+        if "fp8" in wl.op:
+            d["q"] = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            d["qs"] = torch.empty(M, dtype=torch.float32, device=dev)
+        elif "nvfp4" in wl.op:
+            d["q"] = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+            d["qs"] = torch.empty((M, N // 16), dtype=torch.uint8, device=dev)
+        elif wl.op != "fwd_strided":   # the strided forward writes in place
             d["y"] = torch.empty((M, N), dtype=act, device=dev)
         d["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
         if wl.op == "bwd":
@@ -543,6 +555,15 @@ def make_launch(wl, d, stream, rn):
         return lambda: rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], d["y"],
                                                 d["rstd"] if wl.store_rstd else None, M, N,
                                                 eps, wl.x_dtype, wl.w_dtype, stream)
+    if "fp8" in wl.op:
+        return lambda: rn.rmsnorm_fwd_fp8(d["x"], d.get("residual"), d["gamma"], d["q"], d["qs"],
+                                          d["rstd"] if wl.store_rstd else None, M, N, eps,
+                                          wl.x_dtype, wl.w_dtype, stream)
+    if "nvfp4" in wl.op:
+        return lambda: rn.rmsnorm_fwd_nvfp4(d["x"], d.get("residual"), d["gamma"],
+                                            wl.global_scale, d["q"], d["qs"],
+                                            d["rstd"] if wl.store_rstd else None, M, N, eps,
+                                            wl.x_dtype, wl.w_dtype, stream)
     if wl.op == "fwd_strided":   # the q slice of each token, normalised in place
         st, H = wl.stride_token, wl.heads
         return lambda: rn.rmsnorm_fwd_strided(d["x"], st, N, d["gamma"], d["x"], st, N,

@@ -100,6 +100,47 @@ rmsnorm_status_t rmsnorm_fwd_strided(const void* x, int64_t x_stride_token,
                                      cudaStream_t stream);
 
 /*
+ * Forward with FP8 output and one scale per row (token): the quantised-output
+ * norms named in "TIRx kernels", Kernels list (flashinfer.norm: rmsnorm_quant,
+ * fused_add_rmsnorm_quant).  The pages give the names only; this is the plain
+ * reading.  With y the forward's output (of x, or, when residual is not
+ * NULL, of h = residual + x rounded to x_dtype and written over residual as
+ * in rmsnorm_fused_add_fwd):
+ *     scale_i = max_j |y_ij| / 448            fp32, the dequantisation scale
+ *     q_ij    = e4m3(y_ij / scale_i)          so y_ij ~ e4m3_value(q_ij) * scale_i
+ * e4m3: OCP FP8 E4M3 (no infinities, largest finite 448), round to nearest
+ * even, saturating.  A row whose x * gamma (h * gamma) is all zero gets
+ * scale 0 and codes 0 for any eps.  x: M x N (x_dtype); residual: M x N or
+ * NULL; gamma: N (w_dtype); q: M x N bytes; scale: M fp32; rstd: M fp32 or
+ * NULL.  Buffers must not overlap.  Rows that are 16-byte aligned with q
+ * 8-byte aligned take the vectorised kernels; any other layout a scalar one.
+ */
+rmsnorm_status_t rmsnorm_fwd_fp8(const void* x, void* residual, const void* gamma, void* q,
+                                 float* scale, float* rstd, int64_t M, int64_t N, float eps,
+                                 rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                                 cudaStream_t stream);
+
+/*
+ * Forward with NVFP4 output: the FP4 norms named in "TIRx kernels", Kernels
+ * list (flashinfer.norm: rmsnorm_fp4quant, add_rmsnorm_fp4quant; the format
+ * of flashinfer.quantization: nvfp4_quantize).  Plain reading of the names:
+ * N must be a multiple of 16; each row splits into blocks of 16 consecutive
+ * elements; global_scale (gs) is the caller's per-tensor scale, finite and
+ * > 0.  With y as in rmsnorm_fwd_fp8, for block b:
+ *     S_b = e4m3(gs * max_b |y| / 6)          stored in block_scale
+ *     q_j = e2m1(y_j * gs / S_b)              (0 when S_b = 0)
+ * so y_j ~ e2m1_value(q_j) * S_b / gs.  e2m1: FP4 E2M1 (0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6), round to nearest even, saturating.  q: M x N/2 bytes, two codes
+ * per byte, element 2k in the low nibble; block_scale: M x N/16 E4M3 bytes,
+ * row-major (the plain layout, not a tensor-core swizzle).  Other arguments
+ * and the fused residual add as in rmsnorm_fwd_fp8.
+ */
+rmsnorm_status_t rmsnorm_fwd_nvfp4(const void* x, void* residual, const void* gamma,
+                                   float global_scale, void* q, void* block_scale, float* rstd,
+                                   int64_t M, int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                                   rmsnorm_dtype_t w_dtype, cudaStream_t stream);
+
+/*
  * Workspace of rmsnorm_bwd, in bytes, for these sizes on `device` (-1: the
  * current device).  It depends on the device's SM count.  Writes *bytes
  * (0 when M == 0 or no dgamma is wanted is still a valid answer to pass).
@@ -213,7 +254,8 @@ const char* rmsnorm_status_string(rmsnorm_status_t status);
  * The kernel variant the library would launch for this call shape, as text
  * (for example "fwd/cta/vpt4/t256"), into buf (NUL-terminated, truncated to
  * len).  op: 0 forward, 1 fused add, 2 backward, 3 fused-add backward,
- * 4 strided forward (M = tokens x heads rows of N = D elements).  aligned16:
+ * 4 strided forward (M = tokens x heads rows of N = D elements), 5 FP8
+ * forward, 6 fused-add FP8 forward, 7 NVFP4 forward, 8 fused-add NVFP4.  aligned16:
  * nonzero when all operand base pointers (and, for op 4, all strides) are
  * 16-byte aligned.  Returns RMSNORM_OK or an argument error; launches
  * nothing.

@@ -16,6 +16,8 @@ import os
 import threading
 
 __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "OP_FUSED_ADD_BWD", "RMSNormError",
+           "OP_FWD_STRIDED", "OP_FWD_FP8", "OP_FUSED_ADD_FP8", "OP_FWD_NVFP4",
+           "OP_FUSED_ADD_NVFP4", "rmsnorm_fwd_fp8", "rmsnorm_fwd_nvfp4",
            "library_path", "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided",
            "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
@@ -25,12 +27,14 @@ __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "OP_FUSED_ADD_BWD"
 F32 = 0
 BF16 = 1
 OP_FWD, OP_FUSED_ADD, OP_BWD, OP_FUSED_ADD_BWD = 0, 1, 2, 3
+OP_FWD_STRIDED, OP_FWD_FP8, OP_FUSED_ADD_FP8, OP_FWD_NVFP4, OP_FUSED_ADD_NVFP4 = 4, 5, 6, 7, 8
 _DT_NAMES = {"f32": F32, "bf16": BF16}
 
 EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspace_size",
                     "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan",
                     "rmsnorm_bwd_noalloc", "rmsnorm_check_device", "rmsnorm_last_error",
-                    "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided")
+                    "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided", "rmsnorm_fwd_fp8",
+                    "rmsnorm_fwd_nvfp4")
 
 # Size of the library-owned scratch of rmsnorm_bwd_noalloc (16 MiB).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -84,6 +88,10 @@ def load_library():
             lib.rmsnorm_fwd_strided.argtypes = [P, I64, I64, P, P, I64, I64, P, I64, I64, I64, F,
                                                 I, I, P]
             lib.rmsnorm_fwd_strided.restype = I
+            lib.rmsnorm_fwd_fp8.argtypes = [P, P, P, P, P, P, I64, I64, F, I, I, P]
+            lib.rmsnorm_fwd_fp8.restype = I
+            lib.rmsnorm_fwd_nvfp4.argtypes = [P, P, P, F, P, P, P, I64, I64, F, I, I, P]
+            lib.rmsnorm_fwd_nvfp4.restype = I
             lib.rmsnorm_last_error.argtypes = []
             lib.rmsnorm_last_error.restype = ctypes.c_char_p
             _lib = lib
@@ -153,6 +161,23 @@ def rmsnorm_fwd_strided(x, x_stride_token, x_stride_head, gamma, y, y_stride_tok
                                               y_stride_head, _ptr(rstd), T, H, D, eps,
                                               _dt(x_dtype), _dt(w_dtype), _stream(stream)),
            "rmsnorm_fwd_strided")
+
+
+def rmsnorm_fwd_fp8(x, residual, gamma, q, scale, rstd, M, N, eps, x_dtype, w_dtype,
+                    stream=None):
+    _check(load_library().rmsnorm_fwd_fp8(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(q),
+                                          _ptr(scale), _ptr(rstd), M, N, eps, _dt(x_dtype),
+                                          _dt(w_dtype), _stream(stream)),
+           "rmsnorm_fwd_fp8")
+
+
+def rmsnorm_fwd_nvfp4(x, residual, gamma, global_scale, q, block_scale, rstd, M, N, eps,
+                      x_dtype, w_dtype, stream=None):
+    _check(load_library().rmsnorm_fwd_nvfp4(_ptr(x), _ptr(residual), _ptr(gamma),
+                                            float(global_scale), _ptr(q), _ptr(block_scale),
+                                            _ptr(rstd), M, N, eps, _dt(x_dtype), _dt(w_dtype),
+                                            _stream(stream)),
+           "rmsnorm_fwd_nvfp4")
 
 
 def rmsnorm_fused_add_bwd(dy, h, rstd, gamma, dres, dgamma, dgamma_dtype, workspace,

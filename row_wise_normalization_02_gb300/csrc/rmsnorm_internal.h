@@ -25,6 +25,10 @@ enum DT : int { kF32 = 0, kBF16 = 1 };
 //             rows per CTA are in flight independently of register pressure.
 enum Family : int { kSubwarp = 0, kCta = 1, kRagged = 2, kGeneric = 3, kStaged = 4 };
 
+// Forward output kinds: y in the activation dtype, FP8 E4M3 codes with one
+// scale per row, or NVFP4 (E2M1 codes, an E4M3 scale per 16 elements).
+enum OutKind : int { kOutDtype = 0, kOutFp8 = 1, kOutNvfp4 = 2 };
+
 // Shared-memory header of the staged kernels: barriers, reduction scratch
 // and the error flag; the ring of row buffers starts after it.
 constexpr int kStagedMaxStages = 8;
@@ -51,6 +55,11 @@ struct FwdParams {
   // starts at element t * x_st + h * x_sh of x and t * y_st + h * y_sh of y
   int64_t heads;
   int64_t x_st, x_sh, y_st, y_sh;
+  // quantised outputs: y holds the codes (E4M3 bytes, or E2M1 pairs), qs the
+  // scales (fp32 per row for E4M3; E4M3 per 16 elements for NVFP4), gs the
+  // NVFP4 global scale
+  void* qs;
+  float gs;
 };
 
 struct BwdParams {
@@ -86,6 +95,7 @@ struct FwdKey {
   bool fused;
   bool prefetch; // issue the next row's loads before reducing the current row
   bool strided;  // rows addressed through (heads, x_st, x_sh, y_st, y_sh)
+  int out = kOutDtype;   // output kind (kOut*)
 };
 
 struct BwdKey {
@@ -119,6 +129,9 @@ FwdKernel get_fwd_ragged_bf16_f32(const FwdKey& k);
 BwdKernel get_bwd_ragged_f32_f32(const BwdKey& k);
 BwdKernel get_bwd_ragged_bf16_bf16(const BwdKey& k);
 BwdKernel get_bwd_ragged_bf16_f32(const BwdKey& k);
+FwdKernel get_fwd_quant_f32_f32(const FwdKey& k);
+FwdKernel get_fwd_quant_bf16_bf16(const FwdKey& k);
+FwdKernel get_fwd_quant_bf16_f32(const FwdKey& k);
 ReduceKernel get_dgamma_reduce_kernel();
 
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.

@@ -15,7 +15,8 @@ TENSOR_IDS = {"x": 1, "residual": 2, "gamma": 3, "dy": 4}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "fwd", "fused_add", "bwd", "fused_add_bwd", "fwd_strided"
+    op: str                 # "fwd", "fused_add", "bwd", "fused_add_bwd", "fwd_strided",
+                            # "fwd_fp8", "fused_add_fp8", "fwd_nvfp4", "fused_add_nvfp4"
     M: int
     N: int
     x_dtype: str            # "f32" | "bf16"
@@ -29,6 +30,7 @@ class Workload:
     tags: tuple = field(default_factory=tuple)
     heads: int = 0          # strided rows: M = tokens * heads, x is [tokens, stride_token]
     stride_token: int = 0
+    global_scale: float = 0.0   # NVFP4 outputs: the per-tensor scale gs
 
 
 def tensor_recipes(wl: Workload) -> dict:
@@ -39,7 +41,7 @@ def tensor_recipes(wl: Workload) -> dict:
     rec = {"x": act, "gamma": g}
     if wl.op == "fwd_strided":
         rec["x"] = dict(act, shape=(wl.M // wl.heads, wl.stride_token))
-    if wl.op == "fused_add":
+    if wl.op.startswith("fused_add") and wl.op != "fused_add_bwd":
         rec["residual"] = dict(act)
     if wl.op in ("bwd", "fused_add_bwd"):
         rec["dy"] = dict(dist="normal", p0=0.0, p1=1.0, dtype=wl.x_dtype)
@@ -74,6 +76,25 @@ WORKLOADS = {
                                            32768 * 32, 128, "bf16", "bf16", 1e-6, 5,
                                            store_rstd=False, heads=32, stride_token=6144,
                                            tags=("next",)),
+    # quantised outputs at the forward and fused-add shapes (same inputs):
+    # FP8 E4M3 with a scale per row; NVFP4 with E4M3 scales per 16 elements
+    # and a global scale sized for |y| up to 8 (forward) or 128 (fused add,
+    # whose outliers reach |y| ~ 70): gs = 448 * 6 / that bound
+    "fwd_fp8_bf16_m16384_n8192": Workload("fwd_fp8_bf16_m16384_n8192", "fwd_fp8", 16384, 8192,
+                                          "bf16", "bf16", 1e-5, 1, store_rstd=False,
+                                          tags=("next",)),
+    "fwd_nvfp4_bf16_m16384_n8192": Workload("fwd_nvfp4_bf16_m16384_n8192", "fwd_nvfp4", 16384,
+                                            8192, "bf16", "bf16", 1e-5, 1, store_rstd=False,
+                                            global_scale=448.0 * 6 / 8, tags=("next",)),
+    "fadd_fp8_bf16_m32768_n4096": Workload("fadd_fp8_bf16_m32768_n4096", "fused_add_fp8", 32768,
+                                           4096, "bf16", "bf16", 1e-6, 2, store_rstd=False,
+                                           outlier_fraction=1e-3, outlier_scale=100.0,
+                                           tags=("next",)),
+    "fadd_nvfp4_bf16_m32768_n4096": Workload("fadd_nvfp4_bf16_m32768_n4096", "fused_add_nvfp4",
+                                             32768, 4096, "bf16", "bf16", 1e-6, 2,
+                                             store_rstd=False, outlier_fraction=1e-3,
+                                             outlier_scale=100.0, global_scale=448.0 * 6 / 128,
+                                             tags=("next",)),
     # backward: bf16 activations, fp32 gamma; rstd from the oracle forward
     "bwd_bf16_m16384_n8192": Workload("bwd_bf16_m16384_n8192", "bwd", 16384, 8192, "bf16",
                                       "f32", 1e-5, 3, tags=("headline",)),

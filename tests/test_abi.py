@@ -107,6 +107,35 @@ def test_strided_argument_errors_without_gpu(lib, args, status):
     assert e.value.status == status
 
 
+@pytest.mark.parametrize("kind,args,status", [
+    ("nvfp4", dict(N=72), 1),                    # N not a multiple of 16
+    ("nvfp4", dict(gs=0.0), 1), ("nvfp4", dict(gs=-2.0), 1), ("nvfp4", dict(gs=float("inf")), 1),
+    ("nvfp4", dict(gs=float("nan")), 1),
+    ("fp8", dict(q=None), 1), ("fp8", dict(qs=None), 1), ("nvfp4", dict(x=None), 1),
+    ("fp8", dict(qs=FAKE + (4 << 32) + 2), 3),   # fp32 scales not 4-byte aligned
+    ("fp8", dict(x=FAKE + 1), 3),
+    ("fp8", dict(q=FAKE + 64), 1),               # codes overlap x
+    ("nvfp4", dict(qs=FAKE + (3 << 32) + 8), 1),  # scales overlap the codes
+    ("fp8", dict(residual=FAKE + 128), 1),       # residual overlaps x
+    ("fp8", dict(x_dtype=rn.F32, w_dtype=rn.BF16), 2),
+    ("nvfp4", dict(M=-1), 1), ("fp8", dict(eps=-1.0), 1),
+])
+def test_quantised_argument_errors_without_gpu(lib, kind, args, status):
+    a = dict(x=FAKE, residual=None, gamma=FAKE + (1 << 32), q=FAKE + (3 << 32),
+             qs=FAKE + (4 << 32), gs=6.0, rstd=None, M=4, N=64, eps=1e-6, x_dtype=rn.BF16,
+             w_dtype=rn.BF16)
+    a.update(args)
+    with pytest.raises(rn.RMSNormError) as e:
+        if kind == "fp8":
+            rn.rmsnorm_fwd_fp8(a["x"], a["residual"], a["gamma"], a["q"], a["qs"], a["rstd"],
+                               a["M"], a["N"], a["eps"], a["x_dtype"], a["w_dtype"])
+        else:
+            rn.rmsnorm_fwd_nvfp4(a["x"], a["residual"], a["gamma"], a["gs"], a["q"], a["qs"],
+                                 a["rstd"], a["M"], a["N"], a["eps"], a["x_dtype"],
+                                 a["w_dtype"])
+    assert e.value.status == status
+
+
 def test_zero_rows_is_a_no_op(lib):
     # M == 0: nothing to do, no pointer is touched and no CUDA call is made
     rn.rmsnorm_fwd(None, None, None, None, 0, 64, 1e-5, rn.BF16, rn.BF16)
@@ -115,6 +144,8 @@ def test_zero_rows_is_a_no_op(lib):
     assert rn.rmsnorm_bwd_workspace_size(0, 64, rn.BF16, rn.BF16) == 0
     rn.rmsnorm_fwd_strided(None, 0, 0, None, None, 0, 0, None, 0, 8, 128, 1e-6, rn.BF16,
                            rn.BF16)
+    rn.rmsnorm_fwd_fp8(None, None, None, None, None, None, 0, 64, 1e-6, rn.BF16, rn.BF16)
+    rn.rmsnorm_fwd_nvfp4(None, None, None, 1.0, None, None, None, 0, 64, 1e-6, rn.BF16, rn.BF16)
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
