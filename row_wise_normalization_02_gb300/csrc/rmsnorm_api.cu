@@ -224,8 +224,8 @@ void subwarp_shape(int nvec, int* g, int* vpt) {
 }
 
 // Vectors per thread for a row of nvec vectors in one CTA, and the CTA size.
-// op kQuantFwd: the quantised plain forward, whose longer epilogue is best
-// with more vectors per thread (measured at 16384 x 8192 bf16).
+// op kQuantFwd: the quantised forwards, whose longer epilogues are best with
+// more vectors per thread (measured at 16384 x 8192 and 32768 x 4096 bf16).
 constexpr int kQuantFwd = 100;
 bool cta_shape(int op, int nvec, int* vpt, int* threads) {
   static const int pref_fwd[] = {2, 4, 8, 1};
@@ -726,8 +726,11 @@ rmsnorm_status_t fwd_strided_impl(const void* x, int64_t x_st, int64_t x_sh, con
 // stored a vector at a time; anything else the scalar kernel.  Every shape
 // issues the next row's loads before reducing the current one (register
 // prefetch): the epilogue is long enough that without it too few bytes stay
-// in flight (16384 x 8192 bf16 FP8: 0.62 -> 0.87 of the copy bandwidth;
-// 32768 x 4096 fused add: 0.94-0.97 -> 0.97-1.0).
+// in flight (16384 x 8192 bf16 FP8: 0.62 -> 0.85 of the copy bandwidth;
+// 32768 x 4096 fused add: 0.94-0.96 -> 0.97-0.99).  The staged form (rows
+// through the bulk-copy ring) is available as a forced variant; it measured
+// no better here (0.83 / 0.67 plain, 0.93 / 0.79 fused), the kernels being
+// bound by instruction issue rather than by bytes in flight.
 rmsnorm_status_t quant_plan(int out, bool fused, int64_t N, int xd, int wd, bool vec_ok,
                             Plan* res) {
   const int nvec = vec_ok ? (int)(N / per_vec(xd)) : 0;
@@ -738,7 +741,7 @@ rmsnorm_status_t quant_plan(int out, bool fused, int64_t N, int xd, int wd, bool
     p.threads = kSubwarpThreads;
     p.rows_per_cta = kSubwarpThreads / p.g;
     p.prefetch = true;
-  } else if (vec_ok && cta_shape(fused ? kFused : kQuantFwd, nvec, &p.vpt, &p.threads)) {
+  } else if (vec_ok && cta_shape(kQuantFwd, nvec, &p.vpt, &p.threads)) {
     p.family = kCta;
     p.prefetch = p.vpt <= 4;
   } else {
@@ -767,11 +770,21 @@ rmsnorm_status_t quant_plan(int out, bool fused, int64_t N, int xd, int wd, bool
           (int64_t)p.threads * p.vpt < nvec)
         return RMSNORM_ERR_INVALID_ARG;
       p.rows_per_cta = 1;
+    } else if (f.family == kStaged) {
+      if (!vec_ok) return RMSNORM_ERR_INVALID_ARG;
+      p.family = kStaged;
+      p.vpt = f.vpt ? f.vpt : 4;
+      p.threads = f.threads ? f.threads : round_up((nvec + p.vpt - 1) / p.vpt, 32);
+      if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32 ||
+          (int64_t)p.threads * p.vpt < nvec)
+        return RMSNORM_ERR_INVALID_ARG;
+      p.stages = f.st;
+      p.rows_per_cta = 1;
     } else if (f.family >= 0) {
       return RMSNORM_ERR_INVALID_ARG;
     }
     if (f.pf >= 0) p.prefetch = f.pf != 0;
-    if (p.family == kGeneric) p.prefetch = false;
+    if (p.family == kGeneric || p.family == kStaged) p.prefetch = false;
     p.cta_per_sm_cap = f.cps;
   }
   FwdKey k{xd, wd, p.family, p.g, p.vpt, fused, p.prefetch, false, out};
@@ -779,6 +792,20 @@ rmsnorm_status_t quant_plan(int out, bool fused, int64_t N, int xd, int wd, bool
   p.fn = reinterpret_cast<const void*>(p.fwd);
   p.smem = 0;
   if (p.fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
+  if (p.family == kStaged) {
+    // ring of row buffers ([x], or [r | x] fused): as many stages as fit the
+    // half-SM budget (two CTAs per SM), at least two, at most kStagedMaxStages
+    const int64_t stage_bytes = (fused ? 2 : 1) * N * esize(xd);
+    if (p.stages <= 0) {
+      int64_t st = (kStagedSmemBudget - kStagedHeader) / stage_bytes;
+      if (st < 2) st = (kStagedSmemMax - kStagedHeader) / stage_bytes;
+      p.stages = (int)(st > kStagedMaxStages ? kStagedMaxStages : st);
+    }
+    if (p.stages < 2 || p.stages > kStagedMaxStages ||
+        kStagedHeader + p.stages * stage_bytes > kStagedSmemMax)
+      return RMSNORM_ERR_INVALID_ARG;
+    p.smem = (int)(kStagedHeader + p.stages * stage_bytes);
+  }
   *res = p;
   return RMSNORM_OK;
 }
@@ -816,13 +843,17 @@ rmsnorm_status_t fwd_quant_impl(int out, const void* x, void* residual, const vo
     return st;
   int dev;
   if ((st = current_device(&dev)) != RMSNORM_OK) return st;
-  if ((st = size_grid(&p, M, dev)) != RMSNORM_OK) return st;
+  unsigned* status = nullptr;
+  if ((st = size_grid(&p, M, dev, &status)) != RMSNORM_OK) return st;
 
   FwdParams prm = {};
   prm.x = x;
   prm.residual = residual;
   prm.gamma = gamma;
   prm.y = q;
+  prm.stages = p.stages;
+  prm.wait_limit = wait_limit();
+  prm.status = status;
   prm.rstd = rstd;
   prm.M = M;
   prm.N = (int)N;

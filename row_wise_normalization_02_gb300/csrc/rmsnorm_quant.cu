@@ -27,12 +27,15 @@
 // a 128-entry table each CTA builds once (no division per block).  The lane
 // holding the block's first vector writes its scale byte.  The ALU work per
 // element is then unpack, one multiply, one max, one multiply and half a
-// conversion, which the HBM rate leaves room for.
+// conversion; the multiplies, the sum of squares and the fused add run as
+// paired fp32 instructions and the maxima as three-input max, which keeps the
+// kernel under the issue rate the HBM stream allows.
 //
 // Conversions use the sm_100-family cvt.rn.satfinite forms (round to nearest
 // even, saturate to the largest finite value), which are the reading's
 // rounding.  An all-zero row (FP8) or block (NVFP4) gives scale 0 and codes 0.
 #include "rmsnorm_fwd_common.cuh"
+#include "rmsnorm_ring.cuh"
 
 #ifndef RMSN_PAIR
 #error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
@@ -154,6 +157,90 @@ __device__ __forceinline__ void cta_sum_max(float& s, float& m, float* red, int 
   m = tm;
 }
 
+// Maximum of three values (the sm_100-family three-input form).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two bf16 values packed in x_word against the two in g_word, with the
+// mixed-precision FMA (bf16 sources, fp32 result, one rounding): the products
+// x * g, exact in fp32 (the addend -0 keeps the sign of a zero product), and
+// acc += x * x for each.  No unpacking of either operand.
+__device__ __forceinline__ void bf16_pair_products(uint32_t x_word, uint32_t g_word, float& p0,
+                                                   float& p1, float& acc) {
+  asm("{\n\t.reg .b16 xl, xh, gl, gh;\n\t"
+      "mov.b32 {xl, xh}, %3;\n\t"
+      "mov.b32 {gl, gh}, %4;\n\t"
+      "fma.rn.f32.bf16 %0, xl, gl, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %1, xh, gh, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %2, xl, xl, %2;\n\t"
+      "fma.rn.f32.bf16 %2, xh, xh, %2;\n\t}"
+      : "=f"(p0), "=f"(p1), "+f"(acc)
+      : "r"(x_word), "r"(g_word));
+}
+
+// One pass over a thread's slice of the row, in pairs of elements with the
+// paired fp32 instructions (each lane rounds exactly as the scalar op):
+// fused add: h = round(r + x), stored over the residual; then the products
+// p = x * gamma (kept for the epilogue), the maximum |p| of every vector, and
+// the sum of squares of x in two partial sums added at the end.  bf16 x and
+// gamma skip the unpacking: products and squares come from the packed words
+// through the mixed-precision FMA.
+template <typename TX, typename TW, int VPT, bool FUSED, int E = Cfg<TX, TW>::E,
+          int GW = Cfg<TX, TW>::GW>
+__device__ __forceinline__ float quant_row_pass(Slice<VPT, FUSED>& s, const uint4 (&gw)[VPT][GW],
+                                                float2 (&pr)[VPT][E / 2], float (&vmax)[VPT],
+                                                char* hrow, int lane, int L, int nvec,
+                                                bool valid) {
+  float2 acc = make_float2(0.f, 0.f);
+  float acc1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    float f[E], g[E];
+    unpack(s.x[k], f);
+    if constexpr (FUSED) {
+      float rf[E];
+      unpack(s.r[k], rf);
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) {
+        const float2 t = __fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]),
+                                    make_float2(rf[2 * i], rf[2 * i + 1]));
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+      }
+      s.x[k] = pack(f);   // rounds to TX (nearest even)
+      unpack(s.x[k], f);  // the stored h, exactly
+      const int v = lane + k * L;
+      if (valid && v < nvec) st_stream(hrow + (size_t)v * 16, s.x[k]);
+    }
+    float m = 0.f;
+    if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
+      const uint32_t xw[4] = {s.x[k].x, s.x[k].y, s.x[k].z, s.x[k].w};
+      const uint32_t gwd[4] = {gw[k][0].x, gw[k][0].y, gw[k][0].z, gw[k][0].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float p0, p1;
+        bf16_pair_products(xw[i], gwd[i], p0, p1, acc1);
+        pr[k][i] = make_float2(p0, p1);
+        m = max3(m, fabsf(p0), fabsf(p1));
+      }
+    } else {
+      unpack_gamma<TW, E, GW>(gw[k], g);
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) {
+        const float2 x2 = make_float2(f[2 * i], f[2 * i + 1]);
+        acc = __ffma2_rn(x2, x2, acc);
+        pr[k][i] = __fmul2_rn(x2, make_float2(g[2 * i], g[2 * i + 1]));
+        m = max3(m, fabsf(pr[k][i].x), fabsf(pr[k][i].y));
+      }
+    }
+    vmax[k] = m;
+  }
+  return acc.x + acc.y + acc1;
+}
+
 // ---------------------------------------------------------------------------
 // Aligned rows: G lanes per row (G in 4..32, 256 / G rows per CTA iteration)
 // or, with G = 0, the whole CTA per row; persistent grid, gamma in registers.
@@ -203,18 +290,15 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
     const bool valid = row < p.M;
     const int64_t nrow = row + stride;
     if (PF) load_aligned<TX, VPT, FUSED>(nxt, p, nrow, nrow < p.M, lane, L);
-    float ss = slice_sumsq<TX, VPT, FUSED>(s, static_cast<char*>(p.residual) + row * rb, lane,
-                                           L, p.nvec, valid);
+    float2 pr[VPT][E / 2];
+    float vmax[VPT];
+    float ss = quant_row_pass<TX, TW, VPT, FUSED>(s, gw, pr, vmax,
+                                                  static_cast<char*>(p.residual) + row * rb,
+                                                  lane, L, p.nvec, valid);
     float mx = 0.f;
     if constexpr (OUT == kOutFp8) {
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        float f[E], g[E];
-        unpack(s.x[k], f);
-        unpack_gamma<TW, E, GW>(gw[k], g);
-#pragma unroll
-        for (int e = 0; e < E; ++e) mx = fmaxf(mx, fabsf(f[e] * g[e]));
-      }
+      for (int k = 0; k < VPT; ++k) mx = fmaxf(mx, vmax[k]);
     }
     if constexpr (G != 0) {
       ss = group_sum<G>(ss);
@@ -234,6 +318,7 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
 
     if constexpr (OUT == kOutFp8) {
       const float inv = mx > 0.f ? __fdiv_rn(448.f, mx) : 0.f;
+      const float2 inv2 = make_float2(inv, inv);
       if (valid && lane == 0)
         static_cast<float*>(p.qs)[row] = mx > 0.f ? __fdiv_rn(rs * mx, 448.f) : 0.f;
       char* qrow = static_cast<char*>(p.y) + row * (size_t)p.N;
@@ -241,12 +326,14 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
       for (int k = 0; k < VPT; ++k) {
         const int v = lane + k * L;
         if (valid && v < p.nvec) {
-          float f[E], g[E];
-          unpack(s.x[k], f);
-          unpack_gamma<TW, E, GW>(gw[k], g);
+          float o[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) f[e] = (f[e] * g[e]) * inv;
-          store_fp8(qrow + (size_t)v * E, f);
+          for (int i = 0; i < E / 2; ++i) {
+            const float2 t = __fmul2_rn(pr[k][i], inv2);
+            o[2 * i] = t.x;
+            o[2 * i + 1] = t.y;
+          }
+          store_fp8(qrow + (size_t)v * E, o);
         }
       }
     } else {
@@ -256,31 +343,202 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int v = lane + k * L;
-        float o[E], g[E];
-        unpack(s.x[k], o);
-        unpack_gamma<TW, E, GW>(gw[k], g);
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          o[e] = o[e] * g[e];
-          a = fmaxf(a, fabsf(o[e]));
-        }
+        float a = vmax[k];
         // every lane takes part: the block's other vectors are in lanes ^1 (^2)
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
         if constexpr (VB == 4) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
         // an all-zero block gets code 0 even when rstd is infinite (eps = 0)
         const uint32_t code = a > 0.f ? e4m3_code(a * rg6) : 0u;
         const float sc = rs * os_tab[code & 127u];
+        const float2 sc2 = make_float2(sc, sc);
         if (valid && v < p.nvec) {
           if (v % VB == 0) sfrow[v / VB] = (uint8_t)code;
+          float o[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) o[e] *= sc;
+          for (int i = 0; i < E / 2; ++i) {
+            const float2 t = __fmul2_rn(pr[k][i], sc2);
+            o[2 * i] = t.x;
+            o[2 * i + 1] = t.y;
+          }
           store_fp4(qrow + (size_t)v * (E / 2), o, code == 0u);
         }
       }
     }
     if (PF) s = nxt;
     else load_aligned<TX, VPT, FUSED>(s, p, nrow, nrow < p.M, lane, L);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Staged: one row per CTA iteration as above, but the rows ([x], or [r | x]
+// fused) arrive by bulk copies into the shared-memory ring of rmsnorm_ring.cuh,
+// `stages` rows ahead of the CTA, so the bytes in flight per SM are set by the
+// ring rather than by registers.  Every wait is bounded; a wait that runs out
+// is voted on at the reduction barrier, the CTA stores nothing for that row
+// and leaves, and thread 0 drains its copies and raises kStatusWaitTimeout.
+
+// cta_sum_max whose barrier also votes on `pred` (true in every thread when
+// true in any).
+__device__ __forceinline__ bool cta_sum_max_vote(float& s, float& m, float* red, int parity,
+                                                 bool pred) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  s = group_sum<32>(s);
+  m = group_max<32>(m);
+  float* buf = red + parity * 64;
+  if (lane == 0) {
+    buf[warp] = s;
+    buf[32 + warp] = m;
+  }
+  const bool any = __syncthreads_or(pred ? 1 : 0) != 0;
+  float ts = 0.f, tm = 0.f;
+  for (int w = 0; w < nwarps; ++w) {
+    ts += buf[w];
+    tm = fmaxf(tm, buf[32 + w]);
+  }
+  s = ts;
+  m = tm;
+  return any;
+}
+
+template <typename TX, typename TW, int VPT, bool FUSED, int OUT>
+__global__ void __launch_bounds__(kCtaMaxThreads) fwd_quant_staged_kernel(const FwdParams p) {
+  pdl_begin();
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW;
+  constexpr int VB = 16 / E;
+  constexpr int NS = FUSED ? 2 : 1;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float os_tab[128];
+  const Ring rg = ring_of(smem);
+  const int tid = threadIdx.x, T = blockDim.x, S = p.stages;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t nrows = first < p.M ? (p.M - 1 - first) / stride + 1 : 0;
+  const char* xs = static_cast<const char*>(p.x);
+  const char* rsrc = static_cast<const char*>(p.residual);
+  const float gs = p.gs;
+  const float gs6 = __fdiv_rn(gs, 6.f);
+  if constexpr (OUT == kOutNvfp4) {
+    for (int c = tid; c < 128; c += T) os_tab[c] = c ? __fdiv_rn(gs, e4m3_value((uint32_t)c)) : 0.f;
+  }
+  // (the barrier inside ring_start also publishes os_tab)
+  int64_t issued =
+      ring_start<NS>(rg, S, nrows, first, stride, FUSED ? rsrc : xs, xs, nullptr, rb);
+
+  uint4 gw[VPT][GW];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+#pragma unroll
+    for (int w = 0; w < GW; ++w)
+      gw[k][w] = v < p.nvec ? ld_cached(static_cast<const char*>(p.gamma) +
+                                        ((size_t)v * GW + w) * 16)
+                            : make_uint4(0, 0, 0, 0);
+  }
+
+  int parity = 0;
+  int64_t i = 0;
+  bool failed = false;
+  for (; i < nrows; ++i) {
+    const int st_i = (int)(i % S);
+    const int64_t row = first + i * stride;
+    const bool late =
+        !mbar_wait_bounded(rg.full + st_i, (uint32_t)((i / S) & 1), p.wait_limit);
+    const uint4* stg = reinterpret_cast<const uint4*>(rg.buf + (size_t)st_i * NS * rb);
+    Slice<VPT, FUSED> sl;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      const bool in = v < p.nvec && !late;
+      sl.x[k] = in ? stg[FUSED ? p.nvec + v : v] : make_uint4(0, 0, 0, 0);
+      if constexpr (FUSED) sl.r[k] = in ? stg[v] : make_uint4(0, 0, 0, 0);
+    }
+    // h is stored only once the CTA knows that no wait ran out (below)
+    float2 pr[VPT][E / 2];
+    float vmax[VPT];
+    float ss = quant_row_pass<TX, TW, VPT, FUSED>(sl, gw, pr, vmax, nullptr, tid, T, 0, false);
+    float mx = 0.f;
+    bool any_late;
+    if constexpr (OUT == kOutFp8) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) mx = fmaxf(mx, vmax[k]);
+      any_late = cta_sum_max_vote(ss, mx, rg.red, parity, late);
+    } else {
+      float t[1] = {ss};
+      any_late = cta_sum_vote<1>(t, rg.red, parity, late);
+      ss = t[0];
+    }
+    if (any_late) {
+      failed = true;
+      break;
+    }
+    parity ^= 1;
+    // every thread is past its reads of this stage: refill it
+    if (tid == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue_row<NS>(rg, issued, first, stride, S, FUSED ? rsrc : xs, xs, nullptr, rb);
+      ++issued;
+    }
+    const float rs = rsqrtf(fmaf(ss, p.inv_n, p.eps));
+    if (tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+    if constexpr (FUSED) {
+      char* hrow = static_cast<char*>(p.residual) + row * rb;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * T;
+        if (v < p.nvec) st_stream(hrow + (size_t)v * 16, sl.x[k]);
+      }
+    }
+    if constexpr (OUT == kOutFp8) {
+      const float inv = mx > 0.f ? __fdiv_rn(448.f, mx) : 0.f;
+      const float2 inv2 = make_float2(inv, inv);
+      if (tid == 0) static_cast<float*>(p.qs)[row] = mx > 0.f ? __fdiv_rn(rs * mx, 448.f) : 0.f;
+      char* qrow = static_cast<char*>(p.y) + row * (size_t)p.N;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * T;
+        if (v < p.nvec) {
+          float o[E];
+#pragma unroll
+          for (int j = 0; j < E / 2; ++j) {
+            const float2 t = __fmul2_rn(pr[k][j], inv2);
+            o[2 * j] = t.x;
+            o[2 * j + 1] = t.y;
+          }
+          store_fp8(qrow + (size_t)v * E, o);
+        }
+      }
+    } else {
+      char* qrow = static_cast<char*>(p.y) + row * (size_t)(p.N / 2);
+      uint8_t* sfrow = static_cast<uint8_t*>(p.qs) + row * (size_t)(p.N / 16);
+      const float rg6 = rs * gs6;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * T;
+        float a = vmax[k];
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        if constexpr (VB == 4) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        const uint32_t code = a > 0.f ? e4m3_code(a * rg6) : 0u;
+        const float sc = rs * os_tab[code & 127u];
+        const float2 sc2 = make_float2(sc, sc);
+        if (v < p.nvec) {
+          if (v % VB == 0) sfrow[v / VB] = (uint8_t)code;
+          float o[E];
+#pragma unroll
+          for (int j = 0; j < E / 2; ++j) {
+            const float2 t = __fmul2_rn(pr[k][j], sc2);
+            o[2 * j] = t.x;
+            o[2 * j + 1] = t.y;
+          }
+          store_fp4(qrow + (size_t)v * (E / 2), o, code == 0u);
+        }
+      }
+    }
+  }
+  if (failed && tid == 0) {
+    drain(rg, i, issued, S);
+    atomicOr(p.status, kStatusWaitTimeout);
   }
 }
 
@@ -379,6 +637,14 @@ FwdKernel pick_shape(const FwdKey& k) {
 template <typename TX, typename TW, bool FUSED, int OUT>
 FwdKernel pick_out(const FwdKey& k) {
   if (k.family == kGeneric) return fwd_quant_generic_kernel<TX, TW, FUSED, OUT>;
+  if (k.family == kStaged) {
+    switch (k.vpt) {
+      case 1: return fwd_quant_staged_kernel<TX, TW, 1, FUSED, OUT>;
+      case 2: return fwd_quant_staged_kernel<TX, TW, 2, FUSED, OUT>;
+      case 4: return fwd_quant_staged_kernel<TX, TW, 4, FUSED, OUT>;
+      default: return nullptr;
+    }
+  }
   return k.prefetch ? pick_shape<TX, TW, FUSED, OUT, true>(k)
                     : pick_shape<TX, TW, FUSED, OUT, false>(k);
 }

@@ -20,10 +20,7 @@
 // whole CTA agrees: it stores nothing for that row and leaves; thread 0 first
 // waits (bounded) for the copies it has in flight, then raises
 // kStatusWaitTimeout in p.status.
-#include <type_traits>
-
-#include "rmsnorm_device.cuh"
-#include "rmsnorm_internal.h"
+#include "rmsnorm_ring.cuh"
 
 #ifndef RMSN_PAIR
 #error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
@@ -31,79 +28,6 @@
 
 namespace rmsn {
 namespace {
-
-constexpr long long kDrainLimit = 1LL << 34;   // cycles: several seconds
-
-struct Ring {
-  uint64_t* full;       // kStagedMaxStages barriers
-  float* red;           // 2 x 2 x 32 reduction slots
-  unsigned char* buf;   // stages x NS x row bytes
-};
-
-__device__ __forceinline__ Ring ring_of(unsigned char* smem) {
-  Ring r;
-  r.full = reinterpret_cast<uint64_t*>(smem);
-  r.red = reinterpret_cast<float*>(smem + 128);
-  r.buf = smem + kStagedHeader;
-  return r;
-}
-
-// Thread 0: bulk-copy CTA row i of the NS streamed operands into its stage.
-template <int NS>
-__device__ __forceinline__ void issue_row(const Ring& rg, int64_t i, int64_t first, int64_t stride,
-                                          int S, const char* src0, const char* src1,
-                                          const char* src2, size_t rb) {
-  const int s = (int)(i % S);
-  const int64_t row = first + i * stride;
-  uint64_t* bar = rg.full + s;
-  unsigned char* dst = rg.buf + (size_t)s * NS * rb;
-  mbar_arrive_expect_tx(bar, (uint32_t)(NS * rb));
-  bulk_copy_g2s(dst, src0 + row * rb, (uint32_t)rb, bar);
-  if (NS > 1) bulk_copy_g2s(dst + rb, src1 + row * rb, (uint32_t)rb, bar);
-  if (NS > 2) bulk_copy_g2s(dst + 2 * rb, src2 + row * rb, (uint32_t)rb, bar);
-}
-
-// Thread 0, error path: wait (bounded) for rows [from, issued) still in flight.
-__device__ __forceinline__ void drain(const Ring& rg, int64_t from, int64_t issued, int S) {
-  for (int64_t j = from; j < issued; ++j)
-    mbar_wait_bounded(rg.full + (j % S), (uint32_t)((j / S) & 1), kDrainLimit);
-}
-
-// Prologue: barriers initialised, the first min(S, nrows) rows requested.
-template <int NS>
-__device__ __forceinline__ int64_t ring_start(const Ring& rg, int S, int64_t nrows, int64_t first,
-                                              int64_t stride, const char* src0, const char* src1,
-                                              const char* src2, size_t rb) {
-  int64_t issued = 0;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int64_t n0 = nrows < S ? nrows : S;
-    for (; issued < n0; ++issued)
-      issue_row<NS>(rg, issued, first, stride, S, src0, src1, src2, rb);
-  }
-  return issued;
-}
-
-template <typename TW, int E>
-__device__ __forceinline__ void gamma_f32(const void* gamma, int v, float (&g)[E]) {
-  constexpr int GW = E * (int)sizeof(TW) / 16;
-  const char* gp = static_cast<const char*>(gamma) + (size_t)v * GW * 16;
-  if constexpr (std::is_same<TW, float>::value) {
-#pragma unroll
-    for (int w = 0; w < GW; ++w) {
-      float t[4];
-      unpack(ld_cached(gp + w * 16), t);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) g[w * 4 + i] = t[i];
-    }
-  } else {
-    unpack(ld_cached(gp), g);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Forward / fused add.  Stage layout: fused [r | x], forward [x].

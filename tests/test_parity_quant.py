@@ -195,7 +195,8 @@ def test_unaligned_pointers_take_the_scalar_kernel(kind):
 FORCED = ["subwarp:g=32:vpt=2:cps=1", "subwarp:g=8:vpt=2:cps=1", "subwarp:g=16:vpt=1:cps=1",
           "subwarp:g=32:vpt=1:cps=1", "subwarp:g=16:vpt=1:pf=0:cps=1", "cta:vpt=1:cps=1",
           "cta:vpt=2:t=64:cps=1", "cta:vpt=4:t=32:cps=1", "cta:vpt=4:t=32:pf=0:cps=1",
-          "cta:vpt=8:t=32:pf=0:cps=1", "generic:cps=1"]
+          "cta:vpt=8:t=32:pf=0:cps=1", "staged:vpt=1:st=2:cps=1", "staged:vpt=2:t=64:st=3:cps=1",
+          "staged:vpt=4:t=32:st=8:cps=1", "generic:cps=1"]
 
 
 @pytest.mark.parametrize("force", FORCED)
@@ -211,8 +212,46 @@ def test_forced_variants_walk_many_rows(monkeypatch, force, kind):
         check_nvfp4(out, x, g, f32(1e-6), "bf16", "bf16", GS, residual=r)
 
 
+@pytest.mark.parametrize("xd,wd", PAIRS)
+@pytest.mark.parametrize("N", [2064, 8192])
+@pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("fused", [False, True])
+def test_staged_ring_long_rows(monkeypatch, xd, wd, N, kind, fused):
+    # rows arrive through the bulk-copy ring; two stages, so it wraps often
+    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:st=2")
+    x, g, r = inputs(200, N, xd, wd, seed=N + 9, fused=fused, outliers=fused)
+    out = run(kind, x, g, f32(1e-6), xd, wd, residual=r, gs=GS)
+    if kind == "fp8":
+        check_fp8(out, x, g, f32(1e-6), xd, wd, residual=r)
+    else:
+        check_nvfp4(out, x, g, f32(1e-6), xd, wd, GS, residual=r)
+
+
+@pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
+def test_staged_wait_timeout_is_reported_and_the_context_survives(monkeypatch, kind):
+    # the wait limit forced to zero cycles: the first wait for a row still in
+    # flight gives up; the kernel stores nothing more, drains its copies and
+    # raises the flag that rmsnorm_check_device reports and clears
+    x, g, r = inputs(1024, 8192, "bf16", "bf16", seed=43, fused=True)
+    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
+    rn.rmsnorm_check_device()
+    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "0")
+    run(kind, x, g, f32(1e-6), "bf16", "bf16", residual=r, gs=GS)
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_check_device()
+    assert e.value.status == 6
+    rn.rmsnorm_check_device()
+    monkeypatch.delenv("RMSNORM_WAIT_LIMIT_CYCLES")
+    out = run(kind, x, g, f32(1e-6), "bf16", "bf16", residual=r, gs=GS)
+    if kind == "fp8":
+        check_fp8(out, x, g, f32(1e-6), "bf16", "bf16", residual=r)
+    else:
+        check_nvfp4(out, x, g, f32(1e-6), "bf16", "bf16", GS, residual=r)
+    rn.rmsnorm_check_device()
+
+
 @pytest.mark.parametrize("eps", [0.0, 1e-6])
-@pytest.mark.parametrize("force", ["", "generic"])
+@pytest.mark.parametrize("force", ["", "generic", "staged:st=2"])
 def test_zero_rows_and_blocks(monkeypatch, eps, force):
     if force:
         monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
