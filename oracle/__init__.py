@@ -55,6 +55,12 @@ def _load():
             lib.oracle_rmsnorm_fwd_strided.argtypes = [_P, I64, I64, _P, I64, I64, I64, D, I, I,
                                                        _P, I64, I64, _P, _P]
             lib.oracle_rmsnorm_fwd_strided.restype = I
+            lib.oracle_layernorm_fwd.argtypes = [_P, _P, _P, I64, I64, D, I, I, _P, _P, _P, _P,
+                                                 _P, _P]
+            lib.oracle_layernorm_fwd.restype = I
+            lib.oracle_layernorm_bwd.argtypes = [_P, _P, _P, _P, _P, I64, I64, D, I, I, _P, _P,
+                                                 _P, _P, _P, _P, _P]
+            lib.oracle_layernorm_bwd.restype = I
             lib.oracle_rmsnorm_fwd_fp8.argtypes = [_P, _P, _P, I64, I64, D, I, I, _P, _P, _P, _P,
                                                    _P, _P]
             lib.oracle_rmsnorm_fwd_fp8.restype = I
@@ -345,4 +351,54 @@ def unpack_e2m1(q: np.ndarray) -> np.ndarray:
     out = np.empty(q.shape[:-1] + (q.shape[-1] * 2,), np.uint8)
     out[..., 0::2] = q & 0xF
     out[..., 1::2] = q >> 4
+    return out
+
+
+# ---------------------------------------------------------------- LayerNorm
+
+def layernorm_fwd(x, gamma, beta, eps, x_dtype="bf16", w_dtype=None):
+    """(x - mean) / sqrt(var + eps) * gamma + beta per row (beta None: 0).
+    Returns y (x_dtype), y64, mean / rstd (fp32) and mean64 / rstd64."""
+    w_dtype = w_dtype or x_dtype
+    x = _check_in(x, x_dtype)
+    M, N = x.shape
+    gamma = _check_in(gamma, w_dtype, (N,))
+    if beta is not None:
+        beta = _check_in(beta, w_dtype, (N,))
+    out = {"y": np.empty((M, N), _np(x_dtype)), "y64": np.empty((M, N)),
+           "mean": np.empty(M, np.float32), "rstd": np.empty(M, np.float32),
+           "mean64": np.empty(M), "rstd64": np.empty(M)}
+    rc = _load().oracle_layernorm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), M, N, float(eps),
+                                      DTYPE_CODES[x_dtype], DTYPE_CODES[w_dtype], _ptr(out["y"]),
+                                      _ptr(out["y64"]), _ptr(out["mean"]), _ptr(out["rstd"]),
+                                      _ptr(out["mean64"]), _ptr(out["rstd64"]))
+    if rc != 0:
+        raise ValueError("oracle_layernorm_fwd rejected its arguments")
+    return out
+
+
+def layernorm_bwd(dy, x, mean, rstd, gamma, eps, x_dtype="bf16", w_dtype=None):
+    """dx (x_dtype), dgamma and dbeta (fp32) of the LayerNorm forward, with the
+    saved fp32 mean and rstd (both None: recomputed from x and eps).  Also
+    dx64, dgamma64, dbeta64 and dx_scale64 (per row, the size of its terms)."""
+    w_dtype = w_dtype or x_dtype
+    x = _check_in(x, x_dtype)
+    M, N = x.shape
+    dy = _check_in(dy, x_dtype, (M, N))
+    gamma = _check_in(gamma, w_dtype, (N,))
+    if (mean is None) != (rstd is None):
+        raise ValueError("give both saved statistics (mean and rstd) or neither")
+    if mean is not None:
+        mean = _check_in(mean, "f32", (M,))
+        rstd = _check_in(rstd, "f32", (M,))
+    out = {"dx": np.empty((M, N), _np(x_dtype)), "dx64": np.empty((M, N)),
+           "dgamma64": np.empty(N), "dbeta64": np.empty(N), "dgamma": np.empty(N, np.float32),
+           "dbeta": np.empty(N, np.float32), "dx_scale64": np.empty(M)}
+    rc = _load().oracle_layernorm_bwd(_ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma), M,
+                                      N, float(eps), DTYPE_CODES[x_dtype], DTYPE_CODES[w_dtype],
+                                      _ptr(out["dx"]), _ptr(out["dx64"]), _ptr(out["dgamma64"]),
+                                      _ptr(out["dbeta64"]), _ptr(out["dgamma"]),
+                                      _ptr(out["dbeta"]), _ptr(out["dx_scale64"]))
+    if rc != 0:
+        raise ValueError("oracle_layernorm_bwd rejected its arguments")
     return out

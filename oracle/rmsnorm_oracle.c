@@ -21,6 +21,9 @@
  *                  dx_j     = r (gamma_j dy_j - x_j c),  c = r^2/N sum_k gamma_k dy_k x_k
  *                  dgamma_j = sum_rows dy_j x_j r
  *                with r the saved rstd when one is given.
+ *   layernorm    (x - mean) / sqrt(var + eps) * gamma + beta (same guide,
+ *                section 1.1), two passes (mean, then the population variance
+ *                about it), and its backward, derived below.
  *   quantised    the forward (and the fused add) with an FP8 E4M3 output and
  *                one scale per row, or an NVFP4 output (FP4 E2M1 codes with an
  *                E4M3 scale per 16 elements and a global scale); the pages name
@@ -497,5 +500,113 @@ int oracle_rmsnorm_fwd_nvfp4(const void* x, const void* residual, const void* ga
   free(v);
   free(yr);
   free(hr);
+  return 0;
+}
+
+/* ---- LayerNorm ----------------------------------------------------------- */
+
+/* One row of LayerNorm ("Pre-built kernel library guide", section 1.1:
+ * (x - mean) / sqrt(var + eps) * gamma + beta, two passes): mean, then the
+ * population variance about it, each a plain double sum. */
+static void ln_stats(const double* v, int64_t N, double eps, double* mean, double* rstd) {
+  double s = 0.0;
+  for (int64_t j = 0; j < N; ++j) s += v[j];
+  const double mu = s / (double)N;
+  double q = 0.0;
+  for (int64_t j = 0; j < N; ++j) q += (v[j] - mu) * (v[j] - mu);
+  *mean = mu;
+  *rstd = 1.0 / sqrt(q / (double)N + eps);
+}
+
+/* x: M x N (x_dtype); gamma, beta: N (w_dtype; beta may be NULL for 0).
+ * Outputs (each may be NULL): y (x_dtype, rounded once), y64 (double),
+ * mean and rstd (fp32, rounded once), mean64 and rstd64 (double). */
+int oracle_layernorm_fwd(const void* x, const void* gamma, const void* beta, int64_t M,
+                         int64_t N, double eps, int x_dtype, int w_dtype, void* y, double* y64,
+                         float* mean, float* rstd, double* mean64, double* rstd64) {
+  if (M < 0 || N <= 0 || bad_dtypes(x_dtype, w_dtype) || (M > 0 && (!x || !gamma)))
+    return -1;
+  double* v = (double*)malloc((size_t)N * sizeof(double));
+  if (!v) return -1;
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) v[j] = load(x, x_dtype, i * N + j);
+    double mu, r;
+    ln_stats(v, N, eps, &mu, &r);
+    if (mean) mean[i] = (float)mu;
+    if (rstd) rstd[i] = (float)r;
+    if (mean64) mean64[i] = mu;
+    if (rstd64) rstd64[i] = r;
+    for (int64_t j = 0; j < N; ++j) {
+      double b = beta ? load(beta, w_dtype, j) : 0.0;
+      double out = (v[j] - mu) * r * load(gamma, w_dtype, j) + b;
+      if (y) store(y, x_dtype, i * N + j, out);
+      if (y64) y64[i * N + j] = out;
+    }
+  }
+  free(v);
+  return 0;
+}
+
+/* Backward of the LayerNorm forward.  The pages give no formula; with
+ * xhat = (x - mean) rstd and g = dy * gamma, differentiating gives
+ *     dx_j     = rstd (g_j - mean_k g_k - xhat_j mean_k (g_k xhat_k))
+ *     dgamma_j = sum_rows dy_j xhat_j          dbeta_j = sum_rows dy_j
+ * with the saved mean and rstd (fp32, as the forward stored them) when both
+ * are given, else both recomputed from x and eps.  Outputs (each may be
+ * NULL): dx (x_dtype, rounded once), dx64; dgamma64, dbeta64 (double) and
+ * dgamma, dbeta (fp32, rounded once); dx_scale64 (M): rstd * (sum_k |g_k| +
+ * sum_k |g_k xhat_k|) / N, the size of the row terms, for error bounds. */
+int oracle_layernorm_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+                         const void* gamma, int64_t M, int64_t N, double eps, int x_dtype,
+                         int w_dtype, void* dx, double* dx64, double* dgamma64,
+                         double* dbeta64, float* dgamma, float* dbeta, double* dx_scale64) {
+  if (M < 0 || N <= 0 || bad_dtypes(x_dtype, w_dtype) || (M > 0 && (!dy || !x || !gamma)) ||
+      (!mean) != (!rstd))
+    return -1;
+  double* v = (double*)malloc((size_t)N * sizeof(double));
+  double* xh = (double*)malloc((size_t)N * sizeof(double));
+  double* g = (double*)malloc((size_t)N * sizeof(double));
+  double* dg = (double*)calloc((size_t)N, sizeof(double));
+  double* db = (double*)calloc((size_t)N, sizeof(double));
+  if (!v || !xh || !g || !dg || !db) {
+    free(v); free(xh); free(g); free(dg); free(db);
+    return -1;
+  }
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) v[j] = load(x, x_dtype, i * N + j);
+    double mu, r;
+    if (mean) {
+      mu = (double)mean[i];
+      r = (double)rstd[i];
+    } else {
+      ln_stats(v, N, eps, &mu, &r);
+    }
+    double sg = 0.0, sgx = 0.0, ag = 0.0, agx = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+      const double d = load(dy, x_dtype, i * N + j);
+      xh[j] = (v[j] - mu) * r;
+      g[j] = d * load(gamma, w_dtype, j);
+      sg += g[j];
+      sgx += g[j] * xh[j];
+      ag += fabs(g[j]);
+      agx += fabs(g[j] * xh[j]);
+      dg[j] += d * xh[j];
+      db[j] += d;
+    }
+    const double mg = sg / (double)N, mgx = sgx / (double)N;
+    if (dx_scale64) dx_scale64[i] = r * (ag + agx) / (double)N;
+    for (int64_t j = 0; j < N; ++j) {
+      const double out = r * (g[j] - mg - xh[j] * mgx);
+      if (dx) store(dx, x_dtype, i * N + j, out);
+      if (dx64) dx64[i * N + j] = out;
+    }
+  }
+  for (int64_t j = 0; j < N; ++j) {
+    if (dgamma64) dgamma64[j] = dg[j];
+    if (dbeta64) dbeta64[j] = db[j];
+    if (dgamma) dgamma[j] = (float)dg[j];
+    if (dbeta) dbeta[j] = (float)db[j];
+  }
+  free(v); free(xh); free(g); free(dg); free(db);
   return 0;
 }
