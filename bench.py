@@ -56,6 +56,10 @@ def alg_bytes(wl, rows=None) -> int:
         return M * N * 4 * sx + N * sw + rstd
     if wl.op == "fused_add_bwd":   # h, dy, dres in; dh out; dgamma in the weight dtype
         return M * N * 4 * sx + 4 * M + N * sw + N * sw
+    if wl.op == "ln_fwd":    # x in, y out; gamma and beta; mean and rstd out
+        return M * N * 2 * sx + 2 * N * sw + 8 * M
+    if wl.op == "ln_bwd":    # x, dy, mean, rstd in; dx out; dgamma and dbeta out (fp32)
+        return M * N * 3 * sx + 8 * M + N * sw + 8 * N
     if wl.op in ("fwd_fp8", "fused_add_fp8", "fwd_nvfp4", "fused_add_nvfp4"):
         # x (fused: r and x in, h out), then codes and scales out
         act = M * N * (3 if wl.op.startswith("fused") else 1) * sx
@@ -509,7 +513,8 @@ def run_reference(args):
 
 def _op_code(op):
     return {"fwd": 0, "fused_add": 1, "bwd": 2, "fused_add_bwd": 3, "fwd_strided": 4,
-            "fwd_fp8": 5, "fused_add_fp8": 6, "fwd_nvfp4": 7, "fused_add_nvfp4": 8}[op]
+            "fwd_fp8": 5, "fused_add_fp8": 6, "fwd_nvfp4": 7, "fused_add_nvfp4": 8,
+            "ln_fwd": 9, "ln_bwd": 10}[op]
 
 
 def device_sets(wl, inp, dev, l2_bytes, rn):
@@ -526,7 +531,12 @@ def device_sets(wl, inp, dev, l2_bytes, rn):
     sets = []
     for _ in range(nsets):
         d = {k: v.to(dev) for k, v in host.items()}
-        if "fp8" in wl.op:
+        if wl.op.startswith("ln_"):
+            d["y"] = torch.empty((M, N), dtype=act, device=dev)
+            d["mean"] = torch.empty(M, dtype=torch.float32, device=dev)
+            d["dgamma"] = torch.empty(N, dtype=torch.float32, device=dev)
+            d["dbeta"] = torch.empty(N, dtype=torch.float32, device=dev)
+        elif "fp8" in wl.op:
             d["q"] = torch.empty((M, N), dtype=torch.uint8, device=dev)
             d["qs"] = torch.empty(M, dtype=torch.float32, device=dev)
         elif "nvfp4" in wl.op:
@@ -555,6 +565,16 @@ def make_launch(wl, d, stream, rn):
         return lambda: rn.rmsnorm_fused_add_fwd(d["x"], d["residual"], d["gamma"], d["y"],
                                                 d["rstd"] if wl.store_rstd else None, M, N,
                                                 eps, wl.x_dtype, wl.w_dtype, stream)
+    if wl.op == "ln_fwd":
+        return lambda: rn.layernorm_fwd(d["x"], d["gamma"], d["beta"], d["y"], d["mean"],
+                                        d["rstd"], M, N, eps, wl.x_dtype, wl.w_dtype, stream)
+    if wl.op == "ln_bwd":      # mean and rstd: the (untimed) forward's, saved in the set
+        import torch
+        lws = rn.layernorm_bwd_workspace_size(M, N, wl.x_dtype, wl.w_dtype)
+        d["lws"] = torch.empty(max(16, lws), dtype=torch.uint8, device=d["x"].device)
+        return lambda: rn.layernorm_bwd(d["dy"], d["x"], d["mean"], d["rstd"], d["gamma"],
+                                        d["y"], d["dgamma"], d["dbeta"], d["lws"], lws, M, N,
+                                        eps, wl.x_dtype, wl.w_dtype, stream)
     if "fp8" in wl.op:
         return lambda: rn.rmsnorm_fwd_fp8(d["x"], d.get("residual"), d["gamma"], d["q"], d["qs"],
                                           d["rstd"] if wl.store_rstd else None, M, N, eps,
@@ -617,7 +637,12 @@ def run_sweep(args):
         wl = si.WORKLOADS[name]
         inp = si.make_inputs(wl)
         sets = device_sets(wl, inp, dev, l2, rn)
-        for d in sets:   # rstd of x for the backward (the forward kernel, untimed)
+        for d in sets:   # saved statistics for the backward (untimed forward)
+            if wl.op == "ln_bwd":
+                gam = d["gamma"]
+                rn.layernorm_fwd(d["x"], gam, None, d["y"], d["mean"], d["rstd"], wl.M, wl.N,
+                                 float(np.float32(wl.eps)), wl.x_dtype, wl.w_dtype, stream)
+                continue
             if wl.op not in ("bwd", "fused_add_bwd"):
                 break
             rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"], d["rstd"], wl.M, wl.N,

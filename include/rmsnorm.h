@@ -100,6 +100,46 @@ rmsnorm_status_t rmsnorm_fwd_strided(const void* x, int64_t x_stride_token,
                                      cudaStream_t stream);
 
 /*
+ * LayerNorm forward ("Pre-built kernel library guide", section 1.1):
+ *     y_ij = (x_ij - mean_i) * rstd_i * gamma_j + beta_j,
+ *     mean_i = (1/N) sum_j x_ij,   rstd_i = 1 / sqrt((1/N) sum_j (x_ij - mean_i)^2 + eps)
+ * (two passes: the mean, then the population variance about it).  x: M x N
+ * (x_dtype); gamma, beta: N (w_dtype; beta NULL for no shift); y: M x N
+ * (x_dtype); mean, rstd: M fp32 each, or NULL to skip.  Buffers must not
+ * overlap.  Rows that are 16-byte aligned take the vectorised kernels; any
+ * other layout a scalar one.
+ */
+rmsnorm_status_t layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y,
+                               float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                               rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                               cudaStream_t stream);
+
+/* Bytes of device workspace layernorm_bwd needs for these sizes on `device`
+ * (-1: the current device), written to *bytes: the fp32 partial rows of the
+ * two weight gradients. */
+rmsnorm_status_t layernorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
+                                              rmsnorm_dtype_t w_dtype, int device,
+                                              size_t* bytes);
+
+/*
+ * LayerNorm backward.  The pages give no formula; differentiating the forward
+ * with xhat = (x - mean) rstd and g = dy * gamma:
+ *     dx_ij     = rstd_i (g_ij - (1/N) sum_k g_ik - xhat_ij (1/N) sum_k g_ik xhat_ik)
+ *     dgamma_j  = sum_i dy_ij xhat_ij,    dbeta_j = sum_i dy_ij
+ * dy, x: M x N (x_dtype); mean, rstd: the forward's saved statistics (M fp32
+ * each), or both NULL to recompute them from x and eps (eps is used only
+ * then); gamma: N (w_dtype); dx: M x N (x_dtype); dgamma, dbeta: N fp32 each,
+ * either may be NULL to skip it.  The weight gradients are deterministic:
+ * per-CTA partial rows in `workspace` (at least layernorm_bwd_workspace_size
+ * bytes, 16-byte aligned; unused when both are NULL), then a fixed-order sum.
+ */
+rmsnorm_status_t layernorm_bwd(const void* dy, const void* x, const float* mean,
+                               const float* rstd, const void* gamma, void* dx, float* dgamma,
+                               float* dbeta, void* workspace, size_t workspace_bytes, int64_t M,
+                               int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                               rmsnorm_dtype_t w_dtype, cudaStream_t stream);
+
+/*
  * Forward with FP8 output and one scale per row (token): the quantised-output
  * norms named in "TIRx kernels", Kernels list (flashinfer.norm: rmsnorm_quant,
  * fused_add_rmsnorm_quant).  The pages give the names only; this is the plain
@@ -255,7 +295,8 @@ const char* rmsnorm_status_string(rmsnorm_status_t status);
  * (for example "fwd/cta/vpt4/t256"), into buf (NUL-terminated, truncated to
  * len).  op: 0 forward, 1 fused add, 2 backward, 3 fused-add backward,
  * 4 strided forward (M = tokens x heads rows of N = D elements), 5 FP8
- * forward, 6 fused-add FP8 forward, 7 NVFP4 forward, 8 fused-add NVFP4.  aligned16:
+ * forward, 6 fused-add FP8 forward, 7 NVFP4 forward, 8 fused-add NVFP4,
+ * 9 LayerNorm forward, 10 LayerNorm backward.  aligned16:
  * nonzero when all operand base pointers (and, for op 4, all strides) are
  * 16-byte aligned.  Returns RMSNORM_OK or an argument error; launches
  * nothing.

@@ -17,7 +17,8 @@ import threading
 
 __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "OP_FUSED_ADD_BWD", "RMSNormError",
            "OP_FWD_STRIDED", "OP_FWD_FP8", "OP_FUSED_ADD_FP8", "OP_FWD_NVFP4",
-           "OP_FUSED_ADD_NVFP4", "rmsnorm_fwd_fp8", "rmsnorm_fwd_nvfp4",
+           "OP_FUSED_ADD_NVFP4", "rmsnorm_fwd_fp8", "rmsnorm_fwd_nvfp4", "OP_LAYERNORM_FWD",
+           "OP_LAYERNORM_BWD", "layernorm_fwd", "layernorm_bwd_workspace_size", "layernorm_bwd",
            "library_path", "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided",
            "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
@@ -28,13 +29,15 @@ F32 = 0
 BF16 = 1
 OP_FWD, OP_FUSED_ADD, OP_BWD, OP_FUSED_ADD_BWD = 0, 1, 2, 3
 OP_FWD_STRIDED, OP_FWD_FP8, OP_FUSED_ADD_FP8, OP_FWD_NVFP4, OP_FUSED_ADD_NVFP4 = 4, 5, 6, 7, 8
+OP_LAYERNORM_FWD, OP_LAYERNORM_BWD = 9, 10
 _DT_NAMES = {"f32": F32, "bf16": BF16}
 
 EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspace_size",
                     "rmsnorm_bwd", "rmsnorm_status_string", "rmsnorm_describe_plan",
                     "rmsnorm_bwd_noalloc", "rmsnorm_check_device", "rmsnorm_last_error",
                     "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided", "rmsnorm_fwd_fp8",
-                    "rmsnorm_fwd_nvfp4")
+                    "rmsnorm_fwd_nvfp4", "layernorm_fwd", "layernorm_bwd_workspace_size",
+                    "layernorm_bwd")
 
 # Size of the library-owned scratch of rmsnorm_bwd_noalloc (16 MiB).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -88,6 +91,12 @@ def load_library():
             lib.rmsnorm_fwd_strided.argtypes = [P, I64, I64, P, P, I64, I64, P, I64, I64, I64, F,
                                                 I, I, P]
             lib.rmsnorm_fwd_strided.restype = I
+            lib.layernorm_fwd.argtypes = [P, P, P, P, P, P, I64, I64, F, I, I, P]
+            lib.layernorm_fwd.restype = I
+            lib.layernorm_bwd_workspace_size.argtypes = [I64, I64, I, I, I, ctypes.POINTER(SZ)]
+            lib.layernorm_bwd_workspace_size.restype = I
+            lib.layernorm_bwd.argtypes = [P, P, P, P, P, P, P, P, P, SZ, I64, I64, F, I, I, P]
+            lib.layernorm_bwd.restype = I
             lib.rmsnorm_fwd_fp8.argtypes = [P, P, P, P, P, P, I64, I64, F, I, I, P]
             lib.rmsnorm_fwd_fp8.restype = I
             lib.rmsnorm_fwd_nvfp4.argtypes = [P, P, P, F, P, P, P, I64, I64, F, I, I, P]
@@ -161,6 +170,30 @@ def rmsnorm_fwd_strided(x, x_stride_token, x_stride_head, gamma, y, y_stride_tok
                                               y_stride_head, _ptr(rstd), T, H, D, eps,
                                               _dt(x_dtype), _dt(w_dtype), _stream(stream)),
            "rmsnorm_fwd_strided")
+
+
+def layernorm_fwd(x, gamma, beta, y, mean, rstd, M, N, eps, x_dtype, w_dtype, stream=None):
+    _check(load_library().layernorm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean),
+                                        _ptr(rstd), M, N, eps, _dt(x_dtype), _dt(w_dtype),
+                                        _stream(stream)),
+           "layernorm_fwd")
+
+
+def layernorm_bwd_workspace_size(M, N, x_dtype, w_dtype, device=-1):
+    n = ctypes.c_size_t(0)
+    _check(load_library().layernorm_bwd_workspace_size(M, N, _dt(x_dtype), _dt(w_dtype), device,
+                                                       ctypes.byref(n)),
+           "layernorm_bwd_workspace_size")
+    return int(n.value)
+
+
+def layernorm_bwd(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace, workspace_bytes, M, N,
+                  eps, x_dtype, w_dtype, stream=None):
+    _check(load_library().layernorm_bwd(_ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma),
+                                        _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(workspace),
+                                        workspace_bytes, M, N, eps, _dt(x_dtype), _dt(w_dtype),
+                                        _stream(stream)),
+           "layernorm_bwd")
 
 
 def rmsnorm_fwd_fp8(x, residual, gamma, q, scale, rstd, M, N, eps, x_dtype, w_dtype,

@@ -1,7 +1,7 @@
 """Build librmsnorm_gb300.so in-tree with nvcc for sm_103a.
 
-Sixteen translation units (forward, backward, staged, ragged and
-quantised-output kernels once per dtype pair, plus the C ABI) compile in parallel, then link into one
+Nineteen translation units (forward, backward, staged, ragged,
+quantised-output and LayerNorm kernels once per dtype pair, plus the C ABI) compile in parallel, then link into one
 shared library with the CUDA runtime linked statically.  Rebuilds only when a source is newer than the
 library.
 """
@@ -38,6 +38,9 @@ UNITS = [("rmsnorm_fwd.cu", ["-DRMSN_PAIR=0"], "fwd_p0.o"),
          ("rmsnorm_quant.cu", ["-DRMSN_PAIR=0"], "quant_p0.o"),
          ("rmsnorm_quant.cu", ["-DRMSN_PAIR=1"], "quant_p1.o"),
          ("rmsnorm_quant.cu", ["-DRMSN_PAIR=2"], "quant_p2.o"),
+         ("rmsnorm_layernorm.cu", ["-DRMSN_PAIR=0"], "ln_p0.o"),
+         ("rmsnorm_layernorm.cu", ["-DRMSN_PAIR=1"], "ln_p1.o"),
+         ("rmsnorm_layernorm.cu", ["-DRMSN_PAIR=2"], "ln_p2.o"),
          ("rmsnorm_api.cu", [], "api.o")]
 
 

@@ -491,7 +491,7 @@ const char* family_name(int f) {
 void describe(int op, const Plan& p, char* buf, size_t len) {
   static const char* ops[] = {"fwd",     "fused_add",     "bwd",       "fused_add_bwd",
                               "fwd_strided", "fwd_fp8",   "fused_add_fp8", "fwd_nvfp4",
-                              "fused_add_nvfp4"};
+                              "fused_add_nvfp4", "layernorm_fwd", "layernorm_bwd"};
   const bool bwd = op == kBwd || op == kFusedBwd;
   snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d", ops[op],
            family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
@@ -871,6 +871,250 @@ rmsnorm_status_t fwd_quant_impl(int out, const void* x, void* residual, const vo
   return RMSNORM_OK;
 }
 
+// ---------------------------------------------------------------- LayerNorm
+
+LnKernel ln_kernel(const LnKey& k) {
+  if (k.xd == kF32 && k.wd == kF32) return get_ln_kernel_f32_f32(k);
+  if (k.xd == kBF16 && k.wd == kBF16) return get_ln_kernel_bf16_bf16(k);
+  if (k.xd == kBF16 && k.wd == kF32) return get_ln_kernel_bf16_f32(k);
+  return nullptr;
+}
+
+// Plan of the LayerNorm kernels: rows of at most 128 16-byte vectors take the
+// sub-warp form, longer aligned rows one CTA per row (forward: up to 4 vectors
+// per thread, backward: up to 2, since it keeps gamma and the two partials per
+// thread), anything else the scalar kernel.  Next-row prefetch throughout.
+rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool vec_ok,
+                         Plan* res) {
+  const int E = per_vec(xd);
+  const int nvec = vec_ok ? (int)(N / E) : 0;
+  Plan p;
+  p.family = kGeneric;
+  p.threads = 256;
+  if (vec_ok && nvec <= 128) {
+    p.family = kSubwarp;
+    subwarp_shape(nvec, &p.g, &p.vpt);
+    p.threads = kSubwarpThreads;
+    p.rows_per_cta = kSubwarpThreads / p.g;
+    p.prefetch = true;
+  } else if (vec_ok) {
+    static const int pref_fwd[] = {2, 4, 1}, pref_bwd[] = {2, 1};
+    const int* pref = bwd ? pref_bwd : pref_fwd;
+    for (int i = 0; i < (bwd ? 2 : 3); ++i) {
+      const int t = round_up((nvec + pref[i] - 1) / pref[i], 32);
+      if (t >= 64 && t <= kCtaMaxThreads) {
+        p.family = kCta;
+        p.vpt = pref[i];
+        p.threads = t;
+        p.prefetch = true;
+        break;
+      }
+    }
+  }
+  const Force f = read_force();
+  if (f.on) {
+    if (f.family == kGeneric) {
+      p.family = kGeneric;
+      p.threads = 256;
+      p.rows_per_cta = 1;
+    } else if (f.family == kSubwarp) {
+      if (!vec_ok || !f.g || !f.vpt || f.g * f.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
+      p.family = kSubwarp;
+      p.g = f.g;
+      p.vpt = f.vpt;
+      p.threads = kSubwarpThreads;
+      p.rows_per_cta = kSubwarpThreads / p.g;
+    } else if (f.family == kCta) {
+      if (!vec_ok || !f.vpt) return RMSNORM_ERR_INVALID_ARG;
+      p.family = kCta;
+      p.vpt = f.vpt;
+      p.threads = f.threads ? f.threads : round_up((nvec + p.vpt - 1) / p.vpt, 32);
+      if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32 ||
+          (int64_t)p.threads * p.vpt < nvec)
+        return RMSNORM_ERR_INVALID_ARG;
+      p.rows_per_cta = 1;
+    } else if (f.family >= 0) {
+      return RMSNORM_ERR_INVALID_ARG;
+    }
+    if (f.pf >= 0) p.prefetch = f.pf != 0;
+    p.cta_per_sm_cap = f.cps;
+  }
+  if (p.family == kGeneric) {
+    p.g = p.vpt = 0;
+    p.prefetch = false;
+    p.rows_per_cta = 1;
+  }
+  if (p.family != kSubwarp) p.g = 0;
+  LnKey k{xd, wd, p.family, p.g, p.vpt, bwd, p.prefetch};
+  LnKernel fn = ln_kernel(k);
+  if (fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
+  p.fn = reinterpret_cast<const void*>(fn);
+  // sub-warp backward: the groups' partial rows meet in shared memory
+  p.smem = (bwd && p.family == kSubwarp) ? p.rows_per_cta * 2 * nvec * E * 4 : 0;
+  if (bwd) {
+    p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
+    const Force fr = read_force();
+    if (fr.on && fr.mr >= 0) p.min_rows = fr.mr;
+  }
+  (void)M;
+  *res = p;
+  return RMSNORM_OK;
+}
+
+rmsnorm_status_t ln_fwd_impl(const void* x, const void* gamma, const void* beta, void* y,
+                             float* mean, float* rstd, int64_t M, int64_t N, float eps, int xd,
+                             int wd, cudaStream_t stream) {
+  rmsnorm_status_t st = check_sizes(M, N, eps);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if (M == 0) return RMSNORM_OK;
+  if (!x || !gamma || !y) return RMSNORM_ERR_INVALID_ARG;
+  const size_t xs = (size_t)esize(xd), ws = (size_t)esize(wd);
+  if (!aligned_to(x, xs) || !aligned_to(y, xs) || !aligned_to(gamma, ws) ||
+      (beta && !aligned_to(beta, ws)) || (mean && !aligned_to(mean, 4)) ||
+      (rstd && !aligned_to(rstd, 4)))
+    return RMSNORM_ERR_MISALIGNED;
+  const size_t act = (size_t)M * (size_t)N * xs, gb = (size_t)N * ws, rb = (size_t)M * 4;
+  const void* outs[3] = {y, mean, rstd};
+  const size_t olen[3] = {act, rb, rb};
+  const void* ins[3] = {x, gamma, beta};
+  const size_t ilen[3] = {act, gb, gb};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(outs[i], olen[i], ins[j], ilen[j])) return RMSNORM_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], olen[i], outs[j], olen[j])) return RMSNORM_ERR_INVALID_ARG;
+  }
+  const bool vec_ok = aligned_to(x, 16) && aligned_to(y, 16) && aligned_to(gamma, 16) &&
+                      (!beta || aligned_to(beta, 16)) && (N * (int64_t)xs) % 16 == 0;
+  Plan p;
+  if ((st = ln_plan(false, M, N, xd, wd, vec_ok, &p)) != RMSNORM_OK) return st;
+  int dev;
+  if ((st = current_device(&dev)) != RMSNORM_OK) return st;
+  if ((st = size_grid(&p, M, dev)) != RMSNORM_OK) return st;
+  LnParams prm = {};
+  prm.x = x;
+  prm.gamma = gamma;
+  prm.beta = beta;
+  prm.y = y;
+  prm.mean = mean;
+  prm.rstd = rstd;
+  prm.M = M;
+  prm.N = (int)N;
+  prm.nvec = vec_ok ? (int)(N / per_vec(xd)) : 0;
+  prm.eps = eps;
+  prm.inv_n = 1.0f / (float)N;
+  const cudaError_t e =
+      launch(reinterpret_cast<LnKernel>(const_cast<void*>(p.fn)), p.grid, p.threads, p.smem,
+             stream, prm);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "LayerNorm forward launch");
+  }
+  return RMSNORM_OK;
+}
+
+// Stage-1 CTA count bound of the LayerNorm backward for these sizes (the
+// grid of the plan for 16-byte aligned operands; every launch clamps to it).
+rmsnorm_status_t ln_partial_rows(int64_t M, int N, int xd, int wd, int device, int* rows) {
+  Plan pl;
+  rmsnorm_status_t st = ln_plan(true, M, N, xd, wd, (int64_t)N * esize(xd) % 16 == 0, &pl);
+  if (st != RMSNORM_OK) return st;
+  if ((st = size_grid(&pl, M, device)) != RMSNORM_OK) return st;
+  *rows = pl.grid;
+  return RMSNORM_OK;
+}
+
+rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
+                             const float* rstd, const void* gamma, void* dx, float* dgamma,
+                             float* dbeta, void* workspace, size_t workspace_bytes, int64_t M,
+                             int64_t N, float eps, int xd, int wd, cudaStream_t stream) {
+  rmsnorm_status_t st = check_sizes(M, N, eps);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if ((mean == nullptr) != (rstd == nullptr)) return RMSNORM_ERR_INVALID_ARG;
+  if (M == 0) {
+    for (float* out : {dgamma, dbeta})
+      if (out) {
+        const cudaError_t e = cudaMemsetAsync(out, 0, (size_t)N * 4, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync of a weight gradient");
+      }
+    return RMSNORM_OK;
+  }
+  if (!dy || !x || !gamma || !dx) return RMSNORM_ERR_INVALID_ARG;
+  const size_t xs = (size_t)esize(xd), ws = (size_t)esize(wd);
+  if (!aligned_to(dy, xs) || !aligned_to(x, xs) || !aligned_to(dx, xs) ||
+      !aligned_to(gamma, ws) || (mean && (!aligned_to(mean, 4) || !aligned_to(rstd, 4))) ||
+      (dgamma && !aligned_to(dgamma, 4)) || (dbeta && !aligned_to(dbeta, 4)))
+    return RMSNORM_ERR_MISALIGNED;
+  const size_t act = (size_t)M * (size_t)N * xs, gb = (size_t)N * ws, rb = (size_t)M * 4,
+               db = (size_t)N * 4;
+  const bool want = dgamma || dbeta;
+  const int ld_half = round_up((int)N, 4);
+  const void* outs[4] = {dx, dgamma, dbeta, nullptr};   // [3]: the workspace, once sized
+  size_t olen[4] = {act, db, db, 0};
+  const void* ins[5] = {dy, x, gamma, mean, rstd};
+  const size_t ilen[5] = {act, act, gb, rb, rb};
+  auto overlaps = [&]() {
+    for (int i = 0; i < 4; ++i) {
+      for (int j = 0; j < 5; ++j)
+        if (overlap(outs[i], olen[i], ins[j], ilen[j])) return true;
+      for (int j = i + 1; j < 4; ++j)
+        if (overlap(outs[i], olen[i], outs[j], olen[j])) return true;
+    }
+    return false;
+  };
+  if (overlaps()) return RMSNORM_ERR_INVALID_ARG;
+  if (want && (!workspace || !aligned_to(workspace, 16))) return RMSNORM_ERR_WORKSPACE;
+  int dev;
+  if ((st = current_device(&dev)) != RMSNORM_OK) return st;
+  int prows = 0;
+  if (want) {
+    if ((st = ln_partial_rows(M, (int)N, xd, wd, dev, &prows)) != RMSNORM_OK) return st;
+    const size_t need = (size_t)prows * 2 * ld_half * 4;
+    if (workspace_bytes < need) return RMSNORM_ERR_WORKSPACE;
+    outs[3] = workspace;
+    olen[3] = need;
+    if (overlaps()) return RMSNORM_ERR_INVALID_ARG;
+  }
+  const bool vec_ok = aligned_to(x, 16) && aligned_to(dy, 16) && aligned_to(dx, 16) &&
+                      aligned_to(gamma, 16) && (N * (int64_t)xs) % 16 == 0;
+  Plan p;
+  if ((st = ln_plan(true, M, N, xd, wd, vec_ok, &p)) != RMSNORM_OK) return st;
+  if ((st = size_grid(&p, M, dev)) != RMSNORM_OK) return st;
+  if (want && p.grid > prows) p.grid = prows;
+  LnParams prm = {};
+  prm.x = x;
+  prm.dy = dy;
+  prm.gamma = gamma;
+  prm.y = dx;
+  prm.mean = const_cast<float*>(mean);
+  prm.rstd = const_cast<float*>(rstd);
+  prm.partial = want ? static_cast<float*>(workspace) : nullptr;
+  prm.M = M;
+  prm.N = (int)N;
+  prm.nvec = vec_ok ? (int)(N / per_vec(xd)) : 0;
+  prm.ld_half = ld_half;
+  prm.eps = eps;
+  prm.inv_n = 1.0f / (float)N;
+  cudaError_t e = launch(reinterpret_cast<LnKernel>(const_cast<void*>(p.fn)), p.grid, p.threads,
+                         p.smem, stream, prm);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "LayerNorm backward stage-1 launch");
+  }
+  if (!want) return RMSNORM_OK;
+  // stage 2: both halves of the partial rows, summed per column in a fixed order
+  const float* part = static_cast<const float*>(workspace);
+  e = launch(get_ln_reduce_kernel(), (2 * ld_half / 4 + kRedCols - 1) / kRedCols,
+             kRedCols * kRedRows, 0, stream, part, p.grid, (int)N, ld_half, dgamma, dbeta);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "LayerNorm backward stage-2 launch");
+  }
+  return RMSNORM_OK;
+}
+
 // ---------------------------------------------------------------- backward
 
 // Stage-1 CTA count bound for these sizes: the grid of the plan for 16-byte
@@ -1079,6 +1323,41 @@ rmsnorm_status_t rmsnorm_fwd_strided(const void* x, int64_t x_stride_token,
                           y_stride_head, rstd, T, H, D, eps, (int)x_dtype, (int)w_dtype, stream);
 }
 
+rmsnorm_status_t layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y,
+                               float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                               rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
+                               cudaStream_t stream) {
+  return ln_fwd_impl(x, gamma, beta, y, mean, rstd, M, N, eps, (int)x_dtype, (int)w_dtype,
+                     stream);
+}
+
+rmsnorm_status_t layernorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
+                                              rmsnorm_dtype_t w_dtype, int device,
+                                              size_t* bytes) {
+  if (!bytes) return RMSNORM_ERR_INVALID_ARG;
+  *bytes = 0;
+  rmsnorm_status_t st = check_sizes(M, N, 0.f);
+  if (st != RMSNORM_OK) return st;
+  if (!dtype_pair_ok((int)x_dtype, (int)w_dtype)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+  if (M == 0) return RMSNORM_OK;
+  if (device < 0 && (st = current_device(&device)) != RMSNORM_OK) return st;
+  int rows = 0;
+  if ((st = ln_partial_rows(M, (int)N, (int)x_dtype, (int)w_dtype, device, &rows)) !=
+      RMSNORM_OK)
+    return st;
+  *bytes = (size_t)rows * 2 * (size_t)round_up((int)N, 4) * 4;
+  return RMSNORM_OK;
+}
+
+rmsnorm_status_t layernorm_bwd(const void* dy, const void* x, const float* mean,
+                               const float* rstd, const void* gamma, void* dx, float* dgamma,
+                               float* dbeta, void* workspace, size_t workspace_bytes, int64_t M,
+                               int64_t N, float eps, rmsnorm_dtype_t x_dtype,
+                               rmsnorm_dtype_t w_dtype, cudaStream_t stream) {
+  return ln_bwd_impl(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, workspace, workspace_bytes, M,
+                     N, eps, (int)x_dtype, (int)w_dtype, stream);
+}
+
 rmsnorm_status_t rmsnorm_fwd_fp8(const void* x, void* residual, const void* gamma, void* q,
                                  float* scale, float* rstd, int64_t M, int64_t N, float eps,
                                  rmsnorm_dtype_t x_dtype, rmsnorm_dtype_t w_dtype,
@@ -1162,14 +1441,18 @@ const char* rmsnorm_status_string(rmsnorm_status_t status) {
 rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
                                        rmsnorm_dtype_t w_dtype, int aligned16, int device,
                                        char* buf, size_t len) {
-  if (!buf || len == 0 || op < 0 || op > 8) return RMSNORM_ERR_INVALID_ARG;
+  if (!buf || len == 0 || op < 0 || op > 10) return RMSNORM_ERR_INVALID_ARG;
   buf[0] = 0;
   rmsnorm_status_t st = check_sizes(M, N, 0.f);
   if (st != RMSNORM_OK) return st;
   if (!dtype_pair_ok((int)x_dtype, (int)w_dtype)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
   if (device < 0 && (st = current_device(&device)) != RMSNORM_OK) return st;
   Plan pl;
-  if (op >= 5) {
+  if (op >= 9) {
+    if ((st = ln_plan(op == 10, M, N, (int)x_dtype, (int)w_dtype,
+                      aligned16 != 0 && (N * esize((int)x_dtype)) % 16 == 0, &pl)) != RMSNORM_OK)
+      return st;
+  } else if (op >= 5) {
     const int out = op <= 6 ? kOutFp8 : kOutNvfp4;
     if (out == kOutNvfp4 && N % 16 != 0) return RMSNORM_ERR_INVALID_ARG;
     if ((st = quant_plan(out, op == 6 || op == 8, N, (int)x_dtype, (int)w_dtype,

@@ -83,6 +83,24 @@ struct BwdParams {
   int period;
 };
 
+// LayerNorm (forward and backward).
+struct LnParams {
+  const void* x;
+  const void* dy;       // backward only
+  const void* gamma;
+  const void* beta;     // forward: may be null (no shift)
+  void* y;              // forward: y; backward: dx
+  float* mean;          // forward: optional outputs; backward: the saved
+  float* rstd;          //   statistics (both given) or null (recomputed)
+  float* partial;       // backward: [gridDim.x][2 * ld_half] fp32, [dgamma | dbeta]
+  int64_t M;
+  int N;
+  int nvec;
+  int ld_half;          // a multiple of 4 floats, >= N
+  float eps;
+  float inv_n;
+};
+
 using FwdKernel = void (*)(FwdParams);
 using BwdKernel = void (*)(BwdParams);
 using ReduceKernel = void (*)(const float*, int, int, int, void*, int);
@@ -133,6 +151,20 @@ FwdKernel get_fwd_quant_f32_f32(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_bf16(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_f32(const FwdKey& k);
 ReduceKernel get_dgamma_reduce_kernel();
+
+using LnKernel = void (*)(LnParams);
+using LnReduceKernel = void (*)(const float*, int, int, int, float*, float*);
+struct LnKey {
+  int xd, wd;
+  int family;    // kSubwarp, kCta or kGeneric
+  int g, vpt;
+  bool bwd;
+  bool prefetch;
+};
+LnKernel get_ln_kernel_f32_f32(const LnKey& k);
+LnKernel get_ln_kernel_bf16_bf16(const LnKey& k);
+LnKernel get_ln_kernel_bf16_f32(const LnKey& k);
+LnReduceKernel get_ln_reduce_kernel();
 
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;

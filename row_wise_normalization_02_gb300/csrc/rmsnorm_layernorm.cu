@@ -1,0 +1,549 @@
+// LayerNorm forward and backward kernels for sm_103a.
+//
+// y = (x - mean) / sqrt(var + eps) * gamma + beta per row ("Pre-built kernel
+// library guide", section 1.1 LayerNorm: two passes, mean and then the
+// variance; vector loads, XOR-shuffle and shared-memory reductions,
+// non-temporal output stores).  The pages give no backward; with
+// xhat = (x - mean) rstd and g = dy * gamma it is
+//   dx = rstd (g - mean(g) - xhat mean(g xhat)),
+//   dgamma = sum over rows of dy xhat,   dbeta = sum over rows of dy,
+// with the saved mean and rstd when the caller passes them.
+//
+// Same skeleton as the RMSNorm kernels: the row is read once into registers
+// with 16-byte loads, so the guide's second pass (the variance about the
+// mean, with the corrected two-pass algorithm) runs over registers, not
+// memory; G lanes per row for short rows or
+// one CTA per row, persistent grid, next-row prefetch.  The per-element
+// arithmetic uses the paired fp32 instructions.  The weight gradients follow
+// the deterministic two-stage scheme of the RMSNorm backward: each CTA writes
+// one partial row [dgamma | dbeta], and a column reduction sums the partial
+// rows in a fixed order.
+#include "rmsnorm_fwd_common.cuh"
+
+#ifndef RMSN_PAIR
+#error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
+#endif
+
+namespace rmsn {
+namespace {
+
+// Row reductions: G lanes (shuffles only) or, with G = 0, the whole CTA
+// (shuffles, then shared memory; `parity` alternates per call).
+template <int G>
+__device__ __forceinline__ float row_sum(float v, float* red, int& parity) {
+  if constexpr (G != 0) {
+    return group_sum<G>(v);
+  } else {
+    float t[1] = {v};
+    cta_sum<1>(t, red, parity);
+    parity ^= 1;
+    return t[0];
+  }
+}
+template <int G>
+__device__ __forceinline__ void row_sum2(float& a, float& b, float* red, int& parity) {
+  if constexpr (G != 0) {
+    a = group_sum<G>(a);
+    b = group_sum<G>(b);
+  } else {
+    float t[2] = {a, b};
+    cta_sum<2>(t, red, parity);
+    parity ^= 1;
+    a = t[0];
+    b = t[1];
+  }
+}
+
+// VPT 16-byte vectors of row `row` of a row-major activation (zeros beyond
+// the row or for an invalid row).
+template <typename TX, int VPT>
+__device__ __forceinline__ void load_row(uint4 (&dst)[VPT], const void* base, int64_t row,
+                                         bool valid, int lane, int L, int nvec, int N) {
+  const char* r = static_cast<const char*>(base) + row * (size_t)N * sizeof(TX);
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * L;
+    dst[k] = (valid && v < nvec) ? ld_stream(r + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// The packed weight vectors matching activation vector v (kept packed in
+// registers, unpacked where used).
+template <int GW>
+__device__ __forceinline__ void load_weight(uint4 (&w)[GW], const void* base, int v, bool on) {
+#pragma unroll
+  for (int i = 0; i < GW; ++i)
+    w[i] = on ? ld_cached(static_cast<const char*>(base) + ((size_t)v * GW + i) * 16)
+              : make_uint4(0, 0, 0, 0);
+}
+
+// Sum of x over a slice, then the sum of (x - mean)^2 (paired instructions).
+template <int E, int VPT>
+__device__ __forceinline__ float slice_sum(const uint4 (&s)[VPT]) {
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    float f[E];
+    unpack(s[k], f);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) acc = __fadd2_rn(acc, make_float2(f[2 * i], f[2 * i + 1]));
+  }
+  return acc.x + acc.y;
+}
+// Second pass about the first-pass mean m0: sum of d and of d^2, d = x - m0.
+template <int E, int VPT>
+__device__ __forceinline__ void slice_dev(const uint4 (&s)[VPT], float m0, int lane, int L,
+                                          int nvec, float& sd, float& sq) {
+  float2 a1 = make_float2(0.f, 0.f), a2 = make_float2(0.f, 0.f);
+  const float2 nm = make_float2(-m0, -m0);
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    if (lane + k * L >= nvec) continue;   // padding lanes hold zeros, not x
+    float f[E];
+    unpack(s[k], f);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      const float2 d = __fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm);
+      a1 = __fadd2_rn(a1, d);
+      a2 = __ffma2_rn(d, d, a2);
+    }
+  }
+  sd = a1.x + a1.y;
+  sq = a2.x + a2.y;
+}
+
+// Row statistics by the corrected two-pass algorithm (Chan, Golub and
+// LeVeque): m0 = sum(x) / N, then with d = x - m0 the correction
+// c = sum(d) / N and var = sum(d^2) / N - c^2.  The fp32 rounding of the
+// first sum moves m0 by a few ulp of the row's magnitude; c takes it back, so
+// x - mean stays accurate for rows whose mean is large against their spread.
+// Outputs use (x - m0) - c.
+struct RowStats {
+  float m0, c, rs;
+};
+template <int G, int E, int VPT>
+__device__ __forceinline__ RowStats row_stats(const uint4 (&s)[VPT], float* red, int& parity,
+                                              int lane, int L, int nvec, float inv_n,
+                                              float eps) {
+  RowStats st;
+  st.m0 = row_sum<G>(slice_sum<E, VPT>(s), red, parity) * inv_n;
+  float sd, sq;
+  slice_dev<E, VPT>(s, st.m0, lane, L, nvec, sd, sq);
+  row_sum2<G>(sd, sq, red, parity);
+  st.c = sd * inv_n;
+  st.rs = rsqrtf(fmaxf(fmaf(sq, inv_n, -st.c * st.c), 0.f) + eps);
+  return st;
+}
+
+// ---------------------------------------------------------------------------
+// Forward: G lanes per row (G in 4..32) or, with G = 0, one CTA per row.
+template <typename TX, typename TW, int G, int VPT, bool PF>
+__global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
+    ln_fwd_kernel(const LnParams p) {
+  pdl_begin();
+  constexpr int E = Elem<TX>::kPerVec;
+  __shared__ float red[128];
+  const int L = G ? G : (int)blockDim.x;
+  const int lane = G ? (int)threadIdx.x % G : (int)threadIdx.x;
+  const int rpc = G ? kSubwarpThreads / G : 1;
+  const int grp = G ? (int)threadIdx.x / G : 0;
+
+  constexpr int GW = Cfg<TX, TW>::GW;
+  uint4 gw[VPT][GW], bw[VPT][GW];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * L;
+    load_weight<GW>(gw[k], p.gamma, v, v < p.nvec);
+    load_weight<GW>(bw[k], p.beta, v, v < p.nvec && p.beta != nullptr);
+  }
+  const int64_t stride = (int64_t)gridDim.x * rpc;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  int parity = 0;
+  int64_t base = (int64_t)blockIdx.x * rpc;
+  uint4 cur[VPT], nxt[VPT];
+  load_row<TX, VPT>(cur, p.x, base + grp, base + grp < p.M, lane, L, p.nvec, p.N);
+  for (; base < p.M; base += stride) {
+    const int64_t row = base + grp;
+    const bool valid = row < p.M;
+    const int64_t nrow = row + stride;
+    if (PF) load_row<TX, VPT>(nxt, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+    // pass 1: the mean; pass 2: the variance about it (both over registers)
+    const RowStats st = row_stats<G, E, VPT>(cur, red, parity, lane, L, p.nvec, p.inv_n, p.eps);
+    const float rs = st.rs;
+    if (valid && lane == 0) {
+      if (p.mean != nullptr) p.mean[row] = st.m0 + st.c;
+      if (p.rstd != nullptr) p.rstd[row] = rs;
+    }
+    char* yr = static_cast<char*>(p.y) + row * rb;
+    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c),
+                 r2 = make_float2(rs, rs);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * L;
+      if (valid && v < p.nvec) {
+        float f[E], g[E], b[E];
+        unpack(cur[k], f);
+        unpack_gamma<TW, E, GW>(gw[k], g);
+        unpack_gamma<TW, E, GW>(bw[k], b);
+#pragma unroll
+        for (int i = 0; i < E / 2; ++i) {
+          const float2 t = __fmul2_rn(
+              __fadd2_rn(__fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm), nc), r2);
+          const float2 o = __ffma2_rn(t, make_float2(g[2 * i], g[2 * i + 1]),
+                                      make_float2(b[2 * i], b[2 * i + 1]));
+          f[2 * i] = o.x;
+          f[2 * i + 1] = o.y;
+        }
+        st_stream(yr + (size_t)v * 16, pack(f));
+      }
+    }
+    if (PF) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) cur[k] = nxt[k];
+    } else {
+      load_row<TX, VPT>(cur, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward: same shapes.  dgamma / dbeta partials of this CTA's rows are kept
+// in registers per thread; sub-warp groups are combined through shared memory
+// in group order at the end, and one partial row [dgamma | dbeta] is written.
+template <typename TX, typename TW, int G, int VPT, bool PF>
+__global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
+    ln_bwd_kernel(const LnParams p) {
+  pdl_begin();
+  constexpr int E = Elem<TX>::kPerVec;
+  __shared__ float red[128];
+  extern __shared__ float4 smem4[];                // sub-warp: [rpc][2 * nvec * E]
+  float* sacc = reinterpret_cast<float*>(smem4);
+  const int L = G ? G : (int)blockDim.x;
+  const int lane = G ? (int)threadIdx.x % G : (int)threadIdx.x;
+  const int rpc = G ? kSubwarpThreads / G : 1;
+  const int grp = G ? (int)threadIdx.x / G : 0;
+  const bool saved = p.mean != nullptr;
+
+  constexpr int GW = Cfg<TX, TW>::GW;
+  uint4 gw[VPT][GW];
+  float ag[VPT][E], ab[VPT][E];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * L;
+    load_weight<GW>(gw[k], p.gamma, v, v < p.nvec);
+#pragma unroll
+    for (int e = 0; e < E; ++e) ag[k][e] = ab[k][e] = 0.f;
+  }
+  const int64_t stride = (int64_t)gridDim.x * rpc;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  int parity = 0;
+  int64_t base = (int64_t)blockIdx.x * rpc;
+  uint4 cx[VPT], cd[VPT], nx[VPT], nd[VPT];
+  load_row<TX, VPT>(cx, p.x, base + grp, base + grp < p.M, lane, L, p.nvec, p.N);
+  load_row<TX, VPT>(cd, p.dy, base + grp, base + grp < p.M, lane, L, p.nvec, p.N);
+  for (; base < p.M; base += stride) {
+    const int64_t row = base + grp;
+    const bool valid = row < p.M;
+    const int64_t nrow = row + stride;
+    if (PF) {
+      load_row<TX, VPT>(nx, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+      load_row<TX, VPT>(nd, p.dy, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+    }
+    // xhat = ((x - m0) - c) * rs: the saved statistics (c = 0), or recomputed
+    RowStats st;
+    if (saved) {
+      st.m0 = valid ? p.mean[row] : 0.f;
+      st.c = 0.f;
+      st.rs = valid ? p.rstd[row] : 0.f;
+    } else {
+      st = row_stats<G, E, VPT>(cx, red, parity, lane, L, p.nvec, p.inv_n, p.eps);
+    }
+    const float rs = st.rs;
+    // sum g and sum g xhat, g = dy * gamma
+    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c),
+                 r2 = make_float2(rs, rs);
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      float f[E], d[E], gf[E];
+      unpack(cx[k], f);
+      unpack(cd[k], d);
+      unpack_gamma<TW, E, GW>(gw[k], gf);
+      const bool on = lane + k * L < p.nvec;
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) {
+        const float2 xh =
+            on ? __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm), nc),
+                            r2)
+               : make_float2(0.f, 0.f);
+        const float2 g =
+            __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]), make_float2(gf[2 * i], gf[2 * i + 1]));
+        s1 = __fadd2_rn(s1, g);
+        s2 = __ffma2_rn(g, xh, s2);
+      }
+    }
+    float a = s1.x + s1.y, b = s2.x + s2.y;
+    row_sum2<G>(a, b, red, parity);
+    const float mg = a * p.inv_n, mgx = b * p.inv_n;
+    char* dxr = static_cast<char*>(p.y) + row * rb;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * L;
+      if (valid && v < p.nvec) {
+        float f[E], d[E], o[E], gf[E];
+        unpack(cx[k], f);
+        unpack(cd[k], d);
+        unpack_gamma<TW, E, GW>(gw[k], gf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float xh = ((f[e] - st.m0) - st.c) * rs;
+          const float g = d[e] * gf[e];
+          o[e] = rs * (g - fmaf(xh, mgx, mg));
+          ag[k][e] = fmaf(d[e], xh, ag[k][e]);
+          ab[k][e] += d[e];
+        }
+        st_stream(dxr + (size_t)v * 16, pack(o));
+      }
+    }
+    if (PF) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        cx[k] = nx[k];
+        cd[k] = nd[k];
+      }
+    } else {
+      load_row<TX, VPT>(cx, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+      load_row<TX, VPT>(cd, p.dy, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+    }
+  }
+  if (p.partial == nullptr) return;
+  float* prow = p.partial + (size_t)blockIdx.x * 2 * p.ld_half;
+  if constexpr (G != 0) {
+    const int ncol = p.nvec * E;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * L;
+      if (v < p.nvec) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          sacc[(size_t)grp * 2 * ncol + v * E + e] = ag[k][e];
+          sacc[(size_t)grp * 2 * ncol + ncol + v * E + e] = ab[k][e];
+        }
+      }
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < ncol; j += kSubwarpThreads) {
+      float sg = 0.f, sb = 0.f;
+      for (int q = 0; q < rpc; ++q) {
+        sg += sacc[(size_t)q * 2 * ncol + j];
+        sb += sacc[(size_t)q * 2 * ncol + ncol + j];
+      }
+      prow[j] = sg;
+      prow[p.ld_half + j] = sb;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * L;
+      if (v < p.nvec) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+          reinterpret_cast<float4*>(prow + v * E)[q] =
+              make_float4(ag[k][4 * q], ag[k][4 * q + 1], ag[k][4 * q + 2], ag[k][4 * q + 3]);
+          reinterpret_cast<float4*>(prow + p.ld_half + v * E)[q] =
+              make_float4(ab[k][4 * q], ab[k][4 * q + 1], ab[k][4 * q + 2], ab[k][4 * q + 3]);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Any row (scalar, one row per CTA iteration, 256 threads): three passes over
+// the row in global memory (mean, variance, output); the backward's partial
+// row is accumulated in place in the workspace, each column by the one thread
+// that owns it.
+// The corrected two-pass statistics of a row in global memory (CTA-wide).
+template <typename TX>
+__device__ __forceinline__ RowStats generic_stats(const TX* xr, int N, float* red, int& parity,
+                                                  float inv_n, float eps) {
+  const int tid = threadIdx.x, T = blockDim.x;
+  RowStats st;
+  float s = 0.f;
+  for (int j = tid; j < N; j += T) s += ld_scalar(xr + j);
+  st.m0 = row_sum<0>(s, red, parity) * inv_n;
+  float sd = 0.f, sq = 0.f;
+  for (int j = tid; j < N; j += T) {
+    const float d = ld_scalar(xr + j) - st.m0;
+    sd += d;
+    sq = fmaf(d, d, sq);
+  }
+  row_sum2<0>(sd, sq, red, parity);
+  st.c = sd * inv_n;
+  st.rs = rsqrtf(fmaxf(fmaf(sq, inv_n, -st.c * st.c), 0.f) + eps);
+  return st;
+}
+
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(256) ln_fwd_generic_kernel(const LnParams p) {
+  pdl_begin();
+  __shared__ float red[128];
+  const int tid = threadIdx.x, T = blockDim.x, N = p.N;
+  const TW* gam = static_cast<const TW*>(p.gamma);
+  const TW* bet = static_cast<const TW*>(p.beta);
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const TX* xr = static_cast<const TX*>(p.x) + row * (int64_t)N;
+    const RowStats st = generic_stats(xr, N, red, parity, p.inv_n, p.eps);
+    if (tid == 0) {
+      if (p.mean != nullptr) p.mean[row] = st.m0 + st.c;
+      if (p.rstd != nullptr) p.rstd[row] = st.rs;
+    }
+    TX* yr = static_cast<TX*>(p.y) + row * (int64_t)N;
+    for (int j = tid; j < N; j += T) {
+      const float b = bet ? ld_scalar_ro(bet + j) : 0.f;
+      const float t = ((ld_scalar(xr + j) - st.m0) - st.c) * st.rs;
+      st_scalar(yr + j, fmaf(t, ld_scalar_ro(gam + j), b));
+    }
+  }
+}
+
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(256) ln_bwd_generic_kernel(const LnParams p) {
+  pdl_begin();
+  __shared__ float red[128];
+  const int tid = threadIdx.x, T = blockDim.x, N = p.N;
+  const TW* gam = static_cast<const TW*>(p.gamma);
+  float* prow = p.partial ? p.partial + (size_t)blockIdx.x * 2 * p.ld_half : nullptr;
+  if (prow)
+    for (int j = tid; j < N; j += T) prow[j] = prow[p.ld_half + j] = 0.f;
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const TX* xr = static_cast<const TX*>(p.x) + row * (int64_t)N;
+    const TX* dr = static_cast<const TX*>(p.dy) + row * (int64_t)N;
+    RowStats st;
+    if (p.mean != nullptr) {
+      st.m0 = p.mean[row];
+      st.c = 0.f;
+      st.rs = p.rstd[row];
+    } else {
+      st = generic_stats(xr, N, red, parity, p.inv_n, p.eps);
+    }
+    const float rs = st.rs;
+    float a = 0.f, b = 0.f;
+    for (int j = tid; j < N; j += T) {
+      const float xh = ((ld_scalar(xr + j) - st.m0) - st.c) * rs;
+      const float g = ld_scalar(dr + j) * ld_scalar_ro(gam + j);
+      a += g;
+      b = fmaf(g, xh, b);
+    }
+    row_sum2<0>(a, b, red, parity);
+    const float mg = a * p.inv_n, mgx = b * p.inv_n;
+    TX* dxr = static_cast<TX*>(p.y) + row * (int64_t)N;
+    for (int j = tid; j < N; j += T) {
+      const float xh = ((ld_scalar(xr + j) - st.m0) - st.c) * rs;
+      const float d = ld_scalar(dr + j);
+      st_scalar(dxr + j, rs * (d * ld_scalar_ro(gam + j) - fmaf(xh, mgx, mg)));
+      if (prow) {
+        prow[j] = fmaf(d, xh, prow[j]);
+        prow[p.ld_half + j] += d;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Instantiation table (one dtype pair per translation unit).
+
+template <typename TX, typename TW, bool BWD, bool PF>
+LnKernel pick_shape(const LnKey& k) {
+  if (k.family == kCta) {
+    switch (k.vpt) {
+      case 1: return BWD ? ln_bwd_kernel<TX, TW, 0, 1, PF> : ln_fwd_kernel<TX, TW, 0, 1, PF>;
+      case 2: return BWD ? ln_bwd_kernel<TX, TW, 0, 2, PF> : ln_fwd_kernel<TX, TW, 0, 2, PF>;
+      // the backward keeps gamma and both partials in fp32 registers: at most
+      // 2 vectors per thread
+      case 4: return BWD ? nullptr : ln_fwd_kernel<TX, TW, 0, 4, PF>;
+      case 8: return (BWD || PF) ? nullptr : ln_fwd_kernel<TX, TW, 0, 8, false>;
+      default: return nullptr;
+    }
+  }
+  if (k.family == kSubwarp) {
+#define RMSN_LN(G_, V_)                                                                     \
+  if (k.g == G_ && k.vpt == V_)                                                              \
+    return BWD ? ln_bwd_kernel<TX, TW, G_, V_, PF> : ln_fwd_kernel<TX, TW, G_, V_, PF>;
+    RMSN_LN(4, 1) RMSN_LN(8, 1) RMSN_LN(16, 1) RMSN_LN(32, 1)
+    RMSN_LN(8, 2) RMSN_LN(16, 2) RMSN_LN(32, 2) RMSN_LN(32, 3) RMSN_LN(32, 4)
+#undef RMSN_LN
+  }
+  return nullptr;
+}
+
+template <typename TX, typename TW>
+LnKernel pick_ln(const LnKey& k) {
+  if (k.family == kGeneric)
+    return k.bwd ? ln_bwd_generic_kernel<TX, TW> : ln_fwd_generic_kernel<TX, TW>;
+  if (k.bwd)
+    return k.prefetch ? pick_shape<TX, TW, true, true>(k) : pick_shape<TX, TW, true, false>(k);
+  return k.prefetch ? pick_shape<TX, TW, false, true>(k) : pick_shape<TX, TW, false, false>(k);
+}
+
+#if RMSN_PAIR == 0
+// Stage 2 of the weight gradients: dgamma_j = sum_b partial[b][j] and
+// dbeta_j = sum_b partial[b][ld_half + j] over the P stage-1 CTAs.  Each
+// thread sums one float4 column group over rows ty, ty + 32, ... in order;
+// the 32 row sums are then added in row order: the same bits every run.
+// Launched as a programmatic dependent of stage 1.
+__global__ void __launch_bounds__(kRedCols* kRedRows)
+    ln_reduce_kernel(const float* partial, int P, int N, int ld_half, float* dgamma,
+                     float* dbeta) {
+  pdl_begin();
+  __shared__ float4 sh[kRedRows][kRedCols];
+  const int tx = threadIdx.x % kRedCols, ty = threadIdx.x / kRedCols;
+  const int nq = ld_half / 4;                      // float4 groups per half
+  const int q = blockIdx.x * kRedCols + tx;      // in [0, 2 nq)
+  const bool second = q >= nq;
+  const int qh = second ? q - nq : q;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (q < 2 * nq) {
+    const float4* src = reinterpret_cast<const float4*>(partial) + q;
+    for (int b = ty; b < P; b += kRedRows) {
+      const float4 v = __ldcs(src + (size_t)b * 2 * nq);
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+  }
+  sh[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && q < 2 * nq) {
+    float4 t = sh[0][tx];
+    for (int r = 1; r < kRedRows; ++r) {
+      const float4 v = sh[r][tx];
+      t.x += v.x;
+      t.y += v.y;
+      t.z += v.z;
+      t.w += v.w;
+    }
+    float* out = second ? dbeta : dgamma;
+    const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (qh * 4 + u < N && out != nullptr) out[qh * 4 + u] = tv[u];
+  }
+}
+#endif
+
+}  // namespace
+
+#if RMSN_PAIR == 0
+LnReduceKernel get_ln_reduce_kernel() { return ln_reduce_kernel; }
+LnKernel get_ln_kernel_f32_f32(const LnKey& k) { return pick_ln<float, float>(k); }
+#elif RMSN_PAIR == 1
+LnKernel get_ln_kernel_bf16_bf16(const LnKey& k) { return pick_ln<bf16, bf16>(k); }
+#else
+LnKernel get_ln_kernel_bf16_f32(const LnKey& k) { return pick_ln<bf16, float>(k); }
+#endif
+
+}  // namespace rmsn

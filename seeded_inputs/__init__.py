@@ -120,7 +120,7 @@ def splitmix64_next(state: int) -> int:
 
 
 def make_inputs(wl: "Workload", rows: int | None = None) -> dict:
-    """All input tensors of a workload, keyed by name (x, residual, gamma, dy).
+    """All input tensors of a workload, keyed by name (x, residual, gamma, dy, beta).
 
     ``rows`` limits the activations to the first ``rows`` rows (the streams are
     counter based, so those rows are identical to the full tensor's)."""
@@ -130,7 +130,7 @@ def make_inputs(wl: "Workload", rows: int | None = None) -> dict:
         rec = dict(rec)
         shape = rec.pop("shape", None)
         if shape is None:
-            shape = (wl.N,) if name == "gamma" else (m, wl.N)
+            shape = (wl.N,) if name in ("gamma", "beta") else (m, wl.N)
         elif rows is not None:
             shape = (min(rows, shape[0]),) + tuple(shape[1:])
         out[name] = fill(shape, seed=wl.seed, tensor_id=TENSOR_IDS[name], **rec)

@@ -9,14 +9,15 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 
 # stream ids of the tensors (each tensor draws from its own sub-stream)
-TENSOR_IDS = {"x": 1, "residual": 2, "gamma": 3, "dy": 4}
+TENSOR_IDS = {"x": 1, "residual": 2, "gamma": 3, "dy": 4, "beta": 5}
 
 
 @dataclass(frozen=True)
 class Workload:
     name: str
     op: str                 # "fwd", "fused_add", "bwd", "fused_add_bwd", "fwd_strided",
-                            # "fwd_fp8", "fused_add_fp8", "fwd_nvfp4", "fused_add_nvfp4"
+                            # "fwd_fp8", "fused_add_fp8", "fwd_nvfp4", "fused_add_nvfp4",
+                            # "ln_fwd", "ln_bwd"
     M: int
     N: int
     x_dtype: str            # "f32" | "bf16"
@@ -43,8 +44,10 @@ def tensor_recipes(wl: Workload) -> dict:
         rec["x"] = dict(act, shape=(wl.M // wl.heads, wl.stride_token))
     if wl.op.startswith("fused_add") and wl.op != "fused_add_bwd":
         rec["residual"] = dict(act)
-    if wl.op in ("bwd", "fused_add_bwd"):
+    if wl.op in ("bwd", "fused_add_bwd", "ln_bwd"):
         rec["dy"] = dict(dist="normal", p0=0.0, p1=1.0, dtype=wl.x_dtype)
+    if wl.op == "ln_fwd":
+        rec["beta"] = dict(dist="normal", p0=0.0, p1=0.1, dtype=wl.w_dtype)
     if wl.op == "fused_add_bwd":
         rec["residual"] = dict(dist="normal", p0=0.0, p1=1.0, dtype=wl.x_dtype)  # dres
     return rec
@@ -95,6 +98,13 @@ WORKLOADS = {
                                              store_rstd=False, outlier_fraction=1e-3,
                                              outlier_scale=100.0, global_scale=448.0 * 6 / 128,
                                              tags=("next",)),
+    # LayerNorm at the forward / backward shape: bf16 activations and
+    # weights, beta ~ N(0, 0.1); the backward reads the oracle forward's saved
+    # mean and rstd, and writes dx, dgamma and dbeta
+    "ln_fwd_bf16_m16384_n8192": Workload("ln_fwd_bf16_m16384_n8192", "ln_fwd", 16384, 8192,
+                                         "bf16", "bf16", 1e-5, 6, tags=("next",)),
+    "ln_bwd_bf16_m16384_n8192": Workload("ln_bwd_bf16_m16384_n8192", "ln_bwd", 16384, 8192,
+                                         "bf16", "bf16", 1e-5, 6, tags=("next",)),
     # backward: bf16 activations, fp32 gamma; rstd from the oracle forward
     "bwd_bf16_m16384_n8192": Workload("bwd_bf16_m16384_n8192", "bwd", 16384, 8192, "bf16",
                                       "f32", 1e-5, 3, tags=("headline",)),

@@ -16,7 +16,7 @@ HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
 def header_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(rmsnorm_[a-z0-9_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b((?:rmsnorm|layernorm)_[a-z0-9_]+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")
@@ -133,6 +133,43 @@ def test_quantised_argument_errors_without_gpu(lib, kind, args, status):
             rn.rmsnorm_fwd_nvfp4(a["x"], a["residual"], a["gamma"], a["gs"], a["q"], a["qs"],
                                  a["rstd"], a["M"], a["N"], a["eps"], a["x_dtype"],
                                  a["w_dtype"])
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(mean=FAKE + (5 << 32)), 1),            # mean without rstd
+    (dict(x=None), 1), (dict(N=0), 1), (dict(eps=-1.0), 1),
+    (dict(x_dtype=rn.F32, w_dtype=rn.BF16), 2),
+    (dict(x=FAKE + 1), 3), (dict(dgamma=FAKE + (6 << 32) + 2), 3),
+    (dict(dx=FAKE + 64), 1),                     # dx overlaps x
+    (dict(dgamma=FAKE + (6 << 32), dbeta=FAKE + (6 << 32) + 16), 1),   # dgamma overlaps dbeta
+    (dict(workspace=None), 4), (dict(workspace=FAKE + (8 << 32) + 4), 4),
+])
+def test_layernorm_bwd_argument_errors_without_gpu(lib, args, status):
+    a = dict(dy=FAKE + (1 << 32), x=FAKE, mean=None, rstd=None, gamma=FAKE + (2 << 32),
+             dx=FAKE + (3 << 32), dgamma=FAKE + (6 << 32), dbeta=FAKE + (7 << 32),
+             workspace=FAKE + (8 << 32), ws_bytes=1 << 30, M=4, N=64, eps=1e-5,
+             x_dtype=rn.BF16, w_dtype=rn.BF16)
+    a.update(args)
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.layernorm_bwd(a["dy"], a["x"], a["mean"], a["rstd"], a["gamma"], a["dx"], a["dgamma"],
+                         a["dbeta"], a["workspace"], a["ws_bytes"], a["M"], a["N"], a["eps"],
+                         a["x_dtype"], a["w_dtype"])
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(y=None), 1), (dict(y=FAKE + 32), 1), (dict(beta=FAKE + (2 << 32) + 1), 3),
+    (dict(mean=FAKE + (3 << 32), rstd=FAKE + (3 << 32)), 1),   # mean and rstd alias
+    (dict(N=-4), 1),
+])
+def test_layernorm_fwd_argument_errors_without_gpu(lib, args, status):
+    a = dict(x=FAKE, gamma=FAKE + (1 << 32), beta=None, y=FAKE + (4 << 32), mean=None, rstd=None,
+             M=4, N=64)
+    a.update(args)
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.layernorm_fwd(a["x"], a["gamma"], a["beta"], a["y"], a["mean"], a["rstd"], a["M"],
+                         a["N"], 1e-5, rn.BF16, rn.BF16)
     assert e.value.status == status
 
 

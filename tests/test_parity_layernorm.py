@@ -1,0 +1,253 @@
+"""GPU LayerNorm forward and backward against the oracle, element by element.
+
+Bounds (those of the RMSNorm parity tests): bf16 outputs within 2 bf16 ulp of
+the oracle's once-rounded value, fp32 outputs within 1e-5 (1 + |ref|), the
+weight gradients within 1e-4 of max(|ref|, sqrt(sum of squared terms)).  Two
+sums can cancel: y = t * gamma + beta and dx = rstd (g - mean(g) - xhat
+mean(g xhat)), and so can x - mean inside both; where they do, an fp32
+evaluation is bounded by a few fp32 roundings of the terms (x r gamma,
+mean r gamma, beta; the three dx terms with xhat's own), not of the result, so
+a bf16 element beyond 2 ulp is accepted only within 2 ulp plus that floor (16
+or 64 fp32 units of the terms' magnitude), and the test counts how many
+needed it.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import row_wise_normalization_02_gb300 as rn  # noqa: E402
+
+U32 = 2.0 ** -24
+
+
+def f32(v):
+    return float(np.float32(v))
+
+
+def inputs(M, N, xd, wd, seed, beta=True, mean=0.0):
+    x = si.fill((M, N), seed=seed, tensor_id=1, dtype=xd, p0=mean)
+    g = si.fill(N, seed=seed, tensor_id=3, p0=1.0, p1=0.1, dtype=wd)
+    b = si.fill(N, seed=seed, tensor_id=5, p0=0.0, p1=0.1, dtype=wd) if beta else None
+    dy = si.fill((M, N), seed=seed, tensor_id=4, dtype=xd)
+    return x, g, b, dy
+
+
+# ---------------------------------------------------------------- runners
+
+def run_fwd(x, g, b, eps, xd, wd, offsets=None):
+    M, N = x.shape
+    o = offsets or {}
+    bx, bg = pu.dev(x, o.get("x", 0)), pu.dev(g, o.get("gamma", 0))
+    bb = pu.dev(b, o.get("beta", 0)) if b is not None else None
+    by = pu.empty(M * N, xd, o.get("y", 0))
+    bm, br = pu.empty(M, "f32"), pu.empty(M, "f32")
+    rn.layernorm_fwd(bx.ptr, bg.ptr, bb.ptr if bb else None, by.ptr, bm.ptr, br.ptr, M, N, eps,
+                     xd, wd)
+    torch.cuda.synchronize()
+    for buf in (bx, bg, bb, by, bm, br):
+        if buf is not None:
+            assert buf.guards_ok(), "write outside a buffer"
+    return {"y": by.download(pu.np_dtype(xd)).reshape(M, N), "mean": bm.download(np.float32),
+            "rstd": br.download(np.float32)}
+
+
+def run_bwd(dy, x, mean, rstd, g, eps, xd, wd, want=(True, True), offsets=None):
+    M, N = x.shape
+    o = offsets or {}
+    bdy, bx, bg = pu.dev(dy, o.get("dy", 0)), pu.dev(x, o.get("x", 0)), pu.dev(g)
+    bm = pu.dev(mean) if mean is not None else None
+    br = pu.dev(rstd) if rstd is not None else None
+    bdx = pu.empty(M * N, xd, o.get("dx", 0))
+    bdg = pu.empty(N, "f32") if want[0] else None
+    bdb = pu.empty(N, "f32") if want[1] else None
+    ws = rn.layernorm_bwd_workspace_size(M, N, xd, wd)
+    bws = pu.Buf(max(ws, 16))
+    rn.layernorm_bwd(bdy.ptr, bx.ptr, bm.ptr if bm else None, br.ptr if br else None, bg.ptr,
+                     bdx.ptr, bdg.ptr if bdg else None, bdb.ptr if bdb else None, bws.ptr, ws,
+                     M, N, eps, xd, wd)
+    torch.cuda.synchronize()
+    for buf in (bdy, bx, bg, bm, br, bdx, bdg, bdb, bws):
+        if buf is not None:
+            assert buf.guards_ok(), "write outside a buffer"
+    out = {"dx": bdx.download(pu.np_dtype(xd)).reshape(M, N)}
+    if bdg:
+        out["dgamma"] = bdg.download(np.float32)
+    if bdb:
+        out["dbeta"] = bdb.download(np.float32)
+    return out
+
+
+# ---------------------------------------------------------------- checks
+
+def _bf16_with_floor(gpu_bits, ref_bits, ref64, floor, what):
+    d = pu.bf16_ulp_dist(gpu_bits, ref_bits)
+    strict = d > 2
+    if strict.any():
+        gv = oracle.bf16_array_to_f64(gpu_bits)
+        ok = np.abs(gv - ref64) <= 2 * pu.bf16_ulp_of(ref64) + floor
+        bad = strict & ~ok
+        assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond 2 ulp and the "
+                               f"cancellation floor, at {np.argwhere(bad)[:5].tolist()}")
+        assert strict.sum() <= max(2, 1e-4 * d.size), (
+            f"{what}: {int(strict.sum())} of {d.size} elements needed the cancellation floor")
+    return int(strict.sum())
+
+
+def check_fwd(out, x, g, b, eps, xd, wd):
+    ref = oracle.layernorm_fwd(x, g, b, eps, xd, wd)
+    pu.check_f32(out["mean"], ref["mean64"], what="mean")
+    pu.check_f32(out["rstd"], ref["rstd64"], what="rstd")
+    if xd == "bf16":
+        # y = (x - mean) r gamma + beta: the terms are x r gamma, mean r gamma
+        # and beta, and both sums can cancel
+        bv = oracle.to_f64(b, wd) if b is not None else np.zeros(x.shape[1])
+        rg = ref["rstd64"][:, None] * np.abs(oracle.to_f64(g, wd))[None, :]
+        floor = 16 * U32 * (rg * (np.abs(oracle.to_f64(x, xd)) + np.abs(ref["mean64"])[:, None]) +
+                            np.abs(bv)[None, :])
+        return _bf16_with_floor(out["y"], ref["y"], ref["y64"], floor, "y")
+    pu.check_f32(out["y"], ref["y64"], what="y")
+    return 0
+
+
+def check_bwd(out, dy, x, mean, rstd, g, eps, xd, wd):
+    ref = oracle.layernorm_bwd(dy, x, mean, rstd, g, eps, xd, wd)
+    x64, dy64, g64 = oracle.to_f64(x, xd), oracle.to_f64(dy, xd), oracle.to_f64(g, wd)
+    if mean is None:
+        fw = oracle.layernorm_fwd(x, g, None, eps, xd, wd)
+        mu, r = fw["mean64"], fw["rstd64"]
+    else:
+        mu, r = mean.astype(np.float64), rstd.astype(np.float64)
+    xh = (x64 - mu[:, None]) * r[:, None]
+    gg = dy64 * g64[None, :]
+    n = 0
+    if xd == "bf16":
+        N = x.shape[1]
+        # xhat = (x - mean) r itself carries the cancellation of x - mean
+        xh_mag = np.abs(xh) + r[:, None] * (np.abs(x64) + np.abs(mu)[:, None])
+        floor = 64 * U32 * r[:, None] * (np.abs(gg) + np.abs(gg).sum(1, keepdims=True) / N +
+                                         xh_mag * np.abs(gg * xh).sum(1, keepdims=True) / N)
+        n = _bf16_with_floor(out["dx"], ref["dx"], ref["dx64"], floor, "dx")
+    else:
+        pu.check_f32(out["dx"], ref["dx64"], what="dx")
+    if "dgamma" in out:
+        pu.check_dgamma(out["dgamma"], ref["dgamma64"], ((dy64 * xh) ** 2).sum(0))
+    if "dbeta" in out:
+        pu.check_dgamma(out["dbeta"], ref["dbeta64"], (dy64 ** 2).sum(0))
+    return n
+
+
+PAIRS = [("bf16", "bf16"), ("bf16", "f32"), ("f32", "f32")]
+
+
+# ---------------------------------------------------------------- forward
+
+@pytest.mark.parametrize("xd,wd", PAIRS)
+@pytest.mark.parametrize("N", [16, 128, 1000, 4096, 8192, 2049])
+@pytest.mark.parametrize("beta", [True, False])
+def test_forward(xd, wd, N, beta):
+    x, g, b, _ = inputs(300, N, xd, wd, seed=N, beta=beta, mean=0.5)
+    out = run_fwd(x, g, b, f32(1e-5), xd, wd)
+    check_fwd(out, x, g, b, f32(1e-5), xd, wd)
+
+
+@pytest.mark.parametrize("force", ["subwarp:g=16:vpt=1:cps=1", "subwarp:g=32:vpt=1:pf=0:cps=1",
+                                   "subwarp:g=8:vpt=2:cps=1", "cta:vpt=1:cps=1",
+                                   "cta:vpt=2:t=64:cps=1", "cta:vpt=4:t=32:pf=0:cps=1",
+                                   "generic:cps=1"])
+def test_forward_forced_variants_walk_many_rows(monkeypatch, force):
+    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+    x, g, b, _ = inputs(2000, 128, "bf16", "bf16", seed=3)
+    check_fwd(run_fwd(x, g, b, f32(1e-5), "bf16", "bf16"), x, g, b, f32(1e-5), "bf16", "bf16")
+
+
+def test_forward_unaligned_pointers_and_constant_rows():
+    x, g, b, _ = inputs(40, 256, "bf16", "bf16", seed=4)
+    x[3] = x[3, 0]                      # a constant row: y = beta
+    out = run_fwd(x, g, b, f32(1e-5), "bf16", "bf16", offsets={"x": 2, "y": 2})
+    check_fwd(out, x, g, b, f32(1e-5), "bf16", "bf16")
+    assert np.array_equal(out["y"][3], b)
+
+
+def test_forward_large_mean_small_spread():
+    # mean 64, unit spread: the two-pass variance keeps rstd accurate
+    x, g, b, _ = inputs(64, 4096, "f32", "f32", seed=5, mean=64.0)
+    check_fwd(run_fwd(x, g, b, f32(1e-5), "f32", "f32"), x, g, b, f32(1e-5), "f32", "f32")
+
+
+# ---------------------------------------------------------------- backward
+
+@pytest.mark.parametrize("xd,wd", PAIRS)
+@pytest.mark.parametrize("N", [16, 128, 1000, 4096, 8192, 2049])
+@pytest.mark.parametrize("saved", [True, False])
+def test_backward(xd, wd, N, saved):
+    x, g, _, dy = inputs(300, N, xd, wd, seed=N + 1)
+    eps = f32(1e-5)
+    fw = oracle.layernorm_fwd(x, g, None, eps, xd, wd) if saved else None
+    mean, rstd = (fw["mean"], fw["rstd"]) if saved else (None, None)
+    out = run_bwd(dy, x, mean, rstd, g, eps, xd, wd)
+    check_bwd(out, dy, x, mean, rstd, g, eps, xd, wd)
+
+
+@pytest.mark.parametrize("force", ["subwarp:g=16:vpt=1:cps=1", "subwarp:g=32:vpt=1:pf=0:cps=1",
+                                   "subwarp:g=4:vpt=1:cps=1", "cta:vpt=1:cps=1",
+                                   "cta:vpt=2:t=64:cps=1", "cta:vpt=2:t=64:pf=0:cps=1",
+                                   "generic:cps=1", "generic"])
+@pytest.mark.parametrize("N", [128, 32])
+def test_backward_forced_variants_walk_many_rows(monkeypatch, force, N):
+    if "g=4" in force and N != 32:
+        pytest.skip("4 lanes hold at most 4 vectors")
+    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+    x, g, _, dy = inputs(3000, N, "bf16", "bf16", seed=6)
+    fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
+    out = run_bwd(dy, x, fw["mean"], fw["rstd"], g, f32(1e-5), "bf16", "bf16")
+    check_bwd(out, dy, x, fw["mean"], fw["rstd"], g, f32(1e-5), "bf16", "bf16")
+
+
+def test_backward_weight_gradients_are_deterministic_and_optional():
+    x, g, _, dy = inputs(4096, 1024, "bf16", "bf16", seed=7)
+    a = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16")
+    b = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16")
+    assert np.array_equal(a["dgamma"], b["dgamma"]) and np.array_equal(a["dbeta"], b["dbeta"])
+    only = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16", want=(False, True))
+    assert np.array_equal(only["dbeta"], a["dbeta"]) and np.array_equal(only["dx"], a["dx"])
+    none = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16", want=(False, False))
+    assert np.array_equal(none["dx"], a["dx"])
+
+
+def test_backward_unaligned_pointers():
+    x, g, _, dy = inputs(50, 384, "bf16", "bf16", seed=8)
+    out = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16",
+                  offsets={"x": 2, "dy": 4, "dx": 6})
+    check_bwd(out, dy, x, None, None, g, f32(1e-5), "bf16", "bf16")
+
+
+def test_zero_rows():
+    rn.layernorm_fwd(None, None, None, None, None, None, 0, 64, 1e-5, "bf16", "bf16")
+    dg, db = torch.full((64,), 7.0, device="cuda"), torch.full((64,), 7.0, device="cuda")
+    rn.layernorm_bwd(None, None, None, None, None, None, dg.data_ptr(), db.data_ptr(), None, 0, 0,
+                     64, 1e-5, "bf16", "bf16")
+    torch.cuda.synchronize()
+    assert float(dg.abs().sum()) == 0.0 and float(db.abs().sum()) == 0.0
+
+
+def check_workload(wl, inp):
+    """A LayerNorm workload at full size through the default dispatch."""
+    x, g = inp["x"], inp["gamma"]
+    eps = f32(wl.eps)
+    if wl.op == "ln_fwd":
+        b = inp.get("beta")
+        n = check_fwd(run_fwd(x, g, b, eps, wl.x_dtype, wl.w_dtype), x, g, b, eps, wl.x_dtype,
+                      wl.w_dtype)
+    else:
+        fw = oracle.layernorm_fwd(x, g, None, eps, wl.x_dtype, wl.w_dtype)
+        out = run_bwd(inp["dy"], x, fw["mean"], fw["rstd"], g, eps, wl.x_dtype, wl.w_dtype)
+        n = check_bwd(out, inp["dy"], x, fw["mean"], fw["rstd"], g, eps, wl.x_dtype, wl.w_dtype)
+    print(wl.name, {"floor": n})

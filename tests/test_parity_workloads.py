@@ -29,6 +29,9 @@ def test_workload_matches_oracle(name):
         r = inp["residual"]
         out = pu.run_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd)
         check_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, out, want_rstd=wl.store_rstd)
+    elif wl.op in ("ln_fwd", "ln_bwd"):
+        from tests import test_parity_layernorm as tl
+        tl.check_workload(wl, inp)
     elif wl.op in ("fwd_fp8", "fused_add_fp8", "fwd_nvfp4", "fused_add_nvfp4"):
         from tests import test_parity_quant as tq
         tq.check_workload(wl, inp)
