@@ -881,9 +881,14 @@ LnKernel ln_kernel(const LnKey& k) {
 }
 
 // Plan of the LayerNorm kernels: rows of at most 128 16-byte vectors take the
-// sub-warp form, longer aligned rows one CTA per row (forward: up to 4 vectors
-// per thread, backward: up to 2, since it keeps gamma and the two partials per
-// thread), anything else the scalar kernel.  Next-row prefetch throughout.
+// sub-warp form; longer aligned rows one CTA per row with next-row prefetch --
+// the forward with up to 4 vectors per thread (16384 x 8192 bf16: VPT 4 0.84
+// of the copy bandwidth, VPT 2 / 512 threads 0.69: two row barriers per row
+// cost more in a larger CTA), the backward with up to 2 (0.80; it holds gamma
+// and two partial rows per thread).  The staged backward (rows through the
+// bulk-copy ring) is a forced variant only: at 4 vectors per thread it spills
+// (0.70), at 2 it fits one CTA per SM (0.63).  Anything else: the scalar
+// kernel.
 rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool vec_ok,
                          Plan* res) {
   const int E = per_vec(xd);
@@ -898,7 +903,7 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
     p.rows_per_cta = kSubwarpThreads / p.g;
     p.prefetch = true;
   } else if (vec_ok) {
-    static const int pref_fwd[] = {2, 4, 1}, pref_bwd[] = {2, 1};
+    static const int pref_fwd[] = {4, 2, 1}, pref_bwd[] = {2, 1};
     const int* pref = bwd ? pref_bwd : pref_fwd;
     for (int i = 0; i < (bwd ? 2 : 3); ++i) {
       const int t = round_up((nvec + pref[i] - 1) / pref[i], 32);
@@ -933,6 +938,16 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
           (int64_t)p.threads * p.vpt < nvec)
         return RMSNORM_ERR_INVALID_ARG;
       p.rows_per_cta = 1;
+    } else if (f.family == kStaged) {
+      if (!vec_ok || !bwd) return RMSNORM_ERR_INVALID_ARG;
+      p.family = kStaged;
+      p.vpt = f.vpt ? f.vpt : 4;
+      p.threads = f.threads ? f.threads : round_up((nvec + p.vpt - 1) / p.vpt, 32);
+      if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32 ||
+          (int64_t)p.threads * p.vpt < nvec)
+        return RMSNORM_ERR_INVALID_ARG;
+      p.rows_per_cta = 1;
+      p.stages = f.st;
     } else if (f.family >= 0) {
       return RMSNORM_ERR_INVALID_ARG;
     }
@@ -944,13 +959,29 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
     p.prefetch = false;
     p.rows_per_cta = 1;
   }
+  if (p.family == kStaged) {
+    p.prefetch = false;
+    // ring of [x | dy] row pairs: as many stages as fit the half-SM budget
+    // (two CTAs per SM), at least two, at most kStagedMaxStages
+    const int64_t stage_bytes = 2 * N * esize(xd);
+    if (p.stages <= 0) {
+      int64_t st = (kStagedSmemBudget - kStagedHeader) / stage_bytes;
+      if (st < 2) st = (kStagedSmemMax - kStagedHeader) / stage_bytes;
+      p.stages = (int)(st > kStagedMaxStages ? kStagedMaxStages : st);
+    }
+    if (p.stages < 2 || p.stages > kStagedMaxStages ||
+        kStagedHeader + p.stages * stage_bytes > kStagedSmemMax)
+      return RMSNORM_ERR_INVALID_ARG;
+  }
   if (p.family != kSubwarp) p.g = 0;
   LnKey k{xd, wd, p.family, p.g, p.vpt, bwd, p.prefetch};
   LnKernel fn = ln_kernel(k);
   if (fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
   p.fn = reinterpret_cast<const void*>(fn);
-  // sub-warp backward: the groups' partial rows meet in shared memory
+  // sub-warp backward: the groups' partial rows meet in shared memory;
+  // staged: the ring
   p.smem = (bwd && p.family == kSubwarp) ? p.rows_per_cta * 2 * nvec * E * 4 : 0;
+  if (p.family == kStaged) p.smem = (int)(kStagedHeader + p.stages * 2 * N * esize(xd));
   if (bwd) {
     p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
     const Force fr = read_force();
@@ -1081,7 +1112,8 @@ rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
                       aligned_to(gamma, 16) && (N * (int64_t)xs) % 16 == 0;
   Plan p;
   if ((st = ln_plan(true, M, N, xd, wd, vec_ok, &p)) != RMSNORM_OK) return st;
-  if ((st = size_grid(&p, M, dev)) != RMSNORM_OK) return st;
+  unsigned* status = nullptr;
+  if ((st = size_grid(&p, M, dev, &status)) != RMSNORM_OK) return st;
   if (want && p.grid > prows) p.grid = prows;
   LnParams prm = {};
   prm.x = x;
@@ -1097,6 +1129,9 @@ rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
   prm.ld_half = ld_half;
   prm.eps = eps;
   prm.inv_n = 1.0f / (float)N;
+  prm.stages = p.stages;
+  prm.wait_limit = wait_limit();
+  prm.status = status;
   cudaError_t e = launch(reinterpret_cast<LnKernel>(const_cast<void*>(p.fn)), p.grid, p.threads,
                          p.smem, stream, prm);
   if (e != cudaSuccess) {

@@ -99,6 +99,9 @@ struct LnParams {
   int ld_half;          // a multiple of 4 floats, >= N
   float eps;
   float inv_n;
+  int stages;           // staged backward: row buffers in the shared-memory ring
+  long long wait_limit; // staged backward: clock cycles before a wait gives up
+  unsigned* status;     // device status word (kStatus* bits)
 };
 
 using FwdKernel = void (*)(FwdParams);

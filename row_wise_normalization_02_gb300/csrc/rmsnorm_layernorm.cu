@@ -19,6 +19,7 @@
 // one partial row [dgamma | dbeta], and a column reduction sums the partial
 // rows in a fixed order.
 #include "rmsnorm_fwd_common.cuh"
+#include "rmsnorm_ring.cuh"
 
 #ifndef RMSN_PAIR
 #error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
@@ -65,6 +66,15 @@ __device__ __forceinline__ void load_row(uint4 (&dst)[VPT], const void* base, in
     const int v = lane + k * L;
     dst[k] = (valid && v < nvec) ? ld_stream(r + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
   }
+}
+
+// An empty asm that claims to change v: the compiler must unpack v again
+// where it is used instead of keeping the unpacked fp32 values live across
+// the row's reductions (or hoisting the weights' unpacking out of the row
+// loop), which would cost twice the registers and halve the resident CTAs.
+__device__ __forceinline__ uint4 opaque(uint4 v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+  return v;
 }
 
 // The packed weight vectors matching activation vector v (kept packed in
@@ -182,9 +192,15 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
       const int v = lane + k * L;
       if (valid && v < p.nvec) {
         float f[E], g[E], b[E];
-        unpack(cur[k], f);
-        unpack_gamma<TW, E, GW>(gw[k], g);
-        unpack_gamma<TW, E, GW>(bw[k], b);
+        uint4 gk[GW], bk[GW];
+#pragma unroll
+        for (int w = 0; w < GW; ++w) {
+          gk[w] = opaque(gw[k][w]);
+          bk[w] = opaque(bw[k][w]);
+        }
+        unpack(opaque(cur[k]), f);
+        unpack_gamma<TW, E, GW>(gk, g);
+        unpack_gamma<TW, E, GW>(bk, b);
 #pragma unroll
         for (int i = 0; i < E / 2; ++i) {
           const float2 t = __fmul2_rn(
@@ -202,6 +218,96 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
       for (int k = 0; k < VPT; ++k) cur[k] = nxt[k];
     } else {
       load_row<TX, VPT>(cur, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward per-vector work.  With t = x - m0 (the first-pass mean, or the
+// saved mean with c = 0), xhat = (t - c) rstd and g = dy gamma:
+//   row sums    S1 = sum g,  S2 = sum g (t - c)          (sum g xhat = rstd S2)
+//   dx          = rstd g - rstd mean(g) - rstd xhat mean(g xhat)
+//               = (dy rstd) gamma - (B t + C),  B = rstd^2 mean(g xhat),
+//                                               C = rstd mean(g) - B c
+//   dgamma     += (dy rstd)(t - c),   dbeta += dy
+// all in pairs with the paired fp32 instructions: about a dozen instructions
+// per element, down from eighteen in the direct form.
+struct LnBwdRow {
+  float2 nm, nc, r2, nb, ncc;   // -m0, -c, rstd, -B, -C (each in both lanes)
+};
+
+template <typename TW, int E, int GW>
+__device__ __forceinline__ void ln_bwd_dot(const uint4& xv, const uint4& dv,
+                                           const uint4 (&gk)[GW], float2 nm, float2 nc,
+                                           float2& s1, float2& s2) {
+  float f[E], d[E], g[E];
+  unpack(xv, f);
+  unpack(dv, d);
+  unpack_gamma<TW, E, GW>(gk, g);
+#pragma unroll
+  for (int i = 0; i < E / 2; ++i) {
+    const float2 tc = __fadd2_rn(__fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm), nc);
+    const float2 gg = __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]),
+                                 make_float2(g[2 * i], g[2 * i + 1]));
+    s1 = __fadd2_rn(s1, gg);
+    s2 = __ffma2_rn(gg, tc, s2);
+  }
+}
+
+// The row constants once S1 and S2 are known.
+__device__ __forceinline__ LnBwdRow ln_bwd_row(float m0, float c, float rs, float S1, float S2,
+                                               float inv_n) {
+  const float mg = S1 * inv_n, mgx = rs * S2 * inv_n;
+  const float B = rs * rs * mgx, C = fmaf(-B, c, rs * mg);
+  LnBwdRow r;
+  r.nm = make_float2(-m0, -m0);
+  r.nc = make_float2(-c, -c);
+  r.r2 = make_float2(rs, rs);
+  r.nb = make_float2(-B, -B);
+  r.ncc = make_float2(-C, -C);
+  return r;
+}
+
+template <typename TX, typename TW, int E, int GW>
+__device__ __forceinline__ uint4 ln_bwd_apply(const uint4& xv, const uint4& dv,
+                                              const uint4 (&gk)[GW], const LnBwdRow& r,
+                                              float2 (&ag)[E / 2], float2 (&ab)[E / 2]) {
+  float f[E], d[E], g[E], o[E];
+  unpack(xv, f);
+  unpack(dv, d);
+  unpack_gamma<TW, E, GW>(gk, g);
+#pragma unroll
+  for (int i = 0; i < E / 2; ++i) {
+    const float2 d2 = make_float2(d[2 * i], d[2 * i + 1]);
+    const float2 t = __fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), r.nm);
+    const float2 drs = __fmul2_rn(d2, r.r2);
+    const float2 nu = __ffma2_rn(t, r.nb, r.ncc);                    // -(B t + C)
+    const float2 dx = __ffma2_rn(drs, make_float2(g[2 * i], g[2 * i + 1]), nu);
+    ag[i] = __ffma2_rn(drs, __fadd2_rn(t, r.nc), ag[i]);
+    ab[i] = __fadd2_rn(ab[i], d2);
+    o[2 * i] = dx.x;
+    o[2 * i + 1] = dx.y;
+  }
+  return pack(o);
+}
+
+// One thread's columns of the partial row [dgamma | dbeta] (16-byte stores).
+template <int E, int VPT>
+__device__ __forceinline__ void write_partials(float* prow, int ld_half,
+                                               const float2 (&ag)[VPT][E / 2],
+                                               const float2 (&ab)[VPT][E / 2], int lane, int L,
+                                               int nvec) {
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * L;
+    if (v < nvec) {
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        reinterpret_cast<float4*>(prow + v * E)[q] =
+            make_float4(ag[k][2 * q].x, ag[k][2 * q].y, ag[k][2 * q + 1].x, ag[k][2 * q + 1].y);
+        reinterpret_cast<float4*>(prow + ld_half + v * E)[q] =
+            make_float4(ab[k][2 * q].x, ab[k][2 * q].y, ab[k][2 * q + 1].x, ab[k][2 * q + 1].y);
+      }
     }
   }
 }
@@ -226,13 +332,13 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
 
   constexpr int GW = Cfg<TX, TW>::GW;
   uint4 gw[VPT][GW];
-  float ag[VPT][E], ab[VPT][E];
+  float2 ag[VPT][E / 2], ab[VPT][E / 2];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = lane + k * L;
     load_weight<GW>(gw[k], p.gamma, v, v < p.nvec);
 #pragma unroll
-    for (int e = 0; e < E; ++e) ag[k][e] = ab[k][e] = 0.f;
+    for (int e = 0; e < E / 2; ++e) ag[k][e] = ab[k][e] = make_float2(0.f, 0.f);
   }
   const int64_t stride = (int64_t)gridDim.x * rpc;
   const size_t rb = (size_t)p.N * sizeof(TX);
@@ -241,10 +347,21 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
   uint4 cx[VPT], cd[VPT], nx[VPT], nd[VPT];
   load_row<TX, VPT>(cx, p.x, base + grp, base + grp < p.M, lane, L, p.nvec, p.N);
   load_row<TX, VPT>(cd, p.dy, base + grp, base + grp < p.M, lane, L, p.nvec, p.N);
+  // the saved statistics are loaded one row ahead, with the rows
+  float sm = 0.f, sr = 0.f;
+  if (saved && base + grp < p.M) {
+    sm = p.mean[base + grp];
+    sr = p.rstd[base + grp];
+  }
   for (; base < p.M; base += stride) {
     const int64_t row = base + grp;
     const bool valid = row < p.M;
     const int64_t nrow = row + stride;
+    float nsm = 0.f, nsr = 0.f;
+    if (saved && nrow < p.M) {
+      nsm = p.mean[nrow];
+      nsr = p.rstd[nrow];
+    }
     if (PF) {
       load_row<TX, VPT>(nx, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
       load_row<TX, VPT>(nd, p.dy, nrow, nrow < p.M, lane, L, p.nvec, p.N);
@@ -252,59 +369,38 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
     // xhat = ((x - m0) - c) * rs: the saved statistics (c = 0), or recomputed
     RowStats st;
     if (saved) {
-      st.m0 = valid ? p.mean[row] : 0.f;
+      st.m0 = sm;
       st.c = 0.f;
-      st.rs = valid ? p.rstd[row] : 0.f;
+      st.rs = sr;
     } else {
       st = row_stats<G, E, VPT>(cx, red, parity, lane, L, p.nvec, p.inv_n, p.eps);
     }
-    const float rs = st.rs;
-    // sum g and sum g xhat, g = dy * gamma
-    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c),
-                 r2 = make_float2(rs, rs);
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c);
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      float f[E], d[E], gf[E];
-      unpack(cx[k], f);
-      unpack(cd[k], d);
-      unpack_gamma<TW, E, GW>(gw[k], gf);
-      const bool on = lane + k * L < p.nvec;
+    for (int k = 0; k < VPT; ++k) {   // padding lanes hold zeros: g = 0
+      uint4 gk[GW];
 #pragma unroll
-      for (int i = 0; i < E / 2; ++i) {
-        const float2 xh =
-            on ? __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm), nc),
-                            r2)
-               : make_float2(0.f, 0.f);
-        const float2 g =
-            __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]), make_float2(gf[2 * i], gf[2 * i + 1]));
-        s1 = __fadd2_rn(s1, g);
-        s2 = __ffma2_rn(g, xh, s2);
-      }
+      for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+      ln_bwd_dot<TW, E, GW>(cx[k], cd[k], gk, nm, nc, s1, s2);
     }
     float a = s1.x + s1.y, b = s2.x + s2.y;
     row_sum2<G>(a, b, red, parity);
-    const float mg = a * p.inv_n, mgx = b * p.inv_n;
+    const LnBwdRow rc = ln_bwd_row(st.m0, st.c, st.rs, a, b, p.inv_n);
     char* dxr = static_cast<char*>(p.y) + row * rb;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lane + k * L;
       if (valid && v < p.nvec) {
-        float f[E], d[E], o[E], gf[E];
-        unpack(cx[k], f);
-        unpack(cd[k], d);
-        unpack_gamma<TW, E, GW>(gw[k], gf);
+        uint4 gk[GW];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float xh = ((f[e] - st.m0) - st.c) * rs;
-          const float g = d[e] * gf[e];
-          o[e] = rs * (g - fmaf(xh, mgx, mg));
-          ag[k][e] = fmaf(d[e], xh, ag[k][e]);
-          ab[k][e] += d[e];
-        }
-        st_stream(dxr + (size_t)v * 16, pack(o));
+        for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+        st_stream(dxr + (size_t)v * 16,
+                  ln_bwd_apply<TX, TW, E, GW>(opaque(cx[k]), opaque(cd[k]), gk, rc, ag[k], ab[k]));
       }
     }
+    sm = nsm;
+    sr = nsr;
     if (PF) {
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -325,9 +421,12 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
       const int v = lane + k * L;
       if (v < p.nvec) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          sacc[(size_t)grp * 2 * ncol + v * E + e] = ag[k][e];
-          sacc[(size_t)grp * 2 * ncol + ncol + v * E + e] = ab[k][e];
+        for (int e = 0; e < E / 2; ++e) {
+          float* dg = sacc + (size_t)grp * 2 * ncol + v * E + 2 * e;
+          dg[0] = ag[k][e].x;
+          dg[1] = ag[k][e].y;
+          dg[ncol] = ab[k][e].x;
+          dg[ncol + 1] = ab[k][e].y;
         }
       }
     }
@@ -342,20 +441,128 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
       prow[p.ld_half + j] = sb;
     }
   } else {
+    write_partials<E, VPT>(prow, p.ld_half, ag, ab, lane, L, p.nvec);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Staged backward: one row per CTA iteration; the rows [x | dy] arrive by bulk
+// copies into the shared-memory ring of rmsnorm_ring.cuh and are read from
+// the stage twice (row sums, then dx) instead of being held in registers, so
+// the registers hold only gamma and the two partial rows.  A stage is refilled
+// one row late, at the next row's reduction barrier, which proves every thread
+// has finished reading it -- no extra barrier per row.  Every wait is bounded;
+// a wait that runs out is voted on at the row-sum barrier, the CTA stores
+// nothing more and leaves, and thread 0 drains its copies and raises
+// kStatusWaitTimeout.
+template <typename TX, typename TW, int VPT>
+__global__ void __launch_bounds__(kCtaMaxThreads) ln_bwd_staged_kernel(const LnParams p) {
+  pdl_begin();
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int GW = Cfg<TX, TW>::GW;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Ring rg = ring_of(smem);
+  const int tid = threadIdx.x, T = blockDim.x, S = p.stages;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t nrows = first < p.M ? (p.M - 1 - first) / stride + 1 : 0;
+  const char* xs = static_cast<const char*>(p.x);
+  const char* ds = static_cast<const char*>(p.dy);
+  int64_t issued = ring_start<2>(rg, S, nrows, first, stride, xs, ds, nullptr, rb);
+  const bool saved = p.mean != nullptr;
+
+  uint4 gw[VPT][GW];
+  float2 ag[VPT][E / 2], ab[VPT][E / 2];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    load_weight<GW>(gw[k], p.gamma, v, v < p.nvec);
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) ag[k][e] = ab[k][e] = make_float2(0.f, 0.f);
+  }
+  int parity = 0;
+  int64_t i = 0;
+  bool failed = false;
+  // the saved statistics are loaded one row ahead
+  float sm = 0.f, sr = 0.f;
+  if (saved && nrows > 0) {
+    sm = p.mean[first];
+    sr = p.rstd[first];
+  }
+  for (; i < nrows; ++i) {
+    const int st_i = (int)(i % S);
+    const int64_t row = first + i * stride;
+    float nsm = 0.f, nsr = 0.f;
+    if (saved && i + 1 < nrows) {
+      nsm = p.mean[row + stride];
+      nsr = p.rstd[row + stride];
+    }
+    const bool late =
+        !mbar_wait_bounded(rg.full + st_i, (uint32_t)((i / S) & 1), p.wait_limit);
+    const uint4* stg = reinterpret_cast<const uint4*>(rg.buf + (size_t)st_i * 2 * rb);
+    uint4 cx[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int v = lane + k * L;
-      if (v < p.nvec) {
+      const int v = tid + k * T;
+      cx[k] = (!late && v < p.nvec) ? stg[v] : make_uint4(0, 0, 0, 0);
+    }
+    RowStats st;
+    if (saved) {
+      st.m0 = sm;
+      st.c = 0.f;
+      st.rs = sr;
+    } else {
+      st = row_stats<0, E, VPT>(cx, rg.red, parity, tid, T, p.nvec, p.inv_n, p.eps);
+    }
+    sm = nsm;
+    sr = nsr;
+    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c);
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-          reinterpret_cast<float4*>(prow + v * E)[q] =
-              make_float4(ag[k][4 * q], ag[k][4 * q + 1], ag[k][4 * q + 2], ag[k][4 * q + 3]);
-          reinterpret_cast<float4*>(prow + p.ld_half + v * E)[q] =
-              make_float4(ab[k][4 * q], ab[k][4 * q + 1], ab[k][4 * q + 2], ab[k][4 * q + 3]);
-        }
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (late || v >= p.nvec) continue;
+      uint4 gk[GW];
+#pragma unroll
+      for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+      ln_bwd_dot<TW, E, GW>(cx[k], stg[p.nvec + v], gk, nm, nc, s1, s2);
+    }
+    float t[2] = {s1.x + s1.y, s2.x + s2.y};
+    if (cta_sum_vote<2>(t, rg.red, parity, late)) {
+      failed = true;
+      break;
+    }
+    parity ^= 1;
+    // every thread is past row i - 1's epilogue: its stage takes row i - 1 + S
+    if (tid == 0 && i >= 1 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue_row<2>(rg, issued, first, stride, S, xs, ds, nullptr, rb);
+      ++issued;
+    }
+    const LnBwdRow rc = ln_bwd_row(st.m0, st.c, st.rs, t[0], t[1], p.inv_n);
+    char* dxr = static_cast<char*>(p.y) + row * rb;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < p.nvec) {
+        uint4 gk[GW];
+#pragma unroll
+        for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+        st_stream(dxr + (size_t)v * 16,
+                  ln_bwd_apply<TX, TW, E, GW>(stg[v], stg[p.nvec + v], gk, rc, ag[k], ab[k]));
       }
     }
   }
+  if (failed) {
+    if (tid == 0) {
+      drain(rg, i, issued, S);
+      atomicOr(p.status, kStatusWaitTimeout);
+    }
+    return;
+  }
+  if (p.partial == nullptr) return;
+  write_partials<E, VPT>(p.partial + (size_t)blockIdx.x * 2 * p.ld_half, p.ld_half, ag, ab, tid,
+                         T, p.nvec);
 }
 
 // ---------------------------------------------------------------------------
@@ -483,6 +690,15 @@ template <typename TX, typename TW>
 LnKernel pick_ln(const LnKey& k) {
   if (k.family == kGeneric)
     return k.bwd ? ln_bwd_generic_kernel<TX, TW> : ln_fwd_generic_kernel<TX, TW>;
+  if (k.family == kStaged) {
+    if (!k.bwd) return nullptr;
+    switch (k.vpt) {
+      case 1: return ln_bwd_staged_kernel<TX, TW, 1>;
+      case 2: return ln_bwd_staged_kernel<TX, TW, 2>;
+      case 4: return ln_bwd_staged_kernel<TX, TW, 4>;
+      default: return nullptr;
+    }
+  }
   if (k.bwd)
     return k.prefetch ? pick_shape<TX, TW, true, true>(k) : pick_shape<TX, TW, true, false>(k);
   return k.prefetch ? pick_shape<TX, TW, false, true>(k) : pick_shape<TX, TW, false, false>(k);

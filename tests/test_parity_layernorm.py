@@ -6,10 +6,10 @@ weight gradients within 1e-4 of max(|ref|, sqrt(sum of squared terms)).  Two
 sums can cancel: y = t * gamma + beta and dx = rstd (g - mean(g) - xhat
 mean(g xhat)), and so can x - mean inside both; where they do, an fp32
 evaluation is bounded by a few fp32 roundings of the terms (x r gamma,
-mean r gamma, beta; the three dx terms with xhat's own), not of the result, so
-a bf16 element beyond 2 ulp is accepted only within 2 ulp plus that floor (16
-or 64 fp32 units of the terms' magnitude), and the test counts how many
-needed it.
+mean r gamma, beta; the three dx terms with xhat's own) plus, in the forward,
+rstd's relative error (the 1e-5 its own check allows) times |t gamma| -- not
+by roundings of the result -- so a bf16 element beyond 2 ulp is accepted only
+within 2 ulp plus that floor, and the test counts how many needed it.
 """
 import numpy as np
 import pytest
@@ -110,8 +110,11 @@ def check_fwd(out, x, g, b, eps, xd, wd):
         # and beta, and both sums can cancel
         bv = oracle.to_f64(b, wd) if b is not None else np.zeros(x.shape[1])
         rg = ref["rstd64"][:, None] * np.abs(oracle.to_f64(g, wd))[None, :]
-        floor = 16 * U32 * (rg * (np.abs(oracle.to_f64(x, xd)) + np.abs(ref["mean64"])[:, None]) +
-                            np.abs(bv)[None, :])
+        # (plus rstd's own fp32 error, bounded by the 1e-5 checked above, on
+        # the scaled term t gamma = y - beta)
+        floor = (16 * U32 * (rg * (np.abs(oracle.to_f64(x, xd)) + np.abs(ref["mean64"])[:, None])
+                             + np.abs(bv)[None, :]) +
+                 1e-5 * np.abs(ref["y64"] - bv[None, :]))
         return _bf16_with_floor(out["y"], ref["y"], ref["y64"], floor, "y")
     pu.check_f32(out["y"], ref["y64"], what="y")
     return 0
@@ -199,7 +202,8 @@ def test_backward(xd, wd, N, saved):
 @pytest.mark.parametrize("force", ["subwarp:g=16:vpt=1:cps=1", "subwarp:g=32:vpt=1:pf=0:cps=1",
                                    "subwarp:g=4:vpt=1:cps=1", "cta:vpt=1:cps=1",
                                    "cta:vpt=2:t=64:cps=1", "cta:vpt=2:t=64:pf=0:cps=1",
-                                   "generic:cps=1", "generic"])
+                                   "staged:vpt=1:st=2:cps=1", "staged:vpt=2:t=64:st=3:cps=1",
+                                   "staged:vpt=4:t=32:st=8:cps=1", "generic:cps=1", "generic"])
 @pytest.mark.parametrize("N", [128, 32])
 def test_backward_forced_variants_walk_many_rows(monkeypatch, force, N):
     if "g=4" in force and N != 32:
@@ -209,6 +213,28 @@ def test_backward_forced_variants_walk_many_rows(monkeypatch, force, N):
     fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
     out = run_bwd(dy, x, fw["mean"], fw["rstd"], g, f32(1e-5), "bf16", "bf16")
     check_bwd(out, dy, x, fw["mean"], fw["rstd"], g, f32(1e-5), "bf16", "bf16")
+
+
+@pytest.mark.parametrize("saved", [True, False])
+def test_backward_staged_wait_timeout_is_reported_and_the_context_survives(monkeypatch, saved):
+    # wait limit forced to zero cycles: the first wait for a row still in
+    # flight gives up; the kernel stores nothing more, drains its copies and
+    # raises the flag that rmsnorm_check_device reports and clears
+    x, g, _, dy = inputs(1024, 8192, "bf16", "bf16", seed=44)
+    fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
+    mean, rstd = (fw["mean"], fw["rstd"]) if saved else (None, None)
+    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=3")
+    rn.rmsnorm_check_device()
+    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "0")
+    run_bwd(dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
+    with pytest.raises(rn.RMSNormError) as e:
+        rn.rmsnorm_check_device()
+    assert e.value.status == 6
+    rn.rmsnorm_check_device()
+    monkeypatch.delenv("RMSNORM_WAIT_LIMIT_CYCLES")
+    out = run_bwd(dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
+    check_bwd(out, dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
+    rn.rmsnorm_check_device()
 
 
 def test_backward_weight_gradients_are_deterministic_and_optional():
