@@ -112,6 +112,15 @@ __device__ __forceinline__ float ld_scalar_ro(const T* p) {
 __device__ __forceinline__ void st_scalar(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st_scalar(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// An empty asm that claims to change v: the compiler must unpack v (or
+// recompute what it feeds) again where it is used, instead of keeping fp32
+// values derived from it live across a row's reductions or hoisting them out
+// of the row loop -- which would cost registers and resident CTAs.
+__device__ __forceinline__ uint4 opaque(uint4 v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+  return v;
+}
+
 // ---------------------------------------------------------------- launch order
 
 // Programmatic dependent launch: every kernel of the library is launched so

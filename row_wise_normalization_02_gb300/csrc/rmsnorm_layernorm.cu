@@ -68,15 +68,6 @@ __device__ __forceinline__ void load_row(uint4 (&dst)[VPT], const void* base, in
   }
 }
 
-// An empty asm that claims to change v: the compiler must unpack v again
-// where it is used instead of keeping the unpacked fp32 values live across
-// the row's reductions (or hoisting the weights' unpacking out of the row
-// loop), which would cost twice the registers and halve the resident CTAs.
-__device__ __forceinline__ uint4 opaque(uint4 v) {
-  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
-  return v;
-}
-
 // The packed weight vectors matching activation vector v (kept packed in
 // registers, unpacked where used).
 template <int GW>

@@ -181,6 +181,44 @@ __device__ __forceinline__ void bf16_pair_products(uint32_t x_word, uint32_t g_w
       : "r"(x_word), "r"(g_word));
 }
 
+// x * gamma of two bf16 pairs' worth of packed words (mixed-precision FMA,
+// exact products, the addend -0 keeping a zero product's sign).
+__device__ __forceinline__ void bf16_pair_mul(uint32_t x_word, uint32_t g_word, float& p0,
+                                              float& p1) {
+  asm("{\n\t.reg .b16 xl, xh, gl, gh;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "mov.b32 {gl, gh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, xl, gl, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %1, xh, gh, 0f80000000;\n\t}"
+      : "=f"(p0), "=f"(p1)
+      : "r"(x_word), "r"(g_word));
+}
+
+// The products x * gamma of one vector, recomputed where the epilogue uses
+// them: holding the row pass's products across the reduction would take
+// 4 * E registers per thread and a third of the resident CTAs.
+template <typename TX, typename TW, int E, int GW>
+__device__ __forceinline__ void vec_products(uint4 xv, const uint4 (&gw)[GW],
+                                             float2 (&pp)[E / 2]) {
+  xv = opaque(xv);
+  uint4 gk[GW];
+#pragma unroll
+  for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[w]);
+  if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t gwd[4] = {gk[0].x, gk[0].y, gk[0].z, gk[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bf16_pair_mul(xw[i], gwd[i], pp[i].x, pp[i].y);
+  } else {
+    float f[E], g[E];
+    unpack(xv, f);
+    unpack_gamma<TW, E, GW>(gk, g);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i)
+      pp[i] = __fmul2_rn(make_float2(f[2 * i], f[2 * i + 1]), make_float2(g[2 * i], g[2 * i + 1]));
+  }
+}
+
 // One pass over a thread's slice of the row, in pairs of elements with the
 // paired fp32 instructions (each lane rounds exactly as the scalar op):
 // fused add: h = round(r + x), stored over the residual; then the products
@@ -188,8 +226,11 @@ __device__ __forceinline__ void bf16_pair_products(uint32_t x_word, uint32_t g_w
 // the sum of squares of x in two partial sums added at the end.  bf16 x and
 // gamma skip the unpacking: products and squares come from the packed words
 // through the mixed-precision FMA.
-template <typename TX, typename TW, int VPT, bool FUSED, int E = Cfg<TX, TW>::E,
-          int GW = Cfg<TX, TW>::GW>
+// PROD = false (NVFP4: the block maxima are only needed after the row's
+// reduction) skips the products and maxima: the pass is the sum of squares
+// (and the fused add) alone.
+template <typename TX, typename TW, int VPT, bool FUSED, bool PROD = true,
+          int E = Cfg<TX, TW>::E, int GW = Cfg<TX, TW>::GW>
 __device__ __forceinline__ float quant_row_pass(Slice<VPT, FUSED>& s, const uint4 (&gw)[VPT][GW],
                                                 float2 (&pr)[VPT][E / 2], float (&vmax)[VPT],
                                                 char* hrow, int lane, int L, int nvec,
@@ -216,7 +257,13 @@ __device__ __forceinline__ float quant_row_pass(Slice<VPT, FUSED>& s, const uint
       if (valid && v < nvec) st_stream(hrow + (size_t)v * 16, s.x[k]);
     }
     float m = 0.f;
-    if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
+    if constexpr (!PROD) {
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) {
+        const float2 x2 = make_float2(f[2 * i], f[2 * i + 1]);
+        acc = __ffma2_rn(x2, x2, acc);
+      }
+    } else if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
       const uint32_t xw[4] = {s.x[k].x, s.x[k].y, s.x[k].z, s.x[k].w};
       const uint32_t gwd[4] = {gw[k][0].x, gw[k][0].y, gw[k][0].z, gw[k][0].w};
 #pragma unroll
@@ -245,8 +292,16 @@ __device__ __forceinline__ float quant_row_pass(Slice<VPT, FUSED>& s, const uint
 // Aligned rows: G lanes per row (G in 4..32, 256 / G rows per CTA iteration)
 // or, with G = 0, the whole CTA per row; persistent grid, gamma in registers.
 // PF: the next row's loads are issued before the current row is reduced.
+// Registers: 128 caps the CTA form (up to 512 threads); the plain forms with
+// 4 vectors per thread and prefetch are held to 80 so that three 256-thread
+// CTAs fit an SM (NVFP4 otherwise takes 96 and two; no spills at 80).
+template <int G, int VPT, bool FUSED, int OUT, bool PF>
+constexpr int quant_max_regs() {
+  return G ? 255 : (VPT == 4 && PF && !FUSED) ? 80 : 128;
+}
+
 template <typename TX, typename TW, int G, int VPT, bool FUSED, int OUT, bool PF>
-__global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
+__global__ void __maxnreg__((quant_max_regs<G, VPT, FUSED, OUT, PF>()))
     fwd_quant_kernel(const FwdParams p) {
   pdl_begin();
   using C = Cfg<TX, TW>;
@@ -292,9 +347,8 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
     if (PF) load_aligned<TX, VPT, FUSED>(nxt, p, nrow, nrow < p.M, lane, L);
     float2 pr[VPT][E / 2];
     float vmax[VPT];
-    float ss = quant_row_pass<TX, TW, VPT, FUSED>(s, gw, pr, vmax,
-                                                  static_cast<char*>(p.residual) + row * rb,
-                                                  lane, L, p.nvec, valid);
+    float ss = quant_row_pass<TX, TW, VPT, FUSED, OUT == kOutFp8>(
+        s, gw, pr, vmax, static_cast<char*>(p.residual) + row * rb, lane, L, p.nvec, valid);
     float mx = 0.f;
     if constexpr (OUT == kOutFp8) {
 #pragma unroll
@@ -327,9 +381,11 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
         const int v = lane + k * L;
         if (valid && v < p.nvec) {
           float o[E];
+          float2 pp[E / 2];
+          vec_products<TX, TW, E, GW>(s.x[k], gw[k], pp);
 #pragma unroll
           for (int i = 0; i < E / 2; ++i) {
-            const float2 t = __fmul2_rn(pr[k][i], inv2);
+            const float2 t = __fmul2_rn(pp[i], inv2);
             o[2 * i] = t.x;
             o[2 * i + 1] = t.y;
           }
@@ -343,7 +399,12 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int v = lane + k * L;
-        float a = vmax[k];
+        // the products, formed once here (lanes past the row hold zeros)
+        float2 pp[E / 2];
+        vec_products<TX, TW, E, GW>(s.x[k], gw[k], pp);
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < E / 2; ++i) a = max3(a, fabsf(pp[i].x), fabsf(pp[i].y));
         // every lane takes part: the block's other vectors are in lanes ^1 (^2)
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
         if constexpr (VB == 4) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
@@ -356,7 +417,7 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
           float o[E];
 #pragma unroll
           for (int i = 0; i < E / 2; ++i) {
-            const float2 t = __fmul2_rn(pr[k][i], sc2);
+            const float2 t = __fmul2_rn(pp[i], sc2);
             o[2 * i] = t.x;
             o[2 * i + 1] = t.y;
           }
