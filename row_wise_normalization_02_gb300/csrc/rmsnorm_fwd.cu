@@ -22,6 +22,23 @@
 namespace rmsn {
 namespace {
 
+// One output vector: y = x * rs * gamma, rounded once to TX (bf16 x and
+// gamma: (x * gamma) * rs from the packed words, see bf16x8_scale).
+template <typename TX, typename TW, int GW = Cfg<TX, TW>::GW>
+__device__ __forceinline__ uint4 scale_vec(const uint4& xv, const uint4 (&gw)[GW], float rs) {
+  if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
+    return bf16x8_scale(xv, gw[0], rs);
+  } else {
+    constexpr int E = Cfg<TX, TW>::E;
+    float g[E], o[E];
+    unpack_gamma<TW, E, GW>(gw, g);
+    unpack(xv, o);
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
+    return pack(o);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // kSubwarp: G lanes per row, 256 / G rows per CTA iteration, persistent grid.
 template <typename TX, typename TW, int G, int VPT, bool FUSED, bool PF>
@@ -64,14 +81,7 @@ __global__ void __launch_bounds__(kSubwarpThreads)
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lane + k * G;
-      if (valid && v < p.nvec) {
-        float g[E], o[E];
-        unpack_gamma<TW, E, GW>(gw[k], g);
-        unpack(cur.x[k], o);
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
-        st_stream(yr + (size_t)v * 16, pack(o));
-      }
+      if (valid && v < p.nvec) st_stream(yr + (size_t)v * 16, scale_vec<TX, TW>(cur.x[k], gw[k], rs));
     }
     if (PF) cur = nxt;
     else load_aligned<TX, VPT, FUSED>(cur, p, nrow, nrow < p.M, lane, G);
@@ -120,14 +130,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cta_kernel(const FwdParams
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
-      if (v < p.nvec) {
-        float g[E], o[E];
-        unpack_gamma<TW, E, GW>(gw[k], g);
-        unpack(cur.x[k], o);
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
-        st_stream(yrow + (size_t)v * 16, pack(o));
-      }
+      if (v < p.nvec) st_stream(yrow + (size_t)v * 16, scale_vec<TX, TW>(cur.x[k], gw[k], rs));
     }
     if (PF) cur = nxt;
     else if (nrow < p.M) load_aligned<TX, VPT, FUSED>(cur, p, nrow, true, tid, T);
@@ -183,29 +186,26 @@ __global__ void __launch_bounds__(kSubwarpThreads) fwd_strided_kernel(const FwdP
       ++tn;
     }
     if (PF) load(nxt, tn, hn, row + stride < p.M);
-    float ss = 0.f;
+    float ss = 0.f, ss1 = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      float f[E];
-      unpack(cur[k], f);
+      if constexpr (std::is_same<TX, bf16>::value) {
+        bf16x8_sumsq(cur[k], ss, ss1);
+      } else {
+        float f[E];
+        unpack(cur[k], f);
 #pragma unroll
-      for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+        for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+      }
     }
-    ss = group_sum<G>(ss);
+    ss = group_sum<G>(ss + ss1);
     const float rs = rsqrtf(fmaf(ss, p.inv_n, p.eps));
     if (valid && lane == 0 && p.rstd != nullptr) p.rstd[row] = rs;
     TX* yr = y + t * p.y_st + h * p.y_sh;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lane + k * G;
-      if (valid && v < p.nvec) {
-        float g[E], o[E];
-        unpack_gamma<TW, E, GW>(gw[k], g);
-        unpack(cur[k], o);
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
-        st_stream(yr + v * E, pack(o));
-      }
+      if (valid && v < p.nvec) st_stream(yr + v * E, scale_vec<TX, TW>(cur[k], gw[k], rs));
     }
     if (PF) {
 #pragma unroll

@@ -61,6 +61,52 @@ __device__ __forceinline__ void load_aligned(Slice<VPT, FUSED>& s, const FwdPara
   }
 }
 
+// bf16 rows straight from the packed words, with the mixed-precision FMA
+// (bf16 sources, fp32 accumulate, one rounding): the squares of the 8 values
+// of v into two accumulators (even / odd elements), no unpacking.
+__device__ __forceinline__ void bf16x8_sumsq(const uint4& v, float& a0, float& a1) {
+  asm("{\n\t.reg .b16 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      "mov.b32 {l0, h0}, %2;\n\t"
+      "mov.b32 {l1, h1}, %3;\n\t"
+      "mov.b32 {l2, h2}, %4;\n\t"
+      "mov.b32 {l3, h3}, %5;\n\t"
+      "fma.rn.f32.bf16 %0, l0, l0, %0;\n\t"
+      "fma.rn.f32.bf16 %1, h0, h0, %1;\n\t"
+      "fma.rn.f32.bf16 %0, l1, l1, %0;\n\t"
+      "fma.rn.f32.bf16 %1, h1, h1, %1;\n\t"
+      "fma.rn.f32.bf16 %0, l2, l2, %0;\n\t"
+      "fma.rn.f32.bf16 %1, h2, h2, %1;\n\t"
+      "fma.rn.f32.bf16 %0, l3, l3, %0;\n\t"
+      "fma.rn.f32.bf16 %1, h3, h3, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
+// y = (x * g) * rs for 8 bf16 values x and gamma g: the products are exact in
+// fp32 (formed from the packed halves by the mixed-precision FMA, addend -0
+// to keep a zero product's sign), the scaling is a paired multiply, and each
+// result is rounded once to bf16.
+__device__ __forceinline__ uint4 bf16x8_scale(const uint4& x, const uint4& g, float rs) {
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, gw[4] = {g.x, g.y, g.z, g.w};
+  float o[8];
+  const float2 r2 = make_float2(rs, rs);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float p0, p1;
+    asm("{\n\t.reg .b16 xl, xh, gl, gh;\n\t"
+        "mov.b32 {xl, xh}, %2;\n\t"
+        "mov.b32 {gl, gh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, xl, gl, 0f80000000;\n\t"
+        "fma.rn.f32.bf16 %1, xh, gh, 0f80000000;\n\t}"
+        : "=f"(p0), "=f"(p1)
+        : "r"(xw[i]), "r"(gw[i]));
+    const float2 t = __fmul2_rn(make_float2(p0, p1), r2);
+    o[2 * i] = t.x;
+    o[2 * i + 1] = t.y;
+  }
+  return pack(o);
+}
+
 // Sum of squares of this thread's part of the row.  Fused add: the vectors
 // become h = round(r + x), which is written back over the residual and kept
 // (packed) in s.x for the output pass.
@@ -68,7 +114,7 @@ template <typename TX, int VPT, bool FUSED>
 __device__ __forceinline__ float slice_sumsq(Slice<VPT, FUSED>& s, char* res_row_vec0, int lane,
                                              int stride, int nvec_valid, bool valid) {
   constexpr int E = Elem<TX>::kPerVec;
-  float ss = 0.f;
+  float ss = 0.f, ss1 = 0.f;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     float f[E];
@@ -83,10 +129,14 @@ __device__ __forceinline__ float slice_sumsq(Slice<VPT, FUSED>& s, char* res_row
       const int v = lane + k * stride;
       if (valid && v < nvec_valid) st_stream(res_row_vec0 + (size_t)v * 16, s.x[k]);
     }
+    if constexpr (std::is_same<TX, bf16>::value) {
+      bf16x8_sumsq(s.x[k], ss, ss1);
+    } else {
 #pragma unroll
-    for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+      for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
+    }
   }
-  return ss;
+  return ss + ss1;
 }
 
 }  // namespace
