@@ -280,3 +280,13 @@ def check_workload(wl, inp):
         out = run_bwd(inp["dy"], x, fw["mean"], fw["rstd"], g, eps, wl.x_dtype, wl.w_dtype)
         n = check_bwd(out, inp["dy"], x, fw["mean"], fw["rstd"], g, eps, wl.x_dtype, wl.w_dtype)
     print(wl.name, {"floor": n})
+
+
+@pytest.mark.parametrize("N", [20000, 32768])
+def test_long_rows_take_the_scalar_kernels(N):
+    # beyond 2048 vectors per row: the scalar forward and backward
+    x, g, b, dy = inputs(24, N, "bf16", "bf16", seed=N % 97)
+    eps = f32(1e-5)
+    check_fwd(run_fwd(x, g, b, eps, "bf16", "bf16"), x, g, b, eps, "bf16", "bf16")
+    out = run_bwd(dy, x, None, None, g, eps, "bf16", "bf16")
+    check_bwd(out, dy, x, None, None, g, eps, "bf16", "bf16")

@@ -306,3 +306,15 @@ def check_workload(wl, inp):
     else:
         info = check_nvfp4(out, x, g, eps, wl.x_dtype, wl.w_dtype, wl.global_scale, residual=r)
     print(wl.name, info)
+
+
+@pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("N", [20000, 32768])
+def test_long_rows(kind, N):
+    # up to 4096 vectors per row: CTA form with 8 vectors per thread
+    x, g, r = inputs(24, N, "bf16", "bf16", seed=N % 89, fused=True)
+    out = run(kind, x, g, f32(1e-6), "bf16", "bf16", residual=r, gs=GS)
+    if kind == "fp8":
+        check_fp8(out, x, g, f32(1e-6), "bf16", "bf16", residual=r)
+    else:
+        check_nvfp4(out, x, g, f32(1e-6), "bf16", "bf16", GS, residual=r)
