@@ -398,11 +398,36 @@ def run_ours(args, rank, world):
     e1.record(s_in)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, world, dev)
+
+    # the host link's bound for these bytes: the same copies, whole tensors,
+    # with no kernels and no dependencies (copy in and copy out at once).  The
+    # fused add's residual is both input and output: its copy out reads y (same
+    # size) so that the two directions never touch the same buffer.
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(s_in)
+    s_out.wait_event(c0)
+    for _ in range(Ke):
+        for op, (hin, hout) in zip(ops, pin):
+            with torch.cuda.stream(s_in):
+                for k, t in hin.items():
+                    op["d"][k].copy_(t, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                for k, t in hout.items():
+                    t.copy_(op["d"]["y" if k == "residual" else k], non_blocking=True)
+    s_in.wait_stream(s_out)
+    c1.record(s_in)
+    torch.cuda.synchronize()
+    copy_ms = c0.elapsed_time(c1) / Ke
     e2e = {"value": round(job_gbs(step_bytes, e2e_ms, world), 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
            "ms_per_step": round(e2e_ms, 3), "pinned": True,
            "pipeline": f"3 streams (copy in / kernels / copy out), fwd and fused add in "
-                       f"{chunks} row chunks"}
+                       f"{chunks} row chunks",
+           "copy_bound_ms_per_step": round(copy_ms, 3),
+           "frac_of_copy_bound": round(copy_ms / e2e_ms, 4),
+           "copy_bound": "the same host<->device copies alone (no kernels, no dependencies, "
+                         "both directions at once), timed on this GPU"}
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 4),
@@ -637,7 +662,10 @@ def run_sweep(args):
         wl = si.WORKLOADS[name]
         inp = si.make_inputs(wl)
         sets = device_sets(wl, inp, dev, l2, rn)
-        for d in sets:   # saved statistics for the backward (untimed forward)
+        # saved statistics for the backward (untimed forward, default variant
+        # even when RMSNORM_FORCE_VARIANT names a backward-only one)
+        forced = os.environ.pop("RMSNORM_FORCE_VARIANT", None)
+        for d in sets:
             if wl.op == "ln_bwd":
                 gam = d["gamma"]
                 rn.layernorm_fwd(d["x"], gam, None, d["y"], d["mean"], d["rstd"], wl.M, wl.N,
@@ -647,6 +675,9 @@ def run_sweep(args):
                 break
             rn.rmsnorm_fwd(d["x"], d["gamma"], d["y"], d["rstd"], wl.M, wl.N,
                            float(np.float32(wl.eps)), wl.x_dtype, wl.w_dtype, stream)
+        torch.cuda.synchronize()
+        if forced is not None:
+            os.environ["RMSNORM_FORCE_VARIANT"] = forced
         launches = [make_launch(wl, d, stream, rn) for d in sets]
         us = [time_rotation(launches, args.steps, args.warmup, stream) * 1e3
               for _ in range(args.rounds)]

@@ -36,7 +36,8 @@ constexpr int64_t kStagedSmemMax = 226 * 1024;
 constexpr long long kDefaultWaitLimit = 1LL << 32;   // clock cycles (about 2 s)
 
 // Clock cycles a staged kernel waits for a row before giving up: the
-// RMSNORM_WAIT_LIMIT_CYCLES environment variable (a test knob), else ~2 s.
+// RMSNORM_WAIT_LIMIT_CYCLES environment variable (a test knob; a negative
+// value makes every wait give up at once), else ~2 s.
 long long wait_limit() {
   const char* s = getenv("RMSNORM_WAIT_LIMIT_CYCLES");
   if (s && *s) return atoll(s);
@@ -204,6 +205,7 @@ struct Plan {
                              // the dgamma partial rows), unless below 1 CTA/SM
   int period = 1;            // kRagged: the grid is a multiple of it
   int cta_per_sm_cap = 0;    // 0: occupancy limit
+  int l2_ahead = 0;          // LayerNorm register kernels: L2 lookahead in iterations
   const void* fn = nullptr;
   FwdKernel fwd = nullptr;
   BwdKernel bwd = nullptr;
@@ -288,7 +290,8 @@ int ragged_period(int64_t bytes) {
 // runs; a forced variant that cannot serve the call is an argument error.
 struct Force {
   bool on = false;
-  int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0, st = 0, mr = -1;
+  int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0, st = 0, mr = -1,
+      l2 = -1;
 };
 
 Force read_force() {
@@ -320,6 +323,7 @@ Force read_force() {
     else if (!strcmp(tok, "cps")) f.cps = v;
     else if (!strcmp(tok, "st")) f.st = v;
     else if (!strcmp(tok, "mr")) f.mr = v;
+    else if (!strcmp(tok, "l2")) f.l2 = v;
   }
   return f;
 }
@@ -497,9 +501,11 @@ void describe(int op, const Plan& p, char* buf, size_t len) {
                               "fwd_strided", "fwd_fp8",   "fused_add_fp8", "fwd_nvfp4",
                               "fused_add_nvfp4", "layernorm_fwd", "layernorm_bwd"};
   const bool bwd = op == kBwd || op == kFusedBwd;
-  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d", ops[op],
+  char l2[16] = "";
+  if (p.l2_ahead > 0) snprintf(l2, sizeof l2, "/l2ahead%d", p.l2_ahead);
+  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d%s", ops[op],
            family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
-           bwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem);
+           bwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem, l2);
 }
 
 // ---------------------------------------------------------------- launches
@@ -958,11 +964,19 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
     if (f.pf >= 0) p.prefetch = f.pf != 0;
     p.cta_per_sm_cap = f.cps;
   }
+  // register kernels: besides the next row held in registers, the rows two
+  // iterations ahead are requested into L2, doubling the bytes in flight per
+  // SM without holding registers for them (measured, 16384 x 8192 bf16: fwd
+  // 0.88 -> 0.93, bwd 0.82 -> 0.92 of the copy peak; 65536 x 1024: bwd 0.77 ->
+  // 0.83, but the sub-warp forward loses, 0.93 -> 0.84, so it goes without)
+  if (p.prefetch && (p.family == kCta || (p.family == kSubwarp && bwd))) p.l2_ahead = 2;
+  if (f.on && f.l2 >= 0) p.l2_ahead = f.l2;
   if (p.family == kGeneric) {
     p.g = p.vpt = 0;
     p.prefetch = false;
     p.rows_per_cta = 1;
   }
+  if (p.family == kGeneric || p.family == kStaged) p.l2_ahead = 0;
   if (p.family == kStaged) {
     p.prefetch = false;
     // ring of [x | dy] row pairs: as many stages as fit the half-SM budget
@@ -1039,6 +1053,7 @@ rmsnorm_status_t ln_fwd_impl(const void* x, const void* gamma, const void* beta,
   prm.nvec = vec_ok ? (int)(N / per_vec(xd)) : 0;
   prm.eps = eps;
   prm.inv_n = 1.0f / (float)N;
+  prm.l2_rows = p.l2_ahead;
   const cudaError_t e =
       launch(reinterpret_cast<LnKernel>(const_cast<void*>(p.fn)), p.grid, p.threads, p.smem,
              stream, prm);
@@ -1136,6 +1151,7 @@ rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
   prm.stages = p.stages;
   prm.wait_limit = wait_limit();
   prm.status = status;
+  prm.l2_rows = p.l2_ahead;
   cudaError_t e = launch(reinterpret_cast<LnKernel>(const_cast<void*>(p.fn)), p.grid, p.threads,
                          p.smem, stream, prm);
   if (e != cudaSuccess) {

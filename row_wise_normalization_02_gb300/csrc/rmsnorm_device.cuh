@@ -238,6 +238,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Ask for `bytes` of global memory (address 16-byte aligned, size a multiple
+// of 16) to be brought into L2 ahead of use: a hint served by the bulk-copy
+// unit, with nothing to wait for and no registers held.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Non-blocking test of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;
@@ -266,10 +273,12 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity, uint32_
 }
 
 // Wait for the phase with the given parity to complete; false once `limit`
-// SM clock cycles have passed without completion (limit <= 0: do not wait
-// at all, only test).
+// SM clock cycles have passed without completion (limit 0: only test once;
+// limit < 0: give up at once without testing, so that every wait runs out --
+// the deterministic form of the timeout path for tests).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   long long limit) {
+  if (limit < 0) return false;
   if (mbar_test(bar, parity)) return true;
   if (limit <= 0) return false;
   const long long t0 = clock64();

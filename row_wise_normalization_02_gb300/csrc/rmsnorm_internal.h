@@ -102,6 +102,8 @@ struct LnParams {
   int stages;           // staged backward: row buffers in the shared-memory ring
   long long wait_limit; // staged backward: clock cycles before a wait gives up
   unsigned* status;     // device status word (kStatus* bits)
+  int l2_rows;          // register kernels: rows of the CTA's walk fetched into L2
+                        // this many iterations ahead (0: none)
 };
 
 using FwdKernel = void (*)(FwdParams);

@@ -78,33 +78,118 @@ __device__ __forceinline__ void load_weight(uint4 (&w)[GW], const void* base, in
               : make_uint4(0, 0, 0, 0);
 }
 
-// Sum of x over a slice, then the sum of (x - mean)^2 (paired instructions).
-template <int E, int VPT>
+// Element arithmetic on bf16 rows straight from the packed words, with the
+// mixed-precision FMA (bf16 sources, fp32 addend, one rounding): x * 1 + a is
+// x + a rounded once, the same bits as unpacking and adding, in one
+// instruction per element instead of an unpack and half a paired add.
+// d = x - m for the 8 values of v.
+__device__ __forceinline__ void bf16x8_minus(const uint4& v, float nm, float (&d)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .b16 l, h, one;\n\t"
+        "mov.b16 one, 0x3F80;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, l, one, %3;\n\t"
+        "fma.rn.f32.bf16 %1, h, one, %3;\n\t}"
+        : "=f"(d[2 * i]), "=f"(d[2 * i + 1])
+        : "r"(w[i]), "f"(nm));
+}
+// a0 += even elements of v, a1 += odd elements (in element order).
+__device__ __forceinline__ void bf16x8_accumulate(const uint4& v, float& a0, float& a1) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .b16 l, h, one;\n\t"
+        "mov.b16 one, 0x3F80;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, l, one, %0;\n\t"
+        "fma.rn.f32.bf16 %1, h, one, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w[i]));
+}
+// p = a * b for 8 bf16 pairs: exact in fp32 (addend -0 keeps a zero
+// product's sign), the same bits as unpacking both and multiplying.
+__device__ __forceinline__ void bf16x8_products(const uint4& a, const uint4& b, float (&p)[8]) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, 0f80000000;\n\t"
+        "fma.rn.f32.bf16 %1, ah, bh, 0f80000000;\n\t}"
+        : "=f"(p[2 * i]), "=f"(p[2 * i + 1])
+        : "r"(aw[i]), "r"(bw[i]));
+}
+
+// d = x - m for the E values of one activation vector (rounded once).
+template <typename TX, int E>
+__device__ __forceinline__ void vec_minus(const uint4& v, float nm, float (&d)[E]) {
+  if constexpr (std::is_same<TX, bf16>::value) {
+    bf16x8_minus(v, nm, d);
+  } else {
+    unpack(v, d);
+    const float2 n2 = make_float2(nm, nm);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      const float2 t = __fadd2_rn(make_float2(d[2 * i], d[2 * i + 1]), n2);
+      d[2 * i] = t.x;
+      d[2 * i + 1] = t.y;
+    }
+  }
+}
+// g = dy * gamma for one activation vector (exact for bf16 pairs).
+template <typename TX, typename TW, int E, int GW>
+__device__ __forceinline__ void vec_dy_gamma(const uint4& dv, const uint4 (&gk)[GW],
+                                             float (&g)[E]) {
+  if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
+    bf16x8_products(dv, gk[0], g);
+  } else {
+    float d[E], w[E];
+    unpack(dv, d);
+    unpack_gamma<TW, E, GW>(gk, w);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      const float2 t = __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]),
+                                  make_float2(w[2 * i], w[2 * i + 1]));
+      g[2 * i] = t.x;
+      g[2 * i + 1] = t.y;
+    }
+  }
+}
+
+// Sum of x over a slice (even and odd elements in two accumulators), then
+// the sum of (x - m0) and of its square.
+template <typename TX, int E, int VPT>
 __device__ __forceinline__ float slice_sum(const uint4 (&s)[VPT]) {
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
-    float f[E];
-    unpack(s[k], f);
+    if constexpr (std::is_same<TX, bf16>::value) {
+      bf16x8_accumulate(s[k], acc.x, acc.y);
+    } else {
+      float f[E];
+      unpack(s[k], f);
 #pragma unroll
-    for (int i = 0; i < E / 2; ++i) acc = __fadd2_rn(acc, make_float2(f[2 * i], f[2 * i + 1]));
+      for (int i = 0; i < E / 2; ++i) acc = __fadd2_rn(acc, make_float2(f[2 * i], f[2 * i + 1]));
+    }
   }
   return acc.x + acc.y;
 }
 // Second pass about the first-pass mean m0: sum of d and of d^2, d = x - m0.
-template <int E, int VPT>
+template <typename TX, int E, int VPT>
 __device__ __forceinline__ void slice_dev(const uint4 (&s)[VPT], float m0, int lane, int L,
                                           int nvec, float& sd, float& sq) {
   float2 a1 = make_float2(0.f, 0.f), a2 = make_float2(0.f, 0.f);
-  const float2 nm = make_float2(-m0, -m0);
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     if (lane + k * L >= nvec) continue;   // padding lanes hold zeros, not x
     float f[E];
-    unpack(s[k], f);
+    vec_minus<TX, E>(s[k], -m0, f);
 #pragma unroll
     for (int i = 0; i < E / 2; ++i) {
-      const float2 d = __fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm);
+      const float2 d = make_float2(f[2 * i], f[2 * i + 1]);
       a1 = __fadd2_rn(a1, d);
       a2 = __ffma2_rn(d, d, a2);
     }
@@ -122,18 +207,29 @@ __device__ __forceinline__ void slice_dev(const uint4 (&s)[VPT], float m0, int l
 struct RowStats {
   float m0, c, rs;
 };
-template <int G, int E, int VPT>
+template <int G, typename TX, int E, int VPT>
 __device__ __forceinline__ RowStats row_stats(const uint4 (&s)[VPT], float* red, int& parity,
                                               int lane, int L, int nvec, float inv_n,
                                               float eps) {
   RowStats st;
-  st.m0 = row_sum<G>(slice_sum<E, VPT>(s), red, parity) * inv_n;
+  st.m0 = row_sum<G>(slice_sum<TX, E, VPT>(s), red, parity) * inv_n;
   float sd, sq;
-  slice_dev<E, VPT>(s, st.m0, lane, L, nvec, sd, sq);
+  slice_dev<TX, E, VPT>(s, st.m0, lane, L, nvec, sd, sq);
   row_sum2<G>(sd, sq, red, parity);
   st.c = sd * inv_n;
   st.rs = rsqrtf(fmaxf(fmaf(sq, inv_n, -st.c * st.c), 0.f) + eps);
   return st;
+}
+
+// The rows [base, base + rows) of a row-major activation, from `ahead`
+// iterations of the CTA's walk later, requested into L2 by one thread.
+__device__ __forceinline__ void l2_ahead(const void* a, const LnParams& p, int64_t base,
+                                         int64_t stride, int rows, size_t rb) {
+  if (p.l2_rows <= 0 || threadIdx.x != 0) return;
+  const int64_t first = base + (int64_t)p.l2_rows * stride;
+  if (first >= p.M) return;
+  const int64_t n = p.M - first < rows ? p.M - first : rows;
+  bulk_prefetch_l2(static_cast<const char*>(a) + first * rb, (uint32_t)(n * rb));
 }
 
 // ---------------------------------------------------------------------------
@@ -168,16 +264,16 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
     const bool valid = row < p.M;
     const int64_t nrow = row + stride;
     if (PF) load_row<TX, VPT>(nxt, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
+    l2_ahead(p.x, p, base, stride, rpc, rb);
     // pass 1: the mean; pass 2: the variance about it (both over registers)
-    const RowStats st = row_stats<G, E, VPT>(cur, red, parity, lane, L, p.nvec, p.inv_n, p.eps);
+    const RowStats st = row_stats<G, TX, E, VPT>(cur, red, parity, lane, L, p.nvec, p.inv_n, p.eps);
     const float rs = st.rs;
     if (valid && lane == 0) {
       if (p.mean != nullptr) p.mean[row] = st.m0 + st.c;
       if (p.rstd != nullptr) p.rstd[row] = rs;
     }
     char* yr = static_cast<char*>(p.y) + row * rb;
-    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c),
-                 r2 = make_float2(rs, rs);
+    const float2 nc = make_float2(-st.c, -st.c), r2 = make_float2(rs, rs);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lane + k * L;
@@ -189,13 +285,13 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
           gk[w] = opaque(gw[k][w]);
           bk[w] = opaque(bw[k][w]);
         }
-        unpack(opaque(cur[k]), f);
+        vec_minus<TX, E>(opaque(cur[k]), -st.m0, f);
         unpack_gamma<TW, E, GW>(gk, g);
         unpack_gamma<TW, E, GW>(bk, b);
 #pragma unroll
         for (int i = 0; i < E / 2; ++i) {
-          const float2 t = __fmul2_rn(
-              __fadd2_rn(__fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm), nc), r2);
+          const float2 t =
+              __fmul2_rn(__fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nc), r2);
           const float2 o = __ffma2_rn(t, make_float2(g[2 * i], g[2 * i + 1]),
                                       make_float2(b[2 * i], b[2 * i + 1]));
           f[2 * i] = o.x;
@@ -227,19 +323,20 @@ struct LnBwdRow {
   float2 nm, nc, r2, nb, ncc;   // -m0, -c, rstd, -B, -C (each in both lanes)
 };
 
-template <typename TW, int E, int GW>
+// C: the correction c is applied (recomputed statistics); with the saved
+// statistics c = 0 and the add is left out.
+template <typename TX, typename TW, int E, int GW, bool C>
 __device__ __forceinline__ void ln_bwd_dot(const uint4& xv, const uint4& dv,
-                                           const uint4 (&gk)[GW], float2 nm, float2 nc,
+                                           const uint4 (&gk)[GW], float nm, float2 nc,
                                            float2& s1, float2& s2) {
-  float f[E], d[E], g[E];
-  unpack(xv, f);
-  unpack(dv, d);
-  unpack_gamma<TW, E, GW>(gk, g);
+  float t[E], g[E];
+  vec_minus<TX, E>(xv, nm, t);
+  vec_dy_gamma<TX, TW, E, GW>(dv, gk, g);
 #pragma unroll
   for (int i = 0; i < E / 2; ++i) {
-    const float2 tc = __fadd2_rn(__fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), nm), nc);
-    const float2 gg = __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]),
-                                 make_float2(g[2 * i], g[2 * i + 1]));
+    float2 tc = make_float2(t[2 * i], t[2 * i + 1]);
+    if (C) tc = __fadd2_rn(tc, nc);
+    const float2 gg = make_float2(g[2 * i], g[2 * i + 1]);
     s1 = __fadd2_rn(s1, gg);
     s2 = __ffma2_rn(gg, tc, s2);
   }
@@ -259,22 +356,22 @@ __device__ __forceinline__ LnBwdRow ln_bwd_row(float m0, float c, float rs, floa
   return r;
 }
 
-template <typename TX, typename TW, int E, int GW>
+template <typename TX, typename TW, int E, int GW, bool C>
 __device__ __forceinline__ uint4 ln_bwd_apply(const uint4& xv, const uint4& dv,
                                               const uint4 (&gk)[GW], const LnBwdRow& r,
                                               float2 (&ag)[E / 2], float2 (&ab)[E / 2]) {
   float f[E], d[E], g[E], o[E];
-  unpack(xv, f);
+  vec_minus<TX, E>(xv, r.nm.x, f);
   unpack(dv, d);
   unpack_gamma<TW, E, GW>(gk, g);
 #pragma unroll
   for (int i = 0; i < E / 2; ++i) {
     const float2 d2 = make_float2(d[2 * i], d[2 * i + 1]);
-    const float2 t = __fadd2_rn(make_float2(f[2 * i], f[2 * i + 1]), r.nm);
+    const float2 t = make_float2(f[2 * i], f[2 * i + 1]);
     const float2 drs = __fmul2_rn(d2, r.r2);
     const float2 nu = __ffma2_rn(t, r.nb, r.ncc);                    // -(B t + C)
     const float2 dx = __ffma2_rn(drs, make_float2(g[2 * i], g[2 * i + 1]), nu);
-    ag[i] = __ffma2_rn(drs, __fadd2_rn(t, r.nc), ag[i]);
+    ag[i] = __ffma2_rn(drs, C ? __fadd2_rn(t, r.nc) : t, ag[i]);
     ab[i] = __fadd2_rn(ab[i], d2);
     o[2 * i] = dx.x;
     o[2 * i + 1] = dx.y;
@@ -357,6 +454,8 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
       load_row<TX, VPT>(nx, p.x, nrow, nrow < p.M, lane, L, p.nvec, p.N);
       load_row<TX, VPT>(nd, p.dy, nrow, nrow < p.M, lane, L, p.nvec, p.N);
     }
+    l2_ahead(p.x, p, base, stride, rpc, rb);
+    l2_ahead(p.dy, p, base, stride, rpc, rb);
     // xhat = ((x - m0) - c) * rs: the saved statistics (c = 0), or recomputed
     RowStats st;
     if (saved) {
@@ -364,32 +463,41 @@ __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
       st.c = 0.f;
       st.rs = sr;
     } else {
-      st = row_stats<G, E, VPT>(cx, red, parity, lane, L, p.nvec, p.inv_n, p.eps);
+      st = row_stats<G, TX, E, VPT>(cx, red, parity, lane, L, p.nvec, p.inv_n, p.eps);
     }
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c);
+    const float2 nc = make_float2(-st.c, -st.c);
+    auto dot = [&](auto corr) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {   // padding lanes hold zeros: g = 0
-      uint4 gk[GW];
+      for (int k = 0; k < VPT; ++k) {   // padding lanes hold zeros: g = 0
+        uint4 gk[GW];
 #pragma unroll
-      for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
-      ln_bwd_dot<TW, E, GW>(cx[k], cd[k], gk, nm, nc, s1, s2);
-    }
+        for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+        ln_bwd_dot<TX, TW, E, GW, decltype(corr)::value>(cx[k], cd[k], gk, -st.m0, nc, s1, s2);
+      }
+    };
+    if (saved) dot(std::false_type{});
+    else dot(std::true_type{});
     float a = s1.x + s1.y, b = s2.x + s2.y;
     row_sum2<G>(a, b, red, parity);
     const LnBwdRow rc = ln_bwd_row(st.m0, st.c, st.rs, a, b, p.inv_n);
     char* dxr = static_cast<char*>(p.y) + row * rb;
+    auto apply = [&](auto corr) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = lane + k * L;
-      if (valid && v < p.nvec) {
-        uint4 gk[GW];
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lane + k * L;
+        if (valid && v < p.nvec) {
+          uint4 gk[GW];
 #pragma unroll
-        for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
-        st_stream(dxr + (size_t)v * 16,
-                  ln_bwd_apply<TX, TW, E, GW>(opaque(cx[k]), opaque(cd[k]), gk, rc, ag[k], ab[k]));
+          for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+          st_stream(dxr + (size_t)v * 16,
+                    ln_bwd_apply<TX, TW, E, GW, decltype(corr)::value>(
+                        opaque(cx[k]), opaque(cd[k]), gk, rc, ag[k], ab[k]));
+        }
       }
-    }
+    };
+    if (saved) apply(std::false_type{});
+    else apply(std::true_type{});
     sm = nsm;
     sr = nsr;
     if (PF) {
@@ -503,21 +611,26 @@ __global__ void __launch_bounds__(kCtaMaxThreads) ln_bwd_staged_kernel(const LnP
       st.c = 0.f;
       st.rs = sr;
     } else {
-      st = row_stats<0, E, VPT>(cx, rg.red, parity, tid, T, p.nvec, p.inv_n, p.eps);
+      st = row_stats<0, TX, E, VPT>(cx, rg.red, parity, tid, T, p.nvec, p.inv_n, p.eps);
     }
     sm = nsm;
     sr = nsr;
-    const float2 nm = make_float2(-st.m0, -st.m0), nc = make_float2(-st.c, -st.c);
+    const float2 nc = make_float2(-st.c, -st.c);
     float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+    auto dot = [&](auto corr) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = tid + k * T;
-      if (late || v >= p.nvec) continue;
-      uint4 gk[GW];
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * T;
+        if (late || v >= p.nvec) continue;
+        uint4 gk[GW];
 #pragma unroll
-      for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
-      ln_bwd_dot<TW, E, GW>(cx[k], stg[p.nvec + v], gk, nm, nc, s1, s2);
-    }
+        for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+        ln_bwd_dot<TX, TW, E, GW, decltype(corr)::value>(cx[k], stg[p.nvec + v], gk, -st.m0,
+                                                          nc, s1, s2);
+      }
+    };
+    if (saved) dot(std::false_type{});
+    else dot(std::true_type{});
     float t[2] = {s1.x + s1.y, s2.x + s2.y};
     if (cta_sum_vote<2>(t, rg.red, parity, late)) {
       failed = true;
@@ -532,17 +645,22 @@ __global__ void __launch_bounds__(kCtaMaxThreads) ln_bwd_staged_kernel(const LnP
     }
     const LnBwdRow rc = ln_bwd_row(st.m0, st.c, st.rs, t[0], t[1], p.inv_n);
     char* dxr = static_cast<char*>(p.y) + row * rb;
+    auto apply = [&](auto corr) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = tid + k * T;
-      if (v < p.nvec) {
-        uint4 gk[GW];
+      for (int k = 0; k < VPT; ++k) {
+        const int v = tid + k * T;
+        if (v < p.nvec) {
+          uint4 gk[GW];
 #pragma unroll
-        for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
-        st_stream(dxr + (size_t)v * 16,
-                  ln_bwd_apply<TX, TW, E, GW>(stg[v], stg[p.nvec + v], gk, rc, ag[k], ab[k]));
+          for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+          st_stream(dxr + (size_t)v * 16,
+                    ln_bwd_apply<TX, TW, E, GW, decltype(corr)::value>(
+                        stg[v], stg[p.nvec + v], gk, rc, ag[k], ab[k]));
+        }
       }
-    }
+    };
+    if (saved) apply(std::false_type{});
+    else apply(std::true_type{});
   }
   if (failed) {
     if (tid == 0) {

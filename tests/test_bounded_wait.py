@@ -1,9 +1,9 @@
 """The bounded waits of the bulk-copy staged kernels, exercised without any
-fault: the wait limit is forced to zero cycles (RMSNORM_WAIT_LIMIT_CYCLES), so
-the first wait for a row that is still in flight gives up.  The kernel must
-then store nothing more, wait for its own copies, raise the timeout flag and
-return; rmsnorm_check_device reports it, clears it, and the context stays
-usable for a normal call."""
+fault: a negative wait limit (RMSNORM_WAIT_LIMIT_CYCLES=-1) makes every wait
+for a row give up at once, whether or not the row has arrived.  The kernel
+must then store nothing more, wait (with its own bound) for the copies it has
+in flight, raise the timeout flag and return; rmsnorm_check_device reports
+it, clears it, and the context stays usable for a normal call."""
 import numpy as np
 import pytest
 
@@ -32,7 +32,7 @@ def test_timeout_is_reported_and_the_context_survives(monkeypatch, op):
     x, dy, g = _data(M, N, seed=41)
     monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
     rn.rmsnorm_check_device()                    # start from a clear flag
-    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "0")
+    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     if op == "fwd":
         pu.run_fwd(x, g, eps, "bf16", "bf16")
     elif op == "fused":

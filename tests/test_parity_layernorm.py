@@ -220,15 +220,15 @@ def test_backward_forced_variants_walk_many_rows(monkeypatch, force, N):
 
 @pytest.mark.parametrize("saved", [True, False])
 def test_backward_staged_wait_timeout_is_reported_and_the_context_survives(monkeypatch, saved):
-    # wait limit forced to zero cycles: the first wait for a row still in
-    # flight gives up; the kernel stores nothing more, drains its copies and
-    # raises the flag that rmsnorm_check_device reports and clears
+    # a negative wait limit: every wait for a row gives up at once; the kernel
+    # stores nothing more, drains its copies and raises the flag that
+    # rmsnorm_check_device reports and clears
     x, g, _, dy = inputs(1024, 8192, "bf16", "bf16", seed=44)
     fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
     mean, rstd = (fw["mean"], fw["rstd"]) if saved else (None, None)
     monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=3")
     rn.rmsnorm_check_device()
-    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "0")
+    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     run_bwd(dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
     with pytest.raises(rn.RMSNormError) as e:
         rn.rmsnorm_check_device()

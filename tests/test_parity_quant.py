@@ -229,13 +229,13 @@ def test_staged_ring_long_rows(monkeypatch, xd, wd, N, kind, fused):
 
 @pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
 def test_staged_wait_timeout_is_reported_and_the_context_survives(monkeypatch, kind):
-    # the wait limit forced to zero cycles: the first wait for a row still in
-    # flight gives up; the kernel stores nothing more, drains its copies and
-    # raises the flag that rmsnorm_check_device reports and clears
+    # a negative wait limit: every wait for a row gives up at once; the kernel
+    # stores nothing more, drains its copies and raises the flag that
+    # rmsnorm_check_device reports and clears
     x, g, r = inputs(1024, 8192, "bf16", "bf16", seed=43, fused=True)
     monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
     rn.rmsnorm_check_device()
-    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "0")
+    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     run(kind, x, g, f32(1e-6), "bf16", "bf16", residual=r, gs=GS)
     with pytest.raises(rn.RMSNormError) as e:
         rn.rmsnorm_check_device()
