@@ -414,6 +414,14 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32) return RMSNORM_ERR_INVALID_ARG;
   }
 
+  // L2 lookahead (rows two iterations ahead, see the LayerNorm plan): in the
+  // sub-warp backward with next-row prefetch only (262144 x 128 bf16: 0.80 ->
+  // 0.85 of the copy peak); the forward kernels lost with it (16384 x 8192:
+  // 0.97 -> 0.93), so they are built without it
+  if (bwd && p.family == kSubwarp && p.prefetch) p.l2_ahead = 2;
+  if (f.on && f.l2 >= 0) p.l2_ahead = f.l2;
+  if (!bwd || p.family != kSubwarp || !p.prefetch) p.l2_ahead = 0;
+
   // kernel and shared memory
   if (p.family == kStaged) {
     // ring of row buffers: as many stages as fit a half-SM budget (two CTAs
@@ -603,6 +611,7 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   prm.wait_limit = wait_limit();
   prm.status = status;
   prm.period = pl.period;
+  prm.l2_rows = pl.l2_ahead;
   const cudaError_t e = launch(pl.fwd, pl.grid, pl.threads, pl.smem, stream, prm);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -1271,6 +1280,7 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   prm.wait_limit = wait_limit();
   prm.status = status;
   prm.period = pl.period;
+  prm.l2_rows = pl.l2_ahead;
   cudaError_t e = launch(pl.bwd, pl.grid, pl.threads, pl.smem, stream, prm);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -115,6 +115,16 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
     const bool valid = row < p.M;
     const int64_t nrow = row + stride;
     if (PF) bload_aligned<TX, VPT, HAS_RSTD, DRES>(nxt, p, nrow, nrow < p.M, lane, G);
+    // with the next rows in registers, the rows after them are requested
+    // into L2 (compiled into the prefetching forms only: the others keep
+    // their register budget)
+    if (PF && p.l2_rows > 0 && threadIdx.x == 0) {
+      const int64_t ahead = base + (int64_t)p.l2_rows * stride;
+      const size_t rb = (size_t)p.N * sizeof(TX);
+      l2_prefetch_rows(p.x, ahead, RPC, p.M, rb);
+      l2_prefetch_rows(p.dy, ahead, RPC, p.M, rb);
+      if (DRES) l2_prefetch_rows(p.dres, ahead, RPC, p.M, rb);
+    }
 
     float dot = 0.f, ss = 0.f;
 #pragma unroll

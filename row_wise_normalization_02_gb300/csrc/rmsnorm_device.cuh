@@ -245,6 +245,15 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Rows [first, first + rows) of a row-major array with rows of rb bytes
+// (16-byte aligned), clipped to its M rows, requested into L2.
+__device__ __forceinline__ void l2_prefetch_rows(const void* a, int64_t first, int64_t rows,
+                                                 int64_t M, size_t rb) {
+  if (first >= M) return;
+  const int64_t n = M - first < rows ? M - first : rows;
+  bulk_prefetch_l2(static_cast<const char*>(a) + first * rb, (uint32_t)(n * rb));
+}
+
 // Non-blocking test of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;

@@ -60,6 +60,8 @@ struct FwdParams {
   // NVFP4 global scale
   void* qs;
   float gs;
+  int l2_rows;        // register kernels: rows of the CTA's walk fetched into L2
+                      // this many iterations ahead (0: none)
 };
 
 struct BwdParams {
@@ -81,6 +83,7 @@ struct BwdParams {
   long long wait_limit;
   unsigned* status;
   int period;
+  int l2_rows;        // register kernels: L2 lookahead in iterations (0: none)
 };
 
 // LayerNorm (forward and backward).

@@ -226,10 +226,7 @@ __device__ __forceinline__ RowStats row_stats(const uint4 (&s)[VPT], float* red,
 __device__ __forceinline__ void l2_ahead(const void* a, const LnParams& p, int64_t base,
                                          int64_t stride, int rows, size_t rb) {
   if (p.l2_rows <= 0 || threadIdx.x != 0) return;
-  const int64_t first = base + (int64_t)p.l2_rows * stride;
-  if (first >= p.M) return;
-  const int64_t n = p.M - first < rows ? p.M - first : rows;
-  bulk_prefetch_l2(static_cast<const char*>(a) + first * rb, (uint32_t)(n * rb));
+  l2_prefetch_rows(a, base + (int64_t)p.l2_rows * stride, rows, p.M, rb);
 }
 
 // ---------------------------------------------------------------------------
