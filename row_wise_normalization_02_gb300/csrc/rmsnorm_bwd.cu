@@ -46,6 +46,51 @@ __device__ __forceinline__ void load_gamma_vec(const void* gamma, int v, float (
   }
 }
 
+// Per-vector work of the register backward kernels with the paired fp32
+// instructions.  Row sums: dot += sum g dy x over even / odd elements in two
+// lanes (and ss += sum x^2 when the rstd is recomputed).
+template <int E, bool SS>
+__device__ __forceinline__ void bwd_vec_sums(const uint4& xv, const uint4& dv,
+                                             const float (&g)[E], float2& dot, float2& ss) {
+  float xf[E], df[E];
+  unpack(xv, xf);
+  unpack(dv, df);
+#pragma unroll
+  for (int i = 0; i < E / 2; ++i) {
+    const float2 x2 = make_float2(xf[2 * i], xf[2 * i + 1]);
+    const float2 gd = __fmul2_rn(make_float2(g[2 * i], g[2 * i + 1]),
+                                 make_float2(df[2 * i], df[2 * i + 1]));
+    dot = __ffma2_rn(gd, x2, dot);
+    if (SS) ss = __ffma2_rn(x2, x2, ss);
+  }
+}
+// dx = r (g dy - x c) (+ dres) and acc += dy x r, element by element with the
+// same operations as the scalar form, two at a time.
+template <int E, bool DRES>
+__device__ __forceinline__ uint4 bwd_vec_apply(const uint4& xv, const uint4& dv,
+                                               const uint4& rv, const float (&g)[E], float r,
+                                               float c, float (&acc)[E]) {
+  float xf[E], df[E], rf[E], o[E];
+  unpack(xv, xf);
+  unpack(dv, df);
+  if (DRES) unpack(rv, rf);
+  const float2 r2 = make_float2(r, r), nc = make_float2(-c, -c);
+#pragma unroll
+  for (int i = 0; i < E / 2; ++i) {
+    const float2 x2 = make_float2(xf[2 * i], xf[2 * i + 1]);
+    const float2 d2 = make_float2(df[2 * i], df[2 * i + 1]);
+    const float2 gd = __fmul2_rn(make_float2(g[2 * i], g[2 * i + 1]), d2);
+    float2 t = __fmul2_rn(__ffma2_rn(x2, nc, gd), r2);
+    if (DRES) t = __fadd2_rn(t, make_float2(rf[2 * i], rf[2 * i + 1]));
+    const float2 a = __ffma2_rn(__fmul2_rn(d2, x2), r2, make_float2(acc[2 * i], acc[2 * i + 1]));
+    o[2 * i] = t.x;
+    o[2 * i + 1] = t.y;
+    acc[2 * i] = a.x;
+    acc[2 * i + 1] = a.y;
+  }
+  return pack(o);
+}
+
 template <int VPT, bool DRES = false>
 struct BSlice {
   uint4 x[VPT];
@@ -82,7 +127,7 @@ __device__ __forceinline__ void bload_aligned(BSlice<VPT, DRES>& s, const BwdPar
 // dgamma partials in registers; the row groups of a CTA are combined in
 // shared memory (in group order) at the end.
 template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF, bool DRES>
-__global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdParams p) {
+__device__ __forceinline__ void bwd_subwarp_body(const BwdParams& p) {
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int RPC = kSubwarpThreads / G;
@@ -126,19 +171,11 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
       if (DRES) l2_prefetch_rows(p.dres, ahead, RPC, p.M, rb);
     }
 
-    float dot = 0.f, ss = 0.f;
+    float2 dot2 = make_float2(0.f, 0.f), ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      float xf[E], df[E];
-      unpack(cur.x[k], xf);
-      unpack(cur.dy[k], df);
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        dot = fmaf(g[k][e] * df[e], xf[e], dot);
-        if (!HAS_RSTD) ss = fmaf(xf[e], xf[e], ss);
-      }
-    }
-    dot = group_sum<G>(dot);
+    for (int k = 0; k < VPT; ++k)
+      bwd_vec_sums<E, !HAS_RSTD>(cur.x[k], cur.dy[k], g[k], dot2, ss2);
+    float dot = group_sum<G>(dot2.x + dot2.y), ss = ss2.x + ss2.y;
     float r;
     if constexpr (HAS_RSTD) {
       r = cur.r;
@@ -151,17 +188,9 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = lane + k * G;
-      float xf[E], df[E], o[E], rf[E];
-      unpack(cur.x[k], xf);
-      unpack(cur.dy[k], df);
-      if (DRES) unpack(cur.dr[k], rf);
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
-        if (DRES) o[e] += rf[e];
-        acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
-      }
-      if (valid && v < p.nvec) st_stream(dxr + (size_t)v * 16, pack(o));
+      const uint4 o = bwd_vec_apply<E, DRES>(cur.x[k], cur.dy[k], cur.dr[DRES ? k : 0], g[k], r,
+                                             c, acc[k]);
+      if (valid && v < p.nvec) st_stream(dxr + (size_t)v * 16, o);
     }
     if (PF) cur = nxt;
     else bload_aligned<TX, VPT, HAS_RSTD, DRES>(cur, p, nrow, nrow < p.M, lane, G);
@@ -186,6 +215,21 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
     for (int q = 0; q < RPC; ++q) s += sacc[q * ncol + j];
     prow[j] = s;
   }
+}
+
+// Two entry points: the compiler's own register choice, and one held to two
+// resident 256-thread CTAs per SM (128 registers) for the plain backward with
+// two or three vectors per thread, where the paired arithmetic would otherwise
+// take the full-warp, three-vector form to 158 registers and one CTA.  (Asking
+// every form for its minimum explicitly grows the one-vector forms from ~60
+// to 72-95 registers, so the others keep the plain bound.)
+template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF, bool DRES>
+__global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdParams p) {
+  bwd_subwarp_body<TX, TW, G, VPT, HAS_RSTD, PF, DRES>(p);
+}
+template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF, bool DRES>
+__global__ void __launch_bounds__(kSubwarpThreads, 2) bwd_subwarp_kernel_2cta(const BwdParams p) {
+  bwd_subwarp_body<TX, TW, G, VPT, HAS_RSTD, PF, DRES>(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -336,10 +380,15 @@ __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
 
 template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
 BwdKernel pick_subwarp(int g, int vpt, bool pf) {
-#define RMSN_SW(G_, V_)                                                    \
-  if (g == G_ && vpt == V_)                                                \
-    return pf ? bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, true, DRES>   \
-              : bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, false, DRES>;
+#define RMSN_SW(G_, V_)                                                         \
+  if (g == G_ && vpt == V_) {                                                   \
+    if constexpr (V_ >= 2 && V_ <= 3 && !DRES)                                  \
+      return pf ? bwd_subwarp_kernel_2cta<TX, TW, G_, V_, HAS_RSTD, true, DRES>  \
+                : bwd_subwarp_kernel_2cta<TX, TW, G_, V_, HAS_RSTD, false, DRES>; \
+    else                                                                        \
+      return pf ? bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, true, DRES>       \
+                : bwd_subwarp_kernel<TX, TW, G_, V_, HAS_RSTD, false, DRES>;     \
+  }
   RMSN_SW(4, 1) RMSN_SW(8, 1) RMSN_SW(16, 1) RMSN_SW(32, 1)
   RMSN_SW(8, 2) RMSN_SW(16, 2) RMSN_SW(32, 2) RMSN_SW(32, 3) RMSN_SW(32, 4)
 #undef RMSN_SW
