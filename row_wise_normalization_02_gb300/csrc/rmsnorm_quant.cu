@@ -257,7 +257,9 @@ __device__ __forceinline__ float quant_row_pass(Slice<VPT, FUSED>& s, const uint
       if (valid && v < nvec) st_stream(hrow + (size_t)v * 16, s.x[k]);
     }
     float m = 0.f;
-    if constexpr (!PROD) {
+    if constexpr (!PROD && !FUSED && std::is_same<TX, bf16>::value) {
+      bf16x8_sumsq(s.x[k], acc.x, acc.y);   // squares from the packed words
+    } else if constexpr (!PROD) {
 #pragma unroll
       for (int i = 0; i < E / 2; ++i) {
         const float2 x2 = make_float2(f[2 * i], f[2 * i + 1]);
