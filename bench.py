@@ -78,25 +78,32 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The files the step's kernels are compiled from: the forward and fused-add
+# register kernels, the staged backward and its stage 2, and what they include.
+STEP_KERNEL_SOURCES = ("rmsnorm_fwd.cu", "rmsnorm_fwd_common.cuh", "rmsnorm_staged.cu",
+                       "rmsnorm_ring.cuh", "rmsnorm_device.cuh", "rmsnorm_internal.h")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_normalization_02_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in STEP_KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(op: str):
+def ncu_traffic(op: str, variant: str):
     """DRAM bytes per launch of an op from the committed ncu summary, or None
-    when the summary is missing or was taken on other kernel sources."""
+    when the summary is missing, was taken on other kernel sources, or on
+    another variant than the one the dispatch picks now."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_hash") != source_hash():
+    if d.get("source_hash") != source_hash() or d.get("variants", {}).get(op) != variant:
         return None
     v = d.get("per_launch_bytes", {}).get(op)
     return int(v) if v is not None else None
@@ -323,7 +330,7 @@ def run_ours(args, rank, world):
     dom = max(per_op, key=lambda k: per_op[k]["avg_us"])
     d = per_op[dom]
     roofline = {"bound": "hbm", "achieved": d["gbs"], "peak": peak, "unit": "GB/s",
-                "frac": round(d["gbs"] / peak, 4), "traffic": ncu_traffic(dom),
+                "frac": round(d["gbs"] / peak, 4), "traffic": ncu_traffic(dom, d["variant"]),
                 "kernel": f"{dom} ({d['workload']}, {d['variant']})",
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src ==
                 "measured" else "fallback 6800 GB/s"}

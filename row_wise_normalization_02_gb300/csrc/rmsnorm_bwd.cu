@@ -13,8 +13,8 @@
 // library reduces dgamma in a fixed order so the result is bit-for-bit
 // reproducible: stage 1 runs a persistent grid of P CTAs with a fixed
 // row -> CTA map, each CTA accumulating its rows' dy*x*r per column in fp32
-// and writing one partial row; stage 2 sums the P partial rows per column in
-// a fixed order.  Like every kernel here, stage 2 is a programmatic dependent
+// and writing one partial row; stage 2 (dgamma_reduce_kernel, built with the
+// staged kernels) sums the P partial rows per column in a fixed order.  Like every kernel here, stage 2 is a programmatic dependent
 // launch: its launch overlaps stage 1, and it waits for stage 1 to complete
 // before reading the partial rows.
 #include <type_traits>
@@ -433,74 +433,10 @@ BwdKernel pick_rstd(const BwdKey& k) {
   return k.has_rstd ? pick_family<TX, TW, true>(k) : pick_family<TX, TW, false>(k);
 }
 
-#if RMSN_PAIR == 0
-// Stage 2: dgamma_j = sum_b partial[b][j] over the P stage-1 CTAs, in a fixed
-// order, written in fp32 or (out_bf16) rounded once to bf16.  The order:
-// thread (tx, ty) adds rows b = ty, ty + kRedRows, ... in sequence,
-// then the kRedRows chunk sums are added in ty order.  Loads are issued in
-// batches of 8 ahead of the adds (the order of the adds does not change).
-// Launched as a programmatic dependent of stage 1; griddepcontrol.wait
-// returns once stage 1 has completed and its writes are visible.
-__global__ void __launch_bounds__(kRedCols* kRedRows)
-    dgamma_reduce_kernel(const float* partial, int P, int N, int ld, void* dgamma, int out_bf16) {
-  pdl_begin();
-  __shared__ float4 sh[kRedRows][kRedCols];
-  const int tx = threadIdx.x % kRedCols, ty = threadIdx.x / kRedCols;
-  const int q = blockIdx.x * kRedCols + tx;       // float4 column group
-  const int nq = ld / 4;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (q < nq) {
-    const float4* src = reinterpret_cast<const float4*>(partial) + q;
-    int b = ty;
-    constexpr int B = 8;
-    for (; b + (B - 1) * kRedRows < P; b += B * kRedRows) {
-      float4 v[B];
-#pragma unroll
-      for (int u = 0; u < B; ++u) v[u] = __ldcs(src + (size_t)(b + u * kRedRows) * nq);
-#pragma unroll
-      for (int u = 0; u < B; ++u) {
-        s.x += v[u].x;
-        s.y += v[u].y;
-        s.z += v[u].z;
-        s.w += v[u].w;
-      }
-    }
-    for (; b < P; b += kRedRows) {
-      const float4 v = __ldcs(src + (size_t)b * nq);
-      s.x += v.x;
-      s.y += v.y;
-      s.z += v.z;
-      s.w += v.w;
-    }
-  }
-  sh[ty][tx] = s;
-  __syncthreads();
-  if (ty == 0 && q < nq) {
-    float4 t = sh[0][tx];
-    for (int r = 1; r < kRedRows; ++r) {
-      const float4 v = sh[r][tx];
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
-    }
-    const int j = q * 4;
-    const float tv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (j + u < N) {
-        if (out_bf16) static_cast<bf16*>(dgamma)[j + u] = __float2bfloat16_rn(tv[u]);
-        else static_cast<float*>(dgamma)[j + u] = tv[u];
-      }
-    }
-  }
-}
-#endif
 
 }  // namespace
 
 #if RMSN_PAIR == 0
-ReduceKernel get_dgamma_reduce_kernel() { return dgamma_reduce_kernel; }
 BwdKernel get_bwd_kernel_f32_f32(const BwdKey& k) { return pick_rstd<float, float>(k); }
 #elif RMSN_PAIR == 1
 BwdKernel get_bwd_kernel_bf16_bf16(const BwdKey& k) { return pick_rstd<bf16, bf16>(k); }
