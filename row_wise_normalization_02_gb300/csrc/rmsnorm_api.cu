@@ -404,7 +404,10 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (!p.vpt) p.vpt = 4;
       if (!f.threads) p.threads = round_up((nvec + p.vpt - 1) / p.vpt, 32);
       if ((int64_t)p.threads * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
-      p.stages = f.st;
+      // st= sets the ring depth; without it a forced staged plan keeps the
+      // default's depth, or takes as many stages as fit when the default is
+      // another family
+      if (f.st > 0 || f.family == kStaged) p.stages = f.st;
     } else if (p.family == kGeneric) {
       if (!f.threads) p.threads = 256;
       if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
