@@ -263,6 +263,7 @@ def run_ours(args, rank, world):
         host.append(inp)
     torch.cuda.synchronize()
 
+    copy_gbs = inrun_copy_gbs(dev, stream)
     K, W = args.steps, args.warmup
     with torch.cuda.stream(stream):
         for _ in range(W):
@@ -447,6 +448,8 @@ def run_ours(args, rank, world):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "frac_of_measured_peak": round(value / world / peak, 4),
             "frac_of_nominal_7900": round(value / world / NOMINAL_HBM_GBS, 4),
+            "inrun_copy_gbs": round(copy_gbs, 1),
+            "frac_of_inrun_copy": round(value / world / copy_gbs, 4),
             "roofline": roofline, "ops": per_op, "e2e": e2e,
             "gpu_launches": K * sum(LAUNCHES_PER_OP[op["wl"].op] for op in ops),
             "timing": {"value": "CUDA events around K back-to-back steps on the launching stream",
@@ -650,6 +653,28 @@ def time_rotation(launches, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
+def inrun_copy_gbs(dev, stream, nbytes=1 << 30, reps=10):
+    """Device-to-device copy bandwidth measured in this run (cudaMemcpyAsync of
+    a 1 GiB buffer; read + write bytes, the convention of the measured peak)."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b) / reps
+    del src, dst
+    torch.cuda.empty_cache()
+    return 2 * nbytes / (ms * 1e-3) / 1e9
+
+
 def run_sweep(args):
     import torch
 
@@ -661,6 +686,7 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(device=dev)
     peak, _ = measured_peak()
+    copy_gbs = inrun_copy_gbs(dev, stream)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = args.workloads.split(",") if args.workloads else [
         n for n, w in si.WORKLOADS.items()
@@ -694,8 +720,13 @@ def run_sweep(args):
                           "variant": rn.rmsnorm_describe_plan(_op_code(wl.op), wl.M, wl.N,
                                                               wl.x_dtype, wl.w_dtype),
                           "us_per_call": round(med, 2), "rounds_us": [round(u, 2) for u in us],
+                          "min_us": round(min(us), 2),
+                          "spread": round((max(us) - min(us)) / med, 4),
+                          "interference": (max(us) - min(us)) / med > 0.10,
                           "gbs": round(byts / med / 1e3, 1),
                           "frac_of_measured_peak": round(byts / med / 1e3 / peak, 4),
+                          "inrun_copy_gbs": round(copy_gbs, 1),
+                          "frac_of_inrun_copy": round(byts / med / 1e3 / copy_gbs, 4),
                           "rows_per_s": round(wl.M / med * 1e6, 1), "alg_bytes": byts,
                           "l2": f"rotation over {len(sets)} operand set(s) "
                                 f">= 3 x L2, back-to-back launches",

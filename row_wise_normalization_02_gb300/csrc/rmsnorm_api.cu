@@ -421,9 +421,14 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
   // sub-warp backward with next-row prefetch only (262144 x 128 bf16: 0.80 ->
   // 0.85 of the copy peak); the forward kernels lost with it (16384 x 8192:
   // 0.97 -> 0.93), so they are built without it
-  if (bwd && p.family == kSubwarp && p.prefetch) p.l2_ahead = 2;
+  // The ragged kernels (rows not on 16 bytes) request the aligned interior
+  // of the rows two steps ahead in their walk (4096 x 2049 bf16: bwd 0.372 ->
+  // 0.385, fwd 0.546 -> 0.551; their few rows per CTA leave the pipeline's
+  // fill and drain, not the bytes in flight, as the limit).
+  const bool l2_able = p.prefetch && ((bwd && p.family == kSubwarp) || p.family == kRagged);
+  if (l2_able) p.l2_ahead = 2;
   if (f.on && f.l2 >= 0) p.l2_ahead = f.l2;
-  if (!bwd || p.family != kSubwarp || !p.prefetch) p.l2_ahead = 0;
+  if (!l2_able) p.l2_ahead = 0;
 
   // kernel and shared memory
   if (p.family == kStaged) {

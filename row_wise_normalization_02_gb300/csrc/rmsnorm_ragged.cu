@@ -104,6 +104,17 @@ __device__ __forceinline__ void load_row(RowRegs<VPT, TWO, THREE>& R, const TX* 
   R.cs = (THREE && L.scol >= 0) ? ld_scalar(cr + L.scol) : 0.f;
 }
 
+// Row `row` of a row-major array whose rows need not start on 16 bytes,
+// requested into L2 by the calling thread: the 16-byte-aligned interior of
+// the row only, so that every byte asked for lies inside it.
+__device__ __forceinline__ void l2_prefetch_row_interior(const void* a, int64_t row, int64_t M,
+                                                         size_t rb) {
+  if (row >= M) return;
+  const uintptr_t s = reinterpret_cast<uintptr_t>(a) + (uintptr_t)row * rb;
+  const uintptr_t lo = (s + 15) & ~(uintptr_t)15, hi = (s + rb) & ~(uintptr_t)15;
+  if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+}
+
 // ---------------------------------------------------------------------------
 // Forward / fused add (b = residual, in r, out h).
 template <typename TX, typename TW, int VPT, bool FUSED, bool PF>
@@ -127,6 +138,11 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_ragged_kernel(const FwdPar
   for (int64_t row = w.first; row < p.M; row += w.stride) {
     const int64_t nrow = row + w.stride;
     if (PF && nrow < p.M) load_row<TX, VPT, FUSED, true>(nxt, x, res, nrow, N, L, tid, T);
+    if (PF && p.l2_rows > 0 && tid == 0) {   // the row l2_rows steps ahead in this walk
+      const int64_t ahead = row + (int64_t)p.l2_rows * w.stride;
+      l2_prefetch_row_interior(x, ahead, p.M, (size_t)N * sizeof(TX));
+      if (FUSED) l2_prefetch_row_interior(res, ahead, p.M, (size_t)N * sizeof(TX));
+    }
     TX* hr = res + row * (int64_t)N;
     TX* yr = y + row * (int64_t)N;
     float sv = cur.as;
@@ -205,6 +221,12 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
   for (int64_t row = w.first; row < p.M; row += w.stride) {
     const int64_t nrow = row + w.stride;
     if (PF && nrow < p.M) load_row<TX, VPT, true, false, DRES>(nxt, x, dy, nrow, N, L, tid, T, dres);
+    if (PF && p.l2_rows > 0 && tid == 0) {
+      const int64_t ahead = row + (int64_t)p.l2_rows * w.stride;
+      l2_prefetch_row_interior(x, ahead, p.M, (size_t)N * sizeof(TX));
+      l2_prefetch_row_interior(dy, ahead, p.M, (size_t)N * sizeof(TX));
+      if (DRES) l2_prefetch_row_interior(dres, ahead, p.M, (size_t)N * sizeof(TX));
+    }
     TX* dxr = dx + row * (int64_t)N;
     const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
     const float xs = cur.as, ds = cur.bs;

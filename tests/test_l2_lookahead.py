@@ -4,7 +4,7 @@ a hint, so it must change no bit of any output, with or without it and at any
 distance, including the last iterations where the rows ahead run past the end
 and are clipped; and the dispatch turns it on exactly where it was measured
 to pay (the LayerNorm CTA kernels, the sub-warp backward kernels with next-row
-prefetch) and nowhere else."""
+prefetch, the ragged kernels) and nowhere else."""
 import numpy as np
 import pytest
 
@@ -34,6 +34,8 @@ import row_wise_normalization_02_gb300 as rn  # noqa: E402
     (rn.OP_FWD, 16384, 8192, False),
     (rn.OP_FUSED_ADD, 32768, 4096, False),
     (rn.OP_FWD, 262144, 128, False),
+    (rn.OP_FWD, 4096, 2049, True),               # ragged rows: the aligned interior
+    (rn.OP_BWD, 4096, 2049, True),
 ])
 def test_dispatch(op, M, N, on):
     plan = rn.rmsnorm_describe_plan(op, M, N, "bf16", "bf16")
@@ -102,3 +104,14 @@ def test_fused_add_short_row_backward_bits_do_not_depend_on_it(monkeypatch):
     out = _over_distances(
         monkeypatch, lambda: fb.run(h, dy, dres, g, rstd, eps, "bf16", "bf16"))
     fb.check(h, dy, dres, g, rstd, eps, "bf16", "bf16", out)
+
+
+def test_ragged_rows_bits_do_not_depend_on_it(monkeypatch):
+    M, N, eps = 1001, 2049, tl.f32(1e-6)
+    x, g, _, dy = tl.inputs(M, N, "bf16", "bf16", seed=66, beta=False)
+    fwd = _over_distances(monkeypatch, lambda: pu.run_fwd(x, g, eps, "bf16", "bf16"))
+    rstd = oracle.fwd(x, g, eps, "bf16", "bf16", want64=False)["rstd"]
+    bwd = _over_distances(monkeypatch, lambda: pu.run_bwd(dy, x, rstd, g, eps, "bf16", "bf16"))
+    ref = oracle.fwd(x, g, eps, "bf16", "bf16")
+    pu.check_bf16_ulp(fwd["y"], ref["y"], what="y")
+    check_bwd(x, dy, g, rstd, eps, "bf16", "bf16", bwd)
