@@ -61,3 +61,28 @@ def test_algorithmic_bytes_of_the_step():
     assert b[1] == 32768 * 4096 * 8 + 4096 * 2
     # backward: read x and dy, write dx, read rstd, fp32 gamma and dgamma once
     assert b[2] == 16384 * 8192 * 6 + 16384 * 4 + 8192 * 4 + 8192 * 4
+
+
+def test_traffic_record_applies_only_to_the_captured_sources_and_variants(tmp_path, monkeypatch):
+    # a record taken on the current step-kernel sources and these variants
+    import json
+    os.makedirs(tmp_path / "profiles")
+    variants = {"fwd": "fwd/cta/a", "fused_add": "fused_add/cta/b", "bwd": "bwd/staged/c"}
+    rec = {"source_hash": bench.source_hash(), "variants": variants,
+           "per_launch_bytes": {"fwd": 1, "fused_add": 2, "bwd": 3}}
+    with open(tmp_path / "profiles" / "dram_traffic.json", "w") as f:
+        json.dump(rec, f)
+    real_hash = bench.source_hash()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda: real_hash)
+    for op, n in (("fwd", 1), ("fused_add", 2), ("bwd", 3)):
+        assert bench.ncu_traffic(op, variants[op]) == n
+        # another variant picked by the dispatch: no traffic figure
+        assert bench.ncu_traffic(op, variants[op] + "/other") is None
+    # other kernel sources: no traffic figure for any op
+    monkeypatch.setattr(bench, "source_hash", lambda: "0" * 16)
+    for op in variants:
+        assert bench.ncu_traffic(op, variants[op]) is None
+    # no record at all
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path / "none"))
+    assert bench.ncu_traffic("fwd", variants["fwd"]) is None
