@@ -114,6 +114,11 @@ WORKLOADS = {
     "bwd_bf16_m16384_n8192": Workload("bwd_bf16_m16384_n8192", "bwd", 16384, 8192, "bf16",
                                       "f32", 1e-5, 3, tags=("headline",)),
 }
+# fp32 activations and weights at the forward / backward size class
+# (256 MiB per activation tensor; gamma ~ N(1, 0.1), dy ~ N(0, 1))
+for _op in ("fwd", "bwd"):
+    _name = f"sweep_{_op}_f32_m8192_n8192"
+    WORKLOADS[_name] = Workload(_name, _op, 8192, 8192, "f32", "f32", 1e-6, 7, tags=("sweep",))
 for _m, _n in _SWEEP:
     for _op in ("fwd", "bwd"):
         _name = f"sweep_{_op}_bf16_m{_m}_n{_n}"
