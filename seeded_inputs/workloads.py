@@ -105,7 +105,7 @@ WORKLOADS = {
                                          "bf16", "bf16", 1e-5, 6, tags=("next",)),
     "ln_bwd_bf16_m16384_n8192": Workload("ln_bwd_bf16_m16384_n8192", "ln_bwd", 16384, 8192,
                                          "bf16", "bf16", 1e-5, 6, tags=("next",)),
-    # the same at a short hidden size (1024: rows handled by lane groups)
+    # the same at a short hidden size (1024: the forward's rows handled by lane groups)
     "ln_fwd_bf16_m65536_n1024": Workload("ln_fwd_bf16_m65536_n1024", "ln_fwd", 65536, 1024,
                                          "bf16", "bf16", 1e-5, 6, tags=("next",)),
     "ln_bwd_bf16_m65536_n1024": Workload("ln_bwd_bf16_m65536_n1024", "ln_bwd", 65536, 1024,
