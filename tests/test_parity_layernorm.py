@@ -144,7 +144,16 @@ def check_bwd(out, dy, x, mean, rstd, g, eps, xd, wd):
     else:
         pu.check_f32(out["dx"], ref["dx64"], what="dx")
     if "dgamma" in out:
-        pu.check_dgamma(out["dgamma"], ref["dgamma64"], ((dy64 * xh) ** 2).sum(0))
+        # recomputed statistics: the kernel's fp32 mean rounds on the scale of
+        # the row's magnitudes, so each term dy * xhat carries up to a few fp32
+        # units of mean(|x|) r |dy| (the forward's 16-unit floor, reading R22);
+        # it shows where few rows are summed and xhat is near zero
+        dg_floor = None
+        if mean is None:
+            dg_floor = (16 * U32 * np.abs(dy64) * (r[:, None] *
+                        np.abs(x64).mean(axis=1, keepdims=True))).sum(0)
+        pu.check_dgamma(out["dgamma"], ref["dgamma64"], ((dy64 * xh) ** 2).sum(0),
+                        floor=dg_floor)
     if "dbeta" in out:
         pu.check_dgamma(out["dbeta"], ref["dbeta64"], (dy64 ** 2).sum(0))
     return n
