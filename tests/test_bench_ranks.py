@@ -86,3 +86,11 @@ def test_traffic_record_applies_only_to_the_captured_sources_and_variants(tmp_pa
     # no record at all
     monkeypatch.setattr(bench, "ROOT", str(tmp_path / "none"))
     assert bench.ncu_traffic("fwd", variants["fwd"]) is None
+
+
+def test_threaded_oracle_step_covers_the_same_rows():
+    # the all-cores baseline runs the same sample in row blocks: same bytes
+    samples = bench._samples(1 / 4096)
+    t1, b1 = bench._oracle_step(samples)
+    t2, b2 = bench._oracle_step_threads(samples, 3)
+    assert b1 == b2 > 0
