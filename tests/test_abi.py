@@ -204,3 +204,13 @@ def test_workspace_size_matches_plan_on_gpu(lib):
         # at most one partial row per resident CTA, at least one per residue
         # class of ragged rows (16 classes at most)
         assert b <= max(min(M, 152 * 32), 16) * ((N + 3) // 4 * 4) * 4 * 2
+
+
+def test_autograd_functions_reject_host_tensors_before_any_call():
+    torch = pytest.importorskip("torch")
+    from row_wise_normalization_02_gb300 import autograd as ag
+    x, g = torch.randn(4, 8), torch.ones(8)
+    for call in (lambda: ag.rms_norm(x, g), lambda: ag.layer_norm(x, g),
+                 lambda: ag.fused_add_rms_norm(x, torch.randn(4, 8), g)):
+        with pytest.raises(ValueError):
+            call()
