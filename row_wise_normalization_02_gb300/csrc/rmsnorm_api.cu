@@ -517,7 +517,7 @@ void describe(int op, const Plan& p, char* buf, size_t len) {
                               "fwd_strided", "fwd_fp8",   "fused_add_fp8", "fwd_nvfp4",
                               "fused_add_nvfp4", "layernorm_fwd", "layernorm_bwd"};
   const bool bwd = op == kBwd || op == kFusedBwd;
-  char l2[16] = "";
+  char l2[24] = "";
   if (p.l2_ahead > 0) snprintf(l2, sizeof l2, "/l2ahead%d", p.l2_ahead);
   snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d%s", ops[op],
            family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,

@@ -83,7 +83,7 @@ __device__ __forceinline__ void load_weight(uint4 (&w)[GW], const void* base, in
 // x + a rounded once, the same bits as unpacking and adding, in one
 // instruction per element instead of an unpack and half a paired add.
 // d = x - m for the 8 values of v.
-__device__ __forceinline__ void bf16x8_minus(const uint4& v, float nm, float (&d)[8]) {
+[[maybe_unused]] __device__ __forceinline__ void bf16x8_minus(const uint4& v, float nm, float (&d)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -96,7 +96,7 @@ __device__ __forceinline__ void bf16x8_minus(const uint4& v, float nm, float (&d
         : "r"(w[i]), "f"(nm));
 }
 // a0 += even elements of v, a1 += odd elements (in element order).
-__device__ __forceinline__ void bf16x8_accumulate(const uint4& v, float& a0, float& a1) {
+[[maybe_unused]] __device__ __forceinline__ void bf16x8_accumulate(const uint4& v, float& a0, float& a1) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -110,7 +110,7 @@ __device__ __forceinline__ void bf16x8_accumulate(const uint4& v, float& a0, flo
 }
 // p = a * b for 8 bf16 pairs: exact in fp32 (addend -0 keeps a zero
 // product's sign), the same bits as unpacking both and multiplying.
-__device__ __forceinline__ void bf16x8_products(const uint4& a, const uint4& b, float (&p)[8]) {
+[[maybe_unused]] __device__ __forceinline__ void bf16x8_products(const uint4& a, const uint4& b, float (&p)[8]) {
   const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i)

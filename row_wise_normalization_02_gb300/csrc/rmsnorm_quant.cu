@@ -112,17 +112,17 @@ __device__ __forceinline__ void st_cs(void* p, uint32_t a, uint32_t b) {
 }
 
 // E4M3 codes of one vector's E values: E bytes at dst (E-byte aligned).
-__device__ __forceinline__ void store_fp8(char* dst, const float (&o)[8]) {
+[[maybe_unused]] __device__ __forceinline__ void store_fp8(char* dst, const float (&o)[8]) {
   st_cs(dst, e4m3x4(o[0], o[1], o[2], o[3]), e4m3x4(o[4], o[5], o[6], o[7]));
 }
-__device__ __forceinline__ void store_fp8(char* dst, const float (&o)[4]) {
+[[maybe_unused]] __device__ __forceinline__ void store_fp8(char* dst, const float (&o)[4]) {
   st_cs(dst, e4m3x4(o[0], o[1], o[2], o[3]));
 }
 // E2M1 codes of one vector's E values: E / 2 bytes at dst, or zeros.
-__device__ __forceinline__ void store_fp4(char* dst, const float (&o)[8], bool zero) {
+[[maybe_unused]] __device__ __forceinline__ void store_fp4(char* dst, const float (&o)[8], bool zero) {
   st_cs(dst, zero ? 0u : e2m1x8(o));
 }
-__device__ __forceinline__ void store_fp4(char* dst, const float (&o)[4], bool zero) {
+[[maybe_unused]] __device__ __forceinline__ void store_fp4(char* dst, const float (&o)[4], bool zero) {
   st_cs(dst, zero ? (uint16_t)0 : e2m1x4(o));
 }
 
@@ -183,7 +183,7 @@ __device__ __forceinline__ void bf16_pair_products(uint32_t x_word, uint32_t g_w
 
 // x * gamma of two bf16 pairs' worth of packed words (mixed-precision FMA,
 // exact products, the addend -0 keeping a zero product's sign).
-__device__ __forceinline__ void bf16_pair_mul(uint32_t x_word, uint32_t g_word, float& p0,
+[[maybe_unused]] __device__ __forceinline__ void bf16_pair_mul(uint32_t x_word, uint32_t g_word, float& p0,
                                               float& p1) {
   asm("{\n\t.reg .b16 xl, xh, gl, gh;\n\t"
       "mov.b32 {xl, xh}, %2;\n\t"
