@@ -299,30 +299,33 @@ def run_ours(args, rank, world):
     if sampler:
         sampler.stop()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    # timed region 2: the same steps with an event pair around every call, for
-    # each op's own launch duration (the events between the launches cost the
-    # overlap, so these durations add up to slightly more than region 1)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)] for _ in ops]
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            for j, op in enumerate(ops):
-                ev[j][i][0].record(stream)
-                op["launch"]()
-                ev[j][i][1].record(stream)
-    stream.synchronize()
+    # timed region 2: each op alone, K calls back to back in 5 rounds, one
+    # event pair around each round (no events between the launches, so the
+    # launch overlap of consecutive calls stays as in region 1): the op's
+    # steady rate, as in --sweep
     step_bytes = sum(op["bytes"] for op in ops)
     ms_per_step = total_ms / K
     value = job_gbs(step_bytes, ms_per_step, world)
     peak, peak_src = measured_peak()
+    rounds = 5
+    per_round = max(1, K // rounds)
     per_op = {}
-    for j, op in enumerate(ops):
-        times = [a.elapsed_time(b) for a, b in ev[j]]
-        avg = sum(times) / len(times)
+    for op in ops:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(rounds)]
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                a.record(stream)
+                for _ in range(per_round):
+                    op["launch"]()
+                b.record(stream)
+        stream.synchronize()
+        times = [a.elapsed_time(b) / per_round for a, b in ev]
+        avg = statistics.median(times)
         gbs = op["bytes"] / (avg * 1e-3) / 1e9
         wl = op["wl"]
         per_op[wl.op] = {"workload": wl.name, "avg_us": round(avg * 1e3, 2),
-                         "median_us": round(statistics.median(times) * 1e3, 2),
+                         "rounds_us": [round(t * 1e3, 2) for t in times],
                          "min_us": round(min(times) * 1e3, 2), "gbs": round(gbs, 1),
                          "frac_of_measured_peak": round(gbs / peak, 4),
                          "rows_per_s": round(wl.M / (avg * 1e-3), 1),
@@ -452,8 +455,11 @@ def run_ours(args, rank, world):
             "frac_of_inrun_copy": round(value / world / copy_gbs, 4),
             "roofline": roofline, "ops": per_op, "e2e": e2e,
             "gpu_launches": K * sum(LAUNCHES_PER_OP[op["wl"].op] for op in ops),
+            "gpu_launches_per_op_region": {op["wl"].op: per_round * rounds *
+                                           LAUNCHES_PER_OP[op["wl"].op] for op in ops},
             "timing": {"value": "CUDA events around K back-to-back steps on the launching stream",
-                       "ops": "CUDA events around each call, over a second run of K steps"},
+                       "ops": "per op: CUDA events around 5 rounds of K/5 back-to-back calls "
+                              "of that op alone; median round"},
             "clocks": sampler.summary() if sampler else None}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -735,6 +741,8 @@ def run_sweep(args):
         # saved statistics for the backward (untimed forward, default variant
         # even when RMSNORM_FORCE_VARIANT names a backward-only one)
         forced = os.environ.pop("RMSNORM_FORCE_VARIANT", None)
+        if forced is not None:
+            rn.rmsnorm_reload_debug_env()
         for d in sets:
             if wl.op == "ln_bwd":
                 gam = d["gamma"]
@@ -748,6 +756,7 @@ def run_sweep(args):
         torch.cuda.synchronize()
         if forced is not None:
             os.environ["RMSNORM_FORCE_VARIANT"] = forced
+            rn.rmsnorm_reload_debug_env()
         launches = [make_launch(wl, d, stream, rn) for d in sets]
         us = [time_rotation(launches, args.steps, args.warmup, stream) * 1e3
               for _ in range(args.rounds)]

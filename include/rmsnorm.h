@@ -258,6 +258,11 @@ rmsnorm_status_t rmsnorm_fused_add_bwd(const void* dy, const void* h, const floa
  *    needs clearing).  Calls that overlap on the GPU -- for example on two
  *    streams without ordering between them -- race on it and may return a
  *    wrong dgamma; order them on one stream or with events.
+ *  - Lifetime: the looked-up address is kept for the life of the process.
+ *    After cudaDeviceReset (or anything else that destroys the device's
+ *    primary context) the library's device image -- and so the scratch --
+ *    is loaded again at another address; do not call this function on that
+ *    device again in the same process.
  */
 #define RMSNORM_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -286,6 +291,20 @@ rmsnorm_status_t rmsnorm_check_device(cudaStream_t stream);
  * belongs to the library and stays valid until that thread's next call.
  */
 const char* rmsnorm_last_error(void);
+
+/*
+ * Re-read the debug and measurement knobs from the environment.  The library
+ * reads them once when it is loaded, never while launching:
+ *   RMSNORM_FORCE_VARIANT      force a kernel variant (A/B runs, tests); a
+ *                              variant that cannot serve a call makes that
+ *                              call return RMSNORM_ERR_INVALID_ARG
+ *   RMSNORM_WAIT_LIMIT_CYCLES  clock cycles a bulk-copy wait lasts before it
+ *                              gives up (negative: give up at once)
+ *   RMSNORM_NO_PDL=1           launch without programmatic dependent launch
+ * Call it only while no other thread is inside the library.  No page this
+ * library follows has this call; it exists for tests and measurements.
+ */
+void rmsnorm_reload_debug_env(void);
 
 /* Static text of a status code ("unknown status" for other values). */
 const char* rmsnorm_status_string(rmsnorm_status_t status);

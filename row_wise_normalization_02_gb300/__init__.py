@@ -23,7 +23,7 @@ __all__ = ["F32", "BF16", "OP_FWD", "OP_FUSED_ADD", "OP_BWD", "OP_FUSED_ADD_BWD"
            "load_library", "rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_size", "rmsnorm_status_string", "rmsnorm_describe_plan",
            "rmsnorm_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "rmsnorm_check_device",
-           "rmsnorm_last_error", "EXPORTED_SYMBOLS"]
+           "rmsnorm_last_error", "rmsnorm_reload_debug_env", "EXPORTED_SYMBOLS"]
 
 F32 = 0
 BF16 = 1
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = ("rmsnorm_fwd", "rmsnorm_fused_add_fwd", "rmsnorm_bwd_workspa
                     "rmsnorm_bwd_noalloc", "rmsnorm_check_device", "rmsnorm_last_error",
                     "rmsnorm_fused_add_bwd", "rmsnorm_fwd_strided", "rmsnorm_fwd_fp8",
                     "rmsnorm_fwd_nvfp4", "layernorm_fwd", "layernorm_bwd_workspace_size",
-                    "layernorm_bwd")
+                    "layernorm_bwd", "rmsnorm_reload_debug_env")
 
 # Size of the library-owned scratch of rmsnorm_bwd_noalloc (16 MiB).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -103,6 +103,8 @@ def load_library():
             lib.rmsnorm_fwd_nvfp4.restype = I
             lib.rmsnorm_last_error.argtypes = []
             lib.rmsnorm_last_error.restype = ctypes.c_char_p
+            lib.rmsnorm_reload_debug_env.argtypes = []
+            lib.rmsnorm_reload_debug_env.restype = None
             _lib = lib
     return _lib
 
@@ -237,6 +239,13 @@ def rmsnorm_check_device(stream=None):
     """Wait for `stream`, then raise RMSNormError(RMSNORM_ERR_TIMEOUT) if a
     kernel on the current device gave up a bounded wait (clears the flag)."""
     _check(load_library().rmsnorm_check_device(_stream(stream)), "rmsnorm_check_device")
+
+
+def rmsnorm_reload_debug_env():
+    """Re-read RMSNORM_FORCE_VARIANT, RMSNORM_WAIT_LIMIT_CYCLES and
+    RMSNORM_NO_PDL from the environment (the library reads them once at load;
+    call this after changing them, with no other thread inside the library)."""
+    load_library().rmsnorm_reload_debug_env()
 
 
 def rmsnorm_last_error() -> str:

@@ -50,8 +50,10 @@ def _rows(x: torch.Tensor, *weights):
     return (x.numel() // N if N else 0), N
 
 
-def _stream() -> int:
-    return torch.cuda.current_stream().cuda_stream
+def _stream(device) -> int:
+    """The current stream of x's device: the C ABI launches on the current
+    device, so every call below also makes x's device current."""
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:
@@ -64,7 +66,8 @@ class _RMSNorm(torch.autograd.Function):
         M, N = _rows(x, gamma)
         y = torch.empty_like(x)
         rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-        rmsnorm_fwd(x, gamma, y, rstd, M, N, eps, _dt(x), _dt(gamma), _stream())
+        with torch.cuda.device(x.device):
+            rmsnorm_fwd(x, gamma, y, rstd, M, N, eps, _dt(x), _dt(gamma), _stream(x.device))
         ctx.save_for_backward(x, gamma, rstd)
         ctx.eps = eps
         return y
@@ -80,8 +83,9 @@ class _RMSNorm(torch.autograd.Function):
             dgamma = torch.empty(N, dtype=torch.float32, device=x.device)
             nbytes = rmsnorm_bwd_workspace_size(M, N, _dt(x), _dt(gamma), x.device.index)
             ws = _workspace(nbytes, x.device)
-        rmsnorm_bwd(dy, x, rstd, gamma, dx, dgamma, ws, nbytes, M, N, ctx.eps, _dt(x),
-                    _dt(gamma), _stream())
+        with torch.cuda.device(x.device):
+            rmsnorm_bwd(dy, x, rstd, gamma, dx, dgamma, ws, nbytes, M, N, ctx.eps, _dt(x),
+                        _dt(gamma), _stream(x.device))
         return dx, dgamma, None
 
 
@@ -91,10 +95,14 @@ class _FusedAddRMSNorm(torch.autograd.Function):
         M, N = _rows(x, gamma)
         if residual.shape != x.shape or residual.dtype != x.dtype:
             raise ValueError("residual must have the shape and dtype of x")
+        if not residual.is_cuda or residual.device != x.device:
+            raise ValueError(f"residual must be on x's device ({x.device})")
         h = residual.contiguous().clone()
         y = torch.empty_like(x)
         rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-        rmsnorm_fused_add_fwd(x, h, gamma, y, rstd, M, N, eps, _dt(x), _dt(gamma), _stream())
+        with torch.cuda.device(x.device):
+            rmsnorm_fused_add_fwd(x, h, gamma, y, rstd, M, N, eps, _dt(x), _dt(gamma),
+                                  _stream(x.device))
         ctx.save_for_backward(h, gamma, rstd)
         ctx.eps = eps
         return y, h
@@ -112,8 +120,9 @@ class _FusedAddRMSNorm(torch.autograd.Function):
             dgamma = torch.empty(N, dtype=gamma.dtype, device=h.device)
             nbytes = rmsnorm_bwd_workspace_size(M, N, _dt(h), _dt(gamma), h.device.index)
             ws = _workspace(nbytes, h.device)
-        rmsnorm_fused_add_bwd(dy, h, rstd, gamma, dres, dgamma, _dt(gamma), ws, nbytes, M, N,
-                              ctx.eps, _dt(h), _dt(gamma), _stream())
+        with torch.cuda.device(h.device):
+            rmsnorm_fused_add_bwd(dy, h, rstd, gamma, dres, dgamma, _dt(gamma), ws, nbytes, M,
+                                  N, ctx.eps, _dt(h), _dt(gamma), _stream(h.device))
         return dres, dres, dgamma, None
 
 
@@ -124,7 +133,9 @@ class _LayerNorm(torch.autograd.Function):
         y = torch.empty_like(x)
         mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
         rstd = torch.empty_like(mean)
-        layernorm_fwd(x, gamma, beta, y, mean, rstd, M, N, eps, _dt(x), _dt(gamma), _stream())
+        with torch.cuda.device(x.device):
+            layernorm_fwd(x, gamma, beta, y, mean, rstd, M, N, eps, _dt(x), _dt(gamma),
+                          _stream(x.device))
         ctx.save_for_backward(x, gamma, mean, rstd)
         ctx.eps = eps
         ctx.has_beta = beta is not None
@@ -144,8 +155,9 @@ class _LayerNorm(torch.autograd.Function):
         if want_g or want_b:
             nbytes = layernorm_bwd_workspace_size(M, N, _dt(x), _dt(gamma), x.device.index)
             ws = _workspace(nbytes, x.device)
-        layernorm_bwd(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, ws, nbytes, M, N, ctx.eps,
-                      _dt(x), _dt(gamma), _stream())
+        with torch.cuda.device(x.device):
+            layernorm_bwd(dy, x, mean, rstd, gamma, dx, dgamma, dbeta, ws, nbytes, M, N,
+                          ctx.eps, _dt(x), _dt(gamma), _stream(x.device))
         return dx, dgamma, dbeta, None
 
 

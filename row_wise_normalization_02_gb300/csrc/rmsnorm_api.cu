@@ -35,15 +35,6 @@ constexpr int64_t kStagedSmemBudget = 110 * 1024;
 constexpr int64_t kStagedSmemMax = 226 * 1024;
 constexpr long long kDefaultWaitLimit = 1LL << 32;   // clock cycles (about 2 s)
 
-// Clock cycles a staged kernel waits for a row before giving up: the
-// RMSNORM_WAIT_LIMIT_CYCLES environment variable (a test knob; a negative
-// value makes every wait give up at once), else ~2 s.
-long long wait_limit() {
-  const char* s = getenv("RMSNORM_WAIT_LIMIT_CYCLES");
-  if (s && *s) return atoll(s);
-  return kDefaultWaitLimit;
-}
-
 int esize(int dt) { return dt == kF32 ? 4 : 2; }
 int per_vec(int dt) { return 16 / esize(dt); }
 
@@ -283,20 +274,33 @@ int ragged_period(int64_t bytes) {
   return 16 / g;
 }
 
-// RMSNORM_FORCE_VARIANT="family[:key=value...]" with family one of subwarp,
-// cta, ragged, generic, staged and keys g, vpt, t (threads), pf (0/1), acc
-// (0/1 shared-memory dgamma partials), cps (CTAs per SM cap), st (stages),
-// mr (backward: minimum rows per CTA, 0 = none).  For profiling A/B
-// runs; a forced variant that cannot serve the call is an argument error.
+// Debug and A/B knobs, read from the environment once when the library is
+// loaded and again only by rmsnorm_reload_debug_env -- never on the launch
+// path:
+//  RMSNORM_FORCE_VARIANT="family[:key=value...]" with family one of subwarp,
+//    cta, ragged, generic, staged and keys g, vpt, t (threads), pf (0/1),
+//    acc (0/1 shared-memory dgamma partials), cps (CTAs per SM cap), st
+//    (stages), mr (backward: minimum rows per CTA, 0 = none), l2 (L2
+//    lookahead).  For profiling A/B runs; a forced variant that cannot
+//    serve the call is an argument error.
+//  RMSNORM_WAIT_LIMIT_CYCLES: clock cycles a bulk-copy wait lasts before it
+//    gives up (a test knob; a negative value makes every wait give up at
+//    once), else about 2 s.
+//  RMSNORM_NO_PDL=1: launch without programmatic dependent launch.
 struct Force {
   bool on = false;
   int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0, st = 0, mr = -1,
       l2 = -1;
 };
 
-Force read_force() {
+struct DebugEnv {
+  Force force;
+  long long wait_limit = kDefaultWaitLimit;
+  bool no_pdl = false;
+};
+
+Force parse_force(const char* s) {
   Force f;
-  const char* s = getenv("RMSNORM_FORCE_VARIANT");
   if (!s || !*s) return f;
   f.on = true;
   char buf[128];
@@ -327,6 +331,22 @@ Force read_force() {
   }
   return f;
 }
+
+DebugEnv read_debug_env() {
+  DebugEnv e;
+  e.force = parse_force(getenv("RMSNORM_FORCE_VARIANT"));
+  const char* w = getenv("RMSNORM_WAIT_LIMIT_CYCLES");
+  if (w && *w) e.wait_limit = atoll(w);
+  const char* off = getenv("RMSNORM_NO_PDL");
+  e.no_pdl = off && *off && *off != '0';
+  return e;
+}
+
+// Initialised when the library is loaded; replaced by rmsnorm_reload_debug_env.
+DebugEnv g_env = read_debug_env();
+
+const Force& read_force() { return g_env.force; }
+long long wait_limit() { return g_env.wait_limit; }
 
 // Choose the variant.  aligned16: all base pointers 16-byte aligned;
 // same_mod16: all activation base pointers agree modulo 16 bytes.
@@ -373,7 +393,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.prefetch = false;
   }
 
-  const Force f = read_force();
+  const Force& f = read_force();
   if (f.on) {
     if (f.family >= 0) p.family = f.family;
     if (f.g) p.g = f.g;
@@ -451,7 +471,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     // each CTA writes one dgamma partial row (N fp32); keep that traffic to a
     // few percent of the rows it reads
     p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
-    const Force fr = read_force();
+    const Force& fr = read_force();
     if (fr.on && fr.mr >= 0) p.min_rows = fr.mr;
     if (dres && p.family == kCta) return RMSNORM_ERR_INVALID_ARG;
     BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch, dres};
@@ -528,8 +548,8 @@ void describe(int op, const Plan& p, char* buf, size_t len) {
 
 // Every kernel is launched as a programmatic dependent of the previous work on
 // the stream (the kernels wait for it at entry, see pdl_begin), so the launch
-// of one call overlaps the end of the previous one.  RMSNORM_NO_PDL=1 turns
-// the attribute off (for A/B measurements).
+// of one call overlaps the end of the previous one.  RMSNORM_NO_PDL=1 (read
+// with the other debug knobs) turns the attribute off for A/B measurements.
 template <typename... Args>
 cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
                    cudaStream_t stream, Args... args) {
@@ -541,8 +561,7 @@ cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  const char* off = getenv("RMSNORM_NO_PDL");
-  const bool pdl = !(off && *off && *off != '0');
+  const bool pdl = !g_env.no_pdl;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
@@ -657,7 +676,7 @@ rmsnorm_status_t strided_plan(int64_t D, int xd, int wd, bool vec_ok, Plan* out)
     p.family = kGeneric;
     p.threads = 256;
   }
-  const Force f = read_force();
+  const Force& f = read_force();
   if (f.on) {
     if (f.family == kGeneric) {
       p.family = kGeneric;
@@ -775,7 +794,7 @@ rmsnorm_status_t quant_plan(int out, bool fused, int64_t N, int xd, int wd, bool
     p.family = kGeneric;
     p.threads = 256;
   }
-  const Force f = read_force();
+  const Force& f = read_force();
   if (f.on) {
     if (f.family == kGeneric) {
       p.family = kGeneric;
@@ -946,7 +965,7 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
       }
     }
   }
-  const Force f = read_force();
+  const Force& f = read_force();
   if (f.on) {
     if (f.family == kGeneric) {
       p.family = kGeneric;
@@ -1022,7 +1041,7 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
   if (p.family == kStaged) p.smem = (int)(kStagedHeader + p.stages * 2 * N * esize(xd));
   if (bwd) {
     p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
-    const Force fr = read_force();
+    const Force& fr = read_force();
     if (fr.on && fr.mr >= 0) p.min_rows = fr.mr;
   }
   (void)M;
@@ -1500,6 +1519,8 @@ rmsnorm_status_t rmsnorm_check_device(cudaStream_t stream) {
 }
 
 const char* rmsnorm_last_error(void) { return g_last_error; }
+
+void rmsnorm_reload_debug_env(void) { g_env = read_debug_env(); }
 
 const char* rmsnorm_status_string(rmsnorm_status_t status) {
   switch (status) {

@@ -25,3 +25,25 @@ def eval_expr(s: str) -> float:
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture
+def debug_env(monkeypatch):
+    """Set or clear the library's debug knobs (RMSNORM_FORCE_VARIANT,
+    RMSNORM_WAIT_LIMIT_CYCLES, RMSNORM_NO_PDL) for one test.  The library reads
+    them once, so every change is followed by a reload, and the test's own
+    environment is restored and reloaded when it ends."""
+    import row_wise_normalization_02_gb300 as rn
+
+    class _Env:
+        def set(self, name, value):
+            monkeypatch.setenv(name, value)
+            rn.rmsnorm_reload_debug_env()
+
+        def delete(self, name, raising=True):
+            monkeypatch.delenv(name, raising=raising)
+            rn.rmsnorm_reload_debug_env()
+
+    yield _Env()
+    monkeypatch.undo()
+    rn.rmsnorm_reload_debug_env()

@@ -7,14 +7,14 @@ oracle):
     value, distance counted in the ordered integer encoding of bf16.
   * bf16 dx where the two terms of gamma*dy - x*c cancel: an fp32 evaluation
     cannot keep 2 ulp of a result much smaller than its terms, so an element
-    may instead be within 2 ulp(exact) + 64 u32 r (|gamma dy| + |x| r^2/N S) of
-    the exact value, S = sum_k |gamma_k dy_k x_k| (u32 = 2^-24; 64 bounds the
-    depth of the fp32 sums and products).  Such elements are counted and, for
-    rows of 32 or more elements, must stay rare (at most 1e-4 of the tensor).
-    Short rows cancel by construction: for N = 1, dx = r gamma dy eps /
-    (x^2 + eps) is a 1e-5 sliver of its terms, and every element may need the
-    floor.
-  * fp32 outputs (y, rstd): |gpu - ref| <= 1e-5 (1 + |ref|).
+    may instead be within 2 ulp(exact) + 1e-6 r (|gamma dy| + |x c|) of the
+    exact value (c = r^2/N sum_k gamma_k dy_k x_k, signed).  Such elements are
+    counted; for rows of 32 or more elements they may be at most 1e-5 of the
+    tensor (at least one element is allowed in a tensor of fewer than 1e5).
+    Rows shorter than 32 cancel by construction -- for N = 1,
+    dx = r gamma dy eps / (x^2 + eps) is a 1e-5 sliver of its terms -- so
+    there every element may use the floor (the bound itself still holds).
+  * fp32 outputs (y, rstd, dx): |gpu - ref| <= 1e-5 (1 + |ref|).
   * dgamma (fp32): |gpu - ref| <= 1e-4 max(|ref|, sqrt(sum_rows (dy x r)^2)).
   * h of the fused add: bit exact (a correctly rounded sum on both sides).
 """
@@ -177,26 +177,32 @@ def check_f32(gpu, ref64, rtol=1e-5, what="output"):
     return float((err / lim).max()) if err.size else 0.0
 
 
-def check_dx_bf16(gpu_bits, ref_bits, dx64, x64, dy64, g64, r, dot_abs, max_floor_frac=1e-4):
-    """2-ulp gate with the cancellation floor described in the module doc."""
+DX_FLOOR_REL = 1e-6     # of r (|gamma dy| + |x c|)
+DX_FLOOR_CAP = 1e-5     # fraction of the tensor that may use the floor
+
+
+def check_dx_bf16(gpu_bits, ref_bits, dx64, x64, dy64, g64, r, c64, what="dx"):
+    """2-ulp gate with the cancellation floor described in the module doc.
+    Returns (elements that needed the floor, largest ulp distance)."""
     M, N = dx64.shape
     d = bf16_ulp_dist(gpu_bits, ref_bits)
     strict_bad = d > 2
-    n_strict = int(strict_bad.sum())
-    if n_strict:
+    n_floor = int(strict_bad.sum())
+    if n_floor:
         from oracle import bf16_array_to_f64
         gv = bf16_array_to_f64(gpu_bits)
         rr = r[:, None]
-        floor = 64 * U32 * rr * (np.abs(g64[None, :] * dy64) +
-                                 np.abs(x64) * rr * rr / N * dot_abs[:, None])
+        floor = DX_FLOOR_REL * rr * (np.abs(g64[None, :] * dy64) + np.abs(x64 * c64[:, None]))
         lim = 2 * bf16_ulp_of(dx64) + floor
-        ok = np.abs(gv - dx64) <= lim
-        bad = strict_bad & ~ok
-        assert not bad.any(), (f"dx: {int(bad.sum())} elements beyond 2 ulp and the cancellation "
-                               f"floor, at {np.argwhere(bad)[:5].tolist()}")
-        assert N < 32 or n_strict <= max(1, max_floor_frac * d.size), (
-            f"dx: {n_strict} of {d.size} elements needed the cancellation floor")
-    return n_strict, int(d.max())
+        bad = strict_bad & ~(np.abs(gv - dx64) <= lim)
+        assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond 2 ulp and the "
+                               f"cancellation floor ({n_floor} beyond 2 ulp) at "
+                               f"{np.argwhere(bad)[:5].tolist()}")
+        cap = max(1, int(DX_FLOOR_CAP * d.size))
+        assert N < 32 or n_floor <= cap, (
+            f"{what}: {n_floor} of {d.size} elements needed the cancellation floor "
+            f"(at most {cap})")
+    return n_floor, int(d.max())
 
 
 def check_dgamma(gpu, ref64, sq64, rtol=1e-4, floor=None):

@@ -140,3 +140,29 @@ def test_bad_inputs_are_rejected():
         ag.rms_norm(x, torch.ones(32, device="cuda"))
     with pytest.raises(ValueError):
         ag.rms_norm(x.t(), torch.ones(4, device="cuda"))
+
+
+def test_residual_on_another_device_is_rejected_before_any_launch(monkeypatch):
+    import row_wise_normalization_02_gb300.autograd as agm
+    calls = []
+    monkeypatch.setattr(agm, "rmsnorm_fused_add_fwd", lambda *a, **k: calls.append(a))
+    x = torch.randn(4, 64, device="cuda", dtype=torch.bfloat16)
+    g = torch.ones(64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ag.fused_add_rms_norm(x, x.cpu(), g)
+    assert not calls
+
+
+@pytest.mark.skipif(torch.cuda.device_count() < 2, reason="needs two GPUs")
+def test_calls_follow_the_tensors_device():
+    M, N, eps = 64, 1024, 1e-6
+    x1 = torch.randn(M, N, device="cuda:1", dtype=torch.bfloat16)
+    g1 = torch.rand(N, device="cuda:1", dtype=torch.bfloat16) + 0.5
+    with torch.cuda.device(0):
+        y1 = ag.rms_norm(x1, g1, eps)
+    torch.cuda.synchronize(1)
+    with torch.cuda.device(1):
+        y_ref = ag.rms_norm(x1, g1, eps)
+    torch.cuda.synchronize(1)
+    assert y1.device == x1.device
+    assert torch.equal(y1.view(torch.int16), y_ref.view(torch.int16))

@@ -27,12 +27,12 @@ def _data(M, N, seed):
 
 
 @pytest.mark.parametrize("op", ["fwd", "fused", "bwd"])
-def test_timeout_is_reported_and_the_context_survives(monkeypatch, op):
+def test_timeout_is_reported_and_the_context_survives(debug_env, op):
     M, N, eps = 1024, 8192, float(np.float32(1e-5))
     x, dy, g = _data(M, N, seed=41)
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
+    debug_env.set("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
     rn.rmsnorm_check_device()                    # start from a clear flag
-    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
+    debug_env.set("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     if op == "fwd":
         pu.run_fwd(x, g, eps, "bf16", "bf16")
     elif op == "fused":
@@ -45,7 +45,7 @@ def test_timeout_is_reported_and_the_context_survives(monkeypatch, op):
     rn.rmsnorm_check_device()                    # the flag was cleared
 
     # same variant, normal limit: correct results, no flag
-    monkeypatch.delenv("RMSNORM_WAIT_LIMIT_CYCLES")
+    debug_env.delete("RMSNORM_WAIT_LIMIT_CYCLES")
     out = pu.run_fwd(x, g, eps, "bf16", "bf16")
     ref = oracle.fwd(x, g, eps, "bf16", "bf16")
     pu.check_bf16_ulp(out["y"], ref["y"])

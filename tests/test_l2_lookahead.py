@@ -55,63 +55,63 @@ def _same(runs):
             assert np.array_equal(_bits(base[k]), _bits(other[k])), k
 
 
-def _over_distances(monkeypatch, fn):
+def _over_distances(debug_env, fn):
     runs = []
     for l2 in (None, 0, 1, 3):
         if l2 is None:
-            monkeypatch.delenv("RMSNORM_FORCE_VARIANT", raising=False)
+            debug_env.delete("RMSNORM_FORCE_VARIANT", raising=False)
         else:
-            monkeypatch.setenv("RMSNORM_FORCE_VARIANT", f"keep:l2={l2}")
+            debug_env.set("RMSNORM_FORCE_VARIANT", f"keep:l2={l2}")
         runs.append(fn())
-    monkeypatch.delenv("RMSNORM_FORCE_VARIANT", raising=False)
+    debug_env.delete("RMSNORM_FORCE_VARIANT", raising=False)
     _same(runs)
     return runs[0]
 
 
 @pytest.mark.parametrize("M,N", [(3001, 8192), (20001, 1024)])
-def test_layernorm_forward_bits_do_not_depend_on_it(monkeypatch, M, N):
+def test_layernorm_forward_bits_do_not_depend_on_it(debug_env, M, N):
     eps = tl.f32(1e-5)
     x, g, b, _ = tl.inputs(M, N, "bf16", "bf16", seed=61)
-    out = _over_distances(monkeypatch, lambda: tl.run_fwd(x, g, b, eps, "bf16", "bf16"))
+    out = _over_distances(debug_env, lambda: tl.run_fwd(x, g, b, eps, "bf16", "bf16"))
     tl.check_fwd(out, x, g, b, eps, "bf16", "bf16")
 
 
 @pytest.mark.parametrize("M,N,saved", [(3001, 8192, True), (20001, 1024, True),
                                        (20001, 1024, False)])
-def test_layernorm_backward_bits_do_not_depend_on_it(monkeypatch, M, N, saved):
+def test_layernorm_backward_bits_do_not_depend_on_it(debug_env, M, N, saved):
     eps = tl.f32(1e-5)
     x, g, _, dy = tl.inputs(M, N, "bf16", "bf16", seed=62)
     fw = oracle.layernorm_fwd(x, g, None, eps, "bf16", "bf16")
     mean, rstd = (fw["mean"], fw["rstd"]) if saved else (None, None)
     out = _over_distances(
-        monkeypatch, lambda: tl.run_bwd(dy, x, mean, rstd, g, eps, "bf16", "bf16"))
+        debug_env, lambda: tl.run_bwd(dy, x, mean, rstd, g, eps, "bf16", "bf16"))
     tl.check_bwd(out, dy, x, mean, rstd, g, eps, "bf16", "bf16")
 
 
-def test_rmsnorm_short_row_backward_bits_do_not_depend_on_it(monkeypatch):
+def test_rmsnorm_short_row_backward_bits_do_not_depend_on_it(debug_env):
     M, N, eps = 50001, 128, tl.f32(1e-6)
     x, g, _, dy = tl.inputs(M, N, "bf16", "bf16", seed=63, beta=False)
     rstd = oracle.fwd(x, g, eps, "bf16", "bf16", want64=False)["rstd"]
-    out = _over_distances(monkeypatch, lambda: pu.run_bwd(dy, x, rstd, g, eps, "bf16", "bf16"))
+    out = _over_distances(debug_env, lambda: pu.run_bwd(dy, x, rstd, g, eps, "bf16", "bf16"))
     check_bwd(x, dy, g, rstd, eps, "bf16", "bf16", out)
 
 
-def test_fused_add_short_row_backward_bits_do_not_depend_on_it(monkeypatch):
+def test_fused_add_short_row_backward_bits_do_not_depend_on_it(debug_env):
     M, N, eps = 50001, 128, tl.f32(1e-6)
     h, g, _, dy = tl.inputs(M, N, "bf16", "bf16", seed=64, beta=False)
     dres = tl.inputs(M, N, "bf16", "bf16", seed=65, beta=False)[3]
     rstd = oracle.fwd(h, g, eps, "bf16", "bf16", want64=False)["rstd"]
     out = _over_distances(
-        monkeypatch, lambda: fb.run(h, dy, dres, g, rstd, eps, "bf16", "bf16"))
+        debug_env, lambda: fb.run(h, dy, dres, g, rstd, eps, "bf16", "bf16"))
     fb.check(h, dy, dres, g, rstd, eps, "bf16", "bf16", out)
 
 
-def test_ragged_rows_bits_do_not_depend_on_it(monkeypatch):
+def test_ragged_rows_bits_do_not_depend_on_it(debug_env):
     M, N, eps = 1001, 2049, tl.f32(1e-6)
     x, g, _, dy = tl.inputs(M, N, "bf16", "bf16", seed=66, beta=False)
-    fwd = _over_distances(monkeypatch, lambda: pu.run_fwd(x, g, eps, "bf16", "bf16"))
+    fwd = _over_distances(debug_env, lambda: pu.run_fwd(x, g, eps, "bf16", "bf16"))
     rstd = oracle.fwd(x, g, eps, "bf16", "bf16", want64=False)["rstd"]
-    bwd = _over_distances(monkeypatch, lambda: pu.run_bwd(dy, x, rstd, g, eps, "bf16", "bf16"))
+    bwd = _over_distances(debug_env, lambda: pu.run_bwd(dy, x, rstd, g, eps, "bf16", "bf16"))
     ref = oracle.fwd(x, g, eps, "bf16", "bf16")
     pu.check_bf16_ulp(fwd["y"], ref["y"], what="y")
     check_bwd(x, dy, g, rstd, eps, "bf16", "bf16", bwd)

@@ -51,11 +51,11 @@ def check(h, dy, dres, g, rstd, eps, xd, wd, out, dg_dtype="f32"):
     h64, dy64, g64 = oracle.to_f64(h, xd), oracle.to_f64(dy, xd), oracle.to_f64(g, wd)
     r = rstd.astype(np.float64) if rstd is not None else 1.0 / np.sqrt(np.mean(h64 ** 2, 1) + eps)
     if xd == "bf16":
-        pu.check_dx_bf16(out["dh"], ref["dh"], ref["dh64"], h64, dy64, g64, r, aux["dot_abs64"])
+        n_floor, _ = pu.check_dx_bf16(out["dh"], ref["dh"], ref["dh64"], h64, dy64, g64, r,
+                                      aux["c64"], what="dh")
     else:
-        scale = r[:, None] * (np.abs(g64[None, :] * dy64) + np.abs(h64 * aux["c64"][:, None]))
-        err = np.abs(out["dh"].astype(np.float64) - ref["dh64"])
-        assert (err <= 1e-5 * (1 + np.abs(ref["dh64"])) + 64 * pu.U32 * scale).all()
+        n_floor = 0
+        pu.check_f32(out["dh"], ref["dh64"], what="dh")
     if dg_dtype == "f32":
         pu.check_dgamma(out["dgamma"], ref["dgamma64"], aux["dgamma_sq64"])
     else:
@@ -64,6 +64,7 @@ def check(h, dy, dres, g, rstd, eps, xd, wd, out, dg_dtype="f32"):
         # error of a bf16 tie
         d = pu.bf16_ulp_dist(out["dgamma"], ref["dgamma_w"])
         assert (d <= 1).all(), int(d.max())
+    return {"floor": n_floor}
 
 
 PAIRS = [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32")]
@@ -97,8 +98,8 @@ def test_dgamma_in_weight_dtype_and_no_rstd(N):
     ("subwarp:g=32:vpt=3:pf=0:cps=1", 768), ("ragged:vpt=2:pf=1:cps=1", 2049),
     ("ragged:vpt=1:pf=0:cps=1", 2049), ("generic:cps=1", 4096),
 ])
-def test_forced_variants(monkeypatch, force, N):
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+def test_forced_variants(debug_env, force, N):
+    debug_env.set("RMSNORM_FORCE_VARIANT", force)
     M = 2500 if N <= 1024 else 600
     h, dy, dres, g = make(M, N, "bf16", "f32", seed=33)
     eps = f32(1e-5)

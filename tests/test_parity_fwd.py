@@ -103,10 +103,10 @@ def test_fused_add_matches_oracle(xd, wd, M, N):
     ("staged:vpt=1:st=8:cps=1", 2048), ("staged:vpt=4:t=512:st=2:cps=1", 5120),
     ("staged:vpt=4:st=4:cps=1", 1032),
 ])
-def test_forced_variants_walk_several_rows(monkeypatch, op, force, N):
+def test_forced_variants_walk_several_rows(debug_env, op, force, N):
     # one CTA per SM: each CTA walks several rows, exercising the persistent
     # loop, the next-row prefetch and the alternating reduction buffers
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+    debug_env.set("RMSNORM_FORCE_VARIANT", force)
     M = 2000 if N <= 1024 else 700
     x, g = make(M, N, "bf16", "bf16", seed=7)
     eps = f32(1e-6)

@@ -177,8 +177,8 @@ def test_forward(xd, wd, N, beta):
                                    "subwarp:g=8:vpt=2:cps=1", "cta:vpt=1:cps=1",
                                    "cta:vpt=2:t=64:cps=1", "cta:vpt=4:t=32:pf=0:cps=1",
                                    "generic:cps=1"])
-def test_forward_forced_variants_walk_many_rows(monkeypatch, force):
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+def test_forward_forced_variants_walk_many_rows(debug_env, force):
+    debug_env.set("RMSNORM_FORCE_VARIANT", force)
     x, g, b, _ = inputs(2000, 128, "bf16", "bf16", seed=3)
     check_fwd(run_fwd(x, g, b, f32(1e-5), "bf16", "bf16"), x, g, b, f32(1e-5), "bf16", "bf16")
 
@@ -217,10 +217,10 @@ def test_backward(xd, wd, N, saved):
                                    "staged:vpt=1:st=2:cps=1", "staged:vpt=2:t=64:st=3:cps=1",
                                    "staged:vpt=4:t=32:st=8:cps=1", "generic:cps=1", "generic"])
 @pytest.mark.parametrize("N", [128, 32])
-def test_backward_forced_variants_walk_many_rows(monkeypatch, force, N):
+def test_backward_forced_variants_walk_many_rows(debug_env, force, N):
     if "g=4" in force and N != 32:
         pytest.skip("4 lanes hold at most 4 vectors")
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+    debug_env.set("RMSNORM_FORCE_VARIANT", force)
     x, g, _, dy = inputs(3000, N, "bf16", "bf16", seed=6)
     fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
     out = run_bwd(dy, x, fw["mean"], fw["rstd"], g, f32(1e-5), "bf16", "bf16")
@@ -228,22 +228,22 @@ def test_backward_forced_variants_walk_many_rows(monkeypatch, force, N):
 
 
 @pytest.mark.parametrize("saved", [True, False])
-def test_backward_staged_wait_timeout_is_reported_and_the_context_survives(monkeypatch, saved):
+def test_backward_staged_wait_timeout_is_reported_and_the_context_survives(debug_env, saved):
     # a negative wait limit: every wait for a row gives up at once; the kernel
     # stores nothing more, drains its copies and raises the flag that
     # rmsnorm_check_device reports and clears
     x, g, _, dy = inputs(1024, 8192, "bf16", "bf16", seed=44)
     fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
     mean, rstd = (fw["mean"], fw["rstd"]) if saved else (None, None)
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=3")
+    debug_env.set("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=3")
     rn.rmsnorm_check_device()
-    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
+    debug_env.set("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     run_bwd(dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
     with pytest.raises(rn.RMSNormError) as e:
         rn.rmsnorm_check_device()
     assert e.value.status == 6
     rn.rmsnorm_check_device()
-    monkeypatch.delenv("RMSNORM_WAIT_LIMIT_CYCLES")
+    debug_env.delete("RMSNORM_WAIT_LIMIT_CYCLES")
     out = run_bwd(dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
     check_bwd(out, dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
     rn.rmsnorm_check_device()

@@ -201,9 +201,9 @@ FORCED = ["subwarp:g=32:vpt=2:cps=1", "subwarp:g=8:vpt=2:cps=1", "subwarp:g=16:v
 
 @pytest.mark.parametrize("force", FORCED)
 @pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
-def test_forced_variants_walk_many_rows(monkeypatch, force, kind):
+def test_forced_variants_walk_many_rows(debug_env, force, kind):
     # N = 128 bf16: 16 vectors per row; one CTA per SM, so every CTA loops
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+    debug_env.set("RMSNORM_FORCE_VARIANT", force)
     x, g, r = inputs(2000, 128, "bf16", "bf16", seed=5, fused=True)
     out = run(kind, x, g, f32(1e-6), "bf16", "bf16", residual=r, gs=GS)
     if kind == "fp8":
@@ -216,9 +216,9 @@ def test_forced_variants_walk_many_rows(monkeypatch, force, kind):
 @pytest.mark.parametrize("N", [2064, 8192])
 @pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
 @pytest.mark.parametrize("fused", [False, True])
-def test_staged_ring_long_rows(monkeypatch, xd, wd, N, kind, fused):
+def test_staged_ring_long_rows(debug_env, xd, wd, N, kind, fused):
     # rows arrive through the bulk-copy ring; two stages, so it wraps often
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:st=2")
+    debug_env.set("RMSNORM_FORCE_VARIANT", "staged:st=2")
     x, g, r = inputs(200, N, xd, wd, seed=N + 9, fused=fused, outliers=fused)
     out = run(kind, x, g, f32(1e-6), xd, wd, residual=r, gs=GS)
     if kind == "fp8":
@@ -228,20 +228,20 @@ def test_staged_ring_long_rows(monkeypatch, xd, wd, N, kind, fused):
 
 
 @pytest.mark.parametrize("kind", ["fp8", "nvfp4"])
-def test_staged_wait_timeout_is_reported_and_the_context_survives(monkeypatch, kind):
+def test_staged_wait_timeout_is_reported_and_the_context_survives(debug_env, kind):
     # a negative wait limit: every wait for a row gives up at once; the kernel
     # stores nothing more, drains its copies and raises the flag that
     # rmsnorm_check_device reports and clears
     x, g, r = inputs(1024, 8192, "bf16", "bf16", seed=43, fused=True)
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
+    debug_env.set("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
     rn.rmsnorm_check_device()
-    monkeypatch.setenv("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
+    debug_env.set("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     run(kind, x, g, f32(1e-6), "bf16", "bf16", residual=r, gs=GS)
     with pytest.raises(rn.RMSNormError) as e:
         rn.rmsnorm_check_device()
     assert e.value.status == 6
     rn.rmsnorm_check_device()
-    monkeypatch.delenv("RMSNORM_WAIT_LIMIT_CYCLES")
+    debug_env.delete("RMSNORM_WAIT_LIMIT_CYCLES")
     out = run(kind, x, g, f32(1e-6), "bf16", "bf16", residual=r, gs=GS)
     if kind == "fp8":
         check_fp8(out, x, g, f32(1e-6), "bf16", "bf16", residual=r)
@@ -252,9 +252,9 @@ def test_staged_wait_timeout_is_reported_and_the_context_survives(monkeypatch, k
 
 @pytest.mark.parametrize("eps", [0.0, 1e-6])
 @pytest.mark.parametrize("force", ["", "generic", "staged:st=2"])
-def test_zero_rows_and_blocks(monkeypatch, eps, force):
+def test_zero_rows_and_blocks(debug_env, eps, force):
     if force:
-        monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+        debug_env.set("RMSNORM_FORCE_VARIANT", force)
     x, g, _ = inputs(8, 64, "bf16", "bf16", seed=6)
     x[2] = 0                  # an all-zero row
     x[5, 16:32] = 0           # an all-zero block

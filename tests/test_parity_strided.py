@@ -102,7 +102,7 @@ def test_single_head_rows_with_a_token_stride():
 
 @pytest.mark.parametrize("force", ["subwarp:g=16:vpt=1:pf=1:cps=1", "subwarp:g=8:vpt=2:pf=0:cps=1",
                                    "subwarp:g=32:vpt=1:pf=1:cps=1", "generic:cps=1"])
-def test_forced_variants_walk_many_rows(monkeypatch, force):
+def test_forced_variants_walk_many_rows(debug_env, force):
     # few CTAs: every thread steps (token, head) across many rows and wraps
-    monkeypatch.setenv("RMSNORM_FORCE_VARIANT", force)
+    debug_env.set("RMSNORM_FORCE_VARIANT", force)
     run_case(3001, 7, 1, 128, "bf16", "bf16", seed=11)

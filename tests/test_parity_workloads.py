@@ -44,11 +44,13 @@ def test_workload_matches_oracle(name):
         rstd = oracle.fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want64=False)["rstd"]
         out = fb.run(x, inp["dy"], inp["residual"], g, rstd, eps, wl.x_dtype, wl.w_dtype,
                      dg_dtype=wl.w_dtype)
-        fb.check(x, inp["dy"], inp["residual"], g, rstd, eps, wl.x_dtype, wl.w_dtype, out,
-                 dg_dtype=wl.w_dtype)
+        info = fb.check(x, inp["dy"], inp["residual"], g, rstd, eps, wl.x_dtype, wl.w_dtype,
+                        out, dg_dtype=wl.w_dtype)
+        print("FLOOR", name, info["floor"], wl.M * wl.N)
     else:
         # the saved rstd comes from the oracle forward
         rstd = oracle.fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want64=False)["rstd"]
         out = pu.run_bwd(inp["dy"], x, rstd, g, eps, wl.x_dtype, wl.w_dtype)
         info = check_bwd(x, inp["dy"], g, rstd, eps, wl.x_dtype, wl.w_dtype, out)
-        print(name, info)
+        # elements that needed the cancellation floor, of the tensor's size
+        print("FLOOR", name, info.get("floor", 0), wl.M * wl.N, info)

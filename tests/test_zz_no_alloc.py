@@ -5,9 +5,11 @@ the workspace it asks for.  The entry point keeps the dgamma partial rows in a
 scratch array inside the library's device image instead.
 
 Checked through the C ABI against rmsnorm_bwd (with a workspace) on two calls
-in a row with different shapes and data, and for the rejection of a shape
-whose partial rows do not fit the scratch.  This file is collected last; it
-passes alone in a fresh process and after the other tests.
+in a row with different shapes and data -- bit for bit, since both run the
+same kernels -- and against the oracle; also on ragged rows (whose grid is
+whole residue classes of the row alignment) and fp32 operands, and for the
+rejection of a shape whose partial rows do not fit the scratch.  This file is
+collected last; it passes alone in a fresh process and after the other tests.
 """
 import numpy as np
 import pytest
@@ -22,6 +24,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import row_wise_normalization_02_gb300 as rn  # noqa: E402
+from tests.test_parity_bwd import check_bwd  # noqa: E402
 
 
 def _inputs(M, N, xd, wd, seed):
@@ -53,25 +56,28 @@ def _compare_with_workspace_entry_point(M, N, xd, wd, seed):
     for b in (dx_a, dg_a, dx_b, dg_b, bws):
         assert b.guards_ok()
 
-    npd = np.uint16 if xd == "bf16" else np.float32
+    npd = pu.np_dtype(xd)
     a_dx, b_dx = dx_a.download(npd, (M, N)), dx_b.download(npd, (M, N))
     a_dg, b_dg = dg_a.download(np.float32), dg_b.download(np.float32)
-    # within the tolerances the parity tests use: 2 bf16 ulp for dx, 1e-4
-    # relative for dgamma (the two calls run the same kernels, so they agree
-    # exactly in practice)
-    if xd == "bf16":
-        pu.check_bf16_ulp(b_dx, a_dx, what="dx (noalloc vs workspace)")
-    else:
-        pu.check_f32(b_dx, a_dx.astype(np.float64), what="dx (noalloc vs workspace)")
-    scale = np.maximum(np.abs(a_dg.astype(np.float64)), 1e-30)
-    assert (np.abs(b_dg.astype(np.float64) - a_dg) <= 1e-4 * scale).all()
-    return np.array_equal(a_dx, b_dx) and np.array_equal(a_dg, b_dg)
+    # both calls run the same kernels over the same rows in the same order,
+    # so anything short of bit equality is a fault
+    assert np.array_equal(a_dx.view(np.uint8), b_dx.view(np.uint8)), "dx differs"
+    assert np.array_equal(a_dg.view(np.uint32), b_dg.view(np.uint32)), "dgamma differs"
+    # and the result is the backward's, within the parity tolerances
+    check_bwd(x, dy, g, rstd, eps, xd, wd, {"dx": b_dx, "dgamma": b_dg})
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
-    first = _compare_with_workspace_entry_point(4096, 8192, "bf16", "f32", seed=31)
-    second = _compare_with_workspace_entry_point(3000, 2048, "bf16", "bf16", seed=32)
-    print("bit-identical to rmsnorm_bwd:", first, second)
+    # two calls in a row with different shapes and data: the second finds the
+    # first call's partial rows in the scratch and must not depend on them
+    _compare_with_workspace_entry_point(4096, 8192, "bf16", "f32", seed=31)
+    _compare_with_workspace_entry_point(3000, 2048, "bf16", "bf16", seed=32)
+
+
+@pytest.mark.parametrize("M,N,xd,wd", [(4096, 2049, "bf16", "bf16"),   # ragged rows
+                                       (1024, 4096, "f32", "f32")])
+def test_noalloc_ragged_and_fp32_shapes(M, N, xd, wd):
+    _compare_with_workspace_entry_point(M, N, xd, wd, seed=34)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
