@@ -1,9 +1,9 @@
 """Build librmsnorm_gb300.so in-tree with nvcc for sm_103a.
 
-Nineteen translation units (forward, backward, staged, ragged,
-quantised-output and LayerNorm kernels once per dtype pair, plus the C ABI) compile in parallel, then link into one
-shared library with the CUDA runtime linked statically.  Rebuilds only when a source is newer than the
-library.
+Twenty-two translation units (forward, backward, staged, ragged, cluster,
+quantised-output and LayerNorm kernels once per dtype pair, plus the C ABI)
+compile in parallel, then link into one shared library with the CUDA runtime
+linked statically.  Rebuilds only when a source is newer than the library.
 """
 from __future__ import annotations
 
@@ -41,6 +41,9 @@ UNITS = [("rmsnorm_fwd.cu", ["-DRMSN_PAIR=0"], "fwd_p0.o"),
          ("rmsnorm_layernorm.cu", ["-DRMSN_PAIR=0"], "ln_p0.o"),
          ("rmsnorm_layernorm.cu", ["-DRMSN_PAIR=1"], "ln_p1.o"),
          ("rmsnorm_layernorm.cu", ["-DRMSN_PAIR=2"], "ln_p2.o"),
+         ("rmsnorm_cluster.cu", ["-DRMSN_PAIR=0"], "cluster_p0.o"),
+         ("rmsnorm_cluster.cu", ["-DRMSN_PAIR=1"], "cluster_p1.o"),
+         ("rmsnorm_cluster.cu", ["-DRMSN_PAIR=2"], "cluster_p2.o"),
          ("rmsnorm_api.cu", [], "api.o")]
 
 

@@ -55,6 +55,12 @@ FwdKernel fwd_kernel(const FwdKey& k) {
     if (k.xd == kBF16 && k.wd == kF32) return get_fwd_ragged_bf16_f32(k);
     return nullptr;
   }
+  if (k.family == kCluster) {
+    if (k.xd == kF32 && k.wd == kF32) return get_fwd_cluster_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16) return get_fwd_cluster_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32) return get_fwd_cluster_bf16_f32(k);
+    return nullptr;
+  }
   const bool st = k.family == kStaged;
   if (k.xd == kF32 && k.wd == kF32) return st ? get_fwd_staged_f32_f32(k) : get_fwd_kernel_f32_f32(k);
   if (k.xd == kBF16 && k.wd == kBF16)
@@ -68,6 +74,12 @@ BwdKernel bwd_kernel(const BwdKey& k) {
     if (k.xd == kF32 && k.wd == kF32) return get_bwd_ragged_f32_f32(k);
     if (k.xd == kBF16 && k.wd == kBF16) return get_bwd_ragged_bf16_bf16(k);
     if (k.xd == kBF16 && k.wd == kF32) return get_bwd_ragged_bf16_f32(k);
+    return nullptr;
+  }
+  if (k.family == kCluster) {
+    if (k.xd == kF32 && k.wd == kF32) return get_bwd_cluster_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16) return get_bwd_cluster_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32) return get_bwd_cluster_bf16_f32(k);
     return nullptr;
   }
   const bool st = k.family == kStaged;
@@ -153,29 +165,46 @@ cudaError_t ensure_smem(const void* fn, int device, int smem) {
   return cudaSuccess;
 }
 
-// Resident CTAs per SM of (kernel, threads, smem), cached.
+// Resident CTAs per SM of (kernel, threads, smem) -- or, for a cluster size
+// > 0, clusters of that size the whole device holds at once -- cached.
 struct OccEntry {
   const void* fn;
-  int device, threads, smem, blocks;
+  int device, threads, smem, cluster, blocks;
 };
 OccEntry g_occ[512];
 int g_nocc = 0;
 
-cudaError_t occupancy(const void* fn, int device, int threads, int smem, int* blocks) {
+cudaError_t occupancy(const void* fn, int device, int threads, int smem, int* blocks,
+                      int cluster = 0) {
   cudaError_t e = ensure_smem(fn, device, smem);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < g_nocc; ++i)
     if (g_occ[i].fn == fn && g_occ[i].device == device && g_occ[i].threads == threads &&
-        g_occ[i].smem == smem) {
+        g_occ[i].smem == smem && g_occ[i].cluster == cluster) {
       *blocks = g_occ[i].blocks;
       return cudaSuccess;
     }
   int b = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
+  if (cluster > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&b, fn, &cfg);
+  } else {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
+  }
   if (e != cudaSuccess) return e;
   if (b < 1) return cudaErrorInvalidConfiguration;
-  if (g_nocc < 512) g_occ[g_nocc++] = OccEntry{fn, device, threads, smem, b};
+  if (g_nocc < 512) g_occ[g_nocc++] = OccEntry{fn, device, threads, smem, cluster, b};
   *blocks = b;
   return cudaSuccess;
 }
@@ -197,6 +226,8 @@ struct Plan {
   int period = 1;            // kRagged: the grid is a multiple of it
   int cta_per_sm_cap = 0;    // 0: occupancy limit
   int l2_ahead = 0;          // LayerNorm register kernels: L2 lookahead in iterations
+  int cluster = 0;           // kCluster: CTAs per cluster (one row per cluster)
+  int slice = 0;             // kCluster: vectors of each row per CTA
   const void* fn = nullptr;
   FwdKernel fwd = nullptr;
   BwdKernel bwd = nullptr;
@@ -249,6 +280,30 @@ bool cta_shape(int op, int nvec, int* vpt, int* threads) {
   return false;
 }
 
+// Cluster shape for a row of nvec vectors: the fewest CTAs (2, 4 or 8) whose
+// slices hold at most 1024 vectors (4 per thread in 256-thread CTAs, the
+// best forward shape of one CTA per row), else 8 CTAs with up to 2048
+// vectors each (4 per thread, 512 threads) -- or, forward only, 4096 (8 per
+// thread, no next-row prefetch).  cl > 0 fixes the cluster size.  False when
+// the row is too long.
+bool cluster_shape(bool bwd, int nvec, int cl, int* c_out, int* slice, int* vpt, int* threads) {
+  int c = cl;
+  if (c <= 0)
+    for (c = 2; c < 8 && (nvec + c - 1) / c > 1024; c *= 2) {
+    }
+  if (c < 1 || c > 8) return false;
+  const int sl = (nvec + c - 1) / c;
+  const int v = sl <= 2048 ? 4 : 8;
+  if (v == 8 && bwd) return false;
+  const int t = round_up((sl + v - 1) / v, 32);
+  if (t > kCtaMaxThreads) return false;
+  *c_out = c;
+  *slice = sl;
+  *vpt = v;
+  *threads = t < 64 ? 64 : t;
+  return true;
+}
+
 // Vectors per thread (1, 2 or 4) and CTA size for a ragged row of at most
 // nvec vectors; false when the row needs more than 4 x 512.
 bool ragged_shape(int nvec, int* vpt, int* threads) {
@@ -278,11 +333,11 @@ int ragged_period(int64_t bytes) {
 // loaded and again only by rmsnorm_reload_debug_env -- never on the launch
 // path:
 //  RMSNORM_FORCE_VARIANT="family[:key=value...]" with family one of subwarp,
-//    cta, ragged, generic, staged and keys g, vpt, t (threads), pf (0/1),
-//    acc (0/1 shared-memory dgamma partials), cps (CTAs per SM cap), st
-//    (stages), mr (backward: minimum rows per CTA, 0 = none), l2 (L2
-//    lookahead).  For profiling A/B runs; a forced variant that cannot
-//    serve the call is an argument error.
+//    cta, ragged, generic, staged, cluster and keys g, vpt, t (threads), pf
+//    (0/1), acc (0/1 shared-memory dgamma partials), cps (CTAs per SM cap),
+//    st (stages), mr (backward: minimum rows per CTA, 0 = none), l2 (L2
+//    lookahead), cl (CTAs per cluster).  For profiling A/B runs; a forced
+//    variant that cannot serve the call is an argument error.
 //  RMSNORM_WAIT_LIMIT_CYCLES: clock cycles a bulk-copy wait lasts before it
 //    gives up (a test knob; a negative value makes every wait give up at
 //    once), else about 2 s.
@@ -290,7 +345,7 @@ int ragged_period(int64_t bytes) {
 struct Force {
   bool on = false;
   int family = -1, g = 0, vpt = 0, threads = 0, pf = -1, acc = -1, cps = 0, st = 0, mr = -1,
-      l2 = -1;
+      l2 = -1, cl = 0;
 };
 
 struct DebugEnv {
@@ -314,6 +369,7 @@ Force parse_force(const char* s) {
   else if (!strcmp(tok, "ragged")) f.family = kRagged;
   else if (!strcmp(tok, "generic")) f.family = kGeneric;
   else if (!strcmp(tok, "staged")) f.family = kStaged;
+  else if (!strcmp(tok, "cluster")) f.family = kCluster;
   while ((tok = strtok_r(nullptr, ":", &save))) {
     char* eq = strchr(tok, '=');
     if (!eq) continue;
@@ -328,6 +384,7 @@ Force parse_force(const char* s) {
     else if (!strcmp(tok, "st")) f.st = v;
     else if (!strcmp(tok, "mr")) f.mr = v;
     else if (!strcmp(tok, "l2")) f.l2 = v;
+    else if (!strcmp(tok, "cl")) f.cl = v;
   }
   return f;
 }
@@ -374,11 +431,24 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     // 32768 x 4096 bf16: 0.83 -> 1.0 of the copy bandwidth); the plain
     // backward is best at two
     p.stages = dres && kStagedHeader + 3 * 3 * (int64_t)N * esize(xd) <= kStagedSmemMax ? 3 : 2;
+  } else if (rows_aligned && bwd) {
+    // longer rows: one row per cluster, each CTA streaming its slice through
+    // a two-stage bulk-copy ring
+    p.family = kCluster;
+    if (!cluster_shape(true, nvec, 0, &p.cluster, &p.slice, &p.vpt, &p.threads))
+      p.family = kGeneric;
+    p.stages = 2;
   } else if (rows_aligned && nvec <= 4096) {
-    p.family = dres ? kGeneric : kCta;   // the fused-add backward has no kCta form
-    if (p.family == kCta && !cta_shape(op, nvec, &p.vpt, &p.threads)) p.family = kGeneric;
+    p.family = kCta;
+    if (!cta_shape(op, nvec, &p.vpt, &p.threads)) p.family = kGeneric;
     p.prefetch = op == kFwd ? p.vpt <= 4 : (op == kFused ? p.vpt != 2 && p.vpt <= 4 : p.vpt <= 2);
-    p.acc_smem = bwd && p.vpt >= 4;
+  } else if (rows_aligned) {
+    // longer rows: one row per cluster, each CTA holding its slice in
+    // registers with the next row's slice in flight
+    p.family = kCluster;
+    if (!cluster_shape(false, nvec, 0, &p.cluster, &p.slice, &p.vpt, &p.threads))
+      p.family = kGeneric;
+    p.prefetch = p.vpt <= 4;
   } else if (same_mod16 && N <= kRaggedMaxN) {
     p.family = kRagged;
     if (!ragged_shape(N / E + 1, &p.vpt, &p.threads)) p.family = kGeneric;
@@ -428,10 +498,26 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       // default's depth, or takes as many stages as fit when the default is
       // another family
       if (f.st > 0 || f.family == kStaged) p.stages = f.st;
+    } else if (p.family == kCluster) {
+      if (!rows_aligned) return RMSNORM_ERR_INVALID_ARG;
+      if (f.cl || f.family == kCluster) {
+        if (!cluster_shape(bwd, nvec, f.cl, &p.cluster, &p.slice, &p.vpt, &p.threads))
+          return RMSNORM_ERR_INVALID_ARG;
+        if (f.vpt) p.vpt = f.vpt;
+        p.threads = f.threads ? f.threads : round_up((p.slice + p.vpt - 1) / p.vpt, 32);
+        if (f.pf < 0) p.prefetch = !bwd && p.vpt <= 4;
+      }
+      if (p.vpt < 1 || (int64_t)p.threads * p.vpt < p.slice) return RMSNORM_ERR_INVALID_ARG;
+      if (bwd) {
+        p.prefetch = false;
+        if (f.st > 0) p.stages = f.st;
+        if (p.stages < 2) p.stages = 2;
+      }
     } else if (p.family == kGeneric) {
       if (!f.threads) p.threads = 256;
       if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
     }
+    if (p.family != kCluster) p.cluster = p.slice = 0;
     if (p.family != kSubwarp) p.rows_per_cta = 1;
     if (p.family != kRagged) p.period = 1;
     if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32) return RMSNORM_ERR_INVALID_ARG;
@@ -481,7 +567,12 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (p.family == kSubwarp) p.smem = p.rows_per_cta * nvec * E * 4;
     else if (p.family == kCta) p.smem = 512 + (p.acc_smem ? ld * 4 : 0);
     else if (p.family == kRagged) p.smem = 512;
-    else if (p.family != kStaged) p.smem = 0;
+    else if (p.family == kCluster) {
+      // ring of the slice of [x | dy] ([h | dy | dres]) rows
+      const int64_t bytes = kStagedHeader + (int64_t)p.stages * (dres ? 3 : 2) * p.slice * 16;
+      if (p.stages > kStagedMaxStages || bytes > kStagedSmemMax) return RMSNORM_ERR_INVALID_ARG;
+      p.smem = (int)bytes;
+    } else if (p.family != kStaged) p.smem = 0;
   } else {
     FwdKey k{xd, wd, p.family, p.g, p.vpt, op == kFused, p.prefetch, false};
     p.fwd = fwd_kernel(k);
@@ -502,6 +593,28 @@ rmsnorm_status_t size_grid(Plan* p, int64_t M, int device, unsigned** status = n
   if (e != cudaSuccess) return cuda_fail(e, "device attributes");
   if (status) *status = di.status;
   if (p->smem > di.max_smem_optin) return RMSNORM_ERR_INVALID_ARG;
+  if (p->cluster > 0) {
+    // one row per cluster: as many clusters as the device holds at once (the
+    // occupancy query accounts for how clusters pack into the GPCs)
+    int clusters = 0;
+    if ((e = occupancy(p->fn, device, p->threads, p->smem, &clusters, p->cluster)) !=
+        cudaSuccess)
+      return cuda_fail(e, "cluster occupancy query");
+    int64_t cap = clusters;
+    if (p->cta_per_sm_cap > 0) {
+      const int64_t lim = (int64_t)di.sms * p->cta_per_sm_cap / p->cluster;
+      if (cap > lim) cap = lim > 0 ? lim : 1;
+    }
+    if (p->min_rows > 0) {
+      const int64_t want = (M + p->min_rows - 1) / p->min_rows;
+      const int64_t floor_cap = di.sms / p->cluster < cap ? di.sms / p->cluster : cap;
+      cap = want < floor_cap ? floor_cap : (want < cap ? want : cap);
+    }
+    int64_t n = M < cap ? M : cap;
+    if (n < 1) n = 1;
+    p->grid = (int)n * p->cluster;
+    return RMSNORM_OK;
+  }
   int per_sm = 0;
   if ((e = occupancy(p->fn, device, p->threads, p->smem, &per_sm)) != cudaSuccess)
     return cuda_fail(e, "occupancy query");
@@ -528,6 +641,7 @@ const char* family_name(int f) {
     case kCta: return "cta";
     case kRagged: return "ragged";
     case kStaged: return "staged";
+    case kCluster: return "cluster";
     default: return "generic";
   }
 }
@@ -539,9 +653,11 @@ void describe(int op, const Plan& p, char* buf, size_t len) {
   const bool bwd = op == kBwd || op == kFusedBwd;
   char l2[24] = "";
   if (p.l2_ahead > 0) snprintf(l2, sizeof l2, "/l2ahead%d", p.l2_ahead);
-  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d%s", ops[op],
+  char cl[32] = "";
+  if (p.cluster > 0) snprintf(cl, sizeof cl, "/cl%d/slice%d", p.cluster, p.slice);
+  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d%s%s", ops[op],
            family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
-           bwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem, l2);
+           bwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem, l2, cl);
 }
 
 // ---------------------------------------------------------------- launches
@@ -551,20 +667,49 @@ void describe(int op, const Plan& p, char* buf, size_t len) {
 // of one call overlaps the end of the previous one.  RMSNORM_NO_PDL=1 (read
 // with the other debug knobs) turns the attribute off for A/B measurements.
 template <typename... Args>
-cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
-                   cudaStream_t stream, Args... args) {
+cudaError_t launch_in_clusters(int cluster, void (*kernel)(Args...), int grid, int threads,
+                               int smem, cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  const bool pdl = !g_env.no_pdl;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (!g_env.no_pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 0) {   // thread-block clusters of `cluster` consecutive CTAs
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+template <typename... Args>
+cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
+                   cudaStream_t stream, Args... args) {
+  return launch_in_clusters(0, kernel, grid, threads, smem, stream, args...);
+}
+
+// Stage 2 of a backward (column sums of P partial rows of nq float4): C
+// float4 columns per CTA, the largest of 8, 4, 2 that still gives two CTAs
+// per SM (two at least, so that a warp reads whole 32-byte sectors).
+cudaError_t launch_colsum(const float* part, int P, int nq, const ColSumOut& o, int device,
+                          cudaStream_t stream) {
+  DevInfo di;
+  const cudaError_t e = device_info(device, &di);
+  if (e != cudaSuccess) return e;
+  int c = 8;
+  while (c > 2 && (nq + c - 1) / c < 2 * di.sms) c /= 2;
+  return launch(get_colsum_kernel(c), (nq + c - 1) / c, kColSumThreads, 0, stream, part, P, nq,
+                o);
 }
 
 // ---------------------------------------------------------------- validation
@@ -639,7 +784,9 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   prm.status = status;
   prm.period = pl.period;
   prm.l2_rows = pl.l2_ahead;
-  const cudaError_t e = launch(pl.fwd, pl.grid, pl.threads, pl.smem, stream, prm);
+  prm.slice = pl.slice;
+  const cudaError_t e =
+      launch_in_clusters(pl.cluster, pl.fwd, pl.grid, pl.threads, pl.smem, stream, prm);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "forward kernel launch");
@@ -1200,8 +1347,8 @@ rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
   if (!want) return RMSNORM_OK;
   // stage 2: both halves of the partial rows, summed per column in a fixed order
   const float* part = static_cast<const float*>(workspace);
-  e = launch(get_ln_reduce_kernel(), (2 * ld_half / 4 + kRedCols - 1) / kRedCols,
-             kRedCols * kRedRows, 0, stream, part, p.grid, (int)N, ld_half, dgamma, dbeta);
+  e = launch_colsum(part, p.grid, 2 * ld_half / 4,
+                    ColSumOut{dgamma, dbeta, ld_half / 4, (int)N, 0}, dev, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "LayerNorm backward stage-2 launch");
@@ -1223,7 +1370,7 @@ rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, 
     return st;
   }
   if ((st = size_grid(&pl, M, device)) != RMSNORM_OK) return st;
-  *rows = pl.grid;
+  *rows = pl.cluster > 0 ? pl.grid / pl.cluster : pl.grid;   // a partial row per cluster
   return RMSNORM_OK;
 }
 
@@ -1286,7 +1433,11 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
     return st;
   unsigned* status = nullptr;
   if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
-  if (dgamma && pl.grid > prows) pl.grid = prows;
+  if (pl.cluster > 0) {
+    if (dgamma && pl.grid / pl.cluster > prows) pl.grid = prows * pl.cluster;
+  } else if (dgamma && pl.grid > prows) {
+    pl.grid = prows;
+  }
   if (pl.period > 1) {   // ragged rows: whole residue classes only
     pl.grid = pl.grid / pl.period * pl.period;
     if (pl.grid < pl.period) return RMSNORM_ERR_WORKSPACE;
@@ -1311,7 +1462,9 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   prm.status = status;
   prm.period = pl.period;
   prm.l2_rows = pl.l2_ahead;
-  cudaError_t e = launch(pl.bwd, pl.grid, pl.threads, pl.smem, stream, prm);
+  prm.slice = pl.slice;
+  cudaError_t e =
+      launch_in_clusters(pl.cluster, pl.bwd, pl.grid, pl.threads, pl.smem, stream, prm);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "backward stage-1 launch");
@@ -1319,8 +1472,8 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   if (!dgamma) return RMSNORM_OK;
   // stage 2: the P partial rows summed per column in a fixed order
   const float* part = static_cast<const float*>(workspace);
-  e = launch(get_dgamma_reduce_kernel(), (ld / 4 + kRedCols - 1) / kRedCols, kRedCols * kRedRows,
-             0, stream, part, pl.grid, (int)N, ld, dgamma, dgamma_bf16 ? 1 : 0);
+  e = launch_colsum(part, pl.cluster > 0 ? pl.grid / pl.cluster : pl.grid, ld / 4,
+                    ColSumOut{dgamma, nullptr, ld / 4, (int)N, dgamma_bf16 ? 1 : 0}, dev, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "backward stage-2 launch");

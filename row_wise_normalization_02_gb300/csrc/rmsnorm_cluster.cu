@@ -1,0 +1,363 @@
+// RMSNorm forward, fused add, backward and fused-add backward for rows too
+// long for one CTA, on thread-block clusters (sm_103a).
+//
+// Arithmetic as in rmsnorm_fwd.cu / rmsnorm_bwd.cu.  One row is handled by a
+// cluster of C = 2, 4 or 8 CTAs: CTA rank r owns the contiguous slice of
+// vectors [r * slice, (r + 1) * slice) of every row of the cluster's walk, so
+// every element is still read once from HBM with 16-byte accesses and kept on
+// chip until its output is written -- the register-resident path of the
+// "Pre-built kernel library guide" (section 1.1) and the LDS row cache of its
+// section 1.2 carried past the size of one CTA.  Where that guide combines
+// the per-wave partial sums of a row inside one workgroup, a cluster combines
+// the per-CTA sums through distributed shared memory: each CTA publishes its
+// sum in a shared-memory slot, the cluster meets at a hardware cluster
+// barrier, and every thread reads all C slots (mapa + ld.shared::cluster) in
+// rank order, so every CTA obtains the same, fixed-order total.
+//
+//   forward / fused add : the slice in registers, the next row's slice loaded
+//                         before the current row is reduced (as kCta)
+//   backward            : the slices of x and dy (and dres) through a ring of
+//                         bulk copies (as kStaged); dgamma partials in
+//                         registers, one partial row per cluster, each CTA
+//                         writing its slice's columns
+//
+// Slots alternate between two buffers from row to row: a CTA rewrites a slot
+// two rows later, after the next cluster barrier, which no CTA passes before
+// it has read the slot.  Before leaving, every CTA meets the others at one
+// more cluster barrier, so that no CTA's shared memory disappears while a
+// peer may still read it.  The bounded bulk-copy waits of the backward are
+// voted on across the whole cluster along with the sums, so all CTAs of a
+// cluster stop at the same row and every cluster barrier is met by all.
+#include "rmsnorm_fwd_common.cuh"
+#include "rmsnorm_ring.cuh"
+
+#ifndef RMSN_PAIR
+#error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
+#endif
+
+namespace rmsn {
+namespace {
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives (release: its earlier
+// shared-memory writes become visible to the cluster) and waits (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The float at the same shared-memory offset as `p`, in the CTA of `rank`.
+__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// Sum of K values over the cluster, plus a flag raised by any thread of any
+// CTA.  slot: 2 x (K + 1) floats of this CTA's shared memory.
+template <int K>
+__device__ __forceinline__ bool cluster_sum_vote(float (&v)[K], float* red, float* slot,
+                                                 int parity, bool flag, uint32_t C) {
+  const bool any = cta_sum_vote<K>(v, red, parity, flag);
+  float* my = slot + parity * (K + 1);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) my[k] = v[k];
+    my[K] = any ? 1.f : 0.f;
+  }
+  cluster_sync();
+  bool all = false;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    float s = 0.f;
+    for (uint32_t r = 0; r < C; ++r) s += ld_cluster(my + k, r);
+    v[k] = s;
+  }
+  for (uint32_t r = 0; r < C; ++r) all = all || ld_cluster(my + K, r) != 0.f;
+  return all;
+}
+
+// Vectors [v0, v0 + nv) of a row are this CTA's slice.
+struct SliceOf {
+  int v0, nv;
+};
+__device__ __forceinline__ SliceOf slice_of(int slice, int nvec, uint32_t rank) {
+  const int v0 = (int)rank * slice;
+  int nv = nvec - v0;
+  nv = nv < 0 ? 0 : (nv > slice ? slice : nv);
+  return SliceOf{v0, nv};
+}
+
+// ---------------------------------------------------------------------------
+// Forward / fused add: the slice in registers, next-row prefetch (PF).
+template <typename TX, typename TW, int VPT, bool FUSED, bool PF>
+__global__ void __launch_bounds__(kCtaMaxThreads) fwd_cluster_kernel(const FwdParams p0) {
+  pdl_begin();
+  using Cf = Cfg<TX, TW>;
+  constexpr int E = Cf::E, GW = Cf::GW;
+  __shared__ float red[2 * 32];
+  __shared__ float slot[2 * 2];
+  const uint32_t C = cluster_ctas(), rank = cluster_rank();
+  const int tid = threadIdx.x, T = blockDim.x;
+  const SliceOf sl = slice_of(p0.slice, p0.nvec, rank);
+  // the parameters of this CTA's slice: operands shifted to its first vector
+  FwdParams p = p0;
+  const size_t off = (size_t)sl.v0 * 16;
+  p.x = static_cast<const char*>(p0.x) + off;
+  p.y = static_cast<char*>(p0.y) + off;
+  if (FUSED) p.residual = static_cast<char*>(p0.residual) + off;
+  p.nvec = sl.nv;
+  const char* gp = static_cast<const char*>(p0.gamma) + (size_t)sl.v0 * GW * 16;
+
+  uint4 gw[VPT][GW];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+#pragma unroll
+    for (int w = 0; w < GW; ++w)
+      gw[k][w] = v < sl.nv ? ld_cached(gp + ((size_t)v * GW + w) * 16) : make_uint4(0, 0, 0, 0);
+  }
+
+  const int64_t first = blockIdx.x / C, stride = gridDim.x / C;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  int parity = 0;
+  Slice<VPT, FUSED> cur, nxt;
+  if (first < p.M) load_aligned<TX, VPT, FUSED>(cur, p, first, true, tid, T);
+  for (int64_t row = first; row < p.M; row += stride) {
+    const int64_t nrow = row + stride;
+    if (PF && nrow < p.M) load_aligned<TX, VPT, FUSED>(nxt, p, nrow, true, tid, T);
+    char* yrow = static_cast<char*>(p.y) + row * rb;
+    char* hrow = static_cast<char*>(p.residual) + row * rb;
+    float ss[1];
+    ss[0] = slice_sumsq<TX, VPT, FUSED>(cur, hrow, tid, T, sl.nv, true);
+    cluster_sum_vote<1>(ss, red, slot, parity, false, C);
+    parity ^= 1;
+    const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
+    if (rank == 0 && tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < sl.nv) st_stream(yrow + (size_t)v * 16, scale_vec<TX, TW>(cur.x[k], gw[k], rs));
+    }
+    if (PF) cur = nxt;
+    else if (nrow < p.M) load_aligned<TX, VPT, FUSED>(cur, p, nrow, true, tid, T);
+  }
+  cluster_sync();
+}
+
+// ---------------------------------------------------------------------------
+// Backward (fused-add backward: DRES).  Stage layout [x | dy] ([h | dy | dres])
+// of this CTA's slice of the row; the slice's dgamma partials in registers.
+template <int NS>
+__device__ __forceinline__ void issue_slice(const Ring& rg, int64_t i, int64_t first,
+                                            int64_t stride, int S, const char* src0,
+                                            const char* src1, const char* src2, size_t rb,
+                                            uint32_t sb) {
+  const int s = (int)(i % S);
+  const int64_t row = first + i * stride;
+  uint64_t* bar = rg.full + s;
+  unsigned char* dst = rg.buf + (size_t)s * NS * sb;
+  mbar_arrive_expect_tx(bar, NS * sb);
+  if (sb == 0) return;
+  bulk_copy_g2s(dst, src0 + row * rb, sb, bar);
+  if (NS > 1) bulk_copy_g2s(dst + sb, src1 + row * rb, sb, bar);
+  if (NS > 2) bulk_copy_g2s(dst + 2 * sb, src2 + row * rb, sb, bar);
+}
+
+template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool DRES>
+__global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdParams p) {
+  pdl_begin();
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int K = HAS_RSTD ? 1 : 2;
+  constexpr int NS = DRES ? 3 : 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Ring rg = ring_of(smem);
+  float* slot = reinterpret_cast<float*>(smem + 640);   // in the header, after rg.red
+  const uint32_t C = cluster_ctas(), rank = cluster_rank();
+  const int tid = threadIdx.x, T = blockDim.x, S = p.stages;
+  const SliceOf sl = slice_of(p.slice, p.nvec, rank);
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const uint32_t sb = (uint32_t)sl.nv * 16;
+  const size_t off = (size_t)sl.v0 * 16;
+  const int64_t first = blockIdx.x / C, stride = gridDim.x / C;
+  const int64_t nrows = first < p.M ? (p.M - 1 - first) / stride + 1 : 0;
+  const char* xs = static_cast<const char*>(p.x) + off;
+  const char* ds = static_cast<const char*>(p.dy) + off;
+  const char* rs = DRES ? static_cast<const char*>(p.dres) + off : nullptr;
+  char* dxs = static_cast<char*>(p.dx) + off;
+
+  int64_t issued = 0;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int64_t n0 = nrows < S ? nrows : S;
+    for (; issued < n0; ++issued) issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
+  }
+
+  float g[VPT][E], acc[VPT][E];
+  const char* gbase = static_cast<const char*>(p.gamma) + (size_t)sl.v0 * E * sizeof(TW);
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < sl.nv) gamma_f32<TW, E>(gbase, v, g[k]);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) g[k][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+  }
+
+  int parity = 0;
+  int64_t i = 0;
+  bool failed = false;
+  for (; i < nrows; ++i) {
+    const int s = (int)(i % S);
+    const int64_t row = first + i * stride;
+    const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
+    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
+    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * NS * sb);
+    uint4 xv[VPT], dv[VPT];
+    float sums[K];
+#pragma unroll
+    for (int q = 0; q < K; ++q) sums[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      xv[k] = make_uint4(0, 0, 0, 0);
+      dv[k] = make_uint4(0, 0, 0, 0);
+      if (v < sl.nv) {
+        xv[k] = st[v];
+        dv[k] = st[sl.nv + v];
+        float xf[E], df[E];
+        unpack(xv[k], xf);
+        unpack(dv[k], df);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          sums[0] = fmaf(g[k][e] * df[e], xf[e], sums[0]);
+          if (!HAS_RSTD) sums[K - 1] = fmaf(xf[e], xf[e], sums[K - 1]);
+        }
+      }
+    }
+    if (cluster_sum_vote<K>(sums, rg.red, slot, parity, late, C)) {
+      failed = true;
+      break;
+    }
+    parity ^= 1;
+    if (!DRES && tid == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
+      ++issued;
+    }
+    const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
+    const float c = r * r * p.inv_n * sums[0];
+    char* dxrow = dxs + row * rb;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < sl.nv) {
+        float xf[E], df[E], o[E], rf[E];
+        unpack(xv[k], xf);
+        unpack(dv[k], df);
+        if (DRES) unpack(st[2 * sl.nv + v], rf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
+          if (DRES) o[e] += rf[e];
+          acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
+        }
+        st_stream(dxrow + (size_t)v * 16, pack(o));
+      }
+    }
+    if (DRES) {
+      // every thread has read this stage (dres included): refill it
+      __syncthreads();
+      if (tid == 0 && issued < nrows) {
+        fence_proxy_async_smem();
+        issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
+        ++issued;
+      }
+    }
+  }
+  if (failed && tid == 0) {
+    // every CTA of the cluster stops at the same row: wait (bounded) for the
+    // copies still in flight, then report
+    for (int64_t j = i; j < issued; ++j)
+      mbar_wait_bounded(rg.full + (j % S), (uint32_t)((j / S) & 1), kDrainLimit);
+    atomicOr(p.status, kStatusWaitTimeout);
+  }
+  cluster_sync();
+  if (failed || p.partial == nullptr) return;
+  float* prow = p.partial + (size_t)first * p.ld_partial + (size_t)sl.v0 * E;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < sl.nv) {
+      float4* d = reinterpret_cast<float4*>(prow + v * E);
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q)
+        d[q] = make_float4(acc[k][4 * q], acc[k][4 * q + 1], acc[k][4 * q + 2], acc[k][4 * q + 3]);
+    }
+  }
+}
+
+template <typename TX, typename TW, bool FUSED>
+FwdKernel pick_fwd(int vpt, bool pf) {
+  switch (vpt) {
+    case 2: return pf ? fwd_cluster_kernel<TX, TW, 2, FUSED, true>
+                      : fwd_cluster_kernel<TX, TW, 2, FUSED, false>;
+    case 4: return pf ? fwd_cluster_kernel<TX, TW, 4, FUSED, true>
+                      : fwd_cluster_kernel<TX, TW, 4, FUSED, false>;
+    case 8: return pf ? nullptr : fwd_cluster_kernel<TX, TW, 8, FUSED, false>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
+BwdKernel pick_bwd(int vpt) {
+  switch (vpt) {
+    case 2: return bwd_cluster_kernel<TX, TW, 2, HAS_RSTD, DRES>;
+    case 4: return bwd_cluster_kernel<TX, TW, 4, HAS_RSTD, DRES>;
+    default: return nullptr;
+  }
+}
+
+template <typename TX, typename TW>
+FwdKernel cluster_fwd(const FwdKey& k) {
+  if (k.family != kCluster || k.strided || k.out != kOutDtype) return nullptr;
+  return k.fused ? pick_fwd<TX, TW, true>(k.vpt, k.prefetch)
+                 : pick_fwd<TX, TW, false>(k.vpt, k.prefetch);
+}
+template <typename TX, typename TW>
+BwdKernel cluster_bwd(const BwdKey& k) {
+  if (k.family != kCluster) return nullptr;
+  if (k.dres)
+    return k.has_rstd ? pick_bwd<TX, TW, true, true>(k.vpt) : pick_bwd<TX, TW, false, true>(k.vpt);
+  return k.has_rstd ? pick_bwd<TX, TW, true, false>(k.vpt) : pick_bwd<TX, TW, false, false>(k.vpt);
+}
+
+}  // namespace
+
+#if RMSN_PAIR == 0
+FwdKernel get_fwd_cluster_f32_f32(const FwdKey& k) { return cluster_fwd<float, float>(k); }
+BwdKernel get_bwd_cluster_f32_f32(const BwdKey& k) { return cluster_bwd<float, float>(k); }
+#elif RMSN_PAIR == 1
+FwdKernel get_fwd_cluster_bf16_bf16(const FwdKey& k) { return cluster_fwd<bf16, bf16>(k); }
+BwdKernel get_bwd_cluster_bf16_bf16(const BwdKey& k) { return cluster_bwd<bf16, bf16>(k); }
+#else
+FwdKernel get_fwd_cluster_bf16_f32(const FwdKey& k) { return cluster_fwd<bf16, float>(k); }
+BwdKernel get_bwd_cluster_bf16_f32(const BwdKey& k) { return cluster_bwd<bf16, float>(k); }
+#endif
+
+}  // namespace rmsn

@@ -22,23 +22,6 @@
 namespace rmsn {
 namespace {
 
-// One output vector: y = x * rs * gamma, rounded once to TX (bf16 x and
-// gamma: (x * gamma) * rs from the packed words, see bf16x8_scale).
-template <typename TX, typename TW, int GW = Cfg<TX, TW>::GW>
-__device__ __forceinline__ uint4 scale_vec(const uint4& xv, const uint4 (&gw)[GW], float rs) {
-  if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
-    return bf16x8_scale(xv, gw[0], rs);
-  } else {
-    constexpr int E = Cfg<TX, TW>::E;
-    float g[E], o[E];
-    unpack_gamma<TW, E, GW>(gw, g);
-    unpack(xv, o);
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
-    return pack(o);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // kSubwarp: G lanes per row, 256 / G rows per CTA iteration, persistent grid.
 template <typename TX, typename TW, int G, int VPT, bool FUSED, bool PF>

@@ -1,8 +1,8 @@
 // Forward building blocks shared by the translation units of the forward
-// kernels (plain and quantised outputs): dtype-pair constants, gamma
-// unpacking, and the register slice of a row with its aligned load and its
-// sum of squares (which, for the fused add, also forms, rounds and stores
-// h = residual + x).
+// kernels (plain, cluster and quantised outputs): dtype-pair constants, gamma
+// unpacking, the register slice of a row with its aligned load and its sum of
+// squares (which, for the fused add, also forms, rounds and stores
+// h = residual + x), and the scaled output vector.
 #pragma once
 
 #include <type_traits>
@@ -137,6 +137,23 @@ __device__ __forceinline__ float slice_sumsq(Slice<VPT, FUSED>& s, char* res_row
     }
   }
   return ss + ss1;
+}
+
+// One output vector: y = x * rs * gamma, rounded once to TX (bf16 x and
+// gamma: (x * gamma) * rs from the packed words, see bf16x8_scale).
+template <typename TX, typename TW, int GW = Cfg<TX, TW>::GW>
+__device__ __forceinline__ uint4 scale_vec(const uint4& xv, const uint4 (&gw)[GW], float rs) {
+  if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value) {
+    return bf16x8_scale(xv, gw[0], rs);
+  } else {
+    constexpr int E = Cfg<TX, TW>::E;
+    float g[E], o[E];
+    unpack_gamma<TW, E, GW>(gw, g);
+    unpack(xv, o);
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = o[e] * rs * g[e];
+    return pack(o);
+  }
 }
 
 }  // namespace

@@ -23,7 +23,13 @@ enum DT : int { kF32 = 0, kBF16 = 1 };
 //  kStaged  : as kCta, but rows arrive by bulk copies (the 1-D form of TMA)
 //             into a ring of `stages` shared-memory row buffers, so several
 //             rows per CTA are in flight independently of register pressure.
-enum Family : int { kSubwarp = 0, kCta = 1, kRagged = 2, kGeneric = 3, kStaged = 4 };
+//  kCluster : one row per thread-block cluster of 2-8 CTAs, each CTA owning a
+//             contiguous slice of `slice` vectors of every row (forward: in
+//             registers; backward: through a bulk-copy ring); the CTAs' sums
+//             meet in distributed shared memory.  For rows too long for one
+//             CTA; rows 16-byte aligned.
+enum Family : int { kSubwarp = 0, kCta = 1, kRagged = 2, kGeneric = 3, kStaged = 4,
+                    kCluster = 5 };
 
 // Forward output kinds: y in the activation dtype, FP8 E4M3 codes with one
 // scale per row, or NVFP4 (E2M1 codes, an E4M3 scale per 16 elements).
@@ -62,6 +68,7 @@ struct FwdParams {
   float gs;
   int l2_rows;        // register kernels: rows of the CTA's walk fetched into L2
                       // this many iterations ahead (0: none)
+  int slice;          // kCluster: vectors of each row per CTA of the cluster
 };
 
 struct BwdParams {
@@ -84,6 +91,7 @@ struct BwdParams {
   unsigned* status;
   int period;
   int l2_rows;        // register kernels: L2 lookahead in iterations (0: none)
+  int slice;          // kCluster: vectors of each row per CTA of the cluster
 };
 
 // LayerNorm (forward and backward).
@@ -111,7 +119,18 @@ struct LnParams {
 
 using FwdKernel = void (*)(FwdParams);
 using BwdKernel = void (*)(BwdParams);
-using ReduceKernel = void (*)(const float*, int, int, int, void*, int);
+// Stage 2 of every backward: column sums of the P x nq float4 partial rows
+// (row stride nq float4), in a fixed order.  Float4 columns [0, half_q) go to
+// out0 and [half_q, 2 half_q) to out1 (the LayerNorm backward's dgamma and
+// dbeta); N valid columns per output; out0 in bf16 (rounded once) when bf16.
+struct ColSumOut {
+  void* out0;
+  void* out1;
+  int half_q;
+  int N;
+  int bf16;
+};
+using ColSumKernel = void (*)(const float*, int, int, ColSumOut);
 
 struct FwdKey {
   int xd, wd;
@@ -155,13 +174,19 @@ FwdKernel get_fwd_ragged_bf16_f32(const FwdKey& k);
 BwdKernel get_bwd_ragged_f32_f32(const BwdKey& k);
 BwdKernel get_bwd_ragged_bf16_bf16(const BwdKey& k);
 BwdKernel get_bwd_ragged_bf16_f32(const BwdKey& k);
+FwdKernel get_fwd_cluster_f32_f32(const FwdKey& k);
+FwdKernel get_fwd_cluster_bf16_bf16(const FwdKey& k);
+FwdKernel get_fwd_cluster_bf16_f32(const FwdKey& k);
+BwdKernel get_bwd_cluster_f32_f32(const BwdKey& k);
+BwdKernel get_bwd_cluster_bf16_bf16(const BwdKey& k);
+BwdKernel get_bwd_cluster_bf16_f32(const BwdKey& k);
 FwdKernel get_fwd_quant_f32_f32(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_bf16(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_f32(const FwdKey& k);
-ReduceKernel get_dgamma_reduce_kernel();
+// Column sum with C float4 columns per 256-thread CTA (C = 2, 4 or 8).
+ColSumKernel get_colsum_kernel(int c);
 
 using LnKernel = void (*)(LnParams);
-using LnReduceKernel = void (*)(const float*, int, int, int, float*, float*);
 struct LnKey {
   int xd, wd;
   int family;    // kSubwarp, kCta or kGeneric
@@ -172,13 +197,11 @@ struct LnKey {
 LnKernel get_ln_kernel_f32_f32(const LnKey& k);
 LnKernel get_ln_kernel_bf16_bf16(const LnKey& k);
 LnKernel get_ln_kernel_bf16_f32(const LnKey& k);
-LnReduceKernel get_ln_reduce_kernel();
 
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;
 constexpr int kCtaMaxThreads = 512;
-// Stage-2 reduction tile: kRedCols float4 column groups x kRedRows row chunks.
-constexpr int kRedCols = 8;
-constexpr int kRedRows = 32;
+// Threads of a stage-2 (column sum) CTA.
+constexpr int kColSumThreads = 256;
 
 }  // namespace rmsn

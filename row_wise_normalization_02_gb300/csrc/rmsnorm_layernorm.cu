@@ -810,57 +810,10 @@ LnKernel pick_ln(const LnKey& k) {
   return k.prefetch ? pick_shape<TX, TW, false, true>(k) : pick_shape<TX, TW, false, false>(k);
 }
 
-#if RMSN_PAIR == 0
-// Stage 2 of the weight gradients: dgamma_j = sum_b partial[b][j] and
-// dbeta_j = sum_b partial[b][ld_half + j] over the P stage-1 CTAs.  Each
-// thread sums one float4 column group over rows ty, ty + 32, ... in order;
-// the 32 row sums are then added in row order: the same bits every run.
-// Launched as a programmatic dependent of stage 1.
-__global__ void __launch_bounds__(kRedCols* kRedRows)
-    ln_reduce_kernel(const float* partial, int P, int N, int ld_half, float* dgamma,
-                     float* dbeta) {
-  pdl_begin();
-  __shared__ float4 sh[kRedRows][kRedCols];
-  const int tx = threadIdx.x % kRedCols, ty = threadIdx.x / kRedCols;
-  const int nq = ld_half / 4;                      // float4 groups per half
-  const int q = blockIdx.x * kRedCols + tx;      // in [0, 2 nq)
-  const bool second = q >= nq;
-  const int qh = second ? q - nq : q;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (q < 2 * nq) {
-    const float4* src = reinterpret_cast<const float4*>(partial) + q;
-    for (int b = ty; b < P; b += kRedRows) {
-      const float4 v = __ldcs(src + (size_t)b * 2 * nq);
-      s.x += v.x;
-      s.y += v.y;
-      s.z += v.z;
-      s.w += v.w;
-    }
-  }
-  sh[ty][tx] = s;
-  __syncthreads();
-  if (ty == 0 && q < 2 * nq) {
-    float4 t = sh[0][tx];
-    for (int r = 1; r < kRedRows; ++r) {
-      const float4 v = sh[r][tx];
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
-    }
-    float* out = second ? dbeta : dgamma;
-    const float tv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (qh * 4 + u < N && out != nullptr) out[qh * 4 + u] = tv[u];
-  }
-}
-#endif
 
 }  // namespace
 
 #if RMSN_PAIR == 0
-LnReduceKernel get_ln_reduce_kernel() { return ln_reduce_kernel; }
 LnKernel get_ln_kernel_f32_f32(const LnKey& k) { return pick_ln<float, float>(k); }
 #elif RMSN_PAIR == 1
 LnKernel get_ln_kernel_bf16_bf16(const LnKey& k) { return pick_ln<bf16, bf16>(k); }

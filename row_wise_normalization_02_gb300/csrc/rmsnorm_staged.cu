@@ -21,8 +21,8 @@
 // waits (bounded) for the copies it has in flight, then raises
 // kStatusWaitTimeout in p.status.
 //
-// Stage 2 of every backward family (the fixed-order column sum of the
-// dgamma partial rows) is built here too, once (RMSN_PAIR 0).
+// Stage 2 of every backward (the fixed-order column sum of the weight
+// gradients' partial rows, colsum_kernel) is built here too, once (RMSN_PAIR 0).
 #include "rmsnorm_ring.cuh"
 
 #ifndef RMSN_PAIR
@@ -286,63 +286,67 @@ BwdKernel staged_bwd(const BwdKey& k) {
 }
 
 #if RMSN_PAIR == 0
-// Stage 2 of the backward (every family): dgamma_j = sum_b partial[b][j] over the P stage-1 CTAs, in a fixed
-// order, written in fp32 or (out_bf16) rounded once to bf16.  The order:
-// thread (tx, ty) adds rows b = ty, ty + kRedRows, ... in sequence,
-// then the kRedRows chunk sums are added in ty order.  Loads are issued in
-// batches of 8 ahead of the adds (the order of the adds does not change).
-// Launched as a programmatic dependent of stage 1; griddepcontrol.wait
-// returns once stage 1 has completed and its writes are visible.
-__global__ void __launch_bounds__(kRedCols* kRedRows)
-    dgamma_reduce_kernel(const float* partial, int P, int N, int ld, void* dgamma, int out_bf16) {
+// Stage 2 of every backward: out_j = sum_b partial[b][j] over the P stage-1
+// CTAs, in a fixed order, fp32 (or rounded once to bf16).  A CTA owns C
+// float4 columns; its R = 256 / C row lanes each add the rows b = lane,
+// lane + R, ... in sequence (loads issued four ahead; the order of the adds
+// does not change), then the R lane sums meet in a fixed binary tree in
+// shared memory.  C is chosen per call so that the grid covers the GPU even
+// for short rows.  Launched as a programmatic dependent of stage 1:
+// griddepcontrol.wait returns once stage 1 has completed and its writes are
+// visible.
+__device__ __forceinline__ void add4(float4& s, const float4& v) {
+  s.x += v.x;
+  s.y += v.y;
+  s.z += v.z;
+  s.w += v.w;
+}
+
+template <int C>
+__global__ void __launch_bounds__(kColSumThreads)
+    colsum_kernel(const float* partial, int P, int nq, ColSumOut o) {
   pdl_begin();
-  __shared__ float4 sh[kRedRows][kRedCols];
-  const int tx = threadIdx.x % kRedCols, ty = threadIdx.x / kRedCols;
-  const int q = blockIdx.x * kRedCols + tx;       // float4 column group
-  const int nq = ld / 4;
+  constexpr int R = kColSumThreads / C;
+  __shared__ float4 sh[R][C];
+  const int tx = threadIdx.x % C, ty = threadIdx.x / C;
+  const int q = blockIdx.x * C + tx;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (q < nq) {
     const float4* src = reinterpret_cast<const float4*>(partial) + q;
     int b = ty;
-    constexpr int B = 8;
-    for (; b + (B - 1) * kRedRows < P; b += B * kRedRows) {
+    constexpr int B = 4;
+    for (; b + (B - 1) * R < P; b += B * R) {
       float4 v[B];
 #pragma unroll
-      for (int u = 0; u < B; ++u) v[u] = __ldcs(src + (size_t)(b + u * kRedRows) * nq);
+      for (int u = 0; u < B; ++u) v[u] = __ldcs(src + (size_t)(b + u * R) * nq);
 #pragma unroll
-      for (int u = 0; u < B; ++u) {
-        s.x += v[u].x;
-        s.y += v[u].y;
-        s.z += v[u].z;
-        s.w += v[u].w;
-      }
+      for (int u = 0; u < B; ++u) add4(s, v[u]);
     }
-    for (; b < P; b += kRedRows) {
-      const float4 v = __ldcs(src + (size_t)b * nq);
-      s.x += v.x;
-      s.y += v.y;
-      s.z += v.z;
-      s.w += v.w;
-    }
+    for (; b < P; b += R) add4(s, __ldcs(src + (size_t)b * nq));
   }
   sh[ty][tx] = s;
   __syncthreads();
-  if (ty == 0 && q < nq) {
-    float4 t = sh[0][tx];
-    for (int r = 1; r < kRedRows; ++r) {
-      const float4 v = sh[r][tx];
-      t.x += v.x;
-      t.y += v.y;
-      t.z += v.z;
-      t.w += v.w;
+#pragma unroll
+  for (int h = R / 2; h > 0; h >>= 1) {
+    if (ty < h) {
+      float4 t = sh[ty][tx];
+      add4(t, sh[ty + h][tx]);
+      sh[ty][tx] = t;
     }
-    const int j = q * 4;
+    __syncthreads();
+  }
+  if (ty == 0 && q < nq) {
+    const float4 t = sh[0][tx];
+    const bool second = q >= o.half_q;
+    const int j = (second ? q - o.half_q : q) * 4;
+    void* out = second ? o.out1 : o.out0;
+    if (out == nullptr) return;
     const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      if (j + u < N) {
-        if (out_bf16) static_cast<bf16*>(dgamma)[j + u] = __float2bfloat16_rn(tv[u]);
-        else static_cast<float*>(dgamma)[j + u] = tv[u];
+      if (j + u < o.N) {
+        if (o.bf16 && !second) static_cast<bf16*>(out)[j + u] = __float2bfloat16_rn(tv[u]);
+        else static_cast<float*>(out)[j + u] = tv[u];
       }
     }
   }
@@ -352,7 +356,14 @@ __global__ void __launch_bounds__(kRedCols* kRedRows)
 }  // namespace
 
 #if RMSN_PAIR == 0
-ReduceKernel get_dgamma_reduce_kernel() { return dgamma_reduce_kernel; }
+ColSumKernel get_colsum_kernel(int c) {
+  switch (c) {
+    case 2: return colsum_kernel<2>;
+    case 4: return colsum_kernel<4>;
+    case 8: return colsum_kernel<8>;
+    default: return nullptr;
+  }
+}
 FwdKernel get_fwd_staged_f32_f32(const FwdKey& k) { return staged_fwd<float, float>(k); }
 BwdKernel get_bwd_staged_f32_f32(const BwdKey& k) { return staged_bwd<float, float>(k); }
 #elif RMSN_PAIR == 1

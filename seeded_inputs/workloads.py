@@ -124,3 +124,12 @@ for _m, _n in _SWEEP:
         _name = f"sweep_{_op}_bf16_m{_m}_n{_n}"
         WORKLOADS[_name] = Workload(_name, _op, _m, _n, "bf16", "bf16", 1e-6, 4,
                                     tags=("sweep",))
+# rows longer than one CTA holds (65536 bf16: 128 KiB per row), forward and
+# backward, and the fused-add backward at 32768 (64 KiB rows of three operands)
+for _op in ("fwd", "bwd"):
+    _name = f"long_{_op}_bf16_m2048_n65536"
+    WORKLOADS[_name] = Workload(_name, _op, 2048, 65536, "bf16", "bf16", 1e-6, 8,
+                                tags=("sweep",))
+WORKLOADS["fadd_bwd_bf16_m8192_n32768"] = Workload("fadd_bwd_bf16_m8192_n32768", "fused_add_bwd",
+                                                   8192, 32768, "bf16", "bf16", 1e-6, 9,
+                                                   tags=("next",))

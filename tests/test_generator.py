@@ -73,8 +73,8 @@ def test_workload_recipes():
     bwd = si.make_inputs(WORKLOADS["bwd_bf16_m16384_n8192"], rows=4)
     assert bwd["gamma"].dtype == np.float32 and bwd["dy"].dtype == np.uint16
     sweep = [w for w in WORKLOADS.values() if "sweep" in w.tags]
-    # fwd and bwd at six bf16 sizes, and at one fp32 size
-    assert len(sweep) == 14
+    # fwd and bwd at six bf16 sizes, one long-row bf16 size and one fp32 size
+    assert len(sweep) == 16
     assert sorted({(w.x_dtype, w.w_dtype) for w in sweep}) == [("bf16", "bf16"), ("f32", "f32")]
     assert sum(w.x_dtype == "f32" for w in sweep) == 2
 

@@ -57,7 +57,7 @@ def check_fused(x, r, g, eps, xd, wd, out, want_rstd=False):
 N_BF16 = [8, 16, 24, 40, 128, 256, 512, 768, 1024,          # short rows, packed
           1032, 2048, 4096, 5120, 7168, 8192, 16384, 32768,  # one row per CTA
           1, 2, 7, 9, 127, 129, 255, 1023, 1025, 2049, 4095,  # ragged
-          40000]                                             # beyond the register tiers
+          40000]                                             # clusters of CTAs
 N_F32 = [4, 12, 128, 512, 1024, 4096, 8192, 16384, 1, 3, 5, 1023, 2049, 40000]
 
 
@@ -211,6 +211,10 @@ def test_plan_families():
     assert "/cta/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16384, 8192, "bf16", "bf16")
     assert "/cta/" in rn.rmsnorm_describe_plan(rn.OP_FUSED_ADD, 32768, 4096, "bf16", "bf16")
     assert "/ragged/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 4096, 2049, "bf16", "bf16")
-    assert "/generic/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 40000, "bf16", "bf16")
+    assert "/cluster/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 40000, "bf16", "bf16")
+    assert "/cluster/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 16, 40000, "bf16", "bf16")
+    assert "/cluster/" in rn.rmsnorm_describe_plan(rn.OP_FUSED_ADD_BWD, 16, 32768, "bf16", "bf16")
+    assert "/generic/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 40001, "bf16", "bf16")
+    assert "/generic/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 1 << 19, "bf16", "bf16")
     assert "/staged/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 16384, 8192, "bf16", "f32")
     assert "/subwarp/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 262144, 128, "bf16", "bf16")
