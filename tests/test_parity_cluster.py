@@ -115,7 +115,7 @@ def test_forward_forced_clusters_walk_many_rows(debug_env, force, N):
 
 
 @pytest.mark.parametrize("force,N", [
-    ("cluster:cl=2:cps=1", 40000), ("cluster:cl=4:cps=1", 40000), ("cluster:cl=8:cps=1", 40000),
+    ("cluster:cl=2:cps=1", 16392), ("cluster:cl=4:cps=1", 40000), ("cluster:cl=8:cps=1", 40000),
     ("cluster:cl=8:st=3:cps=1", 65536), ("cluster:cl=8:vpt=2:st=2:cps=1", 32776),
     ("cluster:cl=2:cps=1", 8192), ("cluster:cl=4:st=4:cps=1", 24576),
 ])
