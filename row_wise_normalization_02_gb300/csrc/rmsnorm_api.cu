@@ -531,8 +531,9 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
   // of the rows two steps ahead in their walk (4096 x 2049 bf16: bwd 0.372 ->
   // 0.385, fwd 0.546 -> 0.551; their few rows per CTA leave the pipeline's
   // fill and drain, not the bytes in flight, as the limit).
-  const bool l2_able = p.prefetch && ((bwd && p.family == kSubwarp) || p.family == kRagged);
-  if (l2_able) p.l2_ahead = 2;
+  const bool l2_able = p.prefetch && ((bwd && p.family == kSubwarp) || p.family == kRagged ||
+                                      (!bwd && p.family == kCluster));
+  if (l2_able) p.l2_ahead = p.family == kCluster ? 0 : 2;
   if (f.on && f.l2 >= 0) p.l2_ahead = f.l2;
   if (!l2_able) p.l2_ahead = 0;
 

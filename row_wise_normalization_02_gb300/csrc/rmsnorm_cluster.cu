@@ -9,10 +9,12 @@
 // "Pre-built kernel library guide" (section 1.1) and the LDS row cache of its
 // section 1.2 carried past the size of one CTA.  Where that guide combines
 // the per-wave partial sums of a row inside one workgroup, a cluster combines
-// the per-CTA sums through distributed shared memory: each CTA publishes its
-// sum in a shared-memory slot, the cluster meets at a hardware cluster
-// barrier, and every thread reads all C slots (mapa + ld.shared::cluster) in
-// rank order, so every CTA obtains the same, fixed-order total.
+// the per-CTA sums through distributed shared memory: thread 0 of each CTA
+// pushes its CTA's sum into a slot of every CTA of the cluster with st.async,
+// each push completing on the receiving CTA's mbarrier, and every thread adds
+// the C slots in rank order -- so every CTA obtains the same, fixed-order
+// total without a cluster-wide barrier per row (a release at a cluster
+// barrier would wait for every thread's outstanding global stores).
 //
 //   forward / fused add : the slice in registers, the next row's slice loaded
 //                         before the current row is reduced (as kCta)
@@ -21,13 +23,12 @@
 //                         registers, one partial row per cluster, each CTA
 //                         writing its slice's columns
 //
-// Slots alternate between two buffers from row to row: a CTA rewrites a slot
-// two rows later, after the next cluster barrier, which no CTA passes before
-// it has read the slot.  Before leaving, every CTA meets the others at one
-// more cluster barrier, so that no CTA's shared memory disappears while a
-// peer may still read it.  The bounded bulk-copy waits of the backward are
-// voted on across the whole cluster along with the sums, so all CTAs of a
-// cluster stop at the same row and every cluster barrier is met by all.
+// The cluster meets at a hardware cluster barrier twice: once after the
+// exchange barriers are initialised (no push may reach an uninitialised
+// barrier) and once before leaving (no CTA's shared memory may disappear
+// while a peer still pushes into it).  Every exchange wait is bounded; the
+// bounded bulk-copy waits of the backward travel with the sums as a vote, so
+// all CTAs of a cluster stop at the same row.
 #include "rmsnorm_fwd_common.cuh"
 #include "rmsnorm_ring.cuh"
 
@@ -50,40 +51,78 @@ __device__ __forceinline__ uint32_t cluster_ctas() {
 }
 // Every thread of every CTA of the cluster arrives (release: its earlier
 // shared-memory writes become visible to the cluster) and waits (acquire).
+// Used twice per kernel: after the exchange barriers are initialised, and
+// before leaving.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
-// The float at the same shared-memory offset as `p`, in the CTA of `rank`.
-__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+// The shared::cluster address of `local` (this CTA's shared memory) in the
+// CTA of `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
   uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(local)), "r"(rank));
+  return a;
+}
+// Asynchronous 16-byte store into a peer's shared memory, counted as 16
+// bytes of completed transactions on the peer's mbarrier.
+__device__ __forceinline__ void st_async_peer(uint32_t addr, const float4& v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
 }
 
-// Sum of K values over the cluster, plus a flag raised by any thread of any
-// CTA.  slot: 2 x (K + 1) floats of this CTA's shared memory.
-template <int K>
-__device__ __forceinline__ bool cluster_sum_vote(float (&v)[K], float* red, float* slot,
-                                                 int parity, bool flag, uint32_t C) {
-  const bool any = cta_sum_vote<K>(v, red, parity, flag);
-  float* my = slot + parity * (K + 1);
+// Per-row exchange of one float4 per CTA across the cluster, without a
+// cluster barrier: warp 0 pushes this CTA's value into slot[rank] of every
+// CTA (itself included) with st.async, each push completing on the receiving
+// CTA's mbarrier for this row's parity, which that CTA's thread 0 arms for C
+// pushes (a push may land before the arming: the barrier's transaction count
+// then runs below zero until it is armed).  Every thread waits (bounded) on its own barrier and adds the C
+// slots in rank order, so all CTAs obtain the same total.  Slots and barriers
+// alternate between rows: a CTA's slots of parity p are rewritten only by
+// pushes for the row after next, which its peers send only after they have
+// received this CTA's push for the next row -- sent after a CTA barrier that
+// follows this CTA's last read of those slots.
+struct Xchg {
+  uint64_t* bar;   // [2]
+  float4* slot;    // [2][8]
+};
+
+// Thread 0 initialises both barriers; the cluster then meets once, so that
+// no push reaches a barrier before it is initialised.
+__device__ __forceinline__ void xchg_init(const Xchg& x) {
   if (threadIdx.x == 0) {
-#pragma unroll
-    for (int k = 0; k < K; ++k) my[k] = v[k];
-    my[K] = any ? 1.f : 0.f;
+    mbar_init(x.bar, 1);
+    mbar_init(x.bar + 1, 1);
+    mbar_init_fence();
   }
   cluster_sync();
-  bool all = false;
+}
+
+// Exchange of row `it` of this CTA's walk; false if the wait gave up.  Lane r
+// (< C) of warp 0 pushes v, which must be the same in all those lanes, to the
+// CTA of rank r; out[k] receives the sum of component k (k < K).
+template <int K>
+__device__ __forceinline__ bool xchg_sum(const Xchg& x, const float4& v, int64_t it, uint32_t C,
+                                         uint32_t rank, long long limit, float (&out)[K]) {
+  const int p = (int)(it & 1);
+  if (threadIdx.x < C) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(x.bar + p, C * 16u);
+    // earlier generic reads of the slots (ordered before this by the CTA's
+    // reduction barrier) come before the peers' asynchronous writes
+    fence_proxy_async_smem();
+    st_async_peer(peer_addr(x.slot + p * 8 + rank, threadIdx.x), v,
+                  peer_addr(x.bar + p, threadIdx.x));
+  }
+  const bool ok = mbar_wait_bounded(x.bar + p, (uint32_t)((it >> 1) & 1), limit);
+  const float* sl = reinterpret_cast<const float*>(x.slot + p * 8);
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     float s = 0.f;
-    for (uint32_t r = 0; r < C; ++r) s += ld_cluster(my + k, r);
-    v[k] = s;
+    for (uint32_t r = 0; r < C; ++r) s += sl[r * 4 + k];
+    out[k] = s;
   }
-  for (uint32_t r = 0; r < C; ++r) all = all || ld_cluster(my + K, r) != 0.f;
-  return all;
+  return ok;
 }
 
 // Vectors [v0, v0 + nv) of a row are this CTA's slice.
@@ -105,8 +144,11 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cluster_kernel(const FwdPa
   using Cf = Cfg<TX, TW>;
   constexpr int E = Cf::E, GW = Cf::GW;
   __shared__ float red[2 * 32];
-  __shared__ float slot[2 * 2];
+  __shared__ __align__(16) float4 slots[2 * 8];
+  __shared__ __align__(8) uint64_t bars[2];
   const uint32_t C = cluster_ctas(), rank = cluster_rank();
+  const Xchg xc{bars, slots};
+  xchg_init(xc);
   const int tid = threadIdx.x, T = blockDim.x;
   const SliceOf sl = slice_of(p0.slice, p0.nvec, rank);
   // the parameters of this CTA's slice: operands shifted to its first vector
@@ -130,17 +172,33 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cluster_kernel(const FwdPa
   const int64_t first = blockIdx.x / C, stride = gridDim.x / C;
   const size_t rb = (size_t)p.N * sizeof(TX);
   int parity = 0;
+  bool failed = false;
   Slice<VPT, FUSED> cur, nxt;
   if (first < p.M) load_aligned<TX, VPT, FUSED>(cur, p, first, true, tid, T);
-  for (int64_t row = first; row < p.M; row += stride) {
+  int64_t it = 0;
+  for (int64_t row = first; row < p.M; row += stride, ++it) {
     const int64_t nrow = row + stride;
     if (PF && nrow < p.M) load_aligned<TX, VPT, FUSED>(nxt, p, nrow, true, tid, T);
+    // with the next row's slice in registers, the slice of the row l2_rows
+    // steps ahead is requested into L2 (no registers held for it)
+    if (PF && p.l2_rows > 0 && tid == 0 && sl.nv > 0) {
+      const int64_t ahead = row + (int64_t)p.l2_rows * stride;
+      if (ahead < p.M) {
+        bulk_prefetch_l2(static_cast<const char*>(p.x) + ahead * rb, (uint32_t)sl.nv * 16);
+        if (FUSED)
+          bulk_prefetch_l2(static_cast<const char*>(p.residual) + ahead * rb, (uint32_t)sl.nv * 16);
+      }
+    }
     char* yrow = static_cast<char*>(p.y) + row * rb;
     char* hrow = static_cast<char*>(p.residual) + row * rb;
     float ss[1];
     ss[0] = slice_sumsq<TX, VPT, FUSED>(cur, hrow, tid, T, sl.nv, true);
-    cluster_sum_vote<1>(ss, red, slot, parity, false, C);
+    cta_sum<1>(ss, red, parity);
     parity ^= 1;
+    if (!xchg_sum<1>(xc, make_float4(ss[0], 0.f, 0.f, 0.f), it, C, rank, p.wait_limit, ss)) {
+      failed = true;   // a peer stopped answering: leave (it cannot happen while peers run)
+      break;
+    }
     const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
     if (rank == 0 && tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
 #pragma unroll
@@ -151,6 +209,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cluster_kernel(const FwdPa
     if (PF) cur = nxt;
     else if (nrow < p.M) load_aligned<TX, VPT, FUSED>(cur, p, nrow, true, tid, T);
   }
+  if (failed && tid == 0) atomicOr(p.status, kStatusWaitTimeout);
   cluster_sync();
 }
 
@@ -181,7 +240,9 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
   constexpr int NS = DRES ? 3 : 2;
   extern __shared__ __align__(128) unsigned char smem[];
   const Ring rg = ring_of(smem);
-  float* slot = reinterpret_cast<float*>(smem + 640);   // in the header, after rg.red
+  // exchange barriers and slots in the header, after the ring's barriers and
+  // reduction slots
+  const Xchg xc{reinterpret_cast<uint64_t*>(smem + 640), reinterpret_cast<float4*>(smem + 768)};
   const uint32_t C = cluster_ctas(), rank = cluster_rank();
   const int tid = threadIdx.x, T = blockDim.x, S = p.stages;
   const SliceOf sl = slice_of(p.slice, p.nvec, rank);
@@ -200,7 +261,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
     for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
     mbar_init_fence();
   }
-  __syncthreads();
+  xchg_init(xc);   // also orders the ring's barrier initialisation before use
   if (tid == 0) {
     const int64_t n0 = nrows < S ? nrows : S;
     for (; issued < n0; ++issued) issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
@@ -250,11 +311,20 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
         }
       }
     }
-    if (cluster_sum_vote<K>(sums, rg.red, slot, parity, late, C)) {
+    // the CTA's sums and its vote, then the cluster's: every CTA of the
+    // cluster sees the same sums and the same verdict on the waits
+    const bool any_late = cta_sum_vote<K>(sums, rg.red, parity, late);
+    parity ^= 1;
+    float tot[3];
+    const bool answered = xchg_sum<3>(xc, make_float4(sums[0], K > 1 ? sums[K - 1] : 0.f,
+                                                      any_late ? 1.f : 0.f, 0.f),
+                                      i, C, rank, p.wait_limit, tot);
+    if (!answered || tot[2] != 0.f) {
       failed = true;
       break;
     }
-    parity ^= 1;
+    sums[0] = tot[0];
+    if (K > 1) sums[K - 1] = tot[1];
     if (!DRES && tid == 0 && issued < nrows) {
       fence_proxy_async_smem();
       issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
