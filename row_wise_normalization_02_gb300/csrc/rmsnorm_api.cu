@@ -281,15 +281,16 @@ bool cta_shape(int op, int nvec, int* vpt, int* threads) {
 }
 
 // Cluster shape for a row of nvec vectors: the fewest CTAs (2, 4 or 8) whose
-// slices hold at most 1024 vectors (4 per thread in 256-thread CTAs, the
-// best forward shape of one CTA per row), else 8 CTAs with up to 2048
-// vectors each (4 per thread, 512 threads) -- or, forward only, 4096 (8 per
-// thread, no next-row prefetch).  cl > 0 fixes the cluster size.  False when
-// the row is too long.
+// slices hold at most 2048 vectors (4 per thread, up to 512 threads) -- fewer
+// CTAs per row exchange less and pack better into the GPCs (2048 x 65536
+// bf16: forward 0.91 of the copy peak with 4 CTAs of 2048 vectors against
+// 0.86 with 8 of 1024; backward 0.77 against 0.52) -- or, forward only, 8
+// CTAs with up to 4096 vectors (8 per thread, no next-row prefetch).  cl > 0
+// fixes the cluster size.  False when the row is too long.
 bool cluster_shape(bool bwd, int nvec, int cl, int* c_out, int* slice, int* vpt, int* threads) {
   int c = cl;
   if (c <= 0)
-    for (c = 2; c < 8 && (nvec + c - 1) / c > 1024; c *= 2) {
+    for (c = 2; c < 8 && (nvec + c - 1) / c > 2048; c *= 2) {
     }
   if (c < 1 || c > 8) return false;
   const int sl = (nvec + c - 1) / c;
@@ -533,7 +534,9 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
   // fill and drain, not the bytes in flight, as the limit).
   const bool l2_able = p.prefetch && ((bwd && p.family == kSubwarp) || p.family == kRagged ||
                                       (!bwd && p.family == kCluster));
-  if (l2_able) p.l2_ahead = p.family == kCluster ? 0 : 2;
+  // cluster forward: the slice of the row two steps ahead (2048 x 65536 bf16:
+  // 0.77 -> 0.91 of the copy peak)
+  if (l2_able) p.l2_ahead = 2;
   if (f.on && f.l2 >= 0) p.l2_ahead = f.l2;
   if (!l2_able) p.l2_ahead = 0;
 

@@ -315,6 +315,13 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
     // cluster sees the same sums and the same verdict on the waits
     const bool any_late = cta_sum_vote<K>(sums, rg.red, parity, late);
     parity ^= 1;
+    // every thread has read this stage: refill it before the exchange, so
+    // the copy overlaps it (if the cluster then stops, the copy is drained)
+    if (!DRES && !any_late && tid == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
+      ++issued;
+    }
     float tot[3];
     const bool answered = xchg_sum<3>(xc, make_float4(sums[0], K > 1 ? sums[K - 1] : 0.f,
                                                       any_late ? 1.f : 0.f, 0.f),
@@ -325,11 +332,6 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
     }
     sums[0] = tot[0];
     if (K > 1) sums[K - 1] = tot[1];
-    if (!DRES && tid == 0 && issued < nrows) {
-      fence_proxy_async_smem();
-      issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
-      ++issued;
-    }
     const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
     const float c = r * r * p.inv_n * sums[0];
     char* dxrow = dxs + row * rb;
