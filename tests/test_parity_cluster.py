@@ -32,8 +32,9 @@ def plan(op, M, N, xd, wd):
     return rn.rmsnorm_describe_plan(op, M, N, xd, wd)
 
 
-# bf16 row lengths: forward clusters from 4097 vectors on (N > 32768), the
-# backward from 2049 (N > 16384); fp32 rows hold half as many elements
+# bf16 row lengths: the fused add on clusters from 4097 vectors on
+# (N > 32768), the forward and the backward from 2049 (N > 16384); fp32 rows
+# hold half as many elements
 N_FWD = {"bf16": [32776, 40000, 65536, 131072, 262144], "f32": [16388, 40000, 65536]}
 N_BWD = {"bf16": [16392, 20000, 24576, 40000, 65536, 131072], "f32": [8196, 40000, 65536]}
 
@@ -87,7 +88,7 @@ def test_fused_add_backward(xd, wd, N, dg):
 
 
 @pytest.mark.parametrize("M", [1, 2, 3])
-@pytest.mark.parametrize("N", [40000, 65536])
+@pytest.mark.parametrize("N", [24576, 40000, 65536])
 def test_one_to_three_rows(M, N):
     x, g = make(M, N, "bf16", "bf16", seed=M + N)
     check_fwd(x, g, EPS, "bf16", "bf16", pu.run_fwd(x, g, EPS, "bf16", "bf16"))
