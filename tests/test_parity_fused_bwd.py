@@ -60,10 +60,19 @@ def check(h, dy, dres, g, rstd, eps, xd, wd, out, dg_dtype="f32"):
         pu.check_dgamma(out["dgamma"], ref["dgamma64"], aux["dgamma_sq64"])
     else:
         # rounded once to bf16 from the fp32 sum: within 1 ulp of the oracle's
-        # rounding of the exact sum unless that sum sits within the fp32
-        # error of a bf16 tie
+        # rounding of the exact sum, unless that sum sits within the fp32
+        # error of a bf16 tie or cancels -- then within the fp32 sum's bound
+        # (1e-4 of max(|sum|, sqrt(sum of squared terms))) plus one bf16 ulp
         d = pu.bf16_ulp_dist(out["dgamma"], ref["dgamma_w"])
-        assert (d <= 1).all(), int(d.max())
+        far = d > 1
+        if far.any():
+            from oracle import bf16_array_to_f64
+            gv = bf16_array_to_f64(out["dgamma"])
+            ex = ref["dgamma64"]
+            scale = np.maximum(np.abs(ex), np.sqrt(aux["dgamma_sq64"]))
+            ok = np.abs(gv - ex) <= 1e-4 * scale + pu.bf16_ulp_of(ex)
+            assert (ok | ~far).all(), (f"dgamma (bf16): {int((far & ~ok).sum())} columns beyond "
+                                       f"1 ulp and the sum's bound, max {int(d.max())} ulp")
     return {"floor": n_floor}
 
 
