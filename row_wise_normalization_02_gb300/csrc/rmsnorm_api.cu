@@ -82,7 +82,7 @@ BwdKernel bwd_kernel(const BwdKey& k) {
     if (k.xd == kBF16 && k.wd == kF32) return get_bwd_cluster_bf16_f32(k);
     return nullptr;
   }
-  const bool st = k.family == kStaged;
+  const bool st = k.family == kStaged && k.g == 0;   // staged short rows live with the others
   if (k.xd == kF32 && k.wd == kF32) return st ? get_bwd_staged_f32_f32(k) : get_bwd_kernel_f32_f32(k);
   if (k.xd == kBF16 && k.wd == kBF16)
     return st ? get_bwd_staged_bf16_bf16(k) : get_bwd_kernel_bf16_bf16(k);
@@ -493,8 +493,18 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       }
       if ((int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
       p.period = ragged_period((int64_t)N * esize(xd));
+    } else if (p.family == kStaged && bwd && f.g > 0) {
+      // short backward rows through the ring: g lanes per row, 256 / g rows
+      // per CTA iteration
+      if (!f.vpt) p.vpt = (nvec + p.g - 1) / p.g;
+      if (!rows_aligned || p.g > 32 || (int64_t)p.g * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
+      p.threads = kSubwarpThreads;
+      p.rows_per_cta = kSubwarpThreads / p.g;
+      p.prefetch = false;
+      p.stages = f.st;
     } else if (p.family == kStaged) {
       if (!rows_aligned) return RMSNORM_ERR_INVALID_ARG;
+      p.g = 0;
       if (!p.vpt) p.vpt = 4;
       if (!f.threads) p.threads = round_up((nvec + p.vpt - 1) / p.vpt, 32);
       if ((int64_t)p.threads * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
@@ -522,7 +532,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
     }
     if (p.family != kCluster) p.cluster = p.slice = 0;
-    if (p.family != kSubwarp) p.rows_per_cta = 1;
+    if (p.family != kSubwarp && !(p.family == kStaged && p.g > 0)) p.rows_per_cta = 1;
     if (p.family != kRagged) p.period = 1;
     if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32) return RMSNORM_ERR_INVALID_ARG;
   }
@@ -548,7 +558,9 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     // ring of row buffers: as many stages as fit a half-SM budget (two CTAs
     // per SM), at least two, at most kStagedMaxStages
     const int ns = op == kFwd ? 1 : (op == kFusedBwd ? 3 : 2);
-    const int64_t stage_bytes = (int64_t)ns * N * esize(xd);
+    // a stage holds one row per operand, or the rows_per_cta rows of a CTA
+    // iteration of short rows
+    const int64_t stage_bytes = (int64_t)ns * N * esize(xd) * (p.g > 0 ? p.rows_per_cta : 1);
     if (p.stages <= 0) {
       int64_t st = (kStagedSmemBudget - kStagedHeader) / stage_bytes;
       if (st < 2) st = (kStagedSmemMax - kStagedHeader) / stage_bytes;
@@ -558,7 +570,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
         kStagedHeader + p.stages * stage_bytes > kStagedSmemMax)
       return RMSNORM_ERR_INVALID_ARG;
     p.smem = (int)(kStagedHeader + p.stages * stage_bytes);
-    p.rows_per_cta = 1;
+    if (p.g == 0) p.rows_per_cta = 1;
   }
   if (bwd) {
     // each CTA writes one dgamma partial row (N fp32); keep that traffic to a

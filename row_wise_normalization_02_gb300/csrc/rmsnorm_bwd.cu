@@ -13,14 +13,15 @@
 // library reduces dgamma in a fixed order so the result is bit-for-bit
 // reproducible: stage 1 runs a persistent grid of P CTAs with a fixed
 // row -> CTA map, each CTA accumulating its rows' dy*x*r per column in fp32
-// and writing one partial row; stage 2 (dgamma_reduce_kernel, built with the
-// staged kernels) sums the P partial rows per column in a fixed order.  Like every kernel here, stage 2 is a programmatic dependent
-// launch: its launch overlaps stage 1, and it waits for stage 1 to complete
-// before reading the partial rows.
+// and writing one partial row; stage 2 (colsum_kernel, built with the staged
+// kernels) sums the P partial rows per column in a fixed order.  Like every
+// kernel here, stage 2 is a programmatic dependent launch: its launch
+// overlaps stage 1, and it waits for stage 1 to complete before reading the
+// partial rows.
 #include <type_traits>
 
-#include "rmsnorm_device.cuh"
-#include "rmsnorm_internal.h"
+#include "rmsnorm_bwd_common.cuh"
+#include "rmsnorm_ring.cuh"
 
 #ifndef RMSN_PAIR
 #error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
@@ -28,68 +29,6 @@
 
 namespace rmsn {
 namespace {
-
-template <typename TW, int E>
-__device__ __forceinline__ void load_gamma_vec(const void* gamma, int v, float (&g)[E]) {
-  constexpr int GW = E * (int)sizeof(TW) / 16;
-  const char* gp = static_cast<const char*>(gamma) + (size_t)v * GW * 16;
-  if constexpr (std::is_same<TW, float>::value) {
-#pragma unroll
-    for (int w = 0; w < GW; ++w) {
-      float t[4];
-      unpack(ld_cached(gp + w * 16), t);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) g[w * 4 + i] = t[i];
-    }
-  } else {
-    unpack(ld_cached(gp), g);
-  }
-}
-
-// Per-vector work of the register backward kernels with the paired fp32
-// instructions.  Row sums: dot += sum g dy x over even / odd elements in two
-// lanes (and ss += sum x^2 when the rstd is recomputed).
-template <int E, bool SS>
-__device__ __forceinline__ void bwd_vec_sums(const uint4& xv, const uint4& dv,
-                                             const float (&g)[E], float2& dot, float2& ss) {
-  float xf[E], df[E];
-  unpack(xv, xf);
-  unpack(dv, df);
-#pragma unroll
-  for (int i = 0; i < E / 2; ++i) {
-    const float2 x2 = make_float2(xf[2 * i], xf[2 * i + 1]);
-    const float2 gd = __fmul2_rn(make_float2(g[2 * i], g[2 * i + 1]),
-                                 make_float2(df[2 * i], df[2 * i + 1]));
-    dot = __ffma2_rn(gd, x2, dot);
-    if (SS) ss = __ffma2_rn(x2, x2, ss);
-  }
-}
-// dx = r (g dy - x c) (+ dres) and acc += dy x r, element by element with the
-// same operations as the scalar form, two at a time.
-template <int E, bool DRES>
-__device__ __forceinline__ uint4 bwd_vec_apply(const uint4& xv, const uint4& dv,
-                                               const uint4& rv, const float (&g)[E], float r,
-                                               float c, float (&acc)[E]) {
-  float xf[E], df[E], rf[E], o[E];
-  unpack(xv, xf);
-  unpack(dv, df);
-  if (DRES) unpack(rv, rf);
-  const float2 r2 = make_float2(r, r), nc = make_float2(-c, -c);
-#pragma unroll
-  for (int i = 0; i < E / 2; ++i) {
-    const float2 x2 = make_float2(xf[2 * i], xf[2 * i + 1]);
-    const float2 d2 = make_float2(df[2 * i], df[2 * i + 1]);
-    const float2 gd = __fmul2_rn(make_float2(g[2 * i], g[2 * i + 1]), d2);
-    float2 t = __fmul2_rn(__ffma2_rn(x2, nc, gd), r2);
-    if (DRES) t = __fadd2_rn(t, make_float2(rf[2 * i], rf[2 * i + 1]));
-    const float2 a = __ffma2_rn(__fmul2_rn(d2, x2), r2, make_float2(acc[2 * i], acc[2 * i + 1]));
-    o[2 * i] = t.x;
-    o[2 * i + 1] = t.y;
-    acc[2 * i] = a.x;
-    acc[2 * i + 1] = a.y;
-  }
-  return pack(o);
-}
 
 template <int VPT, bool DRES = false>
 struct BSlice {
@@ -230,6 +169,166 @@ __global__ void __launch_bounds__(kSubwarpThreads) bwd_subwarp_kernel(const BwdP
 template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF, bool DRES>
 __global__ void __launch_bounds__(kSubwarpThreads, 2) bwd_subwarp_kernel_2cta(const BwdParams p) {
   bwd_subwarp_body<TX, TW, G, VPT, HAS_RSTD, PF, DRES>(p);
+}
+
+// ---------------------------------------------------------------------------
+// Short rows through a bulk-copy ring (kStaged with G lanes per row): a CTA
+// iteration covers RPC = 256 / G consecutive rows, which are contiguous in
+// memory, so one cp.async.bulk per operand fills a stage of the ring; the
+// CTA keeps stages - 1 iterations of rows in flight without holding them in
+// registers.  The row math is the sub-warp kernel's (paired fp32, shuffle
+// reduction within the G lanes of a row); gamma and the dgamma partials stay
+// in registers.  One CTA barrier per iteration both votes on the bounded
+// waits (so the whole CTA agrees to stop) and proves that every thread has
+// finished the previous iteration's stage, which thread 0 then refills.
+template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool DRES>
+__global__ void __launch_bounds__(kSubwarpThreads)
+    bwd_rows_staged_kernel(const BwdParams p) {
+  pdl_begin();
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int RPC = kSubwarpThreads / G;
+  constexpr int NS = DRES ? 3 : 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Ring rg = ring_of(smem);
+  const int lane = threadIdx.x % G, grp = threadIdx.x / G, tid = threadIdx.x;
+  const int S = p.stages;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  const size_t blk = (size_t)RPC * rb;              // one operand's rows of a stage
+  const int64_t units = (p.M + RPC - 1) / RPC;      // CTA iterations of RPC rows
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t nit = first < units ? (units - 1 - first) / stride + 1 : 0;
+  const char* src[3] = {static_cast<const char*>(p.x), static_cast<const char*>(p.dy),
+                        static_cast<const char*>(p.dres)};
+
+  // thread 0: the rows of iteration j into stage j mod S (the last unit may
+  // hold fewer than RPC rows)
+  auto issue = [&](int64_t j) {
+    const int s = (int)(j % S);
+    const int64_t row0 = (first + j * stride) * RPC;
+    const int64_t n = p.M - row0 < RPC ? p.M - row0 : RPC;
+    const uint32_t bytes = (uint32_t)(n * (int64_t)rb);
+    uint64_t* bar = rg.full + s;
+    unsigned char* dst = rg.buf + (size_t)s * NS * blk;
+    mbar_arrive_expect_tx(bar, NS * bytes);
+#pragma unroll
+    for (int q = 0; q < NS; ++q) bulk_copy_g2s(dst + q * blk, src[q] + row0 * rb, bytes, bar);
+  };
+  int64_t issued = 0;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (; issued < (nit < S ? nit : S); ++issued) issue(issued);
+
+  float g[VPT][E], acc[VPT][E];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+    if (v < p.nvec) load_gamma_vec<TW, E>(p.gamma, v, g[k]);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) g[k][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+  }
+
+  // the saved rstd of this thread's row, one iteration ahead in a register
+  float r_next = 0.f;
+  if (HAS_RSTD && nit > 0) {
+    const int64_t row = first * RPC + grp;
+    r_next = row < p.M ? __ldg(p.rstd + row) : 0.f;
+  }
+  int64_t j = 0;
+  bool failed = false;
+  for (; j < nit; ++j) {
+    const int s = (int)(j % S);
+    const int64_t row = (first + j * stride) * RPC + grp;
+    const bool valid = row < p.M;
+    const float r_saved = r_next;
+    if (HAS_RSTD && j + 1 < nit) {
+      const int64_t nrow = (first + (j + 1) * stride) * RPC + grp;
+      r_next = nrow < p.M ? __ldg(p.rstd + nrow) : 0.f;
+    }
+    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((j / S) & 1), p.wait_limit);
+    if (__syncthreads_or(late ? 1 : 0)) {
+      failed = true;
+      break;
+    }
+    // every thread is done with the previous iteration's stage: refill it
+    if (tid == 0 && j > 0 && issued < nit) {
+      fence_proxy_async_smem();
+      issue(issued);
+      ++issued;
+    }
+    const unsigned char* st = rg.buf + (size_t)s * NS * blk + (size_t)grp * rb;
+    const uint4* xs = reinterpret_cast<const uint4*>(st);
+    const uint4* ds = reinterpret_cast<const uint4*>(st + blk);
+    const uint4* rs = reinterpret_cast<const uint4*>(st + 2 * blk);
+    float2 dot2 = make_float2(0.f, 0.f), ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * G;
+      const bool in = valid && v < p.nvec;
+      const uint4 xv = in ? xs[v] : make_uint4(0, 0, 0, 0);
+      const uint4 dv = in ? ds[v] : make_uint4(0, 0, 0, 0);
+      bwd_vec_sums<E, !HAS_RSTD>(xv, dv, g[k], dot2, ss2);
+    }
+    const float dot = group_sum<G>(dot2.x + dot2.y);
+    float r;
+    if constexpr (HAS_RSTD) {
+      r = r_saved;
+    } else {
+      const float ss = group_sum<G>(ss2.x + ss2.y);
+      r = rsqrtf(fmaf(ss, p.inv_n, p.eps));
+    }
+    const float c = r * r * p.inv_n * dot;
+    char* dxr = static_cast<char*>(p.dx) + row * rb;
+    // the vectors are read again from the stage (not held in registers
+    // across the reduction: that would cost resident CTAs)
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + k * G;
+      const bool in = valid && v < p.nvec;
+      const uint4 xv = in ? ld_shared_v4(xs + v) : make_uint4(0, 0, 0, 0);
+      const uint4 dv = in ? ld_shared_v4(ds + v) : make_uint4(0, 0, 0, 0);
+      const uint4 rv = (DRES && in) ? ld_shared_v4(rs + v) : make_uint4(0, 0, 0, 0);
+      const uint4 o = bwd_vec_apply<E, DRES>(xv, dv, rv, g[k], r, c, acc[k]);
+      if (in) st_stream(dxr + (size_t)v * 16, o);
+    }
+  }
+  if (failed) {
+    if (tid == 0) {
+      drain(rg, j, issued, S);
+      atomicOr(p.status, kStatusWaitTimeout);
+    }
+    return;
+  }
+  if (p.partial == nullptr) return;
+  // the row groups' partial rows meet in shared memory (the ring is free:
+  // every copy has been consumed), added in group order
+  __syncthreads();
+  float* sacc = reinterpret_cast<float*>(rg.buf);
+  const int ncol = p.nvec * E;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+    if (v < p.nvec) {
+      float4* d = reinterpret_cast<float4*>(sacc + grp * ncol + v * E);
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q)
+        d[q] = make_float4(acc[k][4 * q], acc[k][4 * q + 1], acc[k][4 * q + 2],
+                           acc[k][4 * q + 3]);
+    }
+  }
+  __syncthreads();
+  float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
+  for (int c = tid; c < ncol; c += kSubwarpThreads) {
+    float t = 0.f;
+    for (int q = 0; q < RPC; ++q) t += sacc[q * ncol + c];
+    prow[c] = t;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -395,6 +494,16 @@ BwdKernel pick_subwarp(int g, int vpt, bool pf) {
   return nullptr;
 }
 
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
+BwdKernel pick_rows_staged(int g, int vpt) {
+#define RMSN_RS(G_, V_) \
+  if (g == G_ && vpt == V_) return bwd_rows_staged_kernel<TX, TW, G_, V_, HAS_RSTD, DRES>;
+  RMSN_RS(4, 1) RMSN_RS(8, 1) RMSN_RS(16, 1) RMSN_RS(32, 1)
+  RMSN_RS(8, 2) RMSN_RS(16, 2) RMSN_RS(32, 2) RMSN_RS(32, 3) RMSN_RS(32, 4)
+#undef RMSN_RS
+  return nullptr;
+}
+
 template <typename TX, typename TW, bool HAS_RSTD, bool ACC_SMEM>
 BwdKernel pick_cta(int vpt, bool pf) {
   switch (vpt) {
@@ -411,6 +520,9 @@ BwdKernel pick_cta(int vpt, bool pf) {
 
 template <typename TX, typename TW, bool HAS_RSTD>
 BwdKernel pick_family(const BwdKey& k) {
+  if (k.family == kStaged && k.g > 0)   // short rows through the bulk-copy ring
+    return k.dres ? pick_rows_staged<TX, TW, HAS_RSTD, true>(k.g, k.vpt)
+                  : pick_rows_staged<TX, TW, HAS_RSTD, false>(k.g, k.vpt);
   if (k.dres) {   // fused-add backward: subwarp rows or the generic kernel
     switch (k.family) {
       case kSubwarp: return pick_subwarp<TX, TW, HAS_RSTD, true>(k.g, k.vpt, k.prefetch);

@@ -29,6 +29,7 @@
 // while a peer still pushes into it).  Every exchange wait is bounded; the
 // bounded bulk-copy waits of the backward travel with the sums as a vote, so
 // all CTAs of a cluster stop at the same row.
+#include "rmsnorm_bwd_common.cuh"
 #include "rmsnorm_fwd_common.cuh"
 #include "rmsnorm_ring.cuh"
 
@@ -289,28 +290,17 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
     const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
     const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
     const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * NS * sb);
-    uint4 xv[VPT], dv[VPT];
-    float sums[K];
-#pragma unroll
-    for (int q = 0; q < K; ++q) sums[q] = 0.f;
+    float2 dot2 = make_float2(0.f, 0.f), ss2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
-      xv[k] = make_uint4(0, 0, 0, 0);
-      dv[k] = make_uint4(0, 0, 0, 0);
-      if (v < sl.nv) {
-        xv[k] = st[v];
-        dv[k] = st[sl.nv + v];
-        float xf[E], df[E];
-        unpack(xv[k], xf);
-        unpack(dv[k], df);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          sums[0] = fmaf(g[k][e] * df[e], xf[e], sums[0]);
-          if (!HAS_RSTD) sums[K - 1] = fmaf(xf[e], xf[e], sums[K - 1]);
-        }
-      }
+      const uint4 xv = v < sl.nv ? st[v] : make_uint4(0, 0, 0, 0);
+      const uint4 dv = v < sl.nv ? st[sl.nv + v] : make_uint4(0, 0, 0, 0);
+      bwd_vec_sums<E, !HAS_RSTD>(xv, dv, g[k], dot2, ss2);
     }
+    float sums[K];
+    sums[0] = dot2.x + dot2.y;
+    if (K > 1) sums[K - 1] = ss2.x + ss2.y;
     // the CTA's sums and its vote, then the cluster's: every CTA of the
     // cluster sees the same sums and the same verdict on the waits
     const bool any_late = cta_sum_vote<K>(sums, rg.red, parity, late);
@@ -335,21 +325,15 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
     const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
     const float c = r * r * p.inv_n * sums[0];
     char* dxrow = dxs + row * rb;
+    // the vectors are read again from the stage rather than held across the
+    // exchange (registers are what limits this kernel to one CTA per SM)
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
       if (v < sl.nv) {
-        float xf[E], df[E], o[E], rf[E];
-        unpack(xv[k], xf);
-        unpack(dv[k], df);
-        if (DRES) unpack(st[2 * sl.nv + v], rf);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
-          if (DRES) o[e] += rf[e];
-          acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
-        }
-        st_stream(dxrow + (size_t)v * 16, pack(o));
+        const uint4 xv = ld_shared_v4(st + v), dv = ld_shared_v4(st + sl.nv + v);
+        const uint4 rv = DRES ? ld_shared_v4(st + 2 * sl.nv + v) : make_uint4(0, 0, 0, 0);
+        st_stream(dxrow + (size_t)v * 16, bwd_vec_apply<E, DRES>(xv, dv, rv, g[k], r, c, acc[k]));
       }
     }
     if (DRES) {

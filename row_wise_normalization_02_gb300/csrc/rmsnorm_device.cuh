@@ -100,6 +100,16 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
                : "memory");
 }
 
+// A 16-byte shared-memory read the compiler may not merge with an earlier
+// read of the same address (so the earlier value need not stay live).
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+  return v;
+}
+
 template <typename T>
 __device__ __forceinline__ float ld_scalar(const T* p) {
   return Elem<T>::to_f32(*p);
