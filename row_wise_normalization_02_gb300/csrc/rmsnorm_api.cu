@@ -422,6 +422,15 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.threads = kSubwarpThreads;
     p.rows_per_cta = kSubwarpThreads / p.g;
     p.prefetch = !(bwd && p.g == 32);   // full-warp rows: more CTAs beat prefetch
+    if (op == kBwd && p.g == 32 && p.vpt == 3) {
+      // rows of 65-96 vectors: the CTA's eight rows through a three-stage
+      // bulk-copy ring rather than in registers (65536 x 768 bf16: 0.90 of
+      // the copy peak against 0.83; the register form spills at two CTAs per
+      // SM)
+      p.family = kStaged;
+      p.prefetch = false;
+      p.stages = 3;
+    }
   } else if (rows_aligned && bwd && nvec <= 4 * kCtaMaxThreads) {
     // backward: rows streamed by bulk copies, two stages, up to 4 vectors
     // per thread (the dgamma partials and gamma stay in registers)
@@ -438,7 +447,10 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.family = kCluster;
     if (!cluster_shape(true, nvec, 0, &p.cluster, &p.slice, &p.vpt, &p.threads))
       p.family = kGeneric;
-    p.stages = 2;
+    // as many stages as fit one CTA per SM, at most three
+    p.stages = (int)((kStagedSmemMax - kStagedHeader) / ((dres ? 3 : 2) * (int64_t)p.slice * 16));
+    if (p.stages > 3) p.stages = 3;
+    if (p.stages < 2) p.stages = 2;
   } else if (rows_aligned && nvec <= (op == kFwd ? 2048 : 4096)) {
     // one row per CTA; beyond 2048 vectors the forward does better on two-CTA
     // clusters (4096 x 32768 bf16: 0.92 of the copy peak against 0.84 at 8
@@ -493,7 +505,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       }
       if ((int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
       p.period = ragged_period((int64_t)N * esize(xd));
-    } else if (p.family == kStaged && bwd && f.g > 0) {
+    } else if (p.family == kStaged && bwd && (f.g > 0 || (f.family < 0 && p.g > 0))) {
       // short backward rows through the ring: g lanes per row, 256 / g rows
       // per CTA iteration
       if (!f.vpt) p.vpt = (nvec + p.g - 1) / p.g;
@@ -501,7 +513,8 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       p.threads = kSubwarpThreads;
       p.rows_per_cta = kSubwarpThreads / p.g;
       p.prefetch = false;
-      p.stages = f.st;
+      if (f.st > 0) p.stages = f.st;
+      else if (f.family == kStaged) p.stages = 0;   // as many as the budget holds
     } else if (p.family == kStaged) {
       if (!rows_aligned) return RMSNORM_ERR_INVALID_ARG;
       p.g = 0;

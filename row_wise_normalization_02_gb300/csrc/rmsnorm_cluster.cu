@@ -305,13 +305,6 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
     // cluster sees the same sums and the same verdict on the waits
     const bool any_late = cta_sum_vote<K>(sums, rg.red, parity, late);
     parity ^= 1;
-    // every thread has read this stage: refill it before the exchange, so
-    // the copy overlaps it (if the cluster then stops, the copy is drained)
-    if (!DRES && !any_late && tid == 0 && issued < nrows) {
-      fence_proxy_async_smem();
-      issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
-      ++issued;
-    }
     float tot[3];
     const bool answered = xchg_sum<3>(xc, make_float4(sums[0], K > 1 ? sums[K - 1] : 0.f,
                                                       any_late ? 1.f : 0.f, 0.f),
@@ -336,14 +329,13 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
         st_stream(dxrow + (size_t)v * 16, bwd_vec_apply<E, DRES>(xv, dv, rv, g[k], r, c, acc[k]));
       }
     }
-    if (DRES) {
-      // every thread has read this stage (dres included): refill it
-      __syncthreads();
-      if (tid == 0 && issued < nrows) {
-        fence_proxy_async_smem();
-        issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
-        ++issued;
-      }
+    // every thread has read this stage (the output pass reads it again):
+    // refill it
+    __syncthreads();
+    if (tid == 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue_slice<NS>(rg, issued, first, stride, S, xs, ds, rs, rb, sb);
+      ++issued;
     }
   }
   if (failed && tid == 0) {

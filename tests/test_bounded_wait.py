@@ -26,11 +26,14 @@ def _data(M, N, seed):
     return x, dy, g
 
 
-@pytest.mark.parametrize("op", ["fwd", "fused", "bwd"])
+@pytest.mark.parametrize("op", ["fwd", "fused", "bwd", "bwd_short_rows"])
 def test_timeout_is_reported_and_the_context_survives(debug_env, op):
     M, N, eps = 1024, 8192, float(np.float32(1e-5))
+    if op == "bwd_short_rows":     # 32 rows of 128 per stage of the ring
+        M, N = 8192, 128
     x, dy, g = _data(M, N, seed=41)
-    debug_env.set("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=4")
+    debug_env.set("RMSNORM_FORCE_VARIANT",
+                  "staged:g=8:vpt=2:st=4" if op == "bwd_short_rows" else "staged:vpt=4:st=4")
     rn.rmsnorm_check_device()                    # start from a clear flag
     debug_env.set("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     if op == "fwd":
@@ -46,9 +49,14 @@ def test_timeout_is_reported_and_the_context_survives(debug_env, op):
 
     # same variant, normal limit: correct results, no flag
     debug_env.delete("RMSNORM_WAIT_LIMIT_CYCLES")
-    out = pu.run_fwd(x, g, eps, "bf16", "bf16")
-    ref = oracle.fwd(x, g, eps, "bf16", "bf16")
-    pu.check_bf16_ulp(out["y"], ref["y"])
+    if op == "bwd_short_rows":
+        from tests.test_parity_bwd import check_bwd
+        out = pu.run_bwd(dy, x, None, g, eps, "bf16", "bf16")
+        check_bwd(x, dy, g, None, eps, "bf16", "bf16", out)
+    else:
+        out = pu.run_fwd(x, g, eps, "bf16", "bf16")
+        ref = oracle.fwd(x, g, eps, "bf16", "bf16")
+        pu.check_bf16_ulp(out["y"], ref["y"])
     rn.rmsnorm_check_device()
 
 

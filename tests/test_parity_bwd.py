@@ -110,6 +110,11 @@ def test_bwd_without_dgamma(N):
     ("staged:vpt=4:st=3:cps=1", 8192), ("staged:vpt=4:st=2:cps=1", 8192),
     ("staged:vpt=2:st=4:cps=1", 4096), ("staged:vpt=1:st=2:cps=1", 2048),
     ("staged:vpt=4:st=2:cps=1", 5120), ("staged:vpt=4:st=3:cps=1", 1032),
+    # short rows through the ring, 256 / g rows per stage (a partial last stage)
+    ("staged:g=32:vpt=3:cps=1", 768), ("staged:g=32:vpt=3:st=2:cps=1", 520),
+    ("staged:g=8:vpt=2:cps=1", 128), ("staged:g=4:vpt=1:st=3:cps=1", 32),
+    ("staged:g=16:vpt=2:st=8:cps=1", 256), ("staged:g=32:vpt=4:st=2:cps=1", 1024),
+    ("staged:g=32:vpt=1:cps=1", 200),
 ])
 def test_forced_variants_walk_several_rows(debug_env, force, N):
     debug_env.set("RMSNORM_FORCE_VARIANT", force)

@@ -218,3 +218,4 @@ def test_plan_families():
     assert "/generic/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 1 << 19, "bf16", "bf16")
     assert "/staged/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 16384, 8192, "bf16", "f32")
     assert "/subwarp/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 262144, 128, "bf16", "bf16")
+    assert "/staged/g32/vpt3/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 65536, 768, "bf16", "bf16")
