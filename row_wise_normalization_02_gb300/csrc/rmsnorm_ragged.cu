@@ -13,8 +13,8 @@
 // partials stay in registers, exactly as for aligned rows.
 #include <type_traits>
 
-#include "rmsnorm_device.cuh"
-#include "rmsnorm_internal.h"
+#include "rmsnorm_bwd_common.cuh"
+#include "rmsnorm_ring.cuh"
 
 #ifndef RMSN_PAIR
 #error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
@@ -286,6 +286,164 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
   if (L.scol >= 0) prow[L.scol] = acc_s;
 }
 
+// ---------------------------------------------------------------------------
+// Backward with the 16-byte-aligned interior of each row (its vector body)
+// streamed through a ring of `stages` shared-memory buffers by bulk copies,
+// for short row walks: fewer, longer-lived CTAs (and so fewer dgamma partial
+// rows) with several rows in flight each, independently of registers.  The
+// head and tail scalars cannot be bulk-copied (they start off a 16-byte
+// boundary, and for the first and last rows the enclosing 16 bytes leave the
+// buffer): their owner threads load them with plain loads kLag rows ahead,
+// through a short queue of registers.  One CTA barrier per row -- the row
+// reduction's -- also proves that every thread is done with the previous
+// row's stage, which thread 0 then refills, and carries the vote on the
+// bounded waits.
+constexpr int kLag = 3;   // rows of lookahead for the head / tail scalars
+
+template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool DRES>
+__global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const BwdParams p) {
+  pdl_begin();
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int K = HAS_RSTD ? 1 : 2;
+  constexpr int NS = DRES ? 3 : 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Ring rg = ring_of(smem);
+  const int tid = threadIdx.x, T = blockDim.x, N = p.N, S = p.stages;
+  const Walk w = walk_of(p.period, p.M);
+  const TX* src[3] = {static_cast<const TX*>(p.x), static_cast<const TX*>(p.dy),
+                      static_cast<const TX*>(p.dres)};
+  TX* dx = static_cast<TX*>(p.dx);
+  const Layout L = layout_of<TX>(src[0] + w.cls * (int64_t)N, N, tid);
+  const uint32_t body = (uint32_t)L.nb * 16;
+  const int64_t nrows = w.first < p.M ? (p.M - 1 - w.first) / w.stride + 1 : 0;
+
+  auto issue = [&](int64_t i) {   // thread 0: the bodies of walk row i
+    const int s = (int)(i % S);
+    const int64_t row = w.first + i * w.stride;
+    uint64_t* bar = rg.full + s;
+    unsigned char* dst = rg.buf + (size_t)s * NS * body;
+    mbar_arrive_expect_tx(bar, NS * body);
+    if (body == 0) return;
+#pragma unroll
+    for (int q = 0; q < NS; ++q) bulk_copy_g2s(dst + q * body, src[q] + row * (int64_t)N + L.h, body, bar);
+  };
+  int64_t issued = 0;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (; issued < (nrows < S ? nrows : S); ++issued) issue(issued);
+
+  float g[VPT][E], gs, acc[VPT][E], acc_s = 0.f;
+  gather_gamma<TW, TX, VPT>(static_cast<const TW*>(p.gamma), L, tid, T, g, gs);
+#pragma unroll
+  for (int k = 0; k < VPT; ++k)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+
+  // head / tail scalars of this thread's column, kLag rows ahead:
+  // q[d][op] holds walk row i + d during iteration i
+  float q[kLag][NS];
+  auto load_scalars = [&](float (&dst)[NS], int64_t i) {
+    const int64_t row = w.first + i * w.stride;
+    const bool ok = L.scol >= 0 && i < nrows;
+#pragma unroll
+    for (int o = 0; o < NS; ++o) dst[o] = ok ? ld_scalar(src[o] + row * (int64_t)N + L.scol) : 0.f;
+  };
+#pragma unroll
+  for (int d = 0; d < kLag; ++d) load_scalars(q[d], d);
+
+  int parity = 0;
+  int64_t i = 0;
+  bool failed = false;
+  for (; i < nrows; ++i) {
+    const int s = (int)(i % S);
+    const int64_t row = w.first + i * w.stride;
+    const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
+    float sc[NS];
+#pragma unroll
+    for (int o = 0; o < NS; ++o) sc[o] = q[0][o];
+#pragma unroll
+    for (int d = 0; d + 1 < kLag; ++d)
+#pragma unroll
+      for (int o = 0; o < NS; ++o) q[d][o] = q[d + 1][o];
+    load_scalars(q[kLag - 1], i + kLag);
+
+    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
+    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * NS * body);
+    float2 dot2 = make_float2(0.f, 0.f), ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      const uint4 xv = v < L.nb ? st[v] : make_uint4(0, 0, 0, 0);
+      const uint4 dv = v < L.nb ? st[L.nb + v] : make_uint4(0, 0, 0, 0);
+      bwd_vec_sums<E, !HAS_RSTD>(xv, dv, g[k], dot2, ss2);
+    }
+    float sums[K];
+    sums[0] = fmaf(gs * sc[1], sc[0], dot2.x + dot2.y);
+    if (!HAS_RSTD) sums[K - 1] = fmaf(sc[0], sc[0], ss2.x + ss2.y);
+    // the barrier of the row sums: every thread is also done with the
+    // previous row's stage, and the CTA agrees on the waits
+    if (cta_sum_vote<K>(sums, rg.red, parity, late)) {
+      failed = true;
+      break;
+    }
+    parity ^= 1;
+    if (tid == 0 && i > 0 && issued < nrows) {
+      fence_proxy_async_smem();
+      issue(issued);
+      ++issued;
+    }
+    const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
+    const float c = r * r * p.inv_n * sums[0];
+    TX* dxr = dx + row * (int64_t)N;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * T;
+      if (v < L.nb) {
+        const uint4 xv = ld_shared_v4(st + v), dv = ld_shared_v4(st + L.nb + v);
+        const uint4 rv = DRES ? ld_shared_v4(st + 2 * L.nb + v) : make_uint4(0, 0, 0, 0);
+        st_stream(dxr + L.h + v * E, bwd_vec_apply<E, DRES>(xv, dv, rv, g[k], r, c, acc[k]));
+      }
+    }
+    if (L.scol >= 0) {
+      st_scalar(dxr + L.scol, r * fmaf(-sc[0], c, gs * sc[1]) + (DRES ? sc[NS - 1] : 0.f));
+      acc_s = fmaf(sc[1] * sc[0], r, acc_s);
+    }
+  }
+  if (failed) {
+    if (tid == 0) {
+      drain(rg, i, issued, S);
+      atomicOr(p.status, kStatusWaitTimeout);
+    }
+    return;
+  }
+  if (p.partial == nullptr) return;
+  // every column of the partial row is written by exactly one thread
+  float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * T;
+    if (v < L.nb) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) prow[L.h + v * E + e] = acc[k][e];
+    }
+  }
+  if (L.scol >= 0) prow[L.scol] = acc_s;
+}
+
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
+BwdKernel pick_ring(int vpt) {
+  switch (vpt) {
+    case 1: return bwd_ragged_ring_kernel<TX, TW, 1, HAS_RSTD, DRES>;
+    case 2: return bwd_ragged_ring_kernel<TX, TW, 2, HAS_RSTD, DRES>;
+    case 4: return bwd_ragged_ring_kernel<TX, TW, 4, HAS_RSTD, DRES>;
+    default: return nullptr;
+  }
+}
+
 template <typename TX, typename TW, bool FUSED>
 FwdKernel pick_fwd(int vpt, bool pf) {
   switch (vpt) {
@@ -315,6 +473,11 @@ FwdKernel ragged_fwd(const FwdKey& k) {
 }
 template <typename TX, typename TW>
 BwdKernel ragged_bwd(const BwdKey& k) {
+  if (k.ring) {
+    if (k.dres)
+      return k.has_rstd ? pick_ring<TX, TW, true, true>(k.vpt) : pick_ring<TX, TW, false, true>(k.vpt);
+    return k.has_rstd ? pick_ring<TX, TW, true, false>(k.vpt) : pick_ring<TX, TW, false, false>(k.vpt);
+  }
   if (k.dres)
     return k.has_rstd ? pick_bwd<TX, TW, true, true>(k.vpt, k.prefetch)
                       : pick_bwd<TX, TW, false, true>(k.vpt, k.prefetch);

@@ -26,14 +26,18 @@ def _data(M, N, seed):
     return x, dy, g
 
 
-@pytest.mark.parametrize("op", ["fwd", "fused", "bwd", "bwd_short_rows"])
+FORCE = {"bwd_short_rows": "staged:g=8:vpt=2:st=4", "bwd_ragged": "ragged:vpt=1:st=4"}
+
+
+@pytest.mark.parametrize("op", ["fwd", "fused", "bwd", "bwd_short_rows", "bwd_ragged"])
 def test_timeout_is_reported_and_the_context_survives(debug_env, op):
     M, N, eps = 1024, 8192, float(np.float32(1e-5))
     if op == "bwd_short_rows":     # 32 rows of 128 per stage of the ring
         M, N = 8192, 128
+    if op == "bwd_ragged":         # row interiors through the ring
+        M, N = 1024, 2049
     x, dy, g = _data(M, N, seed=41)
-    debug_env.set("RMSNORM_FORCE_VARIANT",
-                  "staged:g=8:vpt=2:st=4" if op == "bwd_short_rows" else "staged:vpt=4:st=4")
+    debug_env.set("RMSNORM_FORCE_VARIANT", FORCE.get(op, "staged:vpt=4:st=4"))
     rn.rmsnorm_check_device()                    # start from a clear flag
     debug_env.set("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     if op == "fwd":
@@ -49,7 +53,7 @@ def test_timeout_is_reported_and_the_context_survives(debug_env, op):
 
     # same variant, normal limit: correct results, no flag
     debug_env.delete("RMSNORM_WAIT_LIMIT_CYCLES")
-    if op == "bwd_short_rows":
+    if op in FORCE:
         from tests.test_parity_bwd import check_bwd
         out = pu.run_bwd(dy, x, None, g, eps, "bf16", "bf16")
         check_bwd(x, dy, g, None, eps, "bf16", "bf16", out)
