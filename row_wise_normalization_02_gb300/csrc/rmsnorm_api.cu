@@ -607,8 +607,9 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (p.family == kSubwarp) p.smem = p.rows_per_cta * nvec * E * 4;
     else if (p.family == kCta) p.smem = 512 + (p.acc_smem ? ld * 4 : 0);
     else if (p.family == kRagged && k.ring) {
-      // ring of row interiors: at most N / E vectors per operand and stage
-      const int64_t bytes = kStagedHeader + (int64_t)p.stages * (dres ? 3 : 2) * (N / E) * 16;
+      // ring of rows: the 16-byte span enclosing a row, at most N / E + 2
+      // vectors per operand and stage
+      const int64_t bytes = kStagedHeader + (int64_t)p.stages * (dres ? 3 : 2) * (N / E + 2) * 16;
       if (p.stages > kStagedMaxStages || bytes > kStagedSmemMax) return RMSNORM_ERR_INVALID_ARG;
       p.smem = (int)bytes;
     } else if (p.family == kRagged) p.smem = 512;

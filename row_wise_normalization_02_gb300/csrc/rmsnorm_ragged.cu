@@ -287,19 +287,20 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
 }
 
 // ---------------------------------------------------------------------------
-// Backward with the 16-byte-aligned interior of each row (its vector body)
-// streamed through a ring of `stages` shared-memory buffers by bulk copies,
-// for short row walks: fewer, longer-lived CTAs (and so fewer dgamma partial
-// rows) with several rows in flight each, independently of registers.  The
-// head and tail scalars cannot be bulk-copied (they start off a 16-byte
-// boundary, and for the first and last rows the enclosing 16 bytes leave the
-// buffer): their owner threads load them with plain loads kLag rows ahead,
-// through a short queue of registers.  One CTA barrier per row -- the row
+// Backward with each row streamed through a ring of `stages` shared-memory
+// buffers by bulk copies, for short row walks: fewer, longer-lived CTAs (and
+// so fewer dgamma partial rows) with several rows in flight each,
+// independently of registers.  A bulk copy needs 16-byte aligned ends, so a
+// row is copied as the 16-byte span that encloses it (a few bytes of its
+// neighbours come along); only where that span would leave the buffer -- the
+// first row when the buffer does not start on 16 bytes, the last row when it
+// does not end on 16 -- is the aligned interior copied alone and the head and
+// tail scalars read from global memory.  The row's element j then sits at
+// byte mis + j * size of its stage buffer (mis = the row start mod 16), the
+// vector body at 16-byte offsets.  One CTA barrier per row -- the row
 // reduction's -- also proves that every thread is done with the previous
 // row's stage, which thread 0 then refills, and carries the vote on the
 // bounded waits.
-constexpr int kLag = 3;   // rows of lookahead for the head / tail scalars
-
 template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool DRES>
 __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const BwdParams p) {
   pdl_begin();
@@ -314,18 +315,36 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const B
                       static_cast<const TX*>(p.dres)};
   TX* dx = static_cast<TX*>(p.dx);
   const Layout L = layout_of<TX>(src[0] + w.cls * (int64_t)N, N, tid);
-  const uint32_t body = (uint32_t)L.nb * 16;
+  const size_t rb = (size_t)N * sizeof(TX);
+  const int mis = (int)(reinterpret_cast<uintptr_t>(src[0] + w.cls * (int64_t)N) & 15);
+  const int body_off = mis ? 16 : 0;                    // the body's offset in a stage buffer
+  const uint32_t slot = (uint32_t)(N / E + 2) * 16;     // bytes per operand and stage
   const int64_t nrows = w.first < p.M ? (p.M - 1 - w.first) / w.stride + 1 : 0;
+  // rows whose enclosing 16-byte span [start - mis, start - mis + span) leaves
+  // the buffer (the same rows for every operand, which agree modulo 16): the
+  // first rows when the buffer does not start on 16 bytes, the last when it
+  // does not end on 16 (more than one only for rows shorter than 16 bytes)
+  const int64_t span = (int64_t)((mis + rb + 15) & ~(size_t)15);
+  auto edge = [&](int64_t row) {
+    const int64_t lo = row * (int64_t)rb - mis;
+    return lo < 0 || lo + span > p.M * (int64_t)rb;
+  };
 
-  auto issue = [&](int64_t i) {   // thread 0: the bodies of walk row i
+  auto issue = [&](int64_t i) {   // thread 0: walk row i into its stage
     const int s = (int)(i % S);
     const int64_t row = w.first + i * w.stride;
     uint64_t* bar = rg.full + s;
-    unsigned char* dst = rg.buf + (size_t)s * NS * body;
-    mbar_arrive_expect_tx(bar, NS * body);
-    if (body == 0) return;
+    unsigned char* dst = rg.buf + (size_t)s * NS * slot;
+    const bool e = edge(row);
+    const uint32_t bytes = e ? (uint32_t)L.nb * 16 : (uint32_t)span;
+    mbar_arrive_expect_tx(bar, NS * bytes);
+    if (bytes == 0) return;
 #pragma unroll
-    for (int q = 0; q < NS; ++q) bulk_copy_g2s(dst + q * body, src[q] + row * (int64_t)N + L.h, body, bar);
+    for (int q = 0; q < NS; ++q) {
+      const char* r0 = reinterpret_cast<const char*>(src[q] + row * (int64_t)N);
+      if (e) bulk_copy_g2s(dst + q * slot + body_off, r0 + L.h * sizeof(TX), bytes, bar);
+      else bulk_copy_g2s(dst + q * slot, r0 - mis, bytes, bar);
+    }
   };
   int64_t issued = 0;
   if (tid == 0) {
@@ -343,18 +362,6 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const B
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
 
-  // head / tail scalars of this thread's column, kLag rows ahead:
-  // q[d][op] holds walk row i + d during iteration i
-  float q[kLag][NS];
-  auto load_scalars = [&](float (&dst)[NS], int64_t i) {
-    const int64_t row = w.first + i * w.stride;
-    const bool ok = L.scol >= 0 && i < nrows;
-#pragma unroll
-    for (int o = 0; o < NS; ++o) dst[o] = ok ? ld_scalar(src[o] + row * (int64_t)N + L.scol) : 0.f;
-  };
-#pragma unroll
-  for (int d = 0; d < kLag; ++d) load_scalars(q[d], d);
-
   int parity = 0;
   int64_t i = 0;
   bool failed = false;
@@ -362,23 +369,29 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const B
     const int s = (int)(i % S);
     const int64_t row = w.first + i * w.stride;
     const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
+    const bool e = edge(row);
+    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
+    const unsigned char* sb = rg.buf + (size_t)s * NS * slot;
+    // this thread's head / tail scalar of each operand
     float sc[NS];
 #pragma unroll
-    for (int o = 0; o < NS; ++o) sc[o] = q[0][o];
-#pragma unroll
-    for (int d = 0; d + 1 < kLag; ++d)
-#pragma unroll
-      for (int o = 0; o < NS; ++o) q[d][o] = q[d + 1][o];
-    load_scalars(q[kLag - 1], i + kLag);
-
-    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
-    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * NS * body);
+    for (int o = 0; o < NS; ++o) {
+      sc[o] = 0.f;
+      if (L.scol >= 0) {
+        if (e) sc[o] = ld_scalar(src[o] + row * (int64_t)N + L.scol);
+        else sc[o] = Elem<TX>::to_f32(*reinterpret_cast<const TX*>(sb + o * slot + mis +
+                                                                    L.scol * sizeof(TX)));
+      }
+    }
+    const uint4* xs = reinterpret_cast<const uint4*>(sb + body_off);
+    const uint4* ds = reinterpret_cast<const uint4*>(sb + slot + body_off);
+    const uint4* rs = reinterpret_cast<const uint4*>(sb + 2 * slot + body_off);
     float2 dot2 = make_float2(0.f, 0.f), ss2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
-      const uint4 xv = v < L.nb ? st[v] : make_uint4(0, 0, 0, 0);
-      const uint4 dv = v < L.nb ? st[L.nb + v] : make_uint4(0, 0, 0, 0);
+      const uint4 xv = v < L.nb ? xs[v] : make_uint4(0, 0, 0, 0);
+      const uint4 dv = v < L.nb ? ds[v] : make_uint4(0, 0, 0, 0);
       bwd_vec_sums<E, !HAS_RSTD>(xv, dv, g[k], dot2, ss2);
     }
     float sums[K];
@@ -403,8 +416,8 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const B
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
       if (v < L.nb) {
-        const uint4 xv = ld_shared_v4(st + v), dv = ld_shared_v4(st + L.nb + v);
-        const uint4 rv = DRES ? ld_shared_v4(st + 2 * L.nb + v) : make_uint4(0, 0, 0, 0);
+        const uint4 xv = ld_shared_v4(xs + v), dv = ld_shared_v4(ds + v);
+        const uint4 rv = DRES ? ld_shared_v4(rs + v) : make_uint4(0, 0, 0, 0);
         st_stream(dxr + L.h + v * E, bwd_vec_apply<E, DRES>(xv, dv, rv, g[k], r, c, acc[k]));
       }
     }

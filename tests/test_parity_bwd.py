@@ -36,7 +36,8 @@ def check_bwd(x, dy, g, rstd, eps, xd, wd, out, want_dgamma=True):
     info = {}
     if xd == "bf16":
         info["floor"], info["max_ulp"] = pu.check_dx_bf16(out["dx"], ref["dx"], ref["dx64"], x64,
-                                                          dy64, g64, r, ref["c64"])
+                                                          dy64, g64, r, ref["c64"],
+                                                          ref["dot_abs64"])
     else:
         pu.check_f32(out["dx"], ref["dx64"], what="dx")
     if want_dgamma:

@@ -52,7 +52,7 @@ def check(h, dy, dres, g, rstd, eps, xd, wd, out, dg_dtype="f32"):
     r = rstd.astype(np.float64) if rstd is not None else 1.0 / np.sqrt(np.mean(h64 ** 2, 1) + eps)
     if xd == "bf16":
         n_floor, _ = pu.check_dx_bf16(out["dh"], ref["dh"], ref["dh64"], h64, dy64, g64, r,
-                                      aux["c64"], what="dh")
+                                      aux["c64"], aux["dot_abs64"], what="dh")
     else:
         n_floor = 0
         pu.check_f32(out["dh"], ref["dh64"], what="dh")
