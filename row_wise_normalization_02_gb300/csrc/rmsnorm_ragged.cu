@@ -362,13 +362,18 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const B
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
 
+  // the saved rstd, a window of rows ahead
+  __shared__ float rwin[2 * kRstdWin];
+  RstdStage rst;
+  if (HAS_RSTD) rstd_begin(rst, p.rstd, w.first, w.stride, nrows);
+
   int parity = 0;
   int64_t i = 0;
   bool failed = false;
   for (; i < nrows; ++i) {
     const int s = (int)(i % S);
     const int64_t row = w.first + i * w.stride;
-    const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
+    if (HAS_RSTD) rstd_stage(rst, rwin, p.rstd, w.first, w.stride, nrows, i);
     const bool e = edge(row);
     const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
     const unsigned char* sb = rg.buf + (size_t)s * NS * slot;
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const B
       issue(issued);
       ++issued;
     }
-    const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
+    const float r = HAS_RSTD ? rstd_of(rwin, i) : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
     const float c = r * r * p.inv_n * sums[0];
     TX* dxr = dx + row * (int64_t)N;
 #pragma unroll
