@@ -505,13 +505,6 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       }
       if ((int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
       p.period = ragged_period((int64_t)N * esize(xd));
-      // st= selects the backward's bulk-copy ring of row interiors (st=0:
-      // the register form)
-      if (bwd && f.st >= 0 && (f.st > 0 || f.family == kRagged)) p.stages = f.st;
-      if (bwd && p.stages > 0) {
-        p.prefetch = false;
-        if (!f.cps) p.cta_per_sm_cap = 2;
-      }
     } else if (p.family == kStaged && bwd && (f.g > 0 || (f.family < 0 && p.g > 0))) {
       // short backward rows through the ring: g lanes per row, 256 / g rows
       // per CTA iteration
@@ -600,19 +593,12 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (fr.on && fr.mr >= 0) p.min_rows = fr.mr;
     if (dres && p.family == kCta) return RMSNORM_ERR_INVALID_ARG;
     BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch, dres};
-    k.ring = p.family == kRagged && p.stages > 0;
     p.bwd = bwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.bwd);
     const int ld = round_up(N, 4);
     if (p.family == kSubwarp) p.smem = p.rows_per_cta * nvec * E * 4;
     else if (p.family == kCta) p.smem = 512 + (p.acc_smem ? ld * 4 : 0);
-    else if (p.family == kRagged && k.ring) {
-      // ring of rows: the 16-byte span enclosing a row, at most N / E + 2
-      // vectors per operand and stage
-      const int64_t bytes = kStagedHeader + (int64_t)p.stages * (dres ? 3 : 2) * (N / E + 2) * 16;
-      if (p.stages > kStagedMaxStages || bytes > kStagedSmemMax) return RMSNORM_ERR_INVALID_ARG;
-      p.smem = (int)bytes;
-    } else if (p.family == kRagged) p.smem = 512;
+    else if (p.family == kRagged) p.smem = 512;
     else if (p.family == kCluster) {
       // ring of the slice of [x | dy] ([h | dy | dres]) rows
       const int64_t bytes = kStagedHeader + (int64_t)p.stages * (dres ? 3 : 2) * p.slice * 16;

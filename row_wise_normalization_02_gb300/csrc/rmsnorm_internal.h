@@ -152,7 +152,6 @@ struct BwdKey {
   bool acc_smem; // kCta: dgamma partials in shared memory instead of registers
   bool prefetch;
   bool dres;     // fused-add backward (adds the residual-path gradient)
-  bool ring = false;   // kRagged: row interiors through a bulk-copy ring
 };
 
 // Kernel for a key, or nullptr when that instantiation does not exist.  Each

@@ -13,8 +13,8 @@
 // partials stay in registers, exactly as for aligned rows.
 #include <type_traits>
 
-#include "rmsnorm_bwd_common.cuh"
-#include "rmsnorm_ring.cuh"
+#include "rmsnorm_device.cuh"
+#include "rmsnorm_internal.h"
 
 #ifndef RMSN_PAIR
 #error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
@@ -286,182 +286,6 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
   if (L.scol >= 0) prow[L.scol] = acc_s;
 }
 
-// ---------------------------------------------------------------------------
-// Backward with each row streamed through a ring of `stages` shared-memory
-// buffers by bulk copies, for short row walks: fewer, longer-lived CTAs (and
-// so fewer dgamma partial rows) with several rows in flight each,
-// independently of registers.  A bulk copy needs 16-byte aligned ends, so a
-// row is copied as the 16-byte span that encloses it (a few bytes of its
-// neighbours come along); only where that span would leave the buffer -- the
-// first row when the buffer does not start on 16 bytes, the last row when it
-// does not end on 16 -- is the aligned interior copied alone and the head and
-// tail scalars read from global memory.  The row's element j then sits at
-// byte mis + j * size of its stage buffer (mis = the row start mod 16), the
-// vector body at 16-byte offsets.  One CTA barrier per row -- the row
-// reduction's -- also proves that every thread is done with the previous
-// row's stage, which thread 0 then refills, and carries the vote on the
-// bounded waits.
-template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool DRES>
-__global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_ring_kernel(const BwdParams p) {
-  pdl_begin();
-  constexpr int E = Elem<TX>::kPerVec;
-  constexpr int K = HAS_RSTD ? 1 : 2;
-  constexpr int NS = DRES ? 3 : 2;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const Ring rg = ring_of(smem);
-  const int tid = threadIdx.x, T = blockDim.x, N = p.N, S = p.stages;
-  const Walk w = walk_of(p.period, p.M);
-  const TX* src[3] = {static_cast<const TX*>(p.x), static_cast<const TX*>(p.dy),
-                      static_cast<const TX*>(p.dres)};
-  TX* dx = static_cast<TX*>(p.dx);
-  const Layout L = layout_of<TX>(src[0] + w.cls * (int64_t)N, N, tid);
-  const size_t rb = (size_t)N * sizeof(TX);
-  const int mis = (int)(reinterpret_cast<uintptr_t>(src[0] + w.cls * (int64_t)N) & 15);
-  const int body_off = mis ? 16 : 0;                    // the body's offset in a stage buffer
-  const uint32_t slot = (uint32_t)(N / E + 2) * 16;     // bytes per operand and stage
-  const int64_t nrows = w.first < p.M ? (p.M - 1 - w.first) / w.stride + 1 : 0;
-  // rows whose enclosing 16-byte span [start - mis, start - mis + span) leaves
-  // the buffer (the same rows for every operand, which agree modulo 16): the
-  // first rows when the buffer does not start on 16 bytes, the last when it
-  // does not end on 16 (more than one only for rows shorter than 16 bytes)
-  const int64_t span = (int64_t)((mis + rb + 15) & ~(size_t)15);
-  auto edge = [&](int64_t row) {
-    const int64_t lo = row * (int64_t)rb - mis;
-    return lo < 0 || lo + span > p.M * (int64_t)rb;
-  };
-
-  auto issue = [&](int64_t i) {   // thread 0: walk row i into its stage
-    const int s = (int)(i % S);
-    const int64_t row = w.first + i * w.stride;
-    uint64_t* bar = rg.full + s;
-    unsigned char* dst = rg.buf + (size_t)s * NS * slot;
-    const bool e = edge(row);
-    const uint32_t bytes = e ? (uint32_t)L.nb * 16 : (uint32_t)span;
-    mbar_arrive_expect_tx(bar, NS * bytes);
-    if (bytes == 0) return;
-#pragma unroll
-    for (int q = 0; q < NS; ++q) {
-      const char* r0 = reinterpret_cast<const char*>(src[q] + row * (int64_t)N);
-      if (e) bulk_copy_g2s(dst + q * slot + body_off, r0 + L.h * sizeof(TX), bytes, bar);
-      else bulk_copy_g2s(dst + q * slot, r0 - mis, bytes, bar);
-    }
-  };
-  int64_t issued = 0;
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
-  if (tid == 0)
-    for (; issued < (nrows < S ? nrows : S); ++issued) issue(issued);
-
-  float g[VPT][E], gs, acc[VPT][E], acc_s = 0.f;
-  gather_gamma<TW, TX, VPT>(static_cast<const TW*>(p.gamma), L, tid, T, g, gs);
-#pragma unroll
-  for (int k = 0; k < VPT; ++k)
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
-
-  // the saved rstd, a window of rows ahead
-  __shared__ float rwin[2 * kRstdWin];
-  RstdStage rst;
-  if (HAS_RSTD) rstd_begin(rst, p.rstd, w.first, w.stride, nrows);
-
-  int parity = 0;
-  int64_t i = 0;
-  bool failed = false;
-  for (; i < nrows; ++i) {
-    const int s = (int)(i % S);
-    const int64_t row = w.first + i * w.stride;
-    if (HAS_RSTD) rstd_stage(rst, rwin, p.rstd, w.first, w.stride, nrows, i);
-    const bool e = edge(row);
-    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
-    const unsigned char* sb = rg.buf + (size_t)s * NS * slot;
-    // this thread's head / tail scalar of each operand
-    float sc[NS];
-#pragma unroll
-    for (int o = 0; o < NS; ++o) {
-      sc[o] = 0.f;
-      if (L.scol >= 0) {
-        if (e) sc[o] = ld_scalar(src[o] + row * (int64_t)N + L.scol);
-        else sc[o] = Elem<TX>::to_f32(*reinterpret_cast<const TX*>(sb + o * slot + mis +
-                                                                    L.scol * sizeof(TX)));
-      }
-    }
-    const uint4* xs = reinterpret_cast<const uint4*>(sb + body_off);
-    const uint4* ds = reinterpret_cast<const uint4*>(sb + slot + body_off);
-    const uint4* rs = reinterpret_cast<const uint4*>(sb + 2 * slot + body_off);
-    float2 dot2 = make_float2(0.f, 0.f), ss2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = tid + k * T;
-      const uint4 xv = v < L.nb ? xs[v] : make_uint4(0, 0, 0, 0);
-      const uint4 dv = v < L.nb ? ds[v] : make_uint4(0, 0, 0, 0);
-      bwd_vec_sums<E, !HAS_RSTD>(xv, dv, g[k], dot2, ss2);
-    }
-    float sums[K];
-    sums[0] = fmaf(gs * sc[1], sc[0], dot2.x + dot2.y);
-    if (!HAS_RSTD) sums[K - 1] = fmaf(sc[0], sc[0], ss2.x + ss2.y);
-    // the barrier of the row sums: every thread is also done with the
-    // previous row's stage, and the CTA agrees on the waits
-    if (cta_sum_vote<K>(sums, rg.red, parity, late)) {
-      failed = true;
-      break;
-    }
-    parity ^= 1;
-    if (tid == 0 && i > 0 && issued < nrows) {
-      fence_proxy_async_smem();
-      issue(issued);
-      ++issued;
-    }
-    const float r = HAS_RSTD ? rstd_of(rwin, i) : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
-    const float c = r * r * p.inv_n * sums[0];
-    TX* dxr = dx + row * (int64_t)N;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = tid + k * T;
-      if (v < L.nb) {
-        const uint4 xv = ld_shared_v4(xs + v), dv = ld_shared_v4(ds + v);
-        const uint4 rv = DRES ? ld_shared_v4(rs + v) : make_uint4(0, 0, 0, 0);
-        st_stream(dxr + L.h + v * E, bwd_vec_apply<E, DRES>(xv, dv, rv, g[k], r, c, acc[k]));
-      }
-    }
-    if (L.scol >= 0) {
-      st_scalar(dxr + L.scol, r * fmaf(-sc[0], c, gs * sc[1]) + (DRES ? sc[NS - 1] : 0.f));
-      acc_s = fmaf(sc[1] * sc[0], r, acc_s);
-    }
-  }
-  if (failed) {
-    if (tid == 0) {
-      drain(rg, i, issued, S);
-      atomicOr(p.status, kStatusWaitTimeout);
-    }
-    return;
-  }
-  if (p.partial == nullptr) return;
-  // every column of the partial row is written by exactly one thread
-  float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = tid + k * T;
-    if (v < L.nb) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) prow[L.h + v * E + e] = acc[k][e];
-    }
-  }
-  if (L.scol >= 0) prow[L.scol] = acc_s;
-}
-
-template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
-BwdKernel pick_ring(int vpt) {
-  switch (vpt) {
-    case 1: return bwd_ragged_ring_kernel<TX, TW, 1, HAS_RSTD, DRES>;
-    case 2: return bwd_ragged_ring_kernel<TX, TW, 2, HAS_RSTD, DRES>;
-    case 4: return bwd_ragged_ring_kernel<TX, TW, 4, HAS_RSTD, DRES>;
-    default: return nullptr;
-  }
-}
-
 template <typename TX, typename TW, bool FUSED>
 FwdKernel pick_fwd(int vpt, bool pf) {
   switch (vpt) {
@@ -491,11 +315,6 @@ FwdKernel ragged_fwd(const FwdKey& k) {
 }
 template <typename TX, typename TW>
 BwdKernel ragged_bwd(const BwdKey& k) {
-  if (k.ring) {
-    if (k.dres)
-      return k.has_rstd ? pick_ring<TX, TW, true, true>(k.vpt) : pick_ring<TX, TW, false, true>(k.vpt);
-    return k.has_rstd ? pick_ring<TX, TW, true, false>(k.vpt) : pick_ring<TX, TW, false, false>(k.vpt);
-  }
   if (k.dres)
     return k.has_rstd ? pick_bwd<TX, TW, true, true>(k.vpt, k.prefetch)
                       : pick_bwd<TX, TW, false, true>(k.vpt, k.prefetch);

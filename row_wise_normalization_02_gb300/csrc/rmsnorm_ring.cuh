@@ -69,41 +69,6 @@ __device__ __forceinline__ int64_t ring_start(const Ring& rg, int S, int64_t nro
   return issued;
 }
 
-// The saved rstd of a CTA's walk rows, staged into shared memory a window of
-// kRstdWin rows at a time, each window loaded a whole window ahead into one
-// register per thread (threads 0..kRstdWin-1, so the CTA needs at least that
-// many), so that no row waits for the load of its own value.  win: 2 x
-// kRstdWin floats of shared memory (two windows: a window is rewritten only
-// after the CTA barrier of the row that follows its last reader).  Call
-// rstd_stage at every row i before the row's CTA barrier, read rstd_of after
-// it.
-constexpr int kRstdWin = 32;
-
-struct RstdStage {
-  float next;   // this thread's value of the next window, in flight
-};
-
-// Row i of the walk is row first + i * stride; nrows rows in all.
-__device__ __forceinline__ void rstd_begin(RstdStage& st, const float* rstd, int64_t first,
-                                           int64_t stride, int64_t nrows) {
-  const int t = threadIdx.x;
-  st.next = (t < kRstdWin && t < nrows) ? __ldg(rstd + first + t * stride) : 0.f;
-}
-__device__ __forceinline__ void rstd_stage(RstdStage& st, float* win, const float* rstd,
-                                           int64_t first, int64_t stride, int64_t nrows,
-                                           int64_t i) {
-  if (i % kRstdWin != 0) return;
-  const int t = threadIdx.x;
-  if (t < kRstdWin) {
-    win[((i / kRstdWin) & 1) * kRstdWin + t] = st.next;
-    const int64_t j = i + kRstdWin + t;
-    st.next = j < nrows ? __ldg(rstd + first + j * stride) : 0.f;
-  }
-}
-__device__ __forceinline__ float rstd_of(const float* win, int64_t i) {
-  return win[((i / kRstdWin) & 1) * kRstdWin + i % kRstdWin];
-}
-
 template <typename TW, int E>
 __device__ __forceinline__ void gamma_f32(const void* gamma, int v, float (&g)[E]) {
   constexpr int GW = E * (int)sizeof(TW) / 16;

@@ -26,16 +26,14 @@ def _data(M, N, seed):
     return x, dy, g
 
 
-FORCE = {"bwd_short_rows": "staged:g=8:vpt=2:st=4", "bwd_ragged": "ragged:vpt=1:st=4"}
+FORCE = {"bwd_short_rows": "staged:g=8:vpt=2:st=4"}
 
 
-@pytest.mark.parametrize("op", ["fwd", "fused", "bwd", "bwd_short_rows", "bwd_ragged"])
+@pytest.mark.parametrize("op", ["fwd", "fused", "bwd", "bwd_short_rows"])
 def test_timeout_is_reported_and_the_context_survives(debug_env, op):
     M, N, eps = 1024, 8192, float(np.float32(1e-5))
     if op == "bwd_short_rows":     # 32 rows of 128 per stage of the ring
         M, N = 8192, 128
-    if op == "bwd_ragged":         # row interiors through the ring
-        M, N = 1024, 2049
     x, dy, g = _data(M, N, seed=41)
     debug_env.set("RMSNORM_FORCE_VARIANT", FORCE.get(op, "staged:vpt=4:st=4"))
     rn.rmsnorm_check_device()                    # start from a clear flag

@@ -116,10 +116,6 @@ def test_bwd_without_dgamma(N):
     ("staged:g=8:vpt=2:cps=1", 128), ("staged:g=4:vpt=1:st=3:cps=1", 32),
     ("staged:g=16:vpt=2:st=8:cps=1", 256), ("staged:g=32:vpt=4:st=2:cps=1", 1024),
     ("staged:g=32:vpt=1:cps=1", 200),
-    # ragged rows with their interiors through the ring
-    ("ragged:vpt=1:st=4:cps=2", 2049), ("ragged:vpt=2:st=3:cps=1", 4095),
-    ("ragged:vpt=1:st=6:cps=1", 1025), ("ragged:vpt=4:st=2:cps=1", 2049),
-    ("ragged:vpt=1:st=8:cps=1", 7),
 ])
 def test_forced_variants_walk_several_rows(debug_env, force, N):
     debug_env.set("RMSNORM_FORCE_VARIANT", force)
