@@ -13,8 +13,7 @@
 // partials stay in registers, exactly as for aligned rows.
 #include <type_traits>
 
-#include "rmsnorm_device.cuh"
-#include "rmsnorm_internal.h"
+#include "rmsnorm_bwd_common.cuh"
 
 #ifndef RMSN_PAIR
 #error "compile once per dtype pair with -DRMSN_PAIR=0 (f32/f32), 1 (bf16/bf16), 2 (bf16/f32)"
@@ -230,20 +229,12 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
     TX* dxr = dx + row * (int64_t)N;
     const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
     const float xs = cur.as, ds = cur.bs;
+    float2 dot2 = make_float2(gs * ds * xs, 0.f), ss2 = make_float2(xs * xs, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) bwd_vec_sums<E, !HAS_RSTD>(cur.a[k], cur.b[k], g[k], dot2, ss2);
     float sums[K];
-    sums[0] = gs * ds * xs;
-    if (!HAS_RSTD) sums[K - 1] = xs * xs;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      float xf[E], df[E];
-      unpack(cur.a[k], xf);
-      unpack(cur.b[k], df);
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        sums[0] = fmaf(g[k][e] * df[e], xf[e], sums[0]);
-        if (!HAS_RSTD) sums[K - 1] = fmaf(xf[e], xf[e], sums[K - 1]);
-      }
-    }
+    sums[0] = dot2.x + dot2.y;
+    if (!HAS_RSTD) sums[K - 1] = ss2.x + ss2.y;
     cta_sum<K>(sums, red, parity);
     parity ^= 1;
     const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
@@ -251,19 +242,9 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdPar
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = tid + k * T;
-      if (v < L.nb) {
-        float xf[E], df[E], o[E], rf[E];
-        unpack(cur.a[k], xf);
-        unpack(cur.b[k], df);
-        if (DRES) unpack(cur.c[k], rf);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
-          if (DRES) o[e] += rf[e];
-          acc[k][e] = fmaf(df[e] * xf[e], r, acc[k][e]);
-        }
-        st_stream(dxr + L.h + v * E, pack(o));
-      }
+      if (v < L.nb)
+        st_stream(dxr + L.h + v * E, bwd_vec_apply<E, DRES>(cur.a[k], cur.b[k], cur.c[DRES ? k : 0],
+                                                            g[k], r, c, acc[k]));
     }
     if (L.scol >= 0) {
       st_scalar(dxr + L.scol, r * fmaf(-xs, c, gs * ds) + (DRES ? cur.cs : 0.f));
