@@ -730,18 +730,17 @@ cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
   return launch_in_clusters(0, kernel, grid, threads, smem, stream, args...);
 }
 
-// Stage 2 of a backward (column sums of P partial rows of nq float4): C
-// float4 columns per CTA, the largest of 8, 4, 2 that still gives two CTAs
-// per SM (two at least, so that a warp reads whole 32-byte sectors).
-cudaError_t launch_colsum(const float* part, int P, int nq, const ColSumOut& o, int device,
+// Stage 2 of a backward (column sums of P partial rows of nq float4): eight
+// float4 columns per CTA.  A wider grid (two or four columns per CTA, to
+// cover the SMs for short rows) lost badly behind the fused-add backward's
+// three-CTA-per-SM ring when launched as a programmatic dependent (32768 x
+// 4096 bf16: 259 / 219 us per call against 159 at eight columns; 161 at any
+// width without the dependent launch), and gained nothing elsewhere: stage 2
+// costs its latency, not its bytes.
+cudaError_t launch_colsum(const float* part, int P, int nq, const ColSumOut& o,
                           cudaStream_t stream) {
-  DevInfo di;
-  const cudaError_t e = device_info(device, &di);
-  if (e != cudaSuccess) return e;
-  int c = 8;
-  while (c > 2 && (nq + c - 1) / c < 2 * di.sms) c /= 2;
-  return launch(get_colsum_kernel(c), (nq + c - 1) / c, kColSumThreads, 0, stream, part, P, nq,
-                o);
+  return launch(get_colsum_kernel(), (nq + kColSumCols - 1) / kColSumCols, kColSumThreads, 0,
+                stream, part, P, nq, o);
 }
 
 // ---------------------------------------------------------------- validation
@@ -1380,7 +1379,7 @@ rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
   // stage 2: both halves of the partial rows, summed per column in a fixed order
   const float* part = static_cast<const float*>(workspace);
   e = launch_colsum(part, p.grid, 2 * ld_half / 4,
-                    ColSumOut{dgamma, dbeta, ld_half / 4, (int)N, 0}, dev, stream);
+                    ColSumOut{dgamma, dbeta, ld_half / 4, (int)N, 0}, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "LayerNorm backward stage-2 launch");
@@ -1505,7 +1504,7 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   // stage 2: the P partial rows summed per column in a fixed order
   const float* part = static_cast<const float*>(workspace);
   e = launch_colsum(part, pl.cluster > 0 ? pl.grid / pl.cluster : pl.grid, ld / 4,
-                    ColSumOut{dgamma, nullptr, ld / 4, (int)N, dgamma_bf16 ? 1 : 0}, dev, stream);
+                    ColSumOut{dgamma, nullptr, ld / 4, (int)N, dgamma_bf16 ? 1 : 0}, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(e, "backward stage-2 launch");

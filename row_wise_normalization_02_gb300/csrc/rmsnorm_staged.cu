@@ -291,8 +291,7 @@ BwdKernel staged_bwd(const BwdKey& k) {
 // float4 columns; its R = 256 / C row lanes each add the rows b = lane,
 // lane + R, ... in sequence (loads issued four ahead; the order of the adds
 // does not change), then the R lane sums meet in a fixed binary tree in
-// shared memory.  C is chosen per call so that the grid covers the GPU even
-// for short rows.  Launched as a programmatic dependent of stage 1:
+// shared memory.  Launched as a programmatic dependent of stage 1:
 // griddepcontrol.wait returns once stage 1 has completed and its writes are
 // visible.
 __device__ __forceinline__ void add4(float4& s, const float4& v) {
@@ -356,14 +355,7 @@ __global__ void __launch_bounds__(kColSumThreads)
 }  // namespace
 
 #if RMSN_PAIR == 0
-ColSumKernel get_colsum_kernel(int c) {
-  switch (c) {
-    case 2: return colsum_kernel<2>;
-    case 4: return colsum_kernel<4>;
-    case 8: return colsum_kernel<8>;
-    default: return nullptr;
-  }
-}
+ColSumKernel get_colsum_kernel() { return colsum_kernel<kColSumCols>; }
 FwdKernel get_fwd_staged_f32_f32(const FwdKey& k) { return staged_fwd<float, float>(k); }
 BwdKernel get_bwd_staged_f32_f32(const BwdKey& k) { return staged_bwd<float, float>(k); }
 #elif RMSN_PAIR == 1
