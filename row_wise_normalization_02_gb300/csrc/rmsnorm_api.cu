@@ -730,20 +730,17 @@ cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
   return launch_in_clusters(0, kernel, grid, threads, smem, stream, args...);
 }
 
-// Stage 2 of a backward (column sums of P partial rows of nq float4): C float4
-// columns per CTA, the fewest of 1, 2, 4, 8 that keeps the grid within 128
-// CTAs -- more row lanes per column for narrow rows (fewer partial rows per
-// lane, so fewer dependent L2 round trips), eight columns otherwise.  A grid
-// wider than that lost badly behind the fused-add backward's three-CTA-per-SM
-// ring when launched as a programmatic dependent (32768 x 4096 bf16: 259 /
-// 219 us per call with 512 / 256 CTAs against 159 with 128; 161 at any width
-// without the dependent launch).
+// Stage 2 of a backward (column sums of P partial rows of nq float4): eight
+// float4 columns per CTA.  A wider grid (two or four columns per CTA, to
+// cover the SMs for short rows) lost badly behind the fused-add backward's
+// three-CTA-per-SM ring when launched as a programmatic dependent (32768 x
+// 4096 bf16: 259 / 219 us per call against 159 at eight columns; 161 at any
+// width without the dependent launch), and gained nothing elsewhere: stage 2
+// costs its latency, not its bytes.
 cudaError_t launch_colsum(const float* part, int P, int nq, const ColSumOut& o,
                           cudaStream_t stream) {
-  int c = 1;
-  while (c < 8 && (nq + c - 1) / c > 128) c *= 2;
-  return launch(get_colsum_kernel(c), (nq + c - 1) / c, kColSumThreads, 0, stream, part, P, nq,
-                o);
+  return launch(get_colsum_kernel(), (nq + kColSumCols - 1) / kColSumCols, kColSumThreads, 0,
+                stream, part, P, nq, o);
 }
 
 // ---------------------------------------------------------------- validation

@@ -183,8 +183,7 @@ BwdKernel get_bwd_cluster_bf16_f32(const BwdKey& k);
 FwdKernel get_fwd_quant_f32_f32(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_bf16(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_f32(const FwdKey& k);
-// Column sum with C float4 columns per 256-thread CTA (C = 1, 2, 4 or 8).
-ColSumKernel get_colsum_kernel(int c);
+ColSumKernel get_colsum_kernel();
 
 using LnKernel = void (*)(LnParams);
 struct LnKey {
@@ -201,7 +200,9 @@ LnKernel get_ln_kernel_bf16_f32(const LnKey& k);
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;
 constexpr int kCtaMaxThreads = 512;
-// Threads of a stage-2 (column sum) CTA.
+// Stage-2 (column sum) CTA: kColSumCols float4 columns x kColSumThreads /
+// kColSumCols row lanes.
 constexpr int kColSumThreads = 256;
+constexpr int kColSumCols = 8;
 
 }  // namespace rmsn

@@ -355,15 +355,7 @@ __global__ void __launch_bounds__(kColSumThreads)
 }  // namespace
 
 #if RMSN_PAIR == 0
-ColSumKernel get_colsum_kernel(int c) {
-  switch (c) {
-    case 1: return colsum_kernel<1>;
-    case 2: return colsum_kernel<2>;
-    case 4: return colsum_kernel<4>;
-    case 8: return colsum_kernel<8>;
-    default: return nullptr;
-  }
-}
+ColSumKernel get_colsum_kernel() { return colsum_kernel<kColSumCols>; }
 FwdKernel get_fwd_staged_f32_f32(const FwdKey& k) { return staged_fwd<float, float>(k); }
 BwdKernel get_bwd_staged_f32_f32(const BwdKey& k) { return staged_bwd<float, float>(k); }
 #elif RMSN_PAIR == 1
