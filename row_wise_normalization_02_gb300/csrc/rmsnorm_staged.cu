@@ -289,8 +289,8 @@ BwdKernel staged_bwd(const BwdKey& k) {
 // Stage 2 of every backward: out_j = sum_b partial[b][j] over the P stage-1
 // CTAs, in a fixed order, fp32 (or rounded once to bf16).  A CTA owns C
 // float4 columns; its R = 256 / C row lanes each add the rows b = lane,
-// lane + R, ... in sequence (loads issued four ahead; the order of the adds
-// does not change), then the R lane sums meet in a fixed binary tree in
+// lane + R, ... in sequence (loads issued sixteen ahead; the order of the
+// adds does not change), then the R lane sums meet in a fixed binary tree in
 // shared memory.  Launched as a programmatic dependent of stage 1:
 // griddepcontrol.wait returns once stage 1 has completed and its writes are
 // visible.
@@ -312,16 +312,18 @@ __global__ void __launch_bounds__(kColSumThreads)
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (q < nq) {
     const float4* src = reinterpret_cast<const float4*>(partial) + q;
-    int b = ty;
-    constexpr int B = 4;
-    for (; b + (B - 1) * R < P; b += B * R) {
+    // up to B rows per lane in flight at once (one round trip for P <= B R),
+    // added in row order
+    constexpr int B = 16;
+    for (int b = ty; b < P; b += B * R) {
       float4 v[B];
 #pragma unroll
-      for (int u = 0; u < B; ++u) v[u] = __ldcs(src + (size_t)(b + u * R) * nq);
+      for (int u = 0; u < B; ++u)
+        if (b + u * R < P) v[u] = __ldcs(src + (size_t)(b + u * R) * nq);
 #pragma unroll
-      for (int u = 0; u < B; ++u) add4(s, v[u]);
+      for (int u = 0; u < B; ++u)
+        if (b + u * R < P) add4(s, v[u]);
     }
-    for (; b < P; b += R) add4(s, __ldcs(src + (size_t)b * nq));
   }
   sh[ty][tx] = s;
   __syncthreads();
