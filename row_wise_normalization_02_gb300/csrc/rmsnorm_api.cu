@@ -731,16 +731,20 @@ cudaError_t launch(void (*kernel)(Args...), int grid, int threads, int smem,
 }
 
 // Stage 2 of a backward (column sums of P partial rows of nq float4): eight
-// float4 columns per CTA.  A wider grid (two or four columns per CTA, to
-// cover the SMs for short rows) lost badly behind the fused-add backward's
-// three-CTA-per-SM ring when launched as a programmatic dependent (32768 x
-// 4096 bf16: 259 / 219 us per call against 159 at eight columns; 161 at any
-// width without the dependent launch), and gained nothing elsewhere: stage 2
-// costs its latency, not its bytes.
+// float4 columns per CTA (32 row lanes), or -- for the few partial rows of
+// clusters and short walks -- sixteen (P <= 256) or thirty-two (P <= 128), so
+// that lanes are not left idle over a wide grid (2048 x 65536 bf16, 36
+// partial rows: 2048 CTAs at eight columns).  A grid wider than eight columns
+// per CTA gives lost badly behind the fused-add backward's three-CTA-per-SM
+// ring when launched as a programmatic dependent (32768 x 4096 bf16: 259 /
+// 219 us per call at two / four columns against 159 at eight; 161 at any
+// width without the dependent launch); stage 2 costs its latency, not its
+// bytes.
 cudaError_t launch_colsum(const float* part, int P, int nq, const ColSumOut& o,
                           cudaStream_t stream) {
-  return launch(get_colsum_kernel(), (nq + kColSumCols - 1) / kColSumCols, kColSumThreads, 0,
-                stream, part, P, nq, o);
+  const int c = P <= 128 ? 32 : (P <= 256 ? 16 : 8);
+  return launch(get_colsum_kernel(c), (nq + c - 1) / c, kColSumThreads, 0, stream, part, P, nq,
+                o);
 }
 
 // ---------------------------------------------------------------- validation

@@ -183,7 +183,8 @@ BwdKernel get_bwd_cluster_bf16_f32(const BwdKey& k);
 FwdKernel get_fwd_quant_f32_f32(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_bf16(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_f32(const FwdKey& k);
-ColSumKernel get_colsum_kernel();
+// Column sum with C float4 columns per 256-thread CTA (C = 8, 16 or 32).
+ColSumKernel get_colsum_kernel(int c);
 
 using LnKernel = void (*)(LnParams);
 struct LnKey {
@@ -200,9 +201,7 @@ LnKernel get_ln_kernel_bf16_f32(const LnKey& k);
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;
 constexpr int kCtaMaxThreads = 512;
-// Stage-2 (column sum) CTA: kColSumCols float4 columns x kColSumThreads /
-// kColSumCols row lanes.
+// Threads of a stage-2 (column sum) CTA.
 constexpr int kColSumThreads = 256;
-constexpr int kColSumCols = 8;
 
 }  // namespace rmsn

@@ -357,7 +357,14 @@ __global__ void __launch_bounds__(kColSumThreads)
 }  // namespace
 
 #if RMSN_PAIR == 0
-ColSumKernel get_colsum_kernel() { return colsum_kernel<kColSumCols>; }
+ColSumKernel get_colsum_kernel(int c) {
+  switch (c) {
+    case 8: return colsum_kernel<8>;
+    case 16: return colsum_kernel<16>;
+    case 32: return colsum_kernel<32>;
+    default: return nullptr;
+  }
+}
 FwdKernel get_fwd_staged_f32_f32(const FwdKey& k) { return staged_fwd<float, float>(k); }
 BwdKernel get_bwd_staged_f32_f32(const BwdKey& k) { return staged_bwd<float, float>(k); }
 #elif RMSN_PAIR == 1
