@@ -67,9 +67,16 @@ __device__ __forceinline__ void bload_aligned(BSlice<VPT, DRES>& s, const BwdPar
 // shared memory (in group order) at the end.
 template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool PF, bool DRES>
 __device__ __forceinline__ void bwd_subwarp_body(const BwdParams& p) {
-  pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int RPC = kSubwarpThreads / G;
+  {  // the first two iterations' rows into L2 while the previous kernel ends
+    const size_t rb = (size_t)p.N * sizeof(TX);
+    const void* r = DRES ? p.dres : nullptr;
+    const int64_t b0 = (int64_t)blockIdx.x * RPC, st = (int64_t)gridDim.x * RPC;
+    l2_warm(p.x, p.dy, r, b0, RPC, p.M, rb);
+    if (PF) l2_warm(p.x, p.dy, r, b0 + st, RPC, p.M, rb);
+  }
+  pdl_begin();
   extern __shared__ float4 smem4[];
   float* sacc = reinterpret_cast<float*>(smem4);   // [RPC][nvec * E]
   const int lane = threadIdx.x % G, grp = threadIdx.x / G;
@@ -184,10 +191,16 @@ __global__ void __launch_bounds__(kSubwarpThreads, 2) bwd_subwarp_kernel_2cta(co
 template <typename TX, typename TW, int G, int VPT, bool HAS_RSTD, bool DRES>
 __global__ void __launch_bounds__(kSubwarpThreads)
     bwd_rows_staged_kernel(const BwdParams p) {
-  pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int RPC = kSubwarpThreads / G;
   constexpr int NS = DRES ? 3 : 2;
+  {  // the rows of the first two iterations into L2 while the previous kernel ends
+    const size_t rb = (size_t)p.N * sizeof(TX);
+    const int64_t b0 = (int64_t)blockIdx.x * RPC, st = (int64_t)gridDim.x * RPC;
+    l2_warm(p.x, p.dy, DRES ? p.dres : nullptr, b0, RPC, p.M, rb);
+    l2_warm(p.x, p.dy, DRES ? p.dres : nullptr, b0 + st, RPC, p.M, rb);
+  }
+  pdl_begin();
   extern __shared__ __align__(128) unsigned char smem[];
   const Ring rg = ring_of(smem);
   const int lane = threadIdx.x % G, grp = threadIdx.x / G, tid = threadIdx.x;

@@ -264,6 +264,22 @@ __device__ __forceinline__ void l2_prefetch_rows(const void* a, int64_t first, i
   bulk_prefetch_l2(static_cast<const char*>(a) + first * rb, (uint32_t)(n * rb));
 }
 
+// Before a kernel waits for the previous one (pdl_begin), thread 0 may ask
+// for the first rows the CTA will read to be brought into L2.  A prefetch
+// returns nothing to the program, and L2 is where every write of the
+// previous kernel lands, so reads after the wait still see those writes: the
+// request only starts the DRAM traffic of the CTA's first rows while the
+// previous kernel's last CTAs finish.  Rows [first, first + n) of up to three
+// row-major operands with rows of rb bytes (16-byte aligned; null operands
+// skipped), clipped to M rows.
+__device__ __forceinline__ void l2_warm(const void* a, const void* b, const void* c,
+                                        int64_t first, int64_t n, int64_t M, size_t rb) {
+  if (threadIdx.x != 0) return;
+  if (a) l2_prefetch_rows(a, first, n, M, rb);
+  if (b) l2_prefetch_rows(b, first, n, M, rb);
+  if (c) l2_prefetch_rows(c, first, n, M, rb);
+}
+
 // Non-blocking test of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;

@@ -27,10 +27,17 @@ namespace {
 template <typename TX, typename TW, int G, int VPT, bool FUSED, bool PF>
 __global__ void __launch_bounds__(kSubwarpThreads)
     fwd_subwarp_kernel(const FwdParams p) {
-  pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW;
   constexpr int RPC = kSubwarpThreads / G;
+  {  // the first two iterations' rows into L2 while the previous kernel ends
+    const size_t rb = (size_t)p.N * sizeof(TX);
+    const void* r = FUSED ? p.residual : nullptr;
+    const int64_t b0 = (int64_t)blockIdx.x * RPC, st = (int64_t)gridDim.x * RPC;
+    l2_warm(p.x, r, nullptr, b0, RPC, p.M, rb);
+    if (PF) l2_warm(p.x, r, nullptr, b0 + st, RPC, p.M, rb);
+  }
+  pdl_begin();
   const int lane = threadIdx.x % G, grp = threadIdx.x / G;
 
   uint4 gw[VPT][GW];
@@ -76,6 +83,12 @@ __global__ void __launch_bounds__(kSubwarpThreads)
 // vectors in registers for the whole kernel.
 template <typename TX, typename TW, int VPT, bool FUSED, bool PF>
 __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cta_kernel(const FwdParams p) {
+  {  // the first two rows into L2 while the previous kernel ends
+    const size_t rb = (size_t)p.N * sizeof(TX);
+    const void* r = FUSED ? p.residual : nullptr;
+    l2_warm(p.x, r, nullptr, blockIdx.x, 1, p.M, rb);
+    if (PF) l2_warm(p.x, r, nullptr, (int64_t)blockIdx.x + gridDim.x, 1, p.M, rb);
+  }
   pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW;
