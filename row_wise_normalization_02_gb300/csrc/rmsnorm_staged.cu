@@ -136,12 +136,6 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int K = HAS_RSTD ? 1 : 2;
   constexpr int NS = DRES ? 3 : 2;
-  {  // the first two rows of the walk into L2 while the previous kernel ends
-    const size_t rb = (size_t)p.N * sizeof(TX);
-    const void* r = DRES ? p.dres : nullptr;
-    l2_warm(p.x, p.dy, r, blockIdx.x, 1, p.M, rb);
-    l2_warm(p.x, p.dy, r, (int64_t)blockIdx.x + gridDim.x, 1, p.M, rb);
-  }
   pdl_begin();
   extern __shared__ __align__(128) unsigned char smem[];
   const Ring rg = ring_of(smem);
