@@ -141,6 +141,20 @@ __device__ __forceinline__ SliceOf slice_of(int slice, int nvec, uint32_t rank) 
 // Forward / fused add: the slice in registers, next-row prefetch (PF).
 template <typename TX, typename TW, int VPT, bool FUSED, bool PF>
 __global__ void __launch_bounds__(kCtaMaxThreads) fwd_cluster_kernel(const FwdParams p0) {
+  if (threadIdx.x == 0) {   // this CTA's slice of its first two rows into L2 before the wait
+    const uint32_t C0 = cluster_ctas();
+    const SliceOf s0 = slice_of(p0.slice, p0.nvec, cluster_rank());
+    const size_t rb0 = (size_t)p0.N * sizeof(TX), o0 = (size_t)s0.v0 * 16;
+    const int64_t r0 = blockIdx.x / C0, st0 = gridDim.x / C0;
+    for (int k = 0; k < 2 && s0.nv > 0; ++k) {
+      const int64_t row = r0 + k * st0;
+      if (row >= p0.M) break;
+      bulk_prefetch_l2(static_cast<const char*>(p0.x) + row * rb0 + o0, (uint32_t)s0.nv * 16);
+      if (FUSED)
+        bulk_prefetch_l2(static_cast<const char*>(p0.residual) + row * rb0 + o0,
+                         (uint32_t)s0.nv * 16);
+    }
+  }
   pdl_begin();
   using Cf = Cfg<TX, TW>;
   constexpr int E = Cf::E, GW = Cf::GW;

@@ -234,6 +234,13 @@ __device__ __forceinline__ void l2_ahead(const void* a, const LnParams& p, int64
 template <typename TX, typename TW, int G, int VPT, bool PF>
 __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
     ln_fwd_kernel(const LnParams p) {
+  {  // the first two iterations' rows into L2 while the previous kernel ends
+    const int rpc0 = G ? kSubwarpThreads / G : 1;
+    const int64_t b0 = (int64_t)blockIdx.x * rpc0, st = (int64_t)gridDim.x * rpc0;
+    const size_t rb0 = (size_t)p.N * sizeof(TX);
+    l2_warm(p.x, nullptr, nullptr, b0, rpc0, p.M, rb0);
+    if (PF) l2_warm(p.x, nullptr, nullptr, b0 + st, rpc0, p.M, rb0);
+  }
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   __shared__ float red[128];
@@ -404,6 +411,13 @@ __device__ __forceinline__ void write_partials(float* prow, int ld_half,
 template <typename TX, typename TW, int G, int VPT, bool PF>
 __global__ void __launch_bounds__(G ? kSubwarpThreads : kCtaMaxThreads)
     ln_bwd_kernel(const LnParams p) {
+  {  // the first two iterations' rows into L2 while the previous kernel ends
+    const int rpc0 = G ? kSubwarpThreads / G : 1;
+    const int64_t b0 = (int64_t)blockIdx.x * rpc0, st = (int64_t)gridDim.x * rpc0;
+    const size_t rb0 = (size_t)p.N * sizeof(TX);
+    l2_warm(p.x, p.dy, nullptr, b0, rpc0, p.M, rb0);
+    if (PF) l2_warm(p.x, p.dy, nullptr, b0 + st, rpc0, p.M, rb0);
+  }
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   __shared__ float red[128];

@@ -305,6 +305,14 @@ constexpr int quant_max_regs() {
 template <typename TX, typename TW, int G, int VPT, bool FUSED, int OUT, bool PF>
 __global__ void __maxnreg__((quant_max_regs<G, VPT, FUSED, OUT, PF>()))
     fwd_quant_kernel(const FwdParams p) {
+  {  // the first two iterations' rows into L2 while the previous kernel ends
+    const int rpc0 = G ? kSubwarpThreads / G : 1;
+    const int64_t b0 = (int64_t)blockIdx.x * rpc0, st = (int64_t)gridDim.x * rpc0;
+    const size_t rb0 = (size_t)p.N * sizeof(TX);
+    const void* r = FUSED ? p.residual : nullptr;
+    l2_warm(p.x, r, nullptr, b0, rpc0, p.M, rb0);
+    if (PF) l2_warm(p.x, r, nullptr, b0 + st, rpc0, p.M, rb0);
+  }
   pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW;

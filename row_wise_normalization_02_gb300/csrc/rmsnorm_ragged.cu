@@ -118,6 +118,14 @@ __device__ __forceinline__ void l2_prefetch_row_interior(const void* a, int64_t 
 // Forward / fused add (b = residual, in r, out h).
 template <typename TX, typename TW, int VPT, bool FUSED, bool PF>
 __global__ void __launch_bounds__(kCtaMaxThreads) fwd_ragged_kernel(const FwdParams p) {
+  if (threadIdx.x == 0) {   // the interiors of the first two rows into L2 before the wait
+    const Walk w0 = walk_of(p.period, p.M);
+    const size_t rb0 = (size_t)p.N * sizeof(TX);
+    for (int k = 0; k < 2; ++k) {
+      l2_prefetch_row_interior(p.x, w0.first + k * w0.stride, p.M, rb0);
+      if (FUSED) l2_prefetch_row_interior(p.residual, w0.first + k * w0.stride, p.M, rb0);
+    }
+  }
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   extern __shared__ float4 smem4[];
@@ -194,6 +202,15 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_ragged_kernel(const FwdPar
 // Backward (a = x, b = dy; fused-add backward: c = dres, added to dx).
 template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool PF, bool DRES>
 __global__ void __launch_bounds__(kCtaMaxThreads) bwd_ragged_kernel(const BwdParams p) {
+  if (threadIdx.x == 0) {   // the interiors of the first two rows into L2 before the wait
+    const Walk w0 = walk_of(p.period, p.M);
+    const size_t rb0 = (size_t)p.N * sizeof(TX);
+    for (int k = 0; k < 2; ++k) {
+      l2_prefetch_row_interior(p.x, w0.first + k * w0.stride, p.M, rb0);
+      l2_prefetch_row_interior(p.dy, w0.first + k * w0.stride, p.M, rb0);
+      if (DRES) l2_prefetch_row_interior(p.dres, w0.first + k * w0.stride, p.M, rb0);
+    }
+  }
   pdl_begin();
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int K = HAS_RSTD ? 1 : 2;
