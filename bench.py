@@ -606,9 +606,23 @@ def device_sets(wl, inp, dev, l2_bytes, rn):
     host = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v)
             for k, v in inp.items()}
     M, N = wl.M, wl.N
+    off = dict(wl.offsets)
+
+    def placed(k, v):
+        # an operand `off[k]` bytes past a 16-byte boundary: a view into a
+        # slightly larger buffer (allocations start on 256 bytes)
+        if not off.get(k):
+            return v.to(dev)
+        e = v.element_size()
+        assert off[k] % e == 0
+        buf = torch.empty(v.numel() + 16 // e, dtype=v.dtype, device=dev)
+        view = buf[off[k] // e: off[k] // e + v.numel()].view(v.shape)
+        view.copy_(v.to(dev))
+        return view
+
     sets = []
     for _ in range(nsets):
-        d = {k: v.to(dev) for k, v in host.items()}
+        d = {k: placed(k, v) for k, v in host.items()}
         if wl.op.startswith("ln_"):
             d["y"] = torch.empty((M, N), dtype=act, device=dev)
             d["mean"] = torch.empty(M, dtype=torch.float32, device=dev)
@@ -733,7 +747,7 @@ def run_sweep(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = args.workloads.split(",") if args.workloads else [
         n for n, w in si.WORKLOADS.items()
-        if "sweep" in w.tags or "headline" in w.tags or "next" in w.tags]
+        if "sweep" in w.tags or "headline" in w.tags or "next" in w.tags or "mixed" in w.tags]
     for name in names:
         wl = si.WORKLOADS[name]
         inp = si.make_inputs(wl)
@@ -763,8 +777,9 @@ def run_sweep(args):
         med = statistics.median(us)
         byts = alg_bytes(wl)
         print(json.dumps({"workload": name, "op": wl.op, "M": wl.M, "N": wl.N,
-                          "variant": rn.rmsnorm_describe_plan(_op_code(wl.op), wl.M, wl.N,
-                                                              wl.x_dtype, wl.w_dtype),
+                          "variant": rn.rmsnorm_describe_plan(
+                              _op_code(wl.op), wl.M, wl.N, wl.x_dtype, wl.w_dtype,
+                              "mixed" if wl.offsets else True),
                           "us_per_call": round(med, 2), "rounds_us": [round(u, 2) for u in us],
                           "min_us": round(min(us), 2),
                           "spread": round((max(us) - min(us)) / med, 4),

@@ -17,7 +17,11 @@
  *  - Dtypes: output dtype = x_dtype; rstd and dgamma are always fp32.
  *    Supported (x_dtype, w_dtype) pairs: (F32, F32), (BF16, BF16), (BF16, F32).
  *  - Alignment: each pointer must be aligned to its element size; 16-byte
- *    alignment of the rows is NOT required (ragged rows take a slower path).
+ *    alignment of the rows is NOT required.  RMSNorm rows that do not start
+ *    on 16 bytes, or inputs (x, dy) whose start differs modulo 16 from the
+ *    outputs', take vectorised kernels with scalar row ends (slower than
+ *    aligned rows); outputs that disagree with each other modulo 16 (y and
+ *    the fused add's residual, dx and dres) take a scalar path.
  *  - Sizes: M == 0 returns RMSNORM_OK without launching; M < 0, N < 1,
  *    N > 2^30, or eps < 0 / NaN return RMSNORM_ERR_INVALID_ARG.
  *  - Aliasing: only fused-add's `residual` is in-out.  Any other overlap of
@@ -317,8 +321,9 @@ const char* rmsnorm_status_string(rmsnorm_status_t status);
  * forward, 6 fused-add FP8 forward, 7 NVFP4 forward, 8 fused-add NVFP4,
  * 9 LayerNorm forward, 10 LayerNorm backward.  aligned16:
  * nonzero when all operand base pointers (and, for op 4, all strides) are
- * 16-byte aligned.  Returns RMSNORM_OK or an argument error; launches
- * nothing.
+ * 16-byte aligned; for ops 0-3, 2 describes outputs on 16 bytes with x (and
+ * dy) off them (for example x a view at an odd element offset).  Returns
+ * RMSNORM_OK or an argument error; launches nothing.
  */
 rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
                                        rmsnorm_dtype_t w_dtype, int aligned16, int device,

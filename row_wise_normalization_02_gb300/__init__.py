@@ -264,8 +264,11 @@ def rmsnorm_status_string(status: int) -> str:
 
 
 def rmsnorm_describe_plan(op, M, N, x_dtype, w_dtype, aligned16=True, device=-1) -> str:
+    """aligned16: True / False, or "mixed" (ops 0-3: outputs on 16 bytes, x and
+    dy off them)."""
     buf = ctypes.create_string_buffer(256)
+    a = 2 if aligned16 == "mixed" else (1 if aligned16 else 0)
     _check(load_library().rmsnorm_describe_plan(op, M, N, _dt(x_dtype), _dt(w_dtype),
-                                                1 if aligned16 else 0, device, buf, 256),
+                                                a, device, buf, 256),
            "rmsnorm_describe_plan")
     return buf.value.decode()

@@ -1,7 +1,8 @@
 """Build librmsnorm_gb300.so in-tree with nvcc for sm_103a.
 
-Twenty-two translation units (forward, backward, staged, ragged, cluster,
-quantised-output and LayerNorm kernels once per dtype pair, plus the C ABI)
+Twenty-five translation units (forward, backward, staged, ragged, mixed-alignment
+ragged, cluster, quantised-output and LayerNorm kernels once per dtype pair, plus
+the C ABI)
 compile in parallel, then link into one shared library with the CUDA runtime
 linked statically.  Rebuilds only when a source is newer than the library.
 """
@@ -35,6 +36,9 @@ UNITS = [("rmsnorm_fwd.cu", ["-DRMSN_PAIR=0"], "fwd_p0.o"),
          ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=0"], "ragged_p0.o"),
          ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=1"], "ragged_p1.o"),
          ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=2"], "ragged_p2.o"),
+         ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=0", "-DRMSN_MIX=1"], "ragged_mix_p0.o"),
+         ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=1", "-DRMSN_MIX=1"], "ragged_mix_p1.o"),
+         ("rmsnorm_ragged.cu", ["-DRMSN_PAIR=2", "-DRMSN_MIX=1"], "ragged_mix_p2.o"),
          ("rmsnorm_quant.cu", ["-DRMSN_PAIR=0"], "quant_p0.o"),
          ("rmsnorm_quant.cu", ["-DRMSN_PAIR=1"], "quant_p1.o"),
          ("rmsnorm_quant.cu", ["-DRMSN_PAIR=2"], "quant_p2.o"),

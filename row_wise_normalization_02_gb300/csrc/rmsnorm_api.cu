@@ -50,9 +50,12 @@ FwdKernel fwd_kernel(const FwdKey& k) {
     return nullptr;
   }
   if (k.family == kRagged) {
-    if (k.xd == kF32 && k.wd == kF32) return get_fwd_ragged_f32_f32(k);
-    if (k.xd == kBF16 && k.wd == kBF16) return get_fwd_ragged_bf16_bf16(k);
-    if (k.xd == kBF16 && k.wd == kF32) return get_fwd_ragged_bf16_f32(k);
+    if (k.xd == kF32 && k.wd == kF32)
+      return k.mix ? get_fwd_ragged_mix_f32_f32(k) : get_fwd_ragged_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16)
+      return k.mix ? get_fwd_ragged_mix_bf16_bf16(k) : get_fwd_ragged_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32)
+      return k.mix ? get_fwd_ragged_mix_bf16_f32(k) : get_fwd_ragged_bf16_f32(k);
     return nullptr;
   }
   if (k.family == kCluster) {
@@ -71,9 +74,12 @@ FwdKernel fwd_kernel(const FwdKey& k) {
 }
 BwdKernel bwd_kernel(const BwdKey& k) {
   if (k.family == kRagged) {
-    if (k.xd == kF32 && k.wd == kF32) return get_bwd_ragged_f32_f32(k);
-    if (k.xd == kBF16 && k.wd == kBF16) return get_bwd_ragged_bf16_bf16(k);
-    if (k.xd == kBF16 && k.wd == kF32) return get_bwd_ragged_bf16_f32(k);
+    if (k.xd == kF32 && k.wd == kF32)
+      return k.mix ? get_bwd_ragged_mix_f32_f32(k) : get_bwd_ragged_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16)
+      return k.mix ? get_bwd_ragged_mix_bf16_bf16(k) : get_bwd_ragged_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32)
+      return k.mix ? get_bwd_ragged_mix_bf16_f32(k) : get_bwd_ragged_bf16_f32(k);
     return nullptr;
   }
   if (k.family == kCluster) {
@@ -224,6 +230,7 @@ struct Plan {
   int min_rows = 0;          // backward: rows per CTA at least this many (bounds
                              // the dgamma partial rows), unless below 1 CTA/SM
   int period = 1;            // kRagged: the grid is a multiple of it
+  bool mix = false;          // kRagged: inputs off the outputs' alignment
   int cta_per_sm_cap = 0;    // 0: occupancy limit
   int l2_ahead = 0;          // LayerNorm register kernels: L2 lookahead in iterations
   int cluster = 0;           // kCluster: CTAs per cluster (one row per cluster)
@@ -305,13 +312,20 @@ bool cluster_shape(bool bwd, int nvec, int cl, int* c_out, int* slice, int* vpt,
   return true;
 }
 
+// Vectors a ragged CTA of `threads` holds at `vpt` per thread: 32 per warp
+// and slot, 31 with mixed alignment (lane 31 carries the next warp's chunk).
+int64_t ragged_capacity(int threads, int vpt, bool mix) {
+  return (int64_t)(threads / 32) * (mix ? 31 : 32) * vpt;
+}
+
 // Vectors per thread (1, 2 or 4) and CTA size for a ragged row of at most
-// nvec vectors; false when the row needs more than 4 x 512.
-bool ragged_shape(int nvec, int* vpt, int* threads) {
+// nvec vectors; false when the row needs more than 4 vectors x 512 threads.
+bool ragged_shape(int nvec, bool mix, int* vpt, int* threads) {
   static const int pref[] = {2, 4, 1};
+  const int per_warp = mix ? 31 : 32;
   for (int i = 0; i < 3; ++i) {
     const int v = pref[i];
-    int t = round_up((nvec + v - 1) / v, 32);
+    int t = 32 * ((nvec + per_warp * v - 1) / (per_warp * v));
     if (t < 64) t = 64;
     if (t <= kCtaMaxThreads) {
       *vpt = v;
@@ -408,13 +422,21 @@ long long wait_limit() { return g_env.wait_limit; }
 
 // Choose the variant.  aligned16: all base pointers 16-byte aligned;
 // same_mod16: all activation base pointers agree modulo 16 bytes.
+// mix_ok: the outputs agree modulo 16 (y with h over the residual; dx with
+// dres) while an input (x, dy) need not -- the ragged kernels' mixed form;
+// frame16: the outputs and gamma are moreover on 16 bytes.
 rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligned16,
-                           bool same_mod16, bool has_rstd, Plan* pl) {
+                           bool same_mod16, bool has_rstd, Plan* pl, bool mix_ok = false,
+                           bool frame16 = false) {
   const bool bwd = op == kBwd || op == kFusedBwd;
   const bool dres = op == kFusedBwd;
   const int E = per_vec(xd);
   const bool rows_aligned = aligned16 && ((int64_t)N * esize(xd)) % 16 == 0;
-  const int nvec = rows_aligned ? N / E : 0;
+  // inputs off the outputs' alignment while the outputs' rows (and gamma) lie
+  // on 16 bytes: the backward's ring copies each input row's enclosing span
+  const bool mixed_rows =
+      !same_mod16 && mix_ok && frame16 && ((int64_t)N * esize(xd)) % 16 == 0;
+  const int nvec = rows_aligned || mixed_rows ? N / E : 0;
   Plan p;
   if (rows_aligned && nvec <= 128) {
     p.family = kSubwarp;
@@ -465,11 +487,26 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (!cluster_shape(false, nvec, 0, &p.cluster, &p.slice, &p.vpt, &p.threads))
       p.family = kGeneric;
     p.prefetch = p.vpt <= 4;
-  } else if (same_mod16 && N <= kRaggedMaxN) {
+  } else if (mixed_rows && bwd && nvec > 128 && nvec <= 4 * kCtaMaxThreads &&
+             cta_shape(kBwd, nvec, &p.vpt, &p.threads) && p.vpt <= 4) {
+    // as the aligned backward, the shifted inputs' rows arriving as their
+    // enclosing 16-byte spans (4096 and 8192 bf16: see the measurements)
+    p.family = kStaged;
+    p.mix = true;
+    p.stages = dres && kStagedHeader + 3 * 3 * ((int64_t)N * esize(xd) + 16) <= kStagedSmemMax
+                   ? 3 : 2;
+  } else if ((same_mod16 || mix_ok) && N <= kRaggedMaxN) {
+    // rows off 16 bytes, or inputs off the outputs' alignment (x a view at an
+    // odd element offset, say): vector body plus scalar head and tail
     p.family = kRagged;
-    if (!ragged_shape(N / E + 1, &p.vpt, &p.threads)) p.family = kGeneric;
+    p.mix = !same_mod16;
+    if (!ragged_shape(N / E + 1, p.mix, &p.vpt, &p.threads)) p.family = kGeneric;
     p.period = ragged_period((int64_t)N * esize(xd));
-    p.prefetch = p.vpt <= 2;
+    // next-row prefetch up to 4 vectors per thread for the plain forward
+    // (64 / 72 registers with packed gamma), up to 2 for the others -- but not
+    // for the mixed fused add, whose extra CTAs beat it (32768 x 4096 bf16,
+    // x off 16 bytes: 0.96 of the copy peak without, 0.90 with)
+    p.prefetch = op == kFwd || (p.vpt <= 2 && !(op == kFused && p.mix));
   } else {
     p.family = kGeneric;
   }
@@ -477,6 +514,8 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.threads = 256;
     p.g = p.vpt = 0;
     p.prefetch = false;
+    p.mix = false;
+    p.period = 1;
   }
 
   const Force& f = read_force();
@@ -497,13 +536,15 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (!f.threads) p.threads = round_up((nvec + p.vpt - 1) / (p.vpt ? p.vpt : 1), 32);
       if (p.vpt < 1 || (int64_t)p.threads * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
     } else if (p.family == kRagged) {
-      if (!same_mod16 || N > kRaggedMaxN) return RMSNORM_ERR_INVALID_ARG;
+      if (!(same_mod16 || mix_ok) || N > kRaggedMaxN) return RMSNORM_ERR_INVALID_ARG;
+      p.mix = !same_mod16;
       if (!p.vpt) p.vpt = 2;
       if (!f.threads) {
-        p.threads = round_up((N / E + 1 + p.vpt - 1) / p.vpt, 32);
+        const int per = (p.mix ? 31 : 32) * p.vpt;
+        p.threads = 32 * ((N / E + 1 + per - 1) / per);
         if (p.threads < 64) p.threads = 64;
       }
-      if ((int64_t)p.threads * p.vpt < N / E) return RMSNORM_ERR_INVALID_ARG;
+      if (ragged_capacity(p.threads, p.vpt, p.mix) < N / E) return RMSNORM_ERR_INVALID_ARG;
       p.period = ragged_period((int64_t)N * esize(xd));
     } else if (p.family == kStaged && bwd && (f.g > 0 || (f.family < 0 && p.g > 0))) {
       // short backward rows through the ring: g lanes per row, 256 / g rows
@@ -516,7 +557,8 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (f.st > 0) p.stages = f.st;
       else if (f.family == kStaged) p.stages = 0;   // as many as the budget holds
     } else if (p.family == kStaged) {
-      if (!rows_aligned) return RMSNORM_ERR_INVALID_ARG;
+      if (!rows_aligned && !(mixed_rows && bwd)) return RMSNORM_ERR_INVALID_ARG;
+      p.mix = !rows_aligned;
       p.g = 0;
       if (!p.vpt) p.vpt = 4;
       if (!f.threads) p.threads = round_up((nvec + p.vpt - 1) / p.vpt, 32);
@@ -547,6 +589,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (p.family != kCluster) p.cluster = p.slice = 0;
     if (p.family != kSubwarp && !(p.family == kStaged && p.g > 0)) p.rows_per_cta = 1;
     if (p.family != kRagged) p.period = 1;
+    if (p.family != kRagged && !(p.family == kStaged && p.g == 0)) p.mix = false;
     if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32) return RMSNORM_ERR_INVALID_ARG;
   }
 
@@ -573,7 +616,8 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     const int ns = op == kFwd ? 1 : (op == kFusedBwd ? 3 : 2);
     // a stage holds one row per operand, or the rows_per_cta rows of a CTA
     // iteration of short rows
-    const int64_t stage_bytes = (int64_t)ns * N * esize(xd) * (p.g > 0 ? p.rows_per_cta : 1);
+    const int64_t stage_bytes =
+        (int64_t)ns * ((int64_t)N * esize(xd) + (p.mix ? 16 : 0)) * (p.g > 0 ? p.rows_per_cta : 1);
     if (p.stages <= 0) {
       int64_t st = (kStagedSmemBudget - kStagedHeader) / stage_bytes;
       if (st < 2) st = (kStagedSmemMax - kStagedHeader) / stage_bytes;
@@ -592,7 +636,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     const Force& fr = read_force();
     if (fr.on && fr.mr >= 0) p.min_rows = fr.mr;
     if (dres && p.family == kCta) return RMSNORM_ERR_INVALID_ARG;
-    BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch, dres};
+    BwdKey k{xd, wd, p.family, p.g, p.vpt, has_rstd, p.acc_smem, p.prefetch, dres, p.mix};
     p.bwd = bwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.bwd);
     const int ld = round_up(N, 4);
@@ -607,6 +651,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     } else if (p.family != kStaged) p.smem = 0;
   } else {
     FwdKey k{xd, wd, p.family, p.g, p.vpt, op == kFused, p.prefetch, false};
+    k.mix = p.mix;
     p.fwd = fwd_kernel(k);
     p.fn = reinterpret_cast<const void*>(p.fwd);
     if (p.family == kCta) p.smem = 256;
@@ -687,8 +732,8 @@ void describe(int op, const Plan& p, char* buf, size_t len) {
   if (p.l2_ahead > 0) snprintf(l2, sizeof l2, "/l2ahead%d", p.l2_ahead);
   char cl[32] = "";
   if (p.cluster > 0) snprintf(cl, sizeof cl, "/cl%d/slice%d", p.cluster, p.slice);
-  snprintf(buf, len, "%s/%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d%s%s", ops[op],
-           family_name(p.family), p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
+  snprintf(buf, len, "%s/%s%s/g%d/vpt%d/t%d/pf%d/st%d/per%d%s/grid%d/smem%d%s%s", ops[op],
+           family_name(p.family), p.mix ? "_mix" : "", p.g, p.vpt, p.threads, p.prefetch ? 1 : 0, p.stages, p.period,
            bwd ? (p.acc_smem ? "/acc_smem" : "/acc_reg") : "", p.grid, p.smem, l2, cl);
 }
 
@@ -791,14 +836,17 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
     return RMSNORM_ERR_INVALID_ARG;
 
   const uintptr_t mx = reinterpret_cast<uintptr_t>(x) & 15;
-  bool same = (reinterpret_cast<uintptr_t>(y) & 15) == mx;
-  if (op == kFused) same = same && (reinterpret_cast<uintptr_t>(residual) & 15) == mx;
+  const uintptr_t my = reinterpret_cast<uintptr_t>(y) & 15;
+  // the outputs (y, and h over the residual) agree modulo 16; x may not
+  const bool out_same = op != kFused || (reinterpret_cast<uintptr_t>(residual) & 15) == my;
+  const bool same = out_same && my == mx;
   const bool aligned16 = same && mx == 0 && aligned_to(gamma, 16);
 
   int dev;
   if ((st = current_device(&dev)) != RMSNORM_OK) return st;
   Plan pl;
-  if ((st = make_plan(op, M, (int)N, xd, wd, aligned16, same, false, &pl)) != RMSNORM_OK)
+  if ((st = make_plan(op, M, (int)N, xd, wd, aligned16, same, false, &pl, out_same)) !=
+      RMSNORM_OK)
     return st;
   unsigned* status = nullptr;
   if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
@@ -820,6 +868,7 @@ rmsnorm_status_t fwd_impl(int op, const void* x, void* residual, const void* gam
   prm.period = pl.period;
   prm.l2_rows = pl.l2_ahead;
   prm.slice = pl.slice;
+  prm.x_shift = (int)((mx - my) & 15);
   const cudaError_t e =
       launch_in_clusters(pl.cluster, pl.fwd, pl.grid, pl.threads, pl.smem, stream, prm);
   if (e != cudaSuccess) {
@@ -1458,13 +1507,16 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   }
 
   const uintptr_t mx = reinterpret_cast<uintptr_t>(x) & 15;
-  const bool same = (reinterpret_cast<uintptr_t>(dy) & 15) == mx &&
-                    (reinterpret_cast<uintptr_t>(dx) & 15) == mx &&
-                    (!dres || (reinterpret_cast<uintptr_t>(dres) & 15) == mx);
+  const uintptr_t mdy = reinterpret_cast<uintptr_t>(dy) & 15;
+  const uintptr_t mdx = reinterpret_cast<uintptr_t>(dx) & 15;
+  // the output dx (and dres, read where dh is written) set the alignment
+  const bool out_same = !dres || (reinterpret_cast<uintptr_t>(dres) & 15) == mdx;
+  const bool same = out_same && mdy == mx && mdx == mx;
   const bool aligned16 = same && mx == 0 && aligned_to(gamma, 16);
   Plan pl;
+  const bool frame16 = mdx == 0 && aligned_to(gamma, 16);
   if ((st = make_plan(dres ? kFusedBwd : kBwd, M, (int)N, xd, wd, aligned16, same,
-                      rstd != nullptr, &pl)) != RMSNORM_OK)
+                      rstd != nullptr, &pl, out_same, frame16)) != RMSNORM_OK)
     return st;
   unsigned* status = nullptr;
   if ((st = size_grid(&pl, M, dev, &status)) != RMSNORM_OK) return st;
@@ -1498,6 +1550,8 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   prm.period = pl.period;
   prm.l2_rows = pl.l2_ahead;
   prm.slice = pl.slice;
+  prm.x_shift = (int)((mx - mdx) & 15);
+  prm.dy_shift = (int)((mdy - mdx) & 15);
   cudaError_t e =
       launch_in_clusters(pl.cluster, pl.bwd, pl.grid, pl.threads, pl.smem, stream, prm);
   if (e != cudaSuccess) {
@@ -1748,6 +1802,10 @@ rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dty
     if ((st = strided_plan(N, (int)x_dtype, (int)w_dtype,
                            aligned16 != 0 && (N * esize((int)x_dtype)) % 16 == 0, &pl)) !=
         RMSNORM_OK)
+      return st;
+  } else if (aligned16 == 2) {   // outputs on 16 bytes, x (and dy) off them
+    if ((st = make_plan(op, M, (int)N, (int)x_dtype, (int)w_dtype, false, false, true, &pl,
+                        true, true)) != RMSNORM_OK)
       return st;
   } else if ((st = make_plan(op, M, (int)N, (int)x_dtype, (int)w_dtype, aligned16 != 0,
                              aligned16 != 0, true, &pl)) != RMSNORM_OK) {

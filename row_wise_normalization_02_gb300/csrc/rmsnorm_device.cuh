@@ -110,6 +110,23 @@ __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
   return v;
 }
 
+// The 16 bytes that start s bytes (0 <= s < 16) into the 32-byte pair
+// (lo, hi) of consecutive aligned chunks.  Words are picked by the two bits of
+// s / 4 (selects, no indexing of a register array) and bytes by one byte
+// permute per word; s == 0 gives lo.
+__device__ __forceinline__ uint4 realign_pair(const uint4& lo, const uint4& hi, int s) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const int q = s >> 2;
+  uint32_t t[6], u[5];
+#pragma unroll
+  for (int i = 0; i < 6; ++i) t[i] = (q & 2) ? w[i + 2] : w[i];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) u[i] = (q & 1) ? t[i + 1] : t[i];
+  const uint32_t sel = 0x3210u + 0x1111u * (uint32_t)(s & 3);
+  return make_uint4(__byte_perm(u[0], u[1], sel), __byte_perm(u[1], u[2], sel),
+                    __byte_perm(u[2], u[3], sel), __byte_perm(u[3], u[4], sel));
+}
+
 template <typename T>
 __device__ __forceinline__ float ld_scalar(const T* p) {
   return Elem<T>::to_f32(*p);

@@ -69,6 +69,8 @@ struct FwdParams {
   int l2_rows;        // register kernels: rows of the CTA's walk fetched into L2
                       // this many iterations ahead (0: none)
   int slice;          // kCluster: vectors of each row per CTA of the cluster
+  int x_shift;        // kRagged with mixed alignment: bytes (mod 16) by which x's
+                      // rows start past the output's (y, or h for the fused add)
 };
 
 struct BwdParams {
@@ -92,6 +94,8 @@ struct BwdParams {
   int period;
   int l2_rows;        // register kernels: L2 lookahead in iterations (0: none)
   int slice;          // kCluster: vectors of each row per CTA of the cluster
+  int x_shift;        // kRagged with mixed alignment: bytes (mod 16) by which the
+  int dy_shift;       //   rows of x and of dy start past those of dx
 };
 
 // LayerNorm (forward and backward).
@@ -141,6 +145,7 @@ struct FwdKey {
   bool prefetch; // issue the next row's loads before reducing the current row
   bool strided;  // rows addressed through (heads, x_st, x_sh, y_st, y_sh)
   int out = kOutDtype;   // output kind (kOut*)
+  bool mix = false;      // kRagged: x need not share the output's alignment
 };
 
 struct BwdKey {
@@ -152,6 +157,7 @@ struct BwdKey {
   bool acc_smem; // kCta: dgamma partials in shared memory instead of registers
   bool prefetch;
   bool dres;     // fused-add backward (adds the residual-path gradient)
+  bool mix = false;   // kRagged: x and dy need not share dx's alignment
 };
 
 // Kernel for a key, or nullptr when that instantiation does not exist.  Each
@@ -174,6 +180,12 @@ FwdKernel get_fwd_ragged_bf16_f32(const FwdKey& k);
 BwdKernel get_bwd_ragged_f32_f32(const BwdKey& k);
 BwdKernel get_bwd_ragged_bf16_bf16(const BwdKey& k);
 BwdKernel get_bwd_ragged_bf16_f32(const BwdKey& k);
+FwdKernel get_fwd_ragged_mix_f32_f32(const FwdKey& k);
+FwdKernel get_fwd_ragged_mix_bf16_bf16(const FwdKey& k);
+FwdKernel get_fwd_ragged_mix_bf16_f32(const FwdKey& k);
+BwdKernel get_bwd_ragged_mix_f32_f32(const BwdKey& k);
+BwdKernel get_bwd_ragged_mix_bf16_bf16(const BwdKey& k);
+BwdKernel get_bwd_ragged_mix_bf16_f32(const BwdKey& k);
 FwdKernel get_fwd_cluster_f32_f32(const FwdKey& k);
 FwdKernel get_fwd_cluster_bf16_bf16(const FwdKey& k);
 FwdKernel get_fwd_cluster_bf16_f32(const FwdKey& k);

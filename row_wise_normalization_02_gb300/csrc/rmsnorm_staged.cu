@@ -130,8 +130,11 @@ __global__ void __launch_bounds__(kCtaMaxThreads) fwd_staged_kernel(const FwdPar
 // dgamma partials of this CTA's rows in registers, written as one partial row
 // at the end.  The fused-add backward reads dres from the stage in its output
 // pass, so it refills the stage after that pass instead of right after the
-// reduction.
-template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool DRES>
+// reduction.  MIX: x (h) and dy may start off dx's 16-byte alignment (dx,
+// dres and gamma on 16 bytes, rows a multiple of 16 bytes): each shifted row
+// arrives as its enclosing aligned span and its vectors are realigned from
+// shared memory (slot_vec).
+template <typename TX, typename TW, int VPT, bool HAS_RSTD, bool DRES, bool MIX>
 __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdParams p) {
   constexpr int E = Elem<TX>::kPerVec;
   constexpr int K = HAS_RSTD ? 1 : 2;
@@ -146,7 +149,9 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
   const char* xs = static_cast<const char*>(p.x);
   const char* ds = static_cast<const char*>(p.dy);
   const char* rs = static_cast<const char*>(p.dres);
-  int64_t issued = ring_start<NS>(rg, S, nrows, first, stride, xs, ds, rs, rb);
+  const int sx = MIX ? p.x_shift : 0, sd = MIX ? p.dy_shift : 0;
+  const RowSpans sp{rb, MIX ? rb + 16 : rb, {sx, sd, 0}};
+  int64_t issued = ring_start<NS>(rg, S, nrows, first, stride, xs, ds, rs, sp);
 
   float g[VPT][E], acc[VPT][E];
 #pragma unroll
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
     const int64_t row = first + i * stride;
     const float r_saved = HAS_RSTD ? __ldg(p.rstd + row) : 0.f;
     const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((i / S) & 1), p.wait_limit);
-    const uint4* st = reinterpret_cast<const uint4*>(rg.buf + (size_t)s * NS * rb);
+    const unsigned char* st = rg.buf + (size_t)s * NS * sp.slot;
     uint4 xv[VPT], dv[VPT];
     float sums[K];
 #pragma unroll
@@ -179,8 +184,8 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
       xv[k] = make_uint4(0, 0, 0, 0);
       dv[k] = make_uint4(0, 0, 0, 0);
       if (v < p.nvec) {
-        xv[k] = st[v];
-        dv[k] = st[p.nvec + v];
+        xv[k] = slot_vec(st, v, sx);
+        dv[k] = slot_vec(st + sp.slot, v, sd);
         float xf[E], df[E];
         unpack(xv[k], xf);
         unpack(dv[k], df);
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
     parity ^= 1;
     if (!DRES && tid == 0 && issued < nrows) {
       fence_proxy_async_smem();
-      issue_row<NS>(rg, issued, first, stride, S, xs, ds, rs, rb);
+      issue_row<NS>(rg, issued, first, stride, S, xs, ds, rs, sp);
       ++issued;
     }
     const float r = HAS_RSTD ? r_saved : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
         float xf[E], df[E], o[E], rf[E];
         unpack(xv[k], xf);
         unpack(dv[k], df);
-        if (DRES) unpack(st[2 * p.nvec + v], rf);
+        if (DRES) unpack(reinterpret_cast<const uint4*>(st + 2 * sp.slot)[v], rf);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           o[e] = r * fmaf(-xf[e], c, g[k][e] * df[e]);
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_staged_kernel(const BwdPar
       __syncthreads();
       if (tid == 0 && issued < nrows) {
         fence_proxy_async_smem();
-        issue_row<NS>(rg, issued, first, stride, S, xs, ds, rs, rb);
+        issue_row<NS>(rg, issued, first, stride, S, xs, ds, rs, sp);
         ++issued;
       }
     }
@@ -264,14 +269,19 @@ FwdKernel pick_fwd(int vpt) {
   }
 }
 
-template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES, bool MIX>
 BwdKernel pick_bwd(int vpt) {
   switch (vpt) {
-    case 1: return bwd_staged_kernel<TX, TW, 1, HAS_RSTD, DRES>;
-    case 2: return bwd_staged_kernel<TX, TW, 2, HAS_RSTD, DRES>;
-    case 4: return bwd_staged_kernel<TX, TW, 4, HAS_RSTD, DRES>;
+    case 1: return bwd_staged_kernel<TX, TW, 1, HAS_RSTD, DRES, MIX>;
+    case 2: return bwd_staged_kernel<TX, TW, 2, HAS_RSTD, DRES, MIX>;
+    case 4: return bwd_staged_kernel<TX, TW, 4, HAS_RSTD, DRES, MIX>;
     default: return nullptr;
   }
+}
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
+BwdKernel pick_bwd(int vpt, bool mix) {
+  return mix ? pick_bwd<TX, TW, HAS_RSTD, DRES, true>(vpt)
+             : pick_bwd<TX, TW, HAS_RSTD, DRES, false>(vpt);
 }
 
 template <typename TX, typename TW>
@@ -281,8 +291,10 @@ FwdKernel staged_fwd(const FwdKey& k) {
 template <typename TX, typename TW>
 BwdKernel staged_bwd(const BwdKey& k) {
   if (k.dres)
-    return k.has_rstd ? pick_bwd<TX, TW, true, true>(k.vpt) : pick_bwd<TX, TW, false, true>(k.vpt);
-  return k.has_rstd ? pick_bwd<TX, TW, true, false>(k.vpt) : pick_bwd<TX, TW, false, false>(k.vpt);
+    return k.has_rstd ? pick_bwd<TX, TW, true, true>(k.vpt, k.mix)
+                      : pick_bwd<TX, TW, false, true>(k.vpt, k.mix);
+  return k.has_rstd ? pick_bwd<TX, TW, true, false>(k.vpt, k.mix)
+                    : pick_bwd<TX, TW, false, false>(k.vpt, k.mix);
 }
 
 #if RMSN_PAIR == 0

@@ -32,6 +32,8 @@ class Workload:
     heads: int = 0          # strided rows: M = tokens * heads, x is [tokens, stride_token]
     stride_token: int = 0
     global_scale: float = 0.0   # NVFP4 outputs: the per-tensor scale gs
+    offsets: tuple = ()     # ((operand, bytes past a 256-byte boundary), ...): operands
+                            # placed off 16 bytes (x a view at an odd element offset)
 
 
 def tensor_recipes(wl: Workload) -> dict:
@@ -133,3 +135,15 @@ for _op in ("fwd", "bwd"):
 WORKLOADS["fadd_bwd_bf16_m8192_n32768"] = Workload("fadd_bwd_bf16_m8192_n32768", "fused_add_bwd",
                                                    8192, 32768, "bf16", "bf16", 1e-6, 9,
                                                    tags=("next",))
+# inputs off the outputs' 16-byte alignment: x (forward) or x (backward) one
+# bf16 element past a 16-byte boundary -- a view at an odd element offset --
+# while y, dy and dx are aligned
+for _op in ("fwd", "bwd"):
+    for _m, _n in ((16384, 8192), (32768, 4096)):
+        _name = f"mixed_{_op}_bf16_m{_m}_n{_n}"
+        WORKLOADS[_name] = Workload(_name, _op, _m, _n, "bf16", "bf16", 1e-6, 10,
+                                    offsets=(("x", 2),), tags=("mixed",))
+# the fused add with x off the residual's (and y's) alignment
+WORKLOADS["mixed_fadd_bf16_m32768_n4096"] = Workload(
+    "mixed_fadd_bf16_m32768_n4096", "fused_add", 32768, 4096, "bf16", "bf16", 1e-6, 10,
+    store_rstd=False, offsets=(("x", 2),), tags=("mixed",))

@@ -22,13 +22,18 @@ def test_workload_matches_oracle(name):
     inp = si.make_inputs(wl)
     eps = float(np.float32(wl.eps))
     x, g = inp["x"], inp["gamma"]
+    off = dict(wl.offsets)
     if wl.op == "fwd":
-        out = pu.run_fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd)
+        out = pu.run_fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd,
+                         offsets=off)
         check_fwd(x, g, eps, wl.x_dtype, wl.w_dtype, out, want_rstd=wl.store_rstd)
     elif wl.op == "fused_add":
         r = inp["residual"]
-        out = pu.run_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd)
+        out = pu.run_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, want_rstd=wl.store_rstd,
+                           offsets=off)
         check_fused(x, r, g, eps, wl.x_dtype, wl.w_dtype, out, want_rstd=wl.store_rstd)
+    elif wl.offsets and wl.op != "bwd":
+        raise AssertionError(f"operand offsets are not wired for {wl.op}")
     elif wl.op in ("ln_fwd", "ln_bwd"):
         from tests import test_parity_layernorm as tl
         tl.check_workload(wl, inp)
@@ -50,7 +55,7 @@ def test_workload_matches_oracle(name):
     else:
         # the saved rstd comes from the oracle forward
         rstd = oracle.fwd(x, g, eps, wl.x_dtype, wl.w_dtype, want64=False)["rstd"]
-        out = pu.run_bwd(inp["dy"], x, rstd, g, eps, wl.x_dtype, wl.w_dtype)
+        out = pu.run_bwd(inp["dy"], x, rstd, g, eps, wl.x_dtype, wl.w_dtype, offsets=off)
         info = check_bwd(x, inp["dy"], g, rstd, eps, wl.x_dtype, wl.w_dtype, out)
         # elements that needed the cancellation floor, of the tensor's size
         print("FLOOR", name, info.get("floor", 0), wl.M * wl.N, info)
