@@ -710,6 +710,34 @@ def time_rotation(launches, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
+def time_graph(launches, calls, reps, stream):
+    """Device time (ms) per call of `calls` back-to-back launches captured once
+    in a CUDA graph (so no host work between them: the GPU-side cost of a call,
+    which the eager rotation hides when the host enqueues slower than the GPU
+    runs); median of `reps` replays, CUDA events around each."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(len(launches)):
+            launches[i]()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(calls):
+            launches[i % len(launches)]()
+    ms = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b) / calls)
+    del g
+    return statistics.median(ms)
+
+
 def inrun_copy_gbs(dev, stream, nbytes=1 << 30, reps=10):
     """Device-to-device copy bandwidth measured in this run (cudaMemcpyAsync of
     a 1 GiB buffer; read + write bytes, the convention of the measured peak)."""
@@ -776,6 +804,14 @@ def run_sweep(args):
               for _ in range(args.rounds)]
         med = statistics.median(us)
         byts = alg_bytes(wl)
+        graph = {}
+        if args.graph:
+            calls = max(len(launches), min(args.steps, 200))
+            g_us = time_graph(launches, calls, args.rounds, stream) * 1e3
+            graph = {"graph_us_per_call": round(g_us, 2),
+                     "graph_frac_of_measured_peak": round(byts / g_us / 1e3 / peak, 4),
+                     "graph": f"{calls} calls captured in one CUDA graph, median of "
+                              f"{args.rounds} replays"}
         print(json.dumps({"workload": name, "op": wl.op, "M": wl.M, "N": wl.N,
                           "variant": rn.rmsnorm_describe_plan(
                               _op_code(wl.op), wl.M, wl.N, wl.x_dtype, wl.w_dtype,
@@ -792,7 +828,7 @@ def run_sweep(args):
                           "l2": f"rotation over {len(sets)} operand set(s) "
                                 f">= 3 x L2, back-to-back launches",
                           "timer": "CUDA events around each round of back-to-back calls; "
-                                   "median of rounds"}), flush=True)
+                                   "median of rounds", **graph}), flush=True)
         del sets, launches
         torch.cuda.empty_cache()
 
@@ -808,6 +844,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--rounds", type=int, default=5, help="--sweep: timed rounds per workload")
+    ap.add_argument("--graph", action="store_true",
+                    help="--sweep: also time the calls captured in a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -12,7 +12,10 @@
  * Conventions shared by every entry point:
  *  - Pointers are DEVICE pointers owned by the caller.  The library never
  *    allocates, frees or synchronises; work is enqueued on `stream` (0 = the
- *    legacy default stream) of the current device.
+ *    legacy default stream) of the current device.  The compute calls may
+ *    therefore be captured into a CUDA graph (stream capture) once a call of
+ *    the same shape has run outside capture on that device (the first call
+ *    sets kernel attributes); rmsnorm_check_device synchronises and may not.
  *  - Layout: contiguous row-major, row stride N elements.
  *  - Dtypes: output dtype = x_dtype; rstd and dgamma are always fp32.
  *    Supported (x_dtype, w_dtype) pairs: (F32, F32), (BF16, BF16), (BF16, F32).
