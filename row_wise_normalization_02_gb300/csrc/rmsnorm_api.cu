@@ -1162,10 +1162,11 @@ LnKernel ln_kernel(const LnKey& k) {
 // the forward with up to 4 vectors per thread (16384 x 8192 bf16: VPT 4 0.84
 // of the copy bandwidth, VPT 2 / 512 threads 0.69: two row barriers per row
 // cost more in a larger CTA), the backward with up to 2 (0.80; it holds gamma
-// and two partial rows per thread).  The staged backward (rows through the
-// bulk-copy ring) is a forced variant only: at 4 vectors per thread it spills
-// (0.70), at 2 it fits one CTA per SM (0.63).  Anything else: the scalar
-// kernel.
+// and two partial rows per thread).  The staged backward with one row per
+// CTA (rows through the bulk-copy ring) is a forced variant only: at 4
+// vectors per thread it spills (0.70), at 2 it fits one CTA per SM (0.63);
+// the backward of rows of 65-128 vectors takes the ring with eight rows of 32
+// lanes per stage.  Anything else: the scalar kernel.
 rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool vec_ok,
                          Plan* res) {
   const int E = per_vec(xd);
@@ -1196,6 +1197,21 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
       }
     }
   }
+  // backward rows of 65-128 vectors: the CTA's eight rows of 32 lanes through
+  // a bulk-copy ring, one copy per operand per stage (65536 x 1024 bf16: 0.94
+  // of the copy peak with three stages, against 0.88 for one 64-thread CTA per
+  // row; two stages 0.88, four 0.67 at one CTA per SM).  Not for bf16
+  // activations with fp32 weights at 4 vectors per lane, whose form spills.
+  if (bwd && vec_ok && nvec > 64 && nvec <= 128 &&
+      !(xd == kBF16 && wd == kF32 && (nvec + 31) / 32 == 4)) {
+    p.family = kStaged;
+    p.g = 32;
+    p.vpt = (nvec + 31) / 32;
+    p.threads = kSubwarpThreads;
+    p.rows_per_cta = kSubwarpThreads / 32;
+    p.prefetch = false;
+    p.stages = 0;
+  }
   const Force& f = read_force();
   if (f.on) {
     if (f.family == kGeneric) {
@@ -1218,9 +1234,20 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
           (int64_t)p.threads * p.vpt < nvec)
         return RMSNORM_ERR_INVALID_ARG;
       p.rows_per_cta = 1;
+    } else if (f.family == kStaged && f.g > 0) {
+      // short rows through the ring: g lanes per row, 256 / g rows per stage
+      if (!vec_ok || !bwd || f.g > 32) return RMSNORM_ERR_INVALID_ARG;
+      p.family = kStaged;
+      p.g = f.g;
+      p.vpt = f.vpt ? f.vpt : (nvec + f.g - 1) / f.g;
+      if ((int64_t)p.g * p.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
+      p.threads = kSubwarpThreads;
+      p.rows_per_cta = kSubwarpThreads / p.g;
+      p.stages = f.st;
     } else if (f.family == kStaged) {
       if (!vec_ok || !bwd) return RMSNORM_ERR_INVALID_ARG;
       p.family = kStaged;
+      p.g = 0;
       p.vpt = f.vpt ? f.vpt : 4;
       p.threads = f.threads ? f.threads : round_up((nvec + p.vpt - 1) / p.vpt, 32);
       if (p.threads < 32 || p.threads > kCtaMaxThreads || p.threads % 32 ||
@@ -1249,9 +1276,10 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
   if (p.family == kGeneric || p.family == kStaged) p.l2_ahead = 0;
   if (p.family == kStaged) {
     p.prefetch = false;
-    // ring of [x | dy] row pairs: as many stages as fit the half-SM budget
-    // (two CTAs per SM), at least two, at most kStagedMaxStages
-    const int64_t stage_bytes = 2 * N * esize(xd);
+    // ring of [x | dy] row pairs (of the CTA's rows_per_cta rows for short
+    // rows): as many stages as fit the half-SM budget (two CTAs per SM), at
+    // least two, at most kStagedMaxStages
+    const int64_t stage_bytes = 2 * N * esize(xd) * p.rows_per_cta;
     if (p.stages <= 0) {
       int64_t st = (kStagedSmemBudget - kStagedHeader) / stage_bytes;
       if (st < 2) st = (kStagedSmemMax - kStagedHeader) / stage_bytes;
@@ -1261,7 +1289,7 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
         kStagedHeader + p.stages * stage_bytes > kStagedSmemMax)
       return RMSNORM_ERR_INVALID_ARG;
   }
-  if (p.family != kSubwarp) p.g = 0;
+  if (p.family != kSubwarp && p.family != kStaged) p.g = 0;
   LnKey k{xd, wd, p.family, p.g, p.vpt, bwd, p.prefetch};
   LnKernel fn = ln_kernel(k);
   if (fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
@@ -1269,7 +1297,8 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
   // sub-warp backward: the groups' partial rows meet in shared memory;
   // staged: the ring
   p.smem = (bwd && p.family == kSubwarp) ? p.rows_per_cta * 2 * nvec * E * 4 : 0;
-  if (p.family == kStaged) p.smem = (int)(kStagedHeader + p.stages * 2 * N * esize(xd));
+  if (p.family == kStaged)
+    p.smem = (int)(kStagedHeader + p.stages * 2 * N * esize(xd) * p.rows_per_cta);
   if (bwd) {
     p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
     const Force& fr = read_force();

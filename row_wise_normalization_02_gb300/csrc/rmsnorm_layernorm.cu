@@ -686,6 +686,203 @@ __global__ void __launch_bounds__(kCtaMaxThreads) ln_bwd_staged_kernel(const LnP
 }
 
 // ---------------------------------------------------------------------------
+// Short rows through the bulk-copy ring (staged with G lanes per row): a CTA
+// iteration covers RPC = 256 / G consecutive rows, contiguous in memory, so
+// one bulk copy per operand fills a ring stage ([x rows | dy rows]).  The row
+// math is the sub-warp backward's (shuffle reductions within the G lanes);
+// the vectors are read from the stage for the statistics, the row sums and
+// dx rather than held in registers, which hold gamma (packed) and the two
+// partial rows.  One CTA barrier per iteration votes on the bounded waits and
+// proves that every thread has finished the previous iteration's stage,
+// which thread 0 then refills.  The saved statistics are loaded one
+// iteration ahead.  Held to two resident CTAs per SM (128 registers; the
+// four-vector form would take 154 and one).
+template <typename TX, typename TW, int G, int VPT>
+__global__ void __launch_bounds__(kSubwarpThreads, 2) ln_bwd_rows_staged_kernel(const LnParams p) {
+  constexpr int E = Elem<TX>::kPerVec;
+  constexpr int GW = Cfg<TX, TW>::GW;
+  constexpr int RPC = kSubwarpThreads / G;
+  const size_t rb = (size_t)p.N * sizeof(TX);
+  {  // the rows of the first two iterations into L2 while the previous kernel ends
+    const int64_t b0 = (int64_t)blockIdx.x * RPC, st0 = (int64_t)gridDim.x * RPC;
+    l2_warm(p.x, p.dy, nullptr, b0, RPC, p.M, rb);
+    l2_warm(p.x, p.dy, nullptr, b0 + st0, RPC, p.M, rb);
+  }
+  pdl_begin();
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Ring rg = ring_of(smem);
+  const int lane = threadIdx.x % G, grp = threadIdx.x / G, tid = threadIdx.x;
+  const int S = p.stages;
+  const size_t blk = (size_t)RPC * rb;              // one operand's rows of a stage
+  const int64_t units = (p.M + RPC - 1) / RPC;      // CTA iterations of RPC rows
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t nit = first < units ? (units - 1 - first) / stride + 1 : 0;
+  const char* src[2] = {static_cast<const char*>(p.x), static_cast<const char*>(p.dy)};
+  const bool saved = p.mean != nullptr;
+
+  // thread 0: the rows of iteration j into stage j mod S (the last unit may
+  // hold fewer than RPC rows)
+  auto issue = [&](int64_t j) {
+    const int s = (int)(j % S);
+    const int64_t row0 = (first + j * stride) * RPC;
+    const int64_t n = p.M - row0 < RPC ? p.M - row0 : RPC;
+    const uint32_t bytes = (uint32_t)(n * (int64_t)rb);
+    uint64_t* bar = rg.full + s;
+    unsigned char* dst = rg.buf + (size_t)s * 2 * blk;
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) bulk_copy_g2s(dst + q * blk, src[q] + row0 * rb, bytes, bar);
+  };
+  int64_t issued = 0;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(rg.full + s, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (; issued < (nit < S ? nit : S); ++issued) issue(issued);
+
+  uint4 gw[VPT][GW];
+  float2 ag[VPT][E / 2], ab[VPT][E / 2];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+    load_weight<GW>(gw[k], p.gamma, v, v < p.nvec);
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) ag[k][e] = ab[k][e] = make_float2(0.f, 0.f);
+  }
+  // this thread's row statistics, one iteration ahead
+  float sm = 0.f, sr = 0.f;
+  if (saved && nit > 0) {
+    const int64_t row = first * RPC + grp;
+    if (row < p.M) {
+      sm = p.mean[row];
+      sr = p.rstd[row];
+    }
+  }
+  int parity = 0;   // unused by the sub-warp reductions
+  int64_t j = 0;
+  bool failed = false;
+  for (; j < nit; ++j) {
+    const int s = (int)(j % S);
+    const int64_t row = (first + j * stride) * RPC + grp;
+    const bool valid = row < p.M;
+    float nsm = 0.f, nsr = 0.f;
+    if (saved && j + 1 < nit) {
+      const int64_t nrow = (first + (j + 1) * stride) * RPC + grp;
+      if (nrow < p.M) {
+        nsm = p.mean[nrow];
+        nsr = p.rstd[nrow];
+      }
+    }
+    const bool late = !mbar_wait_bounded(rg.full + s, (uint32_t)((j / S) & 1), p.wait_limit);
+    if (__syncthreads_or(late ? 1 : 0)) {
+      failed = true;
+      break;
+    }
+    // every thread is done with the previous iteration's stage: refill it
+    if (tid == 0 && j > 0 && issued < nit) {
+      fence_proxy_async_smem();
+      issue(issued);
+      ++issued;
+    }
+    const unsigned char* st = rg.buf + (size_t)s * 2 * blk + (size_t)grp * rb;
+    const uint4* xs = reinterpret_cast<const uint4*>(st);
+    const uint4* ds = reinterpret_cast<const uint4*>(st + blk);
+    RowStats rst;
+    if (saved) {
+      rst.m0 = sm;
+      rst.c = 0.f;
+      rst.rs = sr;
+    } else {
+      uint4 cx[VPT];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lane + k * G;
+        cx[k] = (valid && v < p.nvec) ? xs[v] : make_uint4(0, 0, 0, 0);
+      }
+      rst = row_stats<G, TX, E, VPT>(cx, nullptr, parity, lane, G, p.nvec, p.inv_n, p.eps);
+    }
+    sm = nsm;
+    sr = nsr;
+    const float2 nc = make_float2(-rst.c, -rst.c);
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+    auto dot = [&](auto corr) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lane + k * G;
+        if (!valid || v >= p.nvec) continue;
+        uint4 gk[GW];
+#pragma unroll
+        for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+        ln_bwd_dot<TX, TW, E, GW, decltype(corr)::value>(ld_shared_v4(xs + v), ld_shared_v4(ds + v),
+                                                          gk, -rst.m0, nc, s1, s2);
+      }
+    };
+    if (saved) dot(std::false_type{});
+    else dot(std::true_type{});
+    float a = s1.x + s1.y, b = s2.x + s2.y;
+    row_sum2<G>(a, b, nullptr, parity);
+    const LnBwdRow rc = ln_bwd_row(rst.m0, rst.c, rst.rs, a, b, p.inv_n);
+    char* dxr = static_cast<char*>(p.y) + row * rb;
+    auto apply = [&](auto corr) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int v = lane + k * G;
+        if (valid && v < p.nvec) {
+          uint4 gk[GW];
+#pragma unroll
+          for (int w = 0; w < GW; ++w) gk[w] = opaque(gw[k][w]);
+          st_stream(dxr + (size_t)v * 16,
+                    ln_bwd_apply<TX, TW, E, GW, decltype(corr)::value>(
+                        ld_shared_v4(xs + v), ld_shared_v4(ds + v), gk, rc, ag[k], ab[k]));
+        }
+      }
+    };
+    if (saved) apply(std::false_type{});
+    else apply(std::true_type{});
+  }
+  if (failed) {
+    if (tid == 0) {
+      drain(rg, j, issued, S);
+      atomicOr(p.status, kStatusWaitTimeout);
+    }
+    return;
+  }
+  if (p.partial == nullptr) return;
+  // the row groups' partial rows meet in shared memory (the ring is free:
+  // every copy has been consumed), added in group order
+  __syncthreads();
+  float* sacc = reinterpret_cast<float*>(rg.buf);
+  const int ncol = p.nvec * E;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + k * G;
+    if (v < p.nvec) {
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) {
+        float* dg = sacc + (size_t)grp * 2 * ncol + v * E + 2 * e;
+        dg[0] = ag[k][e].x;
+        dg[1] = ag[k][e].y;
+        dg[ncol] = ab[k][e].x;
+        dg[ncol + 1] = ab[k][e].y;
+      }
+    }
+  }
+  __syncthreads();
+  float* prow = p.partial + (size_t)blockIdx.x * 2 * p.ld_half;
+  for (int c = tid; c < ncol; c += kSubwarpThreads) {
+    float sg = 0.f, sb = 0.f;
+    for (int q = 0; q < RPC; ++q) {
+      sg += sacc[(size_t)q * 2 * ncol + c];
+      sb += sacc[(size_t)q * 2 * ncol + ncol + c];
+    }
+    prow[c] = sg;
+    prow[p.ld_half + c] = sb;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Any row (scalar, one row per CTA iteration, 256 threads): three passes over
 // the row in global memory (mean, variance, output); the backward's partial
 // row is accumulated in place in the workspace, each column by the one thread
@@ -810,6 +1007,15 @@ template <typename TX, typename TW>
 LnKernel pick_ln(const LnKey& k) {
   if (k.family == kGeneric)
     return k.bwd ? ln_bwd_generic_kernel<TX, TW> : ln_fwd_generic_kernel<TX, TW>;
+  if (k.family == kStaged && k.g > 0) {   // short rows through the ring
+    if (!k.bwd) return nullptr;
+#define RMSN_LNRS(G_, V_) \
+  if (k.g == G_ && k.vpt == V_) return ln_bwd_rows_staged_kernel<TX, TW, G_, V_>;
+    RMSN_LNRS(8, 1) RMSN_LNRS(16, 1) RMSN_LNRS(32, 1) RMSN_LNRS(16, 2) RMSN_LNRS(32, 2)
+    RMSN_LNRS(32, 3) RMSN_LNRS(32, 4)
+#undef RMSN_LNRS
+    return nullptr;
+  }
   if (k.family == kStaged) {
     if (!k.bwd) return nullptr;
     switch (k.vpt) {

@@ -215,11 +215,20 @@ def test_backward(xd, wd, N, saved):
                                    "subwarp:g=4:vpt=1:cps=1", "cta:vpt=1:cps=1",
                                    "cta:vpt=2:t=64:cps=1", "cta:vpt=2:t=64:pf=0:cps=1",
                                    "staged:vpt=1:st=2:cps=1", "staged:vpt=2:t=64:st=3:cps=1",
-                                   "staged:vpt=4:t=32:st=8:cps=1", "generic:cps=1", "generic"])
-@pytest.mark.parametrize("N", [128, 32])
+                                   "staged:vpt=4:t=32:st=8:cps=1", "generic:cps=1", "generic",
+                                   # short rows through the ring, 256 / g rows per stage
+                                   "staged:g=32:vpt=4:cps=1", "staged:g=32:vpt=3:st=2:cps=1",
+                                   "staged:g=16:vpt=2:st=4:cps=1", "staged:g=8:vpt=1:st=3:cps=1"])
+@pytest.mark.parametrize("N", [128, 32, 1024, 760])
 def test_backward_forced_variants_walk_many_rows(debug_env, force, N):
     if "g=4" in force and N != 32:
         pytest.skip("4 lanes hold at most 4 vectors")
+    if N >= 760 and "staged:g=" not in force:
+        pytest.skip("the short-row sizes are for the ring forms")
+    import re
+    m = re.search(r"g=(\d+):vpt=(\d+)", force)
+    if m and int(m.group(1)) * int(m.group(2)) * 8 < N:
+        pytest.skip("the forced lanes do not hold the row")
     debug_env.set("RMSNORM_FORCE_VARIANT", force)
     x, g, _, dy = inputs(3000, N, "bf16", "bf16", seed=6)
     fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
@@ -227,15 +236,19 @@ def test_backward_forced_variants_walk_many_rows(debug_env, force, N):
     check_bwd(out, dy, x, fw["mean"], fw["rstd"], g, f32(1e-5), "bf16", "bf16")
 
 
-@pytest.mark.parametrize("saved", [True, False])
-def test_backward_staged_wait_timeout_is_reported_and_the_context_survives(debug_env, saved):
+@pytest.mark.parametrize("saved,force,N", [(True, "staged:vpt=4:st=3", 8192),
+                                           (False, "staged:vpt=4:st=3", 8192),
+                                           (True, "staged:g=32:vpt=4:st=3", 1024),
+                                           (False, "staged:g=32:vpt=4:st=3", 1024)])
+def test_backward_staged_wait_timeout_is_reported_and_the_context_survives(debug_env, saved,
+                                                                           force, N):
     # a negative wait limit: every wait for a row gives up at once; the kernel
     # stores nothing more, drains its copies and raises the flag that
     # rmsnorm_check_device reports and clears
-    x, g, _, dy = inputs(1024, 8192, "bf16", "bf16", seed=44)
+    x, g, _, dy = inputs(1024 if N > 1024 else 4000, N, "bf16", "bf16", seed=44)
     fw = oracle.layernorm_fwd(x, g, None, f32(1e-5), "bf16", "bf16")
     mean, rstd = (fw["mean"], fw["rstd"]) if saved else (None, None)
-    debug_env.set("RMSNORM_FORCE_VARIANT", "staged:vpt=4:st=3")
+    debug_env.set("RMSNORM_FORCE_VARIANT", force)
     rn.rmsnorm_check_device()
     debug_env.set("RMSNORM_WAIT_LIMIT_CYCLES", "-1")
     run_bwd(dy, x, mean, rstd, g, f32(1e-5), "bf16", "bf16")
