@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cluster_kernel(const BwdPa
     sums[0] = dot2.x + dot2.y;
     if (K > 1) sums[K - 1] = ss2.x + ss2.y;
     // the CTA's sums and its vote, then the cluster's: every CTA of the
-    // cluster sees the same sums and the same verdict on the waits
+    // cluster sees the same sums and the same outcome of the waits
     const bool any_late = cta_sum_vote<K>(sums, rg.red, parity, late);
     parity ^= 1;
     float tot[3];
