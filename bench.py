@@ -635,7 +635,13 @@ def device_sets(wl, inp, dev, l2_bytes, rn):
             d["q"] = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
             d["qs"] = torch.empty((M, N // 16), dtype=torch.uint8, device=dev)
         elif wl.op != "fwd_strided":   # the strided forward writes in place
-            d["y"] = torch.empty((M, N), dtype=act, device=dev)
+            yoff = off.get("dx" if wl.op in ("bwd", "fused_add_bwd") else "y", 0)
+            if yoff:   # an output placed off 16 bytes, like `placed`
+                e = torch.empty((), dtype=act).element_size()
+                buf = torch.empty(M * N + 16 // e, dtype=act, device=dev)
+                d["y"] = buf[yoff // e: yoff // e + M * N].view(M, N)
+            else:
+                d["y"] = torch.empty((M, N), dtype=act, device=dev)
         d["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
         if wl.op == "bwd":
             d["dgamma"] = torch.empty(N, dtype=torch.float32, device=dev)
@@ -710,6 +716,18 @@ def time_rotation(launches, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
+def plan_layout(wl):
+    """The layout argument of rmsnorm_describe_plan for a workload's operand
+    offsets: True (all on 16 bytes), "mixed" (inputs off outputs that agree)
+    or False (outputs that disagree: the scalar kernel)."""
+    if not wl.offsets:
+        return True
+    off = dict(wl.offsets)
+    outs = {"fwd": ["y"], "fused_add": ["residual", "y"], "bwd": ["dx"],
+            "fused_add_bwd": ["residual"]}.get(wl.op, ["y"])
+    return "mixed" if len({off.get(k, 0) % 16 for k in outs}) == 1 else False
+
+
 def time_graph(launches, calls, reps, stream):
     """Device time (ms) per call of `calls` back-to-back launches captured once
     in a CUDA graph (so no host work between them: the GPU-side cost of a call,
@@ -775,7 +793,7 @@ def run_sweep(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = args.workloads.split(",") if args.workloads else [
         n for n, w in si.WORKLOADS.items()
-        if "sweep" in w.tags or "headline" in w.tags or "next" in w.tags or "mixed" in w.tags]
+        if set(w.tags) & {"sweep", "headline", "next", "mixed", "generic"}]
     for name in names:
         wl = si.WORKLOADS[name]
         inp = si.make_inputs(wl)
@@ -815,7 +833,7 @@ def run_sweep(args):
         print(json.dumps({"workload": name, "op": wl.op, "M": wl.M, "N": wl.N,
                           "variant": rn.rmsnorm_describe_plan(
                               _op_code(wl.op), wl.M, wl.N, wl.x_dtype, wl.w_dtype,
-                              "mixed" if wl.offsets else True),
+                              plan_layout(wl)),
                           "us_per_call": round(med, 2), "rounds_us": [round(u, 2) for u in us],
                           "min_us": round(min(us), 2),
                           "spread": round((max(us) - min(us)) / med, 4),

@@ -450,11 +450,13 @@ __global__ void __launch_bounds__(kCtaMaxThreads) bwd_cta_kernel(const BwdParams
 // ---------------------------------------------------------------------------
 // kGeneric: any N, any element-aligned pointers.  Pass 1 reduces, pass 2
 // writes dx; the partial row of this CTA is accumulated in place in global
-// memory, each column always by the same thread.
+// memory, each column always by the same thread.  Each thread issues U
+// scalar loads per operand before using any (U requests in flight per warp).
 template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
 __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
   pdl_begin();
   constexpr int K = HAS_RSTD ? 1 : 2;
+  constexpr int U = 4;
   __shared__ float red[2 * 2 * 32];
   const int tid = threadIdx.x, T = blockDim.x;
   const int N = p.N;
@@ -470,22 +472,47 @@ __global__ void __launch_bounds__(256) bwd_generic_kernel(const BwdParams p) {
     float sums[K];
 #pragma unroll
     for (int q = 0; q < K; ++q) sums[q] = 0.f;
-    for (int j = tid; j < N; j += T) {
-      const float xv = ld_scalar(xr + j);
-      sums[0] = fmaf(ld_scalar(gp + j) * ld_scalar(dr + j), xv, sums[0]);
-      if (!HAS_RSTD) sums[K - 1] = fmaf(xv, xv, sums[K - 1]);
+    for (int j0 = tid; j0 < N; j0 += U * T) {
+      float xv[U], dv[U], gv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        xv[u] = j < N ? ld_scalar(xr + j) : 0.f;
+        dv[u] = j < N ? ld_scalar(dr + j) : 0.f;
+        gv[u] = j < N ? ld_scalar(gp + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        sums[0] = fmaf(gv[u] * dv[u], xv[u], sums[0]);
+        if (!HAS_RSTD) sums[K - 1] = fmaf(xv[u], xv[u], sums[K - 1]);
+      }
     }
     cta_sum<K>(sums, red, parity);
     parity ^= 1;
     const float r = HAS_RSTD ? __ldg(p.rstd + row) : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
     const float c = r * r * p.inv_n * sums[0];
     const TX* rr = static_cast<const TX*>(p.dres) + row * (int64_t)N;
-    for (int j = tid; j < N; j += T) {
-      const float xv = ld_scalar(xr + j), dv = ld_scalar(dr + j);
-      float o = r * fmaf(-xv, c, ld_scalar(gp + j) * dv);
-      if (DRES) o += ld_scalar(rr + j);
-      st_scalar(dxr + j, o);
-      if (prow) prow[j] = fmaf(dv * xv, r, prow[j]);
+    for (int j0 = tid; j0 < N; j0 += U * T) {
+      float xv[U], dv[U], gv[U], rv[U], pv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        const bool in = j < N;
+        xv[u] = in ? ld_scalar(xr + j) : 0.f;
+        dv[u] = in ? ld_scalar(dr + j) : 0.f;
+        gv[u] = in ? ld_scalar(gp + j) : 0.f;
+        rv[u] = (DRES && in) ? ld_scalar(rr + j) : 0.f;
+        pv[u] = (prow && in) ? prow[j] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        if (j >= N) continue;
+        float o = r * fmaf(-xv[u], c, gv[u] * dv[u]);
+        if (DRES) o += rv[u];
+        st_scalar(dxr + j, o);
+        if (prow) prow[j] = fmaf(dv[u] * xv[u], r, pv[u]);
+      }
     }
   }
 }

@@ -28,6 +28,11 @@
 namespace rmsn {
 namespace {
 
+// Scalar loads each thread issues per operand before using any, in the
+// kernels for rows that are not 16-byte aligned (a warp keeps that many
+// requests in flight instead of one).
+constexpr int kGenericBatch = 4;
+
 // Row reductions: G lanes (shuffles only) or, with G = 0, the whole CTA
 // (shuffles, then shared memory; `parity` alternates per call).
 template <int G>
@@ -891,16 +896,29 @@ __global__ void __launch_bounds__(kSubwarpThreads, 2) ln_bwd_rows_staged_kernel(
 template <typename TX>
 __device__ __forceinline__ RowStats generic_stats(const TX* xr, int N, float* red, int& parity,
                                                   float inv_n, float eps) {
+  constexpr int U = kGenericBatch;
   const int tid = threadIdx.x, T = blockDim.x;
   RowStats st;
   float s = 0.f;
-  for (int j = tid; j < N; j += T) s += ld_scalar(xr + j);
+  for (int j0 = tid; j0 < N; j0 += U * T) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = j0 + u * T < N ? ld_scalar(xr + j0 + u * T) : 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) s += v[u];
+  }
   st.m0 = row_sum<0>(s, red, parity) * inv_n;
   float sd = 0.f, sq = 0.f;
-  for (int j = tid; j < N; j += T) {
-    const float d = ld_scalar(xr + j) - st.m0;
-    sd += d;
-    sq = fmaf(d, d, sq);
+  for (int j0 = tid; j0 < N; j0 += U * T) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = j0 + u * T < N ? ld_scalar(xr + j0 + u * T) : st.m0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float d = v[u] - st.m0;   // 0 past the row
+      sd += d;
+      sq = fmaf(d, d, sq);
+    }
   }
   row_sum2<0>(sd, sq, red, parity);
   st.c = sd * inv_n;
@@ -911,6 +929,7 @@ __device__ __forceinline__ RowStats generic_stats(const TX* xr, int N, float* re
 template <typename TX, typename TW>
 __global__ void __launch_bounds__(256) ln_fwd_generic_kernel(const LnParams p) {
   pdl_begin();
+  constexpr int U = kGenericBatch;
   __shared__ float red[128];
   const int tid = threadIdx.x, T = blockDim.x, N = p.N;
   const TW* gam = static_cast<const TW*>(p.gamma);
@@ -924,10 +943,23 @@ __global__ void __launch_bounds__(256) ln_fwd_generic_kernel(const LnParams p) {
       if (p.rstd != nullptr) p.rstd[row] = st.rs;
     }
     TX* yr = static_cast<TX*>(p.y) + row * (int64_t)N;
-    for (int j = tid; j < N; j += T) {
-      const float b = bet ? ld_scalar_ro(bet + j) : 0.f;
-      const float t = ((ld_scalar(xr + j) - st.m0) - st.c) * st.rs;
-      st_scalar(yr + j, fmaf(t, ld_scalar_ro(gam + j), b));
+    for (int j0 = tid; j0 < N; j0 += U * T) {
+      float xv[U], gv[U], bv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        const bool in = j < N;
+        xv[u] = in ? ld_scalar(xr + j) : 0.f;
+        gv[u] = in ? ld_scalar_ro(gam + j) : 0.f;
+        bv[u] = (in && bet) ? ld_scalar_ro(bet + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        if (j >= N) continue;
+        const float t = ((xv[u] - st.m0) - st.c) * st.rs;
+        st_scalar(yr + j, fmaf(t, gv[u], bv[u]));
+      }
     }
   }
 }
@@ -935,6 +967,7 @@ __global__ void __launch_bounds__(256) ln_fwd_generic_kernel(const LnParams p) {
 template <typename TX, typename TW>
 __global__ void __launch_bounds__(256) ln_bwd_generic_kernel(const LnParams p) {
   pdl_begin();
+  constexpr int U = kGenericBatch;
   __shared__ float red[128];
   const int tid = threadIdx.x, T = blockDim.x, N = p.N;
   const TW* gam = static_cast<const TW*>(p.gamma);
@@ -955,22 +988,49 @@ __global__ void __launch_bounds__(256) ln_bwd_generic_kernel(const LnParams p) {
     }
     const float rs = st.rs;
     float a = 0.f, b = 0.f;
-    for (int j = tid; j < N; j += T) {
-      const float xh = ((ld_scalar(xr + j) - st.m0) - st.c) * rs;
-      const float g = ld_scalar(dr + j) * ld_scalar_ro(gam + j);
-      a += g;
-      b = fmaf(g, xh, b);
+    for (int j0 = tid; j0 < N; j0 += U * T) {
+      float xv[U], dv[U], gv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        const bool in = j < N;
+        xv[u] = in ? ld_scalar(xr + j) : 0.f;
+        dv[u] = in ? ld_scalar(dr + j) : 0.f;
+        gv[u] = in ? ld_scalar_ro(gam + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float xh = ((xv[u] - st.m0) - st.c) * rs;
+        const float g = dv[u] * gv[u];   // 0 past the row
+        a += g;
+        b = fmaf(g, xh, b);
+      }
     }
     row_sum2<0>(a, b, red, parity);
     const float mg = a * p.inv_n, mgx = b * p.inv_n;
     TX* dxr = static_cast<TX*>(p.y) + row * (int64_t)N;
-    for (int j = tid; j < N; j += T) {
-      const float xh = ((ld_scalar(xr + j) - st.m0) - st.c) * rs;
-      const float d = ld_scalar(dr + j);
-      st_scalar(dxr + j, rs * (d * ld_scalar_ro(gam + j) - fmaf(xh, mgx, mg)));
-      if (prow) {
-        prow[j] = fmaf(d, xh, prow[j]);
-        prow[p.ld_half + j] += d;
+    for (int j0 = tid; j0 < N; j0 += U * T) {
+      float xv[U], dv[U], gv[U], pg[U], pb[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        const bool in = j < N;
+        xv[u] = in ? ld_scalar(xr + j) : 0.f;
+        dv[u] = in ? ld_scalar(dr + j) : 0.f;
+        gv[u] = in ? ld_scalar_ro(gam + j) : 0.f;
+        pg[u] = (prow && in) ? prow[j] : 0.f;
+        pb[u] = (prow && in) ? prow[p.ld_half + j] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * T;
+        if (j >= N) continue;
+        const float xh = ((xv[u] - st.m0) - st.c) * rs;
+        st_scalar(dxr + j, rs * (dv[u] * gv[u] - fmaf(xh, mgx, mg)));
+        if (prow) {
+          prow[j] = fmaf(dv[u], xh, pg[u]);
+          prow[p.ld_half + j] = pb[u] + dv[u];
+        }
       }
     }
   }
