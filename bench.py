@@ -378,6 +378,7 @@ def run_ours(args, rank, world):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     done = [None] * len(ops)       # last device->host copy of each op's previous step
     e0.record(s_in)
+    t_host = time.perf_counter()
     for _ in range(Ke):
         for j, (op, (hin, hout)) in enumerate(zip(ops, pin)):
             wl = op["wl"]
@@ -407,6 +408,7 @@ def run_ours(args, rank, world):
     for ev_done in done:
         s_in.wait_event(ev_done)
     e1.record(s_in)
+    host_ms = (time.perf_counter() - t_host) * 1e3 / Ke   # enqueueing, not waiting
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, world, dev)
 
@@ -436,6 +438,7 @@ def run_ours(args, rank, world):
            "pipeline": f"3 streams (copy in / kernels / copy out), fwd and fused add in "
                        f"{chunks} row chunks",
            "copy_bound_ms_per_step": round(copy_ms, 3),
+           "host_enqueue_ms_per_step": round(host_ms, 3),
            "frac_of_copy_bound": round(copy_ms / e2e_ms, 4),
            "copy_bound": "the same host<->device copies alone (no kernels, no dependencies, "
                          "both directions at once), timed on this GPU"}
