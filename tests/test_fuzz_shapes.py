@@ -6,6 +6,8 @@ cluster rows all occur) and a layout class with byte offsets of the operands
 on the element grid (all aligned, all on one residue modulo 16, inputs off
 the outputs' alignment, every operand anywhere), so the families and their
 boundaries are crossed in combinations no hand-written list enumerates.
+LayerNorm (forward, backward with saved or recomputed statistics) and the
+quantised outputs (FP8, NVFP4; plain or fused add) get their own draws.
 """
 import numpy as np
 import pytest
@@ -108,3 +110,72 @@ def test_draws_cover_the_families():
             seen.add("mixed")
         seen.add("short" if N * es <= 2048 else ("long" if N * es > 65536 else "cta"))
     assert {"aligned", "ragged", "same residue", "mixed", "short", "cta", "long"} <= seen, seen
+
+
+# ---------------------------------------------------------------- LayerNorm
+# and quantised outputs: the same seeded draws for their own entry points
+
+from tests import test_parity_layernorm as tl  # noqa: E402
+from tests import test_parity_quant as tq  # noqa: E402
+
+LN_CASES = 40
+Q_CASES = 40
+
+
+def draw_ln(i):
+    rng = np.random.default_rng(3000 + i)
+    xd, wd = PAIRS[rng.integers(len(PAIRS))]
+    bwd = bool(rng.integers(2))
+    saved = bool(rng.integers(2))
+    N = (max(1, int(np.exp(rng.uniform(0.0, np.log(40000.0))))) if rng.random() < 0.5
+         else 64 * int(rng.integers(2, 257)))
+    M = int(rng.integers(1, max(2, min(600, 3_000_000 // N + 1))))
+    es = 4 if xd == "f32" else 2
+    aligned = rng.random() < 0.6
+    offsets = {} if aligned else {k: int(rng.integers(0, 16 // es)) * es
+                                  for k in (["x", "dy", "dx"] if bwd else ["x", "y"])}
+    return xd, wd, bwd, saved, M, N, offsets
+
+
+@pytest.mark.parametrize("i", range(LN_CASES))
+def test_random_layernorm_case_matches_oracle(i):
+    xd, wd, bwd, saved, M, N, offsets = draw_ln(i)
+    eps = float(np.float32(1e-5))
+    x, g, b, dy = tl.inputs(M, N, xd, wd, seed=7000 + i, beta=not bwd)
+    if not bwd:
+        out = tl.run_fwd(x, g, b, eps, xd, wd, offsets=offsets)
+        tl.check_fwd(out, x, g, b, eps, xd, wd)
+        return
+    mean = rstd = None
+    if saved:
+        fw = oracle.layernorm_fwd(x, g, None, eps, xd, wd)
+        mean, rstd = fw["mean"], fw["rstd"]
+    out = tl.run_bwd(dy, x, mean, rstd, g, eps, xd, wd, offsets=offsets)
+    tl.check_bwd(out, dy, x, mean, rstd, g, eps, xd, wd)
+
+
+def draw_q(i):
+    rng = np.random.default_rng(4000 + i)
+    xd, wd = PAIRS[rng.integers(len(PAIRS))]
+    kind = "fp8" if rng.integers(2) else "nvfp4"
+    fused = bool(rng.integers(2))
+    N = 16 * int(np.exp(rng.uniform(0.0, np.log(2500.0))))   # NVFP4 blocks of 16
+    if kind == "fp8" and rng.random() < 0.3:
+        N += int(rng.integers(1, 16))
+    M = int(rng.integers(1, max(2, min(500, 2_000_000 // N + 1))))
+    es = 4 if xd == "f32" else 2
+    offsets = {} if rng.random() < 0.6 else {"x": int(rng.integers(0, 16 // es)) * es}
+    return xd, wd, kind, fused, M, N, offsets
+
+
+@pytest.mark.parametrize("i", range(Q_CASES))
+def test_random_quantised_case_matches_oracle(i):
+    xd, wd, kind, fused, M, N, offsets = draw_q(i)
+    eps = float(np.float32(1e-6))
+    x, g, r = tq.inputs(M, N, xd, wd, seed=8000 + i, fused=fused)
+    if kind == "fp8":
+        out = tq.run("fp8", x, g, eps, xd, wd, residual=r, offsets=offsets)
+        tq.check_fp8(out, x, g, eps, xd, wd, residual=r)
+    else:
+        out = tq.run("nvfp4", x, g, eps, xd, wd, residual=r, gs=tq.GS, offsets=offsets)
+        tq.check_nvfp4(out, x, g, eps, xd, wd, tq.GS, residual=r)
