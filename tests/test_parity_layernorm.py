@@ -97,7 +97,12 @@ def _bf16_with_floor(gpu_bits, ref_bits, ref64, floor, what):
         bad = strict & ~ok
         assert not bad.any(), (f"{what}: {int(bad.sum())} elements beyond 2 ulp and the "
                                f"cancellation floor, at {np.argwhere(bad)[:5].tolist()}")
-        assert strict.sum() <= max(2, 1e-4 * d.size), (
+        # rows shorter than 32 cancel by construction (N = 1: x - mean = 0 and
+        # dx = 0 exactly; N = 2: xhat = +-sqrt(var / (var + eps)), so dx is an
+        # eps-sized sliver of its terms), so the count is capped for longer
+        # rows only, as for the RMSNorm dx
+        N = d.shape[-1] if d.ndim > 1 else d.size
+        assert N < 32 or strict.sum() <= max(2, 1e-4 * d.size), (
             f"{what}: {int(strict.sum())} of {d.size} elements needed the cancellation floor")
     return int(strict.sum())
 
@@ -134,13 +139,21 @@ def check_bwd(out, dy, x, mean, rstd, g, eps, xd, wd):
     xh = (x64 - mu[:, None]) * r[:, None]
     gg = dy64 * g64[None, :]
     n = 0
+    N = x.shape[1]
+    # xhat = (x - mean) r itself carries the cancellation of x - mean
+    xh_mag = np.abs(xh) + r[:, None] * (np.abs(x64) + np.abs(x64).mean(axis=1, keepdims=True))
+    floor = 64 * U32 * r[:, None] * (np.abs(gg) + np.abs(gg).sum(1, keepdims=True) / N +
+                                     xh_mag * np.abs(gg * xh).sum(1, keepdims=True) / N)
     if xd == "bf16":
-        N = x.shape[1]
-        # xhat = (x - mean) r itself carries the cancellation of x - mean
-        xh_mag = np.abs(xh) + r[:, None] * (np.abs(x64) + np.abs(x64).mean(axis=1, keepdims=True))
-        floor = 64 * U32 * r[:, None] * (np.abs(gg) + np.abs(gg).sum(1, keepdims=True) / N +
-                                         xh_mag * np.abs(gg * xh).sum(1, keepdims=True) / N)
         n = _bf16_with_floor(out["dx"], ref["dx"], ref["dx64"], floor, "dx")
+    elif N < 32:
+        # rows shorter than 32 cancel by construction (N = 1: dx = 0 exactly,
+        # its terms r dy gamma with r up to eps^-1/2): the floor on the terms'
+        # scale joins 1e-5 (1 + |ref|) there (reading R22)
+        err = np.abs(out["dx"].astype(np.float64) - ref["dx64"])
+        lim = 1e-5 * (1 + np.abs(ref["dx64"])) + floor
+        assert (err <= lim).all(), (f"dx: {int((err > lim).sum())} elements beyond "
+                                    f"1e-5(1+|ref|) and the cancellation floor")
     else:
         pu.check_f32(out["dx"], ref["dx64"], what="dx")
     if "dgamma" in out:
