@@ -796,7 +796,7 @@ def run_sweep(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = args.workloads.split(",") if args.workloads else [
         n for n, w in si.WORKLOADS.items()
-        if set(w.tags) & {"sweep", "headline", "next", "mixed", "generic"}]
+        if set(w.tags) & {"sweep", "headline", "next", "mixed", "wide"}]
     for name in names:
         wl = si.WORKLOADS[name]
         inp = si.make_inputs(wl)

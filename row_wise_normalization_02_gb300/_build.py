@@ -1,8 +1,8 @@
 """Build librmsnorm_gb300.so in-tree with nvcc for sm_103a.
 
-Twenty-five translation units (forward, backward, staged, ragged, mixed-alignment
-ragged, cluster, quantised-output and LayerNorm kernels once per dtype pair, plus
-the C ABI)
+Twenty-eight translation units (forward, backward, staged, ragged, mixed-alignment
+ragged, cluster, wide, quantised-output and LayerNorm kernels once per dtype pair,
+plus the C ABI)
 compile in parallel, then link into one shared library with the CUDA runtime
 linked statically.  Rebuilds only when a source is newer than the library.
 """
@@ -48,6 +48,9 @@ UNITS = [("rmsnorm_fwd.cu", ["-DRMSN_PAIR=0"], "fwd_p0.o"),
          ("rmsnorm_cluster.cu", ["-DRMSN_PAIR=0"], "cluster_p0.o"),
          ("rmsnorm_cluster.cu", ["-DRMSN_PAIR=1"], "cluster_p1.o"),
          ("rmsnorm_cluster.cu", ["-DRMSN_PAIR=2"], "cluster_p2.o"),
+         ("rmsnorm_wide.cu", ["-DRMSN_PAIR=0"], "wide_p0.o"),
+         ("rmsnorm_wide.cu", ["-DRMSN_PAIR=1"], "wide_p1.o"),
+         ("rmsnorm_wide.cu", ["-DRMSN_PAIR=2"], "wide_p2.o"),
          ("rmsnorm_api.cu", [], "api.o")]
 
 

@@ -58,6 +58,12 @@ FwdKernel fwd_kernel(const FwdKey& k) {
       return k.mix ? get_fwd_ragged_mix_bf16_f32(k) : get_fwd_ragged_bf16_f32(k);
     return nullptr;
   }
+  if (k.family == kWide) {
+    if (k.xd == kF32 && k.wd == kF32) return get_fwd_wide_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16) return get_fwd_wide_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32) return get_fwd_wide_bf16_f32(k);
+    return nullptr;
+  }
   if (k.family == kCluster) {
     if (k.xd == kF32 && k.wd == kF32) return get_fwd_cluster_f32_f32(k);
     if (k.xd == kBF16 && k.wd == kBF16) return get_fwd_cluster_bf16_bf16(k);
@@ -80,6 +86,12 @@ BwdKernel bwd_kernel(const BwdKey& k) {
       return k.mix ? get_bwd_ragged_mix_bf16_bf16(k) : get_bwd_ragged_bf16_bf16(k);
     if (k.xd == kBF16 && k.wd == kF32)
       return k.mix ? get_bwd_ragged_mix_bf16_f32(k) : get_bwd_ragged_bf16_f32(k);
+    return nullptr;
+  }
+  if (k.family == kWide) {
+    if (k.xd == kF32 && k.wd == kF32) return get_bwd_wide_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16) return get_bwd_wide_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32) return get_bwd_wide_bf16_f32(k);
     return nullptr;
   }
   if (k.family == kCluster) {
@@ -385,6 +397,7 @@ Force parse_force(const char* s) {
   else if (!strcmp(tok, "generic")) f.family = kGeneric;
   else if (!strcmp(tok, "staged")) f.family = kStaged;
   else if (!strcmp(tok, "cluster")) f.family = kCluster;
+  else if (!strcmp(tok, "wide")) f.family = kWide;
   while ((tok = strtok_r(nullptr, ":", &save))) {
     char* eq = strchr(tok, '=');
     if (!eq) continue;
@@ -419,6 +432,20 @@ DebugEnv g_env = read_debug_env();
 
 const Force& read_force() { return g_env.force; }
 long long wait_limit() { return g_env.wait_limit; }
+
+// kWide: the backward keeps its dgamma partial row (N columns, plus a
+// vector's worth on each side for the head and tail of dx's split) in shared
+// memory, and needs dx's split to be the same for every row.
+int64_t wide_smem(int N, int xd) { return round_up(N + 2 * per_vec(xd), 4) * 4LL; }
+bool wide_ok(bool bwd, int N, int xd) {
+  return !bwd || (((int64_t)N * esize(xd)) % 16 == 0 && wide_smem(N, xd) <= kStagedSmemMax);
+}
+// Threads of a wide CTA: about two vectors of the row per thread, 64 to
+// kWideThreads.
+int wide_threads(int N, int E) {
+  const int t = round_up((N / E + 2) / 2, 32);
+  return t < 64 ? 64 : (t > kWideThreads ? kWideThreads : t);
+}
 
 // Choose the variant.  aligned16: all base pointers 16-byte aligned;
 // same_mod16: all activation base pointers agree modulo 16 bytes.
@@ -510,8 +537,19 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
   } else {
     p.family = kGeneric;
   }
+  // what the register, ring and cluster kernels do not take: two passes of
+  // 16-byte vectors (every operand realigned to the pass's frame) where that
+  // kernel applies, else the scalar one
+  if (p.family == kGeneric && wide_ok(bwd, N, xd)) p.family = kWide;
   if (p.family == kGeneric) {
     p.threads = 256;
+    p.g = p.vpt = 0;
+    p.prefetch = false;
+    p.mix = false;
+    p.period = 1;
+  }
+  if (p.family == kWide) {
+    p.threads = wide_threads(N, E);
     p.g = p.vpt = 0;
     p.prefetch = false;
     p.mix = false;
@@ -585,6 +623,11 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     } else if (p.family == kGeneric) {
       if (!f.threads) p.threads = 256;
       if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
+    } else if (p.family == kWide) {
+      if (!wide_ok(bwd, N, xd)) return RMSNORM_ERR_INVALID_ARG;
+      if (!f.threads) p.threads = wide_threads(N, E);
+      p.g = p.vpt = 0;
+      p.prefetch = false;
     }
     if (p.family != kCluster) p.cluster = p.slice = 0;
     if (p.family != kSubwarp && !(p.family == kStaged && p.g > 0)) p.rows_per_cta = 1;
@@ -643,6 +686,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     if (p.family == kSubwarp) p.smem = p.rows_per_cta * nvec * E * 4;
     else if (p.family == kCta) p.smem = 512 + (p.acc_smem ? ld * 4 : 0);
     else if (p.family == kRagged) p.smem = 512;
+    else if (p.family == kWide) p.smem = (int)wide_smem(N, xd);
     else if (p.family == kCluster) {
       // ring of the slice of [x | dy] ([h | dy | dres]) rows
       const int64_t bytes = kStagedHeader + (int64_t)p.stages * (dres ? 3 : 2) * p.slice * 16;
@@ -719,6 +763,7 @@ const char* family_name(int f) {
     case kRagged: return "ragged";
     case kStaged: return "staged";
     case kCluster: return "cluster";
+    case kWide: return "wide";
     default: return "generic";
   }
 }
@@ -1484,6 +1529,12 @@ rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, 
   }
   if ((st = size_grid(&pl, M, device)) != RMSNORM_OK) return st;
   *rows = pl.cluster > 0 ? pl.grid / pl.cluster : pl.grid;   // a partial row per cluster
+  // operands at other offsets may take the wide kernel, whose grid (one row
+  // per CTA, several CTAs per SM) the aligned plan's need not bound
+  Plan pw;
+  if (make_plan(kBwd, M, N, xd, wd, false, false, true, &pw) == RMSNORM_OK &&
+      pw.family == kWide && size_grid(&pw, M, device) == RMSNORM_OK && pw.grid > *rows)
+    *rows = pw.grid;
   return RMSNORM_OK;
 }
 

@@ -28,8 +28,12 @@ enum DT : int { kF32 = 0, kBF16 = 1 };
 //             registers; backward: through a bulk-copy ring); the CTAs' sums
 //             meet in distributed shared memory.  For rows too long for one
 //             CTA; rows 16-byte aligned.
+//  kWide    : any N, any element-aligned pointers (backward: rows a multiple
+//             of 16 bytes, the dgamma partial row in shared memory); two
+//             passes of 16-byte vectors per row, each pass in the frame of one
+//             operand's alignment with the others realigned to it.
 enum Family : int { kSubwarp = 0, kCta = 1, kRagged = 2, kGeneric = 3, kStaged = 4,
-                    kCluster = 5 };
+                    kCluster = 5, kWide = 6 };
 
 // Forward output kinds: y in the activation dtype, FP8 E4M3 codes with one
 // scale per row, or NVFP4 (E2M1 codes, an E4M3 scale per 16 elements).
@@ -192,6 +196,12 @@ FwdKernel get_fwd_cluster_bf16_f32(const FwdKey& k);
 BwdKernel get_bwd_cluster_f32_f32(const BwdKey& k);
 BwdKernel get_bwd_cluster_bf16_bf16(const BwdKey& k);
 BwdKernel get_bwd_cluster_bf16_f32(const BwdKey& k);
+FwdKernel get_fwd_wide_f32_f32(const FwdKey& k);
+FwdKernel get_fwd_wide_bf16_bf16(const FwdKey& k);
+FwdKernel get_fwd_wide_bf16_f32(const FwdKey& k);
+BwdKernel get_bwd_wide_f32_f32(const BwdKey& k);
+BwdKernel get_bwd_wide_bf16_bf16(const BwdKey& k);
+BwdKernel get_bwd_wide_bf16_f32(const BwdKey& k);
 FwdKernel get_fwd_quant_f32_f32(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_bf16(const FwdKey& k);
 FwdKernel get_fwd_quant_bf16_f32(const FwdKey& k);
@@ -213,6 +223,9 @@ LnKernel get_ln_kernel_bf16_f32(const LnKey& k);
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;
 constexpr int kCtaMaxThreads = 512;
+// Most threads of a kWide CTA (built for two CTAs per SM, 64 registers a
+// thread).
+constexpr int kWideThreads = 512;
 // Threads of a stage-2 (column sum) CTA.
 constexpr int kColSumThreads = 256;
 

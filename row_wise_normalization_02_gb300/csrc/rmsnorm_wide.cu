@@ -1,0 +1,415 @@
+// kWide: rows of any length whose operands start at any element-aligned
+// offsets, read and written as 16-byte vectors.  One CTA per row (persistent
+// walk over rows), two passes over each row:
+//   pass 1 reduces the row in the frame of one operand -- x for the forward
+//   and the backward, the residual (which receives h) for the fused add: that
+//   operand's row splits into a scalar head (elements before its first
+//   16-byte boundary), a body of 16-byte vectors and a scalar tail;
+//   pass 2 writes the output in the output's own frame.
+// Every other operand is read in the pass's frame: the frame's body vector v
+// covers 16 bytes of that operand which start s bytes into one of its aligned
+// chunks (s: the difference of the two rows' start addresses modulo 16), so
+// two aligned chunk loads and one byte funnel give it.  No load or store is
+// misaligned whatever the offsets; DRAM sees each byte once, pass 2 re-reading
+// the row from L1 or L2 (a row of tens of KB, read moments before), and a
+// shifted operand's second chunk is the neighbouring vector's first.
+//
+// The backward's dgamma partial row accumulates in shared memory, each column
+// always by the same thread in the CTA's row order (rows a multiple of 16
+// bytes, so dx's split is the same for every row); it is written to the
+// workspace once, at the end.
+//
+// The arithmetic per element is that of the register kernels: the sum of
+// squares (fused add: of h = round(r + x)), rs = 1/sqrt(ss/N + eps),
+// y = x rs gamma (bf16 x and gamma: (x gamma) rs), one rounding per output;
+// dx = r (gamma dy - x c) with c = r^2/N sum gamma dy x ("Pre-built kernel
+// library guide", 1.2 RMSNorm; the backward derived from its forward).
+#include <type_traits>
+
+#include "rmsnorm_bwd_common.cuh"
+#include "rmsnorm_device.cuh"
+#include "rmsnorm_fwd_common.cuh"
+#include "rmsnorm_internal.h"
+
+#ifndef RMSN_PAIR
+#define RMSN_PAIR 1
+#endif
+
+namespace rmsn {
+namespace {
+
+// Split of a row of N elements of es bytes starting at `row`: x = elements
+// before the first 16-byte boundary (at most N), y = whole 16-byte vectors
+// after them; the rest is the tail.
+__device__ __forceinline__ int2 split_row(const void* row, int N, int es) {
+  int head = (int)(((16u - ((unsigned)reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) / es);
+  if (head > N) head = N;
+  return make_int2(head, (int)(((int64_t)(N - head) * es) >> 4));
+}
+
+// An operand read in another row's frame: the frame's body vector v is the
+// 16 bytes at c + 16 v + s (c 16-byte aligned, 0 <= s < 16).
+struct Src {
+  const char* c;
+  int s;
+};
+__device__ __forceinline__ Src src_of(const void* row, int head, int es) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(row) + (uintptr_t)head * es;
+  return Src{reinterpret_cast<const char*>(a & ~(uintptr_t)15), (int)(a & 15)};
+}
+
+// Read of a chunk: read-only data that pass 2 re-reads (L1 allocation),
+// read-only data read once (no L1 allocation), or data this kernel writes
+// (h; the residual-path gradient beside dx) on the coherent path.
+enum Ld : int { kLdKeep = 0, kLdOnce = 1, kLdRw = 2 };
+template <int LD>
+__device__ __forceinline__ uint4 ld_chunk(const char* p) {
+  if constexpr (LD == kLdKeep) return ld_cached(p);
+  else if constexpr (LD == kLdOnce) return ld_stream(p);
+  else return ld_rw(p);
+}
+
+// Body vector v of an operand in the frame.  The second chunk is read only
+// when the operand is shifted: it then holds bytes of this row (the vector's
+// last s bytes), so it lies in the row's enclosing 16-byte span.
+template <int LD>
+__device__ __forceinline__ uint4 vec_at(const Src& o, int v) {
+  const char* p = o.c + (size_t)v * 16;
+  const uint4 lo = ld_chunk<LD>(p);
+  if (o.s == 0) return lo;
+  return realign_pair(lo, ld_chunk<LD>(p + 16), o.s);
+}
+
+// The GW gamma chunks (E columns) of body vector v in the frame.
+template <int GW>
+__device__ __forceinline__ void gamma_at(const Src& g, int v, uint4 (&out)[GW]) {
+  const char* p = g.c + (size_t)v * GW * 16;
+  uint4 c[GW + 1];
+#pragma unroll
+  for (int w = 0; w < GW; ++w) c[w] = ld_cached(p + w * 16);
+  if (g.s == 0) {
+#pragma unroll
+    for (int w = 0; w < GW; ++w) out[w] = c[w];
+    return;
+  }
+  c[GW] = ld_cached(p + GW * 16);
+#pragma unroll
+  for (int w = 0; w < GW; ++w) out[w] = realign_pair(c[w], c[w + 1], g.s);
+}
+
+__device__ __forceinline__ void st_plain(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Scalar read of data this kernel wrote (h), through L2.
+template <typename T>
+__device__ __forceinline__ float ld_scalar_cg(const T* p) {
+  if constexpr (std::is_same<T, float>::value) {
+    return __ldcg(p);
+  } else {
+    const unsigned short b = __ldcg(reinterpret_cast<const unsigned short*>(p));
+    return __uint_as_float((uint32_t)b << 16);
+  }
+}
+
+template <typename TX>
+__device__ __forceinline__ void vec_sumsq(const uint4& v, float& a0, float& a1) {
+  if constexpr (std::is_same<TX, bf16>::value) {
+    bf16x8_sumsq(v, a0, a1);
+  } else {
+    float f[4];
+    unpack(v, f);
+    a0 = fmaf(f[0], f[0], a0);
+    a1 = fmaf(f[1], f[1], a1);
+    a0 = fmaf(f[2], f[2], a0);
+    a1 = fmaf(f[3], f[3], a1);
+  }
+}
+
+// The scalar form of scale_vec.
+template <typename TX, typename TW>
+__device__ __forceinline__ float scale_scalar(float x, float g, float rs) {
+  if constexpr (std::is_same<TX, bf16>::value && std::is_same<TW, bf16>::value)
+    return (x * g) * rs;
+  else
+    return x * rs * g;
+}
+
+// Element of the head or the tail of a split (head, nv) that thread tid
+// handles, or -1: head elements on the first threads, tail elements on the
+// last (both fewer than a vector's elements).
+template <int E>
+__device__ __forceinline__ int edge_elem(int2 f, int N, int tid, int T) {
+  if (tid < f.x) return tid;
+  const int t0 = f.x + f.y * E;
+  const int k = T - 1 - tid;
+  return k < N - t0 ? t0 + k : -1;
+}
+
+// ---------------------------------------------------------------- forward
+
+template <typename TX, typename TW, bool FUSED>
+__global__ void __launch_bounds__(kWideThreads, 2) fwd_wide_kernel(const FwdParams p) {
+  pdl_begin();
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
+  constexpr int U1 = FUSED ? 2 : 4;   // vectors per thread in flight, pass 1
+  constexpr int U2 = 2;               // and pass 2
+  __shared__ float red[64];
+  const int tid = threadIdx.x, T = blockDim.x, N = p.N;
+  const size_t rb = (size_t)N * ES;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const char* xr = static_cast<const char*>(p.x) + row * rb;
+    char* hr = FUSED ? static_cast<char*>(p.residual) + row * rb : nullptr;
+    char* yr = static_cast<char*>(p.y) + row * rb;
+    float s0 = 0.f, s1 = 0.f;
+    {  // pass 1: the sum of squares in the frame of x (fused: of the residual)
+      const char* fr = FUSED ? hr : xr;
+      const int2 f = split_row(fr, N, ES);
+      const char* fb = fr + (size_t)f.x * ES;
+      char* hb = FUSED ? hr + (size_t)f.x * ES : nullptr;
+      if constexpr (!FUSED) {
+        for (int v0 = tid; v0 < f.y; v0 += U1 * T) {
+          uint4 a[U1];
+#pragma unroll
+          for (int u = 0; u < U1; ++u) {
+            const int v = v0 + u * T;
+            a[u] = v < f.y ? ld_cached(fb + (size_t)v * 16) : zero;
+          }
+#pragma unroll
+          for (int u = 0; u < U1; ++u) vec_sumsq<TX>(a[u], s0, s1);
+        }
+      } else {
+        const Src xs = src_of(xr, f.x, ES);
+        for (int v0 = tid; v0 < f.y; v0 += U1 * T) {
+          uint4 a[U1], r[U1];
+#pragma unroll
+          for (int u = 0; u < U1; ++u) {
+            const int v = v0 + u * T;
+            r[u] = v < f.y ? ld_rw(fb + (size_t)v * 16) : zero;
+            a[u] = v < f.y ? vec_at<kLdOnce>(xs, v) : zero;
+          }
+#pragma unroll
+          for (int u = 0; u < U1; ++u) {
+            float hf[E], rf[E];
+            unpack(a[u], hf);
+            unpack(r[u], rf);
+#pragma unroll
+            for (int e = 0; e < E; ++e) hf[e] += rf[e];
+            const uint4 h = pack(hf);   // rounds to TX (nearest even)
+            const int v = v0 + u * T;
+            if (v < f.y) st_plain(hb + (size_t)v * 16, h);
+            vec_sumsq<TX>(h, s0, s1);
+          }
+        }
+      }
+      const int j = edge_elem<E>(f, N, tid, T);
+      if (j >= 0) {
+        float v = ld_scalar(reinterpret_cast<const TX*>(xr) + j);
+        if (FUSED) {
+          v = round_to(v + ld_scalar(reinterpret_cast<const TX*>(hr) + j), (TX*)nullptr);
+          st_scalar(reinterpret_cast<TX*>(hr) + j, v);
+        }
+        s0 = fmaf(v, v, s0);
+      }
+    }
+    float ss[1] = {s0 + s1};
+    cta_sum<1>(ss, red, parity);   // its barrier also publishes h to the CTA
+    parity ^= 1;
+    const float rs = rsqrtf(fmaf(ss[0], p.inv_n, p.eps));
+    if (tid == 0 && p.rstd != nullptr) p.rstd[row] = rs;
+    {  // pass 2: y in its own frame
+      const int2 f = split_row(yr, N, ES);
+      char* yb = yr + (size_t)f.x * ES;
+      const Src xs = src_of(FUSED ? hr : xr, f.x, ES);
+      const Src gs = src_of(p.gamma, f.x, WS);
+      for (int v0 = tid; v0 < f.y; v0 += U2 * T) {
+        uint4 a[U2], g[U2][GW];
+#pragma unroll
+        for (int u = 0; u < U2; ++u) {
+          const int v = v0 + u * T;
+          if (v < f.y) {
+            a[u] = vec_at<FUSED ? kLdRw : kLdKeep>(xs, v);
+            gamma_at<GW>(gs, v, g[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U2; ++u) {
+          const int v = v0 + u * T;
+          if (v < f.y) st_stream(yb + (size_t)v * 16, scale_vec<TX, TW>(a[u], g[u], rs));
+        }
+      }
+      const int j = edge_elem<E>(f, N, tid, T);
+      if (j >= 0) {
+        const float v = FUSED ? ld_scalar_cg(reinterpret_cast<const TX*>(hr) + j)
+                              : ld_scalar(reinterpret_cast<const TX*>(xr) + j);
+        const float g = ld_scalar_ro(static_cast<const TW*>(p.gamma) + j);
+        st_scalar(reinterpret_cast<TX*>(yr) + j, scale_scalar<TX, TW>(v, g, rs));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- backward
+
+template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
+__global__ void __launch_bounds__(kWideThreads, 2) bwd_wide_kernel(const BwdParams p) {
+  pdl_begin();
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
+  constexpr int K = HAS_RSTD ? 1 : 2;
+  constexpr int U1 = 2, U2 = 1;
+  // dgamma partial row: column j at acc_s[j - head + E], head = dx's head
+  extern __shared__ __align__(16) float acc_s[];
+  __shared__ float red[2 * 2 * 32];
+  const int tid = threadIdx.x, T = blockDim.x, N = p.N;
+  const size_t rb = (size_t)N * ES;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const bool dg = p.partial != nullptr;
+  const int2 fo = split_row(p.dx, N, ES);   // the same for every row
+  if (dg)
+    for (int i = tid; i < N + 2 * E; i += T) acc_s[i] = 0.f;
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const char* xr = static_cast<const char*>(p.x) + row * rb;
+    const char* dr = static_cast<const char*>(p.dy) + row * rb;
+    char* dxr = static_cast<char*>(p.dx) + row * rb;
+    const char* rr = DRES ? static_cast<const char*>(p.dres) + row * rb : nullptr;
+    float2 dot = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
+    {  // pass 1: sum gamma dy x (and sum x^2) in the frame of x
+      const int2 f = split_row(xr, N, ES);
+      const char* xb = xr + (size_t)f.x * ES;
+      const Src ds = src_of(dr, f.x, ES), gs = src_of(p.gamma, f.x, WS);
+      for (int v0 = tid; v0 < f.y; v0 += U1 * T) {
+        uint4 a[U1], d[U1], g[U1][GW];
+#pragma unroll
+        for (int u = 0; u < U1; ++u) {
+          const int v = v0 + u * T;
+          if (v < f.y) {
+            a[u] = ld_cached(xb + (size_t)v * 16);
+            d[u] = vec_at<kLdKeep>(ds, v);
+            gamma_at<GW>(gs, v, g[u]);
+          } else {
+            a[u] = d[u] = zero;
+#pragma unroll
+            for (int w = 0; w < GW; ++w) g[u][w] = zero;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U1; ++u) {
+          float gf[E];
+          unpack_gamma<TW, E, GW>(g[u], gf);
+          bwd_vec_sums<E, !HAS_RSTD>(a[u], d[u], gf, dot, sq);
+        }
+      }
+      const int j = edge_elem<E>(f, N, tid, T);
+      if (j >= 0) {
+        const float xv = ld_scalar(reinterpret_cast<const TX*>(xr) + j);
+        const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + j);
+        const float gv = ld_scalar_ro(static_cast<const TW*>(p.gamma) + j);
+        dot.x = fmaf(gv * dv, xv, dot.x);
+        if (!HAS_RSTD) sq.x = fmaf(xv, xv, sq.x);
+      }
+    }
+    float sums[K];
+    sums[0] = dot.x + dot.y;
+    if (!HAS_RSTD) sums[K - 1] = sq.x + sq.y;
+    cta_sum<K>(sums, red, parity);
+    parity ^= 1;
+    const float r = HAS_RSTD ? __ldg(p.rstd + row) : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
+    const float c = r * r * p.inv_n * sums[0];
+    {  // pass 2: dx in its own frame, and the dgamma partial
+      char* ob = dxr + (size_t)fo.x * ES;
+      const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES),
+                gs = src_of(p.gamma, fo.x, WS);
+      const Src rs = DRES ? src_of(rr, fo.x, ES) : Src{nullptr, 0};
+      for (int v0 = tid; v0 < fo.y; v0 += U2 * T) {
+        uint4 a[U2], d[U2], q[U2], g[U2][GW];
+#pragma unroll
+        for (int u = 0; u < U2; ++u) {
+          const int v = v0 + u * T;
+          if (v < fo.y) {
+            a[u] = vec_at<kLdKeep>(xs, v);
+            d[u] = vec_at<kLdKeep>(ds, v);
+            q[u] = DRES ? vec_at<kLdRw>(rs, v) : zero;
+            gamma_at<GW>(gs, v, g[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U2; ++u) {
+          const int v = v0 + u * T;
+          if (v >= fo.y) continue;
+          float gf[E], acc[E];
+          unpack_gamma<TW, E, GW>(g[u], gf);
+          float4* ap = reinterpret_cast<float4*>(acc_s + E + (size_t)v * E);
+#pragma unroll
+          for (int w = 0; w < E / 4; ++w) {
+            const float4 t = dg ? ap[w] : make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[4 * w] = t.x;
+            acc[4 * w + 1] = t.y;
+            acc[4 * w + 2] = t.z;
+            acc[4 * w + 3] = t.w;
+          }
+          const uint4 o = bwd_vec_apply<E, DRES>(a[u], d[u], q[u], gf, r, c, acc);
+          st_stream(ob + (size_t)v * 16, o);
+          if (dg) {
+#pragma unroll
+            for (int w = 0; w < E / 4; ++w)
+              ap[w] = make_float4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]);
+          }
+        }
+      }
+      const int j = edge_elem<E>(fo, N, tid, T);
+      if (j >= 0) {
+        const float xv = ld_scalar(reinterpret_cast<const TX*>(xr) + j);
+        const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + j);
+        const float gv = ld_scalar_ro(static_cast<const TW*>(p.gamma) + j);
+        float o = r * fmaf(-xv, c, gv * dv);
+        if (DRES) o += ld_scalar_cg(reinterpret_cast<const TX*>(rr) + j);
+        st_scalar(reinterpret_cast<TX*>(dxr) + j, o);
+        if (dg) {
+          float* a = acc_s + (j - fo.x + E);
+          *a = fmaf(dv * xv, r, *a);
+        }
+      }
+    }
+  }
+  if (dg) {
+    __syncthreads();
+    float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
+    for (int j = tid; j < N; j += T) prow[j] = acc_s[j - fo.x + E];
+  }
+}
+
+template <typename TX, typename TW>
+FwdKernel pick_fwd(const FwdKey& k) {
+  if (k.family != kWide || k.strided || k.out != kOutDtype) return nullptr;
+  return k.fused ? fwd_wide_kernel<TX, TW, true> : fwd_wide_kernel<TX, TW, false>;
+}
+
+template <typename TX, typename TW>
+BwdKernel pick_bwd(const BwdKey& k) {
+  if (k.family != kWide) return nullptr;
+  if (k.dres)
+    return k.has_rstd ? bwd_wide_kernel<TX, TW, true, true> : bwd_wide_kernel<TX, TW, false, true>;
+  return k.has_rstd ? bwd_wide_kernel<TX, TW, true, false> : bwd_wide_kernel<TX, TW, false, false>;
+}
+
+}  // namespace
+
+#if RMSN_PAIR == 0
+FwdKernel get_fwd_wide_f32_f32(const FwdKey& k) { return pick_fwd<float, float>(k); }
+BwdKernel get_bwd_wide_f32_f32(const BwdKey& k) { return pick_bwd<float, float>(k); }
+#elif RMSN_PAIR == 1
+FwdKernel get_fwd_wide_bf16_bf16(const FwdKey& k) { return pick_fwd<bf16, bf16>(k); }
+BwdKernel get_bwd_wide_bf16_bf16(const BwdKey& k) { return pick_bwd<bf16, bf16>(k); }
+#else
+FwdKernel get_fwd_wide_bf16_f32(const FwdKey& k) { return pick_fwd<bf16, float>(k); }
+BwdKernel get_bwd_wide_bf16_f32(const BwdKey& k) { return pick_bwd<bf16, float>(k); }
+#endif
+
+}  // namespace rmsn

@@ -147,12 +147,16 @@ for _op in ("fwd", "bwd"):
 WORKLOADS["mixed_fadd_bf16_m32768_n4096"] = Workload(
     "mixed_fadd_bf16_m32768_n4096", "fused_add", 32768, 4096, "bf16", "bf16", 1e-6, 10,
     store_rstd=False, offsets=(("x", 2),), tags=("mixed",))
-# what the scalar kernel still serves: outputs that disagree modulo 16 (y one
-# element past 16 bytes, the residual aligned) and rows off 16 bytes beyond
-# the ragged tier (x one element off, 20000 bf16 columns)
-WORKLOADS["generic_fadd_bf16_m32768_n4096"] = Workload(
-    "generic_fadd_bf16_m32768_n4096", "fused_add", 32768, 4096, "bf16", "bf16", 1e-6, 11,
-    store_rstd=False, offsets=(("y", 2),), tags=("generic",))
-WORKLOADS["generic_fwd_bf16_m8192_n20000"] = Workload(
-    "generic_fwd_bf16_m8192_n20000", "fwd", 8192, 20000, "bf16", "bf16", 1e-6, 11,
-    offsets=(("x", 2),), tags=("generic",))
+# what neither the register nor the ring kernels take, served by the wide
+# two-pass kernel: outputs that disagree modulo 16 (y one element past 16
+# bytes, the residual aligned), and rows beyond the mixed-alignment tiers (x
+# one element off, 20000 bf16 columns; forward and backward)
+WORKLOADS["wide_fadd_bf16_m32768_n4096"] = Workload(
+    "wide_fadd_bf16_m32768_n4096", "fused_add", 32768, 4096, "bf16", "bf16", 1e-6, 11,
+    store_rstd=False, offsets=(("y", 2),), tags=("wide",))
+WORKLOADS["wide_fwd_bf16_m8192_n20000"] = Workload(
+    "wide_fwd_bf16_m8192_n20000", "fwd", 8192, 20000, "bf16", "bf16", 1e-6, 11,
+    offsets=(("x", 2),), tags=("wide",))
+WORKLOADS["wide_bwd_bf16_m8192_n20000"] = Workload(
+    "wide_bwd_bf16_m8192_n20000", "bwd", 8192, 20000, "bf16", "bf16", 1e-6, 11,
+    offsets=(("x", 2),), tags=("wide",))

@@ -108,6 +108,7 @@ def test_bwd_without_dgamma(N):
     ("ragged:vpt=4:pf=0:cps=1", 2049), ("ragged:vpt=2:pf=1:mr=0", 1025),
     ("ragged:vpt=1:pf=1:cps=2", 4095),
     ("generic:cps=1", 8192), ("generic:cps=1", 2049),
+    ("wide:cps=1", 8192), ("wide:t=64:cps=1", 1032),
     ("staged:vpt=4:st=3:cps=1", 8192), ("staged:vpt=4:st=2:cps=1", 8192),
     ("staged:vpt=2:st=4:cps=1", 4096), ("staged:vpt=1:st=2:cps=1", 2048),
     ("staged:vpt=4:st=2:cps=1", 5120), ("staged:vpt=4:st=3:cps=1", 1032),
@@ -130,7 +131,7 @@ def test_forced_variants_walk_several_rows(debug_env, force, N):
 @pytest.mark.parametrize("offsets,N", [
     ({"x": 2, "dy": 2, "dx": 2}, 4096),                 # ragged
     ({"x": 2, "dy": 2, "dx": 2, "gamma": 4}, 1000),
-    ({"x": 2, "dy": 4, "dx": 2}, 4096),                 # generic
+    ({"x": 2, "dy": 4, "dx": 2}, 4096),                 # dy off x and dx: ragged mixed form
     ({"gamma": 4, "rstd": 4, "dgamma": 4}, 8192),       # ragged (gamma unaligned)
 ])
 def test_bwd_unaligned_pointers(offsets, N):

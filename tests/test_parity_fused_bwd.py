@@ -105,7 +105,7 @@ def test_dgamma_in_weight_dtype_and_no_rstd(N):
     ("staged:vpt=4:st=2:cps=1", 8192), ("staged:vpt=2:st=3:cps=1", 4096),
     ("staged:vpt=4:st=2:cps=1", 5120), ("subwarp:g=8:vpt=2:pf=1:cps=1", 128),
     ("subwarp:g=32:vpt=3:pf=0:cps=1", 768), ("ragged:vpt=2:pf=1:cps=1", 2049),
-    ("ragged:vpt=1:pf=0:cps=1", 2049), ("generic:cps=1", 4096),
+    ("ragged:vpt=1:pf=0:cps=1", 2049), ("generic:cps=1", 4096), ("wide:cps=1", 4096),
     ("staged:g=32:vpt=3:cps=1", 768), ("staged:g=8:vpt=2:st=4:cps=1", 128),
     ("staged:g=32:vpt=4:st=2:cps=1", 1024),
 ])

@@ -98,6 +98,7 @@ def test_fused_add_matches_oracle(xd, wd, M, N):
     ("cta:vpt=1:pf=1:cps=1", 2048), ("cta:vpt=4:pf=1:t=512:cps=1", 5120),
     ("ragged:vpt=2:pf=1:cps=1", 2049), ("ragged:vpt=1:pf=0:cps=1", 2049),
     ("ragged:vpt=4:pf=0:cps=1", 4096), ("ragged:vpt=2:pf=1:cps=2", 1025), ("generic:cps=1", 8192), ("generic:cps=1", 2049),
+    ("wide:cps=1", 8192), ("wide:cps=1", 2049), ("wide:t=64:cps=1", 1025),
     ("staged:vpt=4:st=3:cps=1", 8192), ("staged:vpt=4:st=2:cps=1", 8192),
     ("staged:vpt=2:st=5:cps=1", 4096), ("staged:vpt=8:st=2:cps=1", 16384),
     ("staged:vpt=1:st=8:cps=1", 2048), ("staged:vpt=4:t=512:st=2:cps=1", 5120),
@@ -122,7 +123,7 @@ def test_forced_variants_walk_several_rows(debug_env, op, force, N):
     ({"x": 2, "y": 2}, 4096),              # same residue: ragged rows
     ({"x": 2, "y": 2, "gamma": 2}, 2048),
     ({"x": 6, "y": 6, "residual": 6}, 1000),
-    ({"x": 2, "y": 4}, 4096),              # residues differ: generic
+    ({"x": 2, "y": 4}, 4096),              # residues differ: x off y (fused: y off h, wide)
     ({"gamma": 2}, 8192),                  # only gamma unaligned: ragged
     ({"x": 14, "y": 14, "residual": 14, "rstd": 4}, 129),
 ])
@@ -214,8 +215,8 @@ def test_plan_families():
     assert "/cluster/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 40000, "bf16", "bf16")
     assert "/cluster/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 16, 40000, "bf16", "bf16")
     assert "/cluster/" in rn.rmsnorm_describe_plan(rn.OP_FUSED_ADD_BWD, 16, 32768, "bf16", "bf16")
-    assert "/generic/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 40001, "bf16", "bf16")
-    assert "/generic/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 1 << 19, "bf16", "bf16")
+    assert "/wide/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 40001, "bf16", "bf16")
+    assert "/wide/" in rn.rmsnorm_describe_plan(rn.OP_FWD, 16, 1 << 19, "bf16", "bf16")
     assert "/staged/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 16384, 8192, "bf16", "f32")
     assert "/subwarp/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 262144, 128, "bf16", "bf16")
     assert "/staged/g32/vpt3/" in rn.rmsnorm_describe_plan(rn.OP_BWD, 65536, 768, "bf16", "bf16")

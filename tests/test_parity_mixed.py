@@ -194,8 +194,10 @@ def test_mixed_plans():
         for N in (2049, 128, 1000):
             assert "/ragged_mix/" in plan(op, N), plan(op, N)
     for op in (0, 1, 2, 3):
-        # beyond four vectors per thread in 512 threads: the scalar kernel
-        for N in (16385, 40001):
-            assert "/generic/" in plan(op, N, 64), plan(op, N, 64)
+        # beyond four vectors per thread in 512 threads: the wide two-pass
+        # kernel, or the scalar one for backward rows off 16 bytes
+        for N in (16385, 40001, 20000):
+            fam = "/wide/" if op < 2 or N == 20000 else "/generic/"
+            assert fam in plan(op, N, 64), plan(op, N, 64)
     # 1024 vectors at 31 per warp and slot: four vectors per thread, 9 warps
     assert "/vpt4/t288/pf1/" in plan(0, 8192), plan(0, 8192)
