@@ -247,6 +247,9 @@ struct Plan {
   int l2_ahead = 0;          // LayerNorm register kernels: L2 lookahead in iterations
   int cluster = 0;           // kCluster: CTAs per cluster (one row per cluster)
   int slice = 0;             // kCluster: vectors of each row per CTA
+  int64_t ahead_bytes = 0;   // kWide: input bytes of one row of every CTA's walk,
+                             // per grid CTA (sizes the L2 lookahead once the grid
+                             // is known; 0: lookahead as set)
   const void* fn = nullptr;
   FwdKernel fwd = nullptr;
   BwdKernel bwd = nullptr;
@@ -440,12 +443,21 @@ int64_t wide_smem(int N, int xd) { return round_up(N + 2 * per_vec(xd), 4) * 4LL
 bool wide_ok(bool bwd, int N, int xd) {
   return !bwd || (((int64_t)N * esize(xd)) % 16 == 0 && wide_smem(N, xd) <= kStagedSmemMax);
 }
-// Threads of a wide CTA: about two vectors of the row per thread, 64 to
-// kWideThreads.
-int wide_threads(int N, int E) {
-  const int t = round_up((N / E + 2) / 2, 32);
-  return t < 64 ? 64 : (t > kWideThreads ? kWideThreads : t);
+// Threads of a wide CTA: about two vectors of the row per thread, from 64 to
+// 256 for the forward (four CTAs per SM beat two of 512 threads: 32768 x 4096
+// bf16 fused add with y off the residual 0.93 of the copy peak against 0.62)
+// and to 512 for the backward (its shared-memory dgamma row allows few CTAs
+// per SM).
+int wide_threads(bool bwd, int N, int E) {
+  const int t = round_up((N / E + 2) / 2, 32), cap = bwd ? kWideBwdThreads : 256;
+  return t < 64 ? 64 : (t > cap ? cap : t);
 }
+// Bytes of input rows the grid of a wide kernel may have requested into L2
+// ahead of its walk (8192 x 20000 bf16 forward, 608 CTAs: 0.75 of the copy
+// peak without lookahead, 0.71 one step ahead, 0.60 two; 32768 x 4096 bf16
+// fused add: 0.87 / 0.93 / 0.92; 8192 x 20000 backward, 304 CTAs: 0.58 /
+// 0.55 / 0.49).
+constexpr int64_t kWideAheadBudget = 12 << 20;
 
 // Choose the variant.  aligned16: all base pointers 16-byte aligned;
 // same_mod16: all activation base pointers agree modulo 16 bytes.
@@ -549,7 +561,7 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
     p.period = 1;
   }
   if (p.family == kWide) {
-    p.threads = wide_threads(N, E);
+    p.threads = wide_threads(bwd, N, E);
     p.g = p.vpt = 0;
     p.prefetch = false;
     p.mix = false;
@@ -625,7 +637,8 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
       if (p.threads != 256) return RMSNORM_ERR_INVALID_ARG;
     } else if (p.family == kWide) {
       if (!wide_ok(bwd, N, xd)) return RMSNORM_ERR_INVALID_ARG;
-      if (!f.threads) p.threads = wide_threads(N, E);
+      if (!f.threads) p.threads = wide_threads(bwd, N, E);
+      if (p.threads > (bwd ? kWideBwdThreads : kWideThreads)) return RMSNORM_ERR_INVALID_ARG;
       p.g = p.vpt = 0;
       p.prefetch = false;
     }
@@ -649,8 +662,16 @@ rmsnorm_status_t make_plan(int op, int64_t M, int N, int xd, int wd, bool aligne
   // cluster forward: the slice of the row two steps ahead (2048 x 65536 bf16:
   // 0.77 -> 0.91 of the copy peak)
   if (l2_able) p.l2_ahead = 2;
-  if (f.on && f.l2 >= 0) p.l2_ahead = f.l2;
-  if (!l2_able) p.l2_ahead = 0;
+  // the wide kernel: input rows requested into L2 up to two steps ahead of
+  // the CTA's walk, as many steps as keep the requests of the whole grid
+  // within kWideAheadBudget (set by size_grid)
+  if (p.family == kWide)
+    p.ahead_bytes = (int64_t)N * esize(xd) * (op == kFwd ? 1 : (op == kFusedBwd ? 3 : 2));
+  if (f.on && f.l2 >= 0) {
+    p.l2_ahead = f.l2;
+    p.ahead_bytes = 0;
+  }
+  if (!l2_able && p.family != kWide) p.l2_ahead = 0;
 
   // kernel and shared memory
   if (p.family == kStaged) {
@@ -749,6 +770,11 @@ rmsnorm_status_t size_grid(Plan* p, int64_t M, int device, unsigned** status = n
   }
   p->grid = (int)(units < cap ? units : cap);
   if (p->grid < 1) p->grid = 1;
+  if (p->family == kWide && p->ahead_bytes > 0) {
+    const int64_t step = p->ahead_bytes * p->grid;
+    const int64_t n = kWideAheadBudget / step;
+    p->l2_ahead = n > 2 ? 2 : (int)n;
+  }
   if (p->period > 1) {   // whole residue classes: a multiple of the period
     p->grid = p->grid / p->period * p->period;
     if (p->grid < p->period) p->grid = p->period;

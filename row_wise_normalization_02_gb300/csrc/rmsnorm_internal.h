@@ -223,9 +223,10 @@ LnKernel get_ln_kernel_bf16_f32(const LnKey& k);
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;
 constexpr int kCtaMaxThreads = 512;
-// Most threads of a kWide CTA (built for two CTAs per SM, 64 registers a
+// Most threads of a kWide CTA, built for two CTAs per SM (64 registers a
 // thread).
 constexpr int kWideThreads = 512;
+constexpr int kWideBwdThreads = 512;
 // Threads of a stage-2 (column sum) CTA.
 constexpr int kColSumThreads = 256;
 

@@ -148,7 +148,37 @@ __device__ __forceinline__ int edge_elem(int2 f, int N, int tid, int T) {
   return k < N - t0 ? t0 + k : -1;
 }
 
+// Row q of a row-major operand (rows of rb bytes, any element-aligned base)
+// requested into L2: its enclosing 16-byte span, by the bulk-copy unit.
+__device__ __forceinline__ void l2_row(const void* base, int64_t q, size_t rb) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(base) + (uintptr_t)q * rb;
+  const uintptr_t lo = a & ~(uintptr_t)15, hi = (a + rb + 15) & ~(uintptr_t)15;
+  if (hi - lo <= (uintptr_t(1) << 24))   // rows up to 16 MB
+    bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+}
+
+// L2 lookahead of the CTA's walk: thread 0 requests the input rows L steps
+// ahead (at the first row also those 1 .. L-1 steps ahead), so that pass 1
+// reads from L2 rather than waiting on DRAM row after row.
+__device__ __forceinline__ void l2_ahead(int L, int64_t row, bool first, int64_t M,
+                                         size_t rb, const void* a, const void* b,
+                                         const void* c) {
+  if (L <= 0 || threadIdx.x != 0) return;
+  for (int k = first ? 1 : L; k <= L; ++k) {
+    const int64_t q = row + (int64_t)k * gridDim.x;
+    if (q >= M) break;
+    if (a) l2_row(a, q, rb);
+    if (b) l2_row(b, q, rb);
+    if (c) l2_row(c, q, rb);
+  }
+}
+
 // ---------------------------------------------------------------- forward
+//
+// Two passes per row.  Pass 1 reads x in its own frame (one aligned chunk a
+// vector, four vectors in flight a thread); fusing pass 2 of a row with pass 1
+// of the next, as the backward does, lost here (8192 x 20000 bf16, x off 16
+// bytes: 0.59 of the copy peak against 0.75).
 
 template <typename TX, typename TW, bool FUSED>
 __global__ void __launch_bounds__(kWideThreads, 2) fwd_wide_kernel(const FwdParams p) {
@@ -166,6 +196,8 @@ __global__ void __launch_bounds__(kWideThreads, 2) fwd_wide_kernel(const FwdPara
     const char* xr = static_cast<const char*>(p.x) + row * rb;
     char* hr = FUSED ? static_cast<char*>(p.residual) + row * rb : nullptr;
     char* yr = static_cast<char*>(p.y) + row * rb;
+    l2_ahead(p.l2_rows, row, row == blockIdx.x, p.M, rb, p.x, FUSED ? p.residual : nullptr,
+             nullptr);
     float s0 = 0.f, s1 = 0.f;
     {  // pass 1: the sum of squares in the frame of x (fused: of the residual)
       const char* fr = FUSED ? hr : xr;
@@ -255,14 +287,20 @@ __global__ void __launch_bounds__(kWideThreads, 2) fwd_wide_kernel(const FwdPara
 }
 
 // ---------------------------------------------------------------- backward
+//
+// Both passes in dx's frame (rows a multiple of 16 bytes: the same split, and
+// the same shifts of x and dy against it, for every row), and pass 2 of a row
+// fused with pass 1 of the CTA's next row: one loop over dx's vectors reads
+// gamma once, the current row's x and dy again (from L1 or L2) and the next
+// row's from DRAM, so every trip to memory carries both rows and the walk has
+// one dependent chain per row, not two.
 
 template <typename TX, typename TW, bool HAS_RSTD, bool DRES>
-__global__ void __launch_bounds__(kWideThreads, 2) bwd_wide_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdParams p) {
   pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
   constexpr int K = HAS_RSTD ? 1 : 2;
-  constexpr int U1 = 2, U2 = 1;
   // dgamma partial row: column j at acc_s[j - head + E], head = dx's head
   extern __shared__ __align__(16) float acc_s[];
   __shared__ float red[2 * 2 * 32];
@@ -270,51 +308,39 @@ __global__ void __launch_bounds__(kWideThreads, 2) bwd_wide_kernel(const BwdPara
   const size_t rb = (size_t)N * ES;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const bool dg = p.partial != nullptr;
-  const int2 fo = split_row(p.dx, N, ES);   // the same for every row
+  const int2 fo = split_row(p.dx, N, ES);
+  const Src gs = src_of(p.gamma, fo.x, WS);
+  const int je = edge_elem<E>(fo, N, tid, T);   // this thread's head or tail element
+  const TW* gp = static_cast<const TW*>(p.gamma);
   if (dg)
     for (int i = tid; i < N + 2 * E; i += T) acc_s[i] = 0.f;
-  int parity = 0;
-  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
-    const char* xr = static_cast<const char*>(p.x) + row * rb;
-    const char* dr = static_cast<const char*>(p.dy) + row * rb;
-    char* dxr = static_cast<char*>(p.dx) + row * rb;
-    const char* rr = DRES ? static_cast<const char*>(p.dres) + row * rb : nullptr;
-    float2 dot = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
-    {  // pass 1: sum gamma dy x (and sum x^2) in the frame of x
-      const int2 f = split_row(xr, N, ES);
-      const char* xb = xr + (size_t)f.x * ES;
-      const Src ds = src_of(dr, f.x, ES), gs = src_of(p.gamma, f.x, WS);
-      for (int v0 = tid; v0 < f.y; v0 += U1 * T) {
-        uint4 a[U1], d[U1], g[U1][GW];
-#pragma unroll
-        for (int u = 0; u < U1; ++u) {
-          const int v = v0 + u * T;
-          if (v < f.y) {
-            a[u] = ld_cached(xb + (size_t)v * 16);
-            d[u] = vec_at<kLdKeep>(ds, v);
-            gamma_at<GW>(gs, v, g[u]);
-          } else {
-            a[u] = d[u] = zero;
-#pragma unroll
-            for (int w = 0; w < GW; ++w) g[u][w] = zero;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U1; ++u) {
-          float gf[E];
-          unpack_gamma<TW, E, GW>(g[u], gf);
-          bwd_vec_sums<E, !HAS_RSTD>(a[u], d[u], gf, dot, sq);
-        }
-      }
-      const int j = edge_elem<E>(f, N, tid, T);
-      if (j >= 0) {
-        const float xv = ld_scalar(reinterpret_cast<const TX*>(xr) + j);
-        const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + j);
-        const float gv = ld_scalar_ro(static_cast<const TW*>(p.gamma) + j);
-        dot.x = fmaf(gv * dv, xv, dot.x);
-        if (!HAS_RSTD) sq.x = fmaf(xv, xv, sq.x);
-      }
+  const char* x0 = static_cast<const char*>(p.x);
+  const char* d0 = static_cast<const char*>(p.dy);
+  int64_t row = blockIdx.x;
+  // pass 1 of the first row
+  float2 dot = make_float2(0.f, 0.f), sq = make_float2(0.f, 0.f);
+  if (row < p.M) {
+    // (the walk reads the row after the current one as it goes: the
+    // lookahead counts from there)
+    l2_ahead(p.l2_rows, row + gridDim.x, true, p.M, rb, p.x, p.dy, DRES ? p.dres : nullptr);
+    const Src xs = src_of(x0 + row * rb, fo.x, ES), ds = src_of(d0 + row * rb, fo.x, ES);
+    for (int v = tid; v < fo.y; v += T) {
+      uint4 g[GW];
+      gamma_at<GW>(gs, v, g);
+      const uint4 a = vec_at<kLdKeep>(xs, v), d = vec_at<kLdKeep>(ds, v);
+      float gf[E];
+      unpack_gamma<TW, E, GW>(g, gf);
+      bwd_vec_sums<E, !HAS_RSTD>(a, d, gf, dot, sq);
     }
+    if (je >= 0) {
+      const float xv = ld_scalar(reinterpret_cast<const TX*>(x0 + row * rb) + je);
+      const float dv = ld_scalar(reinterpret_cast<const TX*>(d0 + row * rb) + je);
+      dot.x = fmaf(ld_scalar_ro(gp + je) * dv, xv, dot.x);
+      if (!HAS_RSTD) sq.x = fmaf(xv, xv, sq.x);
+    }
+  }
+  int parity = 0;
+  for (; row < p.M; row += gridDim.x) {
     float sums[K];
     sums[0] = dot.x + dot.y;
     if (!HAS_RSTD) sums[K - 1] = sq.x + sq.y;
@@ -322,59 +348,64 @@ __global__ void __launch_bounds__(kWideThreads, 2) bwd_wide_kernel(const BwdPara
     parity ^= 1;
     const float r = HAS_RSTD ? __ldg(p.rstd + row) : rsqrtf(fmaf(sums[K - 1], p.inv_n, p.eps));
     const float c = r * r * p.inv_n * sums[0];
-    {  // pass 2: dx in its own frame, and the dgamma partial
-      char* ob = dxr + (size_t)fo.x * ES;
-      const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES),
-                gs = src_of(p.gamma, fo.x, WS);
-      const Src rs = DRES ? src_of(rr, fo.x, ES) : Src{nullptr, 0};
-      for (int v0 = tid; v0 < fo.y; v0 += U2 * T) {
-        uint4 a[U2], d[U2], q[U2], g[U2][GW];
-#pragma unroll
-        for (int u = 0; u < U2; ++u) {
-          const int v = v0 + u * T;
-          if (v < fo.y) {
-            a[u] = vec_at<kLdKeep>(xs, v);
-            d[u] = vec_at<kLdKeep>(ds, v);
-            q[u] = DRES ? vec_at<kLdRw>(rs, v) : zero;
-            gamma_at<GW>(gs, v, g[u]);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U2; ++u) {
-          const int v = v0 + u * T;
-          if (v >= fo.y) continue;
-          float gf[E], acc[E];
-          unpack_gamma<TW, E, GW>(g[u], gf);
-          float4* ap = reinterpret_cast<float4*>(acc_s + E + (size_t)v * E);
-#pragma unroll
-          for (int w = 0; w < E / 4; ++w) {
-            const float4 t = dg ? ap[w] : make_float4(0.f, 0.f, 0.f, 0.f);
-            acc[4 * w] = t.x;
-            acc[4 * w + 1] = t.y;
-            acc[4 * w + 2] = t.z;
-            acc[4 * w + 3] = t.w;
-          }
-          const uint4 o = bwd_vec_apply<E, DRES>(a[u], d[u], q[u], gf, r, c, acc);
-          st_stream(ob + (size_t)v * 16, o);
-          if (dg) {
-#pragma unroll
-            for (int w = 0; w < E / 4; ++w)
-              ap[w] = make_float4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]);
-          }
-        }
+    const int64_t nxt = row + gridDim.x;
+    const bool more = nxt < p.M;   // the same in every thread
+    l2_ahead(p.l2_rows, nxt, false, p.M, rb, p.x, p.dy, DRES ? p.dres : nullptr);
+    const char* xr = x0 + row * rb;
+    const char* dr = d0 + row * rb;
+    char* dxr = static_cast<char*>(p.dx) + row * rb;
+    const char* rr = DRES ? static_cast<const char*>(p.dres) + row * rb : nullptr;
+    char* ob = dxr + (size_t)fo.x * ES;
+    const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES);
+    const Src qs = DRES ? src_of(rr, fo.x, ES) : Src{nullptr, 0};
+    const Src xn = src_of(x0 + (more ? nxt : row) * rb, fo.x, ES);
+    const Src dn = src_of(d0 + (more ? nxt : row) * rb, fo.x, ES);
+    dot = sq = make_float2(0.f, 0.f);
+    for (int v = tid; v < fo.y; v += T) {
+      uint4 g[GW];
+      gamma_at<GW>(gs, v, g);
+      const uint4 a = vec_at<kLdKeep>(xs, v), d = vec_at<kLdKeep>(ds, v);
+      const uint4 q = DRES ? vec_at<kLdRw>(qs, v) : zero;
+      uint4 an = zero, dnv = zero;
+      if (more) {
+        an = vec_at<kLdKeep>(xn, v);
+        dnv = vec_at<kLdKeep>(dn, v);
       }
-      const int j = edge_elem<E>(fo, N, tid, T);
-      if (j >= 0) {
-        const float xv = ld_scalar(reinterpret_cast<const TX*>(xr) + j);
-        const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + j);
-        const float gv = ld_scalar_ro(static_cast<const TW*>(p.gamma) + j);
-        float o = r * fmaf(-xv, c, gv * dv);
-        if (DRES) o += ld_scalar_cg(reinterpret_cast<const TX*>(rr) + j);
-        st_scalar(reinterpret_cast<TX*>(dxr) + j, o);
-        if (dg) {
-          float* a = acc_s + (j - fo.x + E);
-          *a = fmaf(dv * xv, r, *a);
-        }
+      float gf[E], acc[E];
+      unpack_gamma<TW, E, GW>(g, gf);
+      float4* ap = reinterpret_cast<float4*>(acc_s + E + (size_t)v * E);
+#pragma unroll
+      for (int w = 0; w < E / 4; ++w) {
+        const float4 t = dg ? ap[w] : make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[4 * w] = t.x;
+        acc[4 * w + 1] = t.y;
+        acc[4 * w + 2] = t.z;
+        acc[4 * w + 3] = t.w;
+      }
+      st_stream(ob + (size_t)v * 16, bwd_vec_apply<E, DRES>(a, d, q, gf, r, c, acc));
+      if (dg) {
+#pragma unroll
+        for (int w = 0; w < E / 4; ++w)
+          ap[w] = make_float4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]);
+      }
+      if (more) bwd_vec_sums<E, !HAS_RSTD>(an, dnv, gf, dot, sq);
+    }
+    if (je >= 0) {
+      const float gv = ld_scalar_ro(gp + je);
+      const float xv = ld_scalar(reinterpret_cast<const TX*>(xr) + je);
+      const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + je);
+      float o = r * fmaf(-xv, c, gv * dv);
+      if (DRES) o += ld_scalar_cg(reinterpret_cast<const TX*>(rr) + je);
+      st_scalar(reinterpret_cast<TX*>(dxr) + je, o);
+      if (dg) {
+        float* a = acc_s + (je - fo.x + E);
+        *a = fmaf(dv * xv, r, *a);
+      }
+      if (more) {
+        const float xv2 = ld_scalar(reinterpret_cast<const TX*>(x0 + nxt * rb) + je);
+        const float dv2 = ld_scalar(reinterpret_cast<const TX*>(d0 + nxt * rb) + je);
+        dot.x = fmaf(gv * dv2, xv2, dot.x);
+        if (!HAS_RSTD) sq.x = fmaf(xv2, xv2, sq.x);
       }
     }
   }
