@@ -5,7 +5,9 @@ distance, including the last iterations where the rows ahead run past the end
 and are clipped; and the dispatch turns it on exactly where it was measured
 to pay (the LayerNorm CTA kernels, the sub-warp backward kernels with next-row
 prefetch, the ragged kernels) and nowhere else -- not in the ring kernels,
-whose stages keep the rows in flight."""
+whose stages keep the rows in flight.  The wide kernel sizes its lookahead
+to the grid: as many rows ahead (at most two) as keep 12 MB of requests in
+flight."""
 import numpy as np
 import pytest
 
@@ -116,3 +118,36 @@ def test_ragged_rows_bits_do_not_depend_on_it(debug_env):
     ref = oracle.fwd(x, g, eps, "bf16", "bf16")
     pu.check_bf16_ulp(fwd["y"], ref["y"], what="y")
     check_bwd(x, dy, g, rstd, eps, "bf16", "bf16", bwd)
+
+
+@pytest.mark.parametrize("op,M,N,aligned,ahead", [
+    (rn.OP_FUSED_ADD, 32768, 4096, False, 1),    # 608 CTAs x 2 rows of 8 KB: one step
+    (rn.OP_FUSED_ADD, 32768, 2048, False, 2),
+    (rn.OP_FWD, 8192, 20000, "mixed", 0),        # 608 x 40 KB: none
+    (rn.OP_BWD, 8192, 20000, "mixed", 0),
+])
+def test_wide_dispatch(op, M, N, aligned, ahead):
+    plan = rn.rmsnorm_describe_plan(op, M, N, "bf16", "bf16", aligned)
+    assert "/wide/" in plan, plan
+    assert (f"/l2ahead{ahead}" in plan) if ahead else ("/l2ahead" not in plan), plan
+
+
+def test_wide_rows_bits_do_not_depend_on_it(debug_env):
+    import seeded_inputs as si
+    from tests.test_parity_fwd import check_fused
+    M, N, eps = 3001, 4096, tl.f32(1e-6)
+    x, g, _, dy = tl.inputs(M, N, "bf16", "bf16", seed=67, beta=False)
+    r = si.fill((M, N), seed=67, tensor_id=2, dtype="bf16")
+    # y off the residual: the fused add's wide form
+    fused = _over_distances(debug_env, lambda: pu.run_fused(
+        x, r, g, eps, "bf16", "bf16", want_rstd=True, offsets={"y": 2}))
+    check_fused(x, r, g, eps, "bf16", "bf16", fused, want_rstd=True)
+    # x off dy and dx: the wide backward's shifted reads
+    rstd = oracle.fwd(x, g, eps, "bf16", "bf16", want64=False)["rstd"]
+    runs = []
+    for l2 in (0, 1, 3):
+        debug_env.set("RMSNORM_FORCE_VARIANT", f"wide:l2={l2}")
+        runs.append(pu.run_bwd(dy, x, rstd, g, eps, "bf16", "bf16", offsets={"x": 6}))
+    debug_env.delete("RMSNORM_FORCE_VARIANT", raising=False)
+    _same(runs)
+    check_bwd(x, dy, g, rstd, eps, "bf16", "bf16", runs[0])
