@@ -180,8 +180,11 @@ __device__ __forceinline__ void l2_ahead(int L, int64_t row, bool first, int64_t
 // of the next, as the backward does, lost here (8192 x 20000 bf16, x off 16
 // bytes: 0.59 of the copy peak against 0.75).
 
+// The plain forward with gamma no wider than x fits 42 registers (three CTAs
+// of 512 threads, six of 256, per SM); the others take 64.
 template <typename TX, typename TW, bool FUSED>
-__global__ void __launch_bounds__(kWideThreads, 2) fwd_wide_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kWideThreads, (FUSED || sizeof(TW) > sizeof(TX)) ? 2 : 3)
+    fwd_wide_kernel(const FwdParams p) {
   pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);

@@ -122,14 +122,20 @@ def test_ragged_rows_bits_do_not_depend_on_it(debug_env):
 
 @pytest.mark.parametrize("op,M,N,aligned,ahead", [
     (rn.OP_FUSED_ADD, 32768, 4096, False, 1),    # 608 CTAs x 2 rows of 8 KB: one step
-    (rn.OP_FUSED_ADD, 32768, 2048, False, 2),
+    (rn.OP_FUSED_ADD, 32768, 2048, False, None),
+    (rn.OP_BWD, 32768, 4096, False, None),
     (rn.OP_FWD, 8192, 20000, "mixed", 0),        # 608 x 40 KB: none
     (rn.OP_BWD, 8192, 20000, "mixed", 0),
 ])
 def test_wide_dispatch(op, M, N, aligned, ahead):
     plan = rn.rmsnorm_describe_plan(op, M, N, "bf16", "bf16", aligned)
     assert "/wide/" in plan, plan
-    assert (f"/l2ahead{ahead}" in plan) if ahead else ("/l2ahead" not in plan), plan
+    grid = int(plan.split("/grid")[1].split("/")[0])
+    inputs = 1 if op == rn.OP_FWD else 2
+    want = min(2, (12 << 20) // (grid * inputs * N * 2))
+    if ahead is not None:
+        assert want == ahead, plan
+    assert (f"/l2ahead{want}" in plan) if want else ("/l2ahead" not in plan), plan
 
 
 def test_wide_rows_bits_do_not_depend_on_it(debug_env):
