@@ -1222,10 +1222,24 @@ rmsnorm_status_t fwd_quant_impl(int out, const void* x, void* residual, const vo
 // ---------------------------------------------------------------- LayerNorm
 
 LnKernel ln_kernel(const LnKey& k) {
+  if (k.family == kWide) {
+    if (k.xd == kF32 && k.wd == kF32) return get_ln_wide_f32_f32(k);
+    if (k.xd == kBF16 && k.wd == kBF16) return get_ln_wide_bf16_bf16(k);
+    if (k.xd == kBF16 && k.wd == kF32) return get_ln_wide_bf16_f32(k);
+    return nullptr;
+  }
   if (k.xd == kF32 && k.wd == kF32) return get_ln_kernel_f32_f32(k);
   if (k.xd == kBF16 && k.wd == kBF16) return get_ln_kernel_bf16_bf16(k);
   if (k.xd == kBF16 && k.wd == kF32) return get_ln_kernel_bf16_f32(k);
   return nullptr;
+}
+
+// The wide LayerNorm backward keeps its two partial rows in shared memory
+// (each N + 2E floats, rounded to 4) and needs dx's split to be the same for
+// every row.
+int64_t ln_wide_smem(int N, int xd) { return 2 * wide_smem(N, xd); }
+bool ln_wide_ok(bool bwd, int64_t N, int xd) {
+  return !bwd || ((N * esize(xd)) % 16 == 0 && ln_wide_smem((int)N, xd) <= kStagedSmemMax);
 }
 
 // Plan of the LayerNorm kernels: rows of at most 128 16-byte vectors take the
@@ -1283,12 +1297,27 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
     p.prefetch = false;
     p.stages = 0;
   }
+  // what those do not take -- rows or operands off 16 bytes, forward rows
+  // beyond 2048 vectors, backward rows beyond 1024 -- goes to the wide
+  // kernel where it applies, else to the scalar one
+  if (p.family == kGeneric && ln_wide_ok(bwd, N, xd)) {
+    p.family = kWide;
+    p.threads = wide_threads(bwd, (int)N, E);
+  }
   const Force& f = read_force();
   if (f.on) {
     if (f.family == kGeneric) {
       p.family = kGeneric;
       p.threads = 256;
       p.rows_per_cta = 1;
+    } else if (f.family == kWide) {
+      if (!ln_wide_ok(bwd, N, xd)) return RMSNORM_ERR_INVALID_ARG;
+      p.family = kWide;
+      p.threads = f.threads ? f.threads : wide_threads(bwd, (int)N, E);
+      if (p.threads < 64 || p.threads % 32 || p.threads > (bwd ? kWideBwdThreads : kWideThreads))
+        return RMSNORM_ERR_INVALID_ARG;
+      p.rows_per_cta = 1;
+      p.stages = 0;
     } else if (f.family == kSubwarp) {
       if (!vec_ok || !f.g || !f.vpt || f.g * f.vpt < nvec) return RMSNORM_ERR_INVALID_ARG;
       p.family = kSubwarp;
@@ -1339,12 +1368,17 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
   // 0.83, but the sub-warp forward loses, 0.93 -> 0.84, so it goes without)
   if (p.prefetch && (p.family == kCta || (p.family == kSubwarp && bwd))) p.l2_ahead = 2;
   if (f.on && f.l2 >= 0) p.l2_ahead = f.l2;
-  if (p.family == kGeneric) {
+  if (p.family == kGeneric || p.family == kWide) {
     p.g = p.vpt = 0;
     p.prefetch = false;
     p.rows_per_cta = 1;
   }
   if (p.family == kGeneric || p.family == kStaged) p.l2_ahead = 0;
+  // the wide kernel's lookahead, sized to the grid by size_grid
+  if (p.family == kWide && !(f.on && f.l2 >= 0)) {
+    p.l2_ahead = 0;
+    p.ahead_bytes = N * esize(xd) * (bwd ? 2 : 1);
+  }
   if (p.family == kStaged) {
     p.prefetch = false;
     // ring of [x | dy] row pairs (of the CTA's rows_per_cta rows for short
@@ -1370,6 +1404,7 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
   p.smem = (bwd && p.family == kSubwarp) ? p.rows_per_cta * 2 * nvec * E * 4 : 0;
   if (p.family == kStaged)
     p.smem = (int)(kStagedHeader + p.stages * 2 * N * esize(xd) * p.rows_per_cta);
+  if (p.family == kWide && bwd) p.smem = (int)ln_wide_smem((int)N, xd);
   if (bwd) {
     p.min_rows = 8 / p.rows_per_cta > 0 ? 8 / p.rows_per_cta : 1;
     const Force& fr = read_force();
@@ -1442,6 +1477,12 @@ rmsnorm_status_t ln_partial_rows(int64_t M, int N, int xd, int wd, int device, i
   if (st != RMSNORM_OK) return st;
   if ((st = size_grid(&pl, M, device)) != RMSNORM_OK) return st;
   *rows = pl.grid;
+  // operands off 16 bytes may take the wide kernel, whose grid the aligned
+  // plan's need not bound
+  Plan pw;
+  if (ln_plan(true, M, N, xd, wd, false, &pw) == RMSNORM_OK && pw.family == kWide &&
+      size_grid(&pw, M, device) == RMSNORM_OK && pw.grid > *rows)
+    *rows = pw.grid;
   return RMSNORM_OK;
 }
 

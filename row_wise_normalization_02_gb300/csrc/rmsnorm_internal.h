@@ -219,6 +219,9 @@ struct LnKey {
 LnKernel get_ln_kernel_f32_f32(const LnKey& k);
 LnKernel get_ln_kernel_bf16_bf16(const LnKey& k);
 LnKernel get_ln_kernel_bf16_f32(const LnKey& k);
+LnKernel get_ln_wide_f32_f32(const LnKey& k);
+LnKernel get_ln_wide_bf16_bf16(const LnKey& k);
+LnKernel get_ln_wide_bf16_f32(const LnKey& k);
 
 // Threads per CTA of the subwarp families; upper bound of the per-row CTAs.
 constexpr int kSubwarpThreads = 256;

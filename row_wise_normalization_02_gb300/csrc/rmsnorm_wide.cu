@@ -1,5 +1,5 @@
-// kWide: rows of any length whose operands start at any element-aligned
-// offsets, read and written as 16-byte vectors.  One CTA per row (persistent
+// kWide: RMSNorm and LayerNorm rows of any length whose operands start at
+// any element-aligned offsets, read and written as 16-byte vectors.  One CTA per row (persistent
 // walk over rows), two passes over each row:
 //   pass 1 reduces the row in the frame of one operand -- x for the forward
 //   and the backward, the residual (which receives h) for the fused add: that
@@ -419,6 +419,318 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
   }
 }
 
+// ---------------------------------------------------------------- LayerNorm
+//
+// The same frames for LayerNorm.  The statistics are taken in x's frame --
+// m0 = sum x / N and, unless the moments about zero suffice (below), the
+// corrected two-pass moments c = sum (x - m0) / N and
+// rs = 1 / sqrt(sum (x - m0)^2 / N - c^2 + eps), the mean being m0 + c
+// ("Pre-built kernel library guide", 1.1 LayerNorm) -- and the outputs in
+// their own frame: y = ((x - m0) - c) rs gamma + beta; the backward's
+// dx = rs (dy gamma - (mg + xh mgx)) with xh = ((x - m0) - c) rs, mg and mgx
+// the row means of dy gamma and dy gamma xh, dgamma += dy xh, dbeta += dy.
+
+template <typename TX>
+__device__ __forceinline__ void vec_sum(const uint4& v, float& s0, float& s1) {
+  constexpr int E = Elem<TX>::kPerVec;
+  float f[E];
+  unpack(v, f);
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    s0 += f[e];
+    s1 += f[e + 1];
+  }
+}
+
+template <typename TX>
+__device__ __forceinline__ void vec_dev(const uint4& v, float m0, float& sd, float& sq) {
+  constexpr int E = Elem<TX>::kPerVec;
+  float f[E];
+  unpack(v, f);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float d = f[e] - m0;
+    sd += d;
+    sq = fmaf(d, d, sq);
+  }
+}
+
+// (m0, c, rs) of the row at xr, in x's frame; every thread of the CTA gets
+// them.  Pass 1 sums x and x^2.  Where the row's mean is small against its
+// spread (m0^2 <= sum x^2 / N - m0^2, so that the difference loses at most a
+// factor two of its precision), rs comes from those sums with c = 0, and the
+// row is read once; otherwise pass 2 forms the corrected moments about m0.
+template <typename TX>
+__device__ __forceinline__ float3 wide_ln_stats(const char* xr, int N, float* red, int& parity,
+                                                float inv_n, float eps) {
+  constexpr int E = Elem<TX>::kPerVec, ES = (int)sizeof(TX), U = 4;
+  const int tid = threadIdx.x, T = blockDim.x;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const int2 f = split_row(xr, N, ES);
+  const char* xb = xr + (size_t)f.x * ES;
+  const int j = edge_elem<E>(f, N, tid, T);
+  const TX* xe = reinterpret_cast<const TX*>(xr);
+  float s0 = 0.f, s1 = 0.f, q0 = 0.f, q1 = 0.f;
+  for (int v0 = tid; v0 < f.y; v0 += U * T) {
+    uint4 a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * T;
+      a[u] = v < f.y ? ld_cached(xb + (size_t)v * 16) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      vec_sum<TX>(a[u], s0, s1);
+      vec_sumsq<TX>(a[u], q0, q1);
+    }
+  }
+  if (j >= 0) {
+    const float v = ld_scalar(xe + j);
+    s0 += v;
+    q0 = fmaf(v, v, q0);
+  }
+  float t1[2] = {s0 + s1, q0 + q1};
+  cta_sum<2>(t1, red, parity);
+  parity ^= 1;
+  const float m0 = t1[0] * inv_n;
+  const float var1 = fmaf(t1[1], inv_n, -m0 * m0);
+  if (m0 * m0 <= var1) return make_float3(m0, 0.f, rsqrtf(var1 + eps));
+  float sd = 0.f, sq = 0.f;
+  for (int v0 = tid; v0 < f.y; v0 += U * T) {
+    uint4 a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * T;
+      a[u] = v < f.y ? ld_cached(xb + (size_t)v * 16) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (v0 + u * T < f.y) vec_dev<TX>(a[u], m0, sd, sq);
+    }
+  }
+  if (j >= 0) {
+    const float d = ld_scalar(xe + j) - m0;
+    sd += d;
+    sq = fmaf(d, d, sq);
+  }
+  float t2[2] = {sd, sq};
+  cta_sum<2>(t2, red, parity);
+  parity ^= 1;
+  const float c = t2[0] * inv_n;
+  return make_float3(m0, c, rsqrtf(fmaxf(fmaf(t2[1], inv_n, -c * c), 0.f) + eps));
+}
+
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(kWideThreads, 2) ln_fwd_wide_kernel(const LnParams p) {
+  pdl_begin();
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
+  constexpr int U = GW == 2 ? 1 : 2;   // vectors in flight (gamma and beta in fp32: one)
+  __shared__ float red[128];
+  const int tid = threadIdx.x, T = blockDim.x, N = p.N;
+  const size_t rb = (size_t)N * ES;
+  const bool hb = p.beta != nullptr;
+  const TW* gp = static_cast<const TW*>(p.gamma);
+  const TW* bp = static_cast<const TW*>(p.beta);
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const char* xr = static_cast<const char*>(p.x) + row * rb;
+    char* yr = static_cast<char*>(p.y) + row * rb;
+    l2_ahead(p.l2_rows, row, row == blockIdx.x, p.M, rb, p.x, nullptr, nullptr);
+    const float3 st = wide_ln_stats<TX>(xr, N, red, parity, p.inv_n, p.eps);
+    if (tid == 0) {
+      if (p.mean != nullptr) p.mean[row] = st.x + st.y;
+      if (p.rstd != nullptr) p.rstd[row] = st.z;
+    }
+    const int2 f = split_row(yr, N, ES);
+    char* yb = yr + (size_t)f.x * ES;
+    const Src xs = src_of(xr, f.x, ES), gs = src_of(p.gamma, f.x, WS),
+              bs = src_of(hb ? p.beta : p.gamma, f.x, WS);
+    for (int v0 = tid; v0 < f.y; v0 += U * T) {
+      uint4 a[U], g[U][GW], b[U][GW];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * T;
+        if (v < f.y) {
+          a[u] = vec_at<kLdKeep>(xs, v);
+          gamma_at<GW>(gs, v, g[u]);
+          if (hb) gamma_at<GW>(bs, v, b[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * T;
+        if (v >= f.y) continue;
+        float xf[E], gf[E], bf[E];
+        unpack(a[u], xf);
+        unpack_gamma<TW, E, GW>(g[u], gf);
+        if (hb) {
+          unpack_gamma<TW, E, GW>(b[u], bf);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) bf[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) xf[e] = fmaf(((xf[e] - st.x) - st.y) * st.z, gf[e], bf[e]);
+        st_stream(yb + (size_t)v * 16, pack(xf));
+      }
+    }
+    const int j = edge_elem<E>(f, N, tid, T);
+    if (j >= 0) {
+      const float t = ((ld_scalar(reinterpret_cast<const TX*>(xr) + j) - st.x) - st.y) * st.z;
+      st_scalar(reinterpret_cast<TX*>(yr) + j,
+                fmaf(t, ld_scalar_ro(gp + j), hb ? ld_scalar_ro(bp + j) : 0.f));
+    }
+  }
+}
+
+// Backward: rows a multiple of 16 bytes; the partial rows [dgamma | dbeta]
+// in shared memory, each half NA floats laid out as the RMSNorm backward's.
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const LnParams p) {
+  pdl_begin();
+  using C = Cfg<TX, TW>;
+  constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
+  constexpr int U = 2, UB = 1;   // vectors in flight: pass a, pass b
+  extern __shared__ __align__(16) float acc_s[];
+  __shared__ float red[128];
+  const int tid = threadIdx.x, T = blockDim.x, N = p.N;
+  const int NA = (N + 2 * E + 3) / 4 * 4;
+  const size_t rb = (size_t)N * ES;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const bool dg = p.partial != nullptr;
+  const int2 fo = split_row(p.y, N, ES);   // dx's split, the same for every row
+  const Src gs = src_of(p.gamma, fo.x, WS);
+  const int je = edge_elem<E>(fo, N, tid, T);
+  const TW* gp = static_cast<const TW*>(p.gamma);
+  if (dg)
+    for (int i = tid; i < 2 * NA; i += T) acc_s[i] = 0.f;
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    const char* xr = static_cast<const char*>(p.x) + row * rb;
+    const char* dr = static_cast<const char*>(p.dy) + row * rb;
+    char* dxr = static_cast<char*>(p.y) + row * rb;
+    l2_ahead(p.l2_rows, row, row == blockIdx.x, p.M, rb, p.x, p.dy, nullptr);
+    float3 st;
+    if (p.mean != nullptr) st = make_float3(p.mean[row], 0.f, p.rstd[row]);
+    else st = wide_ln_stats<TX>(xr, N, red, parity, p.inv_n, p.eps);
+    const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES);
+    // pass a: the row sums of g = dy gamma and g xh
+    float a = 0.f, b = 0.f;
+    for (int v0 = tid; v0 < fo.y; v0 += U * T) {
+      uint4 xv[U], dv[U], g[U][GW];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * T;
+        if (v < fo.y) {
+          xv[u] = vec_at<kLdKeep>(xs, v);
+          dv[u] = vec_at<kLdKeep>(ds, v);
+          gamma_at<GW>(gs, v, g[u]);
+        } else {
+          xv[u] = dv[u] = zero;
+#pragma unroll
+          for (int w = 0; w < GW; ++w) g[u][w] = zero;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float xf[E], df[E], gf[E];
+        unpack(xv[u], xf);
+        unpack(dv[u], df);
+        unpack_gamma<TW, E, GW>(g[u], gf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float gd = df[e] * gf[e];   // 0 past the row
+          a += gd;
+          b = fmaf(gd, ((xf[e] - st.x) - st.y) * st.z, b);
+        }
+      }
+    }
+    if (je >= 0) {
+      const float xh = ((ld_scalar(reinterpret_cast<const TX*>(xr) + je) - st.x) - st.y) * st.z;
+      const float gd = ld_scalar(reinterpret_cast<const TX*>(dr) + je) * ld_scalar_ro(gp + je);
+      a += gd;
+      b = fmaf(gd, xh, b);
+    }
+    float t[2] = {a, b};
+    cta_sum<2>(t, red, parity);
+    parity ^= 1;
+    const float mg = t[0] * p.inv_n, mgx = t[1] * p.inv_n;
+    // pass b: dx and the partial rows
+    char* ob = dxr + (size_t)fo.x * ES;
+    for (int v0 = tid; v0 < fo.y; v0 += UB * T) {
+      uint4 xv[UB], dv[UB], g[UB][GW];
+#pragma unroll
+      for (int u = 0; u < UB; ++u) {
+        const int v = v0 + u * T;
+        if (v < fo.y) {
+          xv[u] = vec_at<kLdKeep>(xs, v);
+          dv[u] = vec_at<kLdKeep>(ds, v);
+          gamma_at<GW>(gs, v, g[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UB; ++u) {
+        const int v = v0 + u * T;
+        if (v >= fo.y) continue;
+        float xf[E], df[E], gf[E], pg[E], pb[E];
+        unpack(xv[u], xf);
+        unpack(dv[u], df);
+        unpack_gamma<TW, E, GW>(g[u], gf);
+        float4* ag = reinterpret_cast<float4*>(acc_s + E + (size_t)v * E);
+        float4* ab = reinterpret_cast<float4*>(acc_s + NA + E + (size_t)v * E);
+#pragma unroll
+        for (int w = 0; w < E / 4; ++w) {
+          const float4 tg = dg ? ag[w] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 tb = dg ? ab[w] : make_float4(0.f, 0.f, 0.f, 0.f);
+          pg[4 * w] = tg.x; pg[4 * w + 1] = tg.y; pg[4 * w + 2] = tg.z; pg[4 * w + 3] = tg.w;
+          pb[4 * w] = tb.x; pb[4 * w + 1] = tb.y; pb[4 * w + 2] = tb.z; pb[4 * w + 3] = tb.w;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float xh = ((xf[e] - st.x) - st.y) * st.z;
+          xf[e] = st.z * (df[e] * gf[e] - fmaf(xh, mgx, mg));
+          pg[e] = fmaf(df[e], xh, pg[e]);
+          pb[e] += df[e];
+        }
+        st_stream(ob + (size_t)v * 16, pack(xf));
+        if (dg) {
+#pragma unroll
+          for (int w = 0; w < E / 4; ++w) {
+            ag[w] = make_float4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
+            ab[w] = make_float4(pb[4 * w], pb[4 * w + 1], pb[4 * w + 2], pb[4 * w + 3]);
+          }
+        }
+      }
+    }
+    if (je >= 0) {
+      const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + je);
+      const float xh = ((ld_scalar(reinterpret_cast<const TX*>(xr) + je) - st.x) - st.y) * st.z;
+      st_scalar(reinterpret_cast<TX*>(dxr) + je,
+                st.z * (dv * ld_scalar_ro(gp + je) - fmaf(xh, mgx, mg)));
+      if (dg) {
+        float* ag = acc_s + (je - fo.x + E);
+        *ag = fmaf(dv, xh, *ag);
+        ag[NA] += dv;
+      }
+    }
+  }
+  if (dg) {
+    __syncthreads();
+    float* prow = p.partial + (size_t)blockIdx.x * 2 * p.ld_half;
+    for (int j = tid; j < N; j += T) {
+      prow[j] = acc_s[j - fo.x + E];
+      prow[p.ld_half + j] = acc_s[NA + j - fo.x + E];
+    }
+  }
+}
+
+template <typename TX, typename TW>
+LnKernel pick_ln(const LnKey& k) {
+  if (k.family != kWide) return nullptr;
+  return k.bwd ? ln_bwd_wide_kernel<TX, TW> : ln_fwd_wide_kernel<TX, TW>;
+}
+
 template <typename TX, typename TW>
 FwdKernel pick_fwd(const FwdKey& k) {
   if (k.family != kWide || k.strided || k.out != kOutDtype) return nullptr;
@@ -438,12 +750,15 @@ BwdKernel pick_bwd(const BwdKey& k) {
 #if RMSN_PAIR == 0
 FwdKernel get_fwd_wide_f32_f32(const FwdKey& k) { return pick_fwd<float, float>(k); }
 BwdKernel get_bwd_wide_f32_f32(const BwdKey& k) { return pick_bwd<float, float>(k); }
+LnKernel get_ln_wide_f32_f32(const LnKey& k) { return pick_ln<float, float>(k); }
 #elif RMSN_PAIR == 1
 FwdKernel get_fwd_wide_bf16_bf16(const FwdKey& k) { return pick_fwd<bf16, bf16>(k); }
 BwdKernel get_bwd_wide_bf16_bf16(const BwdKey& k) { return pick_bwd<bf16, bf16>(k); }
+LnKernel get_ln_wide_bf16_bf16(const LnKey& k) { return pick_ln<bf16, bf16>(k); }
 #else
 FwdKernel get_fwd_wide_bf16_f32(const FwdKey& k) { return pick_fwd<bf16, float>(k); }
 BwdKernel get_bwd_wide_bf16_f32(const BwdKey& k) { return pick_bwd<bf16, float>(k); }
+LnKernel get_ln_wide_bf16_f32(const LnKey& k) { return pick_ln<bf16, float>(k); }
 #endif
 
 }  // namespace rmsn

@@ -157,6 +157,14 @@ WORKLOADS["wide_fadd_bf16_m32768_n4096"] = Workload(
 WORKLOADS["wide_fwd_bf16_m8192_n20000"] = Workload(
     "wide_fwd_bf16_m8192_n20000", "fwd", 8192, 20000, "bf16", "bf16", 1e-6, 11,
     offsets=(("x", 2),), tags=("wide",))
+# LayerNorm rows beyond its register tiers (forward 2048 vectors, backward
+# 1024): the wide kernels, aligned operands
+WORKLOADS["ln_wide_fwd_bf16_m4096_n32768"] = Workload(
+    "ln_wide_fwd_bf16_m4096_n32768", "ln_fwd", 4096, 32768, "bf16", "bf16", 1e-5, 12,
+    tags=("wide",))
+WORKLOADS["ln_wide_bwd_bf16_m8192_n12288"] = Workload(
+    "ln_wide_bwd_bf16_m8192_n12288", "ln_bwd", 8192, 12288, "bf16", "bf16", 1e-5, 12,
+    tags=("wide",))
 WORKLOADS["wide_bwd_bf16_m8192_n20000"] = Workload(
     "wide_bwd_bf16_m8192_n20000", "bwd", 8192, 20000, "bf16", "bf16", 1e-6, 11,
     offsets=(("x", 2),), tags=("wide",))

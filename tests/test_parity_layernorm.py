@@ -63,7 +63,7 @@ def run_fwd(x, g, b, eps, xd, wd, offsets=None):
 def run_bwd(dy, x, mean, rstd, g, eps, xd, wd, want=(True, True), offsets=None):
     M, N = x.shape
     o = offsets or {}
-    bdy, bx, bg = pu.dev(dy, o.get("dy", 0)), pu.dev(x, o.get("x", 0)), pu.dev(g)
+    bdy, bx, bg = pu.dev(dy, o.get("dy", 0)), pu.dev(x, o.get("x", 0)), pu.dev(g, o.get("gamma", 0))
     bm = pu.dev(mean) if mean is not None else None
     br = pu.dev(rstd) if rstd is not None else None
     bdx = pu.empty(M * N, xd, o.get("dx", 0))
@@ -318,10 +318,90 @@ def check_workload(wl, inp):
 
 
 @pytest.mark.parametrize("N", [20000, 32768])
-def test_long_rows_take_the_scalar_kernels(N):
-    # beyond 2048 vectors per row: the scalar forward and backward
+def test_long_rows(N):
+    # beyond 2048 vectors per row (the forward) and 1024 (the backward): the
+    # wide kernels; the backward's two partial rows fit in shared memory up to
+    # about 28 K columns, the scalar kernel takes longer rows
     x, g, b, dy = inputs(24, N, "bf16", "bf16", seed=N % 97)
     eps = f32(1e-5)
+    assert "/wide/" in rn.rmsnorm_describe_plan(rn.OP_LAYERNORM_FWD, 24, N, "bf16", "bf16")
+    fam = "/wide/" if N == 20000 else "/generic/"
+    assert fam in rn.rmsnorm_describe_plan(rn.OP_LAYERNORM_BWD, 24, N, "bf16", "bf16")
     check_fwd(run_fwd(x, g, b, eps, "bf16", "bf16"), x, g, b, eps, "bf16", "bf16")
     out = run_bwd(dy, x, None, None, g, eps, "bf16", "bf16")
     check_bwd(out, dy, x, None, None, g, eps, "bf16", "bf16")
+
+
+# ---------------------------------------------------------------- the wide kernels:
+# operands at any offsets, rows of any length (the backward: rows a multiple
+# of 16 bytes), forced onto shapes that walk several rows per CTA
+
+def _es(xd):
+    return 4 if xd == "f32" else 2
+
+
+def _scaled(off, xd, wd):
+    return {k: v * (_es(wd) if k in ("gamma", "beta") else _es(xd)) % 16 for k, v in off.items()}
+
+
+LN_FWD_OFFSETS = [{}, {"x": 1}, {"y": 3}, {"x": 5, "y": 2, "gamma": 1, "beta": 3}]
+
+
+@pytest.mark.parametrize("xd,wd", PAIRS)
+@pytest.mark.parametrize("N", [1, 7, 129, 1000, 2049, 8192, 20001])
+@pytest.mark.parametrize("k", range(len(LN_FWD_OFFSETS)))
+def test_wide_forward(debug_env, xd, wd, N, k):
+    if xd == "f32" and N == 20001:
+        N = 10003
+    debug_env.set("RMSNORM_FORCE_VARIANT", "wide:cps=1")
+    M = 37 if N > 8192 else 300
+    x, g, b, _ = inputs(M, N, xd, wd, seed=N + 90 + k, beta=k != 1, mean=0.5)
+    out = run_fwd(x, g, b, f32(1e-5), xd, wd, offsets=_scaled(LN_FWD_OFFSETS[k], xd, wd))
+    check_fwd(out, x, g, b, f32(1e-5), xd, wd)
+
+
+LN_BWD_OFFSETS = [{}, {"x": 1}, {"dy": 3}, {"dx": 1}, {"x": 5, "dy": 2, "dx": 7, "gamma": 1}]
+
+
+@pytest.mark.parametrize("xd,wd", PAIRS)
+@pytest.mark.parametrize("N", [8, 1032, 4096, 20000])
+@pytest.mark.parametrize("k", range(len(LN_BWD_OFFSETS)))
+def test_wide_backward(debug_env, xd, wd, N, k):
+    if xd == "f32":
+        N = N // 2 if N > 8 else 4
+    debug_env.set("RMSNORM_FORCE_VARIANT", "wide:cps=1")
+    M = 37 if N >= 10000 else 500
+    x, g, _, dy = inputs(M, N, xd, wd, seed=N + 91 + k)
+    eps = f32(1e-5)
+    o = _scaled(LN_BWD_OFFSETS[k], xd, wd)
+    fw = oracle.layernorm_fwd(x, g, None, eps, xd, wd)
+    out = run_bwd(dy, x, fw["mean"], fw["rstd"], g, eps, xd, wd, offsets=o)
+    check_bwd(out, dy, x, fw["mean"], fw["rstd"], g, eps, xd, wd)
+    if k % 2 == 0:   # statistics recomputed from x
+        out = run_bwd(dy, x, None, None, g, eps, xd, wd, offsets=o)
+        check_bwd(out, dy, x, None, None, g, eps, xd, wd)
+
+
+def test_wide_backward_is_deterministic_and_gradients_optional(debug_env):
+    debug_env.set("RMSNORM_FORCE_VARIANT", "wide")
+    x, g, _, dy = inputs(2000, 4096, "bf16", "bf16", seed=92)
+    o = {"x": 2, "dy": 6, "dx": 4}
+    a = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16", offsets=o)
+    b = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16", offsets=o)
+    for key in ("dx", "dgamma", "dbeta"):
+        assert np.array_equal(a[key], b[key]), key
+    none = run_bwd(dy, x, None, None, g, f32(1e-5), "bf16", "bf16", want=(False, False),
+                   offsets=o)
+    assert np.array_equal(none["dx"], a["dx"])
+
+
+def test_wide_plans():
+    def plan(op, N, a=True, M=4096):
+        return rn.rmsnorm_describe_plan(op, M, N, "bf16", "bf16", a)
+    fwd, bwd = rn.OP_LAYERNORM_FWD, rn.OP_LAYERNORM_BWD
+    for N in (2049, 1001, 40001):            # rows off 16 bytes
+        assert "/wide/" in plan(fwd, N), plan(fwd, N)
+    assert "/generic/" in plan(bwd, 2049)    # the backward's split would move per row
+    for N in (1024, 8192):                   # operands off 16 bytes
+        assert "/wide/" in plan(fwd, N, False) and "/wide/" in plan(bwd, N, False)
+    assert "/wide/" in plan(fwd, 32768) and "/wide/" in plan(bwd, 12288)
