@@ -436,10 +436,10 @@ DebugEnv g_env = read_debug_env();
 const Force& read_force() { return g_env.force; }
 long long wait_limit() { return g_env.wait_limit; }
 
-// kWide: the backward keeps its dgamma partial row (N columns, plus a
-// vector's worth on each side for the head and tail of dx's split) in shared
-// memory, and needs dx's split to be the same for every row.
-int64_t wide_smem(int N, int xd) { return round_up(N + 2 * per_vec(xd), 4) * 4LL; }
+// kWide: the backward keeps its dgamma partial row (N columns, laid out in
+// groups of 32 vectors with the head and tail of dx's split beside them) in
+// shared memory, and needs dx's split to be the same for every row.
+int64_t wide_smem(int N, int xd) { return wide_acc_floats(N, per_vec(xd)) * 4LL; }
 bool wide_ok(bool bwd, int N, int xd) {
   return !bwd || (((int64_t)N * esize(xd)) % 16 == 0 && wide_smem(N, xd) <= kStagedSmemMax);
 }

@@ -230,6 +230,10 @@ constexpr int kCtaMaxThreads = 512;
 // thread).
 constexpr int kWideThreads = 512;
 constexpr int kWideBwdThreads = 512;
+// Floats of a kWide backward's shared-memory partial row for rows of N
+// elements, E per 16-byte vector (any split of the row): the head's columns,
+// the body in groups of 32 vectors, the tail's columns.
+constexpr int wide_acc_floats(int N, int E) { return 2 * E + (N / E + 32) / 32 * 32 * E; }
 // Threads of a stage-2 (column sum) CTA.
 constexpr int kColSumThreads = 256;
 

@@ -291,6 +291,24 @@ __global__ void __launch_bounds__(kWideThreads, (FUSED || sizeof(TW) > sizeof(TX
 
 // ---------------------------------------------------------------- backward
 //
+// A partial row in shared memory, for dx's split (head, nv): the head's
+// columns at [0, E), then the body in groups of 32 vectors -- for each
+// float4 w of a vector, the group's 32 float4s side by side, so that a warp's
+// access to 32 consecutive vectors covers 512 contiguous bytes (no bank
+// conflict; vectors laid end to end would put a warp's float4s 32 bytes
+// apart for bf16, two to a bank group) -- then the tail's columns.
+template <int E>
+__device__ __forceinline__ int acc_vec(int v, int w) {
+  return E + (v >> 5) * (32 * E) + w * 128 + (v & 31) * 4;
+}
+template <int E>
+__device__ __forceinline__ int acc_col(int j, int2 f) {
+  if (j < f.x) return j;
+  const int b = j - f.x, v = b / E;
+  if (v < f.y) return acc_vec<E>(v, (b - v * E) >> 2) + ((b - v * E) & 3);
+  return E + (f.y + 31) / 32 * (32 * E) + (b - f.y * E);
+}
+//
 // Both passes in dx's frame (rows a multiple of 16 bytes: the same split, and
 // the same shifts of x and dy against it, for every row), and pass 2 of a row
 // fused with pass 1 of the CTA's next row: one loop over dx's vectors reads
@@ -304,7 +322,7 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
   constexpr int K = HAS_RSTD ? 1 : 2;
-  // dgamma partial row: column j at acc_s[j - head + E], head = dx's head
+  // dgamma partial row, laid out by acc_col for dx's split
   extern __shared__ __align__(16) float acc_s[];
   __shared__ float red[2 * 2 * 32];
   const int tid = threadIdx.x, T = blockDim.x, N = p.N;
@@ -316,7 +334,7 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
   const int je = edge_elem<E>(fo, N, tid, T);   // this thread's head or tail element
   const TW* gp = static_cast<const TW*>(p.gamma);
   if (dg)
-    for (int i = tid; i < N + 2 * E; i += T) acc_s[i] = 0.f;
+    for (int i = tid; i < wide_acc_floats(N, E); i += T) acc_s[i] = 0.f;
   const char* x0 = static_cast<const char*>(p.x);
   const char* d0 = static_cast<const char*>(p.dy);
   int64_t row = blockIdx.x;
@@ -376,10 +394,10 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
       }
       float gf[E], acc[E];
       unpack_gamma<TW, E, GW>(g, gf);
-      float4* ap = reinterpret_cast<float4*>(acc_s + E + (size_t)v * E);
 #pragma unroll
       for (int w = 0; w < E / 4; ++w) {
-        const float4 t = dg ? ap[w] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 t = dg ? *reinterpret_cast<const float4*>(acc_s + acc_vec<E>(v, w))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
         acc[4 * w] = t.x;
         acc[4 * w + 1] = t.y;
         acc[4 * w + 2] = t.z;
@@ -389,7 +407,8 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
       if (dg) {
 #pragma unroll
         for (int w = 0; w < E / 4; ++w)
-          ap[w] = make_float4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]);
+          *reinterpret_cast<float4*>(acc_s + acc_vec<E>(v, w)) =
+              make_float4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]);
       }
       if (more) bwd_vec_sums<E, !HAS_RSTD>(an, dnv, gf, dot, sq);
     }
@@ -401,7 +420,7 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
       if (DRES) o += ld_scalar_cg(reinterpret_cast<const TX*>(rr) + je);
       st_scalar(reinterpret_cast<TX*>(dxr) + je, o);
       if (dg) {
-        float* a = acc_s + (je - fo.x + E);
+        float* a = acc_s + acc_col<E>(je, fo);
         *a = fmaf(dv * xv, r, *a);
       }
       if (more) {
@@ -415,7 +434,7 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
   if (dg) {
     __syncthreads();
     float* prow = p.partial + (size_t)blockIdx.x * p.ld_partial;
-    for (int j = tid; j < N; j += T) prow[j] = acc_s[j - fo.x + E];
+    for (int j = tid; j < N; j += T) prow[j] = acc_s[acc_col<E>(j, fo)];
   }
 }
 
@@ -585,7 +604,7 @@ __global__ void __launch_bounds__(kWideThreads, 2) ln_fwd_wide_kernel(const LnPa
 }
 
 // Backward: rows a multiple of 16 bytes; the partial rows [dgamma | dbeta]
-// in shared memory, each half NA floats laid out as the RMSNorm backward's.
+// in shared memory, each NA floats laid out as the RMSNorm backward's.
 template <typename TX, typename TW>
 __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const LnParams p) {
   pdl_begin();
@@ -595,7 +614,7 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
   extern __shared__ __align__(16) float acc_s[];
   __shared__ float red[128];
   const int tid = threadIdx.x, T = blockDim.x, N = p.N;
-  const int NA = (N + 2 * E + 3) / 4 * 4;
+  const int NA = wide_acc_floats(N, E);   // [dgamma | dbeta], each laid out by acc_col
   const size_t rb = (size_t)N * ES;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const bool dg = p.partial != nullptr;
@@ -677,12 +696,12 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
         unpack(xv[u], xf);
         unpack(dv[u], df);
         unpack_gamma<TW, E, GW>(g[u], gf);
-        float4* ag = reinterpret_cast<float4*>(acc_s + E + (size_t)v * E);
-        float4* ab = reinterpret_cast<float4*>(acc_s + NA + E + (size_t)v * E);
 #pragma unroll
         for (int w = 0; w < E / 4; ++w) {
-          const float4 tg = dg ? ag[w] : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4 tb = dg ? ab[w] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float* ag = acc_s + acc_vec<E>(v, w);
+          const float4 tg = dg ? *reinterpret_cast<const float4*>(ag) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 tb = dg ? *reinterpret_cast<const float4*>(ag + NA)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
           pg[4 * w] = tg.x; pg[4 * w + 1] = tg.y; pg[4 * w + 2] = tg.z; pg[4 * w + 3] = tg.w;
           pb[4 * w] = tb.x; pb[4 * w + 1] = tb.y; pb[4 * w + 2] = tb.z; pb[4 * w + 3] = tb.w;
         }
@@ -697,8 +716,11 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
         if (dg) {
 #pragma unroll
           for (int w = 0; w < E / 4; ++w) {
-            ag[w] = make_float4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
-            ab[w] = make_float4(pb[4 * w], pb[4 * w + 1], pb[4 * w + 2], pb[4 * w + 3]);
+            float* ag = acc_s + acc_vec<E>(v, w);
+            *reinterpret_cast<float4*>(ag) =
+                make_float4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
+            *reinterpret_cast<float4*>(ag + NA) =
+                make_float4(pb[4 * w], pb[4 * w + 1], pb[4 * w + 2], pb[4 * w + 3]);
           }
         }
       }
@@ -709,7 +731,7 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
       st_scalar(reinterpret_cast<TX*>(dxr) + je,
                 st.z * (dv * ld_scalar_ro(gp + je) - fmaf(xh, mgx, mg)));
       if (dg) {
-        float* ag = acc_s + (je - fo.x + E);
+        float* ag = acc_s + acc_col<E>(je, fo);
         *ag = fmaf(dv, xh, *ag);
         ag[NA] += dv;
       }
@@ -719,8 +741,9 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
     __syncthreads();
     float* prow = p.partial + (size_t)blockIdx.x * 2 * p.ld_half;
     for (int j = tid; j < N; j += T) {
-      prow[j] = acc_s[j - fo.x + E];
-      prow[p.ld_half + j] = acc_s[NA + j - fo.x + E];
+      const int i = acc_col<E>(j, fo);
+      prow[j] = acc_s[i];
+      prow[p.ld_half + j] = acc_s[NA + i];
     }
   }
 }
