@@ -189,8 +189,10 @@ rmsnorm_status_t rmsnorm_fwd_nvfp4(const void* x, void* residual, const void* ga
 
 /*
  * Workspace of rmsnorm_bwd, in bytes, for these sizes on `device` (-1: the
- * current device).  It depends on the device's SM count.  Writes *bytes
- * (0 when M == 0 or no dgamma is wanted is still a valid answer to pass).
+ * current device).  It depends on the device's SM count, and covers every
+ * alignment of the operands (those off 16 bytes may take a kernel with more
+ * CTAs, hence more partial rows, than aligned ones).  Writes *bytes (0 when
+ * M == 0 or no dgamma is wanted is still a valid answer to pass).
  */
 rmsnorm_status_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, rmsnorm_dtype_t x_dtype,
                                             rmsnorm_dtype_t w_dtype, int device,
@@ -252,9 +254,12 @@ rmsnorm_status_t rmsnorm_fused_add_bwd(const void* dy, const void* h, const floa
  * array of RMSNORM_BWD_NOALLOC_SCRATCH_BYTES that is part of the library's
  * device image.  Neither the library nor the caller allocates anything.
  *
- *  - Limit: shapes whose partial rows need more than the scratch (the size
- *    rmsnorm_bwd_workspace_size reports exceeds RMSNORM_BWD_NOALLOC_SCRATCH_BYTES)
- *    are rejected with RMSNORM_ERR_WORKSPACE before any launch.
+ *  - Limit: a shape whose size from rmsnorm_bwd_workspace_size fits in
+ *    RMSNORM_BWD_NOALLOC_SCRATCH_BYTES always runs.  Where it does not, the
+ *    call runs when the partial rows of 16-byte aligned operands fit (it
+ *    then gives operands at other offsets fewer CTAs than rmsnorm_bwd
+ *    would) and is otherwise rejected with RMSNORM_ERR_WORKSPACE before any
+ *    launch.
  *  - Memory: every GPU that loads the library keeps the scratch until the
  *    process exits.
  *  - Set-up: the first call on each device looks up the scratch's device

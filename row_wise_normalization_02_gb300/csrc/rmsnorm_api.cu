@@ -1586,7 +1586,9 @@ rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
 // Stage-1 CTA count bound for these sizes: the grid of the plan for 16-byte
 // aligned operands.  Every launch clamps its stage-1 grid to it, so the
 // workspace query does not need the pointers.
-rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, int* rows) {
+// aligned_rows (optional): the aligned plan's bound alone.
+rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, int* rows,
+                                  int* aligned_rows = nullptr) {
   Plan pl;
   rmsnorm_status_t st = make_plan(kBwd, M, N, xd, wd, true, true, true, &pl);
   if (st != RMSNORM_OK) {
@@ -1596,6 +1598,7 @@ rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, 
   }
   if ((st = size_grid(&pl, M, device)) != RMSNORM_OK) return st;
   *rows = pl.cluster > 0 ? pl.grid / pl.cluster : pl.grid;   // a partial row per cluster
+  if (aligned_rows) *aligned_rows = *rows;
   // operands at other offsets may take the wide kernel, whose grid (one row
   // per CTA, several CTAs per SM) the aligned plan's need not bound
   Plan pw;
@@ -1607,11 +1610,14 @@ rmsnorm_status_t bwd_partial_rows(int64_t M, int N, int xd, int wd, int device, 
 
 // Backward and fused-add backward.  dres (fused-add backward only) is the
 // residual-path gradient; its result dh = dx + dres goes to dx, which is then
-// the same buffer.  dgamma is fp32, or bf16 when dgamma_bf16.
+// the same buffer.  dgamma is fp32, or bf16 when dgamma_bf16.  fit: a
+// workspace of fixed size (the allocation-free entry point's scratch) that
+// holds the aligned plan's partial rows but not the wide kernel's bounds the
+// stage-1 grid instead of failing.
 rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, const void* gamma,
                           void* dx, const void* dres, void* dgamma, bool dgamma_bf16,
                           void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
-                          float eps, int xd, int wd, cudaStream_t stream) {
+                          float eps, int xd, int wd, cudaStream_t stream, bool fit = false) {
   rmsnorm_status_t st = check_sizes(M, N, eps);
   if (st != RMSNORM_OK) return st;
   if (!dtype_pair_ok(xd, wd)) return RMSNORM_ERR_UNSUPPORTED_DTYPE;
@@ -1641,10 +1647,15 @@ rmsnorm_status_t bwd_impl(const void* dy, const void* x, const float* rstd, cons
   int dev;
   if ((st = current_device(&dev)) != RMSNORM_OK) return st;
   const int ld = round_up((int)N, 4);
-  int prows = 0;
+  int prows = 0, prows_aligned = 0;
   if (dgamma) {
-    if ((st = bwd_partial_rows(M, (int)N, xd, wd, dev, &prows)) != RMSNORM_OK) return st;
-    const size_t need = (size_t)prows * ld * 4;
+    if ((st = bwd_partial_rows(M, (int)N, xd, wd, dev, &prows, &prows_aligned)) != RMSNORM_OK)
+      return st;
+    size_t need = (size_t)prows * ld * 4;
+    if (fit && workspace_bytes < need && workspace_bytes >= (size_t)prows_aligned * ld * 4) {
+      prows = (int)(workspace_bytes / ((size_t)ld * 4));
+      need = (size_t)prows * ld * 4;
+    }
     if (!workspace || workspace_bytes < need || !aligned_to(workspace, 16))
       return RMSNORM_ERR_WORKSPACE;
     if (overlap(workspace, need, dx, act) || overlap(workspace, need, dgamma, db) ||
@@ -1883,10 +1894,11 @@ rmsnorm_status_t rmsnorm_bwd_noalloc(const void* dy, const void* x, const float*
     if ((st = noalloc_scratch(dev, &scratch)) != RMSNORM_OK) return st;
   }
   // the workspace entry point with the static scratch as its workspace: a
-  // shape whose partial rows exceed the scratch gets RMSNORM_ERR_WORKSPACE
+  // shape whose aligned plan's partial rows exceed the scratch gets
+  // RMSNORM_ERR_WORKSPACE; the wide kernel's larger grid is bounded to it
   return bwd_impl(dy, x, rstd, gamma, dx, nullptr, dgamma, false, scratch,
                   scratch ? (size_t)RMSNORM_BWD_NOALLOC_SCRATCH_BYTES : 0, M, N, eps,
-                  (int)x_dtype, (int)w_dtype, stream);
+                  (int)x_dtype, (int)w_dtype, stream, true);
 }
 
 rmsnorm_status_t rmsnorm_check_device(cudaStream_t stream) {

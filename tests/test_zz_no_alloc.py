@@ -7,10 +7,14 @@ scratch array inside the library's device image instead.
 Checked through the C ABI against rmsnorm_bwd (with a workspace) on two calls
 in a row with different shapes and data -- bit for bit, since both run the
 same kernels -- and against the oracle; also on ragged rows (whose grid is
-whole residue classes of the row alignment) and fp32 operands, and for the
-rejection of a shape whose partial rows do not fit the scratch.  This file is
+whole residue classes of the row alignment) and fp32 operands, on operands
+off 16 bytes whose wide kernel wants more partial rows than the scratch holds
+(its grid is bounded to it), and for the rejection of a shape whose partial
+rows do not fit the scratch.  This file is
 collected last; it passes alone in a fresh process and after the other tests.
 """
+import re
+
 import numpy as np
 import pytest
 
@@ -78,6 +82,39 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
                                        (1024, 4096, "f32", "f32")])
 def test_noalloc_ragged_and_fp32_shapes(M, N, xd, wd):
     _compare_with_workspace_entry_point(M, N, xd, wd, seed=34)
+
+
+def test_noalloc_bounds_the_wide_grid_to_its_scratch():
+    # x off 16 bytes at 32768 bf16 columns: the wide backward, one CTA per SM,
+    # wants more partial rows than the scratch holds; the aligned plan's
+    # (clusters) fit, and the call runs with fewer CTAs
+    M, N = 2048, 32768
+    ws = rn.rmsnorm_bwd_workspace_size(M, N, "bf16", "bf16")
+    aligned = rn.rmsnorm_describe_plan(rn.OP_BWD, M, N, "bf16", "bf16", True)
+    grid = int(aligned.split("/grid")[1].split("/")[0])
+    m = re.search(r"/cl(\d+)/", aligned)
+    cl = int(m.group(1)) if m else 1
+    if ws <= rn.NOALLOC_SCRATCH_BYTES or (grid // cl) * N * 4 > rn.NOALLOC_SCRATCH_BYTES:
+        pytest.skip("this device's grids do not give the case")
+    assert "/wide/" in rn.rmsnorm_describe_plan(rn.OP_BWD, M, N, "bf16", "bf16", "mixed")
+    x, dy, g, rstd = _inputs(M, N, "bf16", "bf16", seed=35)
+    eps = float(np.float32(1e-5))
+    bx, bdy, bg, brs = pu.dev(x, 2), pu.dev(dy), pu.dev(g), pu.dev(rstd)
+    dx_a, dg_a = pu.empty(M * N, "bf16"), pu.empty(N, "f32")
+    bws = pu.Buf(ws)
+    rn.rmsnorm_bwd(bdy.ptr, bx.ptr, brs.ptr, bg.ptr, dx_a.ptr, dg_a.ptr, bws.ptr, ws, M, N, eps,
+                   "bf16", "bf16")
+    dx_b, dg_b = pu.empty(M * N, "bf16"), pu.empty(N, "f32")
+    rn.rmsnorm_bwd_noalloc(bdy.ptr, bx.ptr, brs.ptr, bg.ptr, dx_b.ptr, dg_b.ptr, M, N, eps,
+                           "bf16", "bf16")
+    torch.cuda.synchronize()
+    for b in (dx_a, dg_a, dx_b, dg_b, bws):
+        assert b.guards_ok()
+    npd = pu.np_dtype("bf16")
+    a_dx, b_dx = dx_a.download(npd, (M, N)), dx_b.download(npd, (M, N))
+    # dx does not depend on the grid; dgamma's summation order does
+    assert np.array_equal(a_dx.view(np.uint8), b_dx.view(np.uint8)), "dx differs"
+    check_bwd(x, dy, g, rstd, eps, "bf16", "bf16", {"dx": b_dx, "dgamma": dg_b.download(np.float32)})
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
