@@ -449,15 +449,35 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) bwd_wide_kernel(const BwdP
 // dx = rs (dy gamma - (mg + xh mgx)) with xh = ((x - m0) - c) rs, mg and mgx
 // the row means of dy gamma and dy gamma xh, dgamma += dy xh, dbeta += dy.
 
+// Sum of a vector's elements into two accumulators (even / odd elements);
+// bf16 straight from the packed words by the mixed-precision FMA with 1 (one
+// rounding, as the fp32 add of the exact value).
 template <typename TX>
 __device__ __forceinline__ void vec_sum(const uint4& v, float& s0, float& s1) {
-  constexpr int E = Elem<TX>::kPerVec;
-  float f[E];
-  unpack(v, f);
-#pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    s0 += f[e];
-    s1 += f[e + 1];
+  if constexpr (std::is_same<TX, bf16>::value) {
+    asm("{\n\t.reg .b16 l0, h0, l1, h1, l2, h2, l3, h3, one;\n\t"
+        "mov.b16 one, 0x3F80;\n\t"
+        "mov.b32 {l0, h0}, %2;\n\t"
+        "mov.b32 {l1, h1}, %3;\n\t"
+        "mov.b32 {l2, h2}, %4;\n\t"
+        "mov.b32 {l3, h3}, %5;\n\t"
+        "fma.rn.f32.bf16 %0, l0, one, %0;\n\t"
+        "fma.rn.f32.bf16 %1, h0, one, %1;\n\t"
+        "fma.rn.f32.bf16 %0, l1, one, %0;\n\t"
+        "fma.rn.f32.bf16 %1, h1, one, %1;\n\t"
+        "fma.rn.f32.bf16 %0, l2, one, %0;\n\t"
+        "fma.rn.f32.bf16 %1, h2, one, %1;\n\t"
+        "fma.rn.f32.bf16 %0, l3, one, %0;\n\t"
+        "fma.rn.f32.bf16 %1, h3, one, %1;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+  } else {
+    float f[4];
+    unpack(v, f);
+    s0 += f[0];
+    s1 += f[1];
+    s0 += f[2];
+    s1 += f[3];
   }
 }
 
@@ -589,8 +609,18 @@ __global__ void __launch_bounds__(kWideThreads, 2) ln_fwd_wide_kernel(const LnPa
 #pragma unroll
           for (int e = 0; e < E; ++e) bf[e] = 0.f;
         }
+        // ((x - m0) - c) rs gamma + beta, two elements per paired instruction
+        const float2 nm = make_float2(-st.x, -st.x), nc = make_float2(-st.y, -st.y),
+                     r2 = make_float2(st.z, st.z);
 #pragma unroll
-        for (int e = 0; e < E; ++e) xf[e] = fmaf(((xf[e] - st.x) - st.y) * st.z, gf[e], bf[e]);
+        for (int e = 0; e < E; e += 2) {
+          const float2 t = __fmul2_rn(
+              __fadd2_rn(__fadd2_rn(make_float2(xf[e], xf[e + 1]), nm), nc), r2);
+          const float2 o =
+              __ffma2_rn(t, make_float2(gf[e], gf[e + 1]), make_float2(bf[e], bf[e + 1]));
+          xf[e] = o.x;
+          xf[e + 1] = o.y;
+        }
         st_stream(yb + (size_t)v * 16, pack(xf));
       }
     }
@@ -610,7 +640,7 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
   pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
-  constexpr int U = 2, UB = 1;   // vectors in flight: pass a, pass b
+  constexpr int U = GW == 2 ? 1 : 2, UB = 1;   // vectors in flight: pass a, pass b
   extern __shared__ __align__(16) float acc_s[];
   __shared__ float red[128];
   const int tid = threadIdx.x, T = blockDim.x, N = p.N;
@@ -634,8 +664,11 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
     if (p.mean != nullptr) st = make_float3(p.mean[row], 0.f, p.rstd[row]);
     else st = wide_ln_stats<TX>(xr, N, red, parity, p.inv_n, p.eps);
     const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES);
-    // pass a: the row sums of g = dy gamma and g xh
-    float a = 0.f, b = 0.f;
+    // pass a: the row sums of g = dy gamma and g xh (even / odd elements
+    // apart, two per paired instruction)
+    const float2 nm = make_float2(-st.x, -st.x), nc = make_float2(-st.y, -st.y),
+                 r2 = make_float2(st.z, st.z);
+    float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
     for (int v0 = tid; v0 < fo.y; v0 += U * T) {
       uint4 xv[U], dv[U], g[U][GW];
 #pragma unroll
@@ -658,20 +691,23 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
         unpack(dv[u], df);
         unpack_gamma<TW, E, GW>(g[u], gf);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float gd = df[e] * gf[e];   // 0 past the row
-          a += gd;
-          b = fmaf(gd, ((xf[e] - st.x) - st.y) * st.z, b);
+        for (int e = 0; e < E; e += 2) {
+          const float2 gd = __fmul2_rn(make_float2(df[e], df[e + 1]),
+                                       make_float2(gf[e], gf[e + 1]));   // 0 past the row
+          const float2 xh = __fmul2_rn(
+              __fadd2_rn(__fadd2_rn(make_float2(xf[e], xf[e + 1]), nm), nc), r2);
+          a2 = __fadd2_rn(a2, gd);
+          b2 = __ffma2_rn(gd, xh, b2);
         }
       }
     }
     if (je >= 0) {
       const float xh = ((ld_scalar(reinterpret_cast<const TX*>(xr) + je) - st.x) - st.y) * st.z;
       const float gd = ld_scalar(reinterpret_cast<const TX*>(dr) + je) * ld_scalar_ro(gp + je);
-      a += gd;
-      b = fmaf(gd, xh, b);
+      a2.x += gd;
+      b2.x = fmaf(gd, xh, b2.x);
     }
-    float t[2] = {a, b};
+    float t[2] = {a2.x + a2.y, b2.x + b2.y};
     cta_sum<2>(t, red, parity);
     parity ^= 1;
     const float mg = t[0] * p.inv_n, mgx = t[1] * p.inv_n;
@@ -705,12 +741,24 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
           pg[4 * w] = tg.x; pg[4 * w + 1] = tg.y; pg[4 * w + 2] = tg.z; pg[4 * w + 3] = tg.w;
           pb[4 * w] = tb.x; pb[4 * w + 1] = tb.y; pb[4 * w + 2] = tb.z; pb[4 * w + 3] = tb.w;
         }
+        const float2 mgx2 = make_float2(mgx, mgx), mg2 = make_float2(mg, mg);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float xh = ((xf[e] - st.x) - st.y) * st.z;
-          xf[e] = st.z * (df[e] * gf[e] - fmaf(xh, mgx, mg));
-          pg[e] = fmaf(df[e], xh, pg[e]);
-          pb[e] += df[e];
+        for (int e = 0; e < E; e += 2) {
+          const float2 d2 = make_float2(df[e], df[e + 1]);
+          const float2 xh = __fmul2_rn(
+              __fadd2_rn(__fadd2_rn(make_float2(xf[e], xf[e + 1]), nm), nc), r2);
+          const float2 f = __ffma2_rn(xh, mgx2, mg2);
+          const float2 o = __fmul2_rn(
+              r2, __fadd2_rn(__fmul2_rn(d2, make_float2(gf[e], gf[e + 1])),
+                             make_float2(-f.x, -f.y)));
+          const float2 q = __ffma2_rn(d2, xh, make_float2(pg[e], pg[e + 1]));
+          const float2 w = __fadd2_rn(make_float2(pb[e], pb[e + 1]), d2);
+          xf[e] = o.x;
+          xf[e + 1] = o.y;
+          pg[e] = q.x;
+          pg[e + 1] = q.y;
+          pb[e] = w.x;
+          pb[e + 1] = w.y;
         }
         st_stream(ob + (size_t)v * 16, pack(xf));
         if (dg) {
