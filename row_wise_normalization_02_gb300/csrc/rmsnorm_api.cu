@@ -2,18 +2,24 @@
 // dispatch table, grid sizing and launches.  No kernels live here.
 //
 // Dispatch (aligned rows = every base pointer 16-byte aligned and N * size a
-// multiple of 16 bytes; E = elements per 16-byte vector):
+// multiple of 16 bytes; E = elements per 16-byte vector; make_plan has the
+// measured reasons):
 //   N / E <= 128        kSubwarp  G lanes per row (4..32), VPT vectors per lane,
 //                                 several rows per 256-thread CTA; the short-row
 //                                 packing idea of the softmax kernel's
 //                                 THREADS_PER_ROW / ROWS_PER_BLOCK knobs
-//                                 ("Pre-built kernel library guide", 2.1)
-//   N / E <= 4096       kCta      one row per CTA of ceil(N / E / VPT) threads,
-//                                 row in registers
-//   otherwise           kGeneric
-// Rows that are not 16-byte aligned but whose operands agree modulo 16 bytes
-// take kRagged (N <= kRaggedMaxN), anything else kGeneric.  Grids are
-// persistent: min(rows, SMs x resident CTAs per SM).
+//                                 ("Pre-built kernel library guide", 2.1); the
+//                                 backward of 65-96 vectors through kStaged
+//   N / E <= 2048/4096  kCta      one row per CTA of ceil(N / E / VPT) threads,
+//                                 row in registers (backward: kStaged, rows by
+//                                 bulk copies into a shared-memory ring)
+//   longer              kCluster  one row per thread-block cluster
+// Rows off 16 bytes whose operands agree modulo 16 bytes, and inputs off the
+// outputs' alignment, take kRagged (its mixed form) or, for the backward,
+// kStaged's mixed form; what none of these takes goes to kWide (two passes of
+// 16-byte vectors, each operand realigned to the pass's frame) and, where
+// that does not apply either, kGeneric.  Grids are persistent: min(rows, SMs
+// x resident CTAs per SM).
 #include <cuda_runtime.h>
 
 #include <math.h>
