@@ -327,7 +327,8 @@ const char* rmsnorm_status_string(rmsnorm_status_t status);
  * len).  op: 0 forward, 1 fused add, 2 backward, 3 fused-add backward,
  * 4 strided forward (M = tokens x heads rows of N = D elements), 5 FP8
  * forward, 6 fused-add FP8 forward, 7 NVFP4 forward, 8 fused-add NVFP4,
- * 9 LayerNorm forward, 10 LayerNorm backward.  aligned16:
+ * 9 LayerNorm forward, 10 LayerNorm backward (with the forward's mean and
+ * rstd given).  aligned16:
  * nonzero when all operand base pointers (and, for op 4, all strides) are
  * 16-byte aligned; for ops 0-3, 2 describes outputs on 16 bytes with x (and
  * dy) off them (for example x a view at an odd element offset).  Returns

@@ -1259,7 +1259,7 @@ bool ln_wide_ok(bool bwd, int64_t N, int xd) {
 // the backward of rows of 65-128 vectors takes the ring with eight rows of 32
 // lanes per stage.  Anything else: the scalar kernel.
 rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool vec_ok,
-                         Plan* res) {
+                         Plan* res, bool saved = false) {
   const int E = per_vec(xd);
   const int nvec = vec_ok ? (int)(N / E) : 0;
   Plan p;
@@ -1401,7 +1401,14 @@ rmsnorm_status_t ln_plan(bool bwd, int64_t M, int64_t N, int xd, int wd, bool ve
       return RMSNORM_ERR_INVALID_ARG;
   }
   if (p.family != kSubwarp && p.family != kStaged) p.g = 0;
+  // the wide backward with saved statistics: the pipelined form, smaller CTAs
+  const bool wide_saved = bwd && saved && p.family == kWide;
+  if (wide_saved && p.threads > kLnSavedThreads) {
+    if (f.on && f.threads) return RMSNORM_ERR_INVALID_ARG;
+    p.threads = kLnSavedThreads;
+  }
   LnKey k{xd, wd, p.family, p.g, p.vpt, bwd, p.prefetch};
+  k.saved = wide_saved;
   LnKernel fn = ln_kernel(k);
   if (fn == nullptr) return RMSNORM_ERR_INVALID_ARG;
   p.fn = reinterpret_cast<const void*>(fn);
@@ -1547,7 +1554,7 @@ rmsnorm_status_t ln_bwd_impl(const void* dy, const void* x, const float* mean,
   const bool vec_ok = aligned_to(x, 16) && aligned_to(dy, 16) && aligned_to(dx, 16) &&
                       aligned_to(gamma, 16) && (N * (int64_t)xs) % 16 == 0;
   Plan p;
-  if ((st = ln_plan(true, M, N, xd, wd, vec_ok, &p)) != RMSNORM_OK) return st;
+  if ((st = ln_plan(true, M, N, xd, wd, vec_ok, &p, mean != nullptr)) != RMSNORM_OK) return st;
   unsigned* status = nullptr;
   if ((st = size_grid(&p, M, dev, &status)) != RMSNORM_OK) return st;
   if (want && p.grid > prows) p.grid = prows;
@@ -1954,7 +1961,8 @@ rmsnorm_status_t rmsnorm_describe_plan(int op, int64_t M, int64_t N, rmsnorm_dty
   Plan pl;
   if (op >= 9) {
     if ((st = ln_plan(op == 10, M, N, (int)x_dtype, (int)w_dtype,
-                      aligned16 != 0 && (N * esize((int)x_dtype)) % 16 == 0, &pl)) != RMSNORM_OK)
+                      aligned16 != 0 && (N * esize((int)x_dtype)) % 16 == 0, &pl,
+                      op == 10)) != RMSNORM_OK)
       return st;
   } else if (op >= 5) {
     const int out = op <= 6 ? kOutFp8 : kOutNvfp4;

@@ -215,6 +215,7 @@ struct LnKey {
   int g, vpt;
   bool bwd;
   bool prefetch;
+  bool saved = false;   // kWide backward: mean and rstd given (rows pipelined)
 };
 LnKernel get_ln_kernel_f32_f32(const LnKey& k);
 LnKernel get_ln_kernel_bf16_bf16(const LnKey& k);
@@ -230,6 +231,9 @@ constexpr int kCtaMaxThreads = 512;
 // thread).
 constexpr int kWideThreads = 512;
 constexpr int kWideBwdThreads = 512;
+// Most threads of the wide LayerNorm backward with saved statistics, whose
+// fused passes of two rows take 80 registers a thread at two CTAs per SM.
+constexpr int kLnSavedThreads = 384;
 // Floats of a kWide backward's shared-memory partial row for rows of N
 // elements, E per 16-byte vector (any split of the row): the head's columns,
 // the body in groups of 32 vectors, the tail's columns.

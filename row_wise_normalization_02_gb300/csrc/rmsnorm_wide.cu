@@ -635,12 +635,117 @@ __global__ void __launch_bounds__(kWideThreads, 2) ln_fwd_wide_kernel(const LnPa
 
 // Backward: rows a multiple of 16 bytes; the partial rows [dgamma | dbeta]
 // in shared memory, each NA floats laid out as the RMSNorm backward's.
+
+// Pass a of one vector: the row sums of g = dy gamma and g xh, even / odd
+// elements apart, two per paired instruction.
+template <typename TX, int E>
+__device__ __forceinline__ void ln_sums_vec(const uint4& xv, const uint4& dv,
+                                            const float (&gf)[E], float3 st, float2& a2,
+                                            float2& b2) {
+  float xf[E], df[E];
+  unpack(xv, xf);
+  unpack(dv, df);
+  const float2 nm = make_float2(-st.x, -st.x), nc = make_float2(-st.y, -st.y),
+               r2 = make_float2(st.z, st.z);
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const float2 gd =
+        __fmul2_rn(make_float2(df[e], df[e + 1]), make_float2(gf[e], gf[e + 1]));   // 0 past the row
+    const float2 xh =
+        __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(xf[e], xf[e + 1]), nm), nc), r2);
+    a2 = __fadd2_rn(a2, gd);
+    b2 = __ffma2_rn(gd, xh, b2);
+  }
+}
+
+// Pass b of body vector v: dx = rs (dy gamma - (mg + xh mgx)), and
+// dgamma += dy xh, dbeta += dy in the partial rows (when dg).
+template <typename TX, int E>
+__device__ __forceinline__ uint4 ln_dx_vec(int v, const uint4& xv, const uint4& dv,
+                                           const float (&gf)[E], float3 st, float mg,
+                                           float mgx, float* acc_s, int NA, bool dg) {
+  float xf[E], df[E], pg[E], pb[E];
+  unpack(xv, xf);
+  unpack(dv, df);
+#pragma unroll
+  for (int w = 0; w < E / 4; ++w) {
+    const float* ag = acc_s + acc_vec<E>(v, w);
+    const float4 tg = dg ? *reinterpret_cast<const float4*>(ag) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 tb = dg ? *reinterpret_cast<const float4*>(ag + NA)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    pg[4 * w] = tg.x; pg[4 * w + 1] = tg.y; pg[4 * w + 2] = tg.z; pg[4 * w + 3] = tg.w;
+    pb[4 * w] = tb.x; pb[4 * w + 1] = tb.y; pb[4 * w + 2] = tb.z; pb[4 * w + 3] = tb.w;
+  }
+  const float2 nm = make_float2(-st.x, -st.x), nc = make_float2(-st.y, -st.y),
+               r2 = make_float2(st.z, st.z), mgx2 = make_float2(mgx, mgx),
+               mg2 = make_float2(mg, mg);
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const float2 d2 = make_float2(df[e], df[e + 1]);
+    const float2 xh =
+        __fmul2_rn(__fadd2_rn(__fadd2_rn(make_float2(xf[e], xf[e + 1]), nm), nc), r2);
+    const float2 f = __ffma2_rn(xh, mgx2, mg2);
+    const float2 o = __fmul2_rn(
+        r2, __fadd2_rn(__fmul2_rn(d2, make_float2(gf[e], gf[e + 1])), make_float2(-f.x, -f.y)));
+    const float2 q = __ffma2_rn(d2, xh, make_float2(pg[e], pg[e + 1]));
+    const float2 w = __fadd2_rn(make_float2(pb[e], pb[e + 1]), d2);
+    xf[e] = o.x;
+    xf[e + 1] = o.y;
+    pg[e] = q.x;
+    pg[e + 1] = q.y;
+    pb[e] = w.x;
+    pb[e + 1] = w.y;
+  }
+  if (dg) {
+#pragma unroll
+    for (int w = 0; w < E / 4; ++w) {
+      float* ag = acc_s + acc_vec<E>(v, w);
+      *reinterpret_cast<float4*>(ag) =
+          make_float4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
+      *reinterpret_cast<float4*>(ag + NA) =
+          make_float4(pb[4 * w], pb[4 * w + 1], pb[4 * w + 2], pb[4 * w + 3]);
+    }
+  }
+  return pack(xf);
+}
+
+// The head or tail element je of a row: pass a's sums, or pass b's dx and
+// partials.
 template <typename TX, typename TW>
-__global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const LnParams p) {
+__device__ __forceinline__ void ln_sums_edge(const char* xr, const char* dr, const TW* gp, int je,
+                                             float3 st, float2& a2, float2& b2) {
+  const float xh = ((ld_scalar(reinterpret_cast<const TX*>(xr) + je) - st.x) - st.y) * st.z;
+  const float gd = ld_scalar(reinterpret_cast<const TX*>(dr) + je) * ld_scalar_ro(gp + je);
+  a2.x += gd;
+  b2.x = fmaf(gd, xh, b2.x);
+}
+template <typename TX, typename TW, int E>
+__device__ __forceinline__ void ln_dx_edge(const char* xr, const char* dr, char* dxr,
+                                           const TW* gp, int je, int2 fo, float3 st, float mg,
+                                           float mgx, float* acc_s, int NA, bool dg) {
+  const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + je);
+  const float xh = ((ld_scalar(reinterpret_cast<const TX*>(xr) + je) - st.x) - st.y) * st.z;
+  st_scalar(reinterpret_cast<TX*>(dxr) + je,
+            st.z * (dv * ld_scalar_ro(gp + je) - fmaf(xh, mgx, mg)));
+  if (dg) {
+    float* ag = acc_s + acc_col<E>(je, fo);
+    *ag = fmaf(dv, xh, *ag);
+    ag[NA] += dv;
+  }
+}
+
+// SAVED: the forward's mean and rstd are given; pass b of a row then runs
+// fused with pass a of the CTA's next row (one loop over dx's vectors reads
+// gamma once, the current row again and the next row from DRAM), as in the
+// RMSNorm wide backward, in CTAs of at most kLnSavedThreads (80 registers a
+// thread).  Otherwise the statistics, then pass a, then pass b.
+template <typename TX, typename TW, bool SAVED>
+__global__ void __launch_bounds__(SAVED ? kLnSavedThreads : kWideBwdThreads, 2)
+    ln_bwd_wide_kernel(const LnParams p) {
   pdl_begin();
   using C = Cfg<TX, TW>;
   constexpr int E = C::E, GW = C::GW, ES = (int)sizeof(TX), WS = (int)sizeof(TW);
-  constexpr int U = GW == 2 ? 1 : 2, UB = 1;   // vectors in flight: pass a, pass b
+  constexpr int U = GW == 2 ? 1 : 2;   // vectors in flight, pass a of the unsaved form
   extern __shared__ __align__(16) float acc_s[];
   __shared__ float red[128];
   const int tid = threadIdx.x, T = blockDim.x, N = p.N;
@@ -652,137 +757,114 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
   const Src gs = src_of(p.gamma, fo.x, WS);
   const int je = edge_elem<E>(fo, N, tid, T);
   const TW* gp = static_cast<const TW*>(p.gamma);
+  const char* x0 = static_cast<const char*>(p.x);
+  const char* d0 = static_cast<const char*>(p.dy);
+  char* dx0 = static_cast<char*>(p.y);
   if (dg)
     for (int i = tid; i < 2 * NA; i += T) acc_s[i] = 0.f;
   int parity = 0;
-  for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
-    const char* xr = static_cast<const char*>(p.x) + row * rb;
-    const char* dr = static_cast<const char*>(p.dy) + row * rb;
-    char* dxr = static_cast<char*>(p.y) + row * rb;
-    l2_ahead(p.l2_rows, row, row == blockIdx.x, p.M, rb, p.x, p.dy, nullptr);
-    float3 st;
-    if (p.mean != nullptr) st = make_float3(p.mean[row], 0.f, p.rstd[row]);
-    else st = wide_ln_stats<TX>(xr, N, red, parity, p.inv_n, p.eps);
-    const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES);
-    // pass a: the row sums of g = dy gamma and g xh (even / odd elements
-    // apart, two per paired instruction)
-    const float2 nm = make_float2(-st.x, -st.x), nc = make_float2(-st.y, -st.y),
-                 r2 = make_float2(st.z, st.z);
+  if constexpr (SAVED) {
+    int64_t row = blockIdx.x;
     float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
-    for (int v0 = tid; v0 < fo.y; v0 += U * T) {
-      uint4 xv[U], dv[U], g[U][GW];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * T;
-        if (v < fo.y) {
-          xv[u] = vec_at<kLdKeep>(xs, v);
-          dv[u] = vec_at<kLdKeep>(ds, v);
-          gamma_at<GW>(gs, v, g[u]);
-        } else {
-          xv[u] = dv[u] = zero;
-#pragma unroll
-          for (int w = 0; w < GW; ++w) g[u][w] = zero;
-        }
+    if (row < p.M) {   // pass a of the first row
+      l2_ahead(p.l2_rows, row + gridDim.x, true, p.M, rb, p.x, p.dy, nullptr);
+      const float3 st = make_float3(p.mean[row], 0.f, p.rstd[row]);
+      const Src xs = src_of(x0 + row * rb, fo.x, ES), ds = src_of(d0 + row * rb, fo.x, ES);
+      for (int v = tid; v < fo.y; v += T) {
+        uint4 g[GW];
+        gamma_at<GW>(gs, v, g);
+        const uint4 xv = vec_at<kLdKeep>(xs, v), dv = vec_at<kLdKeep>(ds, v);
+        float gf[E];
+        unpack_gamma<TW, E, GW>(g, gf);
+        ln_sums_vec<TX, E>(xv, dv, gf, st, a2, b2);
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float xf[E], df[E], gf[E];
-        unpack(xv[u], xf);
-        unpack(dv[u], df);
-        unpack_gamma<TW, E, GW>(g[u], gf);
-#pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const float2 gd = __fmul2_rn(make_float2(df[e], df[e + 1]),
-                                       make_float2(gf[e], gf[e + 1]));   // 0 past the row
-          const float2 xh = __fmul2_rn(
-              __fadd2_rn(__fadd2_rn(make_float2(xf[e], xf[e + 1]), nm), nc), r2);
-          a2 = __fadd2_rn(a2, gd);
-          b2 = __ffma2_rn(gd, xh, b2);
+      if (je >= 0) ln_sums_edge<TX, TW>(x0 + row * rb, d0 + row * rb, gp, je, st, a2, b2);
+    }
+    for (; row < p.M; row += gridDim.x) {
+      float t[2] = {a2.x + a2.y, b2.x + b2.y};
+      cta_sum<2>(t, red, parity);
+      parity ^= 1;
+      const float mg = t[0] * p.inv_n, mgx = t[1] * p.inv_n;
+      const int64_t nxt = row + gridDim.x;
+      const bool more = nxt < p.M;   // the same in every thread
+      const int64_t qn = more ? nxt : row;
+      l2_ahead(p.l2_rows, nxt, false, p.M, rb, p.x, p.dy, nullptr);
+      const float3 st = make_float3(p.mean[row], 0.f, p.rstd[row]);
+      const float3 sn = make_float3(p.mean[qn], 0.f, p.rstd[qn]);
+      const char* xr = x0 + row * rb;
+      const char* dr = d0 + row * rb;
+      char* dxr = dx0 + row * rb;
+      char* ob = dxr + (size_t)fo.x * ES;
+      const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES);
+      const Src xn = src_of(x0 + qn * rb, fo.x, ES), dn = src_of(d0 + qn * rb, fo.x, ES);
+      a2 = b2 = make_float2(0.f, 0.f);
+      for (int v = tid; v < fo.y; v += T) {
+        uint4 g[GW];
+        gamma_at<GW>(gs, v, g);
+        const uint4 xv = vec_at<kLdKeep>(xs, v), dv = vec_at<kLdKeep>(ds, v);
+        uint4 xv2 = zero, dv2 = zero;
+        if (more) {
+          xv2 = vec_at<kLdKeep>(xn, v);
+          dv2 = vec_at<kLdKeep>(dn, v);
         }
+        float gf[E];
+        unpack_gamma<TW, E, GW>(g, gf);
+        st_stream(ob + (size_t)v * 16,
+                  ln_dx_vec<TX, E>(v, xv, dv, gf, st, mg, mgx, acc_s, NA, dg));
+        if (more) ln_sums_vec<TX, E>(xv2, dv2, gf, sn, a2, b2);
+      }
+      if (je >= 0) {
+        ln_dx_edge<TX, TW, E>(xr, dr, dxr, gp, je, fo, st, mg, mgx, acc_s, NA, dg);
+        if (more) ln_sums_edge<TX, TW>(x0 + nxt * rb, d0 + nxt * rb, gp, je, sn, a2, b2);
       }
     }
-    if (je >= 0) {
-      const float xh = ((ld_scalar(reinterpret_cast<const TX*>(xr) + je) - st.x) - st.y) * st.z;
-      const float gd = ld_scalar(reinterpret_cast<const TX*>(dr) + je) * ld_scalar_ro(gp + je);
-      a2.x += gd;
-      b2.x = fmaf(gd, xh, b2.x);
-    }
-    float t[2] = {a2.x + a2.y, b2.x + b2.y};
-    cta_sum<2>(t, red, parity);
-    parity ^= 1;
-    const float mg = t[0] * p.inv_n, mgx = t[1] * p.inv_n;
-    // pass b: dx and the partial rows
-    char* ob = dxr + (size_t)fo.x * ES;
-    for (int v0 = tid; v0 < fo.y; v0 += UB * T) {
-      uint4 xv[UB], dv[UB], g[UB][GW];
+  } else {
+    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+      const char* xr = x0 + row * rb;
+      const char* dr = d0 + row * rb;
+      char* dxr = dx0 + row * rb;
+      l2_ahead(p.l2_rows, row, row == blockIdx.x, p.M, rb, p.x, p.dy, nullptr);
+      const float3 st = wide_ln_stats<TX>(xr, N, red, parity, p.inv_n, p.eps);
+      const Src xs = src_of(xr, fo.x, ES), ds = src_of(dr, fo.x, ES);
+      float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+      for (int v0 = tid; v0 < fo.y; v0 += U * T) {
+        uint4 xv[U], dv[U], g[U][GW];
 #pragma unroll
-      for (int u = 0; u < UB; ++u) {
-        const int v = v0 + u * T;
-        if (v < fo.y) {
-          xv[u] = vec_at<kLdKeep>(xs, v);
-          dv[u] = vec_at<kLdKeep>(ds, v);
-          gamma_at<GW>(gs, v, g[u]);
-        }
-      }
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * T;
+          if (v < fo.y) {
+            xv[u] = vec_at<kLdKeep>(xs, v);
+            dv[u] = vec_at<kLdKeep>(ds, v);
+            gamma_at<GW>(gs, v, g[u]);
+          } else {
+            xv[u] = dv[u] = zero;
 #pragma unroll
-      for (int u = 0; u < UB; ++u) {
-        const int v = v0 + u * T;
-        if (v >= fo.y) continue;
-        float xf[E], df[E], gf[E], pg[E], pb[E];
-        unpack(xv[u], xf);
-        unpack(dv[u], df);
-        unpack_gamma<TW, E, GW>(g[u], gf);
-#pragma unroll
-        for (int w = 0; w < E / 4; ++w) {
-          const float* ag = acc_s + acc_vec<E>(v, w);
-          const float4 tg = dg ? *reinterpret_cast<const float4*>(ag) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4 tb = dg ? *reinterpret_cast<const float4*>(ag + NA)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-          pg[4 * w] = tg.x; pg[4 * w + 1] = tg.y; pg[4 * w + 2] = tg.z; pg[4 * w + 3] = tg.w;
-          pb[4 * w] = tb.x; pb[4 * w + 1] = tb.y; pb[4 * w + 2] = tb.z; pb[4 * w + 3] = tb.w;
-        }
-        const float2 mgx2 = make_float2(mgx, mgx), mg2 = make_float2(mg, mg);
-#pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const float2 d2 = make_float2(df[e], df[e + 1]);
-          const float2 xh = __fmul2_rn(
-              __fadd2_rn(__fadd2_rn(make_float2(xf[e], xf[e + 1]), nm), nc), r2);
-          const float2 f = __ffma2_rn(xh, mgx2, mg2);
-          const float2 o = __fmul2_rn(
-              r2, __fadd2_rn(__fmul2_rn(d2, make_float2(gf[e], gf[e + 1])),
-                             make_float2(-f.x, -f.y)));
-          const float2 q = __ffma2_rn(d2, xh, make_float2(pg[e], pg[e + 1]));
-          const float2 w = __fadd2_rn(make_float2(pb[e], pb[e + 1]), d2);
-          xf[e] = o.x;
-          xf[e + 1] = o.y;
-          pg[e] = q.x;
-          pg[e + 1] = q.y;
-          pb[e] = w.x;
-          pb[e + 1] = w.y;
-        }
-        st_stream(ob + (size_t)v * 16, pack(xf));
-        if (dg) {
-#pragma unroll
-          for (int w = 0; w < E / 4; ++w) {
-            float* ag = acc_s + acc_vec<E>(v, w);
-            *reinterpret_cast<float4*>(ag) =
-                make_float4(pg[4 * w], pg[4 * w + 1], pg[4 * w + 2], pg[4 * w + 3]);
-            *reinterpret_cast<float4*>(ag + NA) =
-                make_float4(pb[4 * w], pb[4 * w + 1], pb[4 * w + 2], pb[4 * w + 3]);
+            for (int w = 0; w < GW; ++w) g[u][w] = zero;
           }
         }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          float gf[E];
+          unpack_gamma<TW, E, GW>(g[u], gf);
+          ln_sums_vec<TX, E>(xv[u], dv[u], gf, st, a2, b2);
+        }
       }
-    }
-    if (je >= 0) {
-      const float dv = ld_scalar(reinterpret_cast<const TX*>(dr) + je);
-      const float xh = ((ld_scalar(reinterpret_cast<const TX*>(xr) + je) - st.x) - st.y) * st.z;
-      st_scalar(reinterpret_cast<TX*>(dxr) + je,
-                st.z * (dv * ld_scalar_ro(gp + je) - fmaf(xh, mgx, mg)));
-      if (dg) {
-        float* ag = acc_s + acc_col<E>(je, fo);
-        *ag = fmaf(dv, xh, *ag);
-        ag[NA] += dv;
+      if (je >= 0) ln_sums_edge<TX, TW>(xr, dr, gp, je, st, a2, b2);
+      float t[2] = {a2.x + a2.y, b2.x + b2.y};
+      cta_sum<2>(t, red, parity);
+      parity ^= 1;
+      const float mg = t[0] * p.inv_n, mgx = t[1] * p.inv_n;
+      char* ob = dxr + (size_t)fo.x * ES;
+      for (int v = tid; v < fo.y; v += T) {
+        uint4 g[GW];
+        gamma_at<GW>(gs, v, g);
+        const uint4 xv = vec_at<kLdKeep>(xs, v), dv = vec_at<kLdKeep>(ds, v);
+        float gf[E];
+        unpack_gamma<TW, E, GW>(g, gf);
+        st_stream(ob + (size_t)v * 16,
+                  ln_dx_vec<TX, E>(v, xv, dv, gf, st, mg, mgx, acc_s, NA, dg));
       }
+      if (je >= 0) ln_dx_edge<TX, TW, E>(xr, dr, dxr, gp, je, fo, st, mg, mgx, acc_s, NA, dg);
     }
   }
   if (dg) {
@@ -799,7 +881,8 @@ __global__ void __launch_bounds__(kWideBwdThreads, 2) ln_bwd_wide_kernel(const L
 template <typename TX, typename TW>
 LnKernel pick_ln(const LnKey& k) {
   if (k.family != kWide) return nullptr;
-  return k.bwd ? ln_bwd_wide_kernel<TX, TW> : ln_fwd_wide_kernel<TX, TW>;
+  if (!k.bwd) return ln_fwd_wide_kernel<TX, TW>;
+  return k.saved ? ln_bwd_wide_kernel<TX, TW, true> : ln_bwd_wide_kernel<TX, TW, false>;
 }
 
 template <typename TX, typename TW>
