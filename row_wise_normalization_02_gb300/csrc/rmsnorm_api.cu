@@ -30,6 +30,7 @@
 
 #include "../../include/rmsnorm.h"
 #include "rmsnorm_internal.h"
+#include "rmsnorm_wide_layout.h"
 
 namespace rmsn {
 namespace {

@@ -234,10 +234,7 @@ constexpr int kWideBwdThreads = 512;
 // Most threads of the wide LayerNorm backward with saved statistics, whose
 // fused passes of two rows take 80 registers a thread at two CTAs per SM.
 constexpr int kLnSavedThreads = 384;
-// Floats of a kWide backward's shared-memory partial row for rows of N
-// elements, E per 16-byte vector (any split of the row): the head's columns,
-// the body in groups of 32 vectors, the tail's columns.
-constexpr int wide_acc_floats(int N, int E) { return 2 * E + (N / E + 32) / 32 * 32 * E; }
+
 // Threads of a stage-2 (column sum) CTA.
 constexpr int kColSumThreads = 256;
 

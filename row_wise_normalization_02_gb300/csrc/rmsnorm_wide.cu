@@ -30,6 +30,7 @@
 #include "rmsnorm_device.cuh"
 #include "rmsnorm_fwd_common.cuh"
 #include "rmsnorm_internal.h"
+#include "rmsnorm_wide_layout.h"
 
 #ifndef RMSN_PAIR
 #define RMSN_PAIR 1
@@ -42,9 +43,8 @@ namespace {
 // before the first 16-byte boundary (at most N), y = whole 16-byte vectors
 // after them; the rest is the tail.
 __device__ __forceinline__ int2 split_row(const void* row, int N, int es) {
-  int head = (int)(((16u - ((unsigned)reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) / es);
-  if (head > N) head = N;
-  return make_int2(head, (int)(((int64_t)(N - head) * es) >> 4));
+  const int head = wide_head(reinterpret_cast<uintptr_t>(row), N, es);
+  return make_int2(head, wide_nv(N, head, es));
 }
 
 // An operand read in another row's frame: the frame's body vector v is the
@@ -54,8 +54,8 @@ struct Src {
   int s;
 };
 __device__ __forceinline__ Src src_of(const void* row, int head, int es) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(row) + (uintptr_t)head * es;
-  return Src{reinterpret_cast<const char*>(a & ~(uintptr_t)15), (int)(a & 15)};
+  const WideSrc w = wide_src(reinterpret_cast<uintptr_t>(row), head, es);
+  return Src{reinterpret_cast<const char*>(w.base), w.s};
 }
 
 // Read of a chunk: read-only data that pass 2 re-reads (L1 allocation),
@@ -142,19 +142,15 @@ __device__ __forceinline__ float scale_scalar(float x, float g, float rs) {
 // last (both fewer than a vector's elements).
 template <int E>
 __device__ __forceinline__ int edge_elem(int2 f, int N, int tid, int T) {
-  if (tid < f.x) return tid;
-  const int t0 = f.x + f.y * E;
-  const int k = T - 1 - tid;
-  return k < N - t0 ? t0 + k : -1;
+  return wide_edge_elem(f.x, f.y, E, N, tid, T);
 }
 
 // Row q of a row-major operand (rows of rb bytes, any element-aligned base)
 // requested into L2: its enclosing 16-byte span, by the bulk-copy unit.
 __device__ __forceinline__ void l2_row(const void* base, int64_t q, size_t rb) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(base) + (uintptr_t)q * rb;
-  const uintptr_t lo = a & ~(uintptr_t)15, hi = (a + rb + 15) & ~(uintptr_t)15;
-  if (hi - lo <= (uintptr_t(1) << 24))   // rows up to 16 MB
-    bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+  const uint32_t bytes = wide_l2_bytes(a, rb);   // rows up to 16 MB
+  if (bytes) bulk_prefetch_l2(reinterpret_cast<const void*>(wide_l2_lo(a)), bytes);
 }
 
 // L2 lookahead of the CTA's walk: thread 0 requests the input rows L steps
@@ -299,14 +295,11 @@ __global__ void __launch_bounds__(kWideThreads, (FUSED || sizeof(TW) > sizeof(TX
 // apart for bf16, two to a bank group) -- then the tail's columns.
 template <int E>
 __device__ __forceinline__ int acc_vec(int v, int w) {
-  return E + (v >> 5) * (32 * E) + w * 128 + (v & 31) * 4;
+  return wide_acc_vec(v, w, E);
 }
 template <int E>
 __device__ __forceinline__ int acc_col(int j, int2 f) {
-  if (j < f.x) return j;
-  const int b = j - f.x, v = b / E;
-  if (v < f.y) return acc_vec<E>(v, (b - v * E) >> 2) + ((b - v * E) & 3);
-  return E + (f.y + 31) / 32 * (32 * E) + (b - f.y * E);
+  return wide_acc_col(j, f.x, f.y, E);
 }
 //
 // Both passes in dx's frame (rows a multiple of 16 bytes: the same split, and
