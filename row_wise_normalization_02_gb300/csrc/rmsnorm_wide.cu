@@ -1,29 +1,31 @@
 // kWide: RMSNorm and LayerNorm rows of any length whose operands start at
-// any element-aligned offsets, read and written as 16-byte vectors.  One CTA per row (persistent
-// walk over rows), two passes over each row:
-//   pass 1 reduces the row in the frame of one operand -- x for the forward
-//   and the backward, the residual (which receives h) for the fused add: that
-//   operand's row splits into a scalar head (elements before its first
-//   16-byte boundary), a body of 16-byte vectors and a scalar tail;
-//   pass 2 writes the output in the output's own frame.
-// Every other operand is read in the pass's frame: the frame's body vector v
-// covers 16 bytes of that operand which start s bytes into one of its aligned
-// chunks (s: the difference of the two rows' start addresses modulo 16), so
-// two aligned chunk loads and one byte funnel give it.  No load or store is
-// misaligned whatever the offsets; DRAM sees each byte once, pass 2 re-reading
-// the row from L1 or L2 (a row of tens of KB, read moments before), and a
-// shifted operand's second chunk is the neighbouring vector's first.
+// any element-aligned offsets, read and written as 16-byte vectors.  One CTA
+// per row (persistent walk over rows), each pass over a row working in the
+// frame of one operand: that operand's row splits into a scalar head
+// (elements before its first 16-byte boundary), a body of 16-byte vectors
+// and a scalar tail.  Every other operand is read in the pass's frame: the
+// frame's body vector v covers 16 bytes of that operand which start s bytes
+// into one of its aligned chunks (s: the difference of the two rows' start
+// addresses modulo 16), so two aligned chunk loads and one byte funnel give
+// it.  No load or store is misaligned whatever the offsets; DRAM sees each
+// byte once, later passes re-reading the row from L1 or L2 (a row of tens of
+// KB, read moments before), and a shifted operand's second chunk is the
+// neighbouring vector's first.  The index arithmetic is in
+// rmsnorm_wide_layout.h.
 //
-// The backward's dgamma partial row accumulates in shared memory, each column
-// always by the same thread in the CTA's row order (rows a multiple of 16
-// bytes, so dx's split is the same for every row); it is written to the
-// workspace once, at the end.
+// Forward: the reduction in x's frame (fused add: the residual's, which
+// receives h), the output in y's.  Backward: both passes in dx's frame (rows
+// a multiple of 16 bytes, so the split is the same for every row), pass 2 of
+// a row fused with pass 1 of the CTA's next row; the weight-gradient partial
+// rows accumulate in shared memory, each column always by the same thread in
+// the CTA's row order, and are written to the workspace once, at the end.
 //
 // The arithmetic per element is that of the register kernels: the sum of
 // squares (fused add: of h = round(r + x)), rs = 1/sqrt(ss/N + eps),
 // y = x rs gamma (bf16 x and gamma: (x gamma) rs), one rounding per output;
 // dx = r (gamma dy - x c) with c = r^2/N sum gamma dy x ("Pre-built kernel
 // library guide", 1.2 RMSNorm; the backward derived from its forward).
+// LayerNorm below.
 #include <type_traits>
 
 #include "rmsnorm_bwd_common.cuh"
